@@ -1,0 +1,70 @@
+"""Plant plausible mistakes in a copy of the oracle and check that the pins catch each one.
+
+Each mutant is one textual edit of oracle/pkv_oracle.c — a dropped term, a
+wrong sign, a transposed index, an off-by-one — compiled to a temporary
+library and run under tests/test_oracle_pins.py (the oracle loader takes the
+library path from PKV_ORACLE_LIB). A mutant that passes every pin would mean
+the pins cannot tell that mistake from the pages' definition.
+"""
+import concurrent.futures as cf
+import os
+import subprocess
+import sys
+import tempfile
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "pkv_oracle.c")
+
+MUTANTS = {
+    "drop_normalisation": ("for (int d = 0; d < dim; ++d) o[d] /= sum;", ""),
+    "max_subtraction_sign": ("s[j] = exp(s[j] - m);", "s[j] = exp(m - s[j]);"),
+    "drop_scale": ("s[j] = scale * dot;", "s[j] = dot;"),
+    "layout_head_before_kv": ("    i = i * 2 + kv;\n    i = i * g->num_heads + h;",
+                              "    i = i * g->num_heads + h;\n    i = i * 2 + kv;"),
+    "layout_token_dim_swapped": ("    i = i * g->block_size + t;\n    return i * g->head_dim + d;",
+                                 "    i = i * g->head_dim + d;\n    return i * g->block_size + t;"),
+    "gather_last_block_wrong": ("pool[elem(g, table[full], layer, kv, head, t, d)]",
+                                "pool[elem(g, table[0], layer, kv, head, t, d)]"),
+    "slot_forgets_block_scale": ("return (int64_t)table[pos / block_size] * block_size + pos % block_size;",
+                                 "return (int64_t)table[pos / block_size] + pos % block_size;"),
+    "append_v_gets_k": ("pool[elem(g, b, layer, 1, h, t, d)] = v[src];",
+                        "pool[elem(g, b, layer, 1, h, t, d)] = k[src];"),
+    "half_encode_truncates": ("double r = rint(ldexp(a, 10 - ue));", "double r = floor(ldexp(a, 10 - ue));"),
+    "half_decode_subnormal_scale": ("v = ldexp((double)f, -24);", "v = ldexp((double)f, -25);"),
+    "causal_excludes_self": ("pkvo_attend(qd, K, V, pos + 1, D, scale, o);", "pkvo_attend(qd, K, V, pos, D, scale, o);"),
+    "prefill_position_shift": ("pos = n - qlen + i;", "pos = n - qlen + i - (i > 0);"),
+    "merge_unweighted_sum": ("L += w * l[p];", "L += l[p];"),
+    "bytes_drop_kv_factor": ("return 2LL * g->num_layers * g->num_heads * g->head_dim * 2;",
+                             "return 1LL * g->num_layers * g->num_heads * g->head_dim * 2;"),
+    "ceil_becomes_floor": ("return (tokens + block_size - 1) / block_size;", "return tokens / block_size;"),
+    "partial_exp_drops_scale": ("double p = exp(scale * dot - m);", "double p = exp(dot - m);"),
+}
+
+
+def _run_mutant(name, tmp):
+    find, repl = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(find) == 1, f"mutant {name}: pattern must occur exactly once"
+    path_c = os.path.join(tmp, f"{name}.c")
+    path_so = os.path.join(tmp, f"lib{name}.so")
+    with open(path_c, "w") as f:
+        f.write(src.replace(find, repl))
+    subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", "-ffp-contract=off", path_c,
+                    "-o", path_so, "-lm"], check=True)
+    env = dict(os.environ, PKV_ORACLE_LIB=path_so, OMP_NUM_THREADS="2")
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                        os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    return name, r.returncode, r.stdout[-400:]
+
+
+def test_every_planted_mistake_fails_a_pin():
+    with tempfile.TemporaryDirectory() as tmp:
+        with cf.ThreadPoolExecutor(max_workers=max(1, min(8, os.cpu_count() or 1))) as ex:
+            results = list(ex.map(lambda n: _run_mutant(n, tmp), sorted(MUTANTS)))
+    survivors = [(n, out) for n, rc, out in results if rc == 0]
+    assert not survivors, f"mutants not caught by any pin: {survivors}"
+    # a return code of 1 means tests ran and failed (not a crash of the harness)
+    assert all(rc in (1, -11, -6) or rc > 1 for _, rc, _ in results)

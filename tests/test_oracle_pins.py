@@ -1,0 +1,419 @@
+"""Pins for the oracle: facts fixed by the pages or by mathematics, not by the oracle itself.
+
+Every oracle function is checked here against something independent of its
+own code: the pages' printed arithmetic (tests/golden/page_arithmetic.txt),
+numpy's binary16 conversion, numpy's C-order indexing of the block layout,
+closed forms of softmax attention (one-hot and uniform), invariance under a
+permutation of physical blocks, torch's float64 attention on contiguous
+inputs, and the identities between chunked and unchunked prefill and between
+split and unsplit decode. tests/test_oracle_mutants.py plants mistakes in a
+copy of the oracle and checks that this file catches each of them.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import blockmgr
+import workloads
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "page_arithmetic.txt")
+SCALE = oracle.SCALE_FP32
+
+
+def _golden_lines():
+    out = []
+    with open(GOLDEN) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if line:
+                lhs, rhs = line.split("=")
+                out.append((lhs.split(), int(rhs)))
+    return out
+
+
+def _geom_bytes(L, H, D, eb, bs, nblocks=1):
+    assert int(eb) == 2
+    return oracle.geom(nblocks, int(L), int(H), int(D), int(bs))
+
+
+def _eval_golden(args):
+    kind = args[0]
+    if kind == "bytes_per_token":
+        return oracle.bytes_per_token(_geom_bytes(*args[1:6]))
+    if kind == "bytes_per_block":
+        return oracle.bytes_per_block(_geom_bytes(*args[1:6]))
+    if kind in ("pool_blocks", "pool_tokens"):
+        g = _geom_bytes(*args[1:6])
+        budget = int(args[6])
+        n = budget // oracle.bytes_per_block(g)
+        # the next block would not fit
+        assert oracle.pool_bytes(_geom_bytes(*args[1:6], nblocks=n + 1)) > budget
+        assert oracle.pool_bytes(_geom_bytes(*args[1:6], nblocks=n)) <= budget
+        return n if kind == "pool_blocks" else n * int(args[5])
+    if kind == "request_bytes":
+        return oracle.bytes_per_token(_geom_bytes(*args[1:6])) * int(args[6])
+    if kind == "requests_fit":
+        g = _geom_bytes(*args[1:6])
+        n = int(args[6]) // oracle.bytes_per_block(g)
+        return n // oracle.blocks_for_tokens(int(args[7]), int(args[5]))
+    if kind == "batch_gb_rounded":
+        g = _geom_bytes(*args[1:6])
+        return round(oracle.bytes_per_token(g) * int(args[6]) * int(args[7]) / 1e9)
+    if kind == "blocks_for":
+        return oracle.blocks_for_tokens(int(args[2]), int(args[1]))
+    if kind == "blocks_for_list":
+        return sum(oracle.blocks_for_tokens(int(x), int(args[1])) for x in args[2].split(","))
+    if kind == "slots_for_list":
+        return sum(oracle.blocks_for_tokens(int(x), int(args[1])) * int(args[1]) for x in args[2].split(","))
+    if kind == "unused_slots_list":
+        xs = [int(x) for x in args[2].split(",")]
+        return sum(oracle.blocks_for_tokens(x, int(args[1])) * int(args[1]) for x in xs) - sum(xs)
+    if kind == "request_block_bytes":
+        g = _geom_bytes(*args[1:6])
+        return oracle.blocks_for_tokens(int(args[6]), int(args[5])) * int(args[5]) * oracle.bytes_per_token(g)
+    raise KeyError(kind)
+
+
+@pytest.mark.parametrize("args,expected", _golden_lines(), ids=lambda x: str(x)[:60])
+def test_page_arithmetic(args, expected):
+    assert _eval_golden(args) == expected
+
+
+def test_scale_is_fp32_inverse_sqrt_128():
+    assert np.float32(SCALE).view(np.uint32) == 0x3DB504F3
+
+
+# ------------------------------------------------------------------ binary16
+
+def test_half_decode_exhaustive():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ours = oracle.half_to_double(bits)
+    ref = bits.view(np.float16).astype(np.float64)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(ours), nan)
+    assert np.array_equal(ours[~nan], ref[~nan])
+    assert np.array_equal(np.signbit(ours[~nan]), np.signbit(ref[~nan]))
+
+
+def test_half_encode_round_to_nearest_even():
+    rng = np.random.default_rng(1)
+    # every representable value, every midpoint between neighbours, and random doubles
+    fin = np.arange(0, 0x7c00, dtype=np.uint16).view(np.float16).astype(np.float64)
+    mids = (fin[:-1] + fin[1:]) / 2
+    rnd = np.concatenate([rng.standard_normal(100000) * s for s in (1e-6, 1e-3, 1.0, 100.0, 3e4)])
+    x = np.concatenate([fin, mids, -mids, rnd, [65504.0, 65519.99, 65520.0, 1e6, -1e6, 0.0, -0.0]])
+    ours = oracle.double_to_half(x)
+    ref = x.astype(np.float16).view(np.uint16)
+    assert np.array_equal(ours, ref)
+
+
+# ------------------------------------------------------------------ helpers
+
+def _pool(N, L, H, seed=0, D=128):
+    t = workloads.normal_fp16(workloads.pool_shape(N, L, H, D), seed)
+    return t.numpy().view(np.uint16).copy()
+
+
+def _h(x):  # float array -> fp16 bits
+    return np.asarray(x, np.float64).astype(np.float16).view(np.uint16)
+
+
+def _contig(pool6, layer, kv, head, table, n):
+    """Contiguous K or V by numpy fancy indexing of [N, L, 2, H, 16, D]."""
+    pos = np.arange(n)
+    blk = np.asarray(table)[pos // 16]
+    return pool6[blk, layer, kv, head, pos % 16, :].view(np.float16).astype(np.float64)
+
+
+# ------------------------------------------------------------------ layout, append, gather
+
+def test_kv_append_lands_at_numpy_layout():
+    N, L, H = 12, 3, 4
+    g = oracle.geom(N, L, H)
+    pool = np.zeros(workloads.pool_shape(N, L, H), np.uint16)
+    rng = np.random.default_rng(2)
+    T = 9
+    slots = rng.choice(N * 16, T, replace=False).astype(np.int64)
+    k = rng.integers(0, 0x7c00, (T, H, 128)).astype(np.uint16)
+    v = rng.integers(0, 0x7c00, (T, H, 128)).astype(np.uint16)
+    assert oracle.kv_append(pool, g, 2, k, v, slots) == -1
+    expect = np.zeros_like(pool)
+    for i, s in enumerate(slots):
+        expect[s // 16, 2, 0, :, s % 16, :] = k[i]
+        expect[s // 16, 2, 1, :, s % 16, :] = v[i]
+    assert np.array_equal(pool, expect)
+
+
+@pytest.mark.parametrize("bad", [-1, 12 * 16])
+def test_kv_append_rejects_out_of_range_slot(bad):
+    N, L, H = 12, 1, 2
+    g = oracle.geom(N, L, H)
+    pool = np.zeros(workloads.pool_shape(N, L, H), np.uint16)
+    k = np.ones((3, H, 128), np.uint16)
+    assert oracle.kv_append(pool, g, 0, k, k, np.array([0, bad, 5], np.int64)) == 1
+    assert not pool.any()
+
+
+@pytest.mark.parametrize("n", [1, 15, 16, 17, 47, 64])
+def test_append_then_gather_is_identity(n):
+    N, L, H = 16, 2, 3
+    g = oracle.geom(N, L, H)
+    pool = np.zeros(workloads.pool_shape(N, L, H), np.uint16)
+    rng = np.random.default_rng(n)
+    table = rng.permutation(N)[: -(-n // 16)].astype(np.int32)
+    rows = np.zeros((n, H, 128), np.uint16)
+    for p in range(n):   # one token per step, as decode appends them
+        k = _h(rng.standard_normal((1, H, 128)))
+        slot = oracle.slots(table[None, :], np.zeros(1, np.int32), np.array([p]))
+        assert oracle.kv_append(pool, g, 1, k, k, slot) == -1
+        rows[p] = k[0]
+    for h in range(H):
+        for kv in (0, 1):
+            got = oracle.gather(pool, g, 1, kv, h, table, n)
+            assert np.array_equal(got, rows[:, h, :].view(np.float16).astype(np.float64))
+
+
+def test_gather_reads_only_leading_rows_of_last_block():
+    N, L, H = 4, 1, 1
+    g = oracle.geom(N, L, H)
+    pool6 = _pool(N, L, H)
+    table = np.array([2, 0], np.int32)
+    pool6[0, 0, :, 0, 1:, :] = 0x7e00          # NaN beyond the first row of the last block
+    got = oracle.gather(pool6, g, 0, 0, 0, table, 17)
+    assert not np.isnan(got).any()
+    assert np.array_equal(got, _contig(pool6, 0, 0, 0, table, 17))
+
+
+# ------------------------------------------------------------------ attention closed forms
+
+def _decode_inputs(ctx, N=40, L=2, H=4, seed=3):
+    rng = np.random.default_rng(seed)
+    pool6 = _pool(N, L, H, seed)
+    perm = rng.permutation(N).astype(np.int32)
+    nb = [-(-c // 16) for c in ctx]
+    tables = np.full((len(ctx), max(nb)), -1, np.int32)
+    cur = 0
+    for r, b in enumerate(nb):
+        tables[r, :b] = perm[cur:cur + b]
+        cur += b
+    q = _h(rng.standard_normal((len(ctx), H, 128)))
+    return pool6, oracle.geom(N, L, H), tables, np.array(ctx, np.int32), q
+
+
+@pytest.mark.parametrize("j", [0, 15, 16, 31, 36])
+def test_one_hot_softmax_returns_that_value_row(j):
+    ctx = [37]
+    pool6, g, tables, ctx, q = _decode_inputs(ctx)
+    layer, H = 1, g.num_heads
+    pos = np.arange(37)
+    blk, off = tables[0][pos // 16], pos % 16
+    pool6[blk, layer, 0] = 0
+    # logits: q.k_j * scale ~ 128 * |q|^2 * scale >> 745, every other logit is 0
+    pool6[blk[j], layer, 0, :, off[j], :] = _h(128.0 * q[0].view(np.float16).astype(np.float64))
+    o64, o16 = oracle.decode_attn(pool6, g, layer, q, tables, ctx, SCALE)
+    v_j = pool6[blk[j], layer, 1, :, off[j], :]
+    assert np.array_equal(o64[0], v_j.view(np.float16).astype(np.float64))
+    assert np.array_equal(o16[0], v_j)
+
+
+def test_uniform_softmax_is_mean_of_values():
+    pool6, g, tables, ctx, q = _decode_inputs([1, 16, 29, 100])
+    pool6[:, :, 0] = 0
+    o64, _ = oracle.decode_attn(pool6, g, 0, q, tables, ctx, SCALE)
+    for r, n in enumerate(ctx):
+        for h in range(g.num_heads):
+            mean = _contig(pool6, 0, 1, h, tables[r], n).mean(axis=0)
+            assert np.allclose(o64[r, h], mean, rtol=0, atol=1e-13)
+
+
+def test_marker_rows_read_only_their_own_blocks():
+    # 3 rows share 2 full prefix blocks; private values carry a per-row marker.
+    N, L, H = 16, 1, 2
+    g = oracle.geom(N, L, H)
+    pool6 = np.zeros(workloads.pool_shape(N, L, H), np.uint16)
+    shared = [5, 9]
+    private = {0: [1], 1: [2, 3], 2: [4]}
+    priv_tokens = [3, 20, 16]
+    markers = [0.25, 0.5, -1.0]
+    pool6[shared, :, 1] = _h(2.0)
+    for r, blks in private.items():
+        pool6[blks, :, 1] = _h(markers[r])
+    for b in range(N):
+        if b not in shared and all(b not in v for v in private.values()):
+            pool6[b, :, 1] = _h(1000.0)       # foreign blocks: any read shows up
+    tables = np.full((3, 4), -1, np.int32)
+    for r in range(3):
+        row = shared + private[r]
+        tables[r, :len(row)] = row
+    ctx = np.array([32 + t for t in priv_tokens], np.int32)
+    q = _h(np.random.default_rng(0).standard_normal((3, H, 128)))
+    o64, _ = oracle.decode_attn(pool6, g, 0, q, tables, ctx, SCALE)
+    for r in range(3):
+        expect = (32 * 2.0 + priv_tokens[r] * markers[r]) / ctx[r]
+        assert np.allclose(o64[r], expect, rtol=0, atol=1e-12)
+
+
+def test_physical_block_permutation_leaves_output_unchanged():
+    pool6, g, tables, ctx, q = _decode_inputs([5, 33, 64, 90], N=40)
+    o_ref, o16_ref = oracle.decode_attn(pool6, g, 1, q, tables, ctx, SCALE)
+    rng = np.random.default_rng(7)
+    perm = rng.permutation(g.num_blocks)          # block b moves to perm[b]
+    moved = np.empty_like(pool6)
+    moved[perm] = pool6
+    t2 = np.where(tables >= 0, perm[np.maximum(tables, 0)], -1).astype(np.int32)
+    o2, o16 = oracle.decode_attn(moved, g, 1, q, t2, ctx, SCALE)
+    assert np.array_equal(o_ref, o2) and np.array_equal(o16_ref, o16)
+
+
+def test_decode_matches_torch_float64_attention():
+    pool6, g, tables, ctx, q = _decode_inputs([1, 2, 17, 50, 100, 255], N=40)
+    o64, o16 = oracle.decode_attn(pool6, g, 1, q, tables, ctx, SCALE)
+    for r, n in enumerate(ctx):
+        for h in range(g.num_heads):
+            K = torch.from_numpy(_contig(pool6, 1, 0, h, tables[r], n))
+            V = torch.from_numpy(_contig(pool6, 1, 1, h, tables[r], n))
+            qq = torch.from_numpy(q[r, h].view(np.float16).astype(np.float64))
+            ref = torch.nn.functional.scaled_dot_product_attention(qq[None, None], K[None], V[None], scale=SCALE)[0, 0]
+            assert np.allclose(o64[r, h], ref.numpy(), rtol=1e-12, atol=1e-13)
+    assert np.array_equal(o16, oracle.double_to_half(o64))
+
+
+# ------------------------------------------------------------------ prefill
+
+def _prompt_case(n=70, N=12, L=1, H=3, seed=5):
+    rng = np.random.default_rng(seed)
+    pool6 = _pool(N, L, H, seed)
+    table = rng.permutation(N)[: -(-n // 16)].astype(np.int32)
+    q = _h(rng.standard_normal((n, H, 128)))
+    return pool6, oracle.geom(N, L, H), table, q
+
+
+def test_prefill_matches_torch_causal_attention():
+    n = 70
+    pool6, g, table, q = _prompt_case(n)
+    o64, _ = oracle.prefill_attn(pool6, g, 0, q, [0, n], table[None], [n], SCALE)
+    mask = torch.ones(n, n, dtype=torch.bool).tril()
+    for h in range(g.num_heads):
+        K = torch.from_numpy(_contig(pool6, 0, 0, h, table, n))
+        V = torch.from_numpy(_contig(pool6, 0, 1, h, table, n))
+        Q = torch.from_numpy(q[:, h].view(np.float16).astype(np.float64))
+        ref = torch.nn.functional.scaled_dot_product_attention(Q[None], K[None], V[None], attn_mask=mask[None],
+                                                               scale=SCALE)[0]
+        assert np.allclose(o64[:, h], ref.numpy(), rtol=1e-12, atol=1e-13)
+
+
+def test_chunked_prefill_rows_equal_unchunked_rows():
+    n, c = 70, 32
+    pool6, g, table, q = _prompt_case(n)
+    full64, full16 = oracle.prefill_attn(pool6, g, 0, q, [0, n], table[None], [n], SCALE)
+    for s in range(0, n, c):
+        e = min(s + c, n)
+        o64, o16 = oracle.prefill_attn(pool6, g, 0, q[s:e], [0, e - s], table[None], [e], SCALE)
+        assert np.array_equal(o64, full64[s:e]) and np.array_equal(o16, full16[s:e])
+
+
+def test_decode_row_equals_last_prefill_row():
+    n = 45
+    pool6, g, table, q = _prompt_case(n)
+    full64, _ = oracle.prefill_attn(pool6, g, 0, q, [0, n], table[None], [n], SCALE)
+    d64, _ = oracle.decode_attn(pool6, g, 0, q[n - 1:n], table[None], [n], SCALE)
+    assert np.array_equal(d64[0], full64[n - 1])
+
+
+def test_prefill_several_sequences_in_one_call():
+    pool6, g, tables, ctx, q_dec = _decode_inputs([20, 40, 35], N=40, L=1)
+    qlens = [1, 7, 35]
+    qs = np.concatenate([[0], np.cumsum(qlens)]).astype(np.int32)
+    q = _h(np.random.default_rng(11).standard_normal((qs[-1], g.num_heads, 128)))
+    o64, _ = oracle.prefill_attn(pool6, g, 0, q, qs, tables, ctx, SCALE)
+    for s in range(3):
+        for i in range(qlens[s]):
+            pos = ctx[s] - qlens[s] + i
+            d64, _ = oracle.decode_attn(pool6, g, 0, q[qs[s] + i:qs[s] + i + 1], tables[s:s + 1],
+                                        np.array([pos + 1], np.int32), SCALE)
+            assert np.array_equal(o64[qs[s] + i], d64[0])
+
+
+# ------------------------------------------------------------------ split merge
+
+@pytest.mark.parametrize("part", [16, 48, 100, 512, 4096])
+def test_split_merge_equals_unsplit(part):
+    pool6, g, tables, ctx, q = _decode_inputs([1, 16, 17, 250, 600], N=64)
+    ref, _ = oracle.decode_attn(pool6, g, 0, q, tables, ctx, SCALE)
+    got = oracle.decode_attn_split(pool6, g, 0, q, tables, ctx, SCALE, part)
+    assert np.allclose(got, ref, rtol=1e-12, atol=1e-14)
+
+
+def test_merge_of_two_halves_by_hand():
+    rng = np.random.default_rng(4)
+    K = rng.standard_normal((30, 128))
+    V = rng.standard_normal((30, 128))
+    q = rng.standard_normal(128)
+    m1, l1, o1 = oracle.partial(q, K, V, 0, 13, 0.1)
+    m2, l2, o2 = oracle.partial(q, K, V, 13, 30, 0.1)
+    got = oracle.merge([m1, m2], [l1, l2], np.stack([o1, o2]))
+    s = 0.1 * K @ q
+    p = np.exp(s - s.max())
+    assert np.allclose(got, (p / p.sum()) @ V, rtol=1e-12, atol=1e-14)
+
+
+# ------------------------------------------------------------------ block manager
+
+def test_blockmgr_page_example_lengths():
+    bm = blockmgr.BlockManager(7152)
+    for i, n in enumerate([17, 33, 65]):
+        assert bm.grow(i, n) == blockmgr.OK
+    assert 7152 - bm.free_blocks() == 10
+    assert bm.grow(3, 600) == blockmgr.OK and len(bm.tables[3]) == 38
+    assert bm.grow(4, 2300) == blockmgr.OK and len(bm.tables[4]) == 144
+
+
+def test_blockmgr_grow_one_block_every_16_tokens():
+    bm = blockmgr.BlockManager(64)
+    for n in range(1, 200):
+        assert bm.grow(0, n) == blockmgr.OK
+        assert len(bm.tables[0]) == math.ceil(n / 16)
+
+
+def test_blockmgr_nomem_changes_nothing():
+    bm = blockmgr.BlockManager(8)
+    assert bm.grow(0, 100) == blockmgr.OK           # 7 blocks
+    before = (list(bm.free), list(bm.tables[0]), bm.lens[0])
+    assert bm.grow(1, 40) == blockmgr.E_NOMEM
+    assert bm.grow(0, 129) == blockmgr.E_NOMEM
+    assert (list(bm.free), list(bm.tables[0]), bm.lens[0]) == before and 1 not in bm.tables
+
+
+def test_blockmgr_shared_prefix_refcounts_and_soak_returns_all_blocks():
+    bm = blockmgr.BlockManager(7152, free_order=np.random.default_rng(0).permutation(7152))
+    assert bm.grow(0, 2000) == blockmgr.OK
+    for s in range(1, 65):
+        assert bm.share_prefix(s, 0, 125) == blockmgr.OK
+        assert bm.grow(s, 2000 + s) == blockmgr.OK
+    shared = bm.tables[0][:125]
+    assert all(bm.ref[b] == 65 for b in shared)
+    st, tables, ctx, slots, qs = bm.build_step(list(range(1, 65)), [1] * 64, 200)
+    assert st == blockmgr.OK and len(slots) == 64
+    assert all(s // 16 not in shared for s in slots)
+    # a write into a shared block is refused
+    assert bm.grow(99, 0) == blockmgr.OK
+    assert bm.share_prefix(100, 0, 10) == blockmgr.OK
+    assert bm.build_step([100], [1], 200)[0] == blockmgr.E_SHARED
+    for s in list(bm.tables):
+        assert bm.free_seq(s) == blockmgr.OK
+    assert bm.free_blocks() == 7152 and all(r == 0 for r in bm.ref)
+
+
+def test_blockmgr_lifo_reuse_and_invalid_calls():
+    bm = blockmgr.BlockManager(10)
+    assert bm.grow(0, 40) == blockmgr.OK
+    assert bm.tables[0] == [0, 1, 2]
+    assert bm.free_seq(0) == blockmgr.OK
+    assert bm.grow(1, 16) == blockmgr.OK and bm.tables[1] == [2]
+    assert bm.free_seq(7) == blockmgr.E_INVALID
+    assert bm.grow(1, 3) == blockmgr.E_INVALID          # sequences only grow
+    assert bm.share_prefix(2, 1, 2) == blockmgr.E_INVALID  # only full blocks that exist
