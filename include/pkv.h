@@ -1,0 +1,236 @@
+/*
+ * pkv.h — C ABI of libpkv: a paged KV cache on one GB300 (sm_103a).
+ *
+ * The cache is one device allocation of FP16 blocks. A block holds the keys
+ * and values of 16 token positions for every layer, laid out as
+ *     [layer][2 (0 = K, 1 = V)][head][16 tokens][head_dim]
+ * so element (block b, layer l, kv, head h, token t, dim d) sits at
+ *     ((((b*L + l)*2 + kv)*H + h)*16 + t)*head_dim + d
+ * ("llm-inference-batching" (faangrind), the KV pool listing; 524,288 B per
+ * token and 8,388,608 B per block for 32 layers x 32 heads x 128 dims).
+ * A sequence's block table maps its logical block i (positions 16i..16i+15)
+ * to a physical block; position p lives at slot table[p/16]*16 + p%16
+ * (same page, "block_table"; "continuous batching server" (scalablesystem),
+ * "PagedAttention Block Table Lookup").
+ *
+ * Conventions for every call:
+ *   - Ownership: the caller owns every device buffer (pool, q/k/v, tables,
+ *     outputs, workspace); pointers are borrowed for the duration of the
+ *     call. The library owns only the opaque pkv_pool host handle.
+ *   - Asynchrony: kernel calls enqueue work on `stream` (a cudaStream_t,
+ *     NULL = legacy default stream) and return without synchronising.
+ *   - Errors: every call returns a pkv_status. Bad arguments are refused on
+ *     the host before anything is launched (PKV_E_INVALID, with a message in
+ *     pkv_last_error_string()). Inputs that live on the device (tables,
+ *     lengths, slots) are bounds-checked by the kernels: a bad entry skips
+ *     the access and sets a sticky per-device error word that
+ *     pkv_get_status() reads. No C++ exception crosses this boundary.
+ *   - Threads: a pool is not thread-safe; one scheduler thread owns it
+ *     ("llm-inference-batching", step 3: one scheduler thread owns the GPU).
+ *   - Supported geometry: head_dim 128, block_size 16, FP16, any number of
+ *     layers (1..1024) and heads (1..256). Query heads equal K/V heads.
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum pkv_status {
+    PKV_OK = 0,
+    PKV_E_INVALID = 1,  /* bad argument, refused before launch */
+    PKV_E_NOMEM = 2,    /* free list cannot cover the request; nothing changed (caller preempts) */
+    PKV_E_SHARED = 3,   /* a new token would be written into a block whose ref_count > 1 */
+    PKV_E_DEVICE = 4,   /* CUDA error, or a kernel found a bad table entry / slot / length */
+    PKV_E_TIMEOUT = 5   /* a kernel's bounded wait ran out; the kernel returned early */
+} pkv_status;
+
+enum { PKV_DTYPE_FP16 = 0 };
+
+/* Bits of the sticky device error word (pkv_get_status). */
+enum {
+    PKV_DEV_BAD_SLOT = 1u << 0,   /* kv_append: slot outside [0, num_blocks*16) */
+    PKV_DEV_BAD_BLOCK = 1u << 1,  /* attention: block id outside [0, num_blocks) */
+    PKV_DEV_BAD_CTX = 1u << 2,    /* attention: ctx_len < 1 or beyond the table width */
+    PKV_DEV_BAD_QLEN = 1u << 3,   /* prefill: q_len < 1, > ctx_len, or beyond max_q_len */
+    PKV_DEV_TIMEOUT = 1u << 4     /* a bounded wait on an mbarrier ran out */
+};
+
+/* ------------------------------------------------------------------ pool */
+
+typedef struct pkv_pool_desc {
+    int64_t num_blocks;   /* physical blocks in the pool (7,152 for a 60 GB pool) */
+    int32_t num_layers;   /* 32 */
+    int32_t num_heads;    /* 32 (K/V heads = query heads) */
+    int32_t head_dim;     /* must be 128 */
+    int32_t block_size;   /* must be 16 */
+    int32_t dtype;        /* must be PKV_DTYPE_FP16 */
+    int32_t partition_tokens; /* decode split-K partition size in tokens; 0 = default 512;
+                                 must be a multiple of 64. Results depend only on a row's
+                                 ctx_len and this value, never on the rest of the batch. */
+    void* dev_base;       /* device pointer to the pool, 256-byte aligned; NULL makes a host-only
+                             pool (block manager and step metadata only; kernel calls refused) */
+    size_t bytes;         /* size of that allocation, >= pkv_pool_bytes(desc) */
+    const int64_t* free_order; /* optional host array [num_blocks], a permutation: the order in
+                                  which blocks are handed out. NULL = 0, 1, 2, ... */
+} pkv_pool_desc;
+
+typedef struct pkv_pool pkv_pool;
+
+/* Bytes the pool needs: num_blocks * num_layers * 2 * num_heads * block_size * head_dim * 2
+ * ("llm-inference-batching", "KV cache": 8,388,608 B per block for the 7B model).
+ * Returns 0 for an invalid descriptor. */
+size_t pkv_pool_bytes(const pkv_pool_desc* desc);
+
+/* Validate desc, bind the pool to the current CUDA device and build its host handle.
+ * The device memory is not touched. *out receives the handle. With dev_base NULL
+ * no CUDA call is made and the handle serves the block manager only. */
+pkv_status pkv_pool_create(const pkv_pool_desc* desc, pkv_pool** out);
+pkv_status pkv_pool_destroy(pkv_pool* pool);
+
+/* ---------------------------------------------------- block manager (host) */
+/* A ref-counted allocator over the pool's blocks: a free list, one block
+ * table per sequence and ref_count[block] ("llm-inference-batching", the KV
+ * pool listing; "continuous batching server", "The KV Cache Block Manager";
+ * "Serving LLMs" (sreshtalluri), "Paged KV memory"). Host only; no GPU work. */
+
+/* Make seq_id (created on first use) own ceil(new_len/16) blocks and set its
+ * length to new_len. New blocks come off the free list with ref_count 1.
+ * PKV_E_NOMEM if the free list cannot cover it (nothing changes: the caller
+ * preempts); PKV_E_INVALID if new_len is below the current length. */
+pkv_status pkv_seq_grow(pkv_pool* pool, int64_t seq_id, int64_t new_len);
+
+/* Point a new sequence dst_seq at the first n_blocks (full) blocks of src_seq
+ * and raise their ref_count; dst's length becomes 16*n_blocks. Shared blocks
+ * are read-only: a later write into one is refused with PKV_E_SHARED. */
+pkv_status pkv_seq_share_prefix(pkv_pool* pool, int64_t dst_seq, int64_t src_seq, int64_t n_blocks);
+
+/* Finished or cancelled sequence: drop one reference to each of its blocks;
+ * a block whose ref_count reaches 0 returns to the free list. */
+pkv_status pkv_seq_free(pkv_pool* pool, int64_t seq_id);
+
+int64_t pkv_free_blocks(const pkv_pool* pool);                 /* -1 for a NULL pool */
+int32_t pkv_ref_count(const pkv_pool* pool, int64_t block);     /* -1 if out of range */
+int64_t pkv_seq_len(const pkv_pool* pool, int64_t seq_id);      /* -1 if unknown */
+
+/* Copy seq_id's block table (host int32) into out[0..capacity); *n_out = its length. */
+pkv_status pkv_block_table(const pkv_pool* pool, int64_t seq_id, int32_t* out, int64_t capacity,
+                           int64_t* n_out);
+
+/* Host-side metadata for one engine iteration over the listed sequences
+ * ("llm-inference-batching", the step tensors: one flat, unpadded token list
+ * tagged with its request). Row i's new tokens are its last q_lens[i]
+ * positions, i.e. [len - q_lens[i], len) after pkv_seq_grow. Sequences not
+ * listed take no part (finished or cancelled rows leave at a step boundary).
+ * Outputs (host arrays, caller-allocated):
+ *   block_tables [num_seqs, max_blocks] int32, -1 past each row's blocks
+ *   ctx_lens     [num_seqs]             int32, cached tokens incl. the new ones
+ *   slot_mapping [sum q_lens]           int64, slot of each new token, row order
+ *   q_start_loc  [num_seqs + 1]         int32, prefix sums of q_lens
+ * PKV_E_SHARED if a new token falls in a block with ref_count > 1. */
+pkv_status pkv_build_step(const pkv_pool* pool, const int64_t* seq_ids, const int32_t* q_lens, int32_t num_seqs,
+                          int32_t max_blocks, int32_t* block_tables, int32_t* ctx_lens, int64_t* slot_mapping,
+                          int32_t* q_start_loc);
+
+/* ---------------------------------------------------------------- kernels */
+
+/* reshape_and_cache: write token i's keys k[i] and values v[i] (device FP16,
+ * [num_tokens, heads, 128], 16-byte aligned) of layer `layer` into slot
+ * slot_mapping[i] (device int64) of the pool ("llm-inference-batching",
+ * step 7: a row's new keys and values are appended; a row takes a new
+ * block every 16 tokens). Slots must be distinct. A slot outside the pool is
+ * skipped and flagged PKV_DEV_BAD_SLOT. */
+pkv_status pkv_kv_append(pkv_pool* pool, int32_t layer, const void* k, const void* v,
+                         const int64_t* slot_mapping, int32_t num_tokens, void* stream);
+
+/* Workspace bytes pkv_decode_attn needs for num_seqs rows whose tables are
+ * max_blocks wide (split-K partials: un-normalised output, max and sum per
+ * row, head and partition). */
+size_t pkv_decode_workspace_bytes(const pkv_pool* pool, int32_t num_seqs, int32_t max_blocks);
+
+/* Decode attention: for each row r and head h, the single query q[r,h,:]
+ * attends positions 0..ctx_lens[r]-1 of row r's blocks, including the token
+ * appended this step: out = softmax(q K^T * scale) V ("Inference
+ * Infrastructure" (seeitflow), the decode steps). Long rows are split into
+ * partitions of partition_tokens keys whose softmax statistics are merged
+ * exactly ("The inference engine" (wpnews), "IO-aware attention").
+ *   q            device FP16 [num_seqs, heads, 128]
+ *   block_tables device int32 [num_seqs, max_blocks]
+ *   ctx_lens     device int32 [num_seqs], 1 <= ctx_len <= 16*max_blocks
+ *   out          device FP16 [num_seqs, heads, 128], rounded once (RNE)
+ *   workspace    device, >= pkv_decode_workspace_bytes(), 256-byte aligned
+ * FP32 arithmetic; scale is applied in FP32 (1/sqrt(128) = 0x3DB504F3). */
+pkv_status pkv_decode_attn(pkv_pool* pool, int32_t layer, const void* q, const int32_t* block_tables,
+                           int32_t max_blocks, const int32_t* ctx_lens, int32_t num_seqs, float scale, void* out,
+                           void* workspace, size_t workspace_bytes, void* stream);
+
+/* Chunked causal prefill: sequence s owns query tokens
+ * [q_start_loc[s], q_start_loc[s+1]) of q ([num_tokens, heads, 128] FP16);
+ * query i sits at position ctx_lens[s] - q_len + i and attends keys 0..that
+ * position of s's blocks, which already hold the chunk's own K/V
+ * ("llm-inference-batching", "Prefill and decode share each step"; "The
+ * inference engine", "Prefill and decode ask the accelerator for different
+ * work"). max_q_len bounds every q_len (it sizes the grid). Tensor cores
+ * (tcgen05, accumulators in TMEM), FP32 accumulation, FP16 output. */
+pkv_status pkv_prefill_attn(pkv_pool* pool, int32_t layer, const void* q, const int32_t* q_start_loc,
+                            const int32_t* block_tables, int32_t max_blocks, const int32_t* ctx_lens,
+                            int32_t num_seqs, int32_t max_q_len, float scale, void* out, void* stream);
+
+/* ------------------------------------------------------------------- step */
+
+/* One mixed engine iteration: B decode rows then P prefill rows, as one flat
+ * token list ("llm-inference-batching": "One step with B decode rows and a
+ * prefill chunk of C prompt tokens"). Rows 0..B-1 have one token each
+ * (tokens 0..B-1); rows B..B+P-1 are prefill chunks. Per-layer tensors are
+ * given as a base pointer and a stride in elements between layers. */
+typedef struct pkv_step_desc {
+    int32_t num_decode;          /* B */
+    int32_t num_prefill;         /* P */
+    int32_t num_tokens;          /* T = B + sum of prefill q_lens */
+    int32_t max_q_len;           /* largest prefill q_len (grid bound) */
+    int32_t max_blocks;          /* width of block_tables */
+    int32_t first_layer;         /* layers [first_layer, first_layer + num_layers) run in order */
+    int32_t num_layers;
+    float scale;
+    const int32_t* block_tables; /* device [B+P, max_blocks] */
+    const int32_t* ctx_lens;     /* device [B+P] */
+    const int32_t* q_start_loc;  /* device [B+P+1], token offsets into the flat list */
+    const int64_t* slot_mapping; /* device [T] */
+    const void* q;               /* device FP16 [layers][T][heads][128] */
+    const void* k;
+    const void* v;
+    void* out;                   /* device FP16 [layers][T][heads][128] */
+    int64_t q_layer_stride, k_layer_stride, v_layer_stride, out_layer_stride; /* elements */
+} pkv_step_desc;
+
+size_t pkv_step_workspace_bytes(const pkv_pool* pool, const pkv_step_desc* step);
+
+/* For each layer: kv_append of all T tokens, then decode attention over the
+ * B decode rows and causal prefill over the P chunks. */
+pkv_status pkv_step(pkv_pool* pool, const pkv_step_desc* step, void* workspace, size_t workspace_bytes,
+                    void* stream);
+
+/* ----------------------------------------------------------------- status */
+
+/* Synchronise `stream`, read and clear the sticky device error word
+ * (PKV_DEV_* bits into *device_flags if non-NULL). Returns PKV_E_TIMEOUT if
+ * a wait ran out, PKV_E_DEVICE for any other flag or a CUDA error. */
+pkv_status pkv_get_status(pkv_pool* pool, void* stream, uint32_t* device_flags);
+
+/* Message for the last failure on this thread ("" if none). */
+const char* pkv_last_error_string(void);
+const char* pkv_status_string(pkv_status s);
+
+/* Test hook for the bounded-wait path: one CTA waits on an mbarrier that no
+ * one arrives at, gives up after timeout_ns and sets PKV_DEV_TIMEOUT. */
+pkv_status pkv_debug_wait_probe(pkv_pool* pool, uint64_t timeout_ns, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H */

@@ -1,0 +1,485 @@
+// pkv_host.cpp — the C ABI of libpkv: pool handle, ref-counted block manager,
+// step metadata, argument validation, status word, and the per-layer step
+// launcher. Host code only; kernels live in pkv_kernels.cu / pkv_prefill.cu.
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <new>
+
+#include "pkv_internal.h"
+
+namespace {
+thread_local char g_err[512] = "";
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+pkv_status check_pool(const pkv_pool* pool)
+{
+    if (!pool) return pkv::fail(PKV_E_INVALID, "pool is NULL");
+    return PKV_OK;
+}
+
+// Kernel entry points need a pool bound to device memory.
+pkv_status check_device_pool(const pkv_pool* pool)
+{
+    if (!pool) return pkv::fail(PKV_E_INVALID, "pool is NULL");
+    if (pool->host_only) return pkv::fail(PKV_E_INVALID, "pool has no device memory (host-only block manager)");
+    return PKV_OK;
+}
+
+// Make the pool's device current for the duration of a call.
+struct DeviceGuard {
+    int prev = -1;
+    bool ok = true;
+    explicit DeviceGuard(int dev)
+    {
+        if (cudaGetDevice(&prev) != cudaSuccess) { ok = false; return; }
+        if (prev != dev && cudaSetDevice(dev) != cudaSuccess) ok = false;
+    }
+    ~DeviceGuard()
+    {
+        int cur = -1;
+        if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+    }
+};
+}  // namespace
+
+namespace pkv {
+
+pkv_status fail(pkv_status s, const char* fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    std::vsnprintf(g_err, sizeof(g_err), fmt, ap);
+    va_end(ap);
+    return s;
+}
+
+pkv_status cuda_fail(cudaError_t e, const char* what)
+{
+    return fail(PKV_E_DEVICE, "%s: %s", what, cudaGetErrorString(e));
+}
+
+}  // namespace pkv
+
+using pkv::fail;
+
+extern "C" {
+
+const char* pkv_last_error_string(void) { return g_err; }
+
+const char* pkv_status_string(pkv_status s)
+{
+    switch (s) {
+    case PKV_OK: return "ok";
+    case PKV_E_INVALID: return "invalid argument";
+    case PKV_E_NOMEM: return "free list exhausted";
+    case PKV_E_SHARED: return "write into a shared block";
+    case PKV_E_DEVICE: return "device error";
+    case PKV_E_TIMEOUT: return "bounded wait ran out";
+    }
+    return "unknown status";
+}
+
+// ------------------------------------------------------------------ pool
+
+static bool desc_ok(const pkv_pool_desc* d)
+{
+    if (!d) return false;
+    if (d->head_dim != pkv::kHeadDim || d->block_size != pkv::kBlockSize || d->dtype != PKV_DTYPE_FP16) return false;
+    if (d->num_blocks < 1 || d->num_blocks > (int64_t)1 << 31) return false;
+    if (d->num_layers < 1 || d->num_layers > 1024 || d->num_heads < 1 || d->num_heads > 256) return false;
+    return true;
+}
+
+size_t pkv_pool_bytes(const pkv_pool_desc* d)
+{
+    if (!desc_ok(d)) return 0;
+    return (size_t)d->num_blocks * d->num_layers * 2 * d->num_heads * d->block_size * d->head_dim * 2;
+}
+
+static bool bind_device(pkv_pool* p)
+{
+    const pkv_pool_desc* d = &p->desc;
+    cudaError_t e = cudaGetDevice(&p->device);
+    if (e != cudaSuccess) { pkv::cuda_fail(e, "cudaGetDevice"); return false; }
+    cudaPointerAttributes attr;
+    e = cudaPointerGetAttributes(&attr, d->dev_base);
+    if (e != cudaSuccess || attr.type != cudaMemoryTypeDevice || attr.device != p->device) {
+        cudaGetLastError();
+        fail(PKV_E_INVALID, "dev_base is not device memory of the current device");
+        return false;
+    }
+    e = pkv::status_word(p->device, &p->status_dev);
+    if (e != cudaSuccess) { pkv::cuda_fail(e, "status word"); return false; }
+    p->geom.base = static_cast<const char*>(d->dev_base);
+    p->geom.num_blocks = d->num_blocks;
+    p->geom.num_layers = d->num_layers;
+    p->geom.num_heads = d->num_heads;
+    p->geom.kv_bytes = (int64_t)d->num_heads * pkv::kTileBytes;
+    p->geom.layer_bytes = 2 * p->geom.kv_bytes;
+    p->geom.block_bytes = (int64_t)d->num_layers * p->geom.layer_bytes;
+    std::string err;
+    p->kv_tmap_ok = pkv::encode_kv_tmap(p->geom, &p->kv_tmap, &err);
+    return true;
+}
+
+pkv_status pkv_pool_create(const pkv_pool_desc* d, pkv_pool** out)
+{
+    if (!out) return fail(PKV_E_INVALID, "out is NULL");
+    *out = nullptr;
+    if (!desc_ok(d))
+        return fail(PKV_E_INVALID, "unsupported pool descriptor (need head_dim 128, block_size 16, FP16, "
+                                   "1..1024 layers, 1..256 heads, 1..2^31 blocks)");
+    const bool host_only = d->dev_base == nullptr;
+    if (!host_only && !aligned(d->dev_base, 256)) return fail(PKV_E_INVALID, "dev_base not 256-byte aligned");
+    if (!host_only && d->bytes < pkv_pool_bytes(d))
+        return fail(PKV_E_INVALID, "pool allocation smaller than pkv_pool_bytes()");
+    int part = d->partition_tokens ? d->partition_tokens : pkv::kDefaultPartition;
+    if (part % 64 != 0 || part < 64 || part > pkv::kMaxPartition)
+        return fail(PKV_E_INVALID, "partition_tokens must be a multiple of 64 in [64, %d]", pkv::kMaxPartition);
+
+    pkv_pool* p = new (std::nothrow) pkv_pool;
+    if (!p) return fail(PKV_E_NOMEM, "host allocation failed");
+    p->desc = *d;
+    p->desc.free_order = nullptr;
+    p->partition_tokens = part;
+    p->host_only = host_only;
+    if (!host_only && !bind_device(p)) {
+        delete p;
+        return PKV_E_DEVICE;  // message already set
+    }
+
+
+    const int64_t n = d->num_blocks;
+    p->ref.assign(n, 0);
+    p->free_stack.resize(n);
+    if (d->free_order) {
+        std::vector<char> seen(n, 0);
+        for (int64_t i = 0; i < n; ++i) {
+            const int64_t b = d->free_order[i];
+            if (b < 0 || b >= n || seen[b]) {
+                delete p;
+                return fail(PKV_E_INVALID, "free_order is not a permutation of 0..num_blocks-1");
+            }
+            seen[b] = 1;
+            p->free_stack[n - 1 - i] = (int32_t)b;
+        }
+    } else {
+        for (int64_t i = 0; i < n; ++i) p->free_stack[n - 1 - i] = (int32_t)i;
+    }
+    *out = p;
+    return PKV_OK;
+}
+
+pkv_status pkv_pool_destroy(pkv_pool* pool)
+{
+    if (!pool) return fail(PKV_E_INVALID, "pool is NULL");
+    delete pool;
+    return PKV_OK;
+}
+
+// ---------------------------------------------------------- block manager
+
+pkv_status pkv_seq_grow(pkv_pool* pool, int64_t seq_id, int64_t new_len)
+{
+    if (pkv_status s = check_pool(pool)) return s;
+    auto it = pool->seqs.find(seq_id);
+    const int64_t cur_len = it == pool->seqs.end() ? 0 : it->second.len;
+    const int64_t cur_blocks = it == pool->seqs.end() ? 0 : (int64_t)it->second.table.size();
+    if (new_len < cur_len) return fail(PKV_E_INVALID, "seq %lld: new_len %lld below current length %lld",
+                                       (long long)seq_id, (long long)new_len, (long long)cur_len);
+    const int64_t need = (new_len + pkv::kBlockSize - 1) / pkv::kBlockSize - cur_blocks;
+    if (need > (int64_t)pool->free_stack.size())
+        return fail(PKV_E_NOMEM, "seq %lld needs %lld blocks, %zu free", (long long)seq_id, (long long)need,
+                    pool->free_stack.size());
+    pkv::Seq& s = pool->seqs[seq_id];
+    for (int64_t i = 0; i < need; ++i) {
+        const int32_t b = pool->free_stack.back();
+        pool->free_stack.pop_back();
+        pool->ref[b] = 1;
+        s.table.push_back(b);
+    }
+    s.len = new_len;
+    return PKV_OK;
+}
+
+pkv_status pkv_seq_share_prefix(pkv_pool* pool, int64_t dst, int64_t src, int64_t n_blocks)
+{
+    if (pkv_status s = check_pool(pool)) return s;
+    auto it = pool->seqs.find(src);
+    if (it == pool->seqs.end()) return fail(PKV_E_INVALID, "unknown source sequence %lld", (long long)src);
+    if (dst == src || pool->seqs.count(dst)) return fail(PKV_E_INVALID, "destination %lld already exists", (long long)dst);
+    if (n_blocks < 0 || n_blocks * pkv::kBlockSize > it->second.len)
+        return fail(PKV_E_INVALID, "only full blocks of the source can be shared");
+    std::vector<int32_t> shared(it->second.table.begin(), it->second.table.begin() + n_blocks);
+    for (int32_t b : shared) pool->ref[b] += 1;
+    pkv::Seq& d = pool->seqs[dst];
+    d.table = std::move(shared);
+    d.len = n_blocks * pkv::kBlockSize;
+    return PKV_OK;
+}
+
+pkv_status pkv_seq_free(pkv_pool* pool, int64_t seq_id)
+{
+    if (pkv_status s = check_pool(pool)) return s;
+    auto it = pool->seqs.find(seq_id);
+    if (it == pool->seqs.end()) return fail(PKV_E_INVALID, "unknown sequence %lld", (long long)seq_id);
+    for (int32_t b : it->second.table)
+        if (--pool->ref[b] == 0) pool->free_stack.push_back(b);
+    pool->seqs.erase(it);
+    return PKV_OK;
+}
+
+int64_t pkv_free_blocks(const pkv_pool* pool) { return pool ? (int64_t)pool->free_stack.size() : -1; }
+
+int32_t pkv_ref_count(const pkv_pool* pool, int64_t block)
+{
+    if (!pool || block < 0 || block >= pool->desc.num_blocks) return -1;
+    return pool->ref[block];
+}
+
+int64_t pkv_seq_len(const pkv_pool* pool, int64_t seq_id)
+{
+    if (!pool) return -1;
+    auto it = pool->seqs.find(seq_id);
+    return it == pool->seqs.end() ? -1 : it->second.len;
+}
+
+pkv_status pkv_block_table(const pkv_pool* pool, int64_t seq_id, int32_t* out, int64_t capacity, int64_t* n_out)
+{
+    if (pkv_status s = check_pool(pool)) return s;
+    auto it = pool->seqs.find(seq_id);
+    if (it == pool->seqs.end()) return fail(PKV_E_INVALID, "unknown sequence %lld", (long long)seq_id);
+    const int64_t n = (int64_t)it->second.table.size();
+    if (n_out) *n_out = n;
+    if (capacity < n || (n > 0 && !out)) return fail(PKV_E_INVALID, "capacity %lld < table length %lld",
+                                                     (long long)capacity, (long long)n);
+    std::copy(it->second.table.begin(), it->second.table.end(), out);
+    return PKV_OK;
+}
+
+pkv_status pkv_build_step(const pkv_pool* pool, const int64_t* seq_ids, const int32_t* q_lens, int32_t num_seqs,
+                          int32_t max_blocks, int32_t* block_tables, int32_t* ctx_lens, int64_t* slot_mapping,
+                          int32_t* q_start_loc)
+{
+    if (pkv_status s = check_pool(pool)) return s;
+    if (num_seqs < 0 || max_blocks < 1) return fail(PKV_E_INVALID, "num_seqs < 0 or max_blocks < 1");
+    if (num_seqs > 0 && (!seq_ids || !q_lens || !block_tables || !ctx_lens || !slot_mapping || !q_start_loc))
+        return fail(PKV_E_INVALID, "NULL array");
+    if (num_seqs == 0) {
+        if (q_start_loc) q_start_loc[0] = 0;
+        return PKV_OK;
+    }
+    // validate everything first so that a refusal writes nothing
+    int64_t total = 0;
+    for (int32_t i = 0; i < num_seqs; ++i) {
+        auto it = pool->seqs.find(seq_ids[i]);
+        if (it == pool->seqs.end()) return fail(PKV_E_INVALID, "row %d: unknown sequence %lld", i, (long long)seq_ids[i]);
+        const pkv::Seq& s = it->second;
+        if (q_lens[i] < 1 || q_lens[i] > s.len) return fail(PKV_E_INVALID, "row %d: q_len %d outside [1, %lld]", i,
+                                                            q_lens[i], (long long)s.len);
+        if ((int64_t)s.table.size() > max_blocks)
+            return fail(PKV_E_INVALID, "row %d: %zu blocks exceed max_blocks %d", i, s.table.size(), max_blocks);
+        if (s.len > INT32_MAX) return fail(PKV_E_INVALID, "row %d: length exceeds int32", i);
+        for (int64_t p = s.len - q_lens[i]; p < s.len; ++p)
+            if (pool->ref[s.table[p / pkv::kBlockSize]] != 1)
+                return fail(PKV_E_SHARED, "row %d: position %lld falls in a shared block", i, (long long)p);
+        for (int32_t j = 0; j < i; ++j)
+            if (seq_ids[j] == seq_ids[i]) return fail(PKV_E_INVALID, "sequence %lld listed twice", (long long)seq_ids[i]);
+        total += q_lens[i];
+        if (total > INT32_MAX) return fail(PKV_E_INVALID, "too many tokens");
+    }
+    int64_t tok = 0;
+    q_start_loc[0] = 0;
+    for (int32_t i = 0; i < num_seqs; ++i) {
+        const pkv::Seq& s = pool->seqs.find(seq_ids[i])->second;
+        int32_t* row = block_tables + (int64_t)i * max_blocks;
+        std::fill(row, row + max_blocks, -1);
+        std::copy(s.table.begin(), s.table.end(), row);
+        ctx_lens[i] = (int32_t)s.len;
+        for (int64_t p = s.len - q_lens[i]; p < s.len; ++p)
+            slot_mapping[tok++] = (int64_t)s.table[p / pkv::kBlockSize] * pkv::kBlockSize + p % pkv::kBlockSize;
+        q_start_loc[i + 1] = (int32_t)tok;
+    }
+    return PKV_OK;
+}
+
+// ---------------------------------------------------------------- kernels
+
+static pkv_status check_layer(const pkv_pool* pool, int32_t layer)
+{
+    if (layer < 0 || layer >= pool->desc.num_layers)
+        return fail(PKV_E_INVALID, "layer %d outside [0, %d)", layer, pool->desc.num_layers);
+    return PKV_OK;
+}
+
+pkv_status pkv_kv_append(pkv_pool* pool, int32_t layer, const void* k, const void* v, const int64_t* slot_mapping,
+                         int32_t num_tokens, void* stream)
+{
+    if (pkv_status s = check_device_pool(pool)) return s;
+    if (pkv_status s = check_layer(pool, layer)) return s;
+    if (num_tokens < 0) return fail(PKV_E_INVALID, "num_tokens < 0");
+    if (num_tokens == 0) return PKV_OK;
+    if (!k || !v || !slot_mapping) return fail(PKV_E_INVALID, "NULL k, v or slot_mapping");
+    if (!aligned(k, 16) || !aligned(v, 16) || !aligned(slot_mapping, 8))
+        return fail(PKV_E_INVALID, "k/v must be 16-byte aligned, slot_mapping 8-byte aligned");
+    DeviceGuard dg(pool->device);
+    if (!dg.ok) return fail(PKV_E_DEVICE, "cannot select the pool's device");
+    cudaError_t e = pkv::launch_kv_append(pool->geom, layer, k, v, slot_mapping, num_tokens, pool->status_dev,
+                                          static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PKV_OK : pkv::cuda_fail(e, "kv_append launch");
+}
+
+size_t pkv_decode_workspace_bytes(const pkv_pool* pool, int32_t num_seqs, int32_t max_blocks)
+{
+    if (!pool || num_seqs < 0 || max_blocks < 1) return 0;
+    return pkv::decode_workspace_bytes(num_seqs, pool->desc.num_heads, max_blocks, pool->partition_tokens);
+}
+
+static pkv_status check_decode(pkv_pool* pool, int32_t layer, const void* q, const int32_t* tables, int32_t max_blocks,
+                               const int32_t* ctx_lens, int32_t num_seqs, const void* out, const void* ws,
+                               size_t ws_bytes)
+{
+    if (pkv_status s = check_device_pool(pool)) return s;
+    if (pkv_status s = check_layer(pool, layer)) return s;
+    if (num_seqs < 0 || max_blocks < 1 || max_blocks > (1 << 26))
+        return fail(PKV_E_INVALID, "num_seqs < 0 or max_blocks outside [1, 2^26]");
+    if (num_seqs > 65535) return fail(PKV_E_INVALID, "num_seqs above 65,535");
+    if (num_seqs == 0) return PKV_OK;
+    if (!q || !tables || !ctx_lens || !out) return fail(PKV_E_INVALID, "NULL q, tables, ctx_lens or out");
+    if (!aligned(q, 16) || !aligned(out, 16) || !aligned(tables, 4) || !aligned(ctx_lens, 4))
+        return fail(PKV_E_INVALID, "q/out must be 16-byte aligned, tables/ctx_lens 4-byte aligned");
+    const size_t need = pkv::decode_workspace_bytes(num_seqs, pool->desc.num_heads, max_blocks, pool->partition_tokens);
+    if (pkv::decode_max_parts(max_blocks, pool->partition_tokens) > 1) {
+        if (!ws || ws_bytes < need || !aligned(ws, 256))
+            return fail(PKV_E_INVALID, "workspace NULL, unaligned or below %zu bytes", need);
+    }
+    return PKV_OK;
+}
+
+pkv_status pkv_decode_attn(pkv_pool* pool, int32_t layer, const void* q, const int32_t* block_tables,
+                           int32_t max_blocks, const int32_t* ctx_lens, int32_t num_seqs, float scale, void* out,
+                           void* workspace, size_t workspace_bytes, void* stream)
+{
+    if (pkv_status s = check_decode(pool, layer, q, block_tables, max_blocks, ctx_lens, num_seqs, out, workspace,
+                                    workspace_bytes))
+        return s;
+    if (num_seqs == 0) return PKV_OK;
+    DeviceGuard dg(pool->device);
+    if (!dg.ok) return fail(PKV_E_DEVICE, "cannot select the pool's device");
+    cudaError_t e = pkv::launch_decode(pool->geom, layer, q, block_tables, max_blocks, ctx_lens, num_seqs, scale, out,
+                                       workspace, pool->partition_tokens, pool->status_dev,
+                                       static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PKV_OK : pkv::cuda_fail(e, "decode launch");
+}
+
+pkv_status pkv_prefill_attn(pkv_pool* pool, int32_t layer, const void* q, const int32_t* q_start_loc,
+                            const int32_t* block_tables, int32_t max_blocks, const int32_t* ctx_lens, int32_t num_seqs,
+                            int32_t max_q_len, float scale, void* out, void* stream)
+{
+    if (pkv_status s = check_device_pool(pool)) return s;
+    if (pkv_status s = check_layer(pool, layer)) return s;
+    if (num_seqs < 0 || max_blocks < 1 || max_q_len < 0) return fail(PKV_E_INVALID, "bad sizes");
+    if (num_seqs == 0 || max_q_len == 0) return PKV_OK;
+    if (num_seqs > 65535) return fail(PKV_E_INVALID, "num_seqs above 65,535");
+    if (!q || !q_start_loc || !block_tables || !ctx_lens || !out) return fail(PKV_E_INVALID, "NULL argument");
+    if (!aligned(q, 16) || !aligned(out, 16)) return fail(PKV_E_INVALID, "q/out must be 16-byte aligned");
+    if (!pool->kv_tmap_ok) return fail(PKV_E_DEVICE, "TMA descriptor for the pool could not be encoded");
+    DeviceGuard dg(pool->device);
+    if (!dg.ok) return fail(PKV_E_DEVICE, "cannot select the pool's device");
+    cudaError_t e = pkv::launch_prefill(pool, layer, q, q_start_loc, block_tables, max_blocks, ctx_lens, num_seqs,
+                                        max_q_len, scale, out, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PKV_OK : pkv::cuda_fail(e, "prefill launch");
+}
+
+// ------------------------------------------------------------------- step
+
+size_t pkv_step_workspace_bytes(const pkv_pool* pool, const pkv_step_desc* st)
+{
+    if (!pool || !st || st->num_decode < 0 || st->max_blocks < 1) return 0;
+    return pkv::decode_workspace_bytes(st->num_decode, pool->desc.num_heads, st->max_blocks, pool->partition_tokens);
+}
+
+pkv_status pkv_step(pkv_pool* pool, const pkv_step_desc* st, void* workspace, size_t workspace_bytes, void* stream)
+{
+    if (pkv_status s = check_device_pool(pool)) return s;
+    if (!st) return fail(PKV_E_INVALID, "step is NULL");
+    const int B = st->num_decode, P = st->num_prefill;
+    if (B < 0 || P < 0 || st->num_tokens < B + P || st->max_blocks < 1 || st->num_layers < 0)
+        return fail(PKV_E_INVALID, "bad step sizes");
+    if (P > 0 && st->max_q_len < 1) return fail(PKV_E_INVALID, "prefill rows need max_q_len >= 1");
+    if (P == 0 && st->num_tokens != B) return fail(PKV_E_INVALID, "decode-only step must have num_tokens == num_decode");
+    if (st->first_layer < 0 || st->first_layer + st->num_layers > pool->desc.num_layers)
+        return fail(PKV_E_INVALID, "layer range outside the pool");
+    if (st->num_layers == 0 || st->num_tokens == 0) return PKV_OK;
+    if (!st->block_tables || !st->ctx_lens || !st->slot_mapping || !st->q || !st->k || !st->v || !st->out)
+        return fail(PKV_E_INVALID, "NULL step array");
+    if (P > 0 && !st->q_start_loc) return fail(PKV_E_INVALID, "prefill rows need q_start_loc");
+    const int64_t tok_elems = (int64_t)pool->desc.num_heads * pkv::kHeadDim;
+    if (st->q_layer_stride % 8 || st->k_layer_stride % 8 || st->v_layer_stride % 8 || st->out_layer_stride % 8)
+        return fail(PKV_E_INVALID, "layer strides must be multiples of 8 elements");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const char* q = static_cast<const char*>(st->q);
+    const char* k = static_cast<const char*>(st->k);
+    const char* v = static_cast<const char*>(st->v);
+    char* out = static_cast<char*>(st->out);
+    for (int32_t i = 0; i < st->num_layers; ++i) {
+        const int32_t layer = st->first_layer + i;
+        const int64_t li = i;
+        const char* ql = q + li * st->q_layer_stride * 2;
+        char* ol = out + li * st->out_layer_stride * 2;
+        pkv_status r = pkv_kv_append(pool, layer, k + li * st->k_layer_stride * 2, v + li * st->v_layer_stride * 2,
+                                     st->slot_mapping, st->num_tokens, stream);
+        if (r) return r;
+        if (B > 0) {
+            r = pkv_decode_attn(pool, layer, ql, st->block_tables, st->max_blocks, st->ctx_lens, B, st->scale, ol,
+                                workspace, workspace_bytes, stream);
+            if (r) return r;
+        }
+        if (P > 0) {
+            r = pkv_prefill_attn(pool, layer, ql, st->q_start_loc + B, st->block_tables + (int64_t)B * st->max_blocks,
+                                 st->max_blocks, st->ctx_lens + B, P, st->max_q_len, st->scale, ol, stream);
+            if (r) return r;
+        }
+    }
+    (void)tok_elems;
+    (void)s;
+    return PKV_OK;
+}
+
+// ----------------------------------------------------------------- status
+
+pkv_status pkv_get_status(pkv_pool* pool, void* stream, uint32_t* device_flags)
+{
+    if (pkv_status s = check_device_pool(pool)) return s;
+    DeviceGuard dg(pool->device);
+    if (!dg.ok) return fail(PKV_E_DEVICE, "cannot select the pool's device");
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return pkv::cuda_fail(e, "stream synchronize");
+    unsigned int flags = 0;
+    e = cudaMemcpy(&flags, pool->status_dev, sizeof(flags), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return pkv::cuda_fail(e, "read status word");
+    if (flags) {
+        const unsigned int zero = 0;
+        e = cudaMemcpy(pool->status_dev, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) return pkv::cuda_fail(e, "clear status word");
+    }
+    if (device_flags) *device_flags = flags;
+    if (flags & PKV_DEV_TIMEOUT) return fail(PKV_E_TIMEOUT, "a kernel's bounded wait ran out (flags 0x%x)", flags);
+    if (flags) return fail(PKV_E_DEVICE, "a kernel rejected a device-side input (flags 0x%x)", flags);
+    return PKV_OK;
+}
+
+pkv_status pkv_debug_wait_probe(pkv_pool* pool, uint64_t timeout_ns, void* stream)
+{
+    if (pkv_status s = check_device_pool(pool)) return s;
+    if (timeout_ns > 10ull * 1000 * 1000 * 1000) return fail(PKV_E_INVALID, "timeout above 10 s");
+    DeviceGuard dg(pool->device);
+    if (!dg.ok) return fail(PKV_E_DEVICE, "cannot select the pool's device");
+    cudaError_t e = pkv::launch_wait_probe(timeout_ns, pool->status_dev, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PKV_OK : pkv::cuda_fail(e, "probe launch");
+}
+
+}  // extern "C"

@@ -1,0 +1,78 @@
+// pkv_internal.h — shared between libpkv's host code and its kernel launchers.
+#pragma once
+#include <cstdint>
+#include <string>
+#include <unordered_map>
+#include <vector>
+
+#include <cuda_runtime.h>
+
+#include "pkv.h"
+
+namespace pkv {
+
+constexpr int kHeadDim = 128;
+constexpr int kBlockSize = 16;
+constexpr int kTileBytes = kBlockSize * kHeadDim * 2;  // one head of one block: 4,096 B
+constexpr int kDefaultPartition = 512;
+constexpr int kMaxPartition = 2048;
+
+struct Seq {
+    std::vector<int32_t> table;
+    int64_t len = 0;
+};
+
+// Geometry of the device pool in bytes, for the kernels.
+struct PoolGeom {
+    const char* base;
+    int64_t num_blocks;
+    int32_t num_layers;
+    int32_t num_heads;
+    int64_t block_bytes;  // one block, all layers: L * 2 * H * 4096
+    int64_t layer_bytes;  // one layer of one block: 2 * H * 4096
+    int64_t kv_bytes;     // K half to V half: H * 4096
+};
+
+struct alignas(64) TensorMap128 {
+    alignas(64) unsigned char bytes[128];
+};
+
+}  // namespace pkv
+
+struct pkv_pool {
+    pkv_pool_desc desc;
+    int device = 0;
+    bool host_only = false;  // created without device memory: block manager only
+    int partition_tokens = pkv::kDefaultPartition;
+    unsigned int* status_dev = nullptr;  // sticky device error word of this device
+    pkv::PoolGeom geom{};
+    pkv::TensorMap128 kv_tmap{};  // 5-D TMA map over the pool (prefill K/V tiles)
+    bool kv_tmap_ok = false;
+    std::vector<int32_t> ref;
+    std::vector<int32_t> free_stack;  // back() is handed out next
+    std::unordered_map<int64_t, pkv::Seq> seqs;
+};
+
+namespace pkv {
+
+pkv_status fail(pkv_status s, const char* fmt, ...);
+pkv_status cuda_fail(cudaError_t e, const char* what);
+
+// pkv_kernels.cu
+cudaError_t status_word(int device, unsigned int** out);
+cudaError_t launch_kv_append(const PoolGeom& g, int layer, const void* k, const void* v, const int64_t* slots,
+                             int num_tokens, unsigned int* status, cudaStream_t stream);
+int decode_max_parts(int max_blocks, int partition_tokens);
+size_t decode_workspace_bytes(int num_seqs, int num_heads, int max_blocks, int partition_tokens);
+cudaError_t launch_decode(const PoolGeom& g, int layer, const void* q, const int32_t* tables, int max_blocks,
+                          const int32_t* ctx_lens, int num_seqs, float scale, void* out, void* ws,
+                          int partition_tokens, unsigned int* status, cudaStream_t stream);
+cudaError_t launch_wait_probe(uint64_t timeout_ns, unsigned int* status, cudaStream_t stream);
+
+// pkv_prefill.cu
+bool encode_kv_tmap(const PoolGeom& g, TensorMap128* out, std::string* err);
+cudaError_t launch_prefill(const pkv_pool* pool, int layer, const void* q, const int32_t* q_start,
+                           const int32_t* tables, int max_blocks, const int32_t* ctx_lens, int num_seqs,
+                           int max_q_len, float scale, void* out, cudaStream_t stream);
+
+}  // namespace pkv

@@ -1,0 +1,446 @@
+// pkv_kernels.cu — kv_append (reshape_and_cache), split-K paged decode
+// attention and its partition merge, for sm_103a.
+//
+// Pool layout (one block = every layer of 16 token positions):
+//   [block][layer][K,V][head][16 tokens][128 dims] FP16
+// so one head's K (or V) for one block is a contiguous 4,096-byte tile, and
+// consecutive heads of the same block/layer are 4,096 B apart
+// ("llm-inference-batching" (faangrind), the KV pool listing).
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "pkv_internal.h"
+#include "ptx.cuh"
+
+namespace pkv {
+
+// Sticky per-device error word (PKV_DEV_* bits). Host code takes its device
+// address once per device with cudaGetSymbolAddress and passes it to kernels.
+__device__ unsigned int g_status_word;
+
+cudaError_t status_word(int device, unsigned int** out)
+{
+    int cur = 0;
+    cudaError_t e = cudaGetDevice(&cur);
+    if (e != cudaSuccess) return e;
+    if (cur != device && (e = cudaSetDevice(device)) != cudaSuccess) return e;
+    e = cudaGetSymbolAddress(reinterpret_cast<void**>(out), g_status_word);
+    if (cur != device) cudaSetDevice(cur);
+    return e;
+}
+
+// ======================================================================
+// kv_append: one thread moves one 16-byte chunk. A token's K row for one
+// head is 256 B (16 chunks) and lands at tile offset (slot % 16) * 256 of
+// its block's (layer, K, head) tile; V likewise in the V half.
+// "llm-inference-batching", step 7: new keys and values are appended.
+
+__global__ void __launch_bounds__(256) kv_append_kernel(char* __restrict__ pool, int64_t block_bytes,
+                                                        int64_t layer_off, int64_t kv_bytes, int num_heads,
+                                                        const uint4* __restrict__ k, const uint4* __restrict__ v,
+                                                        const int64_t* __restrict__ slots, int num_tokens,
+                                                        int64_t num_slots, unsigned int* status)
+{
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t per_token = 2LL * num_heads * 16;
+    if (i >= per_token * num_tokens) return;
+    const int tok = (int)(i / per_token);
+    const int rem = (int)(i - (int64_t)tok * per_token);
+    const int kv = rem / (num_heads * 16);
+    const int h = (rem / 16) % num_heads;
+    const int chunk = rem & 15;
+    const int64_t slot = __ldg(slots + tok);
+    if (slot < 0 || slot >= num_slots) {
+        if (rem == 0) atomicOr(status, PKV_DEV_BAD_SLOT);
+        return;
+    }
+    const int64_t blk = slot >> 4;
+    const int t = (int)(slot & 15);
+    char* dst = pool + blk * block_bytes + layer_off + kv * kv_bytes + (int64_t)h * kTileBytes + t * 256 + chunk * 16;
+    const uint4* src = (kv ? v : k) + ((int64_t)tok * num_heads + h) * 16 + chunk;
+    *reinterpret_cast<uint4*>(dst) = __ldg(src);
+}
+
+cudaError_t launch_kv_append(const PoolGeom& g, int layer, const void* k, const void* v, const int64_t* slots,
+                             int num_tokens, unsigned int* status, cudaStream_t stream)
+{
+    if (num_tokens == 0) return cudaSuccess;
+    const int64_t total = 2LL * g.num_heads * 16 * num_tokens;
+    const int threads = 256;
+    const int64_t blocks = (total + threads - 1) / threads;
+    kv_append_kernel<<<(unsigned)blocks, threads, 0, stream>>>(
+        const_cast<char*>(g.base), g.block_bytes, (int64_t)layer * g.layer_bytes, g.kv_bytes, g.num_heads,
+        static_cast<const uint4*>(k), static_cast<const uint4*>(v), slots, num_tokens, g.num_blocks * kBlockSize,
+        status);
+    return cudaGetLastError();
+}
+
+// ======================================================================
+// Decode attention.
+//
+// One CTA = (partition p, head h, row r); a partition is partition_tokens
+// consecutive keys (a whole number of blocks). Its WARPS warps take the
+// partition's blocks round-robin; each warp is an independent streaming
+// consumer with a private ring of STAGES stages, one block (K tile + V tile,
+// 8 KB) per stage, filled by 1-D bulk async copies that complete on an
+// mbarrier. Lane 0 of the warp issues the copies; the whole warp consumes.
+//
+// Per block: lane = (token t = lane/2, half hf = lane%2) forms q.k_t over 64
+// dims (the two halves meet with one shuffle), the warp takes the block max
+// (online softmax in the log2 domain, the scale pre-multiplied by log2 e),
+// and each lane then owns 4 output dims for the P.V update.
+//
+// The warps' states merge in shared memory in fixed order; a partition
+// either writes the final FP16 row (single-partition rows) or its
+// un-normalised output, max and sum to the workspace for reduce_kernel.
+// The partition plan depends only on ctx_len and partition_tokens, so a
+// row's result is the same in any batch.
+
+constexpr int kDecodeWarps = 4;
+constexpr int kDecodeStages = 2;
+constexpr int kStageBytes = 2 * kTileBytes;
+
+struct DecodeArgs {
+    const char* pool;
+    int64_t block_bytes;
+    int64_t head_off;   // layer * layer_bytes (the head offset is added per CTA)
+    int64_t kv_bytes;
+    int64_t num_blocks;
+    int num_heads;
+    const __half* q;
+    const int32_t* tables;
+    int max_blocks;
+    const int32_t* ctx_lens;
+    float scale_log2;
+    __half* out;
+    float* ws_o;   // [B][H][max_parts][128]
+    float* ws_ml;  // [B][H][max_parts][2]
+    int max_parts;
+    int part_tokens;
+    unsigned int* status;
+};
+
+template <int WARPS, int STAGES>
+struct DecodeLayout {
+    static constexpr int kRing = WARPS * STAGES * kStageBytes;
+    static constexpr int kPbuf = kRing;                        // [WARPS][16] float
+    static constexpr int kStats = kPbuf + WARPS * 16 * 4;      // [WARPS][2] float
+    static constexpr int kBars = kStats + WARPS * 2 * 4;       // [WARPS][STAGES][2] u64
+    static constexpr int kBytes = kBars + WARPS * STAGES * 2 * 8;
+};
+
+template <int WARPS, int STAGES>
+__global__ void __launch_bounds__(WARPS * 32) decode_kernel(const DecodeArgs a)
+{
+    using Lay = DecodeLayout<WARPS, STAGES>;
+    extern __shared__ __align__(1024) unsigned char smem[];
+    const int p = blockIdx.x, h = blockIdx.y, r = blockIdx.z;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    const int ctx = __ldg(a.ctx_lens + r);
+    if (ctx < 1 || ctx > a.max_blocks * kBlockSize) {
+        if (p == 0 && h == 0 && threadIdx.x == 0) atomicOr(a.status, PKV_DEV_BAD_CTX);
+        return;
+    }
+    const int nparts = (ctx + a.part_tokens - 1) / a.part_tokens;
+    if (p >= nparts) return;
+    const int blk_lo = (p * a.part_tokens) >> 4;
+    const int blk_hi = (min((p + 1) * a.part_tokens, ctx) + 15) >> 4;
+    const int nblk = blk_hi - blk_lo;
+    int count = nblk > warp ? (nblk - warp + WARPS - 1) / WARPS : 0;  // <= 32 by construction
+
+    unsigned char* ring = smem + warp * STAGES * kStageBytes;
+    float* pbuf = reinterpret_cast<float*>(smem + Lay::kPbuf) + warp * 16;
+    float* stats = reinterpret_cast<float*>(smem + Lay::kStats);
+    const uint32_t bar0 = smem_u32(smem + Lay::kBars) + warp * STAGES * 16;
+
+    // Physical block ids of this warp's blocks: lane i holds the i-th.
+    const int32_t* trow = a.tables + (int64_t)r * a.max_blocks;
+    int my_id = 0;
+    bool bad = false;
+    if (lane < count) {
+        my_id = __ldg(trow + blk_lo + warp + lane * WARPS);
+        bad = my_id < 0 || (int64_t)my_id >= a.num_blocks;
+    }
+    if (__any_sync(0xffffffffu, bad)) {
+        if (lane == 0) atomicOr(a.status, PKV_DEV_BAD_BLOCK);
+        count = 0;
+    }
+
+    const char* kbase = a.pool + a.head_off + (int64_t)h * kTileBytes;
+    if (lane == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(bar0 + 16 * s, 1);
+            mbar_init(bar0 + 16 * s + 8, 1);
+        }
+        fence_mbar_init();
+    }
+    __syncwarp();
+
+    // Prologue: fill the ring.
+#pragma unroll
+    for (int s = 0; s < STAGES; ++s) {
+        const int id = __shfl_sync(0xffffffffu, my_id, s);
+        if (s < count && lane == 0) {
+            const char* src = kbase + (int64_t)id * a.block_bytes;
+            const uint32_t dst = smem_u32(ring + s * kStageBytes);
+            mbar_arrive_expect_tx(bar0 + 16 * s, kTileBytes);
+            bulk_g2s(dst, src, kTileBytes, bar0 + 16 * s);
+            mbar_arrive_expect_tx(bar0 + 16 * s + 8, kTileBytes);
+            bulk_g2s(dst + kTileBytes, src + a.kv_bytes, kTileBytes, bar0 + 16 * s + 8);
+        }
+    }
+
+    // q, rotated per lane so that the K-tile reads below are free of bank
+    // conflicts: register chunk j holds dims hf*64 + ((j + lane) & 7)*8 .. +8.
+    const int t = lane >> 1, hf = lane & 1;
+    float qf[8][8];
+    {
+        const __half* qrow = a.q + ((int64_t)r * a.num_heads + h) * kHeadDim + hf * 64;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const uint4 raw = __ldg(reinterpret_cast<const uint4*>(qrow + ((j + lane) & 7) * 8));
+            half8_to_float(raw, qf[j]);
+        }
+    }
+
+    float m_run = -INFINITY, l_lane = 0.f;
+    float o[4] = {0.f, 0.f, 0.f, 0.f};
+    bool timed_out = false;
+    int i = 0;
+    for (; i < count; ++i) {
+        const int s = i % STAGES;
+        const uint32_t par = (uint32_t)(i / STAGES) & 1u;
+        const uint32_t bk = bar0 + 16 * s, bv = bk + 8;
+        const unsigned char* kt = ring + s * kStageBytes;
+        const unsigned char* vt = kt + kTileBytes;
+        const int key0 = (blk_lo + warp + i * WARPS) * kBlockSize;
+        const int nvalid = min(kBlockSize, ctx - key0);
+
+        if (!mbar_wait(bk, par)) { timed_out = true; break; }
+        float acc = 0.f;
+        {
+            const uint4* krow = reinterpret_cast<const uint4*>(kt + t * 256 + hf * 128);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                float kf[8];
+                half8_to_float(krow[(j + lane) & 7], kf);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc = fmaf(qf[j][e], kf[e], acc);
+            }
+        }
+        acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+        const float sc = (t < nvalid) ? acc * a.scale_log2 : -INFINITY;
+        float mb = sc;
+        mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
+        mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 4));
+        mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 8));
+        mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 16));
+        const float m_new = fmaxf(m_run, mb);
+        const float alpha = exp2f(m_run - m_new);
+        const float pt = exp2f(sc - m_new);
+        l_lane = l_lane * alpha + (hf == 0 ? pt : 0.f);
+        m_run = m_new;
+        if (hf == 0) pbuf[t] = pt;
+        __syncwarp();
+
+        if (!mbar_wait(bv, par)) { timed_out = true; break; }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[e] *= alpha;
+        {
+            const float4* pp = reinterpret_cast<const float4*>(pbuf);
+            const unsigned char* vcol = vt + lane * 8;
+#pragma unroll
+            for (int tq = 0; tq < 4; ++tq) {
+                const float4 p4 = pp[tq];
+                const float pv[4] = {p4.x, p4.y, p4.z, p4.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int tt = tq * 4 + e;
+                    if (tt < nvalid) {  // rows past ctx may hold anything, even NaN
+                        float vf[4];
+                        half4_to_float(*reinterpret_cast<const uint2*>(vcol + tt * 256), vf);
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) o[c] = fmaf(pv[e], vf[c], o[c]);
+                    }
+                }
+            }
+        }
+        __syncwarp();
+        if (i + STAGES < count) {
+            const int id = __shfl_sync(0xffffffffu, my_id, i + STAGES);
+            if (lane == 0) {
+                fence_proxy_async_smem();
+                const char* src = kbase + (int64_t)id * a.block_bytes;
+                const uint32_t dst = smem_u32(ring + s * kStageBytes);
+                mbar_arrive_expect_tx(bk, kTileBytes);
+                bulk_g2s(dst, src, kTileBytes, bk);
+                mbar_arrive_expect_tx(bv, kTileBytes);
+                bulk_g2s(dst + kTileBytes, src + a.kv_bytes, kTileBytes, bv);
+            }
+        }
+    }
+    if (timed_out) {
+        // Give the copies still in flight into this warp's ring a bounded
+        // chance to land before the shared memory is reused or released.
+        if (lane == 0) atomicOr(a.status, PKV_DEV_TIMEOUT);
+        for (int k = i; k < count && k < i + STAGES; ++k) {
+            const uint32_t bk = bar0 + 16 * (k % STAGES);
+            const uint32_t par = (uint32_t)(k / STAGES) & 1u;
+            mbar_wait(bk, par);
+            mbar_wait(bk + 8, par);
+        }
+    }
+
+    // Merge the warps. Warp w's partial output goes into its own (now idle) ring.
+    float l_w = l_lane;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) l_w += __shfl_xor_sync(0xffffffffu, l_w, off);
+    float* mo = reinterpret_cast<float*>(ring);
+    *reinterpret_cast<float4*>(mo + lane * 4) = make_float4(o[0], o[1], o[2], o[3]);
+    if (lane == 0) {
+        stats[warp * 2] = m_run;
+        stats[warp * 2 + 1] = l_w;
+    }
+    __syncthreads();
+
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < WARPS; ++w) M = fmaxf(M, stats[w * 2]);
+    float L = 0.f, wt[WARPS];
+#pragma unroll
+    for (int w = 0; w < WARPS; ++w) {
+        wt[w] = (stats[w * 2] == -INFINITY) ? 0.f : exp2f(stats[w * 2] - M);
+        L = fmaf(wt[w], stats[w * 2 + 1], L);
+    }
+    const int64_t rh = (int64_t)r * a.num_heads + h;
+    for (int d = threadIdx.x; d < kHeadDim; d += WARPS * 32) {
+        float O = 0.f;
+#pragma unroll
+        for (int w = 0; w < WARPS; ++w) {
+            const float* mw = reinterpret_cast<const float*>(smem + w * STAGES * kStageBytes);
+            O = fmaf(wt[w], mw[d], O);
+        }
+        if (nparts == 1) {
+            a.out[rh * kHeadDim + d] = __float2half_rn(O / L);
+        } else {
+            const int64_t slot = rh * a.max_parts + p;
+            a.ws_o[slot * kHeadDim + d] = O;
+            if (d == 0) {
+                a.ws_ml[slot * 2] = M;
+                a.ws_ml[slot * 2 + 1] = L;
+            }
+        }
+    }
+}
+
+// Merge a row's partitions: M = max m_p, out = sum 2^(m_p-M) o_p / sum 2^(m_p-M) l_p
+// ("The inference engine" (wpnews), "IO-aware attention": tiles combine
+// exactly through their softmax statistics).
+__global__ void __launch_bounds__(128) reduce_kernel(const int32_t* __restrict__ ctx_lens, int max_blocks,
+                                                     int num_heads, int part_tokens, int max_parts,
+                                                     const float* __restrict__ ws_o, const float* __restrict__ ws_ml,
+                                                     __half* __restrict__ out)
+{
+    const int h = blockIdx.x, r = blockIdx.y, d = threadIdx.x;
+    const int ctx = __ldg(ctx_lens + r);
+    if (ctx < 1 || ctx > max_blocks * kBlockSize) return;
+    const int nparts = (ctx + part_tokens - 1) / part_tokens;
+    if (nparts <= 1) return;
+    const int64_t base = ((int64_t)r * num_heads + h) * max_parts;
+    float M = -INFINITY;
+    for (int q = 0; q < nparts; ++q) M = fmaxf(M, __ldg(ws_ml + (base + q) * 2));
+    float L = 0.f, O = 0.f;
+    for (int q = 0; q < nparts; ++q) {
+        const float w = exp2f(__ldg(ws_ml + (base + q) * 2) - M);
+        L = fmaf(w, __ldg(ws_ml + (base + q) * 2 + 1), L);
+        O = fmaf(w, __ldg(ws_o + (base + q) * kHeadDim + d), O);
+    }
+    out[((int64_t)r * num_heads + h) * kHeadDim + d] = __float2half_rn(O / L);
+}
+
+int decode_max_parts(int max_blocks, int partition_tokens)
+{
+    const int64_t max_tokens = (int64_t)max_blocks * kBlockSize;
+    return (int)((max_tokens + partition_tokens - 1) / partition_tokens);
+}
+
+size_t decode_workspace_bytes(int num_seqs, int num_heads, int max_blocks, int partition_tokens)
+{
+    const int64_t parts = decode_max_parts(max_blocks, partition_tokens);
+    if (parts <= 1) return 256;
+    const int64_t slots = (int64_t)num_seqs * num_heads * parts;
+    size_t o = (size_t)slots * kHeadDim * sizeof(float);
+    o = (o + 255) & ~(size_t)255;
+    return o + (size_t)slots * 2 * sizeof(float) + 256;
+}
+
+cudaError_t launch_decode(const PoolGeom& g, int layer, const void* q, const int32_t* tables, int max_blocks,
+                          const int32_t* ctx_lens, int num_seqs, float scale, void* out, void* ws,
+                          int partition_tokens, unsigned int* status, cudaStream_t stream)
+{
+    if (num_seqs == 0) return cudaSuccess;
+    using Lay = DecodeLayout<kDecodeWarps, kDecodeStages>;
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 64 && !attr_set[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(decode_kernel<kDecodeWarps, kDecodeStages>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kBytes);
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = true;
+    }
+    DecodeArgs a;
+    a.pool = g.base;
+    a.block_bytes = g.block_bytes;
+    a.head_off = (int64_t)layer * g.layer_bytes;
+    a.kv_bytes = g.kv_bytes;
+    a.num_blocks = g.num_blocks;
+    a.num_heads = g.num_heads;
+    a.q = static_cast<const __half*>(q);
+    a.tables = tables;
+    a.max_blocks = max_blocks;
+    a.ctx_lens = ctx_lens;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    a.out = static_cast<__half*>(out);
+    a.max_parts = decode_max_parts(max_blocks, partition_tokens);
+    a.part_tokens = partition_tokens;
+    a.status = status;
+    const int64_t slots = (int64_t)num_seqs * g.num_heads * a.max_parts;
+    a.ws_o = static_cast<float*>(ws);
+    size_t o_bytes = ((size_t)slots * kHeadDim * sizeof(float) + 255) & ~(size_t)255;
+    a.ws_ml = reinterpret_cast<float*>(static_cast<char*>(ws) + o_bytes);
+    dim3 grid(a.max_parts, g.num_heads, num_seqs);
+    decode_kernel<kDecodeWarps, kDecodeStages><<<grid, kDecodeWarps * 32, Lay::kBytes, stream>>>(a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess || a.max_parts <= 1) return e;
+    reduce_kernel<<<dim3(g.num_heads, num_seqs), kHeadDim, 0, stream>>>(
+        ctx_lens, max_blocks, g.num_heads, partition_tokens, a.max_parts, a.ws_o, a.ws_ml, a.out);
+    return cudaGetLastError();
+}
+
+// ======================================================================
+// Bounded-wait probe: one thread waits on an mbarrier that nothing arrives
+// at, gives up after timeout_ns and records PKV_DEV_TIMEOUT.
+
+__global__ void wait_probe_kernel(uint64_t timeout_ns, unsigned int* status)
+{
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        const uint32_t b = smem_u32(&bar);
+        mbar_init(b, 1);
+        fence_mbar_init();
+        if (!mbar_wait(b, 0, timeout_ns)) atomicOr(status, PKV_DEV_TIMEOUT);
+    }
+}
+
+cudaError_t launch_wait_probe(uint64_t timeout_ns, unsigned int* status, cudaStream_t stream)
+{
+    wait_probe_kernel<<<1, 32, 0, stream>>>(timeout_ns, status);
+    return cudaGetLastError();
+}
+
+}  // namespace pkv

@@ -1,0 +1,172 @@
+"""libpkv's C ABI on the host (no GPU): exported symbols, pool arithmetic,
+argument validation, and the ref-counted block manager against the oracle's
+restatement (oracle/blockmgr.py)."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle import blockmgr
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def pkv():
+    from paged_kv_cache_scatter_gb300 import build
+    build.build()
+    import paged_kv_cache_scatter_gb300 as pkv
+    pkv.load()
+    return pkv
+
+
+def _header_functions():
+    src = open(os.path.join(ROOT, "include", "pkv.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(pkv_\w+)\s*\(", src)))
+
+
+def test_library_exports_every_declared_symbol(pkv):
+    names = _header_functions()
+    assert len(names) >= 20
+    lib = pkv.load()
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing
+    assert set(names) == set(pkv.SIGNATURES), "binding and header disagree"
+
+
+def test_pool_bytes_matches_page_ledger(pkv):
+    assert pkv.Pool.bytes_needed(7152) == 7152 * 8388608 == 59995324416
+    assert pkv.Pool.bytes_needed(1) == oracle.bytes_per_block(oracle.geom(1, 32, 32))
+    assert pkv.Pool.bytes_needed(64, num_layers=1) == 64 * 262144
+    bad = pkv.pkv_pool_desc(10, 32, 32, 64, 16, 0, 0, None, 0, None)
+    assert pkv.load().pkv_pool_bytes(ctypes.byref(bad)) == 0
+
+
+@pytest.mark.parametrize("field,value", [("head_dim", 64), ("block_size", 32), ("dtype", 1), ("num_blocks", 0),
+                                         ("partition_tokens", 100), ("partition_tokens", 4096), ("num_heads", 0)])
+def test_pool_create_refuses_bad_descriptor(pkv, field, value):
+    d = pkv.pkv_pool_desc(16, 2, 4, 128, 16, 0, 0, None, 0, None)
+    setattr(d, field, value)
+    h = ctypes.c_void_p()
+    assert pkv.load().pkv_pool_create(ctypes.byref(d), ctypes.byref(h)) == pkv.PKV_E_INVALID
+    assert pkv.load().pkv_last_error_string()
+
+
+def test_free_order_must_be_a_permutation(pkv):
+    with pytest.raises(pkv.PkvError):
+        pkv.Pool(None, 4, num_layers=1, free_order=[0, 1, 1, 2])
+    p = pkv.Pool(None, 4, num_layers=1, free_order=[3, 0, 2, 1])
+    assert p.seq_grow(0, 40) == pkv.PKV_OK
+    assert list(p.block_table(0)) == [3, 0, 2]
+
+
+def test_host_only_pool_refuses_kernel_calls(pkv):
+    p = pkv.Pool(None, 8, num_layers=1)
+    lib = pkv.load()
+    assert lib.pkv_kv_append(p.handle, 0, 16, 16, 8, 1, None) == pkv.PKV_E_INVALID
+    assert lib.pkv_decode_attn(p.handle, 0, 16, 16, 1, 16, 1, 0.1, 16, None, 0, None) == pkv.PKV_E_INVALID
+    assert lib.pkv_get_status(p.handle, None, None) == pkv.PKV_E_INVALID
+
+
+def _compare(p, bm, seqs):
+    assert p.free_blocks() == bm.free_blocks()
+    for b in range(bm.num_blocks):
+        assert p.ref_count(b) == bm.ref[b]
+    for s in seqs:
+        if s in bm.tables:
+            assert list(p.block_table(s)) == bm.tables[s]
+            assert p.seq_len(s) == bm.lens[s]
+        else:
+            assert p.seq_len(s) == -1
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_block_manager_matches_oracle_under_random_ops(pkv, seed):
+    rng = np.random.default_rng(seed)
+    N = 48
+    order = rng.permutation(N)
+    p = pkv.Pool(None, N, num_layers=2, free_order=order)
+    bm = blockmgr.BlockManager(N, free_order=order)
+    seqs = list(range(8))
+    for _ in range(300):
+        op = rng.integers(0, 5)
+        s = int(rng.choice(seqs))
+        if op <= 1:
+            n = int(rng.integers(0, 200))
+            assert p.seq_grow(s, n) == bm.grow(s, n)
+        elif op == 2:
+            src = int(rng.choice(seqs))
+            nb = int(rng.integers(0, 6))
+            assert p.seq_share_prefix(s, src, nb) == bm.share_prefix(s, src, nb)
+        elif op == 3:
+            assert p.seq_free(s) == bm.free_seq(s)
+        else:
+            live = [x for x in seqs if x in bm.tables]
+            if not live:
+                continue
+            k = int(rng.integers(1, len(live) + 1))
+            rows = [int(x) for x in rng.choice(live, k, replace=False)]
+            qls = [int(rng.integers(1, max(2, bm.lens[r] + 1))) if bm.lens[r] > 0 else 1 for r in rows]
+            want = bm.build_step(rows, qls, 16)
+            got = p.build_step(rows, qls, 16)
+            assert got[0] == want[0]
+            if want[0] == blockmgr.OK:
+                assert np.array_equal(got[1], np.array(want[1], np.int32))
+                assert list(got[2]) == want[2]
+                assert list(got[3]) == want[3]
+                assert list(got[4]) == want[4]
+                # slots agree with the oracle's slot function
+                rot = np.repeat(np.arange(len(rows)), qls)
+                pos = np.concatenate([np.arange(c - q, c) for c, q in zip(want[2], qls)])
+                assert np.array_equal(got[3], oracle.slots(got[1], rot, pos))
+        _compare(p, bm, seqs)
+
+
+def test_soak_returns_every_block_to_the_free_list(pkv):
+    # "llm-inference-batching", Cancellation and memory: after a soak the free list is back at 7,152.
+    rng = np.random.default_rng(0)
+    p = pkv.Pool(None, 7152, free_order=rng.permutation(7152))
+    live = {}
+    nxt = 0
+    for step in range(400):
+        # join
+        while len(live) < 32:
+            n = int(np.clip(rng.lognormal(6.5, 1.0), 50, 8000))
+            if p.seq_grow(nxt, n) == pkv.PKV_E_NOMEM:
+                break
+            live[nxt] = int(rng.integers(1, 300))
+            nxt += 1
+        # decode one token per row; cancel ~2% per step; finish when budget is spent
+        for s in list(live):
+            if rng.random() < 0.02 or live[s] == 0:
+                assert p.seq_free(s) == pkv.PKV_OK
+                del live[s]
+                continue
+            st = p.seq_grow(s, p.seq_len(s) + 1)
+            if st == pkv.PKV_E_NOMEM:           # preempt the row
+                assert p.seq_free(s) == pkv.PKV_OK
+                del live[s]
+                continue
+            live[s] -= 1
+    for s in list(live):
+        assert p.seq_free(s) == pkv.PKV_OK
+    assert p.free_blocks() == 7152
+    assert all(p.ref_count(b) == 0 for b in range(0, 7152, 97))
+
+
+def test_build_step_refuses_writes_into_shared_blocks(pkv):
+    p = pkv.Pool(None, 64, num_layers=1)
+    assert p.seq_grow(0, 40) == pkv.PKV_OK
+    assert p.seq_share_prefix(1, 0, 2) == pkv.PKV_OK
+    assert p.ref_count(int(p.block_table(0)[0])) == 2
+    st = p.build_step([1], [1], 8)[0]
+    assert st == pkv.PKV_E_SHARED          # the last position of seq 1 is inside a shared block
+    assert p.seq_grow(1, 33) == pkv.PKV_OK  # a private block for the new token
+    st, tables, ctx, slots, qs = p.build_step([1, 0], [1, 1], 8)
+    assert st == pkv.PKV_OK and list(ctx) == [33, 40] and list(qs) == [0, 1, 2]
+    assert slots[0] // 16 == tables[0][2] and slots[0] % 16 == 0
+    assert p.seq_share_prefix(2, 0, 3) == pkv.PKV_E_INVALID   # block 2 of seq 0 is not full
