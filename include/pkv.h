@@ -180,6 +180,34 @@ pkv_status pkv_prefill_attn(pkv_pool* pool, int32_t layer, const void* q, const 
                             const int32_t* block_tables, int32_t max_blocks, const int32_t* ctx_lens,
                             int32_t num_seqs, int32_t max_q_len, float scale, void* out, void* stream);
 
+/* Decode attention that allocates nothing. The source pages have no
+ * counterpart; this is a convenience of the library.
+ *
+ * Same inputs, output and results as pkv_decode_attn, but the split-K
+ * scratch is a 16 MiB array built into the library (one per GPU that loads
+ * it, held until the process exits) instead of a caller workspace. It is for
+ * callers that cannot call cudaMalloc on the decode path: a plug-in whose
+ * host process owns all device memory through its own allocator, or a
+ * serving loop that forbids cudaMalloc after start-up because the call can
+ * synchronise the device and stall every stream.
+ *
+ *   - Limit: the scratch pkv_decode_workspace_bytes(pool, num_seqs,
+ *     max_blocks) would report must fit in 16 MiB (with 32 heads and
+ *     512-token partitions: num_seqs x ceil(16 x max_blocks / 512) <= ~1,000,
+ *     e.g. 32 rows with tables up to 992 blocks). Larger requests are refused
+ *     with PKV_E_INVALID and a message, before anything is launched.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture.
+ *   - Every call on a device shares the one array and overwrites it. Calls
+ *     whose kernels overlap on the GPU (other streams, other threads) race
+ *     and give wrong results; serialise them. Nothing in it needs clearing
+ *     between calls. No cudaMalloc, cudaFree or allocating library routine
+ *     is called. */
+pkv_status pkv_decode_attn_noalloc(pkv_pool* pool, int32_t layer, const void* q, const int32_t* block_tables,
+                                   int32_t max_blocks, const int32_t* ctx_lens, int32_t num_seqs, float scale,
+                                   void* out, void* stream);
+
 /* ------------------------------------------------------------------- step */
 
 /* One mixed engine iteration: B decode rows then P prefill rows, as one flat

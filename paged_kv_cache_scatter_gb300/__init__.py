@@ -59,6 +59,7 @@ SIGNATURES = {
     "pkv_decode_workspace_bytes": (_sz, [_P, _i32, _i32]),
     "pkv_decode_attn": (_i32, [_P, _i32, _P, _P, _i32, _P, _i32, _f32, _P, _P, _sz, _P]),
     "pkv_prefill_attn": (_i32, [_P, _i32, _P, _P, _P, _i32, _P, _i32, _i32, _f32, _P, _P]),
+    "pkv_decode_attn_noalloc": (_i32, [_P, _i32, _P, _P, _i32, _P, _i32, _f32, _P, _P]),
     "pkv_step_workspace_bytes": (_sz, [_P, _SD]),
     "pkv_step": (_i32, [_P, _SD, _P, _sz, _P]),
     "pkv_get_status": (_i32, [_P, _P, _c.POINTER(_u32)]),
@@ -208,6 +209,12 @@ class Pool:
         _check(load().pkv_decode_attn(self.handle, layer, _ptr(q), _ptr(block_tables), int(block_tables.shape[1]),
                                       _ptr(ctx_lens), int(ctx_lens.shape[0]), float(scale), _ptr(out),
                                       _ptr(workspace), ws_bytes, _stream(stream)))
+
+    def decode_attn_noalloc(self, layer: int, q, block_tables, ctx_lens, scale: float, out, stream=None) -> None:
+        """pkv_decode_attn without a workspace: the library's built-in 16 MiB scratch is used."""
+        _check(load().pkv_decode_attn_noalloc(self.handle, layer, _ptr(q), _ptr(block_tables),
+                                              int(block_tables.shape[1]), _ptr(ctx_lens), int(ctx_lens.shape[0]),
+                                              float(scale), _ptr(out), _stream(stream)))
 
     def prefill_attn(self, layer: int, q, q_start_loc, block_tables, ctx_lens, max_q_len: int, scale: float, out,
                      stream=None) -> None:
