@@ -61,24 +61,30 @@ def _peaks():
     return 6800.0, 1900.0, "fallback"
 
 
-def _kernel_source_hash():
+KERNEL_SOURCES = {
+    "decode_attn": ["pkv_kernels.cu", "ptx.cuh", "pkv_internal.h"],
+    "prefill_attn": ["pkv_prefill.cu", "ptx.cuh", "pkv_internal.h"],
+}
+
+
+def _kernel_source_hash(kernel: str):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_cache_scatter_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in KERNEL_SOURCES[kernel]:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
 
 
 def _traffic(kernel: str, config: str):
-    """DRAM bytes per launch from a committed ncu summary, if it matches the current kernels."""
+    """DRAM bytes per launch from a committed ncu summary, if the kernel's sources are unchanged since."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         d = json.load(f)
     e = d.get(f"{kernel}/{config}")
-    if not e or e.get("source_hash") != _kernel_source_hash():
+    if not e or e.get("source_hash") != _kernel_source_hash(kernel):
         return None
     return e.get("dram_bytes_per_launch")
 
@@ -168,6 +174,8 @@ def run_ours(args):
     pkv.load()
 
     wl = CONFIGS[args.config]()
+    if args.layers:
+        wl.num_layers = args.layers          # same per-layer work, fewer layers (profiling runs)
     L, H, D = wl.num_layers, wl.num_heads, wl.head_dim
     B, T, S = wl.num_seqs, wl.num_tokens, wl.num_seqs
     dev = torch.device("cuda", local)
@@ -436,6 +444,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--layers", type=int, default=0,
+                    help="run only this many layers (smaller pool; per-layer work unchanged; for profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
