@@ -1,6 +1,31 @@
-// pkv_prefill.cu — chunked causal prefill attention over the paged pool.
+// pkv_prefill.cu — chunked causal prefill attention over the paged pool on
+// the 5th-generation tensor cores (tcgen05, accumulators in TMEM), with K/V
+// tiles gathered from the pool's blocks by TMA.
+//
+// One CTA = (query tile of 128 chunk rows, head, sequence). Query row i of a
+// chunk of q_len tokens sits at position ctx - q_len + i and attends keys
+// 0..that position ("llm-inference-batching" (faangrind), "Prefill and
+// decode share each step": a prompt is prefilled in chunks; "The inference
+// engine" (wpnews), "Prefill and decode ask the accelerator for different
+// work": prefill attention respects the causal mask). The chunk's own K/V
+// are already in the pool (kv_append runs first), so keys come only from
+// the pool, 128 at a time (8 blocks).
+//
+// Warp roles (192 threads):
+//   warp 0      TMA producer: K and V tiles of 8 blocks, two 64-dim halves
+//               each (2 KB boxes), into a 2-stage ring per operand.
+//   warp 1      TMEM owner and MMA issuer (one elected lane):
+//               S = Q K^T into one of two S buffers, O_tile = P V into one of
+//               two O buffers, completion signalled with tcgen05.commit.
+//   warps 2..5  softmax: thread r owns query row r (TMEM lane r). Per tile it
+//               reads S, updates the running max / sum in the log2 domain,
+//               writes P (FP16) to shared memory for the P V product, and
+//               folds the previous tile's O_tile into FP32 registers.
+// Shared-memory operands use the 128-byte swizzle: rows of 128 B (64 halves),
+// two slabs per 128-wide operand, 8-row groups 1,024 B apart.
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <string>
@@ -44,10 +69,384 @@ bool encode_kv_tmap(const PoolGeom& g, TensorMap128* out, std::string* err)
     return true;
 }
 
-cudaError_t launch_prefill(const pkv_pool*, int, const void*, const int32_t*, const int32_t*, int, const int32_t*, int,
-                           int, float, void*, cudaStream_t)
+namespace {
+
+constexpr int kRows = 128;     // query rows per CTA (MMA M)
+constexpr int kKeys = 128;     // keys per tile (8 blocks)
+constexpr int kThreads = 192;
+constexpr int kOperandBytes = kRows * kHeadDim * 2;  // 32 KB: one 128 x 128 FP16 operand
+constexpr int kSlabBytes = kOperandBytes / 2;        // 16 KB: 128 rows x 64 halves
+
+// shared-memory map (offsets from a 1,024-byte aligned base)
+constexpr int kSmQ = 0;
+constexpr int kSmK = kSmQ + kOperandBytes;       // 2 stages
+constexpr int kSmV = kSmK + 2 * kOperandBytes;   // 2 stages
+constexpr int kSmP = kSmV + 2 * kOperandBytes;
+constexpr int kSmBars = kSmP + kOperandBytes;
+enum Bar { K_FULL = 0, V_FULL = 2, K_EMPTY = 4, V_EMPTY = 6, S_FULL = 8, P_FULL = 10, O_FULL = 11, O_FREE = 13,
+           MMA_DONE = 15, NUM_BARS = 16 };
+constexpr int kSmTmemSlot = kSmBars + NUM_BARS * 8;
+constexpr int kSmAbort = kSmTmemSlot + 4;
+constexpr int kSmBytes = kSmAbort + 12;
+constexpr int kSmAlloc = kSmBytes + 1024;        // slack to align the base
+
+// TMEM columns: two S buffers then two O buffers, 128 fp32 columns each.
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS = 0;
+constexpr uint32_t kColO = 256;
+
+// Instruction descriptors, kind::f16: D = F32 (bit 4), A = B = F16,
+// N >> 3 at bit 17, M >> 4 at bit 24; bit 16 makes B MN-major.
+constexpr uint32_t kIdescS = (1u << 4) | ((uint32_t)(kKeys >> 3) << 17) | ((uint32_t)(kRows >> 4) << 24);
+constexpr uint32_t kIdescPV = kIdescS | (1u << 16);
+
+struct PrefillArgs {
+    const __half* q;         // [T][H][128], token index from q_start
+    __half* out;             // [T][H][128]
+    const int32_t* q_start;  // [S + 1]
+    const int32_t* tables;   // [S][max_blocks]
+    const int32_t* ctx_lens; // [S]
+    int max_blocks;
+    int num_heads;
+    int layer;
+    int max_q_len;
+    int64_t num_blocks;
+    float scale_log2;
+    unsigned int* status;
+};
+
+// Warp-uniform bounded wait: every lane waits, the warp agrees on the
+// outcome, and a timeout (or an earlier abort by any warp) stops the warp's
+// role loop so that no lane reaches a .sync.aligned instruction alone.
+__device__ __forceinline__ bool flag_wait(uint32_t bar, uint32_t parity, volatile int* abort, unsigned int* status)
 {
-    return cudaErrorNotSupported;
+    const int lane = threadIdx.x & 31;
+    int stop = lane == 0 ? *abort : 0;
+    if (__shfl_sync(0xffffffffu, stop, 0)) return false;
+    const bool ok = __all_sync(0xffffffffu, mbar_wait(bar, parity));
+    if (!ok && lane == 0) {
+        atomicOr(status, PKV_DEV_TIMEOUT);
+        *abort = 1;
+    }
+    return ok;
+}
+
+__global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ CUtensorMap tmap,
+                                                               const PrefillArgs a)
+{
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+    const uint32_t sb = smem_u32(smem);
+    const int qt = blockIdx.x, h = blockIdx.y, s = blockIdx.z;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // ---- validate this sequence's metadata (all threads agree)
+    const int q0 = __ldg(a.q_start + s);
+    const int qlen = __ldg(a.q_start + s + 1) - q0;
+    const int ctx = __ldg(a.ctx_lens + s);
+    if (q0 < 0 || qlen < 1 || qlen > ctx || qlen > a.max_q_len || ctx > a.max_blocks * kBlockSize) {
+        if (qt == 0 && h == 0 && threadIdx.x == 0)
+            atomicOr(a.status, ctx > a.max_blocks * kBlockSize ? PKV_DEV_BAD_CTX : PKV_DEV_BAD_QLEN);
+        return;
+    }
+    if (qt * kRows >= qlen) return;
+    const int rows = min(kRows, qlen - qt * kRows);
+    const int p0 = ctx - qlen + qt * kRows;  // position of row 0
+    const int pos_max = p0 + rows - 1;
+    const int nkt = pos_max / kKeys + 1;
+    const int nblk = pos_max / kBlockSize + 1;
+    const int32_t* trow = a.tables + (int64_t)s * a.max_blocks;
+    bool bad = false;
+    for (int b = threadIdx.x; b < nblk; b += kThreads) {
+        const int id = __ldg(trow + b);
+        bad |= id < 0 || (int64_t)id >= a.num_blocks;
+    }
+    if (__syncthreads_or(bad)) {
+        if (threadIdx.x == 0) atomicOr(a.status, PKV_DEV_BAD_BLOCK);
+        return;
+    }
+
+    // ---- Q tile -> shared memory (swizzled, K-major); rows past the chunk are zero
+    for (int c = threadIdx.x; c < kRows * 16; c += kThreads) {
+        const int r = c >> 4, ch = c & 15;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (r < rows)
+            v = __ldg(reinterpret_cast<const uint4*>(a.q + ((int64_t)(q0 + qt * kRows + r) * a.num_heads + h) * kHeadDim) +
+                      ch);
+        st_shared_v4(sb + kSmQ + (ch >> 3) * kSlabBytes + r * 128 + (((ch & 7) ^ (r & 7)) << 4), v);
+    }
+    fence_proxy_async_smem();
+
+    const uint32_t bars = sb + kSmBars;
+    volatile int* abort = reinterpret_cast<volatile int*>(smem + kSmAbort);
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bars + 8 * (K_FULL + i), 1);
+            mbar_init(bars + 8 * (V_FULL + i), 1);
+            mbar_init(bars + 8 * (K_EMPTY + i), 1);
+            mbar_init(bars + 8 * (V_EMPTY + i), 1);
+            mbar_init(bars + 8 * (S_FULL + i), 1);
+            mbar_init(bars + 8 * (O_FULL + i), 1);
+            mbar_init(bars + 8 * (O_FREE + i), 128);
+        }
+        mbar_init(bars + 8 * P_FULL, 128);
+        mbar_init(bars + 8 * MMA_DONE, 1);
+        *abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(sb + kSmTmemSlot, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kSmTmemSlot);
+
+    if (warp == 0) {
+        // ================================================= TMA producer
+        if (lane == 0) prefetch_tmap(&tmap);
+        int issued = 0;
+        for (int j = 0; j < nkt; ++j) {
+            const int st = j & 1;
+            const uint32_t ph = (uint32_t)(j >> 1) & 1u;
+            const int nb = min(8, nblk - 8 * j);
+            const int id = lane < nb ? __ldg(trow + 8 * j + lane) : 0;
+            if (j >= 2 && !flag_wait(bars + 8 * (K_EMPTY + st), ph ^ 1u, abort, a.status)) break;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(bars + 8 * (K_FULL + st), nb * kTileBytes);
+            }
+            for (int b = 0; b < nb; ++b) {
+                const int idb = __shfl_sync(0xffffffffu, id, b);
+                if (lane == 0)
+                    for (int half = 0; half < 2; ++half)
+                        tma_load_5d(sb + kSmK + st * kOperandBytes + half * kSlabBytes + b * 2048, &tmap, half * 64, 0,
+                                    h, a.layer, idb, bars + 8 * (K_FULL + st));
+            }
+            if (j >= 2 && !flag_wait(bars + 8 * (V_EMPTY + st), ph ^ 1u, abort, a.status)) break;
+            if (lane == 0) mbar_arrive_expect_tx(bars + 8 * (V_FULL + st), nb * kTileBytes);
+            for (int b = 0; b < nb; ++b) {
+                const int idb = __shfl_sync(0xffffffffu, id, b);
+                if (lane == 0)
+                    for (int half = 0; half < 2; ++half)
+                        tma_load_5d(sb + kSmV + st * kOperandBytes + half * kSlabBytes + b * 2048, &tmap, half * 64, 0,
+                                    a.num_heads + h, a.layer, idb, bars + 8 * (V_FULL + st));
+            }
+            issued = j + 1;
+        }
+        __syncwarp();
+        if (*abort && lane == 0) {
+            // let this warp's loads that nobody consumed land before the CTA exits
+            for (int j = (issued > 2 ? issued - 2 : 0); j < issued; ++j) {
+                mbar_wait(bars + 8 * (K_FULL + (j & 1)), (uint32_t)(j >> 1) & 1u);
+                mbar_wait(bars + 8 * (V_FULL + (j & 1)), (uint32_t)(j >> 1) & 1u);
+            }
+        }
+    } else if (warp == 1) {
+        // ================================================= MMA issuer
+        for (int j = 0; j <= nkt; ++j) {
+            if (j < nkt) {
+                const int st = j & 1;
+                const uint32_t ph = (uint32_t)(j >> 1) & 1u;
+                if (!flag_wait(bars + 8 * (K_FULL + st), ph, abort, a.status)) break;
+                tc_fence_after();
+                if (lane == 0) {
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t off = (kk >> 2) * kSlabBytes + (kk & 3) * 32;
+                        tc_mma_f16(tmem + kColS + st * 128, sw128_desc(sb + kSmQ + off, 16, 1024),
+                                   sw128_desc(sb + kSmK + st * kOperandBytes + off, 16, 1024), kIdescS, kk > 0);
+                    }
+                    tc_commit(bars + 8 * (S_FULL + st));
+                    tc_commit(bars + 8 * (K_EMPTY + st));
+                }
+                __syncwarp();
+            }
+            if (j >= 1) {
+                const int i = j - 1, st = i & 1;
+                const uint32_t ph = (uint32_t)(i >> 1) & 1u;
+                if (!flag_wait(bars + 8 * P_FULL, (uint32_t)i & 1u, abort, a.status)) break;
+                if (!flag_wait(bars + 8 * (V_FULL + st), ph, abort, a.status)) break;
+                if (i >= 2 && !flag_wait(bars + 8 * (O_FREE + st), ph ^ 1u, abort, a.status)) break;
+                if (i == nkt - 1) {
+                    // keys past the last row's position may hold anything (even NaN); zero their V rows so
+                    // that P = 0 times V stays 0 in the tensor core
+                    const int first = pos_max + 1 - i * kKeys;
+                    for (int c = first * 8 + lane; c < kKeys * 8; c += 32) {
+                        const int r = c >> 3, ch = c & 7;
+                        const uint32_t base = sb + kSmV + st * kOperandBytes + r * 128 + ch * 16;
+                        st_shared_v4(base, make_uint4(0, 0, 0, 0));
+                        st_shared_v4(base + kSlabBytes, make_uint4(0, 0, 0, 0));
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                }
+                tc_fence_after();
+                if (lane == 0) {
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t aoff = (kk >> 2) * kSlabBytes + (kk & 3) * 32;
+                        tc_mma_f16(tmem + kColO + st * 128, sw128_desc(sb + kSmP + aoff, 16, 1024),
+                                   sw128_desc(sb + kSmV + st * kOperandBytes + kk * 2048, kSlabBytes, 1024), kIdescPV,
+                                   kk > 0);
+                    }
+                    tc_commit(bars + 8 * (O_FULL + st));
+                    tc_commit(bars + 8 * (V_EMPTY + st));
+                }
+                __syncwarp();
+            }
+        }
+        if (lane == 0) {
+            tc_commit(bars + 8 * MMA_DONE);
+            mbar_wait(bars + 8 * MMA_DONE, 0);
+        }
+        __syncwarp();
+    } else {
+        // ================================================= softmax
+        const int qtr = warp & 3;
+        const int row = qtr * 32 + lane;
+        const bool valid = row < rows;
+        const int pos = p0 + row;
+        const uint32_t tl = tmem + ((uint32_t)(qtr * 32) << 16);
+        float o[kHeadDim];
+#pragma unroll
+        for (int d = 0; d < kHeadDim; ++d) o[d] = 0.f;
+        float m_old = -INFINITY, l = 0.f, alpha_prev = 1.f;
+        bool ok = true;
+        for (int j = 0; j < nkt && ok; ++j) {
+            const int st = j & 1;
+            if (!flag_wait(bars + 8 * (S_FULL + st), (uint32_t)(j >> 1) & 1u, abort, a.status)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t sa = tl + kColS + st * 128;
+            const int key0 = j * kKeys;
+            float mx = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                float v[32];
+                tc_ld32(sa + c * 32, v);
+#pragma unroll
+                for (int e = 0; e < 32; ++e)
+                    if (key0 + c * 32 + e <= pos) mx = fmaxf(mx, v[e]);
+            }
+            const float m_new = valid ? fmaxf(m_old, mx * a.scale_log2) : 0.f;
+            const float alpha = ex2(m_old - m_new);
+            if (j >= 1) {
+                const int i = j - 1;
+                if (!flag_wait(bars + 8 * (O_FULL + (i & 1)), (uint32_t)(i >> 1) & 1u, abort, a.status)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    float v[32];
+                    tc_ld32(tl + kColO + (i & 1) * 128 + c * 32, v);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) o[c * 32 + e] = fmaf(o[c * 32 + e], alpha_prev, v[e]);
+                }
+                tc_fence_before();
+                mbar_arrive(bars + 8 * (O_FREE + (i & 1)));
+            }
+            float lsum = 0.f;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                float v[32];
+                tc_ld32(sa + c * 32, v);
+                uint32_t packed[16];
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) {
+                    const bool k0 = valid && key0 + c * 32 + e <= pos;
+                    const bool k1 = valid && key0 + c * 32 + e + 1 <= pos;
+                    const float pa = k0 ? ex2(fmaf(v[e], a.scale_log2, -m_new)) : 0.f;
+                    const float pb = k1 ? ex2(fmaf(v[e + 1], a.scale_log2, -m_new)) : 0.f;
+                    const __half2 hp = __floats2half2_rn(pa, pb);
+                    const float2 back = __half22float2(hp);  // the sum uses the weights the MMA will use
+                    lsum += back.x + back.y;
+                    packed[e >> 1] = *reinterpret_cast<const uint32_t*>(&hp);
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int ch = (c & 1) * 4 + u;  // 16-byte chunk within the 128-byte row
+                    st_shared_v4(sb + kSmP + (c >> 1) * kSlabBytes + row * 128 + ((ch ^ (row & 7)) << 4),
+                                 make_uint4(packed[4 * u], packed[4 * u + 1], packed[4 * u + 2], packed[4 * u + 3]));
+                }
+            }
+            l = fmaf(l, alpha, lsum);
+            m_old = m_new;
+            alpha_prev = alpha;
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(bars + 8 * P_FULL);
+        }
+        if (ok) {
+            const int i = nkt - 1;
+            if (flag_wait(bars + 8 * (O_FULL + (i & 1)), (uint32_t)(i >> 1) & 1u, abort, a.status)) {
+                tc_fence_after();
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    float v[32];
+                    tc_ld32(tl + kColO + (i & 1) * 128 + c * 32, v);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) o[c * 32 + e] = fmaf(o[c * 32 + e], alpha_prev, v[e]);
+                }
+                if (valid) {
+                    const float inv = 1.f / l;
+                    uint4* dst = reinterpret_cast<uint4*>(a.out + ((int64_t)(q0 + qt * kRows + row) * a.num_heads + h) *
+                                                                      kHeadDim);
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) {
+                        uint32_t w[4];
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const __half2 hv = __floats2half2_rn(o[c * 8 + 2 * u] * inv, o[c * 8 + 2 * u + 1] * inv);
+                            w[u] = *reinterpret_cast<const uint32_t*>(&hv);
+                        }
+                        dst[c] = make_uint4(w[0], w[1], w[2], w[3]);
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
+}  // namespace
+
+cudaError_t launch_prefill(const pkv_pool* pool, int layer, const void* q, const int32_t* q_start,
+                           const int32_t* tables, int max_blocks, const int32_t* ctx_lens, int num_seqs, int max_q_len,
+                           float scale, void* out, cudaStream_t stream)
+{
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 64 && !attr_set[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmAlloc);
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = true;
+    }
+    PrefillArgs a;
+    a.q = static_cast<const __half*>(q);
+    a.out = static_cast<__half*>(out);
+    a.q_start = q_start;
+    a.tables = tables;
+    a.ctx_lens = ctx_lens;
+    a.max_blocks = max_blocks;
+    a.num_heads = pool->geom.num_heads;
+    a.layer = layer;
+    a.max_q_len = max_q_len;
+    a.num_blocks = pool->geom.num_blocks;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    a.status = pool->status_dev;
+    CUtensorMap tmap;
+    static_assert(sizeof(tmap) == sizeof(pool->kv_tmap.bytes), "tensor map size");
+    memcpy(&tmap, pool->kv_tmap.bytes, sizeof(tmap));
+    dim3 grid((max_q_len + kRows - 1) / kRows, pool->geom.num_heads, num_seqs);
+    prefill_kernel<<<grid, kThreads, kSmAlloc, stream>>>(tmap, a);
+    return cudaGetLastError();
 }
 
 }  // namespace pkv
