@@ -1,17 +1,23 @@
-"""Benchmark: one engine iteration (32 layers) of paged decode attention on GB300.
+"""Benchmark: one engine iteration (32 layers) of the paged KV cache path on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
 
-A step is one pass of the whole hot path over one batch: for every one of the
-32 layers, kv_append of each row's new token and decode attention of every
-row over its paged context, through libpkv's C ABI (pkv_step). Default
-workload: batch-32 decode with prompt lengths from a clipped lognormal (mean
-1,250, 50..8,000) plus U{0..299} generated tokens, over a 7,152-block (60 GB)
-pool with shuffled block ids, N(0,1) FP16 values (synthetic; no dataset).
+A step is one pass of the whole hot path over one batch, through libpkv's C
+ABI (pkv_step): for each of the 32 layers, kv_append of every new token,
+decode attention of every decode row over its paged context, and causal
+prefill attention of every prompt chunk. Default workload (the headline):
+batch-32 decode with prompt lengths from a clipped lognormal (mean 1,250,
+50..8,000) plus U{0..299} generated tokens, over a 7,152-block (60 GB) pool
+with shuffled block ids, N(0,1) FP16 values (synthetic; no dataset).
 
-One JSON line is printed by rank 0. Under torchrun (N > 1) every rank runs
-its own replica of the workload (weak scaling, no collective on the data
-path); `value` adds the KV bytes of all ranks over the slowest rank's time.
+Other workloads (--config): long_decode (13 x 8,192), shared_prefix_decode
+(64 rows over 125 shared blocks), mixed_prefill (a 4,000-token prompt in
+512-token chunks next to 31 decode rows; one step = the whole 8-chunk
+schedule, i.e. 8 iterations).
+
+Rank 0 prints one JSON line. Under torchrun (N > 1) every rank runs its own
+replica (weak scaling, no collective on the data path); `value` adds all
+ranks' work over the slowest rank's time.
 
 `--impl reference` times the oracle (plain CPU code, oracle/) on the host
 cores on a bounded sample of the same workload: one layer per step.
@@ -35,20 +41,37 @@ sys.path.insert(0, ROOT)
 
 import workloads  # noqa: E402
 
-KV_BYTES_PER_TOKEN_LAYER = 2 * 32 * 128 * 2          # K and V of 32 heads x 128 dims, FP16: 16,384 B
+HEAD_DIM = 128
 SCALE = float(np.float32(1.0 / np.sqrt(np.float32(128.0))))
 
-CONFIGS = {
-    "average_decode": lambda: workloads.average_decode(0),
-    "long_decode": lambda: workloads.long_decode(0),
-    "shared_prefix_decode": lambda: workloads.shared_prefix_decode(0),
-}
+
+def _iterations(config: str):
+    """The workload's engine iterations (one for decode configs, 8 for the chunk schedule)."""
+    if config == "average_decode":
+        return [workloads.average_decode(0)]
+    if config == "long_decode":
+        return [workloads.long_decode(0)]
+    if config == "shared_prefix_decode":
+        return [workloads.shared_prefix_decode(0)]
+    if config == "mixed_prefill":
+        first = workloads.mixed_prefill(0)
+        return [workloads.mixed_prefill(c) for c in range(first.meta["num_chunks"])]
+    raise KeyError(config)
+
+
 CONFIG_TEXT = {
     "average_decode": "batch-32 decode, 32 layers x 32 heads x 128 fp16, context = clipped lognormal prompt "
                       "(mean 1,250) + U{0..299} generated + 1, 7,152-block (60 GB) shuffled pool, kv_append of 1 "
                       "token per row",
     "long_decode": "13 rows x 8,192 context tokens, 32 layers, 7,152-block pool, split-K partitions",
     "shared_prefix_decode": "64 rows sharing 125 ref-counted prefix blocks + 1..300 private tokens, 32 layers",
+    "mixed_prefill": "one 4,000-token prompt prefilled in 512-token chunks (8 iterations) next to 31 decode rows "
+                     "of context U{100..2000} advancing one token per iteration, 32 layers",
+}
+
+KERNEL_SOURCES = {
+    "decode_attn": ["pkv_kernels.cu", "ptx.cuh", "pkv_internal.h"],
+    "prefill_attn": ["pkv_prefill.cu", "ptx.cuh", "pkv_internal.h"],
 }
 
 
@@ -59,12 +82,6 @@ def _peaks():
             d = json.load(f)
         return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
     return 6800.0, 1900.0, "fallback"
-
-
-KERNEL_SOURCES = {
-    "decode_attn": ["pkv_kernels.cu", "ptx.cuh", "pkv_internal.h"],
-    "prefill_attn": ["pkv_prefill.cu", "ptx.cuh", "pkv_internal.h"],
-}
 
 
 def _kernel_source_hash(kernel: str):
@@ -104,7 +121,7 @@ class ClockSampler:
     def start(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -125,22 +142,30 @@ class ClockSampler:
             self.proc.kill()
         if self.thread:
             self.thread.join(timeout=2)
-        sm, smax, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
-            parts = [x.strip() for x in ln.split(",")]
-            if len(parts) < 8:
-                continue
-            try:
-                sm.append(float(parts[0]))
-                smax.append(float(parts[1]))
-            except ValueError:
-                continue
-            for name, val in zip(names, parts[4:8]):
-                if val.lower().startswith("active"):
-                    reasons.add(name)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        return parse_clock_lines(self.lines)
+
+
+def parse_clock_lines(lines):
+    sm, smax, power, reasons = [], [], [], set()
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    for ln in lines:
+        parts = [x.strip() for x in ln.split(",")]
+        if len(parts) < 8:
+            continue
+        try:
+            sm.append(float(parts[0]))
+            smax.append(float(parts[1]))
+        except ValueError:
+            continue
+        try:
+            power.append(float(parts[2]))
+        except ValueError:
+            pass
+        for name, val in zip(names, parts[4:8]):
+            if val.lower().startswith("active"):
+                reasons.add(name)
+    return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+            "reasons": sorted(reasons), "samples": len(sm), "power_w_max": max(power) if power else None}
 
 
 def _gpu_id(torch, dev):
@@ -158,7 +183,85 @@ def _dist():
     return ws, rank, local
 
 
+def aggregate(per_rank_ms, per_rank_units):
+    """Whole-job throughput: all ranks' units over the slowest rank's time (seconds)."""
+    t = max(per_rank_ms) * 1e-3
+    return sum(per_rank_units) / t
+
+
+def prefill_pairs(wl) -> int:
+    """Unmasked (query, key) pairs of the prefill rows: query at position p sees p + 1 keys."""
+    n = 0
+    for c, q in zip(wl.ctx_lens[wl.num_decode:], wl.q_lens[wl.num_decode:]):
+        lo, hi = int(c) - int(q), int(c)
+        n += (lo + 1 + hi) * (hi - lo) // 2
+    return n
+
+
+def kv_bytes(wl, layers) -> int:
+    """K and V bytes the decode rows read: 2 x heads x 128 x 2 bytes per context token per layer."""
+    dec = wl.ctx_lens[:wl.num_decode].astype(np.int64).sum()
+    return int(dec) * 2 * wl.num_heads * HEAD_DIM * 2 * layers
+
+
 # ------------------------------------------------------------------ ours
+
+class StepData:
+    """Device metadata and per-layer tensors of one engine iteration."""
+
+    def __init__(self, torch, pkv, pool, wl, meta, layers, dev, gen):
+        tables, ctx, slots, qs = meta
+        self.wl = wl
+        self.host = [torch.from_numpy(np.ascontiguousarray(x)).pin_memory() for x in (tables, ctx, qs, slots)]
+        self.dev = [x.to(dev) for x in self.host]
+        T, H = wl.num_tokens, wl.num_heads
+        self.q = torch.randn((layers, T, H, HEAD_DIM), generator=gen, device=dev).half()
+        self.k = torch.randn((layers, T, H, HEAD_DIM), generator=gen, device=dev).half()
+        self.v = torch.randn((layers, T, H, HEAD_DIM), generator=gen, device=dev).half()
+        self.out = torch.empty_like(self.q)
+        B = wl.num_decode
+        self.B = B
+        self.max_q = int(wl.q_lens[B:].max()) if wl.num_seqs > B else 0
+        stride = T * H * HEAD_DIM
+        tables_d, ctx_d, qs_d, slots_d = self.dev
+        self.desc = pkv.make_step_desc(num_decode=B, num_prefill=wl.num_seqs - B, num_tokens=T, max_q_len=self.max_q,
+                                       max_blocks=tables.shape[1], first_layer=0, num_layers=layers, scale=SCALE,
+                                       block_tables=tables_d, ctx_lens=ctx_d, q_start_loc=qs_d, slot_mapping=slots_d,
+                                       q=self.q, k=self.k, v=self.v, out=self.out, q_layer_stride=stride,
+                                       k_layer_stride=stride, v_layer_stride=stride, out_layer_stride=stride)
+        self.ws_bytes = pool.step_workspace_bytes(self.desc)
+
+
+def _metadata(pkv, iterations):
+    """Step metadata from libpkv's block manager, iteration after iteration, as a serving loop gets it.
+
+    Blocks are handed out in the order of the first iteration's tables (a
+    random permutation of the pool), so for a single decode iteration the
+    tables equal the workload's own."""
+    wl0 = iterations[0]
+    seen = []
+    for r in range(wl0.num_seqs):
+        seen.extend(int(b) for b in wl0.block_tables[r] if b >= 0)
+    order = list(dict.fromkeys(seen))
+    rest = np.setdiff1d(np.arange(wl0.num_blocks), np.array(order, np.int64))
+    mgr = pkv.Pool(None, wl0.num_blocks, num_layers=wl0.num_layers, num_heads=wl0.num_heads,
+                   free_order=np.concatenate([np.array(order, np.int64), rest]))
+    prefix = int(wl0.meta.get("prefix_blocks", 0))
+    if prefix:
+        assert mgr.seq_grow(-1, prefix * 16) == pkv.PKV_OK
+        for r in range(wl0.num_seqs):
+            assert mgr.seq_share_prefix(r, -1, prefix) == pkv.PKV_OK
+    out = []
+    for wl in iterations:
+        for r in range(wl.num_seqs):
+            assert mgr.seq_grow(r, int(wl.ctx_lens[r])) == pkv.PKV_OK
+        st, tables, ctx, slots, qs = mgr.build_step(np.arange(wl.num_seqs), wl.q_lens, wl0.max_blocks)
+        assert st == pkv.PKV_OK and np.array_equal(ctx, wl.ctx_lens)
+        out.append((tables, ctx, slots, qs))
+    if len(iterations) == 1 and not prefix:
+        assert np.array_equal(out[0][0], wl0.block_tables)
+    return out
+
 
 def run_ours(args):
     import torch
@@ -173,63 +276,56 @@ def run_ours(args):
     pkv_build.build()
     pkv.load()
 
-    wl = CONFIGS[args.config]()
-    if args.layers:
-        wl.num_layers = args.layers          # same per-layer work, fewer layers (profiling runs)
-    L, H, D = wl.num_layers, wl.num_heads, wl.head_dim
-    B, T, S = wl.num_seqs, wl.num_tokens, wl.num_seqs
+    iters = _iterations(args.config)
+    wl0 = iters[0]
+    L = args.layers or wl0.num_layers
+    H = wl0.num_heads
     dev = torch.device("cuda", local)
 
-    pool_t = torch.empty(workloads.pool_shape(wl.num_blocks, L, H), dtype=torch.float16, device=dev)
-    workloads.fill_normal_fp16_(pool_t, workloads.value_seed(wl.seed, "pool"))
-    pool = pkv.Pool(pool_t, wl.num_blocks, num_layers=L, num_heads=H)
-
-    tables, ctx, slots, qs = _metadata_via_block_manager(pkv, pool, wl)
-    tables_h = torch.from_numpy(tables).pin_memory()
-    ctx_h = torch.from_numpy(ctx).pin_memory()
-    qs_h = torch.from_numpy(qs).pin_memory()
-    slots_h = torch.from_numpy(slots).pin_memory()
-    tables_d, ctx_d, qs_d, slots_d = (x.to(dev) for x in (tables_h, ctx_h, qs_h, slots_h))
-
+    pool_t = torch.empty(workloads.pool_shape(wl0.num_blocks, L, H), dtype=torch.float16, device=dev)
+    workloads.fill_normal_fp16_(pool_t, workloads.value_seed(wl0.seed, "pool"))
+    pool = pkv.Pool(pool_t, wl0.num_blocks, num_layers=L, num_heads=H)
     gen = torch.Generator(device=dev)
-    gen.manual_seed(workloads.value_seed(wl.seed, "q"))
-    q = torch.randn((L, T, H, D), generator=gen, device=dev).half()
-    k = torch.randn((L, T, H, D), generator=gen, device=dev).half()
-    v = torch.randn((L, T, H, D), generator=gen, device=dev).half()
-    out = torch.empty_like(q)
-    stride = T * H * D
-    desc = pkv.make_step_desc(num_decode=B, num_prefill=0, num_tokens=T, max_q_len=0, max_blocks=wl.max_blocks,
-                              first_layer=0, num_layers=L, scale=SCALE, block_tables=tables_d, ctx_lens=ctx_d,
-                              q_start_loc=qs_d, slot_mapping=slots_d, q=q, k=k, v=v, out=out,
-                              q_layer_stride=stride, k_layer_stride=stride, v_layer_stride=stride,
-                              out_layer_stride=stride)
-    wsb = pool.step_workspace_bytes(desc)
-    wspace = torch.empty(max(wsb, 256), dtype=torch.uint8, device=dev)
+    gen.manual_seed(workloads.value_seed(wl0.seed, "q"))
+    steps = [StepData(torch, pkv, pool, wl, m, L, dev, gen) for wl, m in zip(iters, _metadata(pkv, iters))]
+    wspace = torch.empty(max(max(s.ws_bytes for s in steps), 256), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
     def step():
-        pool.step(desc, wspace, stream)
+        for s in steps:
+            pool.step(s.desc, wspace, stream)
+
+    def check_status():
+        st, flags = pool.get_status(stream)
+        if st != pkv.PKV_OK:
+            raise RuntimeError(f"device status {st} flags {flags:#x}")
 
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)
-    st, flags = pool.get_status(stream)
-    if st != pkv.PKV_OK:
-        raise RuntimeError(f"device status {st} flags {flags:#x}")
+    check_status()
 
-    kv_bytes_step = int(wl.ctx_lens.astype(np.int64).sum()) * KV_BYTES_PER_TOKEN_LAYER * L
-    att_tokens_step = int(wl.ctx_lens.astype(np.int64).sum())
-    max_parts = -(-wl.max_blocks * 16 // 512)
-    launches_per_layer = 2 + (1 if max_parts > 1 else 0)
+    has_prefill = any(s.max_q for s in steps)
+    has_decode = any(s.B for s in steps)
+    kv_step = sum(kv_bytes(s.wl, L) for s in steps)
+    pairs_step = sum(prefill_pairs(s.wl) for s in steps) * L
+    flops_step = 4 * HEAD_DIM * H * pairs_step
+    tokens_step = sum(int(s.wl.ctx_lens[:s.B].astype(np.int64).sum()) for s in steps) * L
+    launches_step = 0
+    for s in steps:
+        parts = -(-s.desc.max_blocks * 16 // 512)
+        per_layer = 1 + (1 + (parts > 1) if s.B else 0) + (1 if s.max_q else 0)
+        launches_step += per_layer * L
 
     sampler = ClockSampler(_gpu_id(torch, local))
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
     # ---- timed region 1: the whole step through pkv_step
     if ws > 1:
         dist.barrier()
     torch.cuda.synchronize(dev)
     sampler.start()
     time.sleep(0.3)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0, e1 = ev(), ev()
     e0.record(stream)
     for _ in range(args.steps):
         step()
@@ -239,123 +335,135 @@ def run_ours(args):
         dist.barrier()
     t_ms = e0.elapsed_time(e1)
 
-    # ---- timed region 2: same work layer by layer, events around every decode call
-    dec_ev = []
-    e2, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # ---- timed region 2: the same work call by call, events around every attention call
+    dec_ev, pre_ev = [], []
     torch.cuda.synchronize(dev)
-    e2.record(stream)
     for _ in range(args.steps):
-        for l in range(L):
-            pool.kv_append(l, k[l], v[l], slots_d, stream)
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            pool.decode_attn(l, q[l], tables_d, ctx_d, SCALE, out[l], wspace, stream)
-            b.record(stream)
-            dec_ev.append((a, b))
-    e3.record(stream)
+        for s in steps:
+            tables_d, ctx_d, qs_d, slots_d = s.dev
+            for l in range(L):
+                pool.kv_append(l, s.k[l], s.v[l], slots_d, stream)
+                if s.B:
+                    a, b = ev(), ev()
+                    a.record(stream)
+                    pool.decode_attn(l, s.q[l, :s.B], tables_d[:s.B], ctx_d[:s.B], SCALE, s.out[l, :s.B], wspace,
+                                     stream)
+                    b.record(stream)
+                    dec_ev.append((a, b, s))
+                if s.max_q:
+                    a, b = ev(), ev()
+                    a.record(stream)
+                    pool.prefill_attn(l, s.q[l], qs_d[s.B:], tables_d[s.B:], ctx_d[s.B:], s.max_q, SCALE, s.out[l],
+                                      stream)
+                    b.record(stream)
+                    pre_ev.append((a, b, s))
     torch.cuda.synchronize(dev)
     clocks = sampler.stop()
-    t2_ms = e2.elapsed_time(e3)
-    dec_ms = [a.elapsed_time(b) for a, b in dec_ev]
-    dec_avg_ms = sum(dec_ms) / len(dec_ms)
+    check_status()
+    dec_ms = sum(a.elapsed_time(b) for a, b, _ in dec_ev)
+    pre_ms = sum(a.elapsed_time(b) for a, b, _ in pre_ev)
 
     # ---- end to end: host buffers in, host result out, every step
-    q_h, k_h, v_h = (x.cpu().pin_memory() for x in (q, k, v))
-    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    e4, e5 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    host_io = []
+    for s in steps:
+        host_io.append([(x.cpu().pin_memory(), x) for x in (s.q, s.k, s.v)] + list(zip(s.host, s.dev)))
+    outs_h = [torch.empty(s.out.shape, dtype=s.out.dtype).pin_memory() for s in steps]
+    e4, e5 = ev(), ev()
     torch.cuda.synchronize(dev)
     e4.record(stream)
     for _ in range(args.steps):
-        for src, dst in ((q_h, q), (k_h, k), (v_h, v), (tables_h, tables_d), (ctx_h, ctx_d), (qs_h, qs_d),
-                         (slots_h, slots_d)):
-            dst.copy_(src, non_blocking=True)
-        step()
-        out_h.copy_(out, non_blocking=True)
+        for s, io, oh in zip(steps, host_io, outs_h):
+            for src, dst in io:
+                dst.copy_(src, non_blocking=True)
+            pool.step(s.desc, wspace, stream)
+            oh.copy_(s.out, non_blocking=True)
     e5.record(stream)
     torch.cuda.synchronize(dev)
+    check_status()
     e2e_ms = e4.elapsed_time(e5)
-    h2d = sum(x.numel() * x.element_size() for x in (q_h, k_h, v_h, tables_h, ctx_h, qs_h, slots_h))
-    d2h = out_h.numel() * out_h.element_size()
-    st, flags = pool.get_status(stream)
-    if st != pkv.PKV_OK:
-        raise RuntimeError(f"device status {st} flags {flags:#x}")
+    h2d = sum(src.numel() * src.element_size() for io in host_io for src, _ in io)
+    d2h = sum(o.numel() * o.element_size() for o in outs_h)
 
-    # max over ranks
-    times = torch.tensor([t_ms, e2e_ms, dec_avg_ms], dtype=torch.float64, device=dev)
+    times = torch.tensor([t_ms, e2e_ms], dtype=torch.float64, device=dev)
     if ws > 1:
         dist.all_reduce(times, op=dist.ReduceOp.MAX)
-    t_ms, e2e_ms, dec_avg_ms = (float(x) for x in times.tolist())
+    t_ms, e2e_ms = (float(x) for x in times.tolist())
 
     hbm_peak, tf_peak, peak_kind = _peaks()
-    total_kv = kv_bytes_step * args.steps * ws
-    value = total_kv / (t_ms * 1e-3) / 1e9
-    dec_bytes = int(wl.ctx_lens.astype(np.int64).sum()) * KV_BYTES_PER_TOKEN_LAYER + 2 * B * H * D * 2
-    achieved = dec_bytes / (dec_avg_ms * 1e-3) / 1e9
-    traffic = _traffic("decode_attn", args.config)
+    K = args.steps
+    if has_decode:
+        metric = "decode KV GB/s (KV bytes read per 32-layer iteration / iteration time) at batch 32"
+        value = kv_step * K * ws / (t_ms * 1e-3) / 1e9
+        unit = "GB/s"
+        e2e_value = kv_step * K * ws / (e2e_ms * 1e-3) / 1e9
+    else:
+        metric = "prefill attention TFLOP/s"
+        value = flops_step * K * ws / (t_ms * 1e-3) / 1e12
+        unit = "TFLOP/s"
+        e2e_value = flops_step * K * ws / (e2e_ms * 1e-3) / 1e12
+    n_dec = len(dec_ev)
+    dec_bytes_launch = (kv_step / L / len(steps)) + sum(2 * s.B * H * HEAD_DIM * 2 for s in steps) / len(steps)
+    rooflines = {}
+    if n_dec:
+        ach = dec_bytes_launch / (dec_ms / n_dec * 1e-3) / 1e9
+        rooflines["decode"] = {"bound": "hbm", "kernel": "decode_attn (decode_kernel + reduce_kernel)",
+                               "achieved": round(ach, 1), "peak": hbm_peak, "peak_kind": peak_kind, "unit": "GB/s",
+                               "frac": round(ach / hbm_peak, 4),
+                               "traffic": _traffic("decode_attn", args.config),
+                               "algorithmic_bytes_per_launch": int(dec_bytes_launch),
+                               "avg_launch_us": round(dec_ms / n_dec * 1e3, 2)}
+    if pre_ev:
+        fl = 4 * HEAD_DIM * H * sum(prefill_pairs(s.wl) for _, _, s in pre_ev)
+        ach = fl / (pre_ms * 1e-3) / 1e12
+        rooflines["prefill"] = {"bound": "tensor", "kernel": "prefill_kernel (tcgen05)", "achieved": round(ach, 1),
+                                "peak": tf_peak, "peak_kind": peak_kind + " bf16 dense (fp16 runs at the same rate)",
+                                "unit": "TFLOP/s", "frac": round(ach / tf_peak, 4),
+                                "traffic": _traffic("prefill_attn", args.config),
+                                "algorithmic_flops_per_launch": int(fl / len(pre_ev)),
+                                "avg_launch_us": round(pre_ms / len(pre_ev) * 1e3, 2),
+                                "per_chunk_us": [round(sum(a.elapsed_time(b) for a, b, s2 in pre_ev if s2 is s)
+                                                       / max(1, sum(1 for *_, s2 in pre_ev if s2 is s)) * 1e3, 2)
+                                                 for s in steps if s.max_q]}
+    dominant = "decode" if (dec_ms >= pre_ms and n_dec) else "prefill"
 
     result = {
-        "metric": "decode KV GB/s (KV bytes read per 32-layer iteration / iteration time) at batch 32",
+        "metric": metric,
         "value": round(value, 1),
-        "unit": "GB/s",
+        "unit": unit,
         "n_gpus": ws,
-        "steps": args.steps,
+        "steps": K,
         "warmup": args.warmup,
-        "ms_per_step": round(t_ms / args.steps, 4),
-        "us_per_iteration": round(t_ms / args.steps * 1e3, 1),
-        "attention_tokens_per_s": round(att_tokens_step * L * args.steps * ws / (t_ms * 1e-3), 1),
-        "hbm_frac_of_measured_peak": round(value / hbm_peak, 4),
+        "ms_per_step": round(t_ms / K, 4),
+        "us_per_iteration": round(t_ms / K / len(steps) * 1e3, 1),
+        "attention_tokens_per_s": round(tokens_step * K * ws / (t_ms * 1e-3), 1),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "f16 storage, f32 arithmetic",
         "data": "synthetic",
         "config": {"workload": args.config, "description": CONFIG_TEXT[args.config], "num_layers": L,
-                   "num_seqs": B, "heads": H, "head_dim": D, "pool_blocks": wl.num_blocks,
-                   "context_tokens": att_tokens_step, "max_context": int(wl.ctx_lens.max()),
-                   "kv_bytes_per_step": kv_bytes_step, "seed": wl.seed,
-                   "l2": "inputs larger than L2 (every step reads the whole KV context of all 32 layers)"},
+                   "iterations_per_step": len(steps), "num_seqs": wl0.num_seqs, "heads": H, "head_dim": HEAD_DIM,
+                   "pool_blocks": wl0.num_blocks, "kv_bytes_per_step": kv_step,
+                   "prefill_flops_per_step": flops_step, "seed": wl0.seed,
+                   "max_context": int(max(int(s.wl.ctx_lens.max()) for s in steps)),
+                   "l2": "inputs larger than L2 (every step reads the whole KV context of all layers)"},
         "clocks": clocks,
-        "gpu_launches": launches_per_layer * L * args.steps,
-        "roofline": {"bound": "hbm", "kernel": "decode_attn (decode_kernel + reduce_kernel)",
-                     "achieved": round(achieved, 1), "peak": hbm_peak, "peak_kind": peak_kind, "unit": "GB/s",
-                     "frac": round(achieved / hbm_peak, 4), "traffic": traffic,
-                     "algorithmic_bytes_per_launch": dec_bytes, "avg_launch_us": round(dec_avg_ms * 1e3, 2),
-                     "layerwise_ms_per_step": round(t2_ms / args.steps, 4)},
-        "e2e": {"value": round(total_kv / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": round(e2e_ms / args.steps, 4)},
+        "gpu_launches": launches_step * K,
+        "roofline": rooflines[dominant],
+        "rooflines": rooflines,
+        "e2e": {"value": round(e2e_value, 1), "unit": unit, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(e2e_ms / K, 4)},
     }
+    if has_decode:
+        result["hbm_frac_of_measured_peak"] = round(value / hbm_peak, 4)
+    if has_prefill:
+        result["prefill_tflops"] = round(flops_step * K * ws / (t_ms * 1e-3) / 1e12, 1)
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = cpu_baseline(wl, pool_t, args.cpu_seconds)
+        result["cpu_baseline"] = cpu_baseline(iters[0], pool_t, args.cpu_seconds, L)
     if rank == 0:
         print(json.dumps(result), flush=True)
     if ws > 1:
         dist.destroy_process_group()
-
-
-def _metadata_via_block_manager(pkv, pool, wl):
-    """Step metadata from libpkv's block manager, as a serving loop would get it.
-
-    The pool hands blocks out in the workload's permutation order, so the
-    tables equal the workload's own (checked)."""
-    nb_used = int(np.unique(wl.block_tables[wl.block_tables >= 0]).size)
-    perm = np.concatenate([wl.block_tables[r][wl.block_tables[r] >= 0] for r in range(wl.num_seqs)])
-    _, first = np.unique(perm, return_index=True)
-    order = perm[np.sort(first)]
-    rest = np.setdiff1d(np.arange(wl.num_blocks), order)
-    pool_order = np.concatenate([order, rest]).astype(np.int64)
-    mgr = pkv.Pool(None, wl.num_blocks, num_layers=wl.num_layers, num_heads=wl.num_heads, free_order=pool_order)
-    prefix = int(wl.meta.get("prefix_blocks", 0))
-    if prefix:
-        assert mgr.seq_grow(-1, prefix * 16) == pkv.PKV_OK
-    for r in range(wl.num_seqs):
-        if prefix:
-            assert mgr.seq_share_prefix(r, -1, prefix) == pkv.PKV_OK
-        assert mgr.seq_grow(r, int(wl.ctx_lens[r])) == pkv.PKV_OK
-    st, tables, ctx, slots, qs = mgr.build_step(np.arange(wl.num_seqs), wl.q_lens, wl.max_blocks)
-    assert st == pkv.PKV_OK and np.array_equal(tables, wl.block_tables) and np.array_equal(ctx, wl.ctx_lens)
-    assert mgr.free_blocks() == wl.num_blocks - nb_used
-    return tables, ctx, slots, qs
 
 
 # ------------------------------------------------------------------ oracle timings
@@ -377,29 +485,43 @@ def _layer_sample(wl, layer, pool_t=None, seed=0):
     for r in range(wl.num_seqs):
         tables[r, :nb[r]] = inv[cur:cur + nb[r]]
         cur += nb[r]
-    q = workloads.normal_fp16((wl.num_seqs, wl.num_heads, 128), workloads.value_seed(wl.seed, "q", layer)).numpy()
+    q = workloads.normal_fp16((wl.num_tokens, wl.num_heads, HEAD_DIM),
+                              workloads.value_seed(wl.seed, "q", layer)).numpy()
     return np.ascontiguousarray(mini), tables, q.view(np.uint16), len(uniq)
 
 
-def cpu_baseline(wl, pool_t, budget_s):
+def _oracle_layer(oracle, wl, mini, tables, q, n):
+    g = oracle.geom(n, 1, wl.num_heads)
+    B = wl.num_decode
+    if B:
+        oracle.decode_attn(mini, g, 0, q[:B], tables[:B], wl.ctx_lens[:B], SCALE)
+    if wl.num_seqs > B:
+        oracle.prefill_attn(mini, g, 0, q, wl.q_start_loc()[B:], tables[B:], wl.ctx_lens[B:], SCALE)
+
+
+def cpu_baseline(wl, pool_t, budget_s, layers):
     import oracle
     threads = len(os.sched_getaffinity(0))
     oracle.set_num_threads(threads)
-    done_bytes, t_total, layers = 0, 0.0, 0
-    for layer in range(wl.num_layers):
+    t_total, done = 0.0, 0
+    for layer in range(layers):
         mini, tables, q, n = _layer_sample(wl, layer, pool_t)
-        g = oracle.geom(n, 1, wl.num_heads)
         t0 = time.perf_counter()
-        oracle.decode_attn(mini, g, 0, q, tables, wl.ctx_lens, SCALE)
+        _oracle_layer(oracle, wl, mini, tables, q, n)
         t_total += time.perf_counter() - t0
-        done_bytes += int(wl.ctx_lens.astype(np.int64).sum()) * KV_BYTES_PER_TOKEN_LAYER
-        layers += 1
+        done += 1
         if t_total >= budget_s:
             break
-    return {"value": round(done_bytes / t_total / 1e9, 3), "unit": "GB/s", "cores": threads, "kind": "oracle",
-            "sample": f"decode attention of all {wl.num_seqs} rows x {wl.num_heads} heads for {layers} of "
-                      f"{wl.num_layers} layers (referenced blocks copied to host first, copy not timed)",
-            "seconds": round(t_total, 2)}
+    kv = kv_bytes(wl, done)
+    res = {"unit": "GB/s", "cores": threads, "kind": "oracle", "seconds": round(t_total, 2),
+           "sample": f"all rows and heads of the first iteration for {done} of {layers} layers (referenced blocks "
+                     f"copied to host first, copy not timed)"}
+    if wl.num_decode:
+        res["value"] = round(kv / t_total / 1e9, 3)
+    else:
+        res["unit"] = "TFLOP/s"
+        res["value"] = round(4 * HEAD_DIM * wl.num_heads * prefill_pairs(wl) * done / t_total / 1e12, 6)
+    return res
 
 
 def run_reference(args):
@@ -407,31 +529,34 @@ def run_reference(args):
     if rank != 0:
         return
     import oracle
-    wl = CONFIGS[args.config]()
+    wl = _iterations(args.config)[0]
     threads = len(os.sched_getaffinity(0))
     oracle.set_num_threads(threads)
-    samples = [_layer_sample(wl, l % wl.num_layers, None, seed=1) for l in range(min(2, wl.num_layers))]
-    per_step = int(wl.ctx_lens.astype(np.int64).sum()) * KV_BYTES_PER_TOKEN_LAYER
+    samples = [_layer_sample(wl, l, None, seed=1) for l in range(2)]
     times = []
     for i in range(args.warmup + args.steps):
         mini, tables, q, n = samples[i % len(samples)]
         t0 = time.perf_counter()
-        oracle.decode_attn(mini, oracle.geom(n, 1, wl.num_heads), 0, q, tables, wl.ctx_lens, SCALE)
+        _oracle_layer(oracle, wl, mini, tables, q, n)
         dt = time.perf_counter() - t0
         if i >= args.warmup:
             times.append(dt)
     total = sum(times)
-    value = per_step * len(times) / total / 1e9
-    res = {"impl": "reference", "metric": "decode KV GB/s (KV bytes read per 32-layer iteration / iteration time) "
-                                          "at batch 32",
-           "value": round(value, 3), "unit": "GB/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
-           "ms_per_step": round(total / len(times) * 1e3, 2), "higher_is_better": True, "scaling": "weak",
-           "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic",
+    if wl.num_decode:
+        metric = "decode KV GB/s (KV bytes read per 32-layer iteration / iteration time) at batch 32"
+        value, unit = kv_bytes(wl, len(times)) / total / 1e9, "GB/s"
+    else:
+        metric = "prefill attention TFLOP/s"
+        value, unit = 4 * HEAD_DIM * wl.num_heads * prefill_pairs(wl) * len(times) / total / 1e12, "TFLOP/s"
+    res = {"impl": "reference", "metric": metric, "value": round(value, 4), "unit": unit, "n_gpus": ws,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total / len(times) * 1e3, 2),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
+           "data": "synthetic",
            "config": {"workload": args.config, "description": CONFIG_TEXT[args.config],
-                      "step": "one layer of the iteration (bounded sample)"},
-           "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": threads, "kind": "oracle",
-                            "sample": "decode attention of all rows and heads of one layer per step"},
-           "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+                      "step": "one layer of the first iteration (bounded sample)"},
+           "cpu_baseline": {"value": round(value, 4), "unit": unit, "cores": threads, "kind": "oracle",
+                            "sample": "all rows and heads of one layer per step"},
+           "e2e": {"value": round(value, 4), "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(res), flush=True)
 
 
@@ -440,7 +565,8 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", default="average_decode", choices=sorted(CONFIGS))
+    ap.add_argument("--config", default="average_decode",
+                    choices=["average_decode", "long_decode", "shared_prefix_decode", "mixed_prefill"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)

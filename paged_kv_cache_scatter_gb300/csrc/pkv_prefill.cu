@@ -11,16 +11,20 @@
 // are already in the pool (kv_append runs first), so keys come only from
 // the pool, 128 at a time (8 blocks).
 //
-// Warp roles (192 threads):
+// Warp roles (320 threads):
 //   warp 0      TMA producer: K and V tiles of 8 blocks, two 64-dim halves
 //               each (2 KB boxes), into a 2-stage ring per operand.
 //   warp 1      TMEM owner and MMA issuer (one elected lane):
-//               S = Q K^T into one of two S buffers, O_tile = P V into one of
-//               two O buffers, completion signalled with tcgen05.commit.
-//   warps 2..5  softmax: thread r owns query row r (TMEM lane r). Per tile it
-//               reads S, updates the running max / sum in the log2 domain,
-//               writes P (FP16) to shared memory for the P V product, and
-//               folds the previous tile's O_tile into FP32 registers.
+//               S_j = Q K_j^T into S buffer j%2, then O += P_j V_j into the
+//               single O accumulator; completion signalled by tcgen05.commit.
+//   warps 2..9  softmax: two threads per query row r (TMEM lane r), one per
+//               64-key half. Per tile each loads the S row once, releases the
+//               S buffer, and writes its half of P = 2^(s*scale*log2e - m) in
+//               FP16 to P buffer j%2. The running
+//               max m is only raised when the tile's max exceeds it by more
+//               than 8 (a factor 256, far inside FP16/FP32 range); then the
+//               row's O in TMEM and its sum are rescaled once the previous
+//               P V product has landed. The result is exact up to rounding.
 // Shared-memory operands use the 128-byte swizzle: rows of 128 B (64 halves),
 // two slabs per 128-wide operand, 8-row groups 1,024 B apart.
 #include <cuda.h>
@@ -73,24 +77,27 @@ namespace {
 
 constexpr int kRows = 128;     // query rows per CTA (MMA M)
 constexpr int kKeys = 128;     // keys per tile (8 blocks)
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;  // producer, MMA, 8 softmax warps
 constexpr int kOperandBytes = kRows * kHeadDim * 2;  // 32 KB: one 128 x 128 FP16 operand
 constexpr int kSlabBytes = kOperandBytes / 2;        // 16 KB: 128 rows x 64 halves
+constexpr float kRescaleThreshold = 8.f;             // log2 of the largest un-rescaled P (256)
 
 // shared-memory map (offsets from a 1,024-byte aligned base)
 constexpr int kSmQ = 0;
 constexpr int kSmK = kSmQ + kOperandBytes;       // 2 stages
 constexpr int kSmV = kSmK + 2 * kOperandBytes;   // 2 stages
-constexpr int kSmP = kSmV + 2 * kOperandBytes;
-constexpr int kSmBars = kSmP + kOperandBytes;
-enum Bar { K_FULL = 0, V_FULL = 2, K_EMPTY = 4, V_EMPTY = 6, S_FULL = 8, P_FULL = 10, O_FULL = 11, O_FREE = 13,
-           MMA_DONE = 15, NUM_BARS = 16 };
+constexpr int kSmP = kSmV + 2 * kOperandBytes;   // 2 buffers
+constexpr int kSmBars = kSmP + 2 * kOperandBytes;
+enum Bar { K_FULL = 0, V_FULL = 2, K_EMPTY = 4, V_EMPTY = 6, S_FULL = 8, S_FREE = 10, P_FULL = 12, P_EMPTY = 14,
+           MMA_DONE = 16, L_EX = 17, NUM_BARS = 18 };
+constexpr int kSoftmaxThreads = 256;
 constexpr int kSmTmemSlot = kSmBars + NUM_BARS * 8;
 constexpr int kSmAbort = kSmTmemSlot + 4;
-constexpr int kSmBytes = kSmAbort + 12;
+constexpr int kSmLx = kSmAbort + 12;             // [2 halves][128 rows] partial row sums
+constexpr int kSmBytes = kSmLx + 2 * kRows * 4;
 constexpr int kSmAlloc = kSmBytes + 1024;        // slack to align the base
 
-// TMEM columns: two S buffers then two O buffers, 128 fp32 columns each.
+// TMEM columns: two S buffers, then the O accumulator, 128 fp32 columns each.
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;
 constexpr uint32_t kColO = 256;
@@ -130,6 +137,8 @@ __device__ __forceinline__ bool flag_wait(uint32_t bar, uint32_t parity, volatil
     }
     return ok;
 }
+
+__device__ __forceinline__ uint32_t bar_addr(uint32_t bars, int idx) { return bars + 8u * (uint32_t)idx; }
 
 __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ CUtensorMap tmap,
                                                                const PrefillArgs a)
@@ -181,16 +190,17 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     volatile int* abort = reinterpret_cast<volatile int*>(smem + kSmAbort);
     if (threadIdx.x == 0) {
         for (int i = 0; i < 2; ++i) {
-            mbar_init(bars + 8 * (K_FULL + i), 1);
-            mbar_init(bars + 8 * (V_FULL + i), 1);
-            mbar_init(bars + 8 * (K_EMPTY + i), 1);
-            mbar_init(bars + 8 * (V_EMPTY + i), 1);
-            mbar_init(bars + 8 * (S_FULL + i), 1);
-            mbar_init(bars + 8 * (O_FULL + i), 1);
-            mbar_init(bars + 8 * (O_FREE + i), 128);
+            mbar_init(bar_addr(bars, K_FULL + i), 1);
+            mbar_init(bar_addr(bars, V_FULL + i), 1);
+            mbar_init(bar_addr(bars, K_EMPTY + i), 1);
+            mbar_init(bar_addr(bars, V_EMPTY + i), 1);
+            mbar_init(bar_addr(bars, S_FULL + i), 1);
+            mbar_init(bar_addr(bars, S_FREE + i), kSoftmaxThreads);
+            mbar_init(bar_addr(bars, P_FULL + i), kSoftmaxThreads);
+            mbar_init(bar_addr(bars, P_EMPTY + i), 1);
         }
-        mbar_init(bars + 8 * P_FULL, 128);
-        mbar_init(bars + 8 * MMA_DONE, 1);
+        mbar_init(bar_addr(bars, MMA_DONE), 1);
+        mbar_init(bar_addr(bars, L_EX), kSoftmaxThreads);
         *abort = 0;
         fence_mbar_init();
     }
@@ -212,25 +222,23 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             const uint32_t ph = (uint32_t)(j >> 1) & 1u;
             const int nb = min(8, nblk - 8 * j);
             const int id = lane < nb ? __ldg(trow + 8 * j + lane) : 0;
-            if (j >= 2 && !flag_wait(bars + 8 * (K_EMPTY + st), ph ^ 1u, abort, a.status)) break;
-            if (lane == 0) {
-                mbar_arrive_expect_tx(bars + 8 * (K_FULL + st), nb * kTileBytes);
-            }
+            if (j >= 2 && !flag_wait(bar_addr(bars, K_EMPTY + st), ph ^ 1u, abort, a.status)) break;
+            if (lane == 0) mbar_arrive_expect_tx(bar_addr(bars, K_FULL + st), nb * kTileBytes);
             for (int b = 0; b < nb; ++b) {
                 const int idb = __shfl_sync(0xffffffffu, id, b);
                 if (lane == 0)
                     for (int half = 0; half < 2; ++half)
                         tma_load_5d(sb + kSmK + st * kOperandBytes + half * kSlabBytes + b * 2048, &tmap, half * 64, 0,
-                                    h, a.layer, idb, bars + 8 * (K_FULL + st));
+                                    h, a.layer, idb, bar_addr(bars, K_FULL + st));
             }
-            if (j >= 2 && !flag_wait(bars + 8 * (V_EMPTY + st), ph ^ 1u, abort, a.status)) break;
-            if (lane == 0) mbar_arrive_expect_tx(bars + 8 * (V_FULL + st), nb * kTileBytes);
+            if (j >= 2 && !flag_wait(bar_addr(bars, V_EMPTY + st), ph ^ 1u, abort, a.status)) break;
+            if (lane == 0) mbar_arrive_expect_tx(bar_addr(bars, V_FULL + st), nb * kTileBytes);
             for (int b = 0; b < nb; ++b) {
                 const int idb = __shfl_sync(0xffffffffu, id, b);
                 if (lane == 0)
                     for (int half = 0; half < 2; ++half)
                         tma_load_5d(sb + kSmV + st * kOperandBytes + half * kSlabBytes + b * 2048, &tmap, half * 64, 0,
-                                    a.num_heads + h, a.layer, idb, bars + 8 * (V_FULL + st));
+                                    a.num_heads + h, a.layer, idb, bar_addr(bars, V_FULL + st));
             }
             issued = j + 1;
         }
@@ -238,8 +246,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         if (*abort && lane == 0) {
             // let this warp's loads that nobody consumed land before the CTA exits
             for (int j = (issued > 2 ? issued - 2 : 0); j < issued; ++j) {
-                mbar_wait(bars + 8 * (K_FULL + (j & 1)), (uint32_t)(j >> 1) & 1u);
-                mbar_wait(bars + 8 * (V_FULL + (j & 1)), (uint32_t)(j >> 1) & 1u);
+                mbar_wait(bar_addr(bars, K_FULL + (j & 1)), (uint32_t)(j >> 1) & 1u);
+                mbar_wait(bar_addr(bars, V_FULL + (j & 1)), (uint32_t)(j >> 1) & 1u);
             }
         }
     } else if (warp == 1) {
@@ -248,7 +256,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             if (j < nkt) {
                 const int st = j & 1;
                 const uint32_t ph = (uint32_t)(j >> 1) & 1u;
-                if (!flag_wait(bars + 8 * (K_FULL + st), ph, abort, a.status)) break;
+                if (!flag_wait(bar_addr(bars, K_FULL + st), ph, abort, a.status)) break;
+                if (j >= 2 && !flag_wait(bar_addr(bars, S_FREE + st), ph ^ 1u, abort, a.status)) break;
                 tc_fence_after();
                 if (lane == 0) {
 #pragma unroll
@@ -257,17 +266,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                         tc_mma_f16(tmem + kColS + st * 128, sw128_desc(sb + kSmQ + off, 16, 1024),
                                    sw128_desc(sb + kSmK + st * kOperandBytes + off, 16, 1024), kIdescS, kk > 0);
                     }
-                    tc_commit(bars + 8 * (S_FULL + st));
-                    tc_commit(bars + 8 * (K_EMPTY + st));
+                    tc_commit(bar_addr(bars, S_FULL + st));
+                    tc_commit(bar_addr(bars, K_EMPTY + st));
                 }
                 __syncwarp();
             }
             if (j >= 1) {
                 const int i = j - 1, st = i & 1;
                 const uint32_t ph = (uint32_t)(i >> 1) & 1u;
-                if (!flag_wait(bars + 8 * P_FULL, (uint32_t)i & 1u, abort, a.status)) break;
-                if (!flag_wait(bars + 8 * (V_FULL + st), ph, abort, a.status)) break;
-                if (i >= 2 && !flag_wait(bars + 8 * (O_FREE + st), ph ^ 1u, abort, a.status)) break;
+                if (!flag_wait(bar_addr(bars, P_FULL + st), ph, abort, a.status)) break;
+                if (!flag_wait(bar_addr(bars, V_FULL + st), ph, abort, a.status)) break;
                 if (i == nkt - 1) {
                     // keys past the last row's position may hold anything (even NaN); zero their V rows so
                     // that P = 0 times V stays 0 in the tensor core
@@ -286,120 +294,137 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk) {
                         const uint32_t aoff = (kk >> 2) * kSlabBytes + (kk & 3) * 32;
-                        tc_mma_f16(tmem + kColO + st * 128, sw128_desc(sb + kSmP + aoff, 16, 1024),
+                        tc_mma_f16(tmem + kColO, sw128_desc(sb + kSmP + st * kOperandBytes + aoff, 16, 1024),
                                    sw128_desc(sb + kSmV + st * kOperandBytes + kk * 2048, kSlabBytes, 1024), kIdescPV,
-                                   kk > 0);
+                                   (i > 0 || kk > 0) ? 1u : 0u);
                     }
-                    tc_commit(bars + 8 * (O_FULL + st));
-                    tc_commit(bars + 8 * (V_EMPTY + st));
+                    tc_commit(bar_addr(bars, P_EMPTY + st));
+                    tc_commit(bar_addr(bars, V_EMPTY + st));
                 }
                 __syncwarp();
             }
         }
         if (lane == 0) {
-            tc_commit(bars + 8 * MMA_DONE);
-            mbar_wait(bars + 8 * MMA_DONE, 0);
+            tc_commit(bar_addr(bars, MMA_DONE));
+            mbar_wait(bar_addr(bars, MMA_DONE), 0);
         }
         __syncwarp();
     } else {
-        // ================================================= softmax
+        // ================================================= softmax (8 warps)
+        // Warps w and w + 4 share TMEM lane quarter w % 4, i.e. the same 32
+        // rows. Both read the whole S row (for the row max); each then
+        // exponentiates one 64-key half (P slab hv) and owns the matching
+        // 64 columns of O.
         const int qtr = warp & 3;
+        const int hv = (warp - 2) >> 2;
         const int row = qtr * 32 + lane;
         const bool valid = row < rows;
         const int pos = p0 + row;
         const uint32_t tl = tmem + ((uint32_t)(qtr * 32) << 16);
-        float o[kHeadDim];
-#pragma unroll
-        for (int d = 0; d < kHeadDim; ++d) o[d] = 0.f;
-        float m_old = -INFINITY, l = 0.f, alpha_prev = 1.f;
+        float m_used = valid ? -INFINITY : 0.f, l = 0.f;
         bool ok = true;
-        for (int j = 0; j < nkt && ok; ++j) {
+        for (int j = 0; j < nkt; ++j) {
             const int st = j & 1;
-            if (!flag_wait(bars + 8 * (S_FULL + st), (uint32_t)(j >> 1) & 1u, abort, a.status)) { ok = false; break; }
+            const uint32_t ph = (uint32_t)(j >> 1) & 1u;
+            if (!flag_wait(bar_addr(bars, S_FULL + st), ph, abort, a.status)) { ok = false; break; }
             tc_fence_after();
-            const uint32_t sa = tl + kColS + st * 128;
+            uint32_t sr[64], so[64];  // this thread's 64-key half, and the other half
+            tc_ld64_pair(tl + kColS + st * 128 + hv * 64, sr, tl + kColS + st * 128 + (1 - hv) * 64, so);
+            tc_fence_before();
+            mbar_arrive(bar_addr(bars, S_FREE + st));
+
             const int key0 = j * kKeys;
-            float mx = -INFINITY;
+            if (key0 + kKeys - 1 > p0 || !valid) {
+                // diagonal tile or padding row: keys past the row's position count as -inf
+                const int nvis = valid ? pos - key0 + 1 : 0;
+                const int own = hv * 64, oth = (1 - hv) * 64;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                float v[32];
-                tc_ld32(sa + c * 32, v);
-#pragma unroll
-                for (int e = 0; e < 32; ++e)
-                    if (key0 + c * 32 + e <= pos) mx = fmaxf(mx, v[e]);
+                for (int e = 0; e < 64; ++e) {
+                    if (own + e >= nvis) sr[e] = __float_as_uint(-INFINITY);
+                    if (oth + e >= nvis) so[e] = __float_as_uint(-INFINITY);
+                }
             }
-            const float m_new = valid ? fmaxf(m_old, mx * a.scale_log2) : 0.f;
-            const float alpha = ex2(m_old - m_new);
-            if (j >= 1) {
-                const int i = j - 1;
-                if (!flag_wait(bars + 8 * (O_FULL + (i & 1)), (uint32_t)(i >> 1) & 1u, abort, a.status)) {
+            float mxs[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) mxs[u] = fmaxf(__uint_as_float(sr[u]), __uint_as_float(so[u]));
+#pragma unroll
+            for (int e = 8; e < 64; ++e)
+                mxs[e & 7] = fmaxf(mxs[e & 7], fmaxf(__uint_as_float(sr[e]), __uint_as_float(so[e])));
+            const float mx = fmaxf(fmaxf(fmaxf(mxs[0], mxs[1]), fmaxf(mxs[2], mxs[3])),
+                                   fmaxf(fmaxf(mxs[4], mxs[5]), fmaxf(mxs[6], mxs[7])));
+            const float m_tile = mx * a.scale_log2;
+            const bool raise = valid && m_tile > m_used + kRescaleThreshold;
+            if (j > 0 && __any_sync(0xffffffffu, raise)) {
+                // the previous P V product must have landed before O is rescaled
+                if (!flag_wait(bar_addr(bars, P_EMPTY + ((j - 1) & 1)), (uint32_t)((j - 1) >> 1) & 1u, abort,
+                               a.status)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
+                const float f = raise ? ex2(m_used - m_tile) : 1.f;
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    float v[32];
-                    tc_ld32(tl + kColO + (i & 1) * 128 + c * 32, v);
+                for (int c = 0; c < 2; ++c) {
+                    float of[32];
+                    uint32_t o[32];
+                    tc_ld32(tl + kColO + hv * 64 + c * 32, of);
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) o[c * 32 + e] = fmaf(o[c * 32 + e], alpha_prev, v[e]);
+                    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(of[e] * f);
+                    tc_st32(tl + kColO + hv * 64 + c * 32, o);
                 }
-                tc_fence_before();
-                mbar_arrive(bars + 8 * (O_FREE + (i & 1)));
+                l *= f;
             }
-            float lsum = 0.f;
+            if (raise) m_used = m_tile;
+
+            // P buffer st is free once the P V product of tile j-2 has landed
+            if (j >= 2 && !flag_wait(bar_addr(bars, P_EMPTY + st), ph ^ 1u, abort, a.status)) { ok = false; break; }
+            float ls[8];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                float v[32];
-                tc_ld32(sa + c * 32, v);
-                uint32_t packed[16];
+            for (int u = 0; u < 8; ++u) ls[u] = 0.f;
+            const uint32_t prow = sb + kSmP + st * kOperandBytes + hv * kSlabBytes + row * 128;
 #pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    const bool k0 = valid && key0 + c * 32 + e <= pos;
-                    const bool k1 = valid && key0 + c * 32 + e + 1 <= pos;
-                    const float pa = k0 ? ex2(fmaf(v[e], a.scale_log2, -m_new)) : 0.f;
-                    const float pb = k1 ? ex2(fmaf(v[e + 1], a.scale_log2, -m_new)) : 0.f;
-                    const __half2 hp = __floats2half2_rn(pa, pb);
-                    const float2 back = __half22float2(hp);  // the sum uses the weights the MMA will use
-                    lsum += back.x + back.y;
-                    packed[e >> 1] = *reinterpret_cast<const uint32_t*>(&hp);
-                }
+            for (int c = 0; c < 8; ++c) {  // 8 chunks of 8 keys of this half
+                uint32_t packed[4];
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
-                    const int ch = (c & 1) * 4 + u;  // 16-byte chunk within the 128-byte row
-                    st_shared_v4(sb + kSmP + (c >> 1) * kSlabBytes + row * 128 + ((ch ^ (row & 7)) << 4),
-                                 make_uint4(packed[4 * u], packed[4 * u + 1], packed[4 * u + 2], packed[4 * u + 3]));
+                    const int e = c * 8 + 2 * u;
+                    const float pa = ex2(fmaf(__uint_as_float(sr[e]), a.scale_log2, -m_used));
+                    const float pb = ex2(fmaf(__uint_as_float(sr[e + 1]), a.scale_log2, -m_used));
+                    ls[2 * u] += pa;
+                    ls[2 * u + 1] += pb;
+                    const __half2 hp = __floats2half2_rn(pa, pb);
+                    packed[u] = *reinterpret_cast<const uint32_t*>(&hp);
                 }
+                st_shared_v4(prow + ((c ^ (row & 7)) << 4), make_uint4(packed[0], packed[1], packed[2], packed[3]));
             }
-            l = fmaf(l, alpha, lsum);
-            m_old = m_new;
-            alpha_prev = alpha;
+            l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
             fence_proxy_async_smem();
             tc_fence_before();
-            mbar_arrive(bars + 8 * P_FULL);
+            mbar_arrive(bar_addr(bars, P_FULL + st));
         }
         if (ok) {
             const int i = nkt - 1;
-            if (flag_wait(bars + 8 * (O_FULL + (i & 1)), (uint32_t)(i >> 1) & 1u, abort, a.status)) {
+            float* lx = reinterpret_cast<float*>(smem + kSmLx);
+            lx[hv * kRows + row] = l;
+            mbar_arrive(bar_addr(bars, L_EX));
+            if (flag_wait(bar_addr(bars, P_EMPTY + (i & 1)), (uint32_t)(i >> 1) & 1u, abort, a.status) &&
+                flag_wait(bar_addr(bars, L_EX), 0, abort, a.status)) {
                 tc_fence_after();
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    float v[32];
-                    tc_ld32(tl + kColO + (i & 1) * 128 + c * 32, v);
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) o[c * 32 + e] = fmaf(o[c * 32 + e], alpha_prev, v[e]);
-                }
+                const float l_row = l + lx[(1 - hv) * kRows + row];
+                float o[64];
+                tc_ld32(tl + kColO + hv * 64, o);
+                tc_ld32(tl + kColO + hv * 64 + 32, o + 32);
                 if (valid) {
-                    const float inv = 1.f / l;
+                    const float inv = 1.f / l_row;
                     uint4* dst = reinterpret_cast<uint4*>(a.out + ((int64_t)(q0 + qt * kRows + row) * a.num_heads + h) *
-                                                                      kHeadDim);
+                                                                      kHeadDim + hv * 64);
 #pragma unroll
-                    for (int c = 0; c < 16; ++c) {
+                    for (int c = 0; c < 8; ++c) {
                         uint32_t w[4];
 #pragma unroll
                         for (int u = 0; u < 4; ++u) {
-                            const __half2 hv = __floats2half2_rn(o[c * 8 + 2 * u] * inv, o[c * 8 + 2 * u + 1] * inv);
-                            w[u] = *reinterpret_cast<const uint32_t*>(&hv);
+                            const __half2 hq = __floats2half2_rn(o[c * 8 + 2 * u] * inv, o[c * 8 + 2 * u + 1] * inv);
+                            w[u] = *reinterpret_cast<const uint32_t*>(&hq);
                         }
                         dst[c] = make_uint4(w[0], w[1], w[2], w[3]);
                     }
