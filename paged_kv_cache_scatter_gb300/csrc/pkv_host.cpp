@@ -351,6 +351,9 @@ static pkv_status check_decode(pkv_pool* pool, int32_t layer, const void* q, con
     if (!q || !tables || !ctx_lens || !out) return fail(PKV_E_INVALID, "NULL q, tables, ctx_lens or out");
     if (!aligned(q, 16) || !aligned(out, 16) || !aligned(tables, 4) || !aligned(ctx_lens, 4))
         return fail(PKV_E_INVALID, "q/out must be 16-byte aligned, tables/ctx_lens 4-byte aligned");
+    if (pkv::decode_max_parts(max_blocks, pool->partition_tokens) > pkv::kMaxPartitionsPerRow)
+        return fail(PKV_E_INVALID, "block tables of %d blocks need more than %d partitions per row", max_blocks,
+                    pkv::kMaxPartitionsPerRow);
     const size_t need = pkv::decode_workspace_bytes(num_seqs, pool->desc.num_heads, max_blocks, pool->partition_tokens);
     if (pkv::decode_max_parts(max_blocks, pool->partition_tokens) > 1) {
         if (!ws || ws_bytes < need || !aligned(ws, 256))
@@ -369,9 +372,11 @@ pkv_status pkv_decode_attn(pkv_pool* pool, int32_t layer, const void* q, const i
     if (num_seqs == 0) return PKV_OK;
     DeviceGuard dg(pool->device);
     if (!dg.ok) return fail(PKV_E_DEVICE, "cannot select the pool's device");
-    cudaError_t e = pkv::launch_decode(pool->geom, layer, q, block_tables, max_blocks, ctx_lens, num_seqs, scale, out,
-                                       workspace, pool->partition_tokens, pool->status_dev,
-                                       static_cast<cudaStream_t>(stream));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = pkv::clear_decode_counters(pool->geom, num_seqs, max_blocks, pool->partition_tokens, workspace, s);
+    if (e != cudaSuccess) return pkv::cuda_fail(e, "clear decode counters");
+    e = pkv::launch_decode(pool->geom, layer, q, block_tables, max_blocks, ctx_lens, num_seqs, scale, out, workspace,
+                           pool->partition_tokens, nullptr, nullptr, nullptr, pool->status_dev, s);
     return e == cudaSuccess ? PKV_OK : pkv::cuda_fail(e, "decode launch");
 }
 
@@ -417,35 +422,48 @@ pkv_status pkv_step(pkv_pool* pool, const pkv_step_desc* st, void* workspace, si
     if (!st->block_tables || !st->ctx_lens || !st->slot_mapping || !st->q || !st->k || !st->v || !st->out)
         return fail(PKV_E_INVALID, "NULL step array");
     if (P > 0 && !st->q_start_loc) return fail(PKV_E_INVALID, "prefill rows need q_start_loc");
-    const int64_t tok_elems = (int64_t)pool->desc.num_heads * pkv::kHeadDim;
     if (st->q_layer_stride % 8 || st->k_layer_stride % 8 || st->v_layer_stride % 8 || st->out_layer_stride % 8)
         return fail(PKV_E_INVALID, "layer strides must be multiples of 8 elements");
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int64_t tok = (int64_t)pool->desc.num_heads * pkv::kHeadDim * 2;  // bytes of one token's q/k/v row
     const char* q = static_cast<const char*>(st->q);
     const char* k = static_cast<const char*>(st->k);
     const char* v = static_cast<const char*>(st->v);
     char* out = static_cast<char*>(st->out);
+    // Validate the per-layer calls once, on the first layer's pointers (the rest differ only by stride).
+    if (pkv_status r = check_decode(pool, st->first_layer, q, st->block_tables, st->max_blocks, st->ctx_lens, B, out,
+                                    workspace, workspace_bytes))
+        return r;
+    if (!aligned(k, 16) || !aligned(v, 16) || !aligned(st->slot_mapping, 8))
+        return fail(PKV_E_INVALID, "k/v must be 16-byte aligned, slot_mapping 8-byte aligned");
+    DeviceGuard dg(pool->device);
+    if (!dg.ok) return fail(PKV_E_DEVICE, "cannot select the pool's device");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = pkv::clear_decode_counters(pool->geom, B, st->max_blocks, pool->partition_tokens, workspace, s);
+    if (e != cudaSuccess) return pkv::cuda_fail(e, "clear decode counters");
     for (int32_t i = 0; i < st->num_layers; ++i) {
         const int32_t layer = st->first_layer + i;
         const int64_t li = i;
         const char* ql = q + li * st->q_layer_stride * 2;
+        const char* kl = k + li * st->k_layer_stride * 2;
+        const char* vl = v + li * st->v_layer_stride * 2;
         char* ol = out + li * st->out_layer_stride * 2;
-        pkv_status r = pkv_kv_append(pool, layer, k + li * st->k_layer_stride * 2, v + li * st->v_layer_stride * 2,
-                                     st->slot_mapping, st->num_tokens, stream);
-        if (r) return r;
+        if (P > 0) {  // the prefill tokens' kv_append; the decode rows append inside the decode kernel
+            e = pkv::launch_kv_append(pool->geom, layer, kl + B * tok, vl + B * tok, st->slot_mapping + B,
+                                      st->num_tokens - B, pool->status_dev, s);
+            if (e != cudaSuccess) return pkv::cuda_fail(e, "kv_append launch");
+        }
         if (B > 0) {
-            r = pkv_decode_attn(pool, layer, ql, st->block_tables, st->max_blocks, st->ctx_lens, B, st->scale, ol,
-                                workspace, workspace_bytes, stream);
-            if (r) return r;
+            e = pkv::launch_decode(pool->geom, layer, ql, st->block_tables, st->max_blocks, st->ctx_lens, B, st->scale,
+                                   ol, workspace, pool->partition_tokens, kl, vl, st->slot_mapping, pool->status_dev, s);
+            if (e != cudaSuccess) return pkv::cuda_fail(e, "decode launch");
         }
         if (P > 0) {
-            r = pkv_prefill_attn(pool, layer, ql, st->q_start_loc + B, st->block_tables + (int64_t)B * st->max_blocks,
-                                 st->max_blocks, st->ctx_lens + B, P, st->max_q_len, st->scale, ol, stream);
+            pkv_status r = pkv_prefill_attn(pool, layer, ql, st->q_start_loc + B,
+                                            st->block_tables + (int64_t)B * st->max_blocks, st->max_blocks,
+                                            st->ctx_lens + B, P, st->max_q_len, st->scale, ol, stream);
             if (r) return r;
         }
     }
-    (void)tok_elems;
-    (void)s;
     return PKV_OK;
 }
 

@@ -16,6 +16,7 @@ constexpr int kBlockSize = 16;
 constexpr int kTileBytes = kBlockSize * kHeadDim * 2;  // one head of one block: 4,096 B
 constexpr int kDefaultPartition = 512;
 constexpr int kMaxPartition = 2048;
+constexpr int kMaxPartitionsPerRow = 4096;  // the decode kernel merges at most this many partitions of a row
 
 struct Seq {
     std::vector<int32_t> table;
@@ -64,9 +65,15 @@ cudaError_t launch_kv_append(const PoolGeom& g, int layer, const void* k, const 
                              int num_tokens, unsigned int* status, cudaStream_t stream);
 int decode_max_parts(int max_blocks, int partition_tokens);
 size_t decode_workspace_bytes(int num_seqs, int num_heads, int max_blocks, int partition_tokens);
+// Zero the split-K counters of a decode workspace (they return to zero after every
+// completed launch; this covers the first use and any launch that stopped early).
+cudaError_t clear_decode_counters(const PoolGeom& g, int num_seqs, int max_blocks, int partition_tokens, void* ws,
+                                  cudaStream_t stream);
+// k_new/v_new/slots non-NULL: the decode rows' kv_append is done by the same kernel.
 cudaError_t launch_decode(const PoolGeom& g, int layer, const void* q, const int32_t* tables, int max_blocks,
                           const int32_t* ctx_lens, int num_seqs, float scale, void* out, void* ws,
-                          int partition_tokens, unsigned int* status, cudaStream_t stream);
+                          int partition_tokens, const void* k_new, const void* v_new, const int64_t* slots,
+                          unsigned int* status, cudaStream_t stream);
 cudaError_t launch_wait_probe(uint64_t timeout_ns, unsigned int* status, cudaStream_t stream);
 
 // pkv_prefill.cu

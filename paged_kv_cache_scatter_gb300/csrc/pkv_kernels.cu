@@ -93,18 +93,28 @@ cudaError_t launch_kv_append(const PoolGeom& g, int layer, const void* k, const 
 // (online softmax in the log2 domain, the scale pre-multiplied by log2 e),
 // and each lane then owns 4 output dims for the P.V update.
 //
-// The warps' states merge in shared memory in fixed order; a partition
-// either writes the final FP16 row (single-partition rows) or its
-// un-normalised output, max and sum to the workspace for reduce_kernel.
-// The partition plan depends only on ctx_len and partition_tokens, so a
-// row's result is the same in any batch.
+// The warps' states merge in shared memory in fixed order. A single-partition
+// row writes its FP16 output directly. Otherwise each partition writes its
+// un-normalised output, max and sum to the workspace and bumps a per-(row,
+// head) counter; the CTA that brings the counter to the row's partition
+// count merges all partitions in partition order and resets the counter to
+// zero ("The inference engine" (wpnews), "IO-aware attention": tiles combine
+// exactly through their softmax statistics). The partition plan depends only
+// on ctx_len and partition_tokens, so a row's result is the same in any batch.
+//
+// With `append` set, the kernel also performs kv_append for the decode rows:
+// the CTA holding a row's last partition writes the row's new K/V (token r of
+// k_new / v_new) for its head into the slot slot_mapping[r], and the warp that
+// streams that block patches the new row into its shared-memory copy, so the
+// query sees its own new key exactly as if the append had run first.
 
 constexpr int kDecodeWarps = 4;
 constexpr int kDecodeStages = 2;
 constexpr int kStageBytes = 2 * kTileBytes;
+constexpr int kMaxMergeParts = kMaxPartitionsPerRow;  // s_w and s_l of the merge fit in the idle rings
 
 struct DecodeArgs {
-    const char* pool;
+    char* pool;
     int64_t block_bytes;
     int64_t head_off;   // layer * layer_bytes (the head offset is added per CTA)
     int64_t kv_bytes;
@@ -116,10 +126,15 @@ struct DecodeArgs {
     const int32_t* ctx_lens;
     float scale_log2;
     __half* out;
-    float* ws_o;   // [B][H][max_parts][128]
-    float* ws_ml;  // [B][H][max_parts][2]
+    float* ws_o;            // [B][H][max_parts][128]
+    float* ws_ml;           // [B][H][max_parts][2]
+    unsigned int* counters; // [B][H], zero between launches
     int max_parts;
     int part_tokens;
+    const __half* k_new;    // [B][H][128] when append
+    const __half* v_new;
+    const int64_t* slots;   // [B] when append
+    int append;
     unsigned int* status;
 };
 
@@ -129,14 +144,28 @@ struct DecodeLayout {
     static constexpr int kPbuf = kRing;                        // [WARPS][16] float
     static constexpr int kStats = kPbuf + WARPS * 16 * 4;      // [WARPS][2] float
     static constexpr int kBars = kStats + WARPS * 2 * 4;       // [WARPS][STAGES][2] u64
-    static constexpr int kBytes = kBars + WARPS * STAGES * 2 * 8;
+    static constexpr int kFlag = kBars + WARPS * STAGES * 2 * 8;
+    static constexpr int kBytes = kFlag + 16;
 };
+
+// Counter bump with release (prior writes of this CTA, ordered by a CTA
+// barrier, become visible first) and acquire (the other partitions' writes
+// are visible to this CTA afterwards) at GPU scope.
+__device__ __forceinline__ unsigned int atomic_add_acq_rel_gpu(unsigned int* p, unsigned int v)
+{
+    unsigned int old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
 
 template <int WARPS, int STAGES>
 __global__ void __launch_bounds__(WARPS * 32) decode_kernel(const DecodeArgs a)
 {
     using Lay = DecodeLayout<WARPS, STAGES>;
     extern __shared__ __align__(1024) unsigned char smem[];
+    // Grid (partition, head, row): the partitions of one (row, head) are
+    // dispatched next to each other, so their partials are still in L2 when
+    // the last of them merges.
     const int p = blockIdx.x, h = blockIdx.y, r = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -194,6 +223,33 @@ __global__ void __launch_bounds__(WARPS * 32) decode_kernel(const DecodeArgs a)
         }
     }
 
+    // The new token (position ctx - 1) lives in this partition's last block.
+    const int last_local = ((ctx - 1) >> 4) - blk_lo;
+    int patch_iter = -1;  // iteration of this warp that streams the new token's block
+    uint4 knew = make_uint4(0, 0, 0, 0), vnew = make_uint4(0, 0, 0, 0);
+    if (a.append && p == nparts - 1) {
+        const int64_t slot = __ldg(a.slots + r);
+        const int32_t tb = __ldg(trow + ((ctx - 1) >> 4));
+        const bool consistent = slot == (int64_t)tb * kBlockSize + ((ctx - 1) & 15) && tb >= 0 &&
+                                (int64_t)tb < a.num_blocks;
+        if (!consistent) {
+            if (threadIdx.x == 0) atomicOr(a.status, PKV_DEV_BAD_SLOT);
+        } else {
+            const uint4* ks = reinterpret_cast<const uint4*>(a.k_new + ((int64_t)r * a.num_heads + h) * kHeadDim);
+            const uint4* vs = reinterpret_cast<const uint4*>(a.v_new + ((int64_t)r * a.num_heads + h) * kHeadDim);
+            if (warp == last_local % WARPS) {
+                patch_iter = last_local / WARPS;
+                knew = __ldg(ks + (lane & 15));
+                vnew = __ldg(vs + (lane & 15));
+            }
+            if (warp == 0) {  // the global write, for later steps: lanes 0-15 K, 16-31 V
+                char* dst = a.pool + slot / kBlockSize * a.block_bytes + a.head_off + (int64_t)h * kTileBytes +
+                            (slot % kBlockSize) * 256 + (lane & 15) * 16 + (lane < 16 ? 0 : a.kv_bytes);
+                *reinterpret_cast<uint4*>(dst) = __ldg((lane < 16 ? ks : vs) + (lane & 15));
+            }
+        }
+    }
+
     // q, rotated per lane so that the K-tile reads below are free of bank
     // conflicts: register chunk j holds dims hf*64 + ((j + lane) & 7)*8 .. +8.
     const int t = lane >> 1, hf = lane & 1;
@@ -215,12 +271,16 @@ __global__ void __launch_bounds__(WARPS * 32) decode_kernel(const DecodeArgs a)
         const int s = i % STAGES;
         const uint32_t par = (uint32_t)(i / STAGES) & 1u;
         const uint32_t bk = bar0 + 16 * s, bv = bk + 8;
-        const unsigned char* kt = ring + s * kStageBytes;
-        const unsigned char* vt = kt + kTileBytes;
+        unsigned char* kt = ring + s * kStageBytes;
+        unsigned char* vt = kt + kTileBytes;
         const int key0 = (blk_lo + warp + i * WARPS) * kBlockSize;
         const int nvalid = min(kBlockSize, ctx - key0);
 
         if (!mbar_wait(bk, par)) { timed_out = true; break; }
+        if (i == patch_iter) {
+            if (lane < 16) *reinterpret_cast<uint4*>(kt + ((ctx - 1) & 15) * 256 + lane * 16) = knew;
+            __syncwarp();
+        }
         float acc = 0.f;
         {
             const uint4* krow = reinterpret_cast<const uint4*>(kt + t * 256 + hf * 128);
@@ -248,6 +308,10 @@ __global__ void __launch_bounds__(WARPS * 32) decode_kernel(const DecodeArgs a)
         __syncwarp();
 
         if (!mbar_wait(bv, par)) { timed_out = true; break; }
+        if (i == patch_iter) {
+            if (lane < 16) *reinterpret_cast<uint4*>(vt + ((ctx - 1) & 15) * 256 + lane * 16) = vnew;
+            __syncwarp();
+        }
 #pragma unroll
         for (int e = 0; e < 4; ++e) o[e] *= alpha;
         {
@@ -317,49 +381,58 @@ __global__ void __launch_bounds__(WARPS * 32) decode_kernel(const DecodeArgs a)
         L = fmaf(wt[w], stats[w * 2 + 1], L);
     }
     const int64_t rh = (int64_t)r * a.num_heads + h;
+    if (nparts == 1) {
+        for (int d = threadIdx.x; d < kHeadDim; d += WARPS * 32) {
+            float O = 0.f;
+#pragma unroll
+            for (int w = 0; w < WARPS; ++w)
+                O = fmaf(wt[w], reinterpret_cast<const float*>(smem + w * STAGES * kStageBytes)[d], O);
+            a.out[rh * kHeadDim + d] = __float2half_rn(O / L);
+        }
+        return;
+    }
+    const int64_t slot = rh * a.max_parts + p;
     for (int d = threadIdx.x; d < kHeadDim; d += WARPS * 32) {
         float O = 0.f;
 #pragma unroll
-        for (int w = 0; w < WARPS; ++w) {
-            const float* mw = reinterpret_cast<const float*>(smem + w * STAGES * kStageBytes);
-            O = fmaf(wt[w], mw[d], O);
-        }
-        if (nparts == 1) {
-            a.out[rh * kHeadDim + d] = __float2half_rn(O / L);
-        } else {
-            const int64_t slot = rh * a.max_parts + p;
-            a.ws_o[slot * kHeadDim + d] = O;
-            if (d == 0) {
-                a.ws_ml[slot * 2] = M;
-                a.ws_ml[slot * 2 + 1] = L;
-            }
-        }
+        for (int w = 0; w < WARPS; ++w)
+            O = fmaf(wt[w], reinterpret_cast<const float*>(smem + w * STAGES * kStageBytes)[d], O);
+        a.ws_o[slot * kHeadDim + d] = O;
     }
-}
-
-// Merge a row's partitions: M = max m_p, out = sum 2^(m_p-M) o_p / sum 2^(m_p-M) l_p
-// ("The inference engine" (wpnews), "IO-aware attention": tiles combine
-// exactly through their softmax statistics).
-__global__ void __launch_bounds__(128) reduce_kernel(const int32_t* __restrict__ ctx_lens, int max_blocks,
-                                                     int num_heads, int part_tokens, int max_parts,
-                                                     const float* __restrict__ ws_o, const float* __restrict__ ws_ml,
-                                                     __half* __restrict__ out)
-{
-    const int h = blockIdx.x, r = blockIdx.y, d = threadIdx.x;
-    const int ctx = __ldg(ctx_lens + r);
-    if (ctx < 1 || ctx > max_blocks * kBlockSize) return;
-    const int nparts = (ctx + part_tokens - 1) / part_tokens;
-    if (nparts <= 1) return;
-    const int64_t base = ((int64_t)r * num_heads + h) * max_parts;
-    float M = -INFINITY;
-    for (int q = 0; q < nparts; ++q) M = fmaxf(M, __ldg(ws_ml + (base + q) * 2));
-    float L = 0.f, O = 0.f;
-    for (int q = 0; q < nparts; ++q) {
-        const float w = exp2f(__ldg(ws_ml + (base + q) * 2) - M);
-        L = fmaf(w, __ldg(ws_ml + (base + q) * 2 + 1), L);
-        O = fmaf(w, __ldg(ws_o + (base + q) * kHeadDim + d), O);
+    if (threadIdx.x == 0) {
+        a.ws_ml[slot * 2] = M;
+        a.ws_ml[slot * 2 + 1] = L;
     }
-    out[((int64_t)r * num_heads + h) * kHeadDim + d] = __float2half_rn(O / L);
+    // Publish the partial, then count it (one release by thread 0 after the
+    // CTA barrier covers every thread's writes); the last partition to
+    // arrive merges all of them in partition order.
+    __syncthreads();
+    unsigned int* flag = reinterpret_cast<unsigned int*>(smem + Lay::kFlag);
+    if (threadIdx.x == 0) *flag = atomic_add_acq_rel_gpu(a.counters + rh, 1u) == (unsigned int)(nparts - 1);
+    __syncthreads();
+    if (!*flag) return;
+    const int64_t base = rh * a.max_parts;
+    float* s_w = reinterpret_cast<float*>(smem);  // the rings are idle now
+    float* s_l = s_w + kMaxMergeParts;
+    for (int q = threadIdx.x; q < nparts; q += WARPS * 32) {
+        s_w[q] = __ldcg(a.ws_ml + (base + q) * 2);
+        s_l[q] = __ldcg(a.ws_ml + (base + q) * 2 + 1);
+    }
+    __syncthreads();
+    float Mx = -INFINITY;
+    for (int q = 0; q < nparts; ++q) Mx = fmaxf(Mx, s_w[q]);
+    __syncthreads();
+    for (int q = threadIdx.x; q < nparts; q += WARPS * 32) s_w[q] = exp2f(s_w[q] - Mx);
+    __syncthreads();
+    float Lt = 0.f;
+    for (int q = 0; q < nparts; ++q) Lt = fmaf(s_w[q], s_l[q], Lt);
+    for (int d = threadIdx.x; d < kHeadDim; d += WARPS * 32) {
+        float O = 0.f;
+#pragma unroll 8
+        for (int q = 0; q < nparts; ++q) O = fmaf(s_w[q], __ldcg(a.ws_o + (base + q) * kHeadDim + d), O);
+        a.out[rh * kHeadDim + d] = __float2half_rn(O / Lt);
+    }
+    if (threadIdx.x == 0) a.counters[rh] = 0u;
 }
 
 int decode_max_parts(int max_blocks, int partition_tokens)
@@ -368,19 +441,43 @@ int decode_max_parts(int max_blocks, int partition_tokens)
     return (int)((max_tokens + partition_tokens - 1) / partition_tokens);
 }
 
-size_t decode_workspace_bytes(int num_seqs, int num_heads, int max_blocks, int partition_tokens)
+namespace {
+struct WsLayout {
+    size_t o_bytes, ml_off, ctr_off, total;
+};
+
+WsLayout ws_layout(int num_seqs, int num_heads, int max_blocks, int partition_tokens)
 {
     const int64_t parts = decode_max_parts(max_blocks, partition_tokens);
-    if (parts <= 1) return 256;
     const int64_t slots = (int64_t)num_seqs * num_heads * parts;
-    size_t o = (size_t)slots * kHeadDim * sizeof(float);
-    o = (o + 255) & ~(size_t)255;
-    return o + (size_t)slots * 2 * sizeof(float) + 256;
+    WsLayout w;
+    w.o_bytes = ((size_t)slots * kHeadDim * sizeof(float) + 255) & ~(size_t)255;
+    w.ml_off = w.o_bytes;
+    w.ctr_off = (w.ml_off + (size_t)slots * 2 * sizeof(float) + 255) & ~(size_t)255;
+    w.total = w.ctr_off + (((size_t)num_seqs * num_heads * sizeof(unsigned int) + 255) & ~(size_t)255);
+    return w;
+}
+}  // namespace
+
+size_t decode_workspace_bytes(int num_seqs, int num_heads, int max_blocks, int partition_tokens)
+{
+    if (decode_max_parts(max_blocks, partition_tokens) <= 1) return 256;
+    return ws_layout(num_seqs, num_heads, max_blocks, partition_tokens).total;
+}
+
+cudaError_t clear_decode_counters(const PoolGeom& g, int num_seqs, int max_blocks, int partition_tokens, void* ws,
+                                  cudaStream_t stream)
+{
+    if (num_seqs == 0 || decode_max_parts(max_blocks, partition_tokens) <= 1) return cudaSuccess;
+    const WsLayout w = ws_layout(num_seqs, g.num_heads, max_blocks, partition_tokens);
+    return cudaMemsetAsync(static_cast<char*>(ws) + w.ctr_off, 0, (size_t)num_seqs * g.num_heads * sizeof(unsigned int),
+                           stream);
 }
 
 cudaError_t launch_decode(const PoolGeom& g, int layer, const void* q, const int32_t* tables, int max_blocks,
                           const int32_t* ctx_lens, int num_seqs, float scale, void* out, void* ws,
-                          int partition_tokens, unsigned int* status, cudaStream_t stream)
+                          int partition_tokens, const void* k_new, const void* v_new, const int64_t* slots,
+                          unsigned int* status, cudaStream_t stream)
 {
     if (num_seqs == 0) return cudaSuccess;
     using Lay = DecodeLayout<kDecodeWarps, kDecodeStages>;
@@ -394,7 +491,7 @@ cudaError_t launch_decode(const PoolGeom& g, int layer, const void* q, const int
         attr_set[dev] = true;
     }
     DecodeArgs a;
-    a.pool = g.base;
+    a.pool = const_cast<char*>(g.base);
     a.block_bytes = g.block_bytes;
     a.head_off = (int64_t)layer * g.layer_bytes;
     a.kv_bytes = g.kv_bytes;
@@ -408,17 +505,22 @@ cudaError_t launch_decode(const PoolGeom& g, int layer, const void* q, const int
     a.out = static_cast<__half*>(out);
     a.max_parts = decode_max_parts(max_blocks, partition_tokens);
     a.part_tokens = partition_tokens;
+    a.k_new = static_cast<const __half*>(k_new);
+    a.v_new = static_cast<const __half*>(v_new);
+    a.slots = slots;
+    a.append = k_new != nullptr;
     a.status = status;
-    const int64_t slots = (int64_t)num_seqs * g.num_heads * a.max_parts;
-    a.ws_o = static_cast<float*>(ws);
-    size_t o_bytes = ((size_t)slots * kHeadDim * sizeof(float) + 255) & ~(size_t)255;
-    a.ws_ml = reinterpret_cast<float*>(static_cast<char*>(ws) + o_bytes);
+    if (a.max_parts > 1) {
+        const WsLayout w = ws_layout(num_seqs, g.num_heads, max_blocks, partition_tokens);
+        a.ws_o = static_cast<float*>(ws);
+        a.ws_ml = reinterpret_cast<float*>(static_cast<char*>(ws) + w.ml_off);
+        a.counters = reinterpret_cast<unsigned int*>(static_cast<char*>(ws) + w.ctr_off);
+    } else {
+        a.ws_o = a.ws_ml = nullptr;
+        a.counters = nullptr;
+    }
     dim3 grid(a.max_parts, g.num_heads, num_seqs);
     decode_kernel<kDecodeWarps, kDecodeStages><<<grid, kDecodeWarps * 32, Lay::kBytes, stream>>>(a);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess || a.max_parts <= 1) return e;
-    reduce_kernel<<<dim3(g.num_heads, num_seqs), kHeadDim, 0, stream>>>(
-        ctx_lens, max_blocks, g.num_heads, partition_tokens, a.max_parts, a.ws_o, a.ws_ml, a.out);
     return cudaGetLastError();
 }
 
