@@ -11,20 +11,21 @@
 // are already in the pool (kv_append runs first), so keys come only from
 // the pool, 128 at a time (8 blocks).
 //
-// Warp roles (320 threads):
-//   warp 0      TMA producer: K and V tiles of 8 blocks, two 64-dim halves
-//               each (2 KB boxes), into a 2-stage ring per operand.
-//   warp 1      TMEM owner and MMA issuer (one elected lane):
-//               S_j = Q K_j^T into S buffer j%2, then O += P_j V_j into the
-//               single O accumulator; completion signalled by tcgen05.commit.
-//   warps 2..9  softmax: two threads per query row r (TMEM lane r), one per
-//               64-key half. Per tile each loads the S row once, releases the
-//               S buffer, and writes its half of P = 2^(s*scale*log2e - m) in
-//               FP16 to P buffer j%2. The running
-//               max m is only raised when the tile's max exceeds it by more
-//               than 8 (a factor 256, far inside FP16/FP32 range); then the
-//               row's O in TMEM and its sum are rescaled once the previous
-//               P V product has landed. The result is exact up to rounding.
+// Warp roles (352 threads):
+//   warps 0, 10  TMA producers: K (warp 0) and V (warp 10) tiles of 8 blocks,
+//                two 64-dim halves each (2 KB boxes), into 3-stage rings.
+//   warp 1       TMEM owner and MMA issuer (one elected lane): S_j = Q K_j^T
+//                into S buffer j%2 (A and B from shared memory), then
+//                O += P_j V_j with P read from tensor memory; completion is
+//                signalled by tcgen05.commit.
+//   warps 2..9   softmax: two threads per query row r (TMEM lane r), one per
+//                64-key half. Per tile each loads the S row once, releases the
+//                S buffer, and writes its half of P = 2^(s*scale*log2e - m) in
+//                FP16 to P buffer j%2 in tensor memory. The running max m is
+//                only raised when the tile's max exceeds it by more than 8 (a
+//                factor 256, far inside FP16/FP32 range); then the row's O in
+//                TMEM and its sum are rescaled once the previous P V product
+//                has landed. The result is exact up to rounding.
 // Shared-memory operands use the 128-byte swizzle: rows of 128 B (64 halves),
 // two slabs per 128-wide operand, 8-row groups 1,024 B apart.
 #include <cuda.h>
@@ -73,23 +74,24 @@ bool encode_kv_tmap(const PoolGeom& g, TensorMap128* out, std::string* err)
     return true;
 }
 
+
 namespace {
 
 constexpr int kRows = 128;     // query rows per CTA (MMA M)
 constexpr int kKeys = 128;     // keys per tile (8 blocks)
-constexpr int kThreads = 320;  // producer, MMA, 8 softmax warps
+constexpr int kThreads = 352;  // K producer, MMA, 8 softmax warps, V producer
+constexpr int kStages = 3;     // K and V ring depth
 constexpr int kOperandBytes = kRows * kHeadDim * 2;  // 32 KB: one 128 x 128 FP16 operand
 constexpr int kSlabBytes = kOperandBytes / 2;        // 16 KB: 128 rows x 64 halves
 constexpr float kRescaleThreshold = 8.f;             // log2 of the largest un-rescaled P (256)
 
 // shared-memory map (offsets from a 1,024-byte aligned base)
 constexpr int kSmQ = 0;
-constexpr int kSmK = kSmQ + kOperandBytes;       // 2 stages
-constexpr int kSmV = kSmK + 2 * kOperandBytes;   // 2 stages
-constexpr int kSmP = kSmV + 2 * kOperandBytes;   // 2 buffers
-constexpr int kSmBars = kSmP + 2 * kOperandBytes;
-enum Bar { K_FULL = 0, V_FULL = 2, K_EMPTY = 4, V_EMPTY = 6, S_FULL = 8, S_FREE = 10, P_FULL = 12, P_EMPTY = 14,
-           MMA_DONE = 16, L_EX = 17, NUM_BARS = 18 };
+constexpr int kSmK = kSmQ + kOperandBytes;             // kStages stages
+constexpr int kSmV = kSmK + kStages * kOperandBytes;   // kStages stages
+constexpr int kSmBars = kSmV + kStages * kOperandBytes;
+enum Bar { K_FULL = 0, V_FULL = 3, K_EMPTY = 6, V_EMPTY = 9, S_FULL = 12, S_FREE = 14, P_FULL = 16, P_EMPTY = 18,
+           MMA_DONE = 20, L_EX = 21, NUM_BARS = 22 };
 constexpr int kSoftmaxThreads = 256;
 constexpr int kSmTmemSlot = kSmBars + NUM_BARS * 8;
 constexpr int kSmAbort = kSmTmemSlot + 4;
@@ -97,10 +99,12 @@ constexpr int kSmLx = kSmAbort + 12;             // [2 halves][128 rows] partial
 constexpr int kSmBytes = kSmLx + 2 * kRows * 4;
 constexpr int kSmAlloc = kSmBytes + 1024;        // slack to align the base
 
-// TMEM columns: two S buffers, then the O accumulator, 128 fp32 columns each.
+// TMEM columns: two S buffers and the O accumulator (128 fp32 columns each),
+// then two P buffers (128 FP16 keys per row = 64 columns each).
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;
 constexpr uint32_t kColO = 256;
+constexpr uint32_t kColP = 384;
 
 // Instruction descriptors, kind::f16: D = F32 (bit 4), A = B = F16,
 // N >> 3 at bit 17, M >> 4 at bit 24; bit 16 makes B MN-major.
@@ -139,6 +143,39 @@ __device__ __forceinline__ bool flag_wait(uint32_t bar, uint32_t parity, volatil
 }
 
 __device__ __forceinline__ uint32_t bar_addr(uint32_t bars, int idx) { return bars + 8u * (uint32_t)idx; }
+
+// One producer warp: the K (kv = 0) or V (kv = 1) tiles of every key tile,
+// 8 blocks x two 64-dim halves, into a kStages-deep ring.
+__device__ __forceinline__ void produce(const CUtensorMap* tmap, const PrefillArgs& a, const int32_t* trow, int nkt,
+                                        int nblk, int kv, int h, uint32_t ring, uint32_t full0, uint32_t empty0,
+                                        volatile int* abort)
+{
+    const int lane = threadIdx.x & 31;
+    if (lane == 0) prefetch_tmap(tmap);
+    int issued = 0;
+    for (int j = 0; j < nkt; ++j) {
+        const int st = j % kStages;
+        const uint32_t ph = (uint32_t)(j / kStages) & 1u;
+        const int nb = min(8, nblk - 8 * j);
+        const int id = lane < nb ? __ldg(trow + 8 * j + lane) : 0;
+        if (j >= kStages && !flag_wait(empty0 + 8 * st, ph ^ 1u, abort, a.status)) break;
+        if (lane == 0) mbar_arrive_expect_tx(full0 + 8 * st, nb * kTileBytes);
+        for (int b = 0; b < nb; ++b) {
+            const int idb = __shfl_sync(0xffffffffu, id, b);
+            if (lane == 0)
+                for (int half = 0; half < 2; ++half)
+                    tma_load_5d(ring + st * kOperandBytes + half * kSlabBytes + b * 2048, tmap, half * 64, 0,
+                                kv * a.num_heads + h, a.layer, idb, full0 + 8 * st);
+        }
+        issued = j + 1;
+    }
+    __syncwarp();
+    if (*abort && lane == 0) {
+        // let loads that nobody consumed land before the CTA exits
+        for (int j = (issued > kStages ? issued - kStages : 0); j < issued; ++j)
+            mbar_wait(full0 + 8 * (j % kStages), (uint32_t)(j / kStages) & 1u);
+    }
+}
 
 __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ CUtensorMap tmap,
                                                                const PrefillArgs a)
@@ -189,11 +226,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     const uint32_t bars = sb + kSmBars;
     volatile int* abort = reinterpret_cast<volatile int*>(smem + kSmAbort);
     if (threadIdx.x == 0) {
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kStages; ++i) {
             mbar_init(bar_addr(bars, K_FULL + i), 1);
             mbar_init(bar_addr(bars, V_FULL + i), 1);
             mbar_init(bar_addr(bars, K_EMPTY + i), 1);
             mbar_init(bar_addr(bars, V_EMPTY + i), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
             mbar_init(bar_addr(bars, S_FULL + i), 1);
             mbar_init(bar_addr(bars, S_FREE + i), kSoftmaxThreads);
             mbar_init(bar_addr(bars, P_FULL + i), kSoftmaxThreads);
@@ -213,76 +252,43 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kSmTmemSlot);
 
-    if (warp == 0) {
-        // ================================================= TMA producer
-        if (lane == 0) prefetch_tmap(&tmap);
-        int issued = 0;
-        for (int j = 0; j < nkt; ++j) {
-            const int st = j & 1;
-            const uint32_t ph = (uint32_t)(j >> 1) & 1u;
-            const int nb = min(8, nblk - 8 * j);
-            const int id = lane < nb ? __ldg(trow + 8 * j + lane) : 0;
-            if (j >= 2 && !flag_wait(bar_addr(bars, K_EMPTY + st), ph ^ 1u, abort, a.status)) break;
-            if (lane == 0) mbar_arrive_expect_tx(bar_addr(bars, K_FULL + st), nb * kTileBytes);
-            for (int b = 0; b < nb; ++b) {
-                const int idb = __shfl_sync(0xffffffffu, id, b);
-                if (lane == 0)
-                    for (int half = 0; half < 2; ++half)
-                        tma_load_5d(sb + kSmK + st * kOperandBytes + half * kSlabBytes + b * 2048, &tmap, half * 64, 0,
-                                    h, a.layer, idb, bar_addr(bars, K_FULL + st));
-            }
-            if (j >= 2 && !flag_wait(bar_addr(bars, V_EMPTY + st), ph ^ 1u, abort, a.status)) break;
-            if (lane == 0) mbar_arrive_expect_tx(bar_addr(bars, V_FULL + st), nb * kTileBytes);
-            for (int b = 0; b < nb; ++b) {
-                const int idb = __shfl_sync(0xffffffffu, id, b);
-                if (lane == 0)
-                    for (int half = 0; half < 2; ++half)
-                        tma_load_5d(sb + kSmV + st * kOperandBytes + half * kSlabBytes + b * 2048, &tmap, half * 64, 0,
-                                    a.num_heads + h, a.layer, idb, bar_addr(bars, V_FULL + st));
-            }
-            issued = j + 1;
-        }
-        __syncwarp();
-        if (*abort && lane == 0) {
-            // let this warp's loads that nobody consumed land before the CTA exits
-            for (int j = (issued > 2 ? issued - 2 : 0); j < issued; ++j) {
-                mbar_wait(bar_addr(bars, K_FULL + (j & 1)), (uint32_t)(j >> 1) & 1u);
-                mbar_wait(bar_addr(bars, V_FULL + (j & 1)), (uint32_t)(j >> 1) & 1u);
-            }
-        }
+    if (warp == 0 || warp == 10) {
+        // ================================================= TMA producers (K: warp 0, V: warp 10)
+        const int kv = warp == 0 ? 0 : 1;
+        produce(&tmap, a, trow, nkt, nblk, kv, h, sb + (kv ? kSmV : kSmK), bar_addr(bars, kv ? V_FULL : K_FULL),
+                bar_addr(bars, kv ? V_EMPTY : K_EMPTY), abort);
     } else if (warp == 1) {
         // ================================================= MMA issuer
         for (int j = 0; j <= nkt; ++j) {
             if (j < nkt) {
-                const int st = j & 1;
-                const uint32_t ph = (uint32_t)(j >> 1) & 1u;
-                if (!flag_wait(bar_addr(bars, K_FULL + st), ph, abort, a.status)) break;
-                if (j >= 2 && !flag_wait(bar_addr(bars, S_FREE + st), ph ^ 1u, abort, a.status)) break;
+                const int ks = j % kStages, st = j & 1;
+                if (!flag_wait(bar_addr(bars, K_FULL + ks), (uint32_t)(j / kStages) & 1u, abort, a.status)) break;
+                if (j >= 2 && !flag_wait(bar_addr(bars, S_FREE + st), (uint32_t)((j - 2) >> 1) & 1u, abort, a.status))
+                    break;
                 tc_fence_after();
                 if (lane == 0) {
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk) {
                         const uint32_t off = (kk >> 2) * kSlabBytes + (kk & 3) * 32;
                         tc_mma_f16(tmem + kColS + st * 128, sw128_desc(sb + kSmQ + off, 16, 1024),
-                                   sw128_desc(sb + kSmK + st * kOperandBytes + off, 16, 1024), kIdescS, kk > 0);
+                                   sw128_desc(sb + kSmK + ks * kOperandBytes + off, 16, 1024), kIdescS, kk > 0);
                     }
                     tc_commit(bar_addr(bars, S_FULL + st));
-                    tc_commit(bar_addr(bars, K_EMPTY + st));
+                    tc_commit(bar_addr(bars, K_EMPTY + ks));
                 }
                 __syncwarp();
             }
             if (j >= 1) {
-                const int i = j - 1, st = i & 1;
-                const uint32_t ph = (uint32_t)(i >> 1) & 1u;
-                if (!flag_wait(bar_addr(bars, P_FULL + st), ph, abort, a.status)) break;
-                if (!flag_wait(bar_addr(bars, V_FULL + st), ph, abort, a.status)) break;
+                const int i = j - 1, vs = i % kStages, st = i & 1;
+                if (!flag_wait(bar_addr(bars, P_FULL + st), (uint32_t)(i >> 1) & 1u, abort, a.status)) break;
+                if (!flag_wait(bar_addr(bars, V_FULL + vs), (uint32_t)(i / kStages) & 1u, abort, a.status)) break;
                 if (i == nkt - 1) {
                     // keys past the last row's position may hold anything (even NaN); zero their V rows so
                     // that P = 0 times V stays 0 in the tensor core
                     const int first = pos_max + 1 - i * kKeys;
                     for (int c = first * 8 + lane; c < kKeys * 8; c += 32) {
                         const int r = c >> 3, ch = c & 7;
-                        const uint32_t base = sb + kSmV + st * kOperandBytes + r * 128 + ch * 16;
+                        const uint32_t base = sb + kSmV + vs * kOperandBytes + r * 128 + ch * 16;
                         st_shared_v4(base, make_uint4(0, 0, 0, 0));
                         st_shared_v4(base + kSlabBytes, make_uint4(0, 0, 0, 0));
                     }
@@ -292,14 +298,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                 tc_fence_after();
                 if (lane == 0) {
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        const uint32_t aoff = (kk >> 2) * kSlabBytes + (kk & 3) * 32;
-                        tc_mma_f16(tmem + kColO, sw128_desc(sb + kSmP + st * kOperandBytes + aoff, 16, 1024),
-                                   sw128_desc(sb + kSmV + st * kOperandBytes + kk * 2048, kSlabBytes, 1024), kIdescPV,
-                                   (i > 0 || kk > 0) ? 1u : 0u);
-                    }
+                    for (int kk = 0; kk < 8; ++kk)
+                        tc_mma_f16_ts(tmem + kColO, tmem + kColP + st * 64 + kk * 8,
+                                      sw128_desc(sb + kSmV + vs * kOperandBytes + kk * 2048, kSlabBytes, 1024),
+                                      kIdescPV, (i > 0 || kk > 0) ? 1u : 0u);
                     tc_commit(bar_addr(bars, P_EMPTY + st));
-                    tc_commit(bar_addr(bars, V_EMPTY + st));
+                    tc_commit(bar_addr(bars, V_EMPTY + vs));
                 }
                 __syncwarp();
             }
@@ -310,11 +314,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         }
         __syncwarp();
     } else {
-        // ================================================= softmax (8 warps)
+        // ================================================= softmax (warps 2..9)
         // Warps w and w + 4 share TMEM lane quarter w % 4, i.e. the same 32
         // rows. Both read the whole S row (for the row max); each then
-        // exponentiates one 64-key half (P slab hv) and owns the matching
-        // 64 columns of O.
+        // exponentiates one 64-key half, writes that half of P (FP16, two per
+        // column) to TMEM, and owns the matching 64 columns of O.
         const int qtr = warp & 3;
         const int hv = (warp - 2) >> 2;
         const int row = qtr * 32 + lane;
@@ -381,24 +385,18 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             float ls[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) ls[u] = 0.f;
-            const uint32_t prow = sb + kSmP + st * kOperandBytes + hv * kSlabBytes + row * 128;
+            uint32_t packed[32];
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {  // 8 chunks of 8 keys of this half
-                uint32_t packed[4];
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int e = c * 8 + 2 * u;
-                    const float pa = ex2(fmaf(__uint_as_float(sr[e]), a.scale_log2, -m_used));
-                    const float pb = ex2(fmaf(__uint_as_float(sr[e + 1]), a.scale_log2, -m_used));
-                    ls[2 * u] += pa;
-                    ls[2 * u + 1] += pb;
-                    const __half2 hp = __floats2half2_rn(pa, pb);
-                    packed[u] = *reinterpret_cast<const uint32_t*>(&hp);
-                }
-                st_shared_v4(prow + ((c ^ (row & 7)) << 4), make_uint4(packed[0], packed[1], packed[2], packed[3]));
+            for (int e = 0; e < 64; e += 2) {
+                const float pa = ex2(fmaf(__uint_as_float(sr[e]), a.scale_log2, -m_used));
+                const float pb = ex2(fmaf(__uint_as_float(sr[e + 1]), a.scale_log2, -m_used));
+                ls[e & 7] += pa;
+                ls[(e + 1) & 7] += pb;
+                const __half2 hp = __floats2half2_rn(pa, pb);
+                packed[e >> 1] = *reinterpret_cast<const uint32_t*>(&hp);
             }
+            tc_st32(tl + kColP + st * 64 + hv * 32, packed);
             l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
-            fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(bar_addr(bars, P_FULL + st));
         }
