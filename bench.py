@@ -299,9 +299,9 @@ def run_ours(args):
     wspace = torch.empty(max(max(s.ws_bytes for s in steps), 256), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    def step():
+    def step(strm=None):
         for s in steps:
-            pool.step(s.desc, wspace, stream)
+            pool.step(s.desc, wspace, strm if strm is not None else stream)
 
     def check_status():
         st, flags = pool.get_status(stream)
@@ -312,6 +312,20 @@ def run_ours(args):
         step()
     torch.cuda.synchronize(dev)
     check_status()
+
+    # The timed step is a CUDA graph of the whole iteration (all layers), as a serving loop would replay it.
+    graph = None
+    if not args.no_graph:
+        graph = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(stream)
+        with torch.cuda.graph(graph, stream=cap, capture_error_mode="thread_local"):
+            step(torch.cuda.current_stream(dev))
+        torch.cuda.synchronize(dev)
+        for _ in range(2):
+            graph.replay()
+        torch.cuda.synchronize(dev)
+        check_status()
 
     has_prefill = any(s.max_q for s in steps)
     has_decode = any(s.B for s in steps)
@@ -336,7 +350,10 @@ def run_ours(args):
     e0, e1 = ev(), ev()
     e0.record(stream)
     for _ in range(args.steps):
-        step()
+        if graph is not None:
+            graph.replay()
+        else:
+            step()
     e1.record(stream)
     torch.cuda.synchronize(dev)
     if ws > 1:
@@ -464,7 +481,8 @@ def run_ours(args):
                    "pool_blocks": wl0.num_blocks, "kv_bytes_per_step": kv_step,
                    "prefill_flops_per_step": flops_step, "seed": wl0.seed,
                    "max_context": int(max(int(s.wl.ctx_lens.max()) for s in steps)),
-                   "l2": "inputs larger than L2 (every step reads the whole KV context of all layers)"},
+                   "l2": "inputs larger than L2 (every step reads the whole KV context of all layers)",
+                   "cuda_graph": graph is not None},
         "clocks": clocks,
         "gpu_launches": launches_step * K,
         "roofline": rooflines[dominant],
@@ -587,6 +605,7 @@ def main():
                     choices=["average_decode", "long_decode", "shared_prefix_decode", "mixed_prefill"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true", help="launch each step directly instead of replaying a CUDA graph")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--layers", type=int, default=0,
                     help="run only this many layers (smaller pool; per-layer work unchanged; for profiling)")

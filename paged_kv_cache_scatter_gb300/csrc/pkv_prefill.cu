@@ -11,21 +11,28 @@
 // are already in the pool (kv_append runs first), so keys come only from
 // the pool, 128 at a time (8 blocks).
 //
-// Warp roles (352 threads):
-//   warps 0, 10  TMA producers: K (warp 0) and V (warp 10) tiles of 8 blocks,
-//                two 64-dim halves each (2 KB boxes), into 3-stage rings.
-//   warp 1       TMEM owner and MMA issuer (one elected lane): S_j = Q K_j^T
-//                into S buffer j%2 (A and B from shared memory), then
-//                O += P_j V_j with P read from tensor memory; completion is
-//                signalled by tcgen05.commit.
-//   warps 2..9   softmax: two threads per query row r (TMEM lane r), one per
-//                64-key half. Per tile each loads the S row once, releases the
-//                S buffer, and writes its half of P = 2^(s*scale*log2e - m) in
-//                FP16 to P buffer j%2 in tensor memory. The running max m is
-//                only raised when the tile's max exceeds it by more than 8 (a
-//                factor 256, far inside FP16/FP32 range); then the row's O in
-//                TMEM and its sum are rescaled once the previous P V product
-//                has landed. The result is exact up to rounding.
+// Two independent pipelines per CTA split the key range: pipe 0 takes the
+// first half of the 64-key tiles, pipe 1 the rest (the diagonal tiles), so
+// the tensor core works on one pipe's MMAs while the other pipe's softmax
+// runs. Each pipe has its own K/V rings, S/P and O in TMEM, MMA issuer and
+// softmax warps; at the end the two partial results merge exactly through
+// their softmax statistics.
+//
+// Warp roles (448 threads):
+//   warps 0-3    TMA producers, one per (pipe, K|V): 64-key tiles = 4 blocks
+//                x two 64-dim halves (2 KB boxes), into 3-stage rings.
+//   warps 4, 5   MMA issuers of pipe 0 / 1 (one elected lane each; warp 4
+//                also owns the TMEM allocation): S_j = Q K_j^T into S buffer
+//                j%2 (A and B from shared memory), then O += P_j V_j with P
+//                read from tensor memory; completion by tcgen05.commit.
+//   warps 6-9,   softmax of pipe 0 / 1: thread r owns query row r (TMEM lane
+//   10-13        r). Per tile it loads its 64 S values, writes
+//                P = 2^(s*scale*log2e - m) in FP16 over the first half of the
+//                same S buffer, and keeps the running sum. The running max m
+//                is only raised when the tile's max exceeds it by more than 8
+//                (a factor 256, far inside FP16/FP32 range); then the row's O
+//                and sum are rescaled once the previous P V product has
+//                landed. The result is exact up to rounding.
 // Shared-memory operands use the 128-byte swizzle: rows of 128 B (64 halves),
 // two slabs per 128-wide operand, 8-row groups 1,024 B apart.
 #include <cuda.h>
@@ -78,38 +85,42 @@ bool encode_kv_tmap(const PoolGeom& g, TensorMap128* out, std::string* err)
 namespace {
 
 constexpr int kRows = 128;     // query rows per CTA (MMA M)
-constexpr int kKeys = 128;     // keys per tile (8 blocks)
-constexpr int kThreads = 352;  // K producer, MMA, 8 softmax warps, V producer
-constexpr int kStages = 3;     // K and V ring depth
-constexpr int kOperandBytes = kRows * kHeadDim * 2;  // 32 KB: one 128 x 128 FP16 operand
-constexpr int kSlabBytes = kOperandBytes / 2;        // 16 KB: 128 rows x 64 halves
+constexpr int kKeys = 64;      // keys per tile (4 blocks)
+constexpr int kPipes = 2;      // independent key-range pipelines per CTA
+constexpr int kStages = 3;     // K and V ring depth per pipeline
+constexpr int kThreads = 448;  // 4 producers, 2 MMA issuers, 2 x 4 softmax warps
+constexpr int kQBytes = kRows * kHeadDim * 2;        // 32 KB
+constexpr int kQSlab = kQBytes / 2;                  // 16 KB: 128 rows x 64 halves
+constexpr int kTileOpBytes = kKeys * kHeadDim * 2;   // 16 KB: one 64-key K or V tile
+constexpr int kTileSlab = kTileOpBytes / 2;          // 8 KB: 64 rows x 64 halves
 constexpr float kRescaleThreshold = 8.f;             // log2 of the largest un-rescaled P (256)
 
 // shared-memory map (offsets from a 1,024-byte aligned base)
 constexpr int kSmQ = 0;
-constexpr int kSmK = kSmQ + kOperandBytes;             // kStages stages
-constexpr int kSmV = kSmK + kStages * kOperandBytes;   // kStages stages
-constexpr int kSmBars = kSmV + kStages * kOperandBytes;
-enum Bar { K_FULL = 0, V_FULL = 3, K_EMPTY = 6, V_EMPTY = 9, S_FULL = 12, S_FREE = 14, P_FULL = 16, P_EMPTY = 18,
-           MMA_DONE = 20, L_EX = 21, NUM_BARS = 22 };
-constexpr int kSoftmaxThreads = 256;
-constexpr int kSmTmemSlot = kSmBars + NUM_BARS * 8;
+constexpr int kSmRing = kQBytes;                            // [pipe][K,V][stage] tiles
+constexpr int kSmBars = kSmRing + kPipes * 2 * kStages * kTileOpBytes;
+enum Bar { K_FULL = 0, V_FULL = 3, K_EMPTY = 6, V_EMPTY = 9, S_FULL = 12, P_FULL = 14, PV_DONE = 16, MMA_DONE = 18,
+           BARS_PER_PIPE = 19 };
+constexpr int kBarLx = kPipes * BARS_PER_PIPE;              // the final exchange between the pipes
+constexpr int kNumBars = kBarLx + 1;
+constexpr int kSoftmaxThreads = 128;                        // per pipe
+constexpr int kSmTmemSlot = kSmBars + kNumBars * 8;
 constexpr int kSmAbort = kSmTmemSlot + 4;
-constexpr int kSmLx = kSmAbort + 12;             // [2 halves][128 rows] partial row sums
-constexpr int kSmBytes = kSmLx + 2 * kRows * 4;
-constexpr int kSmAlloc = kSmBytes + 1024;        // slack to align the base
+constexpr int kSmBytes = kSmAbort + 12;
+constexpr int kSmAlloc = kSmBytes + 1024;                   // slack to align the base
 
-// TMEM columns: two S buffers and the O accumulator (128 fp32 columns each),
-// then two P buffers (128 FP16 keys per row = 64 columns each).
+// TMEM columns per pipe (base pipe * 256): two S buffers of 64 fp32 columns
+// (P, FP16, overwrites the first 32 columns of its S buffer), then O (128).
 constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kPipeCols = 256;
 constexpr uint32_t kColS = 0;
-constexpr uint32_t kColO = 256;
-constexpr uint32_t kColP = 384;
+constexpr uint32_t kColO = 128;
 
 // Instruction descriptors, kind::f16: D = F32 (bit 4), A = B = F16,
 // N >> 3 at bit 17, M >> 4 at bit 24; bit 16 makes B MN-major.
 constexpr uint32_t kIdescS = (1u << 4) | ((uint32_t)(kKeys >> 3) << 17) | ((uint32_t)(kRows >> 4) << 24);
-constexpr uint32_t kIdescPV = kIdescS | (1u << 16);
+constexpr uint32_t kIdescPV = (1u << 4) | ((uint32_t)(kHeadDim >> 3) << 17) | ((uint32_t)(kRows >> 4) << 24) |
+                              (1u << 16);
 
 struct PrefillArgs {
     const __half* q;         // [T][H][128], token index from q_start
@@ -132,6 +143,7 @@ struct PrefillArgs {
 __device__ __forceinline__ bool flag_wait(uint32_t bar, uint32_t parity, volatile int* abort, unsigned int* status)
 {
     const int lane = threadIdx.x & 31;
+    if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;  // fast path
     int stop = lane == 0 ? *abort : 0;
     if (__shfl_sync(0xffffffffu, stop, 0)) return false;
     const bool ok = __all_sync(0xffffffffu, mbar_wait(bar, parity));
@@ -142,39 +154,9 @@ __device__ __forceinline__ bool flag_wait(uint32_t bar, uint32_t parity, volatil
     return ok;
 }
 
-__device__ __forceinline__ uint32_t bar_addr(uint32_t bars, int idx) { return bars + 8u * (uint32_t)idx; }
-
-// One producer warp: the K (kv = 0) or V (kv = 1) tiles of every key tile,
-// 8 blocks x two 64-dim halves, into a kStages-deep ring.
-__device__ __forceinline__ void produce(const CUtensorMap* tmap, const PrefillArgs& a, const int32_t* trow, int nkt,
-                                        int nblk, int kv, int h, uint32_t ring, uint32_t full0, uint32_t empty0,
-                                        volatile int* abort)
+__device__ __forceinline__ uint32_t bar_addr(uint32_t bars, int pipe, int idx)
 {
-    const int lane = threadIdx.x & 31;
-    if (lane == 0) prefetch_tmap(tmap);
-    int issued = 0;
-    for (int j = 0; j < nkt; ++j) {
-        const int st = j % kStages;
-        const uint32_t ph = (uint32_t)(j / kStages) & 1u;
-        const int nb = min(8, nblk - 8 * j);
-        const int id = lane < nb ? __ldg(trow + 8 * j + lane) : 0;
-        if (j >= kStages && !flag_wait(empty0 + 8 * st, ph ^ 1u, abort, a.status)) break;
-        if (lane == 0) mbar_arrive_expect_tx(full0 + 8 * st, nb * kTileBytes);
-        for (int b = 0; b < nb; ++b) {
-            const int idb = __shfl_sync(0xffffffffu, id, b);
-            if (lane == 0)
-                for (int half = 0; half < 2; ++half)
-                    tma_load_5d(ring + st * kOperandBytes + half * kSlabBytes + b * 2048, tmap, half * 64, 0,
-                                kv * a.num_heads + h, a.layer, idb, full0 + 8 * st);
-        }
-        issued = j + 1;
-    }
-    __syncwarp();
-    if (*abort && lane == 0) {
-        // let loads that nobody consumed land before the CTA exits
-        for (int j = (issued > kStages ? issued - kStages : 0); j < issued; ++j)
-            mbar_wait(full0 + 8 * (j % kStages), (uint32_t)(j / kStages) & 1u);
-    }
+    return bars + 8u * (uint32_t)(pipe * BARS_PER_PIPE + idx);
 }
 
 __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ CUtensorMap tmap,
@@ -199,8 +181,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     const int rows = min(kRows, qlen - qt * kRows);
     const int p0 = ctx - qlen + qt * kRows;  // position of row 0
     const int pos_max = p0 + rows - 1;
-    const int nkt = pos_max / kKeys + 1;
+    const int nkt = pos_max / kKeys + 1;     // 64-key tiles
     const int nblk = pos_max / kBlockSize + 1;
+    // pipe 0 takes key tiles [0, n0), pipe 1 takes [n0, nkt) (the diagonal ones)
+    const int n0 = nkt / 2;
     const int32_t* trow = a.tables + (int64_t)s * a.max_blocks;
     bool bad = false;
     for (int b = threadIdx.x; b < nblk; b += kThreads) {
@@ -219,31 +203,32 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         if (r < rows)
             v = __ldg(reinterpret_cast<const uint4*>(a.q + ((int64_t)(q0 + qt * kRows + r) * a.num_heads + h) * kHeadDim) +
                       ch);
-        st_shared_v4(sb + kSmQ + (ch >> 3) * kSlabBytes + r * 128 + (((ch & 7) ^ (r & 7)) << 4), v);
+        st_shared_v4(sb + kSmQ + (ch >> 3) * kQSlab + r * 128 + (((ch & 7) ^ (r & 7)) << 4), v);
     }
     fence_proxy_async_smem();
 
     const uint32_t bars = sb + kSmBars;
     volatile int* abort = reinterpret_cast<volatile int*>(smem + kSmAbort);
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kStages; ++i) {
-            mbar_init(bar_addr(bars, K_FULL + i), 1);
-            mbar_init(bar_addr(bars, V_FULL + i), 1);
-            mbar_init(bar_addr(bars, K_EMPTY + i), 1);
-            mbar_init(bar_addr(bars, V_EMPTY + i), 1);
+        for (int p = 0; p < kPipes; ++p) {
+            for (int i = 0; i < kStages; ++i) {
+                mbar_init(bar_addr(bars, p, K_FULL + i), 1);
+                mbar_init(bar_addr(bars, p, V_FULL + i), 1);
+                mbar_init(bar_addr(bars, p, K_EMPTY + i), 1);
+                mbar_init(bar_addr(bars, p, V_EMPTY + i), 1);
+            }
+            for (int i = 0; i < 2; ++i) {
+                mbar_init(bar_addr(bars, p, S_FULL + i), 1);
+                mbar_init(bar_addr(bars, p, P_FULL + i), kSoftmaxThreads);
+                mbar_init(bar_addr(bars, p, PV_DONE + i), 1);
+            }
+            mbar_init(bar_addr(bars, p, MMA_DONE), 1);
         }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(bar_addr(bars, S_FULL + i), 1);
-            mbar_init(bar_addr(bars, S_FREE + i), kSoftmaxThreads);
-            mbar_init(bar_addr(bars, P_FULL + i), kSoftmaxThreads);
-            mbar_init(bar_addr(bars, P_EMPTY + i), 1);
-        }
-        mbar_init(bar_addr(bars, MMA_DONE), 1);
-        mbar_init(bar_addr(bars, L_EX), kSoftmaxThreads);
+        mbar_init(bars + 8u * kBarLx, kPipes * kSoftmaxThreads);
         *abort = 0;
         fence_mbar_init();
     }
-    if (warp == 1) {
+    if (warp == 4) {
         tmem_alloc(sb + kSmTmemSlot, kTmemCols);
         tmem_relinquish();
     }
@@ -252,45 +237,81 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kSmTmemSlot);
 
-    if (warp == 0 || warp == 10) {
-        // ================================================= TMA producers (K: warp 0, V: warp 10)
-        const int kv = warp == 0 ? 0 : 1;
-        produce(&tmap, a, trow, nkt, nblk, kv, h, sb + (kv ? kSmV : kSmK), bar_addr(bars, kv ? V_FULL : K_FULL),
-                bar_addr(bars, kv ? V_EMPTY : K_EMPTY), abort);
-    } else if (warp == 1) {
-        // ================================================= MMA issuer
-        for (int j = 0; j <= nkt; ++j) {
-            if (j < nkt) {
-                const int ks = j % kStages, st = j & 1;
-                if (!flag_wait(bar_addr(bars, K_FULL + ks), (uint32_t)(j / kStages) & 1u, abort, a.status)) break;
-                if (j >= 2 && !flag_wait(bar_addr(bars, S_FREE + st), (uint32_t)((j - 2) >> 1) & 1u, abort, a.status))
+    if (warp < 4) {
+        // ================================================= TMA producers: (pipe, K|V) per warp
+        const int pipe = warp >> 1, kv = warp & 1;
+        const int base = pipe ? n0 : 0, n = pipe ? nkt - n0 : n0;
+        const uint32_t ring = sb + kSmRing + (pipe * 2 + kv) * kStages * kTileOpBytes;
+        const uint32_t full0 = bar_addr(bars, pipe, kv ? V_FULL : K_FULL);
+        const uint32_t empty0 = bar_addr(bars, pipe, kv ? V_EMPTY : K_EMPTY);
+        if (lane == 0) prefetch_tmap(&tmap);
+        int issued = 0;
+        for (int j = 0; j < n; ++j) {
+            const int st = j % kStages;
+            const uint32_t ph = (uint32_t)(j / kStages) & 1u;
+            const int g = base + j;
+            const int nb = min(4, nblk - 4 * g);
+            const int id = lane < nb ? __ldg(trow + 4 * g + lane) : 0;
+            if (j >= kStages && !flag_wait(empty0 + 8 * st, ph ^ 1u, abort, a.status)) break;
+            if (lane == 0) mbar_arrive_expect_tx(full0 + 8 * st, nb * kTileBytes);
+            for (int b = 0; b < nb; ++b) {
+                const int idb = __shfl_sync(0xffffffffu, id, b);
+                if (lane == 0)
+                    for (int half = 0; half < 2; ++half)
+                        tma_load_5d(ring + st * kTileOpBytes + half * kTileSlab + b * 2048, &tmap, half * 64, 0,
+                                    kv * a.num_heads + h, a.layer, idb, full0 + 8 * st);
+            }
+            issued = j + 1;
+        }
+        __syncwarp();
+        if (*abort && lane == 0)
+            for (int j = (issued > kStages ? issued - kStages : 0); j < issued; ++j)
+                mbar_wait(full0 + 8 * (j % kStages), (uint32_t)(j / kStages) & 1u);
+    } else if (warp < 6) {
+        // ================================================= MMA issuers, one per pipe
+        const int pipe = warp - 4;
+        const int base = pipe ? n0 : 0, n = pipe ? nkt - n0 : n0;
+        const uint32_t tp = tmem + pipe * kPipeCols;
+        const uint32_t kring = sb + kSmRing + (pipe * 2) * kStages * kTileOpBytes;
+        const uint32_t vring = kring + kStages * kTileOpBytes;
+        for (int j = 0; j <= n; ++j) {
+            if (j < n) {
+                const int ks = j % kStages, sbuf = j & 1;
+                if (!flag_wait(bar_addr(bars, pipe, K_FULL + ks), (uint32_t)(j / kStages) & 1u, abort, a.status))
+                    break;
+                // S buffer sbuf (and the P that overwrote it) is free once P V of tile j-2 is done
+                if (j >= 2 &&
+                    !flag_wait(bar_addr(bars, pipe, PV_DONE + sbuf), (uint32_t)((j - 2) >> 1) & 1u, abort, a.status))
                     break;
                 tc_fence_after();
                 if (lane == 0) {
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk) {
-                        const uint32_t off = (kk >> 2) * kSlabBytes + (kk & 3) * 32;
-                        tc_mma_f16(tmem + kColS + st * 128, sw128_desc(sb + kSmQ + off, 16, 1024),
-                                   sw128_desc(sb + kSmK + ks * kOperandBytes + off, 16, 1024), kIdescS, kk > 0);
+                        tc_mma_f16(tp + kColS + sbuf * 64,
+                                   sw128_desc(sb + kSmQ + (kk >> 2) * kQSlab + (kk & 3) * 32, 16, 1024),
+                                   sw128_desc(kring + ks * kTileOpBytes + (kk >> 2) * kTileSlab + (kk & 3) * 32, 16,
+                                              1024),
+                                   kIdescS, kk > 0);
                     }
-                    tc_commit(bar_addr(bars, S_FULL + st));
-                    tc_commit(bar_addr(bars, K_EMPTY + ks));
+                    tc_commit(bar_addr(bars, pipe, S_FULL + sbuf));
+                    tc_commit(bar_addr(bars, pipe, K_EMPTY + ks));
                 }
                 __syncwarp();
             }
             if (j >= 1) {
-                const int i = j - 1, vs = i % kStages, st = i & 1;
-                if (!flag_wait(bar_addr(bars, P_FULL + st), (uint32_t)(i >> 1) & 1u, abort, a.status)) break;
-                if (!flag_wait(bar_addr(bars, V_FULL + vs), (uint32_t)(i / kStages) & 1u, abort, a.status)) break;
-                if (i == nkt - 1) {
+                const int i = j - 1, vs = i % kStages, sbuf = i & 1;
+                if (!flag_wait(bar_addr(bars, pipe, P_FULL + sbuf), (uint32_t)(i >> 1) & 1u, abort, a.status)) break;
+                if (!flag_wait(bar_addr(bars, pipe, V_FULL + vs), (uint32_t)(i / kStages) & 1u, abort, a.status))
+                    break;
+                if (base + i == nkt - 1) {
                     // keys past the last row's position may hold anything (even NaN); zero their V rows so
                     // that P = 0 times V stays 0 in the tensor core
-                    const int first = pos_max + 1 - i * kKeys;
+                    const int first = pos_max + 1 - (base + i) * kKeys;
                     for (int c = first * 8 + lane; c < kKeys * 8; c += 32) {
                         const int r = c >> 3, ch = c & 7;
-                        const uint32_t base = sb + kSmV + vs * kOperandBytes + r * 128 + ch * 16;
-                        st_shared_v4(base, make_uint4(0, 0, 0, 0));
-                        st_shared_v4(base + kSlabBytes, make_uint4(0, 0, 0, 0));
+                        const uint32_t at = vring + vs * kTileOpBytes + r * 128 + ch * 16;
+                        st_shared_v4(at, make_uint4(0, 0, 0, 0));
+                        st_shared_v4(at + kTileSlab, make_uint4(0, 0, 0, 0));
                     }
                     fence_proxy_async_smem();
                     __syncwarp();
@@ -298,69 +319,61 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                 tc_fence_after();
                 if (lane == 0) {
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
-                        tc_mma_f16_ts(tmem + kColO, tmem + kColP + st * 64 + kk * 8,
-                                      sw128_desc(sb + kSmV + vs * kOperandBytes + kk * 2048, kSlabBytes, 1024),
-                                      kIdescPV, (i > 0 || kk > 0) ? 1u : 0u);
-                    tc_commit(bar_addr(bars, P_EMPTY + st));
-                    tc_commit(bar_addr(bars, V_EMPTY + vs));
+                    for (int kk = 0; kk < 4; ++kk)
+                        tc_mma_f16_ts(tp + kColO, tp + kColS + sbuf * 64 + kk * 8,
+                                      sw128_desc(vring + vs * kTileOpBytes + kk * 2048, kTileSlab, 1024), kIdescPV,
+                                      (i > 0 || kk > 0) ? 1u : 0u);
+                    tc_commit(bar_addr(bars, pipe, PV_DONE + sbuf));
+                    tc_commit(bar_addr(bars, pipe, V_EMPTY + vs));
                 }
                 __syncwarp();
             }
         }
         if (lane == 0) {
-            tc_commit(bar_addr(bars, MMA_DONE));
-            mbar_wait(bar_addr(bars, MMA_DONE), 0);
+            tc_commit(bar_addr(bars, pipe, MMA_DONE));
+            mbar_wait(bar_addr(bars, pipe, MMA_DONE), 0);
         }
         __syncwarp();
     } else {
-        // ================================================= softmax (warps 2..9)
-        // Warps w and w + 4 share TMEM lane quarter w % 4, i.e. the same 32
-        // rows. Both read the whole S row (for the row max); each then
-        // exponentiates one 64-key half, writes that half of P (FP16, two per
-        // column) to TMEM, and owns the matching 64 columns of O.
+        // ================================================= softmax: 4 warps per pipe, thread = query row
+        const int pipe = (warp - 6) >> 2;
+        const int base = pipe ? n0 : 0, n = pipe ? nkt - n0 : n0;
         const int qtr = warp & 3;
-        const int hv = (warp - 2) >> 2;
         const int row = qtr * 32 + lane;
         const bool valid = row < rows;
         const int pos = p0 + row;
-        const uint32_t tl = tmem + ((uint32_t)(qtr * 32) << 16);
-        float m_used = valid ? -INFINITY : 0.f, l = 0.f;
+        const uint32_t tl = tmem + pipe * kPipeCols + ((uint32_t)(qtr * 32) << 16);
+        float m_used = -INFINITY, l = 0.f;
         bool ok = true;
-        for (int j = 0; j < nkt; ++j) {
-            const int st = j & 1;
-            const uint32_t ph = (uint32_t)(j >> 1) & 1u;
-            if (!flag_wait(bar_addr(bars, S_FULL + st), ph, abort, a.status)) { ok = false; break; }
+        for (int j = 0; j < n; ++j) {
+            const int sbuf = j & 1;
+            if (!flag_wait(bar_addr(bars, pipe, S_FULL + sbuf), (uint32_t)(j >> 1) & 1u, abort, a.status)) {
+                ok = false;
+                break;
+            }
             tc_fence_after();
-            uint32_t sr[64], so[64];  // this thread's 64-key half, and the other half
-            tc_ld64_pair(tl + kColS + st * 128 + hv * 64, sr, tl + kColS + st * 128 + (1 - hv) * 64, so);
-            tc_fence_before();
-            mbar_arrive(bar_addr(bars, S_FREE + st));
-
-            const int key0 = j * kKeys;
+            uint32_t sr[kKeys];
+            tc_ld64(tl + kColS + sbuf * 64, sr);
+            const int key0 = (base + j) * kKeys;
             if (key0 + kKeys - 1 > p0 || !valid) {
                 // diagonal tile or padding row: keys past the row's position count as -inf
                 const int nvis = valid ? pos - key0 + 1 : 0;
-                const int own = hv * 64, oth = (1 - hv) * 64;
 #pragma unroll
-                for (int e = 0; e < 64; ++e) {
-                    if (own + e >= nvis) sr[e] = __float_as_uint(-INFINITY);
-                    if (oth + e >= nvis) so[e] = __float_as_uint(-INFINITY);
-                }
+                for (int e = 0; e < kKeys; ++e)
+                    if (e >= nvis) sr[e] = __float_as_uint(-INFINITY);
             }
             float mxs[8];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) mxs[u] = fmaxf(__uint_as_float(sr[u]), __uint_as_float(so[u]));
+            for (int u = 0; u < 8; ++u) mxs[u] = __uint_as_float(sr[u]);
 #pragma unroll
-            for (int e = 8; e < 64; ++e)
-                mxs[e & 7] = fmaxf(mxs[e & 7], fmaxf(__uint_as_float(sr[e]), __uint_as_float(so[e])));
+            for (int e = 8; e < kKeys; ++e) mxs[e & 7] = fmaxf(mxs[e & 7], __uint_as_float(sr[e]));
             const float mx = fmaxf(fmaxf(fmaxf(mxs[0], mxs[1]), fmaxf(mxs[2], mxs[3])),
                                    fmaxf(fmaxf(mxs[4], mxs[5]), fmaxf(mxs[6], mxs[7])));
             const float m_tile = mx * a.scale_log2;
-            const bool raise = valid && m_tile > m_used + kRescaleThreshold;
+            const bool raise = m_tile > m_used + kRescaleThreshold;  // false while the row has seen no key
             if (j > 0 && __any_sync(0xffffffffu, raise)) {
                 // the previous P V product must have landed before O is rescaled
-                if (!flag_wait(bar_addr(bars, P_EMPTY + ((j - 1) & 1)), (uint32_t)((j - 1) >> 1) & 1u, abort,
+                if (!flag_wait(bar_addr(bars, pipe, PV_DONE + ((j - 1) & 1)), (uint32_t)((j - 1) >> 1) & 1u, abort,
                                a.status)) {
                     ok = false;
                     break;
@@ -368,63 +381,80 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                 tc_fence_after();
                 const float f = raise ? ex2(m_used - m_tile) : 1.f;
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
+                for (int c = 0; c < 4; ++c) {
                     float of[32];
                     uint32_t o[32];
-                    tc_ld32(tl + kColO + hv * 64 + c * 32, of);
+                    tc_ld32(tl + kColO + c * 32, of);
 #pragma unroll
                     for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(of[e] * f);
-                    tc_st32(tl + kColO + hv * 64 + c * 32, o);
+                    tc_st32(tl + kColO + c * 32, o);
                 }
                 l *= f;
             }
             if (raise) m_used = m_tile;
-
-            // P buffer st is free once the P V product of tile j-2 has landed
-            if (j >= 2 && !flag_wait(bar_addr(bars, P_EMPTY + st), ph ^ 1u, abort, a.status)) { ok = false; break; }
+            // rows that have seen no visible key keep p = 0 (exp2(-inf - -inf) would be NaN)
+            const float m_sub = m_used == -INFINITY ? 0.f : m_used;
             float ls[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) ls[u] = 0.f;
             uint32_t packed[32];
 #pragma unroll
-            for (int e = 0; e < 64; e += 2) {
-                const float pa = ex2(fmaf(__uint_as_float(sr[e]), a.scale_log2, -m_used));
-                const float pb = ex2(fmaf(__uint_as_float(sr[e + 1]), a.scale_log2, -m_used));
+            for (int e = 0; e < kKeys; e += 2) {
+                const float pa = ex2(fmaf(__uint_as_float(sr[e]), a.scale_log2, -m_sub));
+                const float pb = ex2(fmaf(__uint_as_float(sr[e + 1]), a.scale_log2, -m_sub));
                 ls[e & 7] += pa;
                 ls[(e + 1) & 7] += pb;
                 const __half2 hp = __floats2half2_rn(pa, pb);
                 packed[e >> 1] = *reinterpret_cast<const uint32_t*>(&hp);
             }
-            tc_st32(tl + kColP + st * 64 + hv * 32, packed);
+            tc_st32(tl + kColS + sbuf * 64, packed);  // P over the first 32 columns of its S buffer
             l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
             tc_fence_before();
-            mbar_arrive(bar_addr(bars, P_FULL + st));
+            mbar_arrive(bar_addr(bars, pipe, P_FULL + sbuf));
         }
-        if (ok) {
-            const int i = nkt - 1;
-            float* lx = reinterpret_cast<float*>(smem + kSmLx);
-            lx[hv * kRows + row] = l;
-            mbar_arrive(bar_addr(bars, L_EX));
-            if (flag_wait(bar_addr(bars, P_EMPTY + (i & 1)), (uint32_t)(i >> 1) & 1u, abort, a.status) &&
-                flag_wait(bar_addr(bars, L_EX), 0, abort, a.status)) {
+        // ---- merge the two pipes: pipe p writes output dims [64p, 64p + 64). Each pipe's (m, l) per row
+        // goes into stage 0 of its own K ring, idle once its last P V product has landed.
+        const bool landed = ok && (n == 0 || flag_wait(bar_addr(bars, pipe, PV_DONE + ((n - 1) & 1)),
+                                                       (uint32_t)((n - 1) >> 1) & 1u, abort, a.status));
+        if (landed) {
+            float2* mine = reinterpret_cast<float2*>(smem + kSmRing + pipe * 2 * kStages * kTileOpBytes);
+            const float2* other = reinterpret_cast<const float2*>(smem + kSmRing + (1 - pipe) * 2 * kStages *
+                                                                                     kTileOpBytes);
+            mine[row] = make_float2(m_used, l);
+            tc_fence_before();
+            mbar_arrive(bars + 8u * kBarLx);
+            if (flag_wait(bars + 8u * kBarLx, 0, abort, a.status)) {
                 tc_fence_after();
-                const float l_row = l + lx[(1 - hv) * kRows + row];
-                float o[64];
-                tc_ld32(tl + kColO + hv * 64, o);
-                tc_ld32(tl + kColO + hv * 64 + 32, o + 32);
-                if (valid) {
-                    const float inv = 1.f / l_row;
-                    uint4* dst = reinterpret_cast<uint4*>(a.out + ((int64_t)(q0 + qt * kRows + row) * a.num_heads + h) *
-                                                                      kHeadDim + hv * 64);
+                const float2 s0 = pipe == 0 ? mine[row] : other[row];
+                const float2 s1 = pipe == 0 ? other[row] : mine[row];
+                const float M = fmaxf(s0.x, s1.x);
+                const float w0 = n0 > 0 && s0.x != -INFINITY ? ex2(s0.x - M) : 0.f;
+                const float w1 = nkt - n0 > 0 && s1.x != -INFINITY ? ex2(s1.x - M) : 0.f;
+                const float inv = 1.f / (w0 * s0.y + w1 * s1.y);
+                const uint32_t t0 = tmem + ((uint32_t)(qtr * 32) << 16) + kColO + pipe * 64;
+                uint4* dst = reinterpret_cast<uint4*>(a.out + ((int64_t)(q0 + qt * kRows + row) * a.num_heads + h) *
+                                                                  kHeadDim + pipe * 64);
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        uint32_t w[4];
+                for (int c = 0; c < 2; ++c) {
+                    float o0[32], o1[32];
 #pragma unroll
-                        for (int u = 0; u < 4; ++u) {
-                            const __half2 hq = __floats2half2_rn(o[c * 8 + 2 * u] * inv, o[c * 8 + 2 * u + 1] * inv);
-                            w[u] = *reinterpret_cast<const uint32_t*>(&hq);
+                    for (int u = 0; u < 32; ++u) o0[u] = o1[u] = 0.f;
+                    // a pipe that processed no tile never wrote its O: leave it out
+                    if (n0 > 0) tc_ld32(t0 + c * 32, o0);
+                    if (nkt - n0 > 0) tc_ld32(t0 + kPipeCols + c * 32, o1);
+                    if (valid) {
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4) {
+                            uint32_t w[4];
+#pragma unroll
+                            for (int u = 0; u < 4; ++u) {
+                                const int e = q4 * 8 + 2 * u;
+                                const __half2 hq = __floats2half2_rn(fmaf(w0, o0[e], w1 * o1[e]) * inv,
+                                                                     fmaf(w0, o0[e + 1], w1 * o1[e + 1]) * inv);
+                                w[u] = *reinterpret_cast<const uint32_t*>(&hq);
+                            }
+                            dst[c * 4 + q4] = make_uint4(w[0], w[1], w[2], w[3]);
                         }
-                        dst[c] = make_uint4(w[0], w[1], w[2], w[3]);
                     }
                 }
             }
@@ -434,7 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+    if (warp == 4) tmem_dealloc(tmem, kTmemCols);
 }
 
 }  // namespace
