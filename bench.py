@@ -45,17 +45,17 @@ HEAD_DIM = 128
 SCALE = float(np.float32(1.0 / np.sqrt(np.float32(128.0))))
 
 
-def _iterations(config: str):
+def _iterations(config: str, seed: int = 0):
     """The workload's engine iterations (one for decode configs, 8 for the chunk schedule)."""
     if config == "average_decode":
-        return [workloads.average_decode(0)]
+        return [workloads.average_decode(seed)]
     if config == "long_decode":
-        return [workloads.long_decode(0)]
+        return [workloads.long_decode(seed)]
     if config == "shared_prefix_decode":
-        return [workloads.shared_prefix_decode(0)]
+        return [workloads.shared_prefix_decode(seed)]
     if config == "mixed_prefill":
-        first = workloads.mixed_prefill(0)
-        return [workloads.mixed_prefill(c) for c in range(first.meta["num_chunks"])]
+        first = workloads.mixed_prefill(0, seed=seed)
+        return [workloads.mixed_prefill(c, seed=seed) for c in range(first.meta["num_chunks"])]
     raise KeyError(config)
 
 
@@ -189,6 +189,15 @@ def aggregate(per_rank_ms, per_rank_units):
     return sum(per_rank_units) / t
 
 
+def max_over_ranks(values, dist=None, device=None):
+    """Element-wise maximum of per-rank timings over the process group; every rank gets the result."""
+    import torch
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    if dist is not None:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
 def prefill_pairs(wl) -> int:
     """Unmasked (query, key) pairs of the prefill rows: query at position p sees p + 1 keys."""
     n = 0
@@ -284,7 +293,7 @@ def run_ours(args):
     pkv_build.build()
     pkv.load()
 
-    iters = _iterations(args.config)
+    iters = _iterations(args.config, args.seed)
     wl0 = iters[0]
     L = args.layers or wl0.num_layers
     H = wl0.num_heads
@@ -292,7 +301,7 @@ def run_ours(args):
 
     pool_t = torch.empty(workloads.pool_shape(wl0.num_blocks, L, H), dtype=torch.float16, device=dev)
     workloads.fill_normal_fp16_(pool_t, workloads.value_seed(wl0.seed, "pool"))
-    pool = pkv.Pool(pool_t, wl0.num_blocks, num_layers=L, num_heads=H)
+    pool = pkv.Pool(pool_t, wl0.num_blocks, num_layers=L, num_heads=H, partition_tokens=args.partition_tokens)
     gen = torch.Generator(device=dev)
     gen.manual_seed(workloads.value_seed(wl0.seed, "q"))
     steps = [StepData(torch, pkv, pool, wl, m, L, dev, gen) for wl, m in zip(iters, _metadata(pkv, iters))]
@@ -417,10 +426,7 @@ def run_ours(args):
     h2d = sum(src.numel() * src.element_size() for io in host_io for src, _ in io)
     d2h = sum(o.numel() * o.element_size() for o in outs_h)
 
-    times = torch.tensor([t_ms, e2e_ms], dtype=torch.float64, device=dev)
-    if ws > 1:
-        dist.all_reduce(times, op=dist.ReduceOp.MAX)
-    t_ms, e2e_ms = (float(x) for x in times.tolist())
+    t_ms, e2e_ms = max_over_ranks([t_ms, e2e_ms], dist if ws > 1 else None, dev)
 
     hbm_peak, tf_peak, peak_kind = _peaks()
     K = args.steps
@@ -480,6 +486,7 @@ def run_ours(args):
                    "iterations_per_step": len(steps), "num_seqs": wl0.num_seqs, "heads": H, "head_dim": HEAD_DIM,
                    "pool_blocks": wl0.num_blocks, "kv_bytes_per_step": kv_step,
                    "prefill_flops_per_step": flops_step, "seed": wl0.seed,
+                   "partition_tokens": args.partition_tokens or 512,
                    "max_context": int(max(int(s.wl.ctx_lens.max()) for s in steps)),
                    "l2": "inputs larger than L2 (every step reads the whole KV context of all layers)",
                    "cuda_graph": graph is not None},
@@ -565,7 +572,7 @@ def run_reference(args):
     if rank != 0:
         return
     import oracle
-    wl = _iterations(args.config)[0]
+    wl = _iterations(args.config, args.seed)[0]
     threads = len(os.sched_getaffinity(0))
     oracle.set_num_threads(threads)
     samples = [_layer_sample(wl, l, None, seed=1) for l in range(2)]
@@ -607,6 +614,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="launch each step directly instead of replaying a CUDA graph")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--seed", type=int, default=0, help="seed of the workload's length and block draws")
+    ap.add_argument("--partition-tokens", type=int, default=0,
+                    help="decode split-K partition size of the pool (0 = the library default)")
     ap.add_argument("--layers", type=int, default=0,
                     help="run only this many layers (smaller pool; per-layer work unchanged; for profiling)")
     args = ap.parse_args()
