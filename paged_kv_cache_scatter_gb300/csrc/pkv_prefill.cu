@@ -18,15 +18,16 @@
 // softmax warps; at the end the two partial results merge exactly through
 // their softmax statistics.
 //
-// Warp roles (448 threads):
-//   warps 0-3    TMA producers, one per (pipe, K|V): 64-key tiles = 4 blocks
-//                x two 64-dim halves (2 KB boxes), into 3-stage rings.
-//   warps 4, 5   MMA issuers of pipe 0 / 1 (one elected lane each; warp 4
+// Warp roles (352 threads):
+//   warp 0       TMA producers: lanes 0-3, one per (pipe, K|V), each with its
+//                own loop: 64-key tiles = 4 blocks x two 64-dim halves (2 KB
+//                boxes), into 3-stage rings.
+//   warps 1, 2   MMA issuers of pipe 0 / 1 (one elected lane each; warp 1
 //                also owns the TMEM allocation): S_j = Q K_j^T into S buffer
 //                j%2 (A and B from shared memory), then O += P_j V_j with P
 //                read from tensor memory; completion by tcgen05.commit.
-//   warps 6-9,   softmax of pipe 0 / 1: thread r owns query row r (TMEM lane
-//   10-13        r). Per tile it loads its 64 S values, writes
+//   warps 3-6,   softmax of pipe 0 / 1: thread r owns query row r (TMEM lane
+//   7-10         r). Per tile it loads its 64 S values, writes
 //                P = 2^(s*scale*log2e - m) in FP16 over the first half of the
 //                same S buffer, and keeps the running sum. The running max m
 //                is only raised when the tile's max exceeds it by more than 8
@@ -88,7 +89,7 @@ constexpr int kRows = 128;     // query rows per CTA (MMA M)
 constexpr int kKeys = 64;      // keys per tile (4 blocks)
 constexpr int kPipes = 2;      // independent key-range pipelines per CTA
 constexpr int kStages = 3;     // K and V ring depth per pipeline
-constexpr int kThreads = 448;  // 4 producers, 2 MMA issuers, 2 x 4 softmax warps
+constexpr int kThreads = 352;  // producer warp, 2 MMA issuers, 2 x 4 softmax warps
 constexpr int kQBytes = kRows * kHeadDim * 2;        // 32 KB
 constexpr int kQSlab = kQBytes / 2;                  // 16 KB: 128 rows x 64 halves
 constexpr int kTileOpBytes = kKeys * kHeadDim * 2;   // 16 KB: one 64-key K or V tile
@@ -102,7 +103,8 @@ constexpr int kSmBars = kSmRing + kPipes * 2 * kStages * kTileOpBytes;
 enum Bar { K_FULL = 0, V_FULL = 3, K_EMPTY = 6, V_EMPTY = 9, S_FULL = 12, P_FULL = 14, PV_DONE = 16, MMA_DONE = 18,
            BARS_PER_PIPE = 19 };
 constexpr int kBarLx = kPipes * BARS_PER_PIPE;              // the final exchange between the pipes
-constexpr int kNumBars = kBarLx + 1;
+constexpr int kBarQ = kBarLx + 1;                           // the Q tile is in shared memory
+constexpr int kNumBars = kBarLx + 2;
 constexpr int kSoftmaxThreads = 128;                        // per pipe
 constexpr int kSmTmemSlot = kSmBars + kNumBars * 8;
 constexpr int kSmAbort = kSmTmemSlot + 4;
@@ -154,6 +156,17 @@ __device__ __forceinline__ bool flag_wait(uint32_t bar, uint32_t parity, volatil
     return ok;
 }
 
+// Bounded wait of a single thread (the producer lanes run independent loops).
+__device__ __forceinline__ bool lane_wait(uint32_t bar, uint32_t parity, volatile int* abort, unsigned int* status)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort) return false;
+    if (mbar_wait(bar, parity)) return true;
+    atomicOr(status, PKV_DEV_TIMEOUT);
+    *abort = 1;
+    return false;
+}
+
 __device__ __forceinline__ uint32_t bar_addr(uint32_t bars, int pipe, int idx)
 {
     return bars + 8u * (uint32_t)(pipe * BARS_PER_PIPE + idx);
@@ -196,17 +209,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         return;
     }
 
-    // ---- Q tile -> shared memory (swizzled, K-major); rows past the chunk are zero
-    for (int c = threadIdx.x; c < kRows * 16; c += kThreads) {
-        const int r = c >> 4, ch = c & 15;
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (r < rows)
-            v = __ldg(reinterpret_cast<const uint4*>(a.q + ((int64_t)(q0 + qt * kRows + r) * a.num_heads + h) * kHeadDim) +
-                      ch);
-        st_shared_v4(sb + kSmQ + (ch >> 3) * kQSlab + r * 128 + (((ch & 7) ^ (r & 7)) << 4), v);
-    }
-    fence_proxy_async_smem();
-
     const uint32_t bars = sb + kSmBars;
     volatile int* abort = reinterpret_cast<volatile int*>(smem + kSmAbort);
     if (threadIdx.x == 0) {
@@ -225,10 +227,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             mbar_init(bar_addr(bars, p, MMA_DONE), 1);
         }
         mbar_init(bars + 8u * kBarLx, kPipes * kSoftmaxThreads);
+        mbar_init(bars + 8u * kBarQ, kThreads - 32);
         *abort = 0;
         fence_mbar_init();
     }
-    if (warp == 4) {
+    if (warp == 1) {
         tmem_alloc(sb + kSmTmemSlot, kTmemCols);
         tmem_relinquish();
     }
@@ -237,39 +240,90 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kSmTmemSlot);
 
-    if (warp < 4) {
-        // ================================================= TMA producers: (pipe, K|V) per warp
-        const int pipe = warp >> 1, kv = warp & 1;
-        const int base = pipe ? n0 : 0, n = pipe ? nkt - n0 : n0;
-        const uint32_t ring = sb + kSmRing + (pipe * 2 + kv) * kStages * kTileOpBytes;
-        const uint32_t full0 = bar_addr(bars, pipe, kv ? V_FULL : K_FULL);
-        const uint32_t empty0 = bar_addr(bars, pipe, kv ? V_EMPTY : K_EMPTY);
-        if (lane == 0) prefetch_tmap(&tmap);
-        int issued = 0;
-        for (int j = 0; j < n; ++j) {
-            const int st = j % kStages;
-            const uint32_t ph = (uint32_t)(j / kStages) & 1u;
-            const int g = base + j;
-            const int nb = min(4, nblk - 4 * g);
-            const int id = lane < nb ? __ldg(trow + 4 * g + lane) : 0;
-            if (j >= kStages && !flag_wait(empty0 + 8 * st, ph ^ 1u, abort, a.status)) break;
-            if (lane == 0) mbar_arrive_expect_tx(full0 + 8 * st, nb * kTileBytes);
-            for (int b = 0; b < nb; ++b) {
-                const int idb = __shfl_sync(0xffffffffu, id, b);
-                if (lane == 0)
-                    for (int half = 0; half < 2; ++half)
-                        tma_load_5d(ring + st * kTileOpBytes + half * kTileSlab + b * 2048, &tmap, half * 64, 0,
-                                    kv * a.num_heads + h, a.layer, idb, full0 + 8 * st);
-            }
-            issued = j + 1;
+    if (warp >= 1) {
+        // ---- Q tile -> shared memory (swizzled, K-major), rows past the chunk zero, while the
+        // producers already fetch the first K/V tiles. Loads first, then stores; the MMA
+        // issuers wait for the Q barrier before their first S product.
+        constexpr int kLoaders = kThreads - 32;
+        constexpr int kPer = (kRows * 16 + kLoaders - 1) / kLoaders;
+        const int t = threadIdx.x - 32;
+        uint4 v[kPer];
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+            const int c = t + u * kLoaders, r = c >> 4, ch = c & 15;
+            v[u] = make_uint4(0, 0, 0, 0);
+            if (c < kRows * 16 && r < rows)
+                v[u] = __ldg(reinterpret_cast<const uint4*>(
+                                 a.q + ((int64_t)(q0 + qt * kRows + r) * a.num_heads + h) * kHeadDim) + ch);
         }
-        __syncwarp();
-        if (*abort && lane == 0)
-            for (int j = (issued > kStages ? issued - kStages : 0); j < issued; ++j)
-                mbar_wait(full0 + 8 * (j % kStages), (uint32_t)(j / kStages) & 1u);
-    } else if (warp < 6) {
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+            const int c = t + u * kLoaders, r = c >> 4, ch = c & 15;
+            if (c < kRows * 16)
+                st_shared_v4(sb + kSmQ + (ch >> 3) * kQSlab + r * 128 + (((ch & 7) ^ (r & 7)) << 4), v[u]);
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(bars + 8u * kBarQ);
+    }
+
+    if (warp == 0) {
+        // ================================================= TMA producers: lanes 0-3, one per (pipe, K|V),
+        // each running its own loop (no warp-wide operation in here)
+        if (lane < 4) {
+            const int pipe = lane >> 1, kv = lane & 1;
+            const int base = pipe ? n0 : 0, n = pipe ? nkt - n0 : n0;
+            const uint32_t ring = sb + kSmRing + (pipe * 2 + kv) * kStages * kTileOpBytes;
+            const uint32_t full0 = bar_addr(bars, pipe, kv ? V_FULL : K_FULL);
+            const uint32_t empty0 = bar_addr(bars, pipe, kv ? V_EMPTY : K_EMPTY);
+            if (lane == 0) prefetch_tmap(&tmap);
+            // Block ids of tile j come from a register queue filled kIdAhead tiles in advance, so that
+            // the table reads' latency never sits between two tiles' copies.
+            constexpr int kIdAhead = 4;
+            int idq[kIdAhead][4];
+#pragma unroll
+            for (int u = 0; u < kIdAhead; ++u)
+#pragma unroll
+                for (int b = 0; b < 4; ++b) {
+                    const int blk = 4 * (base + u) + b;
+                    idq[u][b] = u < n && blk < nblk ? __ldg(trow + blk) : 0;
+                }
+            int issued = 0;
+            bool stop = false;
+            for (int j0 = 0; j0 < n && !stop; j0 += kIdAhead) {
+#pragma unroll
+                for (int u = 0; u < kIdAhead; ++u) {
+                    const int j = j0 + u;
+                    if (j >= n || stop) break;
+                    const int st = j % kStages;
+                    const uint32_t ph = (uint32_t)(j / kStages) & 1u;
+                    const int g = base + j;
+                    const int nb = min(4, nblk - 4 * g);
+                    if (j >= kStages && !lane_wait(empty0 + 8 * st, ph ^ 1u, abort, a.status)) {
+                        stop = true;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(full0 + 8 * st, nb * kTileBytes);
+#pragma unroll
+                    for (int b = 0; b < 4; ++b)
+                        if (b < nb)
+                            for (int half = 0; half < 2; ++half)
+                                tma_load_5d(ring + st * kTileOpBytes + half * kTileSlab + b * 2048, &tmap, half * 64,
+                                            0, kv * a.num_heads + h, a.layer, idq[u][b], full0 + 8 * st);
+                    issued = j + 1;
+#pragma unroll
+                    for (int b = 0; b < 4; ++b) {  // refill this slot with tile j + kIdAhead
+                        const int blk = 4 * (g + kIdAhead) + b;
+                        idq[u][b] = j + kIdAhead < n && blk < nblk ? __ldg(trow + blk) : 0;
+                    }
+                }
+            }
+            if (*abort)
+                for (int j = (issued > kStages ? issued - kStages : 0); j < issued; ++j)
+                    mbar_wait(full0 + 8 * (j % kStages), (uint32_t)(j / kStages) & 1u);
+        }
+    } else if (warp < 3) {
         // ================================================= MMA issuers, one per pipe
-        const int pipe = warp - 4;
+        const int pipe = warp - 1;
         const int base = pipe ? n0 : 0, n = pipe ? nkt - n0 : n0;
         const uint32_t tp = tmem + pipe * kPipeCols;
         const uint32_t kring = sb + kSmRing + (pipe * 2) * kStages * kTileOpBytes;
@@ -277,6 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         for (int j = 0; j <= n; ++j) {
             if (j < n) {
                 const int ks = j % kStages, sbuf = j & 1;
+                if (j == 0 && !flag_wait(bars + 8u * kBarQ, 0, abort, a.status)) break;
                 if (!flag_wait(bar_addr(bars, pipe, K_FULL + ks), (uint32_t)(j / kStages) & 1u, abort, a.status))
                     break;
                 // S buffer sbuf (and the P that overwrote it) is free once P V of tile j-2 is done
@@ -336,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         __syncwarp();
     } else {
         // ================================================= softmax: 4 warps per pipe, thread = query row
-        const int pipe = (warp - 6) >> 2;
+        const int pipe = (warp - 3) >> 2;
         const int base = pipe ? n0 : 0, n = pipe ? nkt - n0 : n0;
         const int qtr = warp & 3;
         const int row = qtr * 32 + lane;
@@ -464,7 +519,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 4) tmem_dealloc(tmem, kTmemCols);
+    if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
 }  // namespace
