@@ -8,32 +8,33 @@
 // decode share each step": a prompt is prefilled in chunks; "The inference
 // engine" (wpnews), "Prefill and decode ask the accelerator for different
 // work": prefill attention respects the causal mask). The chunk's own K/V
-// are already in the pool (kv_append runs first), so keys come only from
-// the pool, 128 at a time (8 blocks).
+// are already in the pool (kv_append runs first), so keys come only from the
+// pool, 128 at a time (8 blocks).
 //
-// Two independent pipelines per CTA split the key range: pipe 0 takes the
-// first half of the 64-key tiles, pipe 1 the rest (the diagonal tiles), so
-// the tensor core works on one pipe's MMAs while the other pipe's softmax
-// runs. Each pipe has its own K/V rings, S/P and O in TMEM, MMA issuer and
-// softmax warps; at the end the two partial results merge exactly through
-// their softmax statistics.
+// Tiles are 128 keys: an M=128 N=128 QK^T product keeps the tensor core at
+// its full rate (N=64 runs it at about half). S is double-buffered in tensor
+// memory, so S_{j+1} is computed while the softmax works on S_j; P_j, FP16,
+// overwrites the upper half of its own S buffer and O += P_j V_j reads it
+// from there, so S_{j+2} (same buffer) follows P_j V_j.
 //
-// Warp roles (352 threads):
-//   warp 0       TMA producers: lanes 0-3, one per (pipe, K|V), each with its
-//                own loop: 64-key tiles = 4 blocks x two 64-dim halves (2 KB
-//                boxes), into 3-stage rings.
-//   warps 1, 2   MMA issuers of pipe 0 / 1 (one elected lane each; warp 1
-//                also owns the TMEM allocation): S_j = Q K_j^T into S buffer
-//                j%2 (A and B from shared memory), then O += P_j V_j with P
-//                read from tensor memory; completion by tcgen05.commit.
-//   warps 3-6,   softmax of pipe 0 / 1: thread r owns query row r (TMEM lane
-//   7-10         r). Per tile it loads its 64 S values, writes
-//                P = 2^(s*scale*log2e - m) in FP16 over the first half of the
-//                same S buffer, and keeps the running sum. The running max m
-//                is only raised when the tile's max exceeds it by more than 8
-//                (a factor 256, far inside FP16/FP32 range); then the row's O
-//                and sum are rescaled once the previous P V product has
-//                landed. The result is exact up to rounding.
+// Warp roles (288 threads):
+//   warps 0-3    TMA producers: K low / high 64 dims, V low / high; lanes 0-7
+//                each copy one 2 KB box (one block's 16 rows of one 64-dim
+//                half) of every 128-key tile into a 3-stage ring. Four
+//                issuing warps keep the copy engine's request rate off the
+//                critical path.
+//   warp 4       MMA issuer (one elected lane; the warp owns the TMEM
+//                allocation): S_j = Q K_j^T (A and B from shared memory),
+//                O += P_j V_j (P from tensor memory); completion by
+//                tcgen05.commit.
+//   warps 5-8    softmax: thread r owns query row r (TMEM lane r). Per tile it
+//                reads its 128 S values for the row max, then again by
+//                quarters to write P = 2^(s*scale*log2e - m) and add to the
+//                running sum. The running max m is only raised when the
+//                tile's max exceeds it by more than 8 (a factor 256, far
+//                inside FP16/FP32 range); then the row's O and sum are
+//                rescaled once the previous P V product has landed. The
+//                result is exact up to rounding.
 // Shared-memory operands use the 128-byte swizzle: rows of 128 B (64 halves),
 // two slabs per 128-wide operand, 8-row groups 1,024 B apart.
 #include <cuda.h>
@@ -85,38 +86,52 @@ bool encode_kv_tmap(const PoolGeom& g, TensorMap128* out, std::string* err)
 
 namespace {
 
-constexpr int kRows = 128;     // query rows per CTA (MMA M)
-constexpr int kKeys = 64;      // keys per tile (4 blocks)
-constexpr int kPipes = 2;      // independent key-range pipelines per CTA
-constexpr int kStages = 3;     // K and V ring depth per pipeline
-constexpr int kThreads = 352;  // producer warp, 2 MMA issuers, 2 x 4 softmax warps
+constexpr int kRows = 128;            // query rows per CTA (MMA M)
+constexpr int kKeys = 128;            // keys per tile (8 blocks)
+constexpr int kBlocksPerTile = kKeys / kBlockSize;
+constexpr int kStages = 3;            // K and V ring depth
+constexpr int kProducerWarps = 4;     // K low, K high, V low, V high
+constexpr int kMmaWarp = 4;           // also owns the TMEM allocation
+constexpr int kFirstSoftmaxWarp = 5;
+constexpr int kSoftmaxThreads = 128;
+constexpr int kThreads = (kFirstSoftmaxWarp + 4) * 32;  // 288
 constexpr int kQBytes = kRows * kHeadDim * 2;        // 32 KB
 constexpr int kQSlab = kQBytes / 2;                  // 16 KB: 128 rows x 64 halves
-constexpr int kTileOpBytes = kKeys * kHeadDim * 2;   // 16 KB: one 64-key K or V tile
-constexpr int kTileSlab = kTileOpBytes / 2;          // 8 KB: 64 rows x 64 halves
+constexpr int kTileOpBytes = kKeys * kHeadDim * 2;   // 32 KB: one 128-key K or V tile
+constexpr int kTileSlab = kTileOpBytes / 2;          // 16 KB: 128 rows x 64 halves
 constexpr float kRescaleThreshold = 8.f;             // log2 of the largest un-rescaled P (256)
 
 // shared-memory map (offsets from a 1,024-byte aligned base)
 constexpr int kSmQ = 0;
-constexpr int kSmRing = kQBytes;                            // [pipe][K,V][stage] tiles
-constexpr int kSmBars = kSmRing + kPipes * 2 * kStages * kTileOpBytes;
-enum Bar { K_FULL = 0, V_FULL = 3, K_EMPTY = 6, V_EMPTY = 9, S_FULL = 12, P_FULL = 14, PV_DONE = 16, MMA_DONE = 18,
-           BARS_PER_PIPE = 19 };
-constexpr int kBarLx = kPipes * BARS_PER_PIPE;              // the final exchange between the pipes
-constexpr int kBarQ = kBarLx + 1;                           // the Q tile is in shared memory
-constexpr int kNumBars = kBarLx + 2;
-constexpr int kSoftmaxThreads = 128;                        // per pipe
-constexpr int kSmTmemSlot = kSmBars + kNumBars * 8;
+constexpr int kSmKRing = kQBytes;                             // [stage] K tiles
+constexpr int kSmVRing = kSmKRing + kStages * kTileOpBytes;   // [stage] V tiles
+constexpr int kSmBars = kSmVRing + kStages * kTileOpBytes;
+enum Bar {
+    K_FULL = 0,                   // count 2: both 64-dim halves' producers arm it
+    V_FULL = K_FULL + kStages,    // count 2
+    K_EMPTY = V_FULL + kStages,
+    V_EMPTY = K_EMPTY + kStages,
+    S_FULL = V_EMPTY + kStages,   // [2] per S buffer
+    P_FULL = S_FULL + 2,          // [2] count kSoftmaxThreads
+    PV_DONE = P_FULL + 2,         // [2]
+    V_FIXED = PV_DONE + 2,        // the last tile's V rows past the last position are zeroed
+    Q_READY = V_FIXED + 1,        // count kSoftmaxThreads
+    MMA_DONE = Q_READY + 1,
+    NUM_BARS = MMA_DONE + 1
+};
+constexpr int kSmTmemSlot = kSmBars + NUM_BARS * 8;
 constexpr int kSmAbort = kSmTmemSlot + 4;
 constexpr int kSmBytes = kSmAbort + 12;
-constexpr int kSmAlloc = kSmBytes + 1024;                   // slack to align the base
+constexpr int kSmAlloc = kSmBytes + 1024;  // slack to align the base
+static_assert(kSmAlloc <= 227 * 1024, "shared memory per CTA");
 
-// TMEM columns per pipe (base pipe * 256): two S buffers of 64 fp32 columns
-// (P, FP16, overwrites the first 32 columns of its S buffer), then O (128).
+// TMEM columns: S buffers 0 and 1 (128 fp32 columns each; P, FP16 two per
+// column, overwrites the upper 64 of its buffer), then O (128).
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kPipeCols = 256;
 constexpr uint32_t kColS = 0;
-constexpr uint32_t kColO = 128;
+constexpr uint32_t kSBufCols = 128;
+constexpr uint32_t kColP = 64;  // within an S buffer
+constexpr uint32_t kColO = 256;
 
 // Instruction descriptors, kind::f16: D = F32 (bit 4), A = B = F16,
 // N >> 3 at bit 17, M >> 4 at bit 24; bit 16 makes B MN-major.
@@ -156,20 +171,44 @@ __device__ __forceinline__ bool flag_wait(uint32_t bar, uint32_t parity, volatil
     return ok;
 }
 
-// Bounded wait of a single thread (the producer lanes run independent loops).
-__device__ __forceinline__ bool lane_wait(uint32_t bar, uint32_t parity, volatile int* abort, unsigned int* status)
+// Keys e >= nvis of N S values count as -inf (diagonal tiles and padding rows only).
+template <int N>
+__device__ __forceinline__ void mask_tail(uint32_t* s, int nvis)
 {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (*abort) return false;
-    if (mbar_wait(bar, parity)) return true;
-    atomicOr(status, PKV_DEV_TIMEOUT);
-    *abort = 1;
-    return false;
+#pragma unroll
+    for (int e = 0; e < N; ++e)
+        if (e >= nvis) s[e] = __float_as_uint(-INFINITY);
 }
 
-__device__ __forceinline__ uint32_t bar_addr(uint32_t bars, int pipe, int idx)
+// Max of 64 S values.
+__device__ __forceinline__ float max64(const uint32_t* sr)
 {
-    return bars + 8u * (uint32_t)(pipe * BARS_PER_PIPE + idx);
+    float mxs[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) mxs[u] = __uint_as_float(sr[u]);
+#pragma unroll
+    for (int e = 8; e < 64; ++e) mxs[e & 7] = fmaxf(mxs[e & 7], __uint_as_float(sr[e]));
+    return fmaxf(fmaxf(fmaxf(mxs[0], mxs[1]), fmaxf(mxs[2], mxs[3])),
+                 fmaxf(fmaxf(mxs[4], mxs[5]), fmaxf(mxs[6], mxs[7])));
+}
+
+// Softmax of a quarter tile: 32 S values -> P = 2^(s*scale - m) as 16 FP16 pairs, written in place over
+// s[0..15] (pair e/2 lands on a value already read); the sum is added to l. An s of -inf gives p = 0.
+__device__ __forceinline__ void softmax_quarter(uint32_t* s, float scale_log2, float m_sub, float& l)
+{
+    float ls[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) ls[u] = 0.f;
+#pragma unroll
+    for (int e = 0; e < 32; e += 2) {
+        const float pa = ex2(fmaf(__uint_as_float(s[e]), scale_log2, -m_sub));
+        const float pb = ex2(fmaf(__uint_as_float(s[e + 1]), scale_log2, -m_sub));
+        ls[e & 3] += pa;
+        ls[(e + 1) & 3] += pb;
+        const __half2 hp = __floats2half2_rn(pa, pb);
+        s[e >> 1] = *reinterpret_cast<const uint32_t*>(&hp);
+    }
+    l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
 }
 
 __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ CUtensorMap tmap,
@@ -194,10 +233,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     const int rows = min(kRows, qlen - qt * kRows);
     const int p0 = ctx - qlen + qt * kRows;  // position of row 0
     const int pos_max = p0 + rows - 1;
-    const int nkt = pos_max / kKeys + 1;     // 64-key tiles
+    const int n = pos_max / kKeys + 1;       // 128-key tiles
     const int nblk = pos_max / kBlockSize + 1;
-    // pipe 0 takes key tiles [0, n0), pipe 1 takes [n0, nkt) (the diagonal ones)
-    const int n0 = nkt / 2;
     const int32_t* trow = a.tables + (int64_t)s * a.max_blocks;
     bool bad = false;
     for (int b = threadIdx.x; b < nblk; b += kThreads) {
@@ -210,28 +247,27 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     }
 
     const uint32_t bars = sb + kSmBars;
+    auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
     volatile int* abort = reinterpret_cast<volatile int*>(smem + kSmAbort);
     if (threadIdx.x == 0) {
-        for (int p = 0; p < kPipes; ++p) {
-            for (int i = 0; i < kStages; ++i) {
-                mbar_init(bar_addr(bars, p, K_FULL + i), 1);
-                mbar_init(bar_addr(bars, p, V_FULL + i), 1);
-                mbar_init(bar_addr(bars, p, K_EMPTY + i), 1);
-                mbar_init(bar_addr(bars, p, V_EMPTY + i), 1);
-            }
-            for (int i = 0; i < 2; ++i) {
-                mbar_init(bar_addr(bars, p, S_FULL + i), 1);
-                mbar_init(bar_addr(bars, p, P_FULL + i), kSoftmaxThreads);
-                mbar_init(bar_addr(bars, p, PV_DONE + i), 1);
-            }
-            mbar_init(bar_addr(bars, p, MMA_DONE), 1);
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(bar(K_FULL + i), 2);
+            mbar_init(bar(V_FULL + i), 2);
+            mbar_init(bar(K_EMPTY + i), 1);
+            mbar_init(bar(V_EMPTY + i), 1);
         }
-        mbar_init(bars + 8u * kBarLx, kPipes * kSoftmaxThreads);
-        mbar_init(bars + 8u * kBarQ, kThreads - 32);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar(S_FULL + i), 1);
+            mbar_init(bar(P_FULL + i), kSoftmaxThreads);
+            mbar_init(bar(PV_DONE + i), 1);
+        }
+        mbar_init(bar(V_FIXED), 1);
+        mbar_init(bar(Q_READY), kSoftmaxThreads);
+        mbar_init(bar(MMA_DONE), 1);
         *abort = 0;
         fence_mbar_init();
     }
-    if (warp == 1) {
+    if (warp == kMmaWarp) {
         tmem_alloc(sb + kSmTmemSlot, kTmemCols);
         tmem_relinquish();
     }
@@ -240,196 +276,176 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kSmTmemSlot);
 
-    if (warp >= 1) {
-        // ---- Q tile -> shared memory (swizzled, K-major), rows past the chunk zero, while the
-        // producers already fetch the first K/V tiles. Loads first, then stores; the MMA
-        // issuers wait for the Q barrier before their first S product.
-        constexpr int kLoaders = kThreads - 32;
-        constexpr int kPer = (kRows * 16 + kLoaders - 1) / kLoaders;
-        const int t = threadIdx.x - 32;
-        uint4 v[kPer];
+    if (warp < kProducerWarps) {
+        // ================================================= TMA producers: warp w copies operand w / 2 (K, V),
+        // 64-dim half w % 2; lane b < 8 copies block b of each tile.
+        const int kv = warp >> 1, half = warp & 1;
+        const int b = lane;
+        const bool copier = lane < kBlocksPerTile;
+        const uint32_t ring = sb + (kv ? kSmVRing : kSmKRing) + half * kTileSlab;
+        const uint32_t full0 = bar(kv ? V_FULL : K_FULL);
+        const uint32_t empty0 = bar(kv ? V_EMPTY : K_EMPTY);
+        if (lane == 0) prefetch_tmap(&tmap);
+        // Block ids of tile i come from a register queue filled kIdAhead tiles in advance, so that
+        // the table reads' latency never sits between two tiles' copies.
+        constexpr int kIdAhead = 2;
+        int idq[kIdAhead];
 #pragma unroll
-        for (int u = 0; u < kPer; ++u) {
-            const int c = t + u * kLoaders, r = c >> 4, ch = c & 15;
-            v[u] = make_uint4(0, 0, 0, 0);
-            if (c < kRows * 16 && r < rows)
-                v[u] = __ldg(reinterpret_cast<const uint4*>(
-                                 a.q + ((int64_t)(q0 + qt * kRows + r) * a.num_heads + h) * kHeadDim) + ch);
+        for (int u = 0; u < kIdAhead; ++u) {
+            const int blk = kBlocksPerTile * u + b;
+            idq[u] = copier && u < n && blk < nblk ? __ldg(trow + blk) : 0;
         }
+        int issued = 0;
+        bool stop = false;
+        for (int i0 = 0; i0 < n && !stop; i0 += kIdAhead) {
 #pragma unroll
-        for (int u = 0; u < kPer; ++u) {
-            const int c = t + u * kLoaders, r = c >> 4, ch = c & 15;
-            if (c < kRows * 16)
-                st_shared_v4(sb + kSmQ + (ch >> 3) * kQSlab + r * 128 + (((ch & 7) ^ (r & 7)) << 4), v[u]);
-        }
-        fence_proxy_async_smem();
-        mbar_arrive(bars + 8u * kBarQ);
-    }
-
-    if (warp == 0) {
-        // ================================================= TMA producers: lanes 0-3, one per (pipe, K|V),
-        // each running its own loop (no warp-wide operation in here)
-        if (lane < 4) {
-            const int pipe = lane >> 1, kv = lane & 1;
-            const int base = pipe ? n0 : 0, n = pipe ? nkt - n0 : n0;
-            const uint32_t ring = sb + kSmRing + (pipe * 2 + kv) * kStages * kTileOpBytes;
-            const uint32_t full0 = bar_addr(bars, pipe, kv ? V_FULL : K_FULL);
-            const uint32_t empty0 = bar_addr(bars, pipe, kv ? V_EMPTY : K_EMPTY);
-            if (lane == 0) prefetch_tmap(&tmap);
-            // Block ids of tile j come from a register queue filled kIdAhead tiles in advance, so that
-            // the table reads' latency never sits between two tiles' copies.
-            constexpr int kIdAhead = 4;
-            int idq[kIdAhead][4];
-#pragma unroll
-            for (int u = 0; u < kIdAhead; ++u)
-#pragma unroll
-                for (int b = 0; b < 4; ++b) {
-                    const int blk = 4 * (base + u) + b;
-                    idq[u][b] = u < n && blk < nblk ? __ldg(trow + blk) : 0;
-                }
-            int issued = 0;
-            bool stop = false;
-            for (int j0 = 0; j0 < n && !stop; j0 += kIdAhead) {
-#pragma unroll
-                for (int u = 0; u < kIdAhead; ++u) {
-                    const int j = j0 + u;
-                    if (j >= n || stop) break;
-                    const int st = j % kStages;
-                    const uint32_t ph = (uint32_t)(j / kStages) & 1u;
-                    const int g = base + j;
-                    const int nb = min(4, nblk - 4 * g);
-                    if (j >= kStages && !lane_wait(empty0 + 8 * st, ph ^ 1u, abort, a.status)) {
-                        stop = true;
-                        break;
-                    }
-                    mbar_arrive_expect_tx(full0 + 8 * st, nb * kTileBytes);
-#pragma unroll
-                    for (int b = 0; b < 4; ++b)
-                        if (b < nb)
-                            for (int half = 0; half < 2; ++half)
-                                tma_load_5d(ring + st * kTileOpBytes + half * kTileSlab + b * 2048, &tmap, half * 64,
-                                            0, kv * a.num_heads + h, a.layer, idq[u][b], full0 + 8 * st);
-                    issued = j + 1;
-#pragma unroll
-                    for (int b = 0; b < 4; ++b) {  // refill this slot with tile j + kIdAhead
-                        const int blk = 4 * (g + kIdAhead) + b;
-                        idq[u][b] = j + kIdAhead < n && blk < nblk ? __ldg(trow + blk) : 0;
-                    }
-                }
-            }
-            if (*abort)
-                for (int j = (issued > kStages ? issued - kStages : 0); j < issued; ++j)
-                    mbar_wait(full0 + 8 * (j % kStages), (uint32_t)(j / kStages) & 1u);
-        }
-    } else if (warp < 3) {
-        // ================================================= MMA issuers, one per pipe
-        const int pipe = warp - 1;
-        const int base = pipe ? n0 : 0, n = pipe ? nkt - n0 : n0;
-        const uint32_t tp = tmem + pipe * kPipeCols;
-        const uint32_t kring = sb + kSmRing + (pipe * 2) * kStages * kTileOpBytes;
-        const uint32_t vring = kring + kStages * kTileOpBytes;
-        for (int j = 0; j <= n; ++j) {
-            if (j < n) {
-                const int ks = j % kStages, sbuf = j & 1;
-                if (j == 0 && !flag_wait(bars + 8u * kBarQ, 0, abort, a.status)) break;
-                if (!flag_wait(bar_addr(bars, pipe, K_FULL + ks), (uint32_t)(j / kStages) & 1u, abort, a.status))
+            for (int u = 0; u < kIdAhead; ++u) {
+                const int i = i0 + u;
+                if (i >= n) break;
+                const int st = i % kStages;
+                const uint32_t ph = (uint32_t)(i / kStages) & 1u;
+                const int nb = min(kBlocksPerTile, nblk - kBlocksPerTile * i);
+                if (i >= kStages && !flag_wait(empty0 + 8 * st, ph ^ 1u, abort, a.status)) {
+                    stop = true;
                     break;
-                // S buffer sbuf (and the P that overwrote it) is free once P V of tile j-2 is done
-                if (j >= 2 &&
-                    !flag_wait(bar_addr(bars, pipe, PV_DONE + sbuf), (uint32_t)((j - 2) >> 1) & 1u, abort, a.status))
-                    break;
-                tc_fence_after();
-                if (lane == 0) {
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        tc_mma_f16(tp + kColS + sbuf * 64,
-                                   sw128_desc(sb + kSmQ + (kk >> 2) * kQSlab + (kk & 3) * 32, 16, 1024),
-                                   sw128_desc(kring + ks * kTileOpBytes + (kk >> 2) * kTileSlab + (kk & 3) * 32, 16,
-                                              1024),
-                                   kIdescS, kk > 0);
-                    }
-                    tc_commit(bar_addr(bars, pipe, S_FULL + sbuf));
-                    tc_commit(bar_addr(bars, pipe, K_EMPTY + ks));
                 }
+                if (lane == 0) mbar_arrive_expect_tx(full0 + 8 * st, nb * (kTileBytes / 2));
                 __syncwarp();
+                if (copier && b < nb)
+                    tma_load_5d(ring + st * kTileOpBytes + b * 2048, &tmap, half * 64, 0, kv * a.num_heads + h,
+                                a.layer, idq[u], full0 + 8 * st);
+                issued = i + 1;
+                const int blk = kBlocksPerTile * (i + kIdAhead) + b;  // refill this slot with tile i + kIdAhead
+                idq[u] = copier && i + kIdAhead < n && blk < nblk ? __ldg(trow + blk) : 0;
             }
-            if (j >= 1) {
-                const int i = j - 1, vs = i % kStages, sbuf = i & 1;
-                if (!flag_wait(bar_addr(bars, pipe, P_FULL + sbuf), (uint32_t)(i >> 1) & 1u, abort, a.status)) break;
-                if (!flag_wait(bar_addr(bars, pipe, V_FULL + vs), (uint32_t)(i / kStages) & 1u, abort, a.status))
-                    break;
-                if (base + i == nkt - 1) {
-                    // keys past the last row's position may hold anything (even NaN); zero their V rows so
-                    // that P = 0 times V stays 0 in the tensor core
-                    const int first = pos_max + 1 - (base + i) * kKeys;
-                    for (int c = first * 8 + lane; c < kKeys * 8; c += 32) {
-                        const int r = c >> 3, ch = c & 7;
-                        const uint32_t at = vring + vs * kTileOpBytes + r * 128 + ch * 16;
-                        st_shared_v4(at, make_uint4(0, 0, 0, 0));
-                        st_shared_v4(at + kTileSlab, make_uint4(0, 0, 0, 0));
-                    }
-                    fence_proxy_async_smem();
-                    __syncwarp();
+        }
+        if (warp == 2 && !stop) {
+            // The last tile: keys past the last row's position may hold anything (even NaN), and rows of
+            // blocks past the table's end were not copied at all. Zero those V rows (both halves, once both
+            // have landed) so that P = 0 times V stays 0 in the tensor core, then release the tile.
+            const int i = n - 1, st = i % kStages;
+            if (flag_wait(full0 + 8 * st, (uint32_t)(i / kStages) & 1u, abort, a.status)) {
+                const uint32_t vt = sb + kSmVRing + st * kTileOpBytes;
+                const int first = pos_max + 1 - (n - 1) * kKeys;
+                for (int c = first * 8 + lane; c < kKeys * 8; c += 32) {
+                    const int r = c >> 3, ch = c & 7;
+                    st_shared_v4(vt + r * 128 + ch * 16, make_uint4(0, 0, 0, 0));
+                    st_shared_v4(vt + kTileSlab + r * 128 + ch * 16, make_uint4(0, 0, 0, 0));
                 }
-                tc_fence_after();
-                if (lane == 0) {
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        tc_mma_f16_ts(tp + kColO, tp + kColS + sbuf * 64 + kk * 8,
-                                      sw128_desc(vring + vs * kTileOpBytes + kk * 2048, kTileSlab, 1024), kIdescPV,
-                                      (i > 0 || kk > 0) ? 1u : 0u);
-                    tc_commit(bar_addr(bars, pipe, PV_DONE + sbuf));
-                    tc_commit(bar_addr(bars, pipe, V_EMPTY + vs));
-                }
+                fence_proxy_async_smem();
                 __syncwarp();
+                if (lane == 0) mbar_arrive(bar(V_FIXED));
             }
+        }
+        // copies still in flight (after an abort) must land before the CTA exits
+        for (int i = (issued > kStages ? issued - kStages : 0); i < issued; ++i)
+            mbar_wait(full0 + 8 * (i % kStages), (uint32_t)(i / kStages) & 1u);
+    } else if (warp == kMmaWarp) {
+        // ================================================= MMA issuer (one elected lane).
+        // Order: S_0, S_1, then per tile j: P_j V_j, S_{j+2} (into the buffer P_j V_j just read).
+        const uint32_t kring = sb + kSmKRing, vring = sb + kSmVRing;
+        bool ok = true;
+        auto issue_s = [&](int j) {
+            const int ks = j % kStages, sbuf = j & 1;
+            ok = ok && (j > 0 || flag_wait(bar(Q_READY), 0, abort, a.status)) &&
+                 flag_wait(bar(K_FULL + ks), (uint32_t)(j / kStages) & 1u, abort, a.status) &&
+                 (j < 2 || flag_wait(bar(PV_DONE + sbuf), (uint32_t)((j - 2) >> 1) & 1u, abort, a.status));
+            if (!ok) return;
+            tc_fence_after();
+            if (lane == 0) {
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    tc_mma_f16(tmem + kColS + sbuf * kSBufCols,
+                               sw128_desc(sb + kSmQ + (kk >> 2) * kQSlab + (kk & 3) * 32, 16, 1024),
+                               sw128_desc(kring + ks * kTileOpBytes + (kk >> 2) * kTileSlab + (kk & 3) * 32, 16, 1024),
+                               kIdescS, kk > 0);
+                tc_commit(bar(S_FULL + sbuf));
+                tc_commit(bar(K_EMPTY + ks));
+            }
+            __syncwarp();
+        };
+        issue_s(0);
+        if (n > 1) issue_s(1);
+        for (int j = 0; j < n && ok; ++j) {
+            const int vs = j % kStages, sbuf = j & 1;
+            ok = flag_wait(bar(P_FULL + sbuf), (uint32_t)(j >> 1) & 1u, abort, a.status) &&
+                 (j == n - 1 ? flag_wait(bar(V_FIXED), 0, abort, a.status)
+                             : flag_wait(bar(V_FULL + vs), (uint32_t)(j / kStages) & 1u, abort, a.status));
+            if (!ok) break;
+            tc_fence_after();
+            if (lane == 0) {
+                const uint32_t pcol = tmem + kColS + sbuf * kSBufCols + kColP;
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    tc_mma_f16_ts(tmem + kColO, pcol + kk * 8,
+                                  sw128_desc(vring + vs * kTileOpBytes + kk * 2048, kTileSlab, 1024), kIdescPV,
+                                  (j > 0 || kk > 0) ? 1u : 0u);
+                tc_commit(bar(PV_DONE + sbuf));
+                tc_commit(bar(V_EMPTY + vs));
+            }
+            __syncwarp();
+            if (j + 2 < n) issue_s(j + 2);
         }
         if (lane == 0) {
-            tc_commit(bar_addr(bars, pipe, MMA_DONE));
-            mbar_wait(bar_addr(bars, pipe, MMA_DONE), 0);
+            tc_commit(bar(MMA_DONE));
+            mbar_wait(bar(MMA_DONE), 0);
         }
         __syncwarp();
     } else {
-        // ================================================= softmax: 4 warps per pipe, thread = query row
-        const int pipe = (warp - 3) >> 2;
-        const int base = pipe ? n0 : 0, n = pipe ? nkt - n0 : n0;
+        // ================================================= softmax: thread = query row
         const int qtr = warp & 3;
         const int row = qtr * 32 + lane;
         const bool valid = row < rows;
         const int pos = p0 + row;
-        const uint32_t tl = tmem + pipe * kPipeCols + ((uint32_t)(qtr * 32) << 16);
+        const uint32_t tl = tmem + ((uint32_t)(qtr * 32) << 16);
+        {
+            // ---- Q tile -> shared memory (swizzled, K-major), rows past the chunk zero, while the
+            // producers already fetch the first K/V tiles. Loads first, then stores.
+            constexpr int kPer = kRows * 16 / kSoftmaxThreads;
+            const int t = threadIdx.x - kFirstSoftmaxWarp * 32;
+            uint4 v[kPer];
+#pragma unroll
+            for (int u = 0; u < kPer; ++u) {
+                const int c = t + u * kSoftmaxThreads, r = c >> 4, ch = c & 15;
+                v[u] = make_uint4(0, 0, 0, 0);
+                if (r < rows)
+                    v[u] = __ldg(reinterpret_cast<const uint4*>(
+                                     a.q + ((int64_t)(q0 + qt * kRows + r) * a.num_heads + h) * kHeadDim) +
+                                 ch);
+            }
+#pragma unroll
+            for (int u = 0; u < kPer; ++u) {
+                const int c = t + u * kSoftmaxThreads, r = c >> 4, ch = c & 15;
+                st_shared_v4(sb + kSmQ + (ch >> 3) * kQSlab + r * 128 + (((ch & 7) ^ (r & 7)) << 4), v[u]);
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(bar(Q_READY));
+        }
         float m_used = -INFINITY, l = 0.f;
         bool ok = true;
         for (int j = 0; j < n; ++j) {
             const int sbuf = j & 1;
-            if (!flag_wait(bar_addr(bars, pipe, S_FULL + sbuf), (uint32_t)(j >> 1) & 1u, abort, a.status)) {
+            if (!flag_wait(bar(S_FULL + sbuf), (uint32_t)(j >> 1) & 1u, abort, a.status)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            uint32_t sr[kKeys];
-            tc_ld64(tl + kColS + sbuf * 64, sr);
-            const int key0 = (base + j) * kKeys;
-            if (key0 + kKeys - 1 > p0 || !valid) {
-                // diagonal tile or padding row: keys past the row's position count as -inf
-                const int nvis = valid ? pos - key0 + 1 : 0;
-#pragma unroll
-                for (int e = 0; e < kKeys; ++e)
-                    if (e >= nvis) sr[e] = __float_as_uint(-INFINITY);
-            }
-            float mxs[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) mxs[u] = __uint_as_float(sr[u]);
-#pragma unroll
-            for (int e = 8; e < kKeys; ++e) mxs[e & 7] = fmaxf(mxs[e & 7], __uint_as_float(sr[e]));
-            const float mx = fmaxf(fmaxf(fmaxf(mxs[0], mxs[1]), fmaxf(mxs[2], mxs[3])),
-                                   fmaxf(fmaxf(mxs[4], mxs[5]), fmaxf(mxs[6], mxs[7])));
-            const float m_tile = mx * a.scale_log2;
+            const uint32_t ts = tl + kColS + sbuf * kSBufCols;
+            const int key0 = j * kKeys;
+            // diagonal tile or padding row: keys past the row's position count as -inf
+            const bool diag = !valid || key0 + kKeys - 1 > p0;
+            const int nvis = valid ? pos - key0 + 1 : 0;
+            uint32_t sr[64];
+            tc_ld64(ts, sr);
+            if (diag) mask_tail<64>(sr, nvis);
+            const float mx0 = max64(sr);
+            tc_ld64(ts + 64, sr);
+            if (diag) mask_tail<64>(sr, nvis - 64);
+            const float m_tile = fmaxf(mx0, max64(sr)) * a.scale_log2;
             const bool raise = m_tile > m_used + kRescaleThreshold;  // false while the row has seen no key
             if (j > 0 && __any_sync(0xffffffffu, raise)) {
                 // the previous P V product must have landed before O is rescaled
-                if (!flag_wait(bar_addr(bars, pipe, PV_DONE + ((j - 1) & 1)), (uint32_t)((j - 1) >> 1) & 1u, abort,
-                               a.status)) {
+                if (!flag_wait(bar(PV_DONE + (sbuf ^ 1)), (uint32_t)((j - 1) >> 1) & 1u, abort, a.status)) {
                     ok = false;
                     break;
                 }
@@ -438,78 +454,49 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     float of[32];
-                    uint32_t o[32];
                     tc_ld32(tl + kColO + c * 32, of);
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(of[e] * f);
-                    tc_st32(tl + kColO + c * 32, o);
+                    for (int e = 0; e < 32; ++e) of[e] *= f;
+                    tc_st32(tl + kColO + c * 32, reinterpret_cast<const uint32_t*>(of));
                 }
                 l *= f;
             }
             if (raise) m_used = m_tile;
             // rows that have seen no visible key keep p = 0 (exp2(-inf - -inf) would be NaN)
             const float m_sub = m_used == -INFINITY ? 0.f : m_used;
-            float ls[8];
+            // Quarters of 32 keys, last first: P of keys 32q.. goes to P columns 16q.., i.e. over S
+            // columns 64 + 16q .. 79 + 16q, whose keys belong to a quarter already read.
 #pragma unroll
-            for (int u = 0; u < 8; ++u) ls[u] = 0.f;
-            uint32_t packed[32];
-#pragma unroll
-            for (int e = 0; e < kKeys; e += 2) {
-                const float pa = ex2(fmaf(__uint_as_float(sr[e]), a.scale_log2, -m_sub));
-                const float pb = ex2(fmaf(__uint_as_float(sr[e + 1]), a.scale_log2, -m_sub));
-                ls[e & 7] += pa;
-                ls[(e + 1) & 7] += pb;
-                const __half2 hp = __floats2half2_rn(pa, pb);
-                packed[e >> 1] = *reinterpret_cast<const uint32_t*>(&hp);
+            for (int q = 3; q >= 0; --q) {
+                uint32_t s32[32];
+                tc_ld32(ts + q * 32, reinterpret_cast<float*>(s32));
+                if (diag) mask_tail<32>(s32, nvis - q * 32);
+                softmax_quarter(s32, a.scale_log2, m_sub, l);
+                tc_st16(ts + kColP + q * 16, s32);
             }
-            tc_st32(tl + kColS + sbuf * 64, packed);  // P over the first 32 columns of its S buffer
-            l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
             tc_fence_before();
-            mbar_arrive(bar_addr(bars, pipe, P_FULL + sbuf));
+            mbar_arrive(bar(P_FULL + sbuf));
         }
-        // ---- merge the two pipes: pipe p writes output dims [64p, 64p + 64). Each pipe's (m, l) per row
-        // goes into stage 0 of its own K ring, idle once its last P V product has landed.
-        const bool landed = ok && (n == 0 || flag_wait(bar_addr(bars, pipe, PV_DONE + ((n - 1) & 1)),
-                                                       (uint32_t)((n - 1) >> 1) & 1u, abort, a.status));
-        if (landed) {
-            float2* mine = reinterpret_cast<float2*>(smem + kSmRing + pipe * 2 * kStages * kTileOpBytes);
-            const float2* other = reinterpret_cast<const float2*>(smem + kSmRing + (1 - pipe) * 2 * kStages *
-                                                                                     kTileOpBytes);
-            mine[row] = make_float2(m_used, l);
-            tc_fence_before();
-            mbar_arrive(bars + 8u * kBarLx);
-            if (flag_wait(bars + 8u * kBarLx, 0, abort, a.status)) {
-                tc_fence_after();
-                const float2 s0 = pipe == 0 ? mine[row] : other[row];
-                const float2 s1 = pipe == 0 ? other[row] : mine[row];
-                const float M = fmaxf(s0.x, s1.x);
-                const float w0 = n0 > 0 && s0.x != -INFINITY ? ex2(s0.x - M) : 0.f;
-                const float w1 = nkt - n0 > 0 && s1.x != -INFINITY ? ex2(s1.x - M) : 0.f;
-                const float inv = 1.f / (w0 * s0.y + w1 * s1.y);
-                const uint32_t t0 = tmem + ((uint32_t)(qtr * 32) << 16) + kColO + pipe * 64;
-                uint4* dst = reinterpret_cast<uint4*>(a.out + ((int64_t)(q0 + qt * kRows + row) * a.num_heads + h) *
-                                                                  kHeadDim + pipe * 64);
+        // ---- epilogue: O / l -> FP16 (each row's 256 B written by its thread)
+        if (ok && flag_wait(bar(PV_DONE + ((n - 1) & 1)), (uint32_t)((n - 1) >> 1) & 1u, abort, a.status)) {
+            tc_fence_after();
+            const float inv = 1.f / l;
+            uint4* dst =
+                reinterpret_cast<uint4*>(a.out + ((int64_t)(q0 + qt * kRows + row) * a.num_heads + h) * kHeadDim);
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    float o0[32], o1[32];
+            for (int c = 0; c < 4; ++c) {
+                float o[32];
+                tc_ld32(tl + kColO + c * 32, o);
+                if (valid) {
 #pragma unroll
-                    for (int u = 0; u < 32; ++u) o0[u] = o1[u] = 0.f;
-                    // a pipe that processed no tile never wrote its O: leave it out
-                    if (n0 > 0) tc_ld32(t0 + c * 32, o0);
-                    if (nkt - n0 > 0) tc_ld32(t0 + kPipeCols + c * 32, o1);
-                    if (valid) {
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        uint32_t w[4];
 #pragma unroll
-                        for (int q4 = 0; q4 < 4; ++q4) {
-                            uint32_t w[4];
-#pragma unroll
-                            for (int u = 0; u < 4; ++u) {
-                                const int e = q4 * 8 + 2 * u;
-                                const __half2 hq = __floats2half2_rn(fmaf(w0, o0[e], w1 * o1[e]) * inv,
-                                                                     fmaf(w0, o0[e + 1], w1 * o1[e + 1]) * inv);
-                                w[u] = *reinterpret_cast<const uint32_t*>(&hq);
-                            }
-                            dst[c * 4 + q4] = make_uint4(w[0], w[1], w[2], w[3]);
+                        for (int u = 0; u < 4; ++u) {
+                            const __half2 hq = __floats2half2_rn(o[q4 * 8 + 2 * u] * inv, o[q4 * 8 + 2 * u + 1] * inv);
+                            w[u] = *reinterpret_cast<const uint32_t*>(&hq);
                         }
+                        dst[c * 4 + q4] = make_uint4(w[0], w[1], w[2], w[3]);
                     }
                 }
             }
@@ -519,7 +506,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+    if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
 }
 
 }  // namespace

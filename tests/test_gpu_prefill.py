@@ -93,8 +93,8 @@ def run_step_case(pkv, wl, layers=None, nan_tail=False, use_step=True):
     return errs
 
 
-@pytest.mark.parametrize("ctx,qlen", [(70, 70), (16, 16), (2, 2), (300, 45), (129, 129), (1000, 300),
-                                      (777, 512), (4000, 416)])
+@pytest.mark.parametrize("ctx,qlen", [(70, 70), (16, 16), (2, 2), (64, 64), (300, 45), (129, 129), (200, 200),
+                                      (256, 256), (1000, 300), (777, 512), (4000, 416)])
 def test_prefill_one_sequence(pkv, ctx, qlen):
     run_step_case(pkv, _wl([ctx], [qlen], seed=ctx), use_step=False)
 
