@@ -12,24 +12,29 @@
 // pool, 128 at a time (8 blocks).
 //
 // Tiles are 128 keys: an M=128 N=128 QK^T product keeps the tensor core at
-// its full rate (N=64 runs it at about half). S is double-buffered in tensor
-// memory, so S_{j+1} is computed while the softmax works on S_j; P_j, FP16,
-// overwrites the upper half of its own S buffer and O += P_j V_j reads it
-// from there, so S_{j+2} (same buffer) follows P_j V_j.
+// its full rate (N=64 runs it at about half). Tensor memory holds two S
+// buffers, two P buffers (FP16) and O. The softmax frees S buffer j%2 as soon
+// as it has read S_j, so S_{j+2} is computed while the softmax still works on
+// S_j and never waits for a P V product; P_j goes to P buffer j%2, which
+// P_{j-2} V_{j-2} (two softmax periods earlier) has finished reading, and
+// O += P_j V_j reads it from tensor memory (no shared-memory round trip).
 //
-// Warp roles (288 threads):
-//   warps 0-3    TMA producers: K low / high 64 dims, V low / high; lanes 0-7
-//                each copy one 2 KB box (one block's 16 rows of one 64-dim
-//                half) of every 128-key tile into a 3-stage ring. Four
-//                issuing warps keep the copy engine's request rate off the
-//                critical path.
-//   warp 4       MMA issuer (one elected lane; the warp owns the TMEM
+// Warp roles (256 threads; up to 255 registers a thread, so that a softmax
+// thread keeps its row's 128 S values in registers):
+//   warps 0-2    TMA producers: K low 64 dims (lanes 0-7), K high (lanes
+//                0-7), V both halves (lanes 0-15); each lane copies one 2 KB
+//                box (one block's 16 rows of one 64-dim half) of every
+//                128-key tile into a 3-stage ring. Three issuing warps keep
+//                the copy engine's request rate off the critical path; they
+//                sleep between polls while they wait for a free slot.
+//   warp 3       MMA issuer (one elected lane; the warp owns the TMEM
 //                allocation): S_j = Q K_j^T (A and B from shared memory),
 //                O += P_j V_j (P from tensor memory); completion by
-//                tcgen05.commit.
-//   warps 5-8    softmax: thread r owns query row r (TMEM lane r). Per tile it
-//                reads its 128 S values for the row max, then again by
-//                quarters to write P = 2^(s*scale*log2e - m) and add to the
+//                tcgen05.commit. Order: S_0, S_1, then S_{j+2}, P_j V_j.
+//   warps 4-7    softmax: thread r owns query row r (TMEM lane r). Per tile it
+//                loads its 128 S values into registers (freeing the S
+//                buffer), takes the row max, and writes P =
+//                2^(s*scale*log2e - m) by quarters while adding to the
 //                running sum. The running max m is only raised when the
 //                tile's max exceeds it by more than 8 (a factor 256, far
 //                inside FP16/FP32 range); then the row's O and sum are
@@ -90,11 +95,12 @@ constexpr int kRows = 128;            // query rows per CTA (MMA M)
 constexpr int kKeys = 128;            // keys per tile (8 blocks)
 constexpr int kBlocksPerTile = kKeys / kBlockSize;
 constexpr int kStages = 3;            // K and V ring depth
-constexpr int kProducerWarps = 4;     // K low, K high, V low, V high
-constexpr int kMmaWarp = 4;           // also owns the TMEM allocation
-constexpr int kFirstSoftmaxWarp = 5;
+constexpr int kBufs = 2;              // S buffers and P buffers in tensor memory
+constexpr int kProducerWarps = 3;     // K low, K high, V
+constexpr int kMmaWarp = 3;           // also owns the TMEM allocation
+constexpr int kFirstSoftmaxWarp = 4;
 constexpr int kSoftmaxThreads = 128;
-constexpr int kThreads = (kFirstSoftmaxWarp + 4) * 32;  // 288
+constexpr int kThreads = (kFirstSoftmaxWarp + 4) * 32;  // 256
 constexpr int kQBytes = kRows * kHeadDim * 2;        // 32 KB
 constexpr int kQSlab = kQBytes / 2;                  // 16 KB: 128 rows x 64 halves
 constexpr int kTileOpBytes = kKeys * kHeadDim * 2;   // 32 KB: one 128-key K or V tile
@@ -107,14 +113,15 @@ constexpr int kSmKRing = kQBytes;                             // [stage] K tiles
 constexpr int kSmVRing = kSmKRing + kStages * kTileOpBytes;   // [stage] V tiles
 constexpr int kSmBars = kSmVRing + kStages * kTileOpBytes;
 enum Bar {
-    K_FULL = 0,                   // count 2: both 64-dim halves' producers arm it
-    V_FULL = K_FULL + kStages,    // count 2
+    K_FULL = 0,                   // count 2: the two K producers arm it
+    V_FULL = K_FULL + kStages,
     K_EMPTY = V_FULL + kStages,
     V_EMPTY = K_EMPTY + kStages,
-    S_FULL = V_EMPTY + kStages,   // [2] per S buffer
-    P_FULL = S_FULL + 2,          // [2] count kSoftmaxThreads
-    PV_DONE = P_FULL + 2,         // [2]
-    V_FIXED = PV_DONE + 2,        // the last tile's V rows past the last position are zeroed
+    S_FULL = V_EMPTY + kStages,   // [kBufs] per S buffer
+    S_FREE = S_FULL + kBufs,      // [kBufs] count kSoftmaxThreads: the softmax has read the S buffer
+    P_FULL = S_FREE + kBufs,      // [kBufs] count kSoftmaxThreads
+    PV_DONE = P_FULL + kBufs,     // [kBufs]
+    V_FIXED = PV_DONE + kBufs,    // the last tile's V rows past the last position are zeroed
     Q_READY = V_FIXED + 1,        // count kSoftmaxThreads
     MMA_DONE = Q_READY + 1,
     NUM_BARS = MMA_DONE + 1
@@ -125,13 +132,15 @@ constexpr int kSmBytes = kSmAbort + 12;
 constexpr int kSmAlloc = kSmBytes + 1024;  // slack to align the base
 static_assert(kSmAlloc <= 227 * 1024, "shared memory per CTA");
 
-// TMEM columns: S buffers 0 and 1 (128 fp32 columns each; P, FP16 two per
-// column, overwrites the upper 64 of its buffer), then O (128).
+// TMEM columns: S buffers 0, 1 (128 fp32 columns each), P buffers 0, 1
+// (64 columns each, FP16 two per column), O (128): all 512.
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;
 constexpr uint32_t kSBufCols = 128;
-constexpr uint32_t kColP = 64;  // within an S buffer
-constexpr uint32_t kColO = 256;
+constexpr uint32_t kColP = kBufs * kSBufCols;
+constexpr uint32_t kPBufCols = 64;
+constexpr uint32_t kColO = kColP + kBufs * kPBufCols;
+static_assert(kColO + 128 <= kTmemCols, "tensor memory columns");
 
 // Instruction descriptors, kind::f16: D = F32 (bit 4), A = B = F16,
 // N >> 3 at bit 17, M >> 4 at bit 24; bit 16 makes B MN-major.
@@ -170,6 +179,37 @@ __device__ __forceinline__ bool flag_wait(uint32_t bar, uint32_t parity, volatil
     }
     return ok;
 }
+
+// Bounded wait of a single thread (the MMA issuer's lane runs its loop alone).
+__device__ __forceinline__ bool lane_wait(uint32_t bar, uint32_t parity, volatile int* abort, unsigned int* status)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort) return false;
+    if (mbar_wait(bar, parity)) return true;
+    atomicOr(status, PKV_DEV_TIMEOUT);
+    *abort = 1;
+    return false;
+}
+
+// Bounded wait of a warp off the critical path (a producer waiting for a free ring slot): lane 0
+// polls with a sleep between polls and broadcasts the outcome, so the waiting warp takes almost
+// no issue slots from the softmax and MMA warps that share its scheduler.
+__device__ __forceinline__ bool lazy_wait(uint32_t bar, uint32_t parity, volatile int* abort, unsigned int* status)
+{
+    const int lane = threadIdx.x & 31;
+    int r = 1;  // 1 done, 0 aborted elsewhere, 2 timed out
+    if (lane == 0 && !mbar_try_wait(bar, parity)) r = *abort ? 0 : (mbar_wait_sleep(bar, parity, 256) ? 1 : 2);
+    r = __shfl_sync(0xffffffffu, r, 0);
+    if (r == 2 && lane == 0) {
+        atomicOr(status, PKV_DEV_TIMEOUT);
+        *abort = 1;
+    }
+    return r == 1;
+}
+
+// Shared-memory descriptor of (the operand a descriptor d describes) + off bytes: the start
+// address field is address / 16 in the low 14 bits, and every operand here lies below 256 KB.
+__device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t off) { return d + (uint64_t)(off >> 4); }
 
 // Keys e >= nvis of N S values count as -inf (diagonal tiles and padding rows only).
 template <int N>
@@ -252,12 +292,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) {
             mbar_init(bar(K_FULL + i), 2);
-            mbar_init(bar(V_FULL + i), 2);
+            mbar_init(bar(V_FULL + i), 1);
             mbar_init(bar(K_EMPTY + i), 1);
             mbar_init(bar(V_EMPTY + i), 1);
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kBufs; ++i) {
             mbar_init(bar(S_FULL + i), 1);
+            mbar_init(bar(S_FREE + i), kSoftmaxThreads);
             mbar_init(bar(P_FULL + i), kSoftmaxThreads);
             mbar_init(bar(PV_DONE + i), 1);
         }
@@ -277,11 +318,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kSmTmemSlot);
 
     if (warp < kProducerWarps) {
-        // ================================================= TMA producers: warp w copies operand w / 2 (K, V),
-        // 64-dim half w % 2; lane b < 8 copies block b of each tile.
-        const int kv = warp >> 1, half = warp & 1;
-        const int b = lane;
-        const bool copier = lane < kBlocksPerTile;
+        // ================================================= TMA producers: warps 0, 1 copy K's 64-dim half 0, 1
+        // (lane b < 8: block b of each tile), warp 2 copies V (lane < 16: block lane % 8, half lane / 8).
+        const int kv = warp == 2;
+        const int b = lane & (kBlocksPerTile - 1), half = kv ? lane / kBlocksPerTile : warp;
+        const bool copier = lane < (kv ? 2 : 1) * kBlocksPerTile;
         const uint32_t ring = sb + (kv ? kSmVRing : kSmKRing) + half * kTileSlab;
         const uint32_t full0 = bar(kv ? V_FULL : K_FULL);
         const uint32_t empty0 = bar(kv ? V_EMPTY : K_EMPTY);
@@ -305,11 +346,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                 const int st = i % kStages;
                 const uint32_t ph = (uint32_t)(i / kStages) & 1u;
                 const int nb = min(kBlocksPerTile, nblk - kBlocksPerTile * i);
-                if (i >= kStages && !flag_wait(empty0 + 8 * st, ph ^ 1u, abort, a.status)) {
+                if (i >= kStages && !lazy_wait(empty0 + 8 * st, ph ^ 1u, abort, a.status)) {
                     stop = true;
                     break;
                 }
-                if (lane == 0) mbar_arrive_expect_tx(full0 + 8 * st, nb * (kTileBytes / 2));
+                if (lane == 0) mbar_arrive_expect_tx(full0 + 8 * st, nb * (kv ? kTileBytes : kTileBytes / 2));
                 __syncwarp();
                 if (copier && b < nb)
                     tma_load_5d(ring + st * kTileOpBytes + b * 2048, &tmap, half * 64, 0, kv * a.num_heads + h,
@@ -319,9 +360,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                 idq[u] = copier && i + kIdAhead < n && blk < nblk ? __ldg(trow + blk) : 0;
             }
         }
-        if (warp == 2 && !stop) {
+        if (kv && !stop) {
             // The last tile: keys past the last row's position may hold anything (even NaN), and rows of
-            // blocks past the table's end were not copied at all. Zero those V rows (both halves, once both
+            // blocks past the table's end were not copied at all. Zero those V rows (both halves, once they
             // have landed) so that P = 0 times V stays 0 in the tensor core, then release the tile.
             const int i = n - 1, st = i % kStages;
             if (flag_wait(full0 + 8 * st, (uint32_t)(i / kStages) & 1u, abort, a.status)) {
@@ -341,52 +382,47 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         for (int i = (issued > kStages ? issued - kStages : 0); i < issued; ++i)
             mbar_wait(full0 + 8 * (i % kStages), (uint32_t)(i / kStages) & 1u);
     } else if (warp == kMmaWarp) {
-        // ================================================= MMA issuer (one elected lane).
-        // Order: S_0, S_1, then per tile j: P_j V_j, S_{j+2} (into the buffer P_j V_j just read).
-        const uint32_t kring = sb + kSmKRing, vring = sb + kSmVRing;
-        bool ok = true;
-        auto issue_s = [&](int j) {
-            const int ks = j % kStages, sbuf = j & 1;
-            ok = ok && (j > 0 || flag_wait(bar(Q_READY), 0, abort, a.status)) &&
-                 flag_wait(bar(K_FULL + ks), (uint32_t)(j / kStages) & 1u, abort, a.status) &&
-                 (j < 2 || flag_wait(bar(PV_DONE + sbuf), (uint32_t)((j - 2) >> 1) & 1u, abort, a.status));
-            if (!ok) return;
-            tc_fence_after();
-            if (lane == 0) {
+        // ================================================= MMA issuer: lane 0 alone runs the loop, with
+        // single-thread waits (no warp vote between MMA groups, so the tensor pipe drains less between them).
+        // Order: S_0, S_1, then per tile j: S_{j+2} (once the softmax has read S_j), P_j V_j.
+        if (lane == 0) {
+            // base descriptors; each MMA adds a constant offset (one 64-bit add instead of building a descriptor)
+            const uint64_t dq = sw128_desc(sb + kSmQ, 16, 1024);
+            const uint64_t dk = sw128_desc(sb + kSmKRing, 16, 1024);
+            const uint64_t dv = sw128_desc(sb + kSmVRing, kTileSlab, 1024);
+            bool ok = true;
+            auto issue_s = [&](int j) {
+                const int ks = j % kStages, sbuf = j % kBufs;
+                ok = ok && (j > 0 || lane_wait(bar(Q_READY), 0, abort, a.status)) &&
+                     lane_wait(bar(K_FULL + ks), (uint32_t)(j / kStages) & 1u, abort, a.status) &&
+                     (j < kBufs ||
+                      lane_wait(bar(S_FREE + sbuf), (uint32_t)((j - kBufs) / kBufs) & 1u, abort, a.status));
+                if (!ok) return;
+                tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    tc_mma_f16(tmem + kColS + sbuf * kSBufCols,
-                               sw128_desc(sb + kSmQ + (kk >> 2) * kQSlab + (kk & 3) * 32, 16, 1024),
-                               sw128_desc(kring + ks * kTileOpBytes + (kk >> 2) * kTileSlab + (kk & 3) * 32, 16, 1024),
-                               kIdescS, kk > 0);
+                    tc_mma_f16(tmem + kColS + sbuf * kSBufCols, desc_add(dq, (kk >> 2) * kQSlab + (kk & 3) * 32),
+                               desc_add(dk, ks * kTileOpBytes + (kk >> 2) * kTileSlab + (kk & 3) * 32), kIdescS, kk > 0);
                 tc_commit(bar(S_FULL + sbuf));
                 tc_commit(bar(K_EMPTY + ks));
-            }
-            __syncwarp();
-        };
-        issue_s(0);
-        if (n > 1) issue_s(1);
-        for (int j = 0; j < n && ok; ++j) {
-            const int vs = j % kStages, sbuf = j & 1;
-            ok = flag_wait(bar(P_FULL + sbuf), (uint32_t)(j >> 1) & 1u, abort, a.status) &&
-                 (j == n - 1 ? flag_wait(bar(V_FIXED), 0, abort, a.status)
-                             : flag_wait(bar(V_FULL + vs), (uint32_t)(j / kStages) & 1u, abort, a.status));
-            if (!ok) break;
-            tc_fence_after();
-            if (lane == 0) {
-                const uint32_t pcol = tmem + kColS + sbuf * kSBufCols + kColP;
+            };
+            for (int j = 0; j < kBufs && j < n; ++j) issue_s(j);
+            for (int j = 0; j < n && ok; ++j) {
+                if (j + kBufs < n) issue_s(j + kBufs);
+                const int vs = j % kStages, pbuf = j % kBufs;
+                ok = ok && lane_wait(bar(P_FULL + pbuf), (uint32_t)(j / kBufs) & 1u, abort, a.status) &&
+                     (j == n - 1 ? lane_wait(bar(V_FIXED), 0, abort, a.status)
+                                 : lane_wait(bar(V_FULL + vs), (uint32_t)(j / kStages) & 1u, abort, a.status));
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t pcol = tmem + kColP + pbuf * kPBufCols;
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    tc_mma_f16_ts(tmem + kColO, pcol + kk * 8,
-                                  sw128_desc(vring + vs * kTileOpBytes + kk * 2048, kTileSlab, 1024), kIdescPV,
+                    tc_mma_f16_ts(tmem + kColO, pcol + kk * 8, desc_add(dv, vs * kTileOpBytes + kk * 2048), kIdescPV,
                                   (j > 0 || kk > 0) ? 1u : 0u);
-                tc_commit(bar(PV_DONE + sbuf));
+                tc_commit(bar(PV_DONE + pbuf));
                 tc_commit(bar(V_EMPTY + vs));
             }
-            __syncwarp();
-            if (j + 2 < n) issue_s(j + 2);
-        }
-        if (lane == 0) {
             tc_commit(bar(MMA_DONE));
             mbar_wait(bar(MMA_DONE), 0);
         }
@@ -424,8 +460,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         float m_used = -INFINITY, l = 0.f;
         bool ok = true;
         for (int j = 0; j < n; ++j) {
-            const int sbuf = j & 1;
-            if (!flag_wait(bar(S_FULL + sbuf), (uint32_t)(j >> 1) & 1u, abort, a.status)) {
+            const int sbuf = j % kBufs;
+            if (!flag_wait(bar(S_FULL + sbuf), (uint32_t)(j / kBufs) & 1u, abort, a.status)) {
                 ok = false;
                 break;
             }
@@ -435,50 +471,55 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             // diagonal tile or padding row: keys past the row's position count as -inf
             const bool diag = !valid || key0 + kKeys - 1 > p0;
             const int nvis = valid ? pos - key0 + 1 : 0;
-            uint32_t sr[64];
-            tc_ld64(ts, sr);
-            if (diag) mask_tail<64>(sr, nvis);
-            const float mx0 = max64(sr);
-            tc_ld64(ts + 64, sr);
-            if (diag) mask_tail<64>(sr, nvis - 64);
-            const float m_tile = fmaxf(mx0, max64(sr)) * a.scale_log2;
+            // all of S_j in registers with one load: its buffer is free for S_{j+2} at once
+            uint32_t sr[kKeys];
+            tc_ld128(ts, sr);
+            tc_fence_before();
+            mbar_arrive(bar(S_FREE + sbuf));
+            if (diag) mask_tail<kKeys>(sr, nvis);
+            const float m_tile = fmaxf(max64(sr), max64(sr + 64)) * a.scale_log2;
             const bool raise = m_tile > m_used + kRescaleThreshold;  // false while the row has seen no key
             if (j > 0 && __any_sync(0xffffffffu, raise)) {
                 // the previous P V product must have landed before O is rescaled
-                if (!flag_wait(bar(PV_DONE + (sbuf ^ 1)), (uint32_t)((j - 1) >> 1) & 1u, abort, a.status)) {
+                if (!flag_wait(bar(PV_DONE + (j - 1) % kBufs), (uint32_t)((j - 1) / kBufs) & 1u, abort,
+                               a.status)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 const float f = raise ? ex2(m_used - m_tile) : 1.f;
+#pragma unroll 1
+                for (int c = 0; c < 8; ++c) {  // 16 columns at a time: S_j occupies 128 registers meanwhile
+                    uint32_t o[16];
+                    tc_ld16(tl + kColO + c * 16, o);
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    float of[32];
-                    tc_ld32(tl + kColO + c * 32, of);
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) of[e] *= f;
-                    tc_st32(tl + kColO + c * 32, reinterpret_cast<const uint32_t*>(of));
+                    for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
+                    tc_st16(tl + kColO + c * 16, o);
                 }
                 l *= f;
             }
             if (raise) m_used = m_tile;
             // rows that have seen no visible key keep p = 0 (exp2(-inf - -inf) would be NaN)
             const float m_sub = m_used == -INFINITY ? 0.f : m_used;
-            // Quarters of 32 keys, last first: P of keys 32q.. goes to P columns 16q.., i.e. over S
-            // columns 64 + 16q .. 79 + 16q, whose keys belong to a quarter already read.
-#pragma unroll
-            for (int q = 3; q >= 0; --q) {
-                uint32_t s32[32];
-                tc_ld32(ts + q * 32, reinterpret_cast<float*>(s32));
-                if (diag) mask_tail<32>(s32, nvis - q * 32);
-                softmax_quarter(s32, a.scale_log2, m_sub, l);
-                tc_st16(ts + kColP + q * 16, s32);
+            // P_j goes to P buffer j%2, free once P_{j-2} V_{j-2} is done
+            if (j >= kBufs &&
+                !flag_wait(bar(PV_DONE + sbuf), (uint32_t)((j - kBufs) / kBufs) & 1u, abort, a.status)) {
+                ok = false;
+                break;
             }
+            const uint32_t tp = tl + kColP + sbuf * kPBufCols;
+            // quarters of 32 keys: P of keys 32q.. goes to P columns 16q.., stored without waiting
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                softmax_quarter(sr + q * 32, a.scale_log2, m_sub, l);
+                tc_st16_async(tp + q * 16, sr + q * 32);
+            }
+            tc_wait_st();
             tc_fence_before();
             mbar_arrive(bar(P_FULL + sbuf));
         }
         // ---- epilogue: O / l -> FP16 (each row's 256 B written by its thread)
-        if (ok && flag_wait(bar(PV_DONE + ((n - 1) & 1)), (uint32_t)((n - 1) >> 1) & 1u, abort, a.status)) {
+        if (ok && flag_wait(bar(PV_DONE + (n - 1) % kBufs), (uint32_t)((n - 1) / kBufs) & 1u, abort, a.status)) {
             tc_fence_after();
             const float inv = 1.f / l;
             uint4* dst =
