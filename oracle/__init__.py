@@ -16,8 +16,11 @@ Pins (tests/test_oracle_pins.py): the pages' byte and block arithmetic, the
 exhaustive binary16 table, a one-hot softmax whose output is exactly one V
 row, the uniform-softmax mean, invariance under a permutation of physical
 blocks, brute force against a float64 library attention on tiny inputs,
-chunked prefill against unchunked causal attention, and the split-merge
-identity. Parity is pinned for every function; none is unpinned.
+chunked prefill against unchunked causal attention, the split-merge
+identity, and for grouped-query heads (GQA, MQA) a float64 library attention
+with the K/V heads repeated plus the equality with an MHA pool whose head
+groups hold identical K/V. Parity is pinned for every function; none is
+unpinned.
 """
 from __future__ import annotations
 
@@ -33,7 +36,8 @@ _lib = None
 
 class Geom(ctypes.Structure):
     _fields_ = [("num_blocks", ctypes.c_int64), ("num_layers", ctypes.c_int32),
-                ("num_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("block_size", ctypes.c_int32)]
+                ("num_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("block_size", ctypes.c_int32),
+                ("num_q_heads", ctypes.c_int32)]
 
 
 def lib():
@@ -83,8 +87,16 @@ def _c(a, dtype):
     return np.ascontiguousarray(a, dtype=dtype)
 
 
-def geom(num_blocks, num_layers, num_heads=32, head_dim=128, block_size=16) -> Geom:
-    return Geom(int(num_blocks), int(num_layers), int(num_heads), int(head_dim), int(block_size))
+def geom(num_blocks, num_layers, num_heads=32, head_dim=128, block_size=16, num_q_heads=None) -> Geom:
+    """num_heads: K/V heads stored in the pool; num_q_heads: query heads (default num_heads). Query head h
+    reads K/V head h // (num_q_heads // num_heads) (grouped-query attention; one K/V head for all is MQA)."""
+    return Geom(int(num_blocks), int(num_layers), int(num_heads), int(head_dim), int(block_size),
+                int(num_q_heads or num_heads))
+
+
+def _qh(g: Geom) -> int:
+    """Query heads of a geometry (K/V heads when it has no grouping)."""
+    return g.num_q_heads or g.num_heads
 
 
 # ---------------------------------------------------------------- binary16
@@ -164,8 +176,8 @@ def decode_attn(pool, g: Geom, layer, q, tables, ctx_lens, scale, want_f16=True)
     tables = _c(tables, np.int32)
     ctx = _c(ctx_lens, np.int32)
     B = ctx.shape[0]
-    o64 = np.empty((B, g.num_heads, g.head_dim), np.float64)
-    o16 = np.empty((B, g.num_heads, g.head_dim), np.uint16)
+    o64 = np.empty((B, _qh(g), g.head_dim), np.float64)
+    o16 = np.empty((B, _qh(g), g.head_dim), np.uint16)
     lib().pkvo_decode_attn(_p(pool), ctypes.byref(g), layer, _p(q), _p(tables), tables.shape[1], _p(ctx), B,
                            float(scale), _p(o64), _p(o16))
     return o64, o16
@@ -179,8 +191,8 @@ def prefill_attn(pool, g: Geom, layer, q, q_start, tables, ctx_lens, scale):
     ctx = _c(ctx_lens, np.int32)
     S = ctx.shape[0]
     T = int(qs[-1])
-    o64 = np.zeros((T, g.num_heads, g.head_dim), np.float64)
-    o16 = np.zeros((T, g.num_heads, g.head_dim), np.uint16)
+    o64 = np.zeros((T, _qh(g), g.head_dim), np.float64)
+    o16 = np.zeros((T, _qh(g), g.head_dim), np.uint16)
     lib().pkvo_prefill_attn(_p(pool), ctypes.byref(g), layer, _p(q), _p(qs), _p(tables), tables.shape[1],
                             _p(ctx), S, float(scale), _p(o64), _p(o16))
     return o64, o16
@@ -212,7 +224,7 @@ def decode_attn_split(pool, g: Geom, layer, q, tables, ctx_lens, scale, part_tok
     tables = _c(tables, np.int32)
     ctx = _c(ctx_lens, np.int32)
     B = ctx.shape[0]
-    o64 = np.empty((B, g.num_heads, g.head_dim), np.float64)
+    o64 = np.empty((B, _qh(g), g.head_dim), np.float64)
     lib().pkvo_decode_attn_split(_p(pool), ctypes.byref(g), layer, _p(q), _p(tables), tables.shape[1], _p(ctx), B,
                                  float(scale), int(part_tokens), _p(o64))
     return o64

@@ -33,6 +33,12 @@
  *   split merge         "The inference engine", "IO-aware attention and
  *                       quantization attack different costs": tiles combine
  *                       exactly through their softmax statistics.
+ *   grouped-query heads "Inference Infrastructure" (seeitflow), the KV cache
+ *                       arithmetic: GQA shares one K/V head among a group of
+ *                       query heads, MQA one K/V head among all; the cache
+ *                       holds the K/V heads only. Reading: the group of K/V
+ *                       head k is query heads k*G .. k*G + G-1, G = query
+ *                       heads / K/V heads (query head h reads K/V head h / G).
  */
 #include <math.h>
 #include <stdint.h>
@@ -41,8 +47,13 @@
 
 typedef struct {
     int64_t num_blocks;
-    int32_t num_layers, num_heads, head_dim, block_size;
+    int32_t num_layers, num_heads, head_dim, block_size;  /* num_heads: K/V heads stored in the pool */
+    int32_t num_q_heads;                                  /* query heads; 0 = num_heads (no grouping) */
 } pkvo_geom;
+
+/* Query heads, and the K/V head that query head h reads. */
+static int pkvo_q_heads(const pkvo_geom* g) { return g->num_q_heads > 0 ? g->num_q_heads : g->num_heads; }
+static int pkvo_kv_head(const pkvo_geom* g, int h) { return h / (pkvo_q_heads(g) / g->num_heads); }
 
 /* ---------------------------------------------------------------- binary16 */
 
@@ -199,13 +210,14 @@ void pkvo_attend(const double* q, const double* K, const double* V, int64_t n, i
 }
 
 /* Decode: row r's query (q[r, h, :]) attends positions 0 .. ctx_lens[r]-1 of
- * its own blocks. out_f64 (optional) receives the unrounded result, out_f16
- * (optional) the result rounded once to binary16. Layout [B, heads, dim]. */
+ * its own blocks, through K/V head pkvo_kv_head(h). out_f64 (optional)
+ * receives the unrounded result, out_f16 (optional) the result rounded once
+ * to binary16. Layout [B, query heads, dim]. */
 void pkvo_decode_attn(const uint16_t* pool, const pkvo_geom* g, int layer, const uint16_t* q,
                       const int32_t* tables, int32_t max_blocks, const int32_t* ctx_lens, int32_t B,
                       double scale, double* out_f64, uint16_t* out_f16)
 {
-    const int H = g->num_heads, D = g->head_dim;
+    const int H = pkvo_q_heads(g), D = g->head_dim;
     #pragma omp parallel for collapse(2) schedule(dynamic)
     for (int r = 0; r < B; ++r)
         for (int h = 0; h < H; ++h) {
@@ -214,8 +226,8 @@ void pkvo_decode_attn(const uint16_t* pool, const pkvo_geom* g, int layer, const
             double* V = (double*)malloc(sizeof(double) * (n > 0 ? n : 1) * D);
             double qd[512], o[512];
             const int32_t* table = tables + (int64_t)r * max_blocks;
-            pkvo_gather(pool, g, layer, 0, h, table, n, K);
-            pkvo_gather(pool, g, layer, 1, h, table, n, V);
+            pkvo_gather(pool, g, layer, 0, pkvo_kv_head(g, h), table, n, K);
+            pkvo_gather(pool, g, layer, 1, pkvo_kv_head(g, h), table, n, V);
             for (int d = 0; d < D; ++d) qd[d] = pkvo_half_to_double(q[((int64_t)r * H + h) * D + d]);
             pkvo_attend(qd, K, V, n, D, scale, o);
             for (int d = 0; d < D; ++d) {
@@ -229,14 +241,14 @@ void pkvo_decode_attn(const uint16_t* pool, const pkvo_geom* g, int layer, const
 }
 
 /* Chunked causal prefill: sequence s owns query tokens
- * [q_start[s], q_start[s+1]) of q ([T, heads, dim]); they sit at logical
+ * [q_start[s], q_start[s+1]) of q ([T, query heads, dim]); they sit at logical
  * positions ctx_lens[s] - q_len + i, and query at position p attends keys
- * 0 .. p of its own blocks. */
+ * 0 .. p of its own blocks, through K/V head pkvo_kv_head(h). */
 void pkvo_prefill_attn(const uint16_t* pool, const pkvo_geom* g, int layer, const uint16_t* q,
                        const int32_t* q_start, const int32_t* tables, int32_t max_blocks,
                        const int32_t* ctx_lens, int32_t S, double scale, double* out_f64, uint16_t* out_f16)
 {
-    const int H = g->num_heads, D = g->head_dim;
+    const int H = pkvo_q_heads(g), D = g->head_dim;
     for (int s = 0; s < S; ++s) {
         int64_t n = ctx_lens[s], qlen = q_start[s + 1] - q_start[s];
         const int32_t* table = tables + (int64_t)s * max_blocks;
@@ -245,8 +257,8 @@ void pkvo_prefill_attn(const uint16_t* pool, const pkvo_geom* g, int layer, cons
             double* K = (double*)malloc(sizeof(double) * (n > 0 ? n : 1) * D);
             double* V = (double*)malloc(sizeof(double) * (n > 0 ? n : 1) * D);
             double qd[512], o[512];
-            pkvo_gather(pool, g, layer, 0, h, table, n, K);
-            pkvo_gather(pool, g, layer, 1, h, table, n, V);
+            pkvo_gather(pool, g, layer, 0, pkvo_kv_head(g, h), table, n, K);
+            pkvo_gather(pool, g, layer, 1, pkvo_kv_head(g, h), table, n, V);
             for (int64_t i = 0; i < qlen; ++i) {
                 int64_t tok = q_start[s] + i, pos = n - qlen + i;
                 for (int d = 0; d < D; ++d) qd[d] = pkvo_half_to_double(q[(tok * H + h) * D + d]);
@@ -307,7 +319,7 @@ void pkvo_decode_attn_split(const uint16_t* pool, const pkvo_geom* g, int layer,
                             const int32_t* tables, int32_t max_blocks, const int32_t* ctx_lens, int32_t B,
                             double scale, int64_t part_tokens, double* out_f64)
 {
-    const int H = g->num_heads, D = g->head_dim;
+    const int H = pkvo_q_heads(g), D = g->head_dim;
     #pragma omp parallel for collapse(2) schedule(dynamic)
     for (int r = 0; r < B; ++r)
         for (int h = 0; h < H; ++h) {
@@ -320,8 +332,8 @@ void pkvo_decode_attn_split(const uint16_t* pool, const pkvo_geom* g, int layer,
             double* o = (double*)malloc(sizeof(double) * (P > 0 ? P : 1) * D);
             double qd[512];
             const int32_t* table = tables + (int64_t)r * max_blocks;
-            pkvo_gather(pool, g, layer, 0, h, table, n, K);
-            pkvo_gather(pool, g, layer, 1, h, table, n, V);
+            pkvo_gather(pool, g, layer, 0, pkvo_kv_head(g, h), table, n, K);
+            pkvo_gather(pool, g, layer, 1, pkvo_kv_head(g, h), table, n, V);
             for (int d = 0; d < D; ++d) qd[d] = pkvo_half_to_double(q[((int64_t)r * H + h) * D + d]);
             for (int p = 0; p < P; ++p) {
                 int64_t lo = p * part_tokens, hi = lo + part_tokens < n ? lo + part_tokens : n;

@@ -40,6 +40,9 @@ MUTANTS = {
                              "return 1LL * g->num_layers * g->num_heads * g->head_dim * 2;"),
     "ceil_becomes_floor": ("return (tokens + block_size - 1) / block_size;", "return tokens / block_size;"),
     "partial_exp_drops_scale": ("double p = exp(scale * dot - m);", "double p = exp(dot - m);"),
+    "gqa_heads_interleaved": ("return h / (pkvo_q_heads(g) / g->num_heads);", "return h % g->num_heads;"),
+    "gqa_q_stride_uses_kv_heads": ("    const int H = pkvo_q_heads(g), D = g->head_dim;\n    #pragma omp parallel for collapse(2) schedule(dynamic)\n    for (int r = 0; r < B; ++r)\n        for (int h = 0; h < H; ++h) {\n            int64_t n = ctx_lens[r];\n            double* K",
+                                   "    const int H = g->num_heads, D = g->head_dim;\n    #pragma omp parallel for collapse(2) schedule(dynamic)\n    for (int r = 0; r < B; ++r)\n        for (int h = 0; h < H; ++h) {\n            int64_t n = ctx_lens[r];\n            double* K"),
 }
 
 

@@ -282,6 +282,69 @@ def test_decode_matches_torch_float64_attention():
     assert np.array_equal(o16, oracle.double_to_half(o64))
 
 
+# ------------------------------------------------------------------ grouped-query heads
+# "Inference Infrastructure" (seeitflow), KV cache arithmetic: GQA shares one K/V head among a group of
+# query heads, MQA one K/V head among all. A float64 library attention with the K/V heads repeated
+# (query head h sees K/V head h // group) pins the oracle's grouped path.
+
+def _gqa_case(ctx, hkv, hq, N=40, L=2, seed=11):
+    pool6, _, tables, ctx, _ = _decode_inputs(ctx, N=N, L=L, H=hkv, seed=seed)
+    q = _h(np.random.default_rng(seed + 1).standard_normal((len(ctx), hq, 128)))
+    return pool6, oracle.geom(N, L, hkv, num_q_heads=hq), tables, ctx, q
+
+
+@pytest.mark.parametrize("hkv,hq", [(2, 8), (1, 6), (3, 3)])
+def test_gqa_decode_matches_torch_with_repeated_kv_heads(hkv, hq):
+    pool6, g, tables, ctx, q = _gqa_case([1, 17, 50, 130], hkv, hq)
+    o64, o16 = oracle.decode_attn(pool6, g, 1, q, tables, ctx, SCALE)
+    assert o64.shape == (4, hq, 128)
+    grp = hq // hkv
+    for r, n in enumerate(ctx):
+        K = torch.from_numpy(np.stack([_contig(pool6, 1, 0, k, tables[r], n) for k in range(hkv)]))
+        V = torch.from_numpy(np.stack([_contig(pool6, 1, 1, k, tables[r], n) for k in range(hkv)]))
+        Q = torch.from_numpy(q[r].view(np.float16).astype(np.float64))[:, None]
+        ref = torch.nn.functional.scaled_dot_product_attention(Q, K.repeat_interleave(grp, 0),
+                                                               V.repeat_interleave(grp, 0), scale=SCALE)[:, 0]
+        assert np.allclose(o64[r], ref.numpy(), rtol=1e-12, atol=1e-13)
+    assert np.array_equal(o16, oracle.double_to_half(o64))
+
+
+def test_gqa_equals_mha_with_each_kv_head_repeated():
+    # an MHA pool whose query-head groups hold identical K/V heads gives the grouped result exactly
+    hkv, hq = 2, 6
+    pool6, g, tables, ctx, q = _gqa_case([33, 70], hkv, hq, N=20, L=1, seed=13)
+    mha = np.ascontiguousarray(np.repeat(pool6, hq // hkv, axis=3))
+    gm = oracle.geom(20, 1, hq)
+    a64, a16 = oracle.decode_attn(pool6, g, 0, q, tables, ctx, SCALE)
+    b64, b16 = oracle.decode_attn(mha, gm, 0, q, tables, ctx, SCALE)
+    assert np.array_equal(a64, b64) and np.array_equal(a16, b16)
+    qs = np.array([0, 33, 33 + 70], np.int32)
+    qp = _h(np.random.default_rng(14).standard_normal((103, hq, 128)))
+    c64, c16 = oracle.prefill_attn(pool6, g, 0, qp, qs, tables, ctx, SCALE)
+    d64, d16 = oracle.prefill_attn(mha, gm, 0, qp, qs, tables, ctx, SCALE)
+    assert np.array_equal(c64, d64) and np.array_equal(c16, d16)
+    s64 = oracle.decode_attn_split(pool6, g, 0, q, tables, ctx, SCALE, 32)
+    assert np.allclose(s64, a64, rtol=1e-12, atol=1e-14)
+
+
+def test_gqa_prefill_matches_torch_causal_attention():
+    n, hkv, hq = 70, 2, 8
+    rng = np.random.default_rng(15)
+    pool6 = _pool(12, 1, hkv, 15)
+    table = rng.permutation(12)[: -(-n // 16)].astype(np.int32)
+    q = _h(rng.standard_normal((n, hq, 128)))
+    g = oracle.geom(12, 1, hkv, num_q_heads=hq)
+    o64, _ = oracle.prefill_attn(pool6, g, 0, q, [0, n], table[None], [n], SCALE)
+    mask = torch.ones(n, n, dtype=torch.bool).tril()
+    for h in range(hq):
+        K = torch.from_numpy(_contig(pool6, 0, 0, h // (hq // hkv), table, n))
+        V = torch.from_numpy(_contig(pool6, 0, 1, h // (hq // hkv), table, n))
+        Q = torch.from_numpy(q[:, h].view(np.float16).astype(np.float64))
+        ref = torch.nn.functional.scaled_dot_product_attention(Q[None], K[None], V[None], attn_mask=mask[None],
+                                                               scale=SCALE)[0]
+        assert np.allclose(o64[:, h], ref.numpy(), rtol=1e-12, atol=1e-13)
+
+
 # ------------------------------------------------------------------ prefill
 
 def _prompt_case(n=70, N=12, L=1, H=3, seed=5):
