@@ -13,7 +13,8 @@ with shuffled block ids, N(0,1) FP16 values (synthetic; no dataset).
 Other workloads (--config): long_decode (13 x 8,192), shared_prefix_decode
 (64 rows over 125 shared blocks), mixed_prefill (a 4,000-token prompt in
 512-token chunks next to 31 decode rows; one step = the whole 8-chunk
-schedule, i.e. 8 iterations).
+schedule, i.e. 8 iterations), gqa_decode (32 rows x 2,300 tokens, 8 K/V heads
+serving 32 query heads: 9.65 GB of K/V per step).
 
 Rank 0 prints one JSON line. Under torchrun (N > 1) every rank runs its own
 replica (weak scaling, no collective on the data path); `value` adds all
@@ -53,6 +54,8 @@ def _iterations(config: str, seed: int = 0):
         return [workloads.long_decode(seed)]
     if config == "shared_prefix_decode":
         return [workloads.shared_prefix_decode(seed)]
+    if config == "gqa_decode":
+        return [workloads.gqa_decode(seed)]
     if config == "mixed_prefill":
         first = workloads.mixed_prefill(0, seed=seed)
         return [workloads.mixed_prefill(c, seed=seed) for c in range(first.meta["num_chunks"])]
@@ -67,10 +70,14 @@ CONFIG_TEXT = {
     "shared_prefix_decode": "64 rows sharing 125 ref-counted prefix blocks + 1..300 private tokens, 32 layers",
     "mixed_prefill": "one 4,000-token prompt prefilled in 512-token chunks (8 iterations) next to 31 decode rows "
                      "of context U{100..2000} advancing one token per iteration, 32 layers",
+    "gqa_decode": "batch-32 decode at 2,300 context tokens per row, 32 layers, 8 K/V heads serving 32 query heads "
+                  "(grouped-query attention, 131,072 B of K/V per token), 28,608-block (60 GB) shuffled pool, "
+                  "kv_append of 1 token per row",
 }
 
 KERNEL_SOURCES = {
     "decode_attn": ["pkv_kernels.cu", "ptx.cuh", "pkv_internal.h"],
+    "decode_group_attn": ["pkv_decode_group.cu", "pkv_kernels.cu", "ptx.cuh", "pkv_internal.h"],
     "prefill_attn": ["pkv_prefill.cu", "ptx.cuh", "pkv_internal.h"],
 }
 
@@ -223,29 +230,29 @@ class StepData:
         self.wl = wl
         self.host = [torch.from_numpy(np.ascontiguousarray(x)).pin_memory() for x in (tables, ctx, qs, slots)]
         self.dev = [x.to(dev) for x in self.host]
-        T, H = wl.num_tokens, wl.num_heads
-        self.q = torch.randn((layers, T, H, HEAD_DIM), generator=gen, device=dev).half()
+        T, H, Hq = wl.num_tokens, wl.num_heads, wl.q_heads
+        self.q = torch.randn((layers, T, Hq, HEAD_DIM), generator=gen, device=dev).half()
         self.k = torch.randn((layers, T, H, HEAD_DIM), generator=gen, device=dev).half()
         self.v = torch.randn((layers, T, H, HEAD_DIM), generator=gen, device=dev).half()
         self.out = torch.empty_like(self.q)
         B = wl.num_decode
         self.B = B
         self.max_q = int(wl.q_lens[B:].max()) if wl.num_seqs > B else 0
-        stride = T * H * HEAD_DIM
+        stride, qstride = T * H * HEAD_DIM, T * Hq * HEAD_DIM
         tables_d, ctx_d, qs_d, slots_d = self.dev
         self.desc = pkv.make_step_desc(num_decode=B, num_prefill=wl.num_seqs - B, num_tokens=T, max_q_len=self.max_q,
                                        max_blocks=tables.shape[1], first_layer=0, num_layers=layers, scale=SCALE,
                                        block_tables=tables_d, ctx_lens=ctx_d, q_start_loc=qs_d, slot_mapping=slots_d,
-                                       q=self.q, k=self.k, v=self.v, out=self.out, q_layer_stride=stride,
-                                       k_layer_stride=stride, v_layer_stride=stride, out_layer_stride=stride)
+                                       q=self.q, k=self.k, v=self.v, out=self.out, q_layer_stride=qstride,
+                                       k_layer_stride=stride, v_layer_stride=stride, out_layer_stride=qstride)
         self.ws_bytes = pool.step_workspace_bytes(self.desc)
         # one-layer steps (same kernels as the full step) for per-launch timing of decode-only iterations
         self.layer_desc = [
             pkv.make_step_desc(num_decode=B, num_prefill=0, num_tokens=T, max_q_len=0, max_blocks=tables.shape[1],
                                first_layer=l, num_layers=1, scale=SCALE, block_tables=tables_d, ctx_lens=ctx_d,
                                q_start_loc=qs_d, slot_mapping=slots_d, q=self.q[l], k=self.k[l], v=self.v[l],
-                               out=self.out[l], q_layer_stride=stride, k_layer_stride=stride, v_layer_stride=stride,
-                               out_layer_stride=stride)
+                               out=self.out[l], q_layer_stride=qstride, k_layer_stride=stride,
+                               v_layer_stride=stride, out_layer_stride=qstride)
             for l in range(layers)] if wl.num_seqs == B else None
 
 
@@ -296,12 +303,13 @@ def run_ours(args):
     iters = _iterations(args.config, args.seed)
     wl0 = iters[0]
     L = args.layers or wl0.num_layers
-    H = wl0.num_heads
+    H, Hq = wl0.num_heads, wl0.q_heads
     dev = torch.device("cuda", local)
 
     pool_t = torch.empty(workloads.pool_shape(wl0.num_blocks, L, H), dtype=torch.float16, device=dev)
     workloads.fill_normal_fp16_(pool_t, workloads.value_seed(wl0.seed, "pool"))
-    pool = pkv.Pool(pool_t, wl0.num_blocks, num_layers=L, num_heads=H, partition_tokens=args.partition_tokens)
+    pool = pkv.Pool(pool_t, wl0.num_blocks, num_layers=L, num_heads=H, partition_tokens=args.partition_tokens,
+                    num_q_heads=Hq)
     gen = torch.Generator(device=dev)
     gen.manual_seed(workloads.value_seed(wl0.seed, "q"))
     steps = [StepData(torch, pkv, pool, wl, m, L, dev, gen) for wl, m in zip(iters, _metadata(pkv, iters))]
@@ -340,7 +348,7 @@ def run_ours(args):
     has_decode = any(s.B for s in steps)
     kv_step = sum(kv_bytes(s.wl, L) for s in steps)
     pairs_step = sum(prefill_pairs(s.wl) for s in steps) * L
-    flops_step = 4 * HEAD_DIM * H * pairs_step
+    flops_step = 4 * HEAD_DIM * Hq * pairs_step
     tokens_step = sum(int(s.wl.ctx_lens[:s.B].astype(np.int64).sum()) for s in steps) * L
     launches_step = 0
     for s in steps:
@@ -441,20 +449,23 @@ def run_ours(args):
         unit = "TFLOP/s"
         e2e_value = flops_step * K * ws / (e2e_ms * 1e-3) / 1e12
     n_dec = len(dec_ev)
-    dec_bytes_launch = (kv_step / L / len(steps)) + sum(2 * s.B * H * HEAD_DIM * 2 for s in steps) / len(steps)
+    # K/V context read + q read + out written, per launch
+    dec_bytes_launch = (kv_step / L / len(steps)) + sum(2 * s.B * Hq * HEAD_DIM * 2 for s in steps) / len(steps)
+    dec_kernel = "decode_kernel" if Hq == H else "decode_group_kernel (mma.sync m16n8k16, one K/V read per group)"
+    dec_src = "decode_attn" if Hq == H else "decode_group_attn"
     rooflines = {}
     if n_dec:
         ach = dec_bytes_launch / (dec_ms / n_dec * 1e-3) / 1e9
         rooflines["decode"] = {"bound": "hbm",
-                               "kernel": "decode_kernel (with its split-K merge; decode-only steps: also the decode "
-                                         "rows' kv_append), timed per launch incl. the workspace counter clear",
+                               "kernel": dec_kernel + " (with its split-K merge; decode-only steps: also the "
+                                         "decode rows' kv_append), timed per launch incl. the workspace counter clear",
                                "achieved": round(ach, 1), "peak": hbm_peak, "peak_kind": peak_kind, "unit": "GB/s",
                                "frac": round(ach / hbm_peak, 4),
-                               "traffic": _traffic("decode_attn", args.config),
+                               "traffic": _traffic(dec_src, args.config),
                                "algorithmic_bytes_per_launch": int(dec_bytes_launch),
                                "avg_launch_us": round(dec_ms / n_dec * 1e3, 2)}
     if pre_ev:
-        fl = 4 * HEAD_DIM * H * sum(prefill_pairs(s.wl) for _, _, s in pre_ev)
+        fl = 4 * HEAD_DIM * Hq * sum(prefill_pairs(s.wl) for _, _, s in pre_ev)
         ach = fl / (pre_ms * 1e-3) / 1e12
         rooflines["prefill"] = {"bound": "tensor", "kernel": "prefill_kernel (tcgen05)", "achieved": round(ach, 1),
                                 "peak": tf_peak, "peak_kind": peak_kind + " bf16 dense (fp16 runs at the same rate)",
@@ -483,10 +494,11 @@ def run_ours(args):
         "dtype": "f16 storage, f32 arithmetic",
         "data": "synthetic",
         "config": {"workload": args.config, "description": CONFIG_TEXT[args.config], "num_layers": L,
-                   "iterations_per_step": len(steps), "num_seqs": wl0.num_seqs, "heads": H, "head_dim": HEAD_DIM,
+                   "iterations_per_step": len(steps), "num_seqs": wl0.num_seqs, "heads": H, "query_heads": Hq,
+                   "head_dim": HEAD_DIM,
                    "pool_blocks": wl0.num_blocks, "kv_bytes_per_step": kv_step,
                    "prefill_flops_per_step": flops_step, "seed": wl0.seed,
-                   "partition_tokens": args.partition_tokens or 512,
+                   "partition_tokens": args.partition_tokens or 1024,
                    "max_context": int(max(int(s.wl.ctx_lens.max()) for s in steps)),
                    "l2": "inputs larger than L2 (every step reads the whole KV context of all layers)",
                    "cuda_graph": graph is not None},
@@ -528,13 +540,13 @@ def _layer_sample(wl, layer, pool_t=None, seed=0):
     for r in range(wl.num_seqs):
         tables[r, :nb[r]] = inv[cur:cur + nb[r]]
         cur += nb[r]
-    q = workloads.normal_fp16((wl.num_tokens, wl.num_heads, HEAD_DIM),
+    q = workloads.normal_fp16((wl.num_tokens, wl.q_heads, HEAD_DIM),
                               workloads.value_seed(wl.seed, "q", layer)).numpy()
     return np.ascontiguousarray(mini), tables, q.view(np.uint16), len(uniq)
 
 
 def _oracle_layer(oracle, wl, mini, tables, q, n):
-    g = oracle.geom(n, 1, wl.num_heads)
+    g = oracle.geom(n, 1, wl.num_heads, num_q_heads=wl.q_heads)
     B = wl.num_decode
     if B:
         oracle.decode_attn(mini, g, 0, q[:B], tables[:B], wl.ctx_lens[:B], SCALE)
@@ -563,7 +575,7 @@ def cpu_baseline(wl, pool_t, budget_s, layers):
         res["value"] = round(kv / t_total / 1e9, 3)
     else:
         res["unit"] = "TFLOP/s"
-        res["value"] = round(4 * HEAD_DIM * wl.num_heads * prefill_pairs(wl) * done / t_total / 1e12, 6)
+        res["value"] = round(4 * HEAD_DIM * wl.q_heads * prefill_pairs(wl) * done / t_total / 1e12, 6)
     return res
 
 
@@ -590,7 +602,7 @@ def run_reference(args):
         value, unit = kv_bytes(wl, len(times)) / total / 1e9, "GB/s"
     else:
         metric = "prefill attention TFLOP/s"
-        value, unit = 4 * HEAD_DIM * wl.num_heads * prefill_pairs(wl) * len(times) / total / 1e12, "TFLOP/s"
+        value, unit = 4 * HEAD_DIM * wl.q_heads * prefill_pairs(wl) * len(times) / total / 1e12, "TFLOP/s"
     res = {"impl": "reference", "metric": metric, "value": round(value, 4), "unit": unit, "n_gpus": ws,
            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total / len(times) * 1e3, 2),
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
@@ -609,7 +621,7 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", default="average_decode",
-                    choices=["average_decode", "long_decode", "shared_prefix_decode", "mixed_prefill"])
+                    choices=["average_decode", "long_decode", "shared_prefix_decode", "mixed_prefill", "gqa_decode"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="launch each step directly instead of replaying a CUDA graph")

@@ -65,7 +65,7 @@ enum {
 typedef struct pkv_pool_desc {
     int64_t num_blocks;   /* physical blocks in the pool (7,152 for a 60 GB pool) */
     int32_t num_layers;   /* 32 */
-    int32_t num_heads;    /* 32 (K/V heads = query heads) */
+    int32_t num_heads;    /* K/V heads stored per layer: 32 for the MHA model, 8 for GQA */
     int32_t head_dim;     /* must be 128 */
     int32_t block_size;   /* must be 16 */
     int32_t dtype;        /* must be PKV_DTYPE_FP16 */
@@ -77,6 +77,13 @@ typedef struct pkv_pool_desc {
     size_t bytes;         /* size of that allocation, >= pkv_pool_bytes(desc) */
     const int64_t* free_order; /* optional host array [num_blocks], a permutation: the order in
                                   which blocks are handed out. NULL = 0, 1, 2, ... */
+    int32_t num_q_heads;  /* query heads; 0 = num_heads (MHA). A multiple of num_heads, at most
+                             1,024: each K/V head serves G = num_q_heads / num_heads consecutive
+                             query heads, query head h reading K/V head h / G (grouped-query
+                             attention, "Inference Infrastructure" (seeitflow), the KV cache
+                             arithmetic: 8 K/V heads, 131,072 B per token over 32 layers;
+                             num_heads = 1 is multi-query attention). q and out of the attention
+                             calls are [.., num_q_heads, 128]; k, v and the pool hold num_heads. */
 } pkv_pool_desc;
 
 typedef struct pkv_pool pkv_pool;
@@ -139,7 +146,7 @@ pkv_status pkv_build_step(const pkv_pool* pool, const int64_t* seq_ids, const in
 /* ---------------------------------------------------------------- kernels */
 
 /* reshape_and_cache: write token i's keys k[i] and values v[i] (device FP16,
- * [num_tokens, heads, 128], 16-byte aligned) of layer `layer` into slot
+ * [num_tokens, num_heads, 128], 16-byte aligned) of layer `layer` into slot
  * slot_mapping[i] (device int64) of the pool ("llm-inference-batching",
  * step 7: a row's new keys and values are appended; a row takes a new
  * block every 16 tokens). Slots must be distinct. A slot outside the pool is
@@ -158,18 +165,21 @@ size_t pkv_decode_workspace_bytes(const pkv_pool* pool, int32_t num_seqs, int32_
  * Infrastructure" (seeitflow), the decode steps). Long rows are split into
  * partitions of partition_tokens keys whose softmax statistics are merged
  * exactly ("The inference engine" (wpnews), "IO-aware attention").
- *   q            device FP16 [num_seqs, heads, 128]
+ *   q            device FP16 [num_seqs, num_q_heads, 128]
  *   block_tables device int32 [num_seqs, max_blocks]
  *   ctx_lens     device int32 [num_seqs], 1 <= ctx_len <= 16*max_blocks
- *   out          device FP16 [num_seqs, heads, 128], rounded once (RNE)
+ *   out          device FP16 [num_seqs, num_q_heads, 128], rounded once (RNE)
  *   workspace    device, >= pkv_decode_workspace_bytes(), 256-byte aligned
- * FP32 arithmetic; scale is applied in FP32 (1/sqrt(128) = 0x3DB504F3). */
+ * FP32 arithmetic; scale is applied in FP32 (1/sqrt(128) = 0x3DB504F3).
+ * Pools with num_q_heads > num_heads: one CTA reads each K/V block once for
+ * up to 16 query heads of its group and runs q K^T and P V on the tensor
+ * cores (FP16 operands, P rounded to FP16, FP32 accumulation). */
 pkv_status pkv_decode_attn(pkv_pool* pool, int32_t layer, const void* q, const int32_t* block_tables,
                            int32_t max_blocks, const int32_t* ctx_lens, int32_t num_seqs, float scale, void* out,
                            void* workspace, size_t workspace_bytes, void* stream);
 
 /* Chunked causal prefill: sequence s owns query tokens
- * [q_start_loc[s], q_start_loc[s+1]) of q ([num_tokens, heads, 128] FP16);
+ * [q_start_loc[s], q_start_loc[s+1]) of q ([num_tokens, num_q_heads, 128] FP16);
  * query i sits at position ctx_lens[s] - q_len + i and attends keys 0..that
  * position of s's blocks, which already hold the chunk's own K/V
  * ("llm-inference-batching", "Prefill and decode share each step"; "The
@@ -228,10 +238,10 @@ typedef struct pkv_step_desc {
     const int32_t* ctx_lens;     /* device [B+P] */
     const int32_t* q_start_loc;  /* device [B+P+1], token offsets into the flat list */
     const int64_t* slot_mapping; /* device [T] */
-    const void* q;               /* device FP16 [layers][T][heads][128] */
+    const void* q;               /* device FP16 [layers][T][num_q_heads][128] */
     const void* k;
     const void* v;
-    void* out;                   /* device FP16 [layers][T][heads][128] */
+    void* out;                   /* device FP16 [layers][T][num_q_heads][128] */
     int64_t q_layer_stride, k_layer_stride, v_layer_stride, out_layer_stride; /* elements */
 } pkv_step_desc;
 

@@ -27,7 +27,7 @@ _i32, _i64, _u32, _u64, _f32, _sz = _c.c_int32, _c.c_int64, _c.c_uint32, _c.c_ui
 class pkv_pool_desc(_c.Structure):
     _fields_ = [("num_blocks", _i64), ("num_layers", _i32), ("num_heads", _i32), ("head_dim", _i32),
                 ("block_size", _i32), ("dtype", _i32), ("partition_tokens", _i32), ("dev_base", _P),
-                ("bytes", _sz), ("free_order", _P)]
+                ("bytes", _sz), ("free_order", _P), ("num_q_heads", _i32)]
 
 
 class pkv_step_desc(_c.Structure):
@@ -122,10 +122,13 @@ class Pool:
     bookkeeping calls work without a GPU and its kernel calls are refused."""
 
     def __init__(self, storage, num_blocks: int, num_layers: int = 32, num_heads: int = 32,
-                 partition_tokens: int = 0, free_order=None):
+                 partition_tokens: int = 0, free_order=None, num_q_heads: int = 0):
+        """num_heads: K/V heads stored per layer; num_q_heads: query heads (0 = num_heads), a multiple
+        of num_heads (grouped-query attention: query head h reads K/V head h // (num_q_heads // num_heads))."""
         lib = load()
         self._storage = storage
         self.num_blocks, self.num_layers, self.num_heads = int(num_blocks), int(num_layers), int(num_heads)
+        self.num_q_heads = int(num_q_heads) or self.num_heads
         self._order = None
         if free_order is not None:
             import numpy as np
@@ -133,7 +136,7 @@ class Pool:
         self.desc = pkv_pool_desc(self.num_blocks, self.num_layers, self.num_heads, 128, 16, PKV_DTYPE_FP16,
                                   int(partition_tokens), _ptr(storage),
                                   0 if storage is None else storage.numel() * storage.element_size(),
-                                  None if self._order is None else self._order.ctypes.data)
+                                  None if self._order is None else self._order.ctypes.data, self.num_q_heads)
         h = _P()
         _check(lib.pkv_pool_create(_c.byref(self.desc), _c.byref(h)))
         self.handle = h

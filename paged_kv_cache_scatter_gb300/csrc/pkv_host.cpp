@@ -90,6 +90,9 @@ static bool desc_ok(const pkv_pool_desc* d)
     if (d->head_dim != pkv::kHeadDim || d->block_size != pkv::kBlockSize || d->dtype != PKV_DTYPE_FP16) return false;
     if (d->num_blocks < 1 || d->num_blocks > (int64_t)1 << 31) return false;
     if (d->num_layers < 1 || d->num_layers > 1024 || d->num_heads < 1 || d->num_heads > 256) return false;
+    if (d->num_q_heads != 0 &&
+        (d->num_q_heads < d->num_heads || d->num_q_heads > 1024 || d->num_q_heads % d->num_heads != 0))
+        return false;
     return true;
 }
 
@@ -117,6 +120,8 @@ static bool bind_device(pkv_pool* p)
     p->geom.num_blocks = d->num_blocks;
     p->geom.num_layers = d->num_layers;
     p->geom.num_heads = d->num_heads;
+    p->geom.num_q_heads = d->num_q_heads;
+    p->geom.group = d->num_q_heads / d->num_heads;
     p->geom.kv_bytes = (int64_t)d->num_heads * pkv::kTileBytes;
     p->geom.layer_bytes = 2 * p->geom.kv_bytes;
     p->geom.block_bytes = (int64_t)d->num_layers * p->geom.layer_bytes;
@@ -131,7 +136,8 @@ pkv_status pkv_pool_create(const pkv_pool_desc* d, pkv_pool** out)
     *out = nullptr;
     if (!desc_ok(d))
         return fail(PKV_E_INVALID, "unsupported pool descriptor (need head_dim 128, block_size 16, FP16, "
-                                   "1..1024 layers, 1..256 heads, 1..2^31 blocks)");
+                                   "1..1024 layers, 1..256 K/V heads, 1..2^31 blocks, num_q_heads 0 or a "
+                                   "multiple of num_heads up to 1024)");
     const bool host_only = d->dev_base == nullptr;
     if (!host_only && !aligned(d->dev_base, 256)) return fail(PKV_E_INVALID, "dev_base not 256-byte aligned");
     if (!host_only && d->bytes < pkv_pool_bytes(d))
@@ -144,6 +150,7 @@ pkv_status pkv_pool_create(const pkv_pool_desc* d, pkv_pool** out)
     if (!p) return fail(PKV_E_NOMEM, "host allocation failed");
     p->desc = *d;
     p->desc.free_order = nullptr;
+    if (p->desc.num_q_heads == 0) p->desc.num_q_heads = d->num_heads;
     p->partition_tokens = part;
     p->host_only = host_only;
     if (!host_only && !bind_device(p)) {
@@ -335,7 +342,21 @@ pkv_status pkv_kv_append(pkv_pool* pool, int32_t layer, const void* k, const voi
 size_t pkv_decode_workspace_bytes(const pkv_pool* pool, int32_t num_seqs, int32_t max_blocks)
 {
     if (!pool || num_seqs < 0 || max_blocks < 1) return 0;
-    return pkv::decode_workspace_bytes(num_seqs, pool->desc.num_heads, max_blocks, pool->partition_tokens);
+    return pkv::decode_workspace_bytes(num_seqs, pool->desc.num_q_heads, max_blocks, pool->partition_tokens);
+}
+
+// The one-head decode kernel for MHA pools, the group kernel when K/V heads serve several query heads.
+static cudaError_t launch_decode_any(const pkv_pool* pool, int32_t layer, const void* q, const int32_t* tables,
+                                     int32_t max_blocks, const int32_t* ctx_lens, int32_t num_seqs, float scale,
+                                     void* out, void* ws, const void* k_new, const void* v_new, const int64_t* slots,
+                                     cudaStream_t s)
+{
+    if (pool->geom.group == 1)
+        return pkv::launch_decode(pool->geom, layer, q, tables, max_blocks, ctx_lens, num_seqs, scale, out, ws,
+                                  pool->partition_tokens, k_new, v_new, slots, pool->status_dev, s);
+    const pkv::DecodeWs w = pkv::decode_ws(pool->geom, ws, num_seqs, max_blocks, pool->partition_tokens);
+    return pkv::launch_decode_group(pool->geom, pool->kv_tmap, layer, q, tables, max_blocks, ctx_lens, num_seqs, scale,
+                                    out, w, pool->partition_tokens, k_new, v_new, slots, pool->status_dev, s);
 }
 
 static pkv_status check_decode(pkv_pool* pool, int32_t layer, const void* q, const int32_t* tables, int32_t max_blocks,
@@ -349,12 +370,15 @@ static pkv_status check_decode(pkv_pool* pool, int32_t layer, const void* q, con
     if (num_seqs > 65535) return fail(PKV_E_INVALID, "num_seqs above 65,535");
     if (num_seqs == 0) return PKV_OK;
     if (!q || !tables || !ctx_lens || !out) return fail(PKV_E_INVALID, "NULL q, tables, ctx_lens or out");
+    if (pool->geom.group > 1 && !pool->kv_tmap_ok)
+        return fail(PKV_E_DEVICE, "TMA descriptor for the pool could not be encoded");
     if (!aligned(q, 16) || !aligned(out, 16) || !aligned(tables, 4) || !aligned(ctx_lens, 4))
         return fail(PKV_E_INVALID, "q/out must be 16-byte aligned, tables/ctx_lens 4-byte aligned");
     if (pkv::decode_max_parts(max_blocks, pool->partition_tokens) > pkv::kMaxPartitionsPerRow)
         return fail(PKV_E_INVALID, "block tables of %d blocks need more than %d partitions per row", max_blocks,
                     pkv::kMaxPartitionsPerRow);
-    const size_t need = pkv::decode_workspace_bytes(num_seqs, pool->desc.num_heads, max_blocks, pool->partition_tokens);
+    const size_t need =
+        pkv::decode_workspace_bytes(num_seqs, pool->desc.num_q_heads, max_blocks, pool->partition_tokens);
     if (pkv::decode_max_parts(max_blocks, pool->partition_tokens) > 1) {
         if (!ws || ws_bytes < need || !aligned(ws, 256))
             return fail(PKV_E_INVALID, "workspace NULL, unaligned or below %zu bytes", need);
@@ -375,8 +399,8 @@ pkv_status pkv_decode_attn(pkv_pool* pool, int32_t layer, const void* q, const i
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = pkv::clear_decode_counters(pool->geom, num_seqs, max_blocks, pool->partition_tokens, workspace, s);
     if (e != cudaSuccess) return pkv::cuda_fail(e, "clear decode counters");
-    e = pkv::launch_decode(pool->geom, layer, q, block_tables, max_blocks, ctx_lens, num_seqs, scale, out, workspace,
-                           pool->partition_tokens, nullptr, nullptr, nullptr, pool->status_dev, s);
+    e = launch_decode_any(pool, layer, q, block_tables, max_blocks, ctx_lens, num_seqs, scale, out, workspace, nullptr,
+                          nullptr, nullptr, s);
     return e == cudaSuccess ? PKV_OK : pkv::cuda_fail(e, "decode launch");
 }
 
@@ -404,7 +428,8 @@ pkv_status pkv_prefill_attn(pkv_pool* pool, int32_t layer, const void* q, const 
 size_t pkv_step_workspace_bytes(const pkv_pool* pool, const pkv_step_desc* st)
 {
     if (!pool || !st || st->num_decode < 0 || st->max_blocks < 1) return 0;
-    return pkv::decode_workspace_bytes(st->num_decode, pool->desc.num_heads, st->max_blocks, pool->partition_tokens);
+    return pkv::decode_workspace_bytes(st->num_decode, pool->desc.num_q_heads, st->max_blocks,
+                                       pool->partition_tokens);
 }
 
 pkv_status pkv_step(pkv_pool* pool, const pkv_step_desc* st, void* workspace, size_t workspace_bytes, void* stream)
@@ -424,7 +449,7 @@ pkv_status pkv_step(pkv_pool* pool, const pkv_step_desc* st, void* workspace, si
     if (P > 0 && !st->q_start_loc) return fail(PKV_E_INVALID, "prefill rows need q_start_loc");
     if (st->q_layer_stride % 8 || st->k_layer_stride % 8 || st->v_layer_stride % 8 || st->out_layer_stride % 8)
         return fail(PKV_E_INVALID, "layer strides must be multiples of 8 elements");
-    const int64_t tok = (int64_t)pool->desc.num_heads * pkv::kHeadDim * 2;  // bytes of one token's q/k/v row
+    const int64_t tok = (int64_t)pool->desc.num_heads * pkv::kHeadDim * 2;  // bytes of one token's k or v row
     const char* q = static_cast<const char*>(st->q);
     const char* k = static_cast<const char*>(st->k);
     const char* v = static_cast<const char*>(st->v);
@@ -453,8 +478,8 @@ pkv_status pkv_step(pkv_pool* pool, const pkv_step_desc* st, void* workspace, si
             if (e != cudaSuccess) return pkv::cuda_fail(e, "kv_append launch");
         }
         if (B > 0) {
-            e = pkv::launch_decode(pool->geom, layer, ql, st->block_tables, st->max_blocks, st->ctx_lens, B, st->scale,
-                                   ol, workspace, pool->partition_tokens, kl, vl, st->slot_mapping, pool->status_dev, s);
+            e = launch_decode_any(pool, layer, ql, st->block_tables, st->max_blocks, st->ctx_lens, B, st->scale, ol,
+                                  workspace, kl, vl, st->slot_mapping, s);
             if (e != cudaSuccess) return pkv::cuda_fail(e, "decode launch");
         }
         if (P > 0) {

@@ -32,10 +32,19 @@ struct PoolGeom {
     const char* base;
     int64_t num_blocks;
     int32_t num_layers;
-    int32_t num_heads;
+    int32_t num_heads;    // K/V heads stored per layer
+    int32_t num_q_heads;  // query heads (a multiple of num_heads)
+    int32_t group;        // num_q_heads / num_heads: query head h reads K/V head h / group
     int64_t block_bytes;  // one block, all layers: L * 2 * H * 4096
     int64_t layer_bytes;  // one layer of one block: 2 * H * 4096
     int64_t kv_bytes;     // K half to V half: H * 4096
+};
+
+// Split-K scratch of one decode launch, carved from the caller's workspace.
+struct DecodeWs {
+    float* o;                // [B][num_q_heads][max_parts][128] un-normalised partial outputs
+    float* ml;               // [B][num_q_heads][max_parts][2] partial max and sum
+    unsigned int* counters;  // [B][num_q_heads] arrival counters, zero between launches
 };
 
 struct alignas(64) TensorMap128 {
@@ -68,7 +77,8 @@ cudaError_t status_word(int device, unsigned int** out);
 cudaError_t launch_kv_append(const PoolGeom& g, int layer, const void* k, const void* v, const int64_t* slots,
                              int num_tokens, unsigned int* status, cudaStream_t stream);
 int decode_max_parts(int max_blocks, int partition_tokens);
-size_t decode_workspace_bytes(int num_seqs, int num_heads, int max_blocks, int partition_tokens);
+size_t decode_workspace_bytes(int num_seqs, int num_q_heads, int max_blocks, int partition_tokens);
+DecodeWs decode_ws(const PoolGeom& g, void* ws, int num_seqs, int max_blocks, int partition_tokens);
 // Zero the split-K counters of a decode workspace (they return to zero after every
 // completed launch; this covers the first use and any launch that stopped early).
 cudaError_t clear_decode_counters(const PoolGeom& g, int num_seqs, int max_blocks, int partition_tokens, void* ws,
@@ -78,6 +88,13 @@ cudaError_t launch_decode(const PoolGeom& g, int layer, const void* q, const int
                           const int32_t* ctx_lens, int num_seqs, float scale, void* out, void* ws,
                           int partition_tokens, const void* k_new, const void* v_new, const int64_t* slots,
                           unsigned int* status, cudaStream_t stream);
+
+// pkv_decode_group.cu: decode attention for pools whose K/V heads serve groups of query heads.
+int decode_group_slices(int group);
+cudaError_t launch_decode_group(const PoolGeom& g, const TensorMap128& kv_tmap, int layer, const void* q,
+                                const int32_t* tables, int max_blocks, const int32_t* ctx_lens, int num_seqs,
+                                float scale, void* out, const DecodeWs& ws, int partition_tokens, const void* k_new,
+                                const void* v_new, const int64_t* slots, unsigned int* status, cudaStream_t stream);
 cudaError_t launch_wait_probe(uint64_t timeout_ns, unsigned int* status, cudaStream_t stream);
 
 // pkv_prefill.cu

@@ -446,32 +446,43 @@ struct WsLayout {
     size_t o_bytes, ml_off, ctr_off, total;
 };
 
-WsLayout ws_layout(int num_seqs, int num_heads, int max_blocks, int partition_tokens)
+WsLayout ws_layout(int num_seqs, int num_q_heads, int max_blocks, int partition_tokens)
 {
     const int64_t parts = decode_max_parts(max_blocks, partition_tokens);
-    const int64_t slots = (int64_t)num_seqs * num_heads * parts;
+    const int64_t slots = (int64_t)num_seqs * num_q_heads * parts;
     WsLayout w;
     w.o_bytes = ((size_t)slots * kHeadDim * sizeof(float) + 255) & ~(size_t)255;
     w.ml_off = w.o_bytes;
     w.ctr_off = (w.ml_off + (size_t)slots * 2 * sizeof(float) + 255) & ~(size_t)255;
-    w.total = w.ctr_off + (((size_t)num_seqs * num_heads * sizeof(unsigned int) + 255) & ~(size_t)255);
+    w.total = w.ctr_off + (((size_t)num_seqs * num_q_heads * sizeof(unsigned int) + 255) & ~(size_t)255);
     return w;
 }
 }  // namespace
 
-size_t decode_workspace_bytes(int num_seqs, int num_heads, int max_blocks, int partition_tokens)
+size_t decode_workspace_bytes(int num_seqs, int num_q_heads, int max_blocks, int partition_tokens)
 {
     if (decode_max_parts(max_blocks, partition_tokens) <= 1) return 256;
-    return ws_layout(num_seqs, num_heads, max_blocks, partition_tokens).total;
+    return ws_layout(num_seqs, num_q_heads, max_blocks, partition_tokens).total;
+}
+
+DecodeWs decode_ws(const PoolGeom& g, void* ws, int num_seqs, int max_blocks, int partition_tokens)
+{
+    DecodeWs d{nullptr, nullptr, nullptr};
+    if (decode_max_parts(max_blocks, partition_tokens) <= 1) return d;
+    const WsLayout w = ws_layout(num_seqs, g.num_q_heads, max_blocks, partition_tokens);
+    d.o = static_cast<float*>(ws);
+    d.ml = reinterpret_cast<float*>(static_cast<char*>(ws) + w.ml_off);
+    d.counters = reinterpret_cast<unsigned int*>(static_cast<char*>(ws) + w.ctr_off);
+    return d;
 }
 
 cudaError_t clear_decode_counters(const PoolGeom& g, int num_seqs, int max_blocks, int partition_tokens, void* ws,
                                   cudaStream_t stream)
 {
     if (num_seqs == 0 || decode_max_parts(max_blocks, partition_tokens) <= 1) return cudaSuccess;
-    const WsLayout w = ws_layout(num_seqs, g.num_heads, max_blocks, partition_tokens);
-    return cudaMemsetAsync(static_cast<char*>(ws) + w.ctr_off, 0, (size_t)num_seqs * g.num_heads * sizeof(unsigned int),
-                           stream);
+    const WsLayout w = ws_layout(num_seqs, g.num_q_heads, max_blocks, partition_tokens);
+    return cudaMemsetAsync(static_cast<char*>(ws) + w.ctr_off, 0,
+                           (size_t)num_seqs * g.num_q_heads * sizeof(unsigned int), stream);
 }
 
 cudaError_t launch_decode(const PoolGeom& g, int layer, const void* q, const int32_t* tables, int max_blocks,
@@ -510,15 +521,10 @@ cudaError_t launch_decode(const PoolGeom& g, int layer, const void* q, const int
     a.slots = slots;
     a.append = k_new != nullptr;
     a.status = status;
-    if (a.max_parts > 1) {
-        const WsLayout w = ws_layout(num_seqs, g.num_heads, max_blocks, partition_tokens);
-        a.ws_o = static_cast<float*>(ws);
-        a.ws_ml = reinterpret_cast<float*>(static_cast<char*>(ws) + w.ml_off);
-        a.counters = reinterpret_cast<unsigned int*>(static_cast<char*>(ws) + w.ctr_off);
-    } else {
-        a.ws_o = a.ws_ml = nullptr;
-        a.counters = nullptr;
-    }
+    const DecodeWs w = decode_ws(g, ws, num_seqs, max_blocks, partition_tokens);
+    a.ws_o = w.o;
+    a.ws_ml = w.ml;
+    a.counters = w.counters;
     dim3 grid(a.max_parts, g.num_heads, num_seqs);
     decode_kernel<kDecodeWarps, kDecodeStages><<<grid, kDecodeWarps * 32, Lay::kBytes, stream>>>(a);
     return cudaGetLastError();

@@ -155,7 +155,9 @@ struct PrefillArgs {
     const int32_t* tables;   // [S][max_blocks]
     const int32_t* ctx_lens; // [S]
     int max_blocks;
-    int num_heads;
+    int num_heads;     // K/V heads of the pool
+    int num_q_heads;   // query heads: q and out rows are [num_q_heads][128]
+    int group;         // query heads per K/V head; query head h reads K/V head h / group
     int layer;
     int max_q_len;
     int64_t num_blocks;
@@ -353,7 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                 if (lane == 0) mbar_arrive_expect_tx(full0 + 8 * st, nb * (kv ? kTileBytes : kTileBytes / 2));
                 __syncwarp();
                 if (copier && b < nb)
-                    tma_load_5d(ring + st * kTileOpBytes + b * 2048, &tmap, half * 64, 0, kv * a.num_heads + h,
+                    tma_load_5d(ring + st * kTileOpBytes + b * 2048, &tmap, half * 64, 0, kv * a.num_heads + h / a.group,
                                 a.layer, idq[u], full0 + 8 * st);
                 issued = i + 1;
                 const int blk = kBlocksPerTile * (i + kIdAhead) + b;  // refill this slot with tile i + kIdAhead
@@ -446,7 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                 v[u] = make_uint4(0, 0, 0, 0);
                 if (r < rows)
                     v[u] = __ldg(reinterpret_cast<const uint4*>(
-                                     a.q + ((int64_t)(q0 + qt * kRows + r) * a.num_heads + h) * kHeadDim) +
+                                     a.q + ((int64_t)(q0 + qt * kRows + r) * a.num_q_heads + h) * kHeadDim) +
                                  ch);
             }
 #pragma unroll
@@ -523,7 +525,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             tc_fence_after();
             const float inv = 1.f / l;
             uint4* dst =
-                reinterpret_cast<uint4*>(a.out + ((int64_t)(q0 + qt * kRows + row) * a.num_heads + h) * kHeadDim);
+                reinterpret_cast<uint4*>(a.out + ((int64_t)(q0 + qt * kRows + row) * a.num_q_heads + h) * kHeadDim);
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 float o[32];
@@ -572,6 +574,8 @@ cudaError_t launch_prefill(const pkv_pool* pool, int layer, const void* q, const
     a.ctx_lens = ctx_lens;
     a.max_blocks = max_blocks;
     a.num_heads = pool->geom.num_heads;
+    a.num_q_heads = pool->geom.num_q_heads;
+    a.group = pool->geom.group;
     a.layer = layer;
     a.max_q_len = max_q_len;
     a.num_blocks = pool->geom.num_blocks;
@@ -580,7 +584,7 @@ cudaError_t launch_prefill(const pkv_pool* pool, int layer, const void* q, const
     CUtensorMap tmap;
     static_assert(sizeof(tmap) == sizeof(pool->kv_tmap.bytes), "tensor map size");
     memcpy(&tmap, pool->kv_tmap.bytes, sizeof(tmap));
-    dim3 grid((max_q_len + kRows - 1) / kRows, pool->geom.num_heads, num_seqs);
+    dim3 grid((max_q_len + kRows - 1) / kRows, pool->geom.num_q_heads, num_seqs);
     prefill_kernel<<<grid, kThreads, kSmAlloc, stream>>>(tmap, a);
     return cudaGetLastError();
 }

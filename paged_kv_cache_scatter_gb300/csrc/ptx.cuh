@@ -120,6 +120,44 @@ __device__ __forceinline__ void prefetch_tmap(const void* tmap)
     asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }
 
+// ------------------------------------------------- warp-level tensor-core ops
+
+// Four 8x8 FP16 matrices from shared memory: lane i gives the address of row
+// i % 8 of matrix i / 8; r[j] receives this lane's part of matrix j.
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t* r)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr)
+                 : "memory");
+}
+
+// As ldsm_x4, each matrix transposed.
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t* r)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr)
+                 : "memory");
+}
+
+// d += A (16x16, row-major fragments) * B (16x8, column fragments); FP16
+// inputs, FP32 accumulation.
+__device__ __forceinline__ void mma_16816(float* d, const uint32_t* a, uint32_t b0, uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi)
+{
+    const __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+
 // ---------------------------------------------------------------- helpers
 
 __device__ __forceinline__ void half8_to_float(const uint4& raw, float* f)

@@ -47,13 +47,29 @@ def test_pool_bytes_matches_page_ledger(pkv):
 
 
 @pytest.mark.parametrize("field,value", [("head_dim", 64), ("block_size", 32), ("dtype", 1), ("num_blocks", 0),
-                                         ("partition_tokens", 100), ("partition_tokens", 4096), ("num_heads", 0)])
+                                         ("partition_tokens", 100), ("partition_tokens", 4096), ("num_heads", 0),
+                                         ("num_q_heads", 6), ("num_q_heads", 2), ("num_q_heads", 2048)])
 def test_pool_create_refuses_bad_descriptor(pkv, field, value):
     d = pkv.pkv_pool_desc(16, 2, 4, 128, 16, 0, 0, None, 0, None)
     setattr(d, field, value)
     h = ctypes.c_void_p()
     assert pkv.load().pkv_pool_create(ctypes.byref(d), ctypes.byref(h)) == pkv.PKV_E_INVALID
     assert pkv.load().pkv_last_error_string()
+
+
+def test_grouped_query_pool_ledger_and_workspace(pkv):
+    # "Inference Infrastructure" (seeitflow), KV cache arithmetic: 8 K/V heads x 128 dims x 2 (K and V)
+    # x 2 bytes x 32 layers = 131,072 B per token, 2,097,152 B per 16-token block.
+    assert pkv.Pool.bytes_needed(1, num_heads=8) == 16 * 131072 == oracle.bytes_per_block(oracle.geom(1, 32, 8))
+    gqa = pkv.Pool(None, 64, num_heads=8, num_q_heads=32)
+    mha = pkv.Pool(None, 64, num_heads=32)
+    mqa = pkv.Pool(None, 64, num_heads=1, num_q_heads=32)
+    # split-K partials are per query head: the workspace follows num_q_heads, not the K/V heads
+    for rows, width in [(32, 300), (5, 17), (1, 4)]:
+        assert gqa.decode_workspace_bytes(rows, width) == mha.decode_workspace_bytes(rows, width)
+        assert mqa.decode_workspace_bytes(rows, width) == mha.decode_workspace_bytes(rows, width)
+    assert pkv.Pool(None, 64, num_heads=8, num_q_heads=8).decode_workspace_bytes(32, 300) < \
+        gqa.decode_workspace_bytes(32, 300)
 
 
 def test_free_order_must_be_a_permutation(pkv):

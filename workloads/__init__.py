@@ -49,10 +49,15 @@ class Workload:
     ctx_lens: np.ndarray         # int32 [S]
     q_lens: np.ndarray           # int32 [S]
     seed: int
-    num_heads: int = NUM_HEADS
+    num_heads: int = NUM_HEADS   # K/V heads stored in the pool
     head_dim: int = HEAD_DIM
     block_size: int = BLOCK_SIZE
     meta: dict = field(default_factory=dict)
+    num_q_heads: int = 0         # query heads; 0 = num_heads (grouped-query attention when larger)
+
+    @property
+    def q_heads(self) -> int:
+        return self.num_q_heads or self.num_heads
 
     @property
     def num_seqs(self) -> int:
@@ -205,6 +210,23 @@ def shared_prefix_decode(seed: int = 0, num_layers: int = NUM_LAYERS, num_blocks
     tables = _tables_from_perm(perm[prefix_blocks:], [_blocks_for(x) for x in u], shared=shared)
     return Workload("shared_prefix_decode", num_layers, num_blocks, tables, ctx, np.ones(batch, np.int32), seed,
                     meta={"prefix_blocks": prefix_blocks, "private_tokens": u.tolist()})
+
+
+GQA_KV_HEADS = 8
+GQA_POOL_BLOCKS = 28608     # 60 GB / 2,097,152 B per block (8 K/V heads, 32 layers)
+
+
+def gqa_decode(seed: int = 0, num_layers: int = NUM_LAYERS, num_blocks: int = GQA_POOL_BLOCKS,
+               batch: int = 32, ctx_len: int = 2300, kv_heads: int = GQA_KV_HEADS,
+               q_heads: int = NUM_HEADS) -> Workload:
+    """Grouped-query decode: 32 rows at 2,300 context tokens, 8 K/V heads serving 32 query heads
+    (131,072 B of K/V per token over 32 layers, so one step reads 9.65 GB), shuffled 60 GB pool."""
+    rng = np.random.default_rng(seed)
+    ctx = np.full(batch, ctx_len, dtype=np.int32)
+    perm = rng.permutation(num_blocks).astype(np.int32)
+    tables = _tables_from_perm(perm, [_blocks_for(c) for c in ctx])
+    return Workload("gqa_decode", num_layers, num_blocks, tables, ctx, np.ones(batch, np.int32), seed,
+                    num_heads=kv_heads, num_q_heads=q_heads)
 
 
 def random_step(seed: int, num_seqs: int, max_ctx: int, num_blocks: int, num_layers: int = 1,
