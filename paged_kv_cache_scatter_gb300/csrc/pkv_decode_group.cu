@@ -10,8 +10,9 @@
 // all from one copy of each K/V block (slices = 1 whenever G <= 16, so every
 // K/V byte is read from memory once per group). Its four warps stream the
 // partition's blocks round-robin (warp w takes blocks w, w+4, ...), each with
-// its own two-stage ring filled by TMA (the pool's 5-D tensor map, two
-// 64-dimension halves of 16 rows x 128 B per tile, 128-byte swizzle).
+// its own two-stage ring filled by TMA: one copy per 4 KB K or V tile, whose
+// 16 token rows land as 32 rows of 128 B (token t's dimensions 0-63 in row
+// 2t, 64-127 in row 2t+1) with the 128-byte swizzle.
 //
 // Per block a warp runs the group's attention on the tensor cores with
 // mma.sync m16n8k16 (FP16 operands, FP32 accumulation): S = Q K^T with the R
@@ -39,6 +40,7 @@
 // memory before P V: P is zero there, but the pool may hold anything (even
 // NaN) in unwritten slots, and 0 x NaN would poison the tensor-core sum.
 #include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -99,12 +101,13 @@ struct GroupArgs {
     unsigned int* status;
 };
 
-// Byte offset of 16-byte chunk ch (dimensions 8ch .. 8ch+7) of token t in a K
-// or V tile stored as two 64-dimension halves of 16 rows x 128 B with the
-// 128-byte swizzle: chunk j of row t sits at position j ^ (t % 8).
+// Byte offset of 16-byte chunk ch (dimensions 8ch .. 8ch+7) of token t in a
+// K or V tile in shared memory: row r = 2t + ch / 8 of 128 B, and the
+// 128-byte swizzle puts chunk j of row r at position j ^ (r % 8).
 __device__ __forceinline__ uint32_t sw_off(int t, int ch)
 {
-    return (uint32_t)((ch >> 3) * 2048 + t * 128 + (((ch & 7) ^ (t & 7)) << 4));
+    const int r = 2 * t + (ch >> 3);
+    return (uint32_t)(r * 128 + (((ch & 7) ^ (r & 7)) << 4));
 }
 
 __device__ __forceinline__ unsigned int group_atomic_add_acq_rel(unsigned int* p, unsigned int v)
@@ -165,10 +168,9 @@ __global__ void __launch_bounds__(kGWarps * 32) decode_group_kernel(const __grid
         const int id = ids[warp + li * kGWarps];
         const uint32_t dst = ring + s * kGStage, bar = bar0 + 8 * s;
         mbar_arrive_expect_tx(bar, kGStage);
-        tma_load_5d(dst, &tmap, 0, 0, kvh, a.layer, id, bar);
-        tma_load_5d(dst + 2048, &tmap, 64, 0, kvh, a.layer, id, bar);
-        tma_load_5d(dst + kTileBytes, &tmap, 0, 0, a.num_kv_heads + kvh, a.layer, id, bar);
-        tma_load_5d(dst + kTileBytes + 2048, &tmap, 64, 0, a.num_kv_heads + kvh, a.layer, id, bar);
+        const int tile = a.layer * 2 * a.num_kv_heads + kvh;  // K tile of (layer, head); V is num_kv_heads later
+        tma_load_5d(dst, &tmap, 0, 0, 0, tile, id, bar);
+        tma_load_5d(dst + kTileBytes, &tmap, 0, 0, 0, tile + a.num_kv_heads, id, bar);
     };
     int issued = min(nloc, kGStages);
     if (lane == 0)
@@ -418,6 +420,38 @@ cudaError_t launch_group(const CUtensorMap& tmap, const GroupArgs& a, int num_se
 }
 
 }  // namespace
+
+// Map over the pool seen as [num_blocks][layers * 2 * heads tiles][16 tokens][2 halves][64 dims]:
+// one box is a whole 4 KB tile, copied as 32 rows of 128 B with the 128-byte swizzle.
+bool encode_tile_tmap(const PoolGeom& g, TensorMap128* out, std::string* err)
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+    if (!encode) {
+        cudaDriverEntryPointQueryResult q;
+        void* fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || !fn) {
+            if (err) *err = "cuTensorMapEncodeTiled unavailable";
+            return false;
+        }
+        encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    const cuuint64_t dims[5] = {64, 2, (cuuint64_t)kBlockSize, (cuuint64_t)g.num_layers * 2 * g.num_heads,
+                                (cuuint64_t)g.num_blocks};
+    const cuuint64_t strides[4] = {128, (cuuint64_t)kHeadDim * 2, (cuuint64_t)kTileBytes, (cuuint64_t)g.block_bytes};
+    const cuuint32_t box[5] = {64, 2, (cuuint32_t)kBlockSize, 1, 1};
+    const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    CUresult r = encode(reinterpret_cast<CUtensorMap*>(out->bytes), CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 5,
+                        const_cast<char*>(g.base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        if (err) *err = "cuTensorMapEncodeTiled failed";
+        return false;
+    }
+    return true;
+}
 
 int decode_group_slices(int group)
 {

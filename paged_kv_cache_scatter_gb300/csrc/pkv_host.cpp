@@ -127,6 +127,7 @@ static bool bind_device(pkv_pool* p)
     p->geom.block_bytes = (int64_t)d->num_layers * p->geom.layer_bytes;
     std::string err;
     p->kv_tmap_ok = pkv::encode_kv_tmap(p->geom, &p->kv_tmap, &err);
+    p->tile_tmap_ok = pkv::encode_tile_tmap(p->geom, &p->tile_tmap, &err);
     return true;
 }
 
@@ -355,7 +356,7 @@ static cudaError_t launch_decode_any(const pkv_pool* pool, int32_t layer, const 
         return pkv::launch_decode(pool->geom, layer, q, tables, max_blocks, ctx_lens, num_seqs, scale, out, ws,
                                   pool->partition_tokens, k_new, v_new, slots, pool->status_dev, s);
     const pkv::DecodeWs w = pkv::decode_ws(pool->geom, ws, num_seqs, max_blocks, pool->partition_tokens);
-    return pkv::launch_decode_group(pool->geom, pool->kv_tmap, layer, q, tables, max_blocks, ctx_lens, num_seqs, scale,
+    return pkv::launch_decode_group(pool->geom, pool->tile_tmap, layer, q, tables, max_blocks, ctx_lens, num_seqs, scale,
                                     out, w, pool->partition_tokens, k_new, v_new, slots, pool->status_dev, s);
 }
 
@@ -370,7 +371,7 @@ static pkv_status check_decode(pkv_pool* pool, int32_t layer, const void* q, con
     if (num_seqs > 65535) return fail(PKV_E_INVALID, "num_seqs above 65,535");
     if (num_seqs == 0) return PKV_OK;
     if (!q || !tables || !ctx_lens || !out) return fail(PKV_E_INVALID, "NULL q, tables, ctx_lens or out");
-    if (pool->geom.group > 1 && !pool->kv_tmap_ok)
+    if (pool->geom.group > 1 && !pool->tile_tmap_ok)
         return fail(PKV_E_DEVICE, "TMA descriptor for the pool could not be encoded");
     if (!aligned(q, 16) || !aligned(out, 16) || !aligned(tables, 4) || !aligned(ctx_lens, 4))
         return fail(PKV_E_INVALID, "q/out must be 16-byte aligned, tables/ctx_lens 4-byte aligned");

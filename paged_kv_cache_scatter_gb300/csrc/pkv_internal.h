@@ -62,6 +62,8 @@ struct pkv_pool {
     pkv::PoolGeom geom{};
     pkv::TensorMap128 kv_tmap{};  // 5-D TMA map over the pool (prefill K/V tiles)
     bool kv_tmap_ok = false;
+    pkv::TensorMap128 tile_tmap{};  // TMA map whose box is one whole 4 KB K or V tile (grouped decode)
+    bool tile_tmap_ok = false;
     std::vector<int32_t> ref;
     std::vector<int32_t> free_stack;  // back() is handed out next
     std::unordered_map<int64_t, pkv::Seq> seqs;
@@ -90,6 +92,7 @@ cudaError_t launch_decode(const PoolGeom& g, int layer, const void* q, const int
                           unsigned int* status, cudaStream_t stream);
 
 // pkv_decode_group.cu: decode attention for pools whose K/V heads serve groups of query heads.
+bool encode_tile_tmap(const PoolGeom& g, TensorMap128* out, std::string* err);
 int decode_group_slices(int group);
 cudaError_t launch_decode_group(const PoolGeom& g, const TensorMap128& kv_tmap, int layer, const void* q,
                                 const int32_t* tables, int max_blocks, const int32_t* ctx_lens, int num_seqs,
