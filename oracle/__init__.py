@@ -19,8 +19,13 @@ blocks, brute force against a float64 library attention on tiny inputs,
 chunked prefill against unchunked causal attention, the split-merge
 identity, and for grouped-query heads (GQA, MQA) a float64 library attention
 with the K/V heads repeated plus the equality with an MHA pool whose head
-groups hold identical K/V. Parity is pinned for every function; none is
-unpinned.
+groups hold identical K/V. The 8-bit cache (INT8 codes, one float32 scale per
+(token, head) row) is pinned by the pages' halving of the cache bytes, exact
+round trips of rows built from integer codes and power-of-two scales, the
+half-step error bound and nearest-code rule checked in float64, byte
+placement checked with numpy's own indexing, and attention over exactly
+stored values equal to the FP16 pool's. Parity is pinned for every function;
+none is unpinned.
 """
 from __future__ import annotations
 
@@ -37,7 +42,10 @@ _lib = None
 class Geom(ctypes.Structure):
     _fields_ = [("num_blocks", ctypes.c_int64), ("num_layers", ctypes.c_int32),
                 ("num_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("block_size", ctypes.c_int32),
-                ("num_q_heads", ctypes.c_int32)]
+                ("num_q_heads", ctypes.c_int32), ("dtype", ctypes.c_int32)]
+
+
+FP16, INT8 = 0, 1
 
 
 def lib():
@@ -68,6 +76,9 @@ def lib():
             "pkvo_partial": (None, [P, P, P, i64, i64, ctypes.c_int, dbl, P, P, P]),
             "pkvo_merge": (None, [P, P, P, ctypes.c_int, ctypes.c_int, P]),
             "pkvo_decode_attn_split": (None, [P, G, ctypes.c_int, P, P, i32, P, i32, dbl, i64, P]),
+            "pkvo_i8_tile_bytes": (i64, [G]),
+            "pkvo_i8_quantize_row": (None, [P, ctypes.c_int, P, P]),
+            "pkvo_i8_dequant": (dbl, [ctypes.c_int8, ctypes.c_float]),
             "pkvo_num_threads": (ctypes.c_int, []),
             "pkvo_set_num_threads": (None, [ctypes.c_int]),
         }
@@ -87,11 +98,14 @@ def _c(a, dtype):
     return np.ascontiguousarray(a, dtype=dtype)
 
 
-def geom(num_blocks, num_layers, num_heads=32, head_dim=128, block_size=16, num_q_heads=None) -> Geom:
+def geom(num_blocks, num_layers, num_heads=32, head_dim=128, block_size=16, num_q_heads=None,
+         dtype=FP16) -> Geom:
     """num_heads: K/V heads stored in the pool; num_q_heads: query heads (default num_heads). Query head h
-    reads K/V head h // (num_q_heads // num_heads) (grouped-query attention; one K/V head for all is MQA)."""
+    reads K/V head h // (num_q_heads // num_heads) (grouped-query attention; one K/V head for all is MQA).
+    dtype FP16: the pool is uint16 (binary16 bits); INT8: the pool is bytes, each (block, layer, K/V, head)
+    tile holding 16 x head_dim int8 codes followed by 16 float32 scales."""
     return Geom(int(num_blocks), int(num_layers), int(num_heads), int(head_dim), int(block_size),
-                int(num_q_heads or num_heads))
+                int(num_q_heads or num_heads), int(dtype))
 
 
 def _qh(g: Geom) -> int:
@@ -129,6 +143,30 @@ def pool_bytes(g: Geom) -> int:
     return lib().pkvo_pool_bytes(ctypes.byref(g))
 
 
+def i8_tile_bytes(g: Geom) -> int:
+    return lib().pkvo_i8_tile_bytes(ctypes.byref(g))
+
+
+def i8_quantize_row(x_bits):
+    """(int8 codes, float32 scale) of one row of FP16 values (uint16 bits)."""
+    x = _c(x_bits, np.uint16)
+    codes = np.empty(x.shape[0], np.int8)
+    scale = ctypes.c_float()
+    lib().pkvo_i8_quantize_row(_p(x), x.shape[0], _p(codes), ctypes.byref(scale))
+    return codes, np.float32(scale.value)
+
+
+def i8_dequant(code: int, scale) -> float:
+    return lib().pkvo_i8_dequant(int(code), float(scale))
+
+
+def empty_pool(g: Geom) -> np.ndarray:
+    """A zeroed host pool of the geometry's element type (uint16 for FP16, bytes for INT8)."""
+    if g.dtype == INT8:
+        return np.zeros(pool_bytes(g), np.uint8)
+    return np.zeros(pool_bytes(g) // 2, np.uint16)
+
+
 def blocks_for_tokens(tokens: int, block_size: int = 16) -> int:
     return lib().pkvo_blocks_for_tokens(int(tokens), int(block_size))
 
@@ -146,8 +184,9 @@ def slots(tables, row_of_token, positions, block_size=16) -> np.ndarray:
 # ------------------------------------------------------------ the kernels
 
 def kv_append(pool: np.ndarray, g: Geom, layer: int, k, v, slot_mapping) -> int:
-    """In-place on ``pool`` (uint16 view of FP16). Returns -1 or the first bad token index."""
-    assert pool.dtype == np.uint16 and pool.flags.c_contiguous
+    """In-place on ``pool`` (uint16 view of FP16, or bytes for an INT8 geometry). Returns -1 or the first
+    bad token index. k and v are FP16 bits [T, num_heads, head_dim]; an INT8 pool stores them quantised."""
+    assert pool.dtype == (np.uint8 if g.dtype == INT8 else np.uint16) and pool.flags.c_contiguous
     k = _c(k, np.uint16)
     v = _c(v, np.uint16)
     s = _c(slot_mapping, np.int64)

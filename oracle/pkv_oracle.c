@@ -39,6 +39,17 @@
  *                       holds the K/V heads only. Reading: the group of K/V
  *                       head k is query heads k*G .. k*G + G-1, G = query
  *                       heads / K/V heads (query head h reads K/V head h / G).
+ *   8-bit cache         "Inference Infrastructure", the KV cache arithmetic
+ *                       (8 bits per element halve the cache) and "The
+ *                       inference engine", "IO-aware attention and
+ *                       quantization attack different costs" (scales are
+ *                       metadata carried with the data). Reading (the pages
+ *                       fix no scale rule): INT8, symmetric, one FP32 scale
+ *                       per (token, head) vector of K or V, scale =
+ *                       max|x| / 127 and code = round-half-even(x / scale),
+ *                       both in IEEE single precision; the stored value is
+ *                       code * scale in single precision. A tile holds the
+ *                       16 x head_dim codes, then the 16 scales.
  */
 #include <math.h>
 #include <stdint.h>
@@ -49,7 +60,10 @@ typedef struct {
     int64_t num_blocks;
     int32_t num_layers, num_heads, head_dim, block_size;  /* num_heads: K/V heads stored in the pool */
     int32_t num_q_heads;                                  /* query heads; 0 = num_heads (no grouping) */
+    int32_t dtype;                                        /* 0: FP16 elements, 1: INT8 codes + FP32 scales */
 } pkvo_geom;
+
+enum { PKVO_FP16 = 0, PKVO_INT8 = 1 };
 
 /* Query heads, and the K/V head that query head h reads. */
 static int pkvo_q_heads(const pkvo_geom* g) { return g->num_q_heads > 0 ? g->num_q_heads : g->num_heads; }
@@ -104,6 +118,8 @@ void pkvo_doubles_to_halves(const double* in, uint16_t* out, int64_t n)
 
 int64_t pkvo_bytes_per_token(const pkvo_geom* g)
 {
+    if (g->dtype == PKVO_INT8)  /* one byte per element plus one 4-byte scale per (layer, K/V, head) row */
+        return 2LL * g->num_layers * g->num_heads * (g->head_dim + 4);
     return 2LL * g->num_layers * g->num_heads * g->head_dim * 2;
 }
 
@@ -151,11 +167,26 @@ void pkvo_slots(const int32_t* tables, int32_t max_blocks, const int32_t* row_of
 /* Write token i's K row (all heads) and V row to the slot slots[i]. Returns
  * the index of the first out-of-range slot, or -1 when all were written.
  * Slots are checked before anything is written. */
-int64_t pkvo_kv_append(uint16_t* pool, const pkvo_geom* g, int layer, const uint16_t* k,
+static void pkvo_i8_append_row(uint8_t* pool, const pkvo_geom* g, int64_t b, int layer, int kv, int h, int t,
+                               const uint16_t* x);
+
+int64_t pkvo_kv_append(void* pool_v, const pkvo_geom* g, int layer, const uint16_t* k,
                        const uint16_t* v, const int64_t* slots, int64_t T)
 {
+    uint16_t* pool = (uint16_t*)pool_v;
     for (int64_t i = 0; i < T; ++i)
         if (slots[i] < 0 || slots[i] >= g->num_blocks * g->block_size) return i;
+    if (g->dtype == PKVO_INT8) {
+        for (int64_t i = 0; i < T; ++i)
+            for (int h = 0; h < g->num_heads; ++h) {
+                int64_t src = (i * g->num_heads + h) * g->head_dim;
+                pkvo_i8_append_row((uint8_t*)pool_v, g, slots[i] / g->block_size, layer, 0, h,
+                                   (int)(slots[i] % g->block_size), k + src);
+                pkvo_i8_append_row((uint8_t*)pool_v, g, slots[i] / g->block_size, layer, 1, h,
+                                   (int)(slots[i] % g->block_size), v + src);
+            }
+        return -1;
+    }
     for (int64_t i = 0; i < T; ++i) {
         int64_t b = slots[i] / g->block_size;
         int t = (int)(slots[i] % g->block_size);
@@ -174,9 +205,17 @@ int64_t pkvo_kv_append(uint16_t* pool, const pkvo_geom* g, int layer, const uint
 /* Contiguous [seq_len, head_dim] copy of one head's K (kv = 0) or V (kv = 1):
  * the full blocks in table order, then the first seq_len % 16 rows of the
  * next block. */
-void pkvo_gather(const uint16_t* pool, const pkvo_geom* g, int layer, int kv, int head,
+static void pkvo_i8_gather(const uint8_t* pool, const pkvo_geom* g, int layer, int kv, int head,
+                           const int32_t* table, int64_t seq_len, double* out);
+
+void pkvo_gather(const void* pool_v, const pkvo_geom* g, int layer, int kv, int head,
                  const int32_t* table, int64_t seq_len, double* out)
 {
+    const uint16_t* pool = (const uint16_t*)pool_v;
+    if (g->dtype == PKVO_INT8) {
+        pkvo_i8_gather((const uint8_t*)pool_v, g, layer, kv, head, table, seq_len, out);
+        return;
+    }
     int64_t full = seq_len / g->block_size, rem = seq_len % g->block_size, row = 0;
     for (int64_t i = 0; i < full; ++i)
         for (int t = 0; t < g->block_size; ++t, ++row)
@@ -213,7 +252,7 @@ void pkvo_attend(const double* q, const double* K, const double* V, int64_t n, i
  * its own blocks, through K/V head pkvo_kv_head(h). out_f64 (optional)
  * receives the unrounded result, out_f16 (optional) the result rounded once
  * to binary16. Layout [B, query heads, dim]. */
-void pkvo_decode_attn(const uint16_t* pool, const pkvo_geom* g, int layer, const uint16_t* q,
+void pkvo_decode_attn(const void* pool, const pkvo_geom* g, int layer, const uint16_t* q,
                       const int32_t* tables, int32_t max_blocks, const int32_t* ctx_lens, int32_t B,
                       double scale, double* out_f64, uint16_t* out_f16)
 {
@@ -244,7 +283,7 @@ void pkvo_decode_attn(const uint16_t* pool, const pkvo_geom* g, int layer, const
  * [q_start[s], q_start[s+1]) of q ([T, query heads, dim]); they sit at logical
  * positions ctx_lens[s] - q_len + i, and query at position p attends keys
  * 0 .. p of its own blocks, through K/V head pkvo_kv_head(h). */
-void pkvo_prefill_attn(const uint16_t* pool, const pkvo_geom* g, int layer, const uint16_t* q,
+void pkvo_prefill_attn(const void* pool, const pkvo_geom* g, int layer, const uint16_t* q,
                        const int32_t* q_start, const int32_t* tables, int32_t max_blocks,
                        const int32_t* ctx_lens, int32_t S, double scale, double* out_f64, uint16_t* out_f16)
 {
@@ -273,6 +312,81 @@ void pkvo_prefill_attn(const uint16_t* pool, const pkvo_geom* g, int layer, cons
             free(V);
         }
     }
+}
+
+/* ----------------------------------------------------------- 8-bit cache */
+
+/* Bytes of one (block, layer, K/V, head) tile: the codes [16][head_dim], then 16 FP32 scales. */
+int64_t pkvo_i8_tile_bytes(const pkvo_geom* g)
+{
+    return (int64_t)g->block_size * g->head_dim + 4LL * g->block_size;
+}
+
+/* Byte offset of tile (b, l, kv, h) in the pool. */
+static int64_t i8_tile(const pkvo_geom* g, int64_t b, int l, int kv, int h)
+{
+    int64_t tiles_before = ((b * g->num_layers + l) * 2 + kv) * g->num_heads + h;
+    return tiles_before * pkvo_i8_tile_bytes(g);
+}
+
+/* Quantise one row of n FP16 values: amax = max |x|, scale = amax / 127 and
+ * code = round-half-even(x / scale) clamped to [-127, 127], all in IEEE single
+ * precision (each operation rounded to float); a row of zeros has scale 0 and
+ * codes 0. Inputs must be finite. */
+void pkvo_i8_quantize_row(const uint16_t* x, int n, int8_t* codes, float* scale_out)
+{
+    float amax = 0.0f;
+    for (int i = 0; i < n; ++i) {
+        float a = (float)fabs(pkvo_half_to_double(x[i]));  /* binary16 -> float is exact */
+        if (a > amax) amax = a;
+    }
+    float scale = (float)(amax / 127.0f);
+    for (int i = 0; i < n; ++i) {
+        int c = 0;
+        if (amax > 0.0f) {
+            float qv = (float)((float)pkvo_half_to_double(x[i]) / scale);
+            c = (int)rintf(qv);  /* default rounding mode: to nearest, ties to even */
+            if (c > 127) c = 127;
+            if (c < -127) c = -127;
+        }
+        codes[i] = (int8_t)c;
+    }
+    *scale_out = scale;
+}
+
+/* The stored value of a code: code * scale, rounded to float. */
+double pkvo_i8_dequant(int8_t code, float scale)
+{
+    return (double)(float)((float)code * scale);
+}
+
+static void pkvo_i8_append_row(uint8_t* pool, const pkvo_geom* g, int64_t b, int layer, int kv, int h, int t,
+                               const uint16_t* x)
+{
+    int8_t codes[512];
+    float scale;
+    pkvo_i8_quantize_row(x, g->head_dim, codes, &scale);
+    uint8_t* tile = pool + i8_tile(g, b, layer, kv, h);
+    memcpy(tile + (int64_t)t * g->head_dim, codes, (size_t)g->head_dim);
+    memcpy(tile + (int64_t)g->block_size * g->head_dim + 4LL * t, &scale, 4);
+}
+
+static double i8_value(const uint8_t* pool, const pkvo_geom* g, int64_t b, int layer, int kv, int h, int t, int d)
+{
+    const uint8_t* tile = pool + i8_tile(g, b, layer, kv, h);
+    float scale;
+    memcpy(&scale, tile + (int64_t)g->block_size * g->head_dim + 4LL * t, 4);
+    return pkvo_i8_dequant((int8_t)tile[(int64_t)t * g->head_dim + d], scale);
+}
+
+/* As pkvo_gather, reading codes and scales and returning the stored values. */
+static void pkvo_i8_gather(const uint8_t* pool, const pkvo_geom* g, int layer, int kv, int head,
+                           const int32_t* table, int64_t seq_len, double* out)
+{
+    for (int64_t j = 0; j < seq_len; ++j)
+        for (int d = 0; d < g->head_dim; ++d)
+            out[j * g->head_dim + d] =
+                i8_value(pool, g, table[j / g->block_size], layer, kv, head, (int)(j % g->block_size), d);
 }
 
 /* ------------------------------------------------------------- split merge */
@@ -315,7 +429,7 @@ void pkvo_merge(const double* m, const double* l, const double* o, int P, int di
 }
 
 /* Decode attention computed as partitions of part_tokens keys, then merged. */
-void pkvo_decode_attn_split(const uint16_t* pool, const pkvo_geom* g, int layer, const uint16_t* q,
+void pkvo_decode_attn_split(const void* pool, const pkvo_geom* g, int layer, const uint16_t* q,
                             const int32_t* tables, int32_t max_blocks, const int32_t* ctx_lens, int32_t B,
                             double scale, int64_t part_tokens, double* out_f64)
 {

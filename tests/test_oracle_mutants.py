@@ -41,6 +41,13 @@ MUTANTS = {
     "ceil_becomes_floor": ("return (tokens + block_size - 1) / block_size;", "return tokens / block_size;"),
     "partial_exp_drops_scale": ("double p = exp(scale * dot - m);", "double p = exp(dot - m);"),
     "gqa_heads_interleaved": ("return h / (pkvo_q_heads(g) / g->num_heads);", "return h % g->num_heads;"),
+    "i8_reads_scale_of_token0": ("memcpy(&scale, tile + (int64_t)g->block_size * g->head_dim + 4LL * t, 4);\n    return",
+                                 "memcpy(&scale, tile + (int64_t)g->block_size * g->head_dim, 4);\n    return"),
+    "i8_amax_signed": ("float a = (float)fabs(pkvo_half_to_double(x[i]));",
+                       "float a = (float)pkvo_half_to_double(x[i]);"),
+    "i8_code_truncates": ("c = (int)rintf(qv);", "c = (int)qv;"),
+    "i8_tile_head_before_kv": ("((b * g->num_layers + l) * 2 + kv) * g->num_heads + h;",
+                               "((b * g->num_layers + l) * g->num_heads + h) * 2 + kv;"),
     "gqa_q_stride_uses_kv_heads": ("    const int H = pkvo_q_heads(g), D = g->head_dim;\n    #pragma omp parallel for collapse(2) schedule(dynamic)\n    for (int r = 0; r < B; ++r)\n        for (int h = 0; h < H; ++h) {\n            int64_t n = ctx_lens[r];\n            double* K",
                                    "    const int H = g->num_heads, D = g->head_dim;\n    #pragma omp parallel for collapse(2) schedule(dynamic)\n    for (int r = 0; r < B; ++r)\n        for (int h = 0; h < H; ++h) {\n            int64_t n = ctx_lens[r];\n            double* K"),
 }

@@ -480,3 +480,160 @@ def test_blockmgr_lifo_reuse_and_invalid_calls():
     assert bm.free_seq(7) == blockmgr.E_INVALID
     assert bm.grow(1, 3) == blockmgr.E_INVALID          # sequences only grow
     assert bm.share_prefix(2, 1, 2) == blockmgr.E_INVALID  # only full blocks that exist
+
+
+# ------------------------------------------------------------------ 8-bit cache
+# Reading (the pages fix no scale rule): INT8 codes, one float32 scale per (token, head) row of K or V,
+# scale = max|x| / 127, code = round-half-even(x / scale); the stored value is code * scale.
+
+def test_int8_codes_halve_the_pages_cache_figure():
+    # "Inference Infrastructure" (seeitflow), KV cache arithmetic: 8 bits per element halve the cache, the
+    # 512 MiB of a 4,096-token sequence (32 layers, 8 K/V heads, 128 dims) becoming 256 MiB. The scales
+    # (4 B per row of 128 codes) are metadata on top ("The inference engine", quantisation costs).
+    g16 = oracle.geom(1, 32, 8)
+    g8 = oracle.geom(1, 32, 8, dtype=oracle.INT8)
+    tile = oracle.i8_tile_bytes(g8)
+    assert tile == 16 * 128 + 16 * 4
+    code_bytes_per_token = 2 * 32 * 8 * (tile - 16 * 4) // 16
+    assert code_bytes_per_token * 2 == oracle.bytes_per_token(g16) == 131072
+    assert code_bytes_per_token * 4096 == 256 * 2**20
+    assert oracle.bytes_per_token(g8) - code_bytes_per_token == 2 * 32 * 8 * 4
+    # the 32-head model's 60 GB pool: 4,325,376 B per block, 13,871 blocks (7,152 at FP16)
+    m8 = oracle.geom(1, 32, 32, dtype=oracle.INT8)
+    assert oracle.bytes_per_block(m8) == 32 * 2 * 32 * tile == 4325376
+    assert 60_000_000_000 // oracle.bytes_per_block(m8) == 13871
+
+
+def _exact_rows(rng, n_rows, D=128, kmin=0, kmax=8):
+    """Rows x = c * 2^-k with integer |c| <= 127 and max |c| = 127: exactly representable in FP16 and
+    exactly recoverable from an INT8 code and a power-of-two scale."""
+    c = rng.integers(-127, 128, (n_rows, D))
+    c[np.arange(n_rows), rng.integers(0, D, n_rows)] = rng.choice([-127, 127], n_rows)
+    k = rng.integers(kmin, kmax + 1, n_rows)
+    s = np.ldexp(1.0, -k)
+    x = (c * s[:, None]).astype(np.float16)
+    assert np.array_equal(x.astype(np.float64), c * s[:, None])
+    return x, c.astype(np.int8), s.astype(np.float32)
+
+
+def test_int8_quantise_exactly_representable_rows():
+    rng = np.random.default_rng(0)
+    x, c, s = _exact_rows(rng, 200)
+    for i in range(200):
+        codes, scale = oracle.i8_quantize_row(x[i].view(np.uint16))
+        assert scale == s[i]
+        assert np.array_equal(codes, c[i])
+        assert all(oracle.i8_dequant(int(codes[d]), scale) == float(x[i, d]) for d in range(0, 128, 17))
+
+
+@pytest.mark.parametrize("mag", [1e-3, 1.0, 100.0])
+def test_int8_quantise_error_bound_and_nearest_code(mag):
+    rng = np.random.default_rng(int(mag * 1000) + 1)
+    for _ in range(100):
+        x = (rng.standard_normal(128) * mag).astype(np.float16)
+        xd = x.astype(np.float64)
+        codes, scale = oracle.i8_quantize_row(x.view(np.uint16))
+        amax = np.abs(xd).max()
+        assert abs(float(scale) - amax / 127) <= amax / 127 * 2.0**-23
+        assert codes.min() >= -127 and codes.max() <= 127
+        j = int(np.argmax(np.abs(xd)))
+        assert int(codes[j]) == (127 if xd[j] > 0 else -127)
+        # the nearest integer to x / scale (float64), away from exact midpoints
+        r = xd / np.float64(scale)
+        clear = np.abs(np.abs(r - np.floor(r)) - 0.5) > 1e-5
+        assert np.array_equal(codes[clear].astype(np.int64), np.rint(r[clear]).astype(np.int64))
+        back = np.array([oracle.i8_dequant(int(cc), scale) for cc in codes])
+        assert np.all(np.abs(back - xd) <= float(scale) * (0.5 + 1e-5))
+
+
+def test_int8_quantise_zero_row():
+    codes, scale = oracle.i8_quantize_row(np.zeros(128, np.uint16))
+    assert scale == 0 and not codes.any()
+
+
+def _i8_case(rng, N=24, L=2, H=3, T=40):
+    x_k, c_k, s_k = _exact_rows(rng, T * H)
+    x_v, c_v, s_v = _exact_rows(rng, T * H)
+    slots = rng.choice(N * 16, T, replace=False).astype(np.int64)
+    return (x_k.reshape(T, H, 128), c_k.reshape(T, H, 128), s_k.reshape(T, H),
+            x_v.reshape(T, H, 128), c_v.reshape(T, H, 128), s_v.reshape(T, H), slots)
+
+
+def test_int8_append_places_codes_and_scales():
+    # byte placement checked with numpy's own C-order view of [block, layer, K/V, head, tile bytes]
+    rng = np.random.default_rng(3)
+    N, L, H, T = 24, 2, 3, 40
+    xk, ck, sk, xv, cv, sv, slots = _i8_case(rng, N, L, H, T)
+    g = oracle.geom(N, L, H, dtype=oracle.INT8)
+    pool = oracle.empty_pool(g)
+    pool[:] = 0xA5
+    layer = 1
+    assert oracle.kv_append(pool, g, layer, xk.view(np.uint16), xv.view(np.uint16), slots) == -1
+    tiles = pool.reshape(N, L, 2, H, 2112)
+    touched = np.zeros((N, L, 2, H, 16), bool)
+    for i, slot in enumerate(slots):
+        b, t = divmod(int(slot), 16)
+        for h in range(H):
+            for kv, (c, s) in enumerate(((ck, sk), (cv, sv))):
+                tile = tiles[b, layer, kv, h]
+                assert np.array_equal(tile[t * 128:(t + 1) * 128].view(np.int8), c[i, h])
+                assert tile[2048 + 4 * t:2048 + 4 * t + 4].view(np.float32)[0] == s[i, h]
+                touched[b, layer, kv, h, t] = True
+    # every other code row and scale is untouched
+    for b in range(N):
+        for l in range(L):
+            for kv in range(2):
+                for h in range(H):
+                    for t in range(16):
+                        if not touched[b, l, kv, h, t]:
+                            assert (tiles[b, l, kv, h, t * 128:(t + 1) * 128] == 0xA5).all()
+                            assert (tiles[b, l, kv, h, 2048 + 4 * t:2052 + 4 * t] == 0xA5).all()
+
+
+def test_int8_attention_equals_fp16_attention_on_exact_values():
+    # appended values that INT8 stores exactly: decode, split decode and prefill over the INT8 pool equal
+    # the same computations over an FP16 pool holding the same values (pins INT8 gather and indexing
+    # against the FP16 path, which the tests above pin)
+    rng = np.random.default_rng(4)
+    N, L, H, T = 24, 2, 3, 40
+    xk, ck, sk, xv, cv, sv, _ = _i8_case(rng, N, L, H, T)
+    perm = rng.permutation(N).astype(np.int32)
+    ctx = np.array([40], np.int32)
+    table = perm[None, :3]
+    slots = oracle.slots(table, np.zeros(T, np.int32), np.arange(T))
+    g16 = oracle.geom(N, L, H)
+    g8 = oracle.geom(N, L, H, dtype=oracle.INT8)
+    p16, p8 = oracle.empty_pool(g16), oracle.empty_pool(g8)
+    for l in range(L):
+        oracle.kv_append(p16, g16, l, xk.view(np.uint16), xv.view(np.uint16), slots)
+        oracle.kv_append(p8, g8, l, xk.view(np.uint16), xv.view(np.uint16), slots)
+    q = workloads.normal_fp16((T, H, 128), 9).numpy().view(np.uint16)
+    for l in range(L):
+        a16, _ = oracle.decode_attn(p16, g16, l, q[-1:], table, ctx, SCALE)
+        a8, _ = oracle.decode_attn(p8, g8, l, q[-1:], table, ctx, SCALE)
+        assert np.array_equal(a16, a8)
+        s16 = oracle.decode_attn_split(p16, g16, l, q[-1:], table, ctx, SCALE, 16)
+        s8 = oracle.decode_attn_split(p8, g8, l, q[-1:], table, ctx, SCALE, 16)
+        assert np.array_equal(s16, s8)
+        qs = np.array([0, T], np.int32)
+        f16, _ = oracle.prefill_attn(p16, g16, l, q, qs, table, ctx, SCALE)
+        f8, _ = oracle.prefill_attn(p8, g8, l, q, qs, table, ctx, SCALE)
+        assert np.array_equal(f16, f8)
+
+
+def test_int8_attention_close_to_fp16_attention_on_gaussian_values():
+    # not a parity bound: the quantisation error of N(0,1) rows stays small against the FP16 result
+    rng = np.random.default_rng(5)
+    N, L, H, T = 40, 1, 4, 300
+    k = workloads.normal_fp16((T, H, 128), 1).numpy().view(np.uint16)
+    v = workloads.normal_fp16((T, H, 128), 2).numpy().view(np.uint16)
+    q = workloads.normal_fp16((1, H, 128), 3).numpy().view(np.uint16)
+    table = rng.permutation(N).astype(np.int32)[None, :19]
+    slots = oracle.slots(table, np.zeros(T, np.int32), np.arange(T))
+    g16, g8 = oracle.geom(N, L, H), oracle.geom(N, L, H, dtype=oracle.INT8)
+    p16, p8 = oracle.empty_pool(g16), oracle.empty_pool(g8)
+    oracle.kv_append(p16, g16, 0, k, v, slots)
+    oracle.kv_append(p8, g8, 0, k, v, slots)
+    a16, _ = oracle.decode_attn(p16, g16, 0, q, table, np.array([T], np.int32), SCALE)
+    a8, _ = oracle.decode_attn(p8, g8, 0, q, table, np.array([T], np.int32), SCALE)
+    assert np.abs(a16 - a8).max() < 0.02 and not np.array_equal(a16, a8)
