@@ -14,7 +14,9 @@ Other workloads (--config): long_decode (13 x 8,192), shared_prefix_decode
 (64 rows over 125 shared blocks), mixed_prefill (a 4,000-token prompt in
 512-token chunks next to 31 decode rows; one step = the whole 8-chunk
 schedule, i.e. 8 iterations), gqa_decode (32 rows x 2,300 tokens, 8 K/V heads
-serving 32 query heads: 9.65 GB of K/V per step).
+serving 32 query heads: 9.65 GB of K/V per step), average_decode_int8 (the
+headline workload over an 8-bit pool: INT8 codes plus one FP32 scale per
+128-value row, 132 bytes per row instead of 256).
 
 Rank 0 prints one JSON line. Under torchrun (N > 1) every rank runs its own
 replica (weak scaling, no collective on the data path); `value` adds all
@@ -48,7 +50,7 @@ SCALE = float(np.float32(1.0 / np.sqrt(np.float32(128.0))))
 
 def _iterations(config: str, seed: int = 0):
     """The workload's engine iterations (one for decode configs, 8 for the chunk schedule)."""
-    if config == "average_decode":
+    if config in ("average_decode", "average_decode_int8"):
         return [workloads.average_decode(seed)]
     if config == "long_decode":
         return [workloads.long_decode(seed)]
@@ -70,14 +72,19 @@ CONFIG_TEXT = {
     "shared_prefix_decode": "64 rows sharing 125 ref-counted prefix blocks + 1..300 private tokens, 32 layers",
     "mixed_prefill": "one 4,000-token prompt prefilled in 512-token chunks (8 iterations) next to 31 decode rows "
                      "of context U{100..2000} advancing one token per iteration, 32 layers",
+    "average_decode_int8": "the average_decode workload over an 8-bit pool (INT8 codes, one FP32 scale per "
+                           "(token, head) row of K or V; 2,112-byte tiles), 7,152 blocks (30.9 GB)",
     "gqa_decode": "batch-32 decode at 2,300 context tokens per row, 32 layers, 8 K/V heads serving 32 query heads "
                   "(grouped-query attention, 131,072 B of K/V per token), 28,608-block (60 GB) shuffled pool, "
                   "kv_append of 1 token per row",
 }
 
+CONFIG_DTYPE = {"average_decode_int8": "int8"}
+
 KERNEL_SOURCES = {
     "decode_attn": ["pkv_kernels.cu", "ptx.cuh", "pkv_internal.h"],
     "decode_group_attn": ["pkv_decode_group.cu", "pkv_kernels.cu", "ptx.cuh", "pkv_internal.h"],
+    "decode_i8_attn": ["pkv_int8.cu", "ptx.cuh", "pkv_internal.h"],
     "prefill_attn": ["pkv_prefill.cu", "ptx.cuh", "pkv_internal.h"],
 }
 
@@ -214,10 +221,15 @@ def prefill_pairs(wl) -> int:
     return n
 
 
-def kv_bytes(wl, layers) -> int:
-    """K and V bytes the decode rows read: 2 x heads x 128 x 2 bytes per context token per layer."""
+def row_bytes(dtype: str) -> int:
+    """Bytes of one (token, head) row of K or V: 128 FP16 values, or 128 INT8 codes and a 4-byte scale."""
+    return HEAD_DIM * 2 if dtype == "fp16" else HEAD_DIM + 4
+
+
+def kv_bytes(wl, layers, dtype="fp16") -> int:
+    """K and V bytes the decode rows read: 2 x heads x row bytes per context token per layer."""
     dec = wl.ctx_lens[:wl.num_decode].astype(np.int64).sum()
-    return int(dec) * 2 * wl.num_heads * HEAD_DIM * 2 * layers
+    return int(dec) * 2 * wl.num_heads * row_bytes(dtype) * layers
 
 
 # ------------------------------------------------------------------ ours
@@ -304,12 +316,17 @@ def run_ours(args):
     wl0 = iters[0]
     L = args.layers or wl0.num_layers
     H, Hq = wl0.num_heads, wl0.q_heads
+    dtype = CONFIG_DTYPE.get(args.config, "fp16")
     dev = torch.device("cuda", local)
 
-    pool_t = torch.empty(workloads.pool_shape(wl0.num_blocks, L, H), dtype=torch.float16, device=dev)
-    workloads.fill_normal_fp16_(pool_t, workloads.value_seed(wl0.seed, "pool"))
+    if dtype == "int8":
+        pool_t = torch.empty(pkv.Pool.bytes_needed(wl0.num_blocks, L, H, "int8"), dtype=torch.uint8, device=dev)
+        workloads.fill_int8_tiles_(pool_t, workloads.value_seed(wl0.seed, "pool"))
+    else:
+        pool_t = torch.empty(workloads.pool_shape(wl0.num_blocks, L, H), dtype=torch.float16, device=dev)
+        workloads.fill_normal_fp16_(pool_t, workloads.value_seed(wl0.seed, "pool"))
     pool = pkv.Pool(pool_t, wl0.num_blocks, num_layers=L, num_heads=H, partition_tokens=args.partition_tokens,
-                    num_q_heads=Hq)
+                    num_q_heads=Hq, dtype=dtype)
     gen = torch.Generator(device=dev)
     gen.manual_seed(workloads.value_seed(wl0.seed, "q"))
     steps = [StepData(torch, pkv, pool, wl, m, L, dev, gen) for wl, m in zip(iters, _metadata(pkv, iters))]
@@ -346,7 +363,7 @@ def run_ours(args):
 
     has_prefill = any(s.max_q for s in steps)
     has_decode = any(s.B for s in steps)
-    kv_step = sum(kv_bytes(s.wl, L) for s in steps)
+    kv_step = sum(kv_bytes(s.wl, L, dtype) for s in steps)
     pairs_step = sum(prefill_pairs(s.wl) for s in steps) * L
     flops_step = 4 * HEAD_DIM * Hq * pairs_step
     tokens_step = sum(int(s.wl.ctx_lens[:s.B].astype(np.int64).sum()) for s in steps) * L
@@ -453,6 +470,8 @@ def run_ours(args):
     dec_bytes_launch = (kv_step / L / len(steps)) + sum(2 * s.B * Hq * HEAD_DIM * 2 for s in steps) / len(steps)
     dec_kernel = "decode_kernel" if Hq == H else "decode_group_kernel (mma.sync m16n8k16, one K/V read per group)"
     dec_src = "decode_attn" if Hq == H else "decode_group_attn"
+    if dtype == "int8":
+        dec_kernel, dec_src = "decode_i8_kernel (INT8 codes dequantised in the loaders)", "decode_i8_attn"
     rooflines = {}
     if n_dec:
         ach = dec_bytes_launch / (dec_ms / n_dec * 1e-3) / 1e9
@@ -491,10 +510,11 @@ def run_ours(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "f16 storage, f32 arithmetic",
+        "dtype": "f16 storage, f32 arithmetic" if dtype == "fp16" else "int8 storage (fp32 scales), f32 arithmetic",
         "data": "synthetic",
         "config": {"workload": args.config, "description": CONFIG_TEXT[args.config], "num_layers": L,
                    "iterations_per_step": len(steps), "num_seqs": wl0.num_seqs, "heads": H, "query_heads": Hq,
+                   "kv_dtype": dtype,
                    "head_dim": HEAD_DIM,
                    "pool_blocks": wl0.num_blocks, "kv_bytes_per_step": kv_step,
                    "prefill_flops_per_step": flops_step, "seed": wl0.seed,
@@ -514,7 +534,7 @@ def run_ours(args):
     if has_prefill:
         result["prefill_tflops"] = round(flops_step * K * ws / (t_ms * 1e-3) / 1e12, 1)
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = cpu_baseline(iters[0], pool_t, args.cpu_seconds, L)
+        result["cpu_baseline"] = cpu_baseline(iters[0], pool_t, args.cpu_seconds, L, dtype)
     if rank == 0:
         print(json.dumps(result), flush=True)
     if ws > 1:
@@ -523,13 +543,22 @@ def run_ours(args):
 
 # ------------------------------------------------------------------ oracle timings
 
-def _layer_sample(wl, layer, pool_t=None, seed=0):
+def _layer_sample(wl, layer, pool_t=None, seed=0, dtype="fp16"):
     """Host mini-pool of one layer's referenced blocks (renumbered), its tables and q."""
     import torch
     nb = -(-wl.ctx_lens.astype(np.int64) // 16)
     ids = np.concatenate([wl.block_tables[r, :nb[r]] for r in range(wl.num_seqs)]).astype(np.int64)
     uniq, inv = np.unique(ids, return_inverse=True)
-    if pool_t is not None:
+    if dtype == "int8":
+        layer_bytes = 2 * wl.num_heads * 2112
+        if pool_t is not None:
+            blocks = pool_t.view(wl.num_blocks, -1, layer_bytes)
+            sub = blocks.index_select(0, torch.from_numpy(uniq).to(pool_t.device))[:, layer].contiguous()
+            mini = sub.cpu().numpy().reshape(-1)
+        else:
+            t = torch.empty(len(uniq) * layer_bytes, dtype=torch.uint8)
+            mini = workloads.fill_int8_tiles_(t, seed + layer).numpy()
+    elif pool_t is not None:
         sub = pool_t.index_select(0, torch.from_numpy(uniq).to(pool_t.device))[:, layer:layer + 1].contiguous()
         mini = sub.cpu().view(torch.int16).numpy().view(np.uint16)
     else:
@@ -545,8 +574,8 @@ def _layer_sample(wl, layer, pool_t=None, seed=0):
     return np.ascontiguousarray(mini), tables, q.view(np.uint16), len(uniq)
 
 
-def _oracle_layer(oracle, wl, mini, tables, q, n):
-    g = oracle.geom(n, 1, wl.num_heads, num_q_heads=wl.q_heads)
+def _oracle_layer(oracle, wl, mini, tables, q, n, dtype="fp16"):
+    g = oracle.geom(n, 1, wl.num_heads, num_q_heads=wl.q_heads, dtype=oracle.INT8 if dtype == "int8" else oracle.FP16)
     B = wl.num_decode
     if B:
         oracle.decode_attn(mini, g, 0, q[:B], tables[:B], wl.ctx_lens[:B], SCALE)
@@ -554,20 +583,20 @@ def _oracle_layer(oracle, wl, mini, tables, q, n):
         oracle.prefill_attn(mini, g, 0, q, wl.q_start_loc()[B:], tables[B:], wl.ctx_lens[B:], SCALE)
 
 
-def cpu_baseline(wl, pool_t, budget_s, layers):
+def cpu_baseline(wl, pool_t, budget_s, layers, dtype="fp16"):
     import oracle
     threads = len(os.sched_getaffinity(0))
     oracle.set_num_threads(threads)
     t_total, done = 0.0, 0
     for layer in range(layers):
-        mini, tables, q, n = _layer_sample(wl, layer, pool_t)
+        mini, tables, q, n = _layer_sample(wl, layer, pool_t, dtype=dtype)
         t0 = time.perf_counter()
-        _oracle_layer(oracle, wl, mini, tables, q, n)
+        _oracle_layer(oracle, wl, mini, tables, q, n, dtype)
         t_total += time.perf_counter() - t0
         done += 1
         if t_total >= budget_s:
             break
-    kv = kv_bytes(wl, done)
+    kv = kv_bytes(wl, done, dtype)
     res = {"unit": "GB/s", "cores": threads, "kind": "oracle", "seconds": round(t_total, 2),
            "sample": f"all rows and heads of the first iteration for {done} of {layers} layers (referenced blocks "
                      f"copied to host first, copy not timed)"}
@@ -585,21 +614,22 @@ def run_reference(args):
         return
     import oracle
     wl = _iterations(args.config, args.seed)[0]
+    dtype = CONFIG_DTYPE.get(args.config, "fp16")
     threads = len(os.sched_getaffinity(0))
     oracle.set_num_threads(threads)
-    samples = [_layer_sample(wl, l, None, seed=1) for l in range(2)]
+    samples = [_layer_sample(wl, l, None, seed=1, dtype=dtype) for l in range(2)]
     times = []
     for i in range(args.warmup + args.steps):
         mini, tables, q, n = samples[i % len(samples)]
         t0 = time.perf_counter()
-        _oracle_layer(oracle, wl, mini, tables, q, n)
+        _oracle_layer(oracle, wl, mini, tables, q, n, dtype)
         dt = time.perf_counter() - t0
         if i >= args.warmup:
             times.append(dt)
     total = sum(times)
     if wl.num_decode:
         metric = "decode KV GB/s (KV bytes read per 32-layer iteration / iteration time) at batch 32"
-        value, unit = kv_bytes(wl, len(times)) / total / 1e9, "GB/s"
+        value, unit = kv_bytes(wl, len(times), dtype) / total / 1e9, "GB/s"
     else:
         metric = "prefill attention TFLOP/s"
         value, unit = 4 * HEAD_DIM * wl.q_heads * prefill_pairs(wl) * len(times) / total / 1e12, "TFLOP/s"
@@ -621,7 +651,8 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", default="average_decode",
-                    choices=["average_decode", "long_decode", "shared_prefix_decode", "mixed_prefill", "gqa_decode"])
+                    choices=["average_decode", "long_decode", "shared_prefix_decode", "mixed_prefill", "gqa_decode",
+                             "average_decode_int8"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="launch each step directly instead of replaying a CUDA graph")

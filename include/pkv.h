@@ -49,7 +49,18 @@ typedef enum pkv_status {
     PKV_E_TIMEOUT = 5   /* a kernel's bounded wait ran out; the kernel returned early */
 } pkv_status;
 
-enum { PKV_DTYPE_FP16 = 0 };
+/* Element types of a pool. PKV_DTYPE_INT8 is the 8-bit cache ("Inference
+ * Infrastructure" (seeitflow), the KV cache arithmetic: 8 bits per element
+ * halve the cache): each (block, layer, K/V, head) tile holds the 16 x 128
+ * INT8 codes, token-major, then 16 FP32 scales, one per token row (2,112 B
+ * instead of 4,096). Rule: scale = max|x| / 127 over the row's 128 FP16
+ * values, code = round-half-even(x / scale) clamped to +-127, both in IEEE
+ * single precision; attention reads code * scale. kv_append quantises,
+ * decode attention dequantises in its loaders (tensor cores: codes become
+ * FP16 exactly, the K scale multiplies the scores, the V scale folds into the
+ * softmax weights, which are rounded to FP16). Prefill attention over an INT8
+ * pool is not built (PKV_E_INVALID). */
+enum { PKV_DTYPE_FP16 = 0, PKV_DTYPE_INT8 = 1 };
 
 /* Bits of the sticky device error word (pkv_get_status). */
 enum {
@@ -68,7 +79,7 @@ typedef struct pkv_pool_desc {
     int32_t num_heads;    /* K/V heads stored per layer: 32 for the MHA model, 8 for GQA */
     int32_t head_dim;     /* must be 128 */
     int32_t block_size;   /* must be 16 */
-    int32_t dtype;        /* must be PKV_DTYPE_FP16 */
+    int32_t dtype;        /* PKV_DTYPE_FP16 or PKV_DTYPE_INT8 */
     int32_t partition_tokens; /* decode split-K partition size in tokens; 0 = default 1024;
                                  a multiple of 64 in [64, 2048]. Results depend only on a
                                  row's ctx_len and this value, never on the rest of the batch. */
@@ -88,8 +99,9 @@ typedef struct pkv_pool_desc {
 
 typedef struct pkv_pool pkv_pool;
 
-/* Bytes the pool needs: num_blocks * num_layers * 2 * num_heads * block_size * head_dim * 2
- * ("llm-inference-batching", "KV cache": 8,388,608 B per block for the 7B model).
+/* Bytes the pool needs: num_blocks * num_layers * 2 * num_heads * tile, tile =
+ * block_size * head_dim * 2 = 4,096 B for FP16 ("llm-inference-batching", "KV
+ * cache": 8,388,608 B per block for the 7B model) or 2,112 B for INT8.
  * Returns 0 for an invalid descriptor. */
 size_t pkv_pool_bytes(const pkv_pool_desc* desc);
 

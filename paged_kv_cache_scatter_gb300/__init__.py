@@ -18,6 +18,8 @@ LIB_PATH = os.path.join(_PKG, "libpkv.so")
 PKV_OK, PKV_E_INVALID, PKV_E_NOMEM, PKV_E_SHARED, PKV_E_DEVICE, PKV_E_TIMEOUT = range(6)
 PKV_DEV_BAD_SLOT, PKV_DEV_BAD_BLOCK, PKV_DEV_BAD_CTX, PKV_DEV_BAD_QLEN, PKV_DEV_TIMEOUT = 1, 2, 4, 8, 16
 PKV_DTYPE_FP16 = 0
+PKV_DTYPE_INT8 = 1
+_DTYPES = {"fp16": PKV_DTYPE_FP16, "int8": PKV_DTYPE_INT8}
 
 _c = ctypes
 _P = _c.c_void_p
@@ -122,18 +124,21 @@ class Pool:
     bookkeeping calls work without a GPU and its kernel calls are refused."""
 
     def __init__(self, storage, num_blocks: int, num_layers: int = 32, num_heads: int = 32,
-                 partition_tokens: int = 0, free_order=None, num_q_heads: int = 0):
+                 partition_tokens: int = 0, free_order=None, num_q_heads: int = 0, dtype: str = "fp16"):
         """num_heads: K/V heads stored per layer; num_q_heads: query heads (0 = num_heads), a multiple
-        of num_heads (grouped-query attention: query head h reads K/V head h // (num_q_heads // num_heads))."""
+        of num_heads (grouped-query attention: query head h reads K/V head h // (num_q_heads // num_heads)).
+        dtype "fp16" or "int8" (the 8-bit cache: 2,112-byte tiles of INT8 codes and FP32 scales; the
+        storage is then any device buffer of pkv_pool_bytes bytes, e.g. a uint8 tensor)."""
         lib = load()
         self._storage = storage
         self.num_blocks, self.num_layers, self.num_heads = int(num_blocks), int(num_layers), int(num_heads)
         self.num_q_heads = int(num_q_heads) or self.num_heads
+        self.dtype = dtype
         self._order = None
         if free_order is not None:
             import numpy as np
             self._order = np.ascontiguousarray(free_order, dtype=np.int64)
-        self.desc = pkv_pool_desc(self.num_blocks, self.num_layers, self.num_heads, 128, 16, PKV_DTYPE_FP16,
+        self.desc = pkv_pool_desc(self.num_blocks, self.num_layers, self.num_heads, 128, 16, _DTYPES[dtype],
                                   int(partition_tokens), _ptr(storage),
                                   0 if storage is None else storage.numel() * storage.element_size(),
                                   None if self._order is None else self._order.ctypes.data, self.num_q_heads)
@@ -142,8 +147,8 @@ class Pool:
         self.handle = h
 
     @staticmethod
-    def bytes_needed(num_blocks: int, num_layers: int = 32, num_heads: int = 32) -> int:
-        d = pkv_pool_desc(int(num_blocks), int(num_layers), int(num_heads), 128, 16, PKV_DTYPE_FP16, 0, None, 0, None)
+    def bytes_needed(num_blocks: int, num_layers: int = 32, num_heads: int = 32, dtype: str = "fp16") -> int:
+        d = pkv_pool_desc(int(num_blocks), int(num_layers), int(num_heads), 128, 16, _DTYPES[dtype], 0, None, 0, None)
         return load().pkv_pool_bytes(_c.byref(d))
 
     def close(self):

@@ -87,7 +87,8 @@ const char* pkv_status_string(pkv_status s)
 static bool desc_ok(const pkv_pool_desc* d)
 {
     if (!d) return false;
-    if (d->head_dim != pkv::kHeadDim || d->block_size != pkv::kBlockSize || d->dtype != PKV_DTYPE_FP16) return false;
+    if (d->head_dim != pkv::kHeadDim || d->block_size != pkv::kBlockSize) return false;
+    if (d->dtype != PKV_DTYPE_FP16 && d->dtype != PKV_DTYPE_INT8) return false;
     if (d->num_blocks < 1 || d->num_blocks > (int64_t)1 << 31) return false;
     if (d->num_layers < 1 || d->num_layers > 1024 || d->num_heads < 1 || d->num_heads > 256) return false;
     if (d->num_q_heads != 0 &&
@@ -96,10 +97,15 @@ static bool desc_ok(const pkv_pool_desc* d)
     return true;
 }
 
+static int64_t tile_bytes(const pkv_pool_desc* d)
+{
+    return d->dtype == PKV_DTYPE_INT8 ? pkv::kTileBytesI8 : pkv::kTileBytes;
+}
+
 size_t pkv_pool_bytes(const pkv_pool_desc* d)
 {
     if (!desc_ok(d)) return 0;
-    return (size_t)d->num_blocks * d->num_layers * 2 * d->num_heads * d->block_size * d->head_dim * 2;
+    return (size_t)d->num_blocks * d->num_layers * 2 * d->num_heads * (size_t)tile_bytes(d);
 }
 
 static bool bind_device(pkv_pool* p)
@@ -122,12 +128,18 @@ static bool bind_device(pkv_pool* p)
     p->geom.num_heads = d->num_heads;
     p->geom.num_q_heads = d->num_q_heads;
     p->geom.group = d->num_q_heads / d->num_heads;
-    p->geom.kv_bytes = (int64_t)d->num_heads * pkv::kTileBytes;
+    p->geom.dtype = d->dtype;
+    p->geom.tile_bytes = tile_bytes(d);
+    p->geom.kv_bytes = (int64_t)d->num_heads * p->geom.tile_bytes;
     p->geom.layer_bytes = 2 * p->geom.kv_bytes;
     p->geom.block_bytes = (int64_t)d->num_layers * p->geom.layer_bytes;
     std::string err;
-    p->kv_tmap_ok = pkv::encode_kv_tmap(p->geom, &p->kv_tmap, &err);
-    p->tile_tmap_ok = pkv::encode_tile_tmap(p->geom, &p->tile_tmap, &err);
+    if (d->dtype == PKV_DTYPE_FP16) {
+        p->kv_tmap_ok = pkv::encode_kv_tmap(p->geom, &p->kv_tmap, &err);
+        p->tile_tmap_ok = pkv::encode_tile_tmap(p->geom, &p->tile_tmap, &err);
+    } else {
+        p->tile_tmap_ok = pkv::encode_i8_tmap(p->geom, &p->tile_tmap, &err);
+    }
     return true;
 }
 
@@ -138,7 +150,7 @@ pkv_status pkv_pool_create(const pkv_pool_desc* d, pkv_pool** out)
     if (!desc_ok(d))
         return fail(PKV_E_INVALID, "unsupported pool descriptor (need head_dim 128, block_size 16, FP16, "
                                    "1..1024 layers, 1..256 K/V heads, 1..2^31 blocks, num_q_heads 0 or a "
-                                   "multiple of num_heads up to 1024)");
+                                   "multiple of num_heads up to 1024; FP16 or INT8)");
     const bool host_only = d->dev_base == nullptr;
     if (!host_only && !aligned(d->dev_base, 256)) return fail(PKV_E_INVALID, "dev_base not 256-byte aligned");
     if (!host_only && d->bytes < pkv_pool_bytes(d))
@@ -323,6 +335,9 @@ static pkv_status check_layer(const pkv_pool* pool, int32_t layer)
     return PKV_OK;
 }
 
+static cudaError_t launch_append_any(const pkv_pool* pool, int32_t layer, const void* k, const void* v,
+                                     const int64_t* slots, int32_t num_tokens, cudaStream_t s);
+
 pkv_status pkv_kv_append(pkv_pool* pool, int32_t layer, const void* k, const void* v, const int64_t* slot_mapping,
                          int32_t num_tokens, void* stream)
 {
@@ -335,8 +350,7 @@ pkv_status pkv_kv_append(pkv_pool* pool, int32_t layer, const void* k, const voi
         return fail(PKV_E_INVALID, "k/v must be 16-byte aligned, slot_mapping 8-byte aligned");
     DeviceGuard dg(pool->device);
     if (!dg.ok) return fail(PKV_E_DEVICE, "cannot select the pool's device");
-    cudaError_t e = pkv::launch_kv_append(pool->geom, layer, k, v, slot_mapping, num_tokens, pool->status_dev,
-                                          static_cast<cudaStream_t>(stream));
+    cudaError_t e = launch_append_any(pool, layer, k, v, slot_mapping, num_tokens, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PKV_OK : pkv::cuda_fail(e, "kv_append launch");
 }
 
@@ -346,12 +360,28 @@ size_t pkv_decode_workspace_bytes(const pkv_pool* pool, int32_t num_seqs, int32_
     return pkv::decode_workspace_bytes(num_seqs, pool->desc.num_q_heads, max_blocks, pool->partition_tokens);
 }
 
-// The one-head decode kernel for MHA pools, the group kernel when K/V heads serve several query heads.
+// kv_append for the pool's element type.
+static cudaError_t launch_append_any(const pkv_pool* pool, int32_t layer, const void* k, const void* v,
+                                     const int64_t* slots, int32_t num_tokens, cudaStream_t s)
+{
+    if (pool->geom.dtype == PKV_DTYPE_INT8)
+        return pkv::launch_kv_append_i8(pool->geom, layer, k, v, slots, num_tokens, pool->status_dev, s);
+    return pkv::launch_kv_append(pool->geom, layer, k, v, slots, num_tokens, pool->status_dev, s);
+}
+
+// The one-head decode kernel for MHA pools, the group kernel when K/V heads serve several query heads,
+// the 8-bit kernel for INT8 pools.
 static cudaError_t launch_decode_any(const pkv_pool* pool, int32_t layer, const void* q, const int32_t* tables,
                                      int32_t max_blocks, const int32_t* ctx_lens, int32_t num_seqs, float scale,
                                      void* out, void* ws, const void* k_new, const void* v_new, const int64_t* slots,
                                      cudaStream_t s)
 {
+    if (pool->geom.dtype == PKV_DTYPE_INT8) {
+        const pkv::DecodeWs w = pkv::decode_ws(pool->geom, ws, num_seqs, max_blocks, pool->partition_tokens);
+        return pkv::launch_decode_i8(pool->geom, pool->tile_tmap, layer, q, tables, max_blocks, ctx_lens, num_seqs,
+                                     scale, out, w,
+                                     pool->partition_tokens, k_new, v_new, slots, pool->status_dev, s);
+    }
     if (pool->geom.group == 1)
         return pkv::launch_decode(pool->geom, layer, q, tables, max_blocks, ctx_lens, num_seqs, scale, out, ws,
                                   pool->partition_tokens, k_new, v_new, slots, pool->status_dev, s);
@@ -371,7 +401,7 @@ static pkv_status check_decode(pkv_pool* pool, int32_t layer, const void* q, con
     if (num_seqs > 65535) return fail(PKV_E_INVALID, "num_seqs above 65,535");
     if (num_seqs == 0) return PKV_OK;
     if (!q || !tables || !ctx_lens || !out) return fail(PKV_E_INVALID, "NULL q, tables, ctx_lens or out");
-    if (pool->geom.group > 1 && !pool->tile_tmap_ok)
+    if ((pool->geom.group > 1 || pool->geom.dtype == PKV_DTYPE_INT8) && !pool->tile_tmap_ok)
         return fail(PKV_E_DEVICE, "TMA descriptor for the pool could not be encoded");
     if (!aligned(q, 16) || !aligned(out, 16) || !aligned(tables, 4) || !aligned(ctx_lens, 4))
         return fail(PKV_E_INVALID, "q/out must be 16-byte aligned, tables/ctx_lens 4-byte aligned");
@@ -416,6 +446,7 @@ pkv_status pkv_prefill_attn(pkv_pool* pool, int32_t layer, const void* q, const 
     if (num_seqs > 65535) return fail(PKV_E_INVALID, "num_seqs above 65,535");
     if (!q || !q_start_loc || !block_tables || !ctx_lens || !out) return fail(PKV_E_INVALID, "NULL argument");
     if (!aligned(q, 16) || !aligned(out, 16)) return fail(PKV_E_INVALID, "q/out must be 16-byte aligned");
+    if (pool->geom.dtype == PKV_DTYPE_INT8) return fail(PKV_E_INVALID, "prefill over an INT8 pool is not built");
     if (!pool->kv_tmap_ok) return fail(PKV_E_DEVICE, "TMA descriptor for the pool could not be encoded");
     DeviceGuard dg(pool->device);
     if (!dg.ok) return fail(PKV_E_DEVICE, "cannot select the pool's device");
@@ -448,6 +479,8 @@ pkv_status pkv_step(pkv_pool* pool, const pkv_step_desc* st, void* workspace, si
     if (!st->block_tables || !st->ctx_lens || !st->slot_mapping || !st->q || !st->k || !st->v || !st->out)
         return fail(PKV_E_INVALID, "NULL step array");
     if (P > 0 && !st->q_start_loc) return fail(PKV_E_INVALID, "prefill rows need q_start_loc");
+    if (P > 0 && pool->geom.dtype == PKV_DTYPE_INT8)
+        return fail(PKV_E_INVALID, "prefill over an INT8 pool is not built");
     if (st->q_layer_stride % 8 || st->k_layer_stride % 8 || st->v_layer_stride % 8 || st->out_layer_stride % 8)
         return fail(PKV_E_INVALID, "layer strides must be multiples of 8 elements");
     const int64_t tok = (int64_t)pool->desc.num_heads * pkv::kHeadDim * 2;  // bytes of one token's k or v row
@@ -474,8 +507,7 @@ pkv_status pkv_step(pkv_pool* pool, const pkv_step_desc* st, void* workspace, si
         const char* vl = v + li * st->v_layer_stride * 2;
         char* ol = out + li * st->out_layer_stride * 2;
         if (P > 0) {  // the prefill tokens' kv_append; the decode rows append inside the decode kernel
-            e = pkv::launch_kv_append(pool->geom, layer, kl + B * tok, vl + B * tok, st->slot_mapping + B,
-                                      st->num_tokens - B, pool->status_dev, s);
+            e = launch_append_any(pool, layer, kl + B * tok, vl + B * tok, st->slot_mapping + B, st->num_tokens - B, s);
             if (e != cudaSuccess) return pkv::cuda_fail(e, "kv_append launch");
         }
         if (B > 0) {

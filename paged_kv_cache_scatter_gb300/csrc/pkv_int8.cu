@@ -1,0 +1,614 @@
+// pkv_int8.cu — the 8-bit KV cache: kv_append that quantises, and decode
+// attention that dequantises in its loaders.
+//
+// An 8-bit cache halves the bytes every decode step reads ("Inference
+// Infrastructure" (seeitflow), the KV cache arithmetic); its scales are
+// metadata stored with the data ("The inference engine" (wpnews),
+// "IO-aware attention and quantization attack different costs"). The pages
+// fix no scale rule; the library's: INT8 codes, symmetric, one FP32 scale per
+// (token, head) row of K or V:
+//   amax  = max |x|                      over the row's 128 FP16 values
+//   scale = amax / 127                   IEEE single precision
+//   code  = round-half-even(x / scale)   IEEE single division, then clamp to +-127
+//   value = code * scale                 what attention reads
+// A row of zeros has scale 0 and codes 0.
+//
+// Tile layout: each (block, layer, K/V, head) tile is 2,112 bytes, the 16 x 128
+// codes (token-major) followed by the 16 scales, so one bulk copy moves a tile
+// with its metadata. A block is layers x 2 x heads tiles.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include "pkv_internal.h"
+#include "ptx.cuh"
+
+namespace pkv {
+namespace {
+
+constexpr int kCodesBytes = kBlockSize * kHeadDim;  // 2,048
+static_assert(kTileBytesI8 == kCodesBytes + 4 * kBlockSize, "8-bit tile: codes then scales");
+
+// Quantise one row of 128 FP16 values held 4 per lane (lane l: values 4l .. 4l+3).
+// Returns the lane's 4 codes packed little-endian; *scale receives the row's scale.
+__device__ __forceinline__ uint32_t quantize_row_warp(const uint2 raw, float* scale)
+{
+    float x[4];
+    half4_to_float(raw, x);
+    float amax = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    const float s = __fdiv_rn(amax, 127.f);
+    uint32_t packed = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        int c = 0;
+        if (amax > 0.f) c = min(max(__float2int_rn(__fdiv_rn(x[i], s)), -127), 127);
+        packed |= (uint32_t)(c & 0xff) << (8 * i);
+    }
+    *scale = s;
+    return packed;
+}
+
+// ---------------------------------------------------------------- kv_append
+
+// One warp per (token, K/V, head) row: quantise and store its 128 codes and scale.
+__global__ void __launch_bounds__(256) kv_append_i8_kernel(char* __restrict__ pool, int64_t block_bytes,
+                                                           int64_t layer_off, int64_t kv_bytes, int num_heads,
+                                                           const __half* __restrict__ k, const __half* __restrict__ v,
+                                                           const int64_t* __restrict__ slots, int num_tokens,
+                                                           int64_t num_slots, unsigned int* status)
+{
+    const int64_t row = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (row >= 2LL * num_heads * num_tokens) return;
+    const int tok = (int)(row / (2 * num_heads));
+    const int rem = (int)(row - (int64_t)tok * 2 * num_heads);
+    const int kv = rem / num_heads, h = rem % num_heads;
+    const int64_t slot = __ldg(slots + tok);
+    if (slot < 0 || slot >= num_slots) {
+        if (rem == 0 && lane == 0) atomicOr(status, PKV_DEV_BAD_SLOT);
+        return;
+    }
+    const __half* src = (kv ? v : k) + ((int64_t)tok * num_heads + h) * kHeadDim;
+    float s;
+    const uint32_t codes = quantize_row_warp(__ldg(reinterpret_cast<const uint2*>(src) + lane), &s);
+    const int t = (int)(slot % kBlockSize);
+    char* tile = pool + slot / kBlockSize * block_bytes + layer_off + kv * kv_bytes + (int64_t)h * kTileBytesI8;
+    reinterpret_cast<uint32_t*>(tile + t * kHeadDim)[lane] = codes;
+    if (lane == 0) *reinterpret_cast<float*>(tile + kCodesBytes + 4 * t) = s;
+}
+
+// ---------------------------------------------------------------- decode
+//
+// One CTA = (partition p, K/V head k with query-head slice c, row r); it
+// computes R query heads (R = 1 for a pool without grouped heads, otherwise
+// up to 16 of k's group) from one copy of each 8-bit tile. Its four warps take
+// the partition's blocks round-robin, each with a private two-stage ring:
+// per stage the K and V codes (16 x 128 bytes each, one 4 KB stage) arrive by
+// TMA with the 128-byte swizzle and the two 64-byte scale rows by bulk copies
+// into a side array, all on one mbarrier. (Four stages measured slower than
+// two: the rate is not set by the bytes in flight.) Per block a warp runs the attention on the tensor cores with
+// mma.sync m16n8k16 (FP16 operands, FP32 accumulation):
+//   S = Q C_K^T      codes become FP16 exactly (byte + 1024 - 1152), each
+//                    32-bit word of 4 codes feeding one k-step pair; the
+//                    contraction order of the 16 dims in a chunk is permuted
+//                    (dims 4j..4j+1 to k 2j..2j+1, 4j+2..4j+3 to k 2j+8..)
+//                    and q's fragments use the same order;
+//   S_t *= scale_K[t], then online softmax in the log2 domain;
+//   O += (P * scale_V) C_V   the V scale folds into P (rows past the context
+//                    get exactly 0, never 0 x a garbage scale); a transposed
+//                    ldmatrix of the codes yields token pairs for the even and
+//                    for the odd dimensions of a 16-dim chunk, so each chunk
+//                    is two N = 8 tiles.
+// The warps merge through shared memory in warp order; split-K partials merge
+// across partitions in partition order, as in the FP16 kernels. With
+// `append`, the CTA with c == 0 holding a row's last partition stores the
+// quantised new K/V, and the warp streaming that block quantises the same
+// rows (the same arithmetic as kv_append) into its shared-memory copy.
+
+constexpr int kQWarps = 4;
+constexpr int kQStages = 2;
+constexpr int kQStage = 2 * kCodesBytes;  // K codes at 0, V codes at 2,048: both 1 KB aligned for the swizzle
+constexpr int kQScaleStage = 2 * 4 * kBlockSize;  // K scales, then V scales
+constexpr int kQRows = 16;
+constexpr int kQMaxBlocks = kMaxPartition / kBlockSize;
+constexpr int kQMergeStride = kHeadDim + 4;
+
+constexpr int kQSmRing = 0;
+constexpr int kQSmScales = kQSmRing + kQWarps * kQStages * kQStage;  // [warp][stage] 128 B
+constexpr int kQSmIds = kQSmScales + kQWarps * kQStages * kQScaleStage;
+constexpr int kQSmBars = kQSmIds + kQMaxBlocks * 4;
+constexpr int kQSmFlag = kQSmBars + kQWarps * kQStages * 8;
+constexpr int kQSmBytes = kQSmFlag + 16;
+constexpr int kQSmAlloc = kQSmBytes + 1024;
+constexpr int kQSmMergeO = 0;
+constexpr int kQSmMergeML = kQWarps * kQRows * kQMergeStride * 4;
+static_assert(kQSmMergeML + kQWarps * kQRows * 8 <= kQSmBars, "merge scratch fits in the idle rings, scales and ids");
+
+struct I8Args {
+    const __half* q;
+    __half* out;
+    const int32_t* tables;
+    int max_blocks;
+    const int32_t* ctx_lens;
+    char* pool;
+    int64_t block_bytes;
+    int64_t head_off;
+    int64_t kv_bytes;
+    int64_t num_blocks;
+    int layer;
+    int num_kv_heads;
+    int num_q_heads;
+    int group;
+    int rows;
+    int slices;
+    float scale_log2;
+    float* ws_o;
+    float* ws_ml;
+    unsigned int* counters;  // [B][num_kv_heads * slices]
+    int max_parts;
+    int part_tokens;
+    const __half* k_new;     // [B][num_kv_heads][128] when append
+    const __half* v_new;
+    const int64_t* slots;
+    int append;
+    unsigned int* status;
+};
+
+// Byte offset of byte b of token t's 128 codes in a swizzled 16 x 128 B code tile.
+__device__ __forceinline__ uint32_t code_off(int t, int b)
+{
+    return (uint32_t)(t * 128 + ((((b >> 4) ^ (t & 7))) << 4) + (b & 15));
+}
+
+// Two biased code bytes (byte + 128) selected by `sel` into a half2 of the codes, exactly.
+__device__ __forceinline__ uint32_t codes2_to_half2(uint32_t biased, uint32_t sel)
+{
+    const uint32_t h = __byte_perm(biased, 0x64646464u, sel);  // halves 1024 + byte
+    const __half2 r = __hsub2(*reinterpret_cast<const __half2*>(&h), __half2half2(__ushort_as_half(0x6480)));
+    return *reinterpret_cast<const uint32_t*>(&r);
+}
+
+__device__ __forceinline__ unsigned int q_atomic_add_acq_rel(unsigned int* p, unsigned int v)
+{
+    unsigned int old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
+template <bool ROWS16>
+__global__ void __launch_bounds__(kQWarps * 32) decode_i8_kernel(const __grid_constant__ CUtensorMap tmap,
+                                                                 const I8Args a)
+{
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+    const uint32_t sb = smem_u32(smem);
+    const int p = blockIdx.x, r = blockIdx.z;
+    const int kvh = blockIdx.y / a.slices, c = blockIdx.y % a.slices;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, tq = lane & 3;
+    const int h0 = kvh * a.group + c * a.rows;
+
+    const int ctx = __ldg(a.ctx_lens + r);
+    if (ctx < 1 || ctx > a.max_blocks * kBlockSize) {
+        if (p == 0 && blockIdx.y == 0 && threadIdx.x == 0) atomicOr(a.status, PKV_DEV_BAD_CTX);
+        return;
+    }
+    const int nparts = (ctx + a.part_tokens - 1) / a.part_tokens;
+    if (p >= nparts) return;
+    const int blk_lo = p * a.part_tokens / kBlockSize;
+    const int blk_hi = (min((p + 1) * a.part_tokens, ctx) + kBlockSize - 1) / kBlockSize;
+    const int count = blk_hi - blk_lo;
+
+    int32_t* ids = reinterpret_cast<int32_t*>(smem + kQSmIds);
+    const int32_t* trow = a.tables + (int64_t)r * a.max_blocks;
+    bool bad = false;
+    for (int i = threadIdx.x; i < count; i += kQWarps * 32) {
+        const int id = __ldg(trow + blk_lo + i);
+        ids[i] = id;
+        bad |= id < 0 || (int64_t)id >= a.num_blocks;
+    }
+    const uint32_t bar0 = sb + kQSmBars + warp * kQStages * 8;
+    if (lane == 0) {
+        for (int s = 0; s < kQStages; ++s) mbar_init(bar0 + 8 * s, 1);
+        fence_mbar_init();
+    }
+    if (__syncthreads_or(bad)) {
+        if (threadIdx.x == 0) atomicOr(a.status, PKV_DEV_BAD_BLOCK);
+        return;
+    }
+
+    const int nloc = count > warp ? (count - warp + kQWarps - 1) / kQWarps : 0;
+    const uint32_t ring = sb + kQSmRing + warp * kQStages * kQStage;
+    const uint32_t sring = sb + kQSmScales + warp * kQStages * kQScaleStage;
+    const char* tile_k = a.pool + a.head_off + (int64_t)kvh * kTileBytesI8;
+    auto issue = [&](int li) {
+        const int s = li % kQStages;
+        const int id = ids[warp + li * kQWarps];
+        const uint32_t dst = ring + s * kQStage, bar = bar0 + 8 * s;
+        const char* src = tile_k + (int64_t)id * a.block_bytes;
+        mbar_arrive_expect_tx(bar, 2 * kTileBytesI8);
+        tma_load_5d(dst, &tmap, 0, 0, kvh, a.layer, id, bar);
+        tma_load_5d(dst + kCodesBytes, &tmap, 0, 0, a.num_kv_heads + kvh, a.layer, id, bar);
+        bulk_g2s(sring + s * kQScaleStage, src + kCodesBytes, 4 * kBlockSize, bar);
+        bulk_g2s(sring + s * kQScaleStage + 4 * kBlockSize, src + a.kv_bytes + kCodesBytes, 4 * kBlockSize, bar);
+    };
+    int issued = min(nloc, kQStages);
+    if (lane == 0)
+        for (int li = 0; li < issued; ++li) issue(li);
+
+    // The new token: quantised here by the warp that streams its block, and stored by c == 0's warp 0.
+    const int new_t = (ctx - 1) % kBlockSize, new_i = (ctx - 1) / kBlockSize - blk_lo;
+    int patch_li = -1;
+    uint32_t kcodes = 0, vcodes = 0;
+    float kscale = 0.f, vscale = 0.f;
+    if (a.append && p == nparts - 1) {
+        const int64_t slot = __ldg(a.slots + r);
+        const int32_t tb = __ldg(trow + (ctx - 1) / kBlockSize);
+        const bool consistent =
+            tb >= 0 && (int64_t)tb < a.num_blocks && slot == (int64_t)tb * kBlockSize + new_t;
+        if (!consistent) {
+            if (threadIdx.x == 0) atomicOr(a.status, PKV_DEV_BAD_SLOT);
+        } else if (warp == new_i % kQWarps || (c == 0 && warp == 0)) {
+            const int64_t src = ((int64_t)r * a.num_kv_heads + kvh) * kHeadDim;
+            kcodes = quantize_row_warp(__ldg(reinterpret_cast<const uint2*>(a.k_new + src) + lane), &kscale);
+            vcodes = quantize_row_warp(__ldg(reinterpret_cast<const uint2*>(a.v_new + src) + lane), &vscale);
+            if (warp == new_i % kQWarps) patch_li = new_i / kQWarps;
+            if (c == 0 && warp == 0) {
+                char* tile = a.pool + slot / kBlockSize * a.block_bytes + a.head_off + (int64_t)kvh * kTileBytesI8;
+                reinterpret_cast<uint32_t*>(tile + new_t * kHeadDim)[lane] = kcodes;
+                reinterpret_cast<uint32_t*>(tile + a.kv_bytes + new_t * kHeadDim)[lane] = vcodes;
+                if (lane == 0) {
+                    *reinterpret_cast<float*>(tile + kCodesBytes + 4 * new_t) = kscale;
+                    *reinterpret_cast<float*>(tile + a.kv_bytes + kCodesBytes + 4 * new_t) = vscale;
+                }
+            }
+        }
+    }
+
+    // q as the A operand in the permuted contraction order: for chunk j (dims 16j..16j+15),
+    // register 0 holds dims 16j+4tq, +1 and register 2 holds dims 16j+4tq+2, +3 of row g.
+    uint32_t qa[8][4];
+    {
+        const uint32_t* qlo = reinterpret_cast<const uint32_t*>(a.q + ((int64_t)r * a.num_q_heads + h0 + g) * kHeadDim);
+        const uint32_t* qhi = qlo + 8 * kHeadDim / 2;
+        const bool lo_ok = g < a.rows, hi_ok = ROWS16 && g + 8 < a.rows;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            qa[j][0] = lo_ok ? __ldg(qlo + 8 * j + 2 * tq) : 0u;
+            qa[j][1] = hi_ok ? __ldg(qhi + 8 * j + 2 * tq) : 0u;
+            qa[j][2] = lo_ok ? __ldg(qlo + 8 * j + 2 * tq + 1) : 0u;
+            qa[j][3] = hi_ok ? __ldg(qhi + 8 * j + 2 * tq + 1) : 0u;
+        }
+    }
+
+    float o[16][4];
+#pragma unroll
+    for (int nt = 0; nt < 16; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+    float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.f, l_hi = 0.f;
+    const int mi = lane >> 3, rr = lane & 7;
+    bool ok = true;
+    for (int li = 0; li < nloc; ++li) {
+        const int s = li % kQStages;
+        const uint32_t kt = ring + s * kQStage, vt = kt + kCodesBytes;
+        const uint32_t ks_s = sring + s * kQScaleStage, vs_s = ks_s + 4 * kBlockSize;
+        const int nvalid = min(kBlockSize, ctx - (blk_lo + warp + li * kQWarps) * kBlockSize);
+        if (!mbar_wait(bar0 + 8 * s, (uint32_t)(li / kQStages) & 1u)) {
+            ok = false;
+            break;
+        }
+        if (li == patch_li) {
+            const uint32_t off = code_off(new_t, 4 * lane);
+            asm volatile("st.shared.u32 [%0], %1;" ::"r"(kt + off), "r"(kcodes) : "memory");
+            asm volatile("st.shared.u32 [%0], %1;" ::"r"(vt + off), "r"(vcodes) : "memory");
+            if (lane == 0) {
+                asm volatile("st.shared.f32 [%0], %1;" ::"r"(ks_s + 4 * new_t), "f"(kscale) : "memory");
+                asm volatile("st.shared.f32 [%0], %1;" ::"r"(vs_s + 4 * new_t), "f"(vscale) : "memory");
+            }
+            __syncwarp();
+        }
+
+        // S = Q C_K^T over chunk pairs (j, j+1); matrices (tokens 0-7 | 8-15) x (chunk j | j+1).
+        float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+        for (int j = 0; j < 8; j += 2) {
+            uint32_t w[4];
+            ldsm_x4(kt + code_off(rr + (mi & 1) * 8, 16 * (j + (mi >> 1))), w);
+#pragma unroll
+            for (int jj = 0; jj < 2; ++jj)
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    const uint32_t bw = w[jj * 2 + nt] ^ 0x80808080u;
+                    mma_16816(sacc[nt], qa[j + jj], codes2_to_half2(bw, 0x4140u), codes2_to_half2(bw, 0x4342u));
+                }
+        }
+        // element e of tile nt: row g (e < 2) or g + 8, token 8nt + 2tq + (e & 1)
+        float ksc[2][2], vsc[2][2];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            float2 kk, vv;
+            asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(kk.x), "=f"(kk.y) : "r"(ks_s + 4 * (nt * 8 + 2 * tq)));
+            asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(vv.x), "=f"(vv.y) : "r"(vs_s + 4 * (nt * 8 + 2 * tq)));
+            ksc[nt][0] = kk.x; ksc[nt][1] = kk.y;
+            vsc[nt][0] = vv.x; vsc[nt][1] = vv.y;
+        }
+        float sv[2][4];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                sv[nt][e] = (nt * 8 + 2 * tq + (e & 1) < nvalid) ? sacc[nt][e] * ksc[nt][e & 1] * a.scale_log2
+                                                                : -INFINITY;
+        float mx = fmaxf(fmaxf(sv[0][0], sv[0][1]), fmaxf(sv[1][0], sv[1][1]));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        const float mn_lo = fmaxf(m_lo, mx);
+        const float al_lo = exp2f(m_lo - mn_lo);
+        m_lo = mn_lo;
+        float pr[2][4];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            pr[nt][0] = exp2f(sv[nt][0] - mn_lo);
+            pr[nt][1] = exp2f(sv[nt][1] - mn_lo);
+        }
+        l_lo = l_lo * al_lo + ((pr[0][0] + pr[0][1]) + (pr[1][0] + pr[1][1]));
+        float al_hi = 1.f;
+        if (ROWS16) {
+            float mh = fmaxf(fmaxf(sv[0][2], sv[0][3]), fmaxf(sv[1][2], sv[1][3]));
+            mh = fmaxf(mh, __shfl_xor_sync(0xffffffffu, mh, 1));
+            mh = fmaxf(mh, __shfl_xor_sync(0xffffffffu, mh, 2));
+            const float mn_hi = fmaxf(m_hi, mh);
+            al_hi = exp2f(m_hi - mn_hi);
+            m_hi = mn_hi;
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                pr[nt][2] = exp2f(sv[nt][2] - mn_hi);
+                pr[nt][3] = exp2f(sv[nt][3] - mn_hi);
+            }
+            l_hi = l_hi * al_hi + ((pr[0][2] + pr[0][3]) + (pr[1][2] + pr[1][3]));
+        } else {
+            pr[0][2] = pr[0][3] = pr[1][2] = pr[1][3] = 0.f;
+        }
+        // P * scale_V as the A operand (k = tokens); tokens past the context contribute exactly 0
+        float pw[2][4];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                pw[nt][e] = (nt * 8 + 2 * tq + (e & 1) < nvalid) ? pr[nt][e] * vsc[nt][e & 1] : 0.f;
+        const uint32_t pa[4] = {pack_half2(pw[0][0], pw[0][1]), pack_half2(pw[0][2], pw[0][3]),
+                                pack_half2(pw[1][0], pw[1][1]), pack_half2(pw[1][2], pw[1][3])};
+#pragma unroll
+        for (int nt = 0; nt < 16; ++nt) {
+            o[nt][0] *= al_lo;
+            o[nt][1] *= al_lo;
+            if (ROWS16) {
+                o[nt][2] *= al_hi;
+                o[nt][3] *= al_hi;
+            }
+        }
+        // O += P' C_V over chunk pairs; matrices (tokens 0-7 | 8-15) x (chunk cc | cc+1), transposed:
+        // a word holds (token 2tq: dims 2g, 2g+1; token 2tq+1: dims 2g, 2g+1) of its chunk.
+#pragma unroll
+        for (int cc = 0; cc < 8; cc += 2) {
+            uint32_t w[4];
+            ldsm_x4_t(vt + code_off(rr + (mi & 1) * 8, 16 * (cc + (mi >> 1))), w);
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const uint32_t lo = w[2 * u] ^ 0x80808080u, hi = w[2 * u + 1] ^ 0x80808080u;
+                mma_16816(o[2 * (cc + u)], pa, codes2_to_half2(lo, 0x4240u), codes2_to_half2(hi, 0x4240u));
+                mma_16816(o[2 * (cc + u) + 1], pa, codes2_to_half2(lo, 0x4341u), codes2_to_half2(hi, 0x4341u));
+            }
+        }
+        __syncwarp();
+        if (li + kQStages < nloc) {
+            if (lane == 0) {
+                fence_proxy_async_smem();
+                issue(li + kQStages);
+            }
+            ++issued;
+        }
+    }
+    if (!ok) {
+        if (lane == 0) {
+            atomicOr(a.status, PKV_DEV_TIMEOUT);
+            for (int li = max(0, issued - kQStages); li < issued; ++li)
+                mbar_wait(bar0 + 8 * (li % kQStages), (uint32_t)(li / kQStages) & 1u);
+        }
+        __syncwarp();
+    }
+    l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 1);
+    l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 2);
+    if (ROWS16) {
+        l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 1);
+        l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 2);
+    }
+
+    // ---- merge the four warps (warp order); O tile nt = 2 * chunk + parity holds dims 16 chunk + 4tq + 2e + parity
+    __syncthreads();
+    {
+        float* mo = reinterpret_cast<float*>(smem + kQSmMergeO) + warp * kQRows * kQMergeStride;
+        float* mml = reinterpret_cast<float*>(smem + kQSmMergeML) + warp * kQRows * 2;
+#pragma unroll
+        for (int nt = 0; nt < 16; ++nt) {
+            const int d0 = 16 * (nt >> 1) + 4 * tq + (nt & 1);
+            mo[g * kQMergeStride + d0] = o[nt][0];
+            mo[g * kQMergeStride + d0 + 2] = o[nt][1];
+            if (ROWS16) {
+                mo[(g + 8) * kQMergeStride + d0] = o[nt][2];
+                mo[(g + 8) * kQMergeStride + d0 + 2] = o[nt][3];
+            }
+        }
+        if (tq == 0) {
+            mml[2 * g] = m_lo;
+            mml[2 * g + 1] = l_lo;
+            if (ROWS16) {
+                mml[2 * (g + 8)] = m_hi;
+                mml[2 * (g + 8) + 1] = l_hi;
+            }
+        }
+    }
+    __syncthreads();
+    const int d = threadIdx.x;
+    const float* mo = reinterpret_cast<const float*>(smem + kQSmMergeO);
+    const float* mml = reinterpret_cast<const float*>(smem + kQSmMergeML);
+    const int64_t rh0 = (int64_t)r * a.num_q_heads + h0;
+    for (int row = 0; row < a.rows; ++row) {
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kQWarps; ++w) M = fmaxf(M, mml[(w * kQRows + row) * 2]);
+        float L = 0.f, O = 0.f;
+#pragma unroll
+        for (int w = 0; w < kQWarps; ++w) {
+            const float wt = exp2f(mml[(w * kQRows + row) * 2] - M);
+            L = fmaf(wt, mml[(w * kQRows + row) * 2 + 1], L);
+            O = fmaf(wt, mo[(w * kQRows + row) * kQMergeStride + d], O);
+        }
+        if (nparts == 1) {
+            a.out[(rh0 + row) * kHeadDim + d] = __float2half_rn(O * (1.f / L));
+        } else {
+            const int64_t slot = (rh0 + row) * a.max_parts + p;
+            a.ws_o[slot * kHeadDim + d] = O;
+            if (d == 0) {
+                a.ws_ml[slot * 2] = M;
+                a.ws_ml[slot * 2 + 1] = L;
+            }
+        }
+    }
+    if (nparts == 1) return;
+
+    __syncthreads();
+    unsigned int* counter = a.counters + ((int64_t)r * a.num_kv_heads + kvh) * a.slices + c;
+    unsigned int* flag = reinterpret_cast<unsigned int*>(smem + kQSmFlag);
+    if (threadIdx.x == 0) *flag = q_atomic_add_acq_rel(counter, 1u) == (unsigned int)(nparts - 1);
+    __syncthreads();
+    if (!*flag) return;
+    for (int row = 0; row < a.rows; ++row) {
+        const int64_t base = (rh0 + row) * a.max_parts;
+        float M = -INFINITY;
+        for (int q = 0; q < nparts; ++q) M = fmaxf(M, __ldcg(a.ws_ml + (base + q) * 2));
+        float L = 0.f, O = 0.f;
+        for (int q = 0; q < nparts; ++q) {
+            const float wt = exp2f(__ldcg(a.ws_ml + (base + q) * 2) - M);
+            L = fmaf(wt, __ldcg(a.ws_ml + (base + q) * 2 + 1), L);
+            O = fmaf(wt, __ldcg(a.ws_o + (base + q) * kHeadDim + d), O);
+        }
+        a.out[(rh0 + row) * kHeadDim + d] = __float2half_rn(O * (1.f / L));
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) *counter = 0u;
+}
+
+template <bool ROWS16>
+cudaError_t launch_i8(const CUtensorMap& tmap, const I8Args& a, int num_seqs, cudaStream_t stream)
+{
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 64 && !attr_set[dev]) {
+        cudaError_t e =
+            cudaFuncSetAttribute(decode_i8_kernel<ROWS16>, cudaFuncAttributeMaxDynamicSharedMemorySize, kQSmAlloc);
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = true;
+    }
+    dim3 grid(a.max_parts, a.num_kv_heads * a.slices, num_seqs);
+    decode_i8_kernel<ROWS16><<<grid, kQWarps * 32, kQSmAlloc, stream>>>(tmap, a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_kv_append_i8(const PoolGeom& g, int layer, const void* k, const void* v, const int64_t* slots,
+                                int num_tokens, unsigned int* status, cudaStream_t stream)
+{
+    if (num_tokens == 0) return cudaSuccess;
+    const int64_t threads_total = 2LL * g.num_heads * num_tokens * 32;
+    const int threads = 256;
+    const int64_t blocks = (threads_total + threads - 1) / threads;
+    kv_append_i8_kernel<<<(unsigned)blocks, threads, 0, stream>>>(
+        const_cast<char*>(g.base), g.block_bytes, (int64_t)layer * g.layer_bytes, g.kv_bytes, g.num_heads,
+        static_cast<const __half*>(k), static_cast<const __half*>(v), slots, num_tokens, g.num_blocks * kBlockSize,
+        status);
+    return cudaGetLastError();
+}
+
+// Map over an 8-bit pool's code tiles: [block][layer][2 x heads tiles, 2,112 B apart][16 rows][128 bytes];
+// one box is a tile's 2,048 code bytes, copied with the 128-byte swizzle.
+bool encode_i8_tmap(const PoolGeom& g, TensorMap128* out, std::string* err)
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+    if (!encode) {
+        cudaDriverEntryPointQueryResult q;
+        void* fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || !fn) {
+            if (err) *err = "cuTensorMapEncodeTiled unavailable";
+            return false;
+        }
+        encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    const cuuint64_t dims[5] = {(cuuint64_t)kHeadDim, (cuuint64_t)kBlockSize, (cuuint64_t)(2 * g.num_heads),
+                                (cuuint64_t)g.num_layers, (cuuint64_t)g.num_blocks};
+    const cuuint64_t strides[4] = {(cuuint64_t)kHeadDim, (cuuint64_t)kTileBytesI8, (cuuint64_t)g.layer_bytes,
+                                   (cuuint64_t)g.block_bytes};
+    const cuuint32_t box[5] = {(cuuint32_t)kHeadDim, (cuuint32_t)kBlockSize, 1, 1, 1};
+    const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    CUresult r = encode(reinterpret_cast<CUtensorMap*>(out->bytes), CU_TENSOR_MAP_DATA_TYPE_UINT8, 5,
+                        const_cast<char*>(g.base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        if (err) *err = "cuTensorMapEncodeTiled failed";
+        return false;
+    }
+    return true;
+}
+
+cudaError_t launch_decode_i8(const PoolGeom& g, const TensorMap128& i8_tmap, int layer, const void* q,
+                             const int32_t* tables, int max_blocks, const int32_t* ctx_lens, int num_seqs,
+                             float scale, void* out, const DecodeWs& ws, int partition_tokens, const void* k_new,
+                             const void* v_new, const int64_t* slots, unsigned int* status, cudaStream_t stream)
+{
+    if (num_seqs == 0) return cudaSuccess;
+    I8Args a;
+    a.q = static_cast<const __half*>(q);
+    a.out = static_cast<__half*>(out);
+    a.tables = tables;
+    a.max_blocks = max_blocks;
+    a.ctx_lens = ctx_lens;
+    a.pool = const_cast<char*>(g.base);
+    a.block_bytes = g.block_bytes;
+    a.head_off = (int64_t)layer * g.layer_bytes;
+    a.kv_bytes = g.kv_bytes;
+    a.num_blocks = g.num_blocks;
+    a.layer = layer;
+    a.num_kv_heads = g.num_heads;
+    a.num_q_heads = g.num_q_heads;
+    a.group = g.group;
+    a.slices = decode_group_slices(g.group);
+    a.rows = g.group / a.slices;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    a.ws_o = ws.o;
+    a.ws_ml = ws.ml;
+    a.counters = ws.counters;
+    a.max_parts = decode_max_parts(max_blocks, partition_tokens);
+    a.part_tokens = partition_tokens;
+    a.k_new = static_cast<const __half*>(k_new);
+    a.v_new = static_cast<const __half*>(v_new);
+    a.slots = slots;
+    a.append = k_new != nullptr;
+    a.status = status;
+    CUtensorMap tmap;
+    static_assert(sizeof(tmap) == sizeof(i8_tmap.bytes), "tensor map size");
+    memcpy(&tmap, i8_tmap.bytes, sizeof(tmap));
+    return a.rows > 8 ? launch_i8<true>(tmap, a, num_seqs, stream) : launch_i8<false>(tmap, a, num_seqs, stream);
+}
+
+}  // namespace pkv

@@ -14,6 +14,8 @@ namespace pkv {
 constexpr int kHeadDim = 128;
 constexpr int kBlockSize = 16;
 constexpr int kTileBytes = kBlockSize * kHeadDim * 2;  // one head of one block: 4,096 B
+// 8-bit pools: a tile is the 16 x 128 INT8 codes followed by 16 FP32 scales (one per token row).
+constexpr int kTileBytesI8 = kBlockSize * kHeadDim + 4 * kBlockSize;  // 2,112 B
 // Decode split-K partition: large enough that a CTA's start-up (metadata loads,
 // first copies) is a small part of its life, small enough that long rows still
 // spread over the GPU. Measured on the batch-32 decode workloads (1,024 beat
@@ -35,9 +37,11 @@ struct PoolGeom {
     int32_t num_heads;    // K/V heads stored per layer
     int32_t num_q_heads;  // query heads (a multiple of num_heads)
     int32_t group;        // num_q_heads / num_heads: query head h reads K/V head h / group
-    int64_t block_bytes;  // one block, all layers: L * 2 * H * 4096
-    int64_t layer_bytes;  // one layer of one block: 2 * H * 4096
-    int64_t kv_bytes;     // K half to V half: H * 4096
+    int32_t dtype;        // PKV_DTYPE_FP16 or PKV_DTYPE_INT8
+    int64_t tile_bytes;   // one (block, layer, K/V, head) tile: kTileBytes or kTileBytesI8
+    int64_t block_bytes;  // one block, all layers: L * 2 * H * tile_bytes
+    int64_t layer_bytes;  // one layer of one block: 2 * H * tile_bytes
+    int64_t kv_bytes;     // K half to V half: H * tile_bytes
 };
 
 // Split-K scratch of one decode launch, carved from the caller's workspace.
@@ -62,7 +66,7 @@ struct pkv_pool {
     pkv::PoolGeom geom{};
     pkv::TensorMap128 kv_tmap{};  // 5-D TMA map over the pool (prefill K/V tiles)
     bool kv_tmap_ok = false;
-    pkv::TensorMap128 tile_tmap{};  // TMA map whose box is one whole 4 KB K or V tile (grouped decode)
+    pkv::TensorMap128 tile_tmap{};  // decode map: a whole 4 KB FP16 tile (grouped decode) or an 8-bit tile's codes
     bool tile_tmap_ok = false;
     std::vector<int32_t> ref;
     std::vector<int32_t> free_stack;  // back() is handed out next
@@ -90,6 +94,15 @@ cudaError_t launch_decode(const PoolGeom& g, int layer, const void* q, const int
                           const int32_t* ctx_lens, int num_seqs, float scale, void* out, void* ws,
                           int partition_tokens, const void* k_new, const void* v_new, const int64_t* slots,
                           unsigned int* status, cudaStream_t stream);
+
+// pkv_int8.cu: the 8-bit cache (quantising kv_append; decode that dequantises in its loaders).
+cudaError_t launch_kv_append_i8(const PoolGeom& g, int layer, const void* k, const void* v, const int64_t* slots,
+                                int num_tokens, unsigned int* status, cudaStream_t stream);
+bool encode_i8_tmap(const PoolGeom& g, TensorMap128* out, std::string* err);
+cudaError_t launch_decode_i8(const PoolGeom& g, const TensorMap128& i8_tmap, int layer, const void* q,
+                             const int32_t* tables, int max_blocks, const int32_t* ctx_lens, int num_seqs,
+                             float scale, void* out, const DecodeWs& ws, int partition_tokens, const void* k_new,
+                             const void* v_new, const int64_t* slots, unsigned int* status, cudaStream_t stream);
 
 // pkv_decode_group.cu: decode attention for pools whose K/V heads serve groups of query heads.
 bool encode_tile_tmap(const PoolGeom& g, TensorMap128* out, std::string* err);

@@ -31,6 +31,17 @@ def device_pool(num_blocks, num_layers, num_heads=32, seed=0, on_gpu_rng=False):
     return workloads.normal_fp16(shape, workloads.value_seed(seed, "pool")).cuda()
 
 
+def device_pool_i8(num_blocks, num_layers, num_heads=32, seed=0):
+    """An 8-bit pool with valid contents everywhere: codes uniform in [-127, 127], scales in [0.004, 0.03)
+    (about what N(0,1) rows quantise to). Returns the device uint8 tensor [blocks, layers, 2, heads, 2112]."""
+    rng = np.random.default_rng(workloads.value_seed(seed, "pool") + 7)
+    tiles = np.empty((num_blocks, num_layers, 2, num_heads, 2112), np.uint8)
+    tiles[..., :2048] = rng.integers(-127, 128, tiles[..., :2048].shape).astype(np.int8).view(np.uint8)
+    scales = rng.uniform(0.004, 0.03, (num_blocks, num_layers, 2, num_heads, 16)).astype(np.float32)
+    tiles[..., 2048:] = scales.view(np.uint8).reshape(num_blocks, num_layers, 2, num_heads, 64)
+    return torch.from_numpy(tiles).cuda()
+
+
 def to_bits(t: torch.Tensor) -> np.ndarray:
     return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
 

@@ -46,7 +46,7 @@ def test_pool_bytes_matches_page_ledger(pkv):
     assert pkv.load().pkv_pool_bytes(ctypes.byref(bad)) == 0
 
 
-@pytest.mark.parametrize("field,value", [("head_dim", 64), ("block_size", 32), ("dtype", 1), ("num_blocks", 0),
+@pytest.mark.parametrize("field,value", [("head_dim", 64), ("block_size", 32), ("dtype", 2), ("num_blocks", 0),
                                          ("partition_tokens", 100), ("partition_tokens", 4096), ("num_heads", 0),
                                          ("num_q_heads", 6), ("num_q_heads", 2), ("num_q_heads", 2048)])
 def test_pool_create_refuses_bad_descriptor(pkv, field, value):
@@ -70,6 +70,17 @@ def test_grouped_query_pool_ledger_and_workspace(pkv):
         assert mqa.decode_workspace_bytes(rows, width) == mha.decode_workspace_bytes(rows, width)
     assert pkv.Pool(None, 64, num_heads=8, num_q_heads=8).decode_workspace_bytes(32, 300) < \
         gqa.decode_workspace_bytes(32, 300)
+
+
+def test_int8_pool_bytes_and_refusals(pkv):
+    # 8-bit tiles: 16 x 128 codes + 16 float32 scales = 2,112 B; the oracle's own ledger agrees
+    for n, L, H in [(7152, 32, 32), (64, 1, 32), (10, 3, 8)]:
+        got = pkv.Pool.bytes_needed(n, num_layers=L, num_heads=H, dtype="int8")
+        assert got == n * L * 2 * H * 2112 == oracle.pool_bytes(oracle.geom(n, L, H, dtype=oracle.INT8))
+    assert pkv.Pool.bytes_needed(1, dtype="int8") * 2 < pkv.Pool.bytes_needed(1) * 1.04
+    # grouped query heads work over an 8-bit pool too; the workspace follows the query heads
+    p = pkv.Pool(None, 64, num_heads=8, num_q_heads=32, dtype="int8")
+    assert p.decode_workspace_bytes(32, 300) == pkv.Pool(None, 64, num_heads=32).decode_workspace_bytes(32, 300)
 
 
 def test_free_order_must_be_a_permutation(pkv):

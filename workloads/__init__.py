@@ -275,6 +275,22 @@ def fill_normal_fp16_(t, seed: int, chunk_elems: int = 1 << 28):
     return t
 
 
+def fill_int8_tiles_(t, seed: int, scale: float = 0.02, chunk_tiles: int = 1 << 17):
+    """Fill an 8-bit pool (uint8 tensor of whole 2,112-byte tiles) in place: codes uniform in [-127, 127],
+    every scale ``scale`` (about what N(0,1) rows quantise to), chunk by chunk on the tensor's device."""
+    import torch
+    tiles = t.view(-1, 2112)
+    gen = torch.Generator(device=t.device)
+    gen.manual_seed(seed)
+    sbytes = torch.full((16,), scale, dtype=torch.float32).view(torch.uint8).to(t.device)
+    for s in range(0, tiles.shape[0], chunk_tiles):
+        n = min(chunk_tiles, tiles.shape[0] - s)
+        codes = torch.randint(-127, 128, (n, 2048), generator=gen, device=t.device, dtype=torch.int16)
+        tiles[s:s + n, :2048].copy_(codes.to(torch.int8).view(torch.uint8))
+        tiles[s:s + n, 2048:].copy_(sbytes.expand(n, 64))
+    return t
+
+
 def pool_shape(num_blocks: int, num_layers: int, num_heads: int = NUM_HEADS, head_dim: int = HEAD_DIM,
                block_size: int = BLOCK_SIZE):
     """[block, layer, K/V, head, token-in-block, dim] — one block holds every layer."""
