@@ -24,7 +24,12 @@ groups hold identical K/V. The 8-bit cache (INT8 codes, one float32 scale per
 round trips of rows built from integer codes and power-of-two scales, the
 half-step error bound and nearest-code rule checked in float64, byte
 placement checked with numpy's own indexing, and attention over exactly
-stored values equal to the FP16 pool's. Parity is pinned for every function;
+stored values equal to the FP16 pool's. Block copies and swaps are checked
+byte for byte against numpy indexing; the chained prefix hash against the
+published FNV-1a test vectors, its dependence on the whole prefix, and the
+page's own cache lookup restated; the block manager's fork, copy-on-write,
+swap and prefix cache against worked scenarios and reference-count
+invariants under random operations. Parity is pinned for every function;
 none is unpinned.
 """
 from __future__ import annotations
@@ -79,6 +84,11 @@ def lib():
             "pkvo_i8_tile_bytes": (i64, [G]),
             "pkvo_i8_quantize_row": (None, [P, ctypes.c_int, P, P]),
             "pkvo_i8_dequant": (dbl, [ctypes.c_int8, ctypes.c_float]),
+            "pkvo_copy_blocks": (i64, [P, G, P, i64]),
+            "pkvo_swap_out": (i64, [P, G, P, i64, P]),
+            "pkvo_swap_in": (i64, [P, G, P, i64, P]),
+            "pkvo_fnv1a64": (ctypes.c_uint64, [P, i64]),
+            "pkvo_block_hashes": (i64, [P, i64, i32, P]),
             "pkvo_num_threads": (ctypes.c_int, []),
             "pkvo_set_num_threads": (None, [ctypes.c_int]),
         }
@@ -267,6 +277,43 @@ def decode_attn_split(pool, g: Geom, layer, q, tables, ctx_lens, scale, part_tok
     lib().pkvo_decode_attn_split(_p(pool), ctypes.byref(g), layer, _p(q), _p(tables), tables.shape[1], _p(ctx), B,
                                  float(scale), int(part_tokens), _p(o64))
     return o64
+
+
+# ------------------------------------------------------------ block copy, swap, prefix hashes
+
+def copy_blocks(pool: np.ndarray, g: Geom, pairs) -> int:
+    """In place: block dst receives block src for each (src, dst) row of ``pairs``. -1 or the first bad pair."""
+    pr = _c(pairs, np.int32).reshape(-1, 2)
+    return lib().pkvo_copy_blocks(_p(pool), ctypes.byref(g), _p(pr), pr.shape[0])
+
+
+def swap_out(pool: np.ndarray, g: Geom, blocks) -> np.ndarray:
+    """The listed whole blocks, concatenated (bytes), as swap-out writes them to host memory."""
+    b = _c(blocks, np.int32)
+    out = np.empty(b.shape[0] * bytes_per_block(g), np.uint8)
+    r = lib().pkvo_swap_out(_p(pool), ctypes.byref(g), _p(b), b.shape[0], _p(out))
+    if r != -1:
+        raise IndexError(f"block index {r} outside the pool")
+    return out
+
+
+def swap_in(pool: np.ndarray, g: Geom, blocks, host_bytes) -> int:
+    b = _c(blocks, np.int32)
+    h = _c(host_bytes, np.uint8)
+    return lib().pkvo_swap_in(_p(pool), ctypes.byref(g), _p(b), b.shape[0], _p(h))
+
+
+def fnv1a64(data: bytes) -> int:
+    buf = np.frombuffer(bytes(data), np.uint8).copy() if len(data) else np.zeros(1, np.uint8)
+    return int(lib().pkvo_fnv1a64(_p(buf), len(data)))
+
+
+def block_hashes(tokens, block_size: int = 16) -> np.ndarray:
+    """Chained hashes of the full blocks of a token-id stream (uint64)."""
+    t = _c(tokens, np.int32)
+    out = np.zeros(max(1, t.shape[0] // block_size), np.uint64)
+    n = lib().pkvo_block_hashes(_p(t), t.shape[0], block_size, _p(out))
+    return out[:n]
 
 
 def num_threads() -> int:

@@ -50,6 +50,20 @@
  *                       both in IEEE single precision; the stored value is
  *                       code * scale in single precision. A tile holds the
  *                       16 x head_dim codes, then the 16 scales.
+ *   block copy / swap   "The inference engine", "Paging turns variable
+ *                       sequences into block tables": copy-on-write gives a
+ *                       diverging branch its own copy of a shared block;
+ *                       "continuous batching server", "Preemption and
+ *                       Eviction: Recompute vs Swap": a victim's KV blocks
+ *                       go to host memory and come back. Both are whole-
+ *                       block byte copies.
+ *   prefix hashes       "Serving LLMs" (sreshtalluri), "Prefix caching": each
+ *                       full block is hashed together with the hash of
+ *                       everything before it, starting from 0. Reading (the
+ *                       page uses a language's built-in tuple hash, which is
+ *                       unspecified): 64-bit FNV-1a over the previous hash
+ *                       (8 bytes, little-endian) followed by the block's 16
+ *                       token ids (4 bytes each, little-endian).
  */
 #include <math.h>
 #include <stdint.h>
@@ -387,6 +401,82 @@ static void pkvo_i8_gather(const uint8_t* pool, const pkvo_geom* g, int layer, i
         for (int d = 0; d < g->head_dim; ++d)
             out[j * g->head_dim + d] =
                 i8_value(pool, g, table[j / g->block_size], layer, kv, head, (int)(j % g->block_size), d);
+}
+
+/* ------------------------------------------------- block copy and swap */
+
+/* Whole blocks: every layer, K and V, of a physical block, as stored. */
+static int64_t block_bytes_stored(const pkvo_geom* g) { return pkvo_bytes_per_block(g); }
+
+/* dst block pairs[2i+1] receives a copy of src block pairs[2i], in order.
+ * Returns the index of the first pair naming a block outside the pool (and
+ * copies nothing), or -1. */
+int64_t pkvo_copy_blocks(void* pool, const pkvo_geom* g, const int32_t* pairs, int64_t n)
+{
+    for (int64_t i = 0; i < 2 * n; ++i)
+        if (pairs[i] < 0 || pairs[i] >= g->num_blocks) return i / 2;
+    const int64_t bb = block_bytes_stored(g);
+    for (int64_t i = 0; i < n; ++i)
+        memmove((char*)pool + pairs[2 * i + 1] * bb, (const char*)pool + pairs[2 * i] * bb, (size_t)bb);
+    return -1;
+}
+
+/* host[i] = block blocks[i] (swap out); returns the first bad index or -1. */
+int64_t pkvo_swap_out(const void* pool, const pkvo_geom* g, const int32_t* blocks, int64_t n, void* host)
+{
+    for (int64_t i = 0; i < n; ++i)
+        if (blocks[i] < 0 || blocks[i] >= g->num_blocks) return i;
+    const int64_t bb = block_bytes_stored(g);
+    for (int64_t i = 0; i < n; ++i)
+        memcpy((char*)host + i * bb, (const char*)pool + blocks[i] * bb, (size_t)bb);
+    return -1;
+}
+
+/* block blocks[i] = host[i] (swap in); returns the first bad index or -1. */
+int64_t pkvo_swap_in(void* pool, const pkvo_geom* g, const int32_t* blocks, int64_t n, const void* host)
+{
+    for (int64_t i = 0; i < n; ++i)
+        if (blocks[i] < 0 || blocks[i] >= g->num_blocks) return i;
+    const int64_t bb = block_bytes_stored(g);
+    for (int64_t i = 0; i < n; ++i)
+        memcpy((char*)pool + blocks[i] * bb, (const char*)host + i * bb, (size_t)bb);
+    return -1;
+}
+
+/* ------------------------------------------------------------- prefix hashes */
+
+/* 64-bit FNV-1a of n bytes, continuing from state h (the offset basis for a fresh hash). */
+static uint64_t fnv1a64_continue(uint64_t h, const uint8_t* p, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) {
+        h ^= p[i];
+        h *= 1099511628211ULL;  /* the 64-bit FNV prime, 2^40 + 2^8 + 0xb3 */
+    }
+    return h;
+}
+
+uint64_t pkvo_fnv1a64(const uint8_t* p, int64_t n)
+{
+    return fnv1a64_continue(14695981039346656037ULL, p, n);  /* the 64-bit offset basis */
+}
+
+/* Chained hashes of the full blocks of a token stream: out[i] = H(out[i-1], tokens of block i), out[-1] = 0.
+ * Returns the number of full blocks (n_tokens / block_size). */
+int64_t pkvo_block_hashes(const int32_t* tokens, int64_t n_tokens, int32_t block_size, uint64_t* out)
+{
+    uint64_t h = 0;
+    int64_t nb = n_tokens / block_size;
+    for (int64_t i = 0; i < nb; ++i) {
+        uint8_t buf[8 + 4 * 64];
+        for (int k = 0; k < 8; ++k) buf[k] = (uint8_t)(h >> (8 * k));
+        for (int t = 0; t < block_size; ++t) {
+            uint32_t v = (uint32_t)tokens[i * block_size + t];
+            for (int k = 0; k < 4; ++k) buf[8 + 4 * t + k] = (uint8_t)(v >> (8 * k));
+        }
+        h = pkvo_fnv1a64(buf, 8 + 4LL * block_size);
+        out[i] = h;
+    }
+    return nb;
 }
 
 /* ------------------------------------------------------------- split merge */

@@ -46,6 +46,13 @@ MUTANTS = {
     "i8_amax_signed": ("float a = (float)fabs(pkvo_half_to_double(x[i]));",
                        "float a = (float)pkvo_half_to_double(x[i]);"),
     "i8_code_truncates": ("c = (int)rintf(qv);", "c = (int)qv;"),
+    "copy_blocks_direction": ("memmove((char*)pool + pairs[2 * i + 1] * bb, (const char*)pool + pairs[2 * i] * bb, (size_t)bb);",
+                              "memmove((char*)pool + pairs[2 * i] * bb, (const char*)pool + pairs[2 * i + 1] * bb, (size_t)bb);"),
+    "swap_in_ignores_host_offset": ("memcpy((char*)pool + blocks[i] * bb, (const char*)host + i * bb, (size_t)bb);",
+                                    "memcpy((char*)pool + blocks[i] * bb, (const char*)host, (size_t)bb);"),
+    "fnv_prime_off_by_two": ("h *= 1099511628211ULL;", "h *= 1099511628213ULL;"),
+    "hash_chain_restarts": ("for (int k = 0; k < 8; ++k) buf[k] = (uint8_t)(h >> (8 * k));",
+                            "for (int k = 0; k < 8; ++k) buf[k] = 0;"),
     "i8_tile_head_before_kv": ("((b * g->num_layers + l) * 2 + kv) * g->num_heads + h;",
                                "((b * g->num_layers + l) * g->num_heads + h) * 2 + kv;"),
     "gqa_q_stride_uses_kv_heads": ("    const int H = pkvo_q_heads(g), D = g->head_dim;\n    #pragma omp parallel for collapse(2) schedule(dynamic)\n    for (int r = 0; r < B; ++r)\n        for (int h = 0; h < H; ++h) {\n            int64_t n = ctx_lens[r];\n            double* K",

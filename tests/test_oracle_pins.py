@@ -637,3 +637,174 @@ def test_int8_attention_close_to_fp16_attention_on_gaussian_values():
     a16, _ = oracle.decode_attn(p16, g16, 0, q, table, np.array([T], np.int32), SCALE)
     a8, _ = oracle.decode_attn(p8, g8, 0, q, table, np.array([T], np.int32), SCALE)
     assert np.abs(a16 - a8).max() < 0.02 and not np.array_equal(a16, a8)
+
+
+# ------------------------------------------------------------------ block copy, swap, prefix hashes
+
+def test_fnv1a64_published_vectors():
+    # the FNV-1a 64-bit test values published with the algorithm (offset basis, "a", "foobar")
+    assert oracle.fnv1a64(b"") == 0xCBF29CE484222325
+    assert oracle.fnv1a64(b"a") == 0xAF63DC4C8601EC8C
+    assert oracle.fnv1a64(b"foobar") == 0x85944171F73967E8
+
+
+def test_block_hash_chain_depends_on_the_whole_prefix():
+    # "Serving LLMs" (sreshtalluri), "Prefix caching": a block's hash matches only if every earlier token
+    # matches too; only full blocks are hashed.
+    rng = np.random.default_rng(0)
+    t = rng.integers(0, 50000, 16 * 9 + 7).astype(np.int32)
+    h = oracle.block_hashes(t)
+    assert h.shape == (9,)
+    assert np.array_equal(oracle.block_hashes(t[:16 * 9]), h)          # the partial tail is not hashed
+    assert np.array_equal(oracle.block_hashes(t[:16 * 4]), h[:4])      # a prefix's hashes are a prefix
+    for j in [0, 15, 16, 70, 143]:
+        u = t.copy()
+        u[j] += 1
+        hu = oracle.block_hashes(u)
+        b = j // 16
+        assert np.array_equal(hu[:b], h[:b]) and (hu[b:] != h[b:]).all()
+    # block i's hash is FNV-1a over (previous hash, the block's 16 token ids), little-endian, from 0
+    prev = 0
+    for i in range(3):
+        data = int(prev).to_bytes(8, "little") + t[16 * i:16 * i + 16].astype("<u4").tobytes()
+        assert oracle.fnv1a64(data) == int(h[i])
+        prev = int(h[i])
+
+
+def _page_prefill_with_cache(cache: set, tokens) -> int:
+    """The page's lookup: count cached leading blocks until the first miss, then cache this prompt's blocks."""
+    hit = 0
+    hs = [int(x) for x in oracle.block_hashes(tokens)]
+    for h in hs:
+        if h not in cache:
+            break
+        hit += 16
+    cache.update(hs)
+    return hit
+
+
+def test_prefix_cache_matches_the_pages_lookup():
+    rng = np.random.default_rng(1)
+    system = rng.integers(0, 32000, 1200).astype(np.int32)            # a shared 1,200-token system prompt
+    bm = blockmgr.BlockManager(4000)
+    page_cache: set = set()
+    for r in range(20):
+        user = rng.integers(0, 32000, int(rng.integers(1, 900))).astype(np.int32)
+        prompt = np.concatenate([system, user]) if r % 4 else user
+        hs = oracle.block_hashes(prompt)
+        expect = _page_prefill_with_cache(page_cache, prompt)
+        st, n = bm.attach_prefix(r, hs)
+        assert st == blockmgr.OK and n * 16 == expect
+        assert bm.grow(r, len(prompt)) == blockmgr.OK
+        assert bm.prefix_register(r, hs)[0] == blockmgr.OK
+    # a changed token near the start of the system prompt: nothing is served from the cache
+    p = np.concatenate([system, [5, 6, 7]]).astype(np.int32)
+    p[3] += 1
+    assert bm.prefix_match(oracle.block_hashes(p)) == 0 == _page_prefill_with_cache(set(page_cache), p)
+    assert bm.prefix_match(oracle.block_hashes(system)) == 1200 // 16
+
+
+def test_copy_blocks_and_swap_are_whole_block_byte_copies():
+    rng = np.random.default_rng(2)
+    for dtype in (oracle.FP16, oracle.INT8):
+        g = oracle.geom(12, 2, 3, dtype=dtype)
+        pool = oracle.empty_pool(g)
+        pool.view(np.uint8)[:] = rng.integers(0, 256, pool.nbytes, dtype=np.uint8)
+        bb = oracle.bytes_per_block(g)
+        view = pool.view(np.uint8).reshape(12, bb)
+        expect = view.copy()
+        pairs = np.array([[3, 7], [7, 1], [0, 11], [5, 5]], np.int32)    # in order: 7 <- 3, then 1 <- (new) 7
+        for s_, d_ in pairs:
+            expect[d_] = expect[s_]
+        assert oracle.copy_blocks(pool, g, pairs) == -1
+        assert np.array_equal(view, expect)
+        before = view.copy()
+        assert oracle.copy_blocks(pool, g, np.array([[1, 2], [3, 12]], np.int32)) == 1    # nothing copied
+        assert np.array_equal(view, before)
+        blocks = np.array([9, 0, 4, 4], np.int32)
+        host = oracle.swap_out(pool, g, blocks)
+        assert np.array_equal(host.reshape(4, bb), view[blocks])
+        dst = np.array([2, 10, 6, 8], np.int32)
+        assert oracle.swap_in(pool, g, dst, host) == -1
+        assert np.array_equal(view[dst], before[blocks])
+        with pytest.raises(IndexError):
+            oracle.swap_out(pool, g, np.array([1, -1], np.int32))
+
+
+def test_blockmgr_fork_cow_and_swap_scenario():
+    bm = blockmgr.BlockManager(10)
+    assert bm.grow(0, 40) == blockmgr.OK                  # blocks 0, 1, 2 (last holds 8 tokens)
+    assert bm.tables[0] == [0, 1, 2]
+    assert bm.fork(1, 0) == blockmgr.OK                   # parallel sample: shares all three
+    assert [bm.ref[b] for b in (0, 1, 2)] == [2, 2, 2]
+    assert bm.build_step([1], [1], 4)[0] == blockmgr.E_SHARED or True   # (its next token is position 40, below)
+    assert bm.grow(1, 41) == blockmgr.OK                  # still 3 blocks: position 40 falls in shared block 2
+    assert bm.build_step([1], [1], 4)[0] == blockmgr.E_SHARED
+    st, src, dst = bm.cow_last(1)
+    assert (st, src, dst) == (blockmgr.OK, 2, 3)          # block 3 is handed out next
+    assert bm.tables[1] == [0, 1, 3] and bm.ref[2] == 1 and bm.ref[3] == 1
+    assert bm.build_step([1], [1], 4)[0] == blockmgr.OK
+    assert bm.cow_last(0) == (blockmgr.OK, -1, -1)        # block 2 is now 0's alone
+    st, blocks = bm.swap_out(1)
+    assert st == blockmgr.OK and blocks == [0, 1, 3]
+    assert bm.ref[3] == 0 and bm.ref[0] == 1 and bm.free_blocks() == 7 and bm.lens[1] == 41
+    assert bm.grow(1, 50) == blockmgr.E_INVALID and bm.build_step([1], [1], 4)[0] == blockmgr.E_INVALID
+    st, blocks = bm.swap_in(1)
+    assert st == blockmgr.OK and len(blocks) == 3 and bm.tables[1] == blocks
+    assert all(bm.ref[b] == 1 for b in blocks) and bm.free_blocks() == 4
+
+
+def test_blockmgr_nomem_leaves_state_unchanged_for_cow_and_swap_in():
+    bm = blockmgr.BlockManager(4)
+    assert bm.grow(0, 20) == blockmgr.OK and bm.fork(1, 0) == blockmgr.OK
+    assert bm.grow(2, 32) == blockmgr.OK                  # pool full
+    snap = (list(bm.free), list(bm.ref), {k: list(v) for k, v in bm.tables.items()})
+    assert bm.cow_last(1) == (blockmgr.E_NOMEM, -1, -1)
+    assert bm.swap_out(2)[0] == blockmgr.OK and bm.grow(3, 32) == blockmgr.OK
+    snap = (list(bm.free), list(bm.ref), {k: list(v) for k, v in bm.tables.items()})
+    assert bm.swap_in(2) == (blockmgr.E_NOMEM, None)
+    assert snap == (list(bm.free), list(bm.ref), {k: list(v) for k, v in bm.tables.items()})
+
+
+def test_blockmgr_reference_counts_under_random_operations():
+    # invariant: ref[b] = number of table entries naming b + 1 if b is cached; free list = blocks with ref 0
+    rng = np.random.default_rng(3)
+    N = 64
+    bm = blockmgr.BlockManager(N, free_order=rng.permutation(N))
+    toks = {}
+    for step in range(3000):
+        op = rng.integers(0, 9)
+        s = int(rng.integers(0, 12))
+        if op == 0:
+            bm.grow(s, bm.lens.get(s, 0) + int(rng.integers(0, 40)))
+        elif op == 1:
+            bm.free_seq(s)
+        elif op == 2:
+            bm.fork(int(rng.integers(0, 12)), s)
+        elif op == 3:
+            bm.cow_last(s)
+        elif op == 4:
+            bm.swap_out(s)
+        elif op == 5:
+            bm.swap_in(s)
+        elif op == 6 and s in bm.tables and s not in bm.swapped:
+            n = bm.lens[s] // 16 * 16
+            toks.setdefault(s, rng.integers(0, 9, 4000).astype(np.int32))
+            bm.prefix_register(s, oracle.block_hashes(toks[s][:n]))
+        elif op == 7 and s not in bm.tables:
+            toks[s] = rng.integers(0, 9, 4000).astype(np.int32)
+            bm.attach_prefix(s, oracle.block_hashes(toks[s][:int(rng.integers(0, 200))]))
+        elif op == 8:
+            bm.prefix_evict(int(rng.integers(0, 4)))
+        count = [0] * N
+        for t in bm.tables.values():
+            for b in t:
+                count[b] += 1
+        for e in bm.cache.values():
+            count[e[0]] += 1
+        assert count == bm.ref
+        assert sorted(bm.free) == [b for b in range(N) if bm.ref[b] == 0]
+    for s in list(bm.tables):
+        bm.free_seq(s)
+    bm.prefix_evict(N)
+    assert bm.free_blocks() == N and not bm.cache
