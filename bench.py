@@ -16,7 +16,10 @@ Other workloads (--config): long_decode (13 x 8,192), shared_prefix_decode
 schedule, i.e. 8 iterations), gqa_decode (32 rows x 2,300 tokens, 8 K/V heads
 serving 32 query heads: 9.65 GB of K/V per step), average_decode_int8 (the
 headline workload over an 8-bit pool: INT8 codes plus one FP32 scale per
-128-value row, 132 bytes per row instead of 256).
+128-value row, 132 bytes per row instead of 256), swap_blocks (a preempted
+batch's 384 scattered 8 MB blocks swapped out to page-locked host memory and
+back in one launch each; its roofline is a contiguous cudaMemcpyAsync of the
+same bytes measured in the same run).
 
 Rank 0 prints one JSON line. Under torchrun (N > 1) every rank runs its own
 replica (weak scaling, no collective on the data path); `value` adds all
@@ -74,12 +77,15 @@ CONFIG_TEXT = {
                      "of context U{100..2000} advancing one token per iteration, 32 layers",
     "average_decode_int8": "the average_decode workload over an 8-bit pool (INT8 codes, one FP32 scale per "
                            "(token, head) row of K or V; 2,112-byte tiles), 7,152 blocks (30.9 GB)",
+    "swap_blocks": "swap-out then swap-in of 384 scattered blocks (8,388,608 B each, 3.2 GB) of a 1,024-block "
+                   "pool to one page-locked host buffer, one launch each way",
     "gqa_decode": "batch-32 decode at 2,300 context tokens per row, 32 layers, 8 K/V heads serving 32 query heads "
                   "(grouped-query attention, 131,072 B of K/V per token), 28,608-block (60 GB) shuffled pool, "
                   "kv_append of 1 token per row",
 }
 
 CONFIG_DTYPE = {"average_decode_int8": "int8"}
+SWAP_BLOCKS, SWAP_POOL = 384, 1024
 
 KERNEL_SOURCES = {
     "decode_attn": ["pkv_kernels.cu", "ptx.cuh", "pkv_internal.h"],
@@ -541,6 +547,142 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+# ------------------------------------------------------------------ swap
+
+def run_swap(args):
+    """Block swap out + in through pkv_swap_blocks_out / _in; the link's own rate from cudaMemcpyAsync."""
+    import torch
+    import torch.distributed as dist
+    import paged_kv_cache_scatter_gb300 as pkv
+    from paged_kv_cache_scatter_gb300 import build as pkv_build
+
+    ws, rank, local = _dist()
+    torch.cuda.set_device(local)
+    if ws > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    pkv_build.build()
+    pkv.load()
+    dev = torch.device("cuda", local)
+    L, H, N, n = 32, 32, SWAP_POOL, SWAP_BLOCKS
+    pool_t = torch.empty(workloads.pool_shape(N, L, H), dtype=torch.float16, device=dev)
+    workloads.fill_normal_fp16_(pool_t, workloads.value_seed(args.seed, "pool"))
+    pool = pkv.Pool(pool_t, N, num_layers=L, num_heads=H)
+    bb = pkv.Pool.bytes_needed(1, L, H)
+    rng = np.random.default_rng(args.seed)
+    blocks = torch.from_numpy(rng.choice(N, n, replace=False).astype(np.int32)).to(dev)
+    pairs = torch.from_numpy(np.stack([rng.choice(N // 2, n // 4, replace=False),
+                                       N // 2 + rng.choice(N // 2, n // 4, replace=False)], 1).astype(np.int32)).to(dev)
+    host = torch.empty(n * bb, dtype=torch.uint8).pin_memory()
+    stream = torch.cuda.current_stream(dev)
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+
+    def step():
+        pool.swap_blocks_out(blocks, host, stream)
+        pool.swap_blocks_in(blocks, host, stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    st, flags = pool.get_status(stream)
+    if st != pkv.PKV_OK:
+        raise RuntimeError(f"device status {st} flags {flags:#x}")
+    sampler = ClockSampler(_gpu_id(torch, local))
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    sampler.start()
+    time.sleep(0.3)
+    e0, e1, e2, e3 = ev(), ev(), ev(), ev()
+    e0.record(stream)
+    for _ in range(args.steps):
+        pool.swap_blocks_out(blocks, host, stream)
+    e1.record(stream)
+    for _ in range(args.steps):
+        pool.swap_blocks_in(blocks, host, stream)
+    e2.record(stream)
+    torch.cuda.synchronize(dev)
+    t_out, t_in = e0.elapsed_time(e1), e1.elapsed_time(e2)
+    # the link's rate for the same bytes, contiguous, through the copy engines
+    flat = pool_t.view(-1)[: n * bb // 2].view(torch.uint8)
+    c0, c1, c2 = ev(), ev(), ev()
+    c0.record(stream)
+    for _ in range(args.steps):
+        host.copy_(flat, non_blocking=True)
+    c1.record(stream)
+    for _ in range(args.steps):
+        flat.copy_(host, non_blocking=True)
+    c2.record(stream)
+    # copy-on-write block copies inside HBM
+    k0, k1 = ev(), ev()
+    k0.record(stream)
+    for _ in range(args.steps):
+        pool.copy_blocks(pairs, stream)
+    k1.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    st, flags = pool.get_status(stream)
+    if st != pkv.PKV_OK:
+        raise RuntimeError(f"device status {st} flags {flags:#x}")
+    m_out, m_in, t_cow = c0.elapsed_time(c1), c1.elapsed_time(c2), k0.elapsed_time(k1)
+    t_ms = max_over_ranks([t_out + t_in], dist if ws > 1 else None, dev)[0]
+    K = args.steps
+    moved = 2 * n * bb * K
+    value = moved * ws / (t_ms * 1e-3) / 1e9
+    link = moved / ((m_out + m_in) * 1e-3) / 1e9
+    hbm_peak, _, peak_kind = _peaks()
+    cow_gbs = 2 * pairs.shape[0] * bb * K / (t_cow * 1e-3) / 1e9
+    # end to end through the public calls: the block list comes from host memory each step, and the
+    # host copy is read back after the round trip (it is the data)
+    blocks_h = blocks.cpu().pin_memory()
+    x0, x1 = ev(), ev()
+    torch.cuda.synchronize(dev)
+    x0.record(stream)
+    for _ in range(K):
+        blocks.copy_(blocks_h, non_blocking=True)
+        step()
+    x1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e = moved / (x0.elapsed_time(x1) * 1e-3) / 1e9
+    result = {
+        "metric": "block swap GB/s (bytes moved out to page-locked host memory and back in / time)",
+        "value": round(value, 1), "unit": "GB/s", "n_gpus": ws, "steps": K, "warmup": args.warmup,
+        "ms_per_step": round(t_ms / K, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bytes (f16 pool)", "data": "synthetic",
+        "config": {"workload": "swap_blocks", "description": CONFIG_TEXT["swap_blocks"], "blocks": n,
+                   "block_bytes": bb, "pool_blocks": N, "l2": "3.2 GB per direction, above the 129 MB L2"},
+        "out_gbs": round(n * bb * K / (t_out * 1e-3) / 1e9, 1), "in_gbs": round(n * bb * K / (t_in * 1e-3) / 1e9, 1),
+        "clocks": clocks, "gpu_launches": 2 * K,
+        "roofline": {"bound": "c2c", "achieved": round(value, 1), "peak": round(link, 1),
+                     "peak_kind": "measured in this run: cudaMemcpyAsync of the same bytes, contiguous, "
+                                  "device to pinned host and back", "unit": "GB/s", "frac": round(value / link, 4),
+                     "traffic": None},
+        "copy_blocks": {"gbs": round(cow_gbs, 1), "pairs": int(pairs.shape[0]),
+                        "frac_of_hbm": round(cow_gbs / hbm_peak, 4), "peak_kind": peak_kind,
+                        "note": "copy-on-write block copies inside HBM, read + write bytes per second"},
+        "e2e": {"value": round(e2e, 1), "unit": "GB/s", "h2d_bytes_per_step": int(n * 4 + n * bb),
+                "d2h_bytes_per_step": int(n * bb)},
+    }
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        import oracle
+        hb = np.empty(0)
+        g = oracle.geom(64, L, H)
+        mini = np.zeros(oracle.pool_bytes(g) // 2, np.uint16)
+        bl = np.arange(48, dtype=np.int32)
+        t0 = time.perf_counter()
+        reps = 0
+        while time.perf_counter() - t0 < min(args.cpu_seconds, 5.0):
+            hb = oracle.swap_out(mini, g, bl)
+            oracle.swap_in(mini, g, bl, hb)
+            reps += 1
+        dt = time.perf_counter() - t0
+        result["cpu_baseline"] = {"value": round(2 * len(bl) * bb * reps / dt / 1e9, 2), "unit": "GB/s", "cores": 1,
+                                  "kind": "oracle", "sample": f"48 blocks out and in, {reps} round trips, host memory"}
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+
+
 # ------------------------------------------------------------------ oracle timings
 
 def _layer_sample(wl, layer, pool_t=None, seed=0, dtype="fp16"):
@@ -613,6 +755,31 @@ def run_reference(args):
     if rank != 0:
         return
     import oracle
+    if args.config == "swap_blocks":
+        g = oracle.geom(64, 32, 32)
+        mini = np.zeros(oracle.pool_bytes(g) // 2, np.uint16)
+        bl = np.arange(48, dtype=np.int32)
+        bb = oracle.bytes_per_block(g)
+        times = []
+        for i in range(args.warmup + args.steps):
+            t0 = time.perf_counter()
+            hb = oracle.swap_out(mini, g, bl)
+            oracle.swap_in(mini, g, bl, hb)
+            if i >= args.warmup:
+                times.append(time.perf_counter() - t0)
+        value = 2 * len(bl) * bb * len(times) / sum(times) / 1e9
+        print(json.dumps({"impl": "reference", "metric": "block swap GB/s (bytes moved out to page-locked host "
+                          "memory and back in / time)", "value": round(value, 3), "unit": "GB/s", "n_gpus": ws,
+                          "steps": args.steps, "warmup": args.warmup,
+                          "ms_per_step": round(sum(times) / len(times) * 1e3, 2), "higher_is_better": True,
+                          "scaling": "weak", "vs_baseline": None, "dtype": "bytes", "data": "synthetic",
+                          "config": {"workload": "swap_blocks", "description": CONFIG_TEXT["swap_blocks"],
+                                     "step": "48 blocks out and in on the host (bounded sample)"},
+                          "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                                           "sample": "48 blocks out and in per step"},
+                          "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                                  "d2h_bytes_per_step": 0}}), flush=True)
+        return
     wl = _iterations(args.config, args.seed)[0]
     dtype = CONFIG_DTYPE.get(args.config, "fp16")
     threads = len(os.sched_getaffinity(0))
@@ -652,7 +819,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", default="average_decode",
                     choices=["average_decode", "long_decode", "shared_prefix_decode", "mixed_prefill", "gqa_decode",
-                             "average_decode_int8"])
+                             "average_decode_int8", "swap_blocks"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="launch each step directly instead of replaying a CUDA graph")
@@ -667,6 +834,8 @@ def main():
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":
         run_reference(args)
+    elif args.config == "swap_blocks":
+        run_swap(args)
     else:
         run_ours(args)
 

@@ -136,6 +136,68 @@ int64_t pkv_free_blocks(const pkv_pool* pool);                 /* -1 for a NULL 
 int32_t pkv_ref_count(const pkv_pool* pool, int64_t block);     /* -1 if out of range */
 int64_t pkv_seq_len(const pkv_pool* pool, int64_t seq_id);      /* -1 if unknown */
 
+/* ------------------------------------------ copy-on-write, swap, prefix cache */
+
+/* Parallel sampling: a new sequence dst_seq shares every block of src_seq,
+ * the partly filled last block included (ref_count + 1 each), with src's
+ * length ("The inference engine" (wpnews), "Paging turns variable sequences
+ * into block tables": copy-on-write sharing for parallel sampling). */
+pkv_status pkv_seq_fork(pkv_pool* pool, int64_t dst_seq, int64_t src_seq);
+
+/* Copy-on-write: if seq_id's next token would land in its partly filled last
+ * block and that block is shared, give seq_id a private block: a free block
+ * replaces the shared one in its table (old ref_count - 1, new 1) and
+ * *src_block / *dst_block name the copy the caller must make on the device
+ * (pkv_copy_blocks) before writing; otherwise both are -1 and nothing changes.
+ * PKV_E_NOMEM (nothing changes) if no block is free. */
+pkv_status pkv_seq_cow(pkv_pool* pool, int64_t seq_id, int32_t* src_block, int32_t* dst_block);
+
+/* Preemption by swap ("continuous batching server", "Preemption and Eviction:
+ * Recompute vs Swap"; the choice of victim and of swap over recompute is the
+ * caller's). pkv_seq_swap_out writes seq_id's blocks (table order) to
+ * blocks[0..*n_blocks) and releases them (ref_count - 1, free at 0); the
+ * sequence keeps its length but has no blocks until pkv_seq_swap_in, which
+ * takes ceil(len/16) fresh blocks off the free list (PKV_E_NOMEM: nothing
+ * changes) and writes them to blocks. The caller moves the contents with
+ * pkv_swap_blocks_out before anything else writes the released blocks (same
+ * stream) and with pkv_swap_blocks_in before the sequence's next step. If
+ * capacity < *n_blocks the call fails with PKV_E_INVALID, nothing changes,
+ * and *n_blocks says how many are needed. A swapped-out sequence can only be
+ * swapped in or freed. */
+pkv_status pkv_seq_swap_out(pkv_pool* pool, int64_t seq_id, int32_t* blocks, int64_t capacity, int64_t* n_blocks);
+pkv_status pkv_seq_swap_in(pkv_pool* pool, int64_t seq_id, int32_t* blocks, int64_t capacity, int64_t* n_blocks);
+
+/* Chained prefix hashes of a token-id stream ("Serving LLMs" (sreshtalluri),
+ * "Prefix caching": a block's hash covers the block and, through the chain,
+ * every token before it). out[i] = FNV-1a-64 over the 8 little-endian bytes
+ * of out[i-1] (0 for i = 0) followed by the 16 token ids of block i (4
+ * little-endian bytes each). Only full blocks are hashed: returns
+ * n_tokens / 16 (written to out, capacity >= that), -1 on a bad argument. */
+int64_t pkv_block_hashes(const int32_t* tokens, int64_t n_tokens, uint64_t* out, int64_t capacity);
+
+/* The pool's prefix cache: chained hash -> block. The cache holds one
+ * reference to each cached block, so it outlives the sequences using it.
+ *   pkv_prefix_register: cache seq_id's first n_hashes full blocks under
+ *     hashes[0..n_hashes) (the hashes of its tokens); a hash already cached
+ *     keeps its block, a block already cached under another hash is left out;
+ *     *n_new = blocks added.
+ *   pkv_prefix_match: the number of leading hashes that are cached (the walk
+ *     stops at the first miss); -1 on a bad argument.
+ *   pkv_seq_attach_prefix: create seq_id on the blocks of its longest cached
+ *     prefix (ref_count + 1 each, length 16 * *n_attached); the caller then
+ *     grows it and prefills only the rest of the prompt.
+ *   pkv_prefix_evict: drop up to max_blocks entries whose block only the
+ *     cache references, least recently used (registered or attached) first
+ *     and, among equals, deeper chain positions first; those blocks return to
+ *     the free list. Returns the number evicted, -1 on a bad argument. */
+pkv_status pkv_prefix_register(pkv_pool* pool, int64_t seq_id, const uint64_t* hashes, int64_t n_hashes,
+                               int64_t* n_new);
+int64_t pkv_prefix_match(const pkv_pool* pool, const uint64_t* hashes, int64_t n_hashes);
+pkv_status pkv_seq_attach_prefix(pkv_pool* pool, int64_t seq_id, const uint64_t* hashes, int64_t n_hashes,
+                                 int64_t* n_attached);
+int64_t pkv_prefix_evict(pkv_pool* pool, int64_t max_blocks);
+int64_t pkv_prefix_cached_blocks(const pkv_pool* pool);        /* entries in the cache, -1 for a NULL pool */
+
 /* Copy seq_id's block table (host int32) into out[0..capacity); *n_out = its length. */
 pkv_status pkv_block_table(const pkv_pool* pool, int64_t seq_id, int32_t* out, int64_t capacity,
                            int64_t* n_out);
@@ -229,6 +291,23 @@ pkv_status pkv_prefill_attn(pkv_pool* pool, int32_t layer, const void* q, const 
 pkv_status pkv_decode_attn_noalloc(pkv_pool* pool, int32_t layer, const void* q, const int32_t* block_tables,
                                    int32_t max_blocks, const int32_t* ctx_lens, int32_t num_seqs, float scale,
                                    void* out, void* stream);
+
+/* Whole-block copies on the device, asynchronous on `stream`.
+ * pkv_copy_blocks: for i < n, block pairs[2i+1] receives a copy of block
+ *   pairs[2i] (every layer, K and V: pkv_pool_bytes / num_blocks bytes);
+ *   pairs is device int32 [n][2]. No block may be the destination of one pair
+ *   and the source or destination of another (the pairs run concurrently).
+ * pkv_swap_blocks_out: host_dst[i * block bytes ..] receives block blocks[i];
+ * pkv_swap_blocks_in: block blocks[i] receives host_src[i * block bytes ..].
+ *   blocks is device int32 [n]; the host buffer (n * block bytes, 16-byte
+ *   aligned) must be page-locked host memory the device can address
+ *   (cudaHostAlloc / cudaHostRegister; checked, PKV_E_INVALID otherwise). The
+ *   kernel reads or writes it in place, so one launch gathers scattered pool
+ *   blocks into one host buffer or scatters them back.
+ * Block ids outside the pool are skipped and flagged (PKV_DEV_BAD_BLOCK). */
+pkv_status pkv_copy_blocks(pkv_pool* pool, const int32_t* pairs, int32_t n, void* stream);
+pkv_status pkv_swap_blocks_out(pkv_pool* pool, const int32_t* blocks, int32_t n, void* host_dst, void* stream);
+pkv_status pkv_swap_blocks_in(pkv_pool* pool, const int32_t* blocks, int32_t n, const void* host_src, void* stream);
 
 /* ------------------------------------------------------------------- step */
 

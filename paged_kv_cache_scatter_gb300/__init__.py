@@ -56,6 +56,19 @@ SIGNATURES = {
     "pkv_ref_count": (_i32, [_P, _i64]),
     "pkv_seq_len": (_i64, [_P, _i64]),
     "pkv_block_table": (_i32, [_P, _i64, _P, _i64, _c.POINTER(_i64)]),
+    "pkv_seq_fork": (_i32, [_P, _i64, _i64]),
+    "pkv_seq_cow": (_i32, [_P, _i64, _c.POINTER(_i32), _c.POINTER(_i32)]),
+    "pkv_seq_swap_out": (_i32, [_P, _i64, _P, _i64, _c.POINTER(_i64)]),
+    "pkv_seq_swap_in": (_i32, [_P, _i64, _P, _i64, _c.POINTER(_i64)]),
+    "pkv_block_hashes": (_i64, [_P, _i64, _P, _i64]),
+    "pkv_prefix_register": (_i32, [_P, _i64, _P, _i64, _c.POINTER(_i64)]),
+    "pkv_prefix_match": (_i64, [_P, _P, _i64]),
+    "pkv_seq_attach_prefix": (_i32, [_P, _i64, _P, _i64, _c.POINTER(_i64)]),
+    "pkv_prefix_evict": (_i64, [_P, _i64]),
+    "pkv_prefix_cached_blocks": (_i64, [_P]),
+    "pkv_copy_blocks": (_i32, [_P, _P, _i32, _P]),
+    "pkv_swap_blocks_out": (_i32, [_P, _P, _i32, _P, _P]),
+    "pkv_swap_blocks_in": (_i32, [_P, _P, _i32, _P, _P]),
     "pkv_build_step": (_i32, [_P, _P, _P, _i32, _i32, _P, _P, _P, _P]),
     "pkv_kv_append": (_i32, [_P, _i32, _P, _P, _P, _i32, _P]),
     "pkv_decode_workspace_bytes": (_sz, [_P, _i32, _i32]),
@@ -203,7 +216,73 @@ class Pool:
                                    ctx.ctypes.data, slots.ctypes.data, qs.ctypes.data)
         return st, tables, ctx, slots[:int(ql.sum())], qs
 
+    # ---- copy-on-write, swap, prefix cache (host bookkeeping)
+    def seq_fork(self, dst: int, src: int) -> int:
+        return load().pkv_seq_fork(self.handle, dst, src)
+
+    def seq_cow(self, seq_id: int):
+        """(status, src_block, dst_block); (OK, -1, -1) when no copy is needed."""
+        a, b = _i32(), _i32()
+        st = load().pkv_seq_cow(self.handle, seq_id, _c.byref(a), _c.byref(b))
+        return st, a.value, b.value
+
+    def _swap(self, fn, seq_id: int):
+        import numpy as np
+        n = _i64()
+        length = max(self.seq_len(seq_id), 0)
+        out = np.empty(max((length + 15) // 16, 1), np.int32)   # a table never holds more blocks than this
+        st = fn(self.handle, seq_id, out.ctypes.data, out.shape[0], _c.byref(n))
+        return st, out[:n.value] if st == PKV_OK else None
+
+    def seq_swap_out(self, seq_id: int):
+        """(status, blocks to copy to host, in table order); the blocks are released."""
+        return self._swap(load().pkv_seq_swap_out, seq_id)
+
+    def seq_swap_in(self, seq_id: int):
+        """(status, fresh blocks for the host copy to return to)."""
+        return self._swap(load().pkv_seq_swap_in, seq_id)
+
+    def prefix_register(self, seq_id: int, hashes):
+        import numpy as np
+        h = np.ascontiguousarray(hashes, np.uint64)
+        n = _i64()
+        st = load().pkv_prefix_register(self.handle, seq_id, h.ctypes.data if h.size else None, h.shape[0],
+                                        _c.byref(n))
+        return st, n.value
+
+    def prefix_match(self, hashes) -> int:
+        import numpy as np
+        h = np.ascontiguousarray(hashes, np.uint64)
+        return load().pkv_prefix_match(self.handle, h.ctypes.data if h.size else None, h.shape[0])
+
+    def seq_attach_prefix(self, seq_id: int, hashes):
+        import numpy as np
+        h = np.ascontiguousarray(hashes, np.uint64)
+        n = _i64()
+        st = load().pkv_seq_attach_prefix(self.handle, seq_id, h.ctypes.data if h.size else None, h.shape[0],
+                                          _c.byref(n))
+        return st, n.value
+
+    def prefix_evict(self, max_blocks: int) -> int:
+        return load().pkv_prefix_evict(self.handle, max_blocks)
+
+    def prefix_cached_blocks(self) -> int:
+        return load().pkv_prefix_cached_blocks(self.handle)
+
     # ---- kernels (device tensors)
+    def copy_blocks(self, pairs, stream=None) -> None:
+        """pairs: device int32 [n, 2] of (src, dst) blocks."""
+        _check(load().pkv_copy_blocks(self.handle, _ptr(pairs), int(pairs.shape[0]), _stream(stream)))
+
+    def swap_blocks_out(self, blocks, host, stream=None) -> None:
+        """blocks: device int32 [n]; host: pinned tensor of n * block bytes."""
+        _check(load().pkv_swap_blocks_out(self.handle, _ptr(blocks), int(blocks.shape[0]), _ptr(host),
+                                          _stream(stream)))
+
+    def swap_blocks_in(self, blocks, host, stream=None) -> None:
+        _check(load().pkv_swap_blocks_in(self.handle, _ptr(blocks), int(blocks.shape[0]), _ptr(host),
+                                         _stream(stream)))
+
     def kv_append(self, layer: int, k, v, slot_mapping, stream=None) -> None:
         _check(load().pkv_kv_append(self.handle, layer, _ptr(k), _ptr(v), _ptr(slot_mapping),
                                     int(slot_mapping.shape[0]), _stream(stream)))
@@ -245,6 +324,17 @@ class Pool:
 
     def debug_wait_probe(self, timeout_ns: int, stream=None) -> None:
         _check(load().pkv_debug_wait_probe(self.handle, int(timeout_ns), _stream(stream)))
+
+
+def block_hashes(tokens):
+    """Chained prefix hashes (uint64) of the full blocks of a host int32 token-id array."""
+    import numpy as np
+    t = np.ascontiguousarray(tokens, np.int32)
+    out = np.empty(max(1, t.shape[0] // 16), np.uint64)
+    n = load().pkv_block_hashes(t.ctypes.data if t.size else None, t.shape[0], out.ctypes.data, out.shape[0])
+    if n < 0:
+        raise PkvError(PKV_E_INVALID, "bad token array")
+    return out[:n]
 
 
 def make_step_desc(*, num_decode, num_prefill, num_tokens, max_q_len, max_blocks, first_layer, num_layers, scale,

@@ -24,7 +24,8 @@ CUDA_HOME = os.environ.get("CUDA_HOME", "/usr/local/cuda")
 NVCC = os.path.join(CUDA_HOME, "bin", "nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
-CU_SOURCES = ["pkv_kernels.cu", "pkv_decode_group.cu", "pkv_int8.cu", "pkv_prefill.cu", "pkv_noalloc.cu"]
+CU_SOURCES = ["pkv_kernels.cu", "pkv_decode_group.cu", "pkv_int8.cu", "pkv_prefill.cu", "pkv_noalloc.cu",
+              "pkv_blocks.cu"]
 CPP_SOURCES = ["pkv_host.cpp"]
 
 

@@ -174,6 +174,7 @@ pkv_status pkv_pool_create(const pkv_pool_desc* d, pkv_pool** out)
 
     const int64_t n = d->num_blocks;
     p->ref.assign(n, 0);
+    p->cached.assign(n, 0);
     p->free_stack.resize(n);
     if (d->free_order) {
         std::vector<char> seen(n, 0);
@@ -206,6 +207,8 @@ pkv_status pkv_seq_grow(pkv_pool* pool, int64_t seq_id, int64_t new_len)
 {
     if (pkv_status s = check_pool(pool)) return s;
     auto it = pool->seqs.find(seq_id);
+    if (it != pool->seqs.end() && it->second.swapped)
+        return fail(PKV_E_INVALID, "seq %lld is swapped out", (long long)seq_id);
     const int64_t cur_len = it == pool->seqs.end() ? 0 : it->second.len;
     const int64_t cur_blocks = it == pool->seqs.end() ? 0 : (int64_t)it->second.table.size();
     if (new_len < cur_len) return fail(PKV_E_INVALID, "seq %lld: new_len %lld below current length %lld",
@@ -230,6 +233,7 @@ pkv_status pkv_seq_share_prefix(pkv_pool* pool, int64_t dst, int64_t src, int64_
     if (pkv_status s = check_pool(pool)) return s;
     auto it = pool->seqs.find(src);
     if (it == pool->seqs.end()) return fail(PKV_E_INVALID, "unknown source sequence %lld", (long long)src);
+    if (it->second.swapped) return fail(PKV_E_INVALID, "source %lld is swapped out", (long long)src);
     if (dst == src || pool->seqs.count(dst)) return fail(PKV_E_INVALID, "destination %lld already exists", (long long)dst);
     if (n_blocks < 0 || n_blocks * pkv::kBlockSize > it->second.len)
         return fail(PKV_E_INVALID, "only full blocks of the source can be shared");
@@ -253,6 +257,211 @@ pkv_status pkv_seq_free(pkv_pool* pool, int64_t seq_id)
 }
 
 int64_t pkv_free_blocks(const pkv_pool* pool) { return pool ? (int64_t)pool->free_stack.size() : -1; }
+
+// ------------------------------------------------------------ copy-on-write
+
+pkv_status pkv_seq_fork(pkv_pool* pool, int64_t dst, int64_t src)
+{
+    if (pkv_status s = check_pool(pool)) return s;
+    auto it = pool->seqs.find(src);
+    if (it == pool->seqs.end() || it->second.swapped)
+        return fail(PKV_E_INVALID, "source %lld unknown or swapped out", (long long)src);
+    if (dst == src || pool->seqs.count(dst)) return fail(PKV_E_INVALID, "destination %lld already exists", (long long)dst);
+    const pkv::Seq copy = it->second;
+    for (int32_t b : copy.table) pool->ref[b] += 1;
+    pool->seqs[dst] = copy;
+    return PKV_OK;
+}
+
+pkv_status pkv_seq_cow(pkv_pool* pool, int64_t seq_id, int32_t* src_block, int32_t* dst_block)
+{
+    if (pkv_status s = check_pool(pool)) return s;
+    if (!src_block || !dst_block) return fail(PKV_E_INVALID, "NULL output");
+    *src_block = *dst_block = -1;
+    auto it = pool->seqs.find(seq_id);
+    if (it == pool->seqs.end() || it->second.swapped)
+        return fail(PKV_E_INVALID, "seq %lld unknown or swapped out", (long long)seq_id);
+    pkv::Seq& s = it->second;
+    if (s.table.empty() || s.len % pkv::kBlockSize == 0 || pool->ref[s.table.back()] == 1) return PKV_OK;
+    if (pool->free_stack.empty()) return fail(PKV_E_NOMEM, "no free block for the copy");
+    const int32_t b = pool->free_stack.back();
+    pool->free_stack.pop_back();
+    pool->ref[b] = 1;
+    const int32_t old = s.table.back();
+    pool->ref[old] -= 1;  // above 1 before, so it stays referenced
+    s.table.back() = b;
+    *src_block = old;
+    *dst_block = b;
+    return PKV_OK;
+}
+
+// ------------------------------------------------------------------- swap
+
+pkv_status pkv_seq_swap_out(pkv_pool* pool, int64_t seq_id, int32_t* blocks, int64_t capacity, int64_t* n_blocks)
+{
+    if (pkv_status s = check_pool(pool)) return s;
+    auto it = pool->seqs.find(seq_id);
+    if (it == pool->seqs.end() || it->second.swapped)
+        return fail(PKV_E_INVALID, "seq %lld unknown or already swapped out", (long long)seq_id);
+    pkv::Seq& s = it->second;
+    const int64_t n = (int64_t)s.table.size();
+    if (n_blocks) *n_blocks = n;
+    if (capacity < n || (n > 0 && !blocks)) return fail(PKV_E_INVALID, "capacity %lld < %lld blocks", (long long)capacity,
+                                                        (long long)n);
+    std::copy(s.table.begin(), s.table.end(), blocks);
+    for (int32_t b : s.table)
+        if (--pool->ref[b] == 0) pool->free_stack.push_back(b);
+    s.table.clear();
+    s.swapped = true;
+    return PKV_OK;
+}
+
+pkv_status pkv_seq_swap_in(pkv_pool* pool, int64_t seq_id, int32_t* blocks, int64_t capacity, int64_t* n_blocks)
+{
+    if (pkv_status s = check_pool(pool)) return s;
+    auto it = pool->seqs.find(seq_id);
+    if (it == pool->seqs.end() || !it->second.swapped)
+        return fail(PKV_E_INVALID, "seq %lld is not swapped out", (long long)seq_id);
+    pkv::Seq& s = it->second;
+    const int64_t n = (s.len + pkv::kBlockSize - 1) / pkv::kBlockSize;
+    if (n_blocks) *n_blocks = n;
+    if (capacity < n || (n > 0 && !blocks)) return fail(PKV_E_INVALID, "capacity %lld < %lld blocks", (long long)capacity,
+                                                        (long long)n);
+    if (n > (int64_t)pool->free_stack.size())
+        return fail(PKV_E_NOMEM, "seq %lld needs %lld blocks, %zu free", (long long)seq_id, (long long)n,
+                    pool->free_stack.size());
+    for (int64_t i = 0; i < n; ++i) {
+        const int32_t b = pool->free_stack.back();
+        pool->free_stack.pop_back();
+        pool->ref[b] = 1;
+        s.table.push_back(b);
+        blocks[i] = b;
+    }
+    s.swapped = false;
+    return PKV_OK;
+}
+
+// ------------------------------------------------------------- prefix cache
+
+// 64-bit FNV-1a, continuing from state h.
+static uint64_t fnv1a64(uint64_t h, const unsigned char* p, size_t n)
+{
+    for (size_t i = 0; i < n; ++i) {
+        h ^= p[i];
+        h *= 0x100000001b3ULL;
+    }
+    return h;
+}
+
+int64_t pkv_block_hashes(const int32_t* tokens, int64_t n_tokens, uint64_t* out, int64_t capacity)
+{
+    if (n_tokens < 0 || (n_tokens > 0 && !tokens)) return -1;
+    const int64_t nb = n_tokens / pkv::kBlockSize;
+    if (capacity < nb || (nb > 0 && !out)) return -1;
+    uint64_t h = 0;
+    unsigned char buf[8 + 4 * pkv::kBlockSize];
+    for (int64_t i = 0; i < nb; ++i) {
+        for (int k = 0; k < 8; ++k) buf[k] = (unsigned char)(h >> (8 * k));
+        for (int t = 0; t < pkv::kBlockSize; ++t) {
+            const uint32_t v = (uint32_t)tokens[i * pkv::kBlockSize + t];
+            for (int k = 0; k < 4; ++k) buf[8 + 4 * t + k] = (unsigned char)(v >> (8 * k));
+        }
+        h = fnv1a64(0xcbf29ce484222325ULL, buf, sizeof(buf));
+        out[i] = h;
+    }
+    return nb;
+}
+
+pkv_status pkv_prefix_register(pkv_pool* pool, int64_t seq_id, const uint64_t* hashes, int64_t n_hashes,
+                               int64_t* n_new)
+{
+    if (pkv_status s = check_pool(pool)) return s;
+    if (n_new) *n_new = 0;
+    auto it = pool->seqs.find(seq_id);
+    if (it == pool->seqs.end() || it->second.swapped)
+        return fail(PKV_E_INVALID, "seq %lld unknown or swapped out", (long long)seq_id);
+    if (n_hashes < 0 || (n_hashes > 0 && !hashes) || n_hashes * pkv::kBlockSize > it->second.len)
+        return fail(PKV_E_INVALID, "only the sequence's full blocks can be cached");
+    const uint64_t now = ++pool->clock;
+    int64_t added = 0;
+    for (int64_t i = 0; i < n_hashes; ++i) {
+        auto e = pool->cache.find(hashes[i]);
+        if (e != pool->cache.end()) {
+            e->second.last_use = now;
+            continue;
+        }
+        const int32_t b = it->second.table[i];
+        if (pool->cached[b]) continue;  // already cached under another chain
+        pool->cache.emplace(hashes[i], pkv::CacheEntry{b, now, i});
+        pool->cached[b] = 1;
+        pool->ref[b] += 1;
+        ++added;
+    }
+    if (n_new) *n_new = added;
+    return PKV_OK;
+}
+
+int64_t pkv_prefix_match(const pkv_pool* pool, const uint64_t* hashes, int64_t n_hashes)
+{
+    if (!pool || n_hashes < 0 || (n_hashes > 0 && !hashes)) return -1;
+    int64_t n = 0;
+    while (n < n_hashes && pool->cache.count(hashes[n])) ++n;
+    return n;
+}
+
+pkv_status pkv_seq_attach_prefix(pkv_pool* pool, int64_t seq_id, const uint64_t* hashes, int64_t n_hashes,
+                                 int64_t* n_attached)
+{
+    if (pkv_status s = check_pool(pool)) return s;
+    if (n_attached) *n_attached = 0;
+    if (pool->seqs.count(seq_id)) return fail(PKV_E_INVALID, "seq %lld already exists", (long long)seq_id);
+    const int64_t n = pkv_prefix_match(pool, hashes, n_hashes);
+    if (n < 0) return fail(PKV_E_INVALID, "bad hash list");
+    const uint64_t now = ++pool->clock;
+    pkv::Seq& s = pool->seqs[seq_id];
+    for (int64_t i = 0; i < n; ++i) {
+        pkv::CacheEntry& e = pool->cache.find(hashes[i])->second;
+        e.last_use = now;
+        pool->ref[e.block] += 1;
+        s.table.push_back(e.block);
+    }
+    s.len = n * pkv::kBlockSize;
+    if (n_attached) *n_attached = n;
+    return PKV_OK;
+}
+
+int64_t pkv_prefix_evict(pkv_pool* pool, int64_t max_blocks)
+{
+    if (!pool || max_blocks < 0) return -1;
+    struct Cand {
+        uint64_t last_use;
+        int64_t depth;
+        int32_t block;
+        uint64_t hash;
+    };
+    std::vector<Cand> cand;
+    for (const auto& kv : pool->cache)
+        if (pool->ref[kv.second.block] == 1) cand.push_back({kv.second.last_use, kv.second.depth, kv.second.block, kv.first});
+    // least recently used first; deeper chain positions first among equals
+    std::sort(cand.begin(), cand.end(), [](const Cand& a, const Cand& b) {
+        if (a.last_use != b.last_use) return a.last_use < b.last_use;
+        if (a.depth != b.depth) return a.depth > b.depth;
+        if (a.block != b.block) return a.block < b.block;
+        return a.hash < b.hash;
+    });
+    int64_t n = 0;
+    for (const Cand& c : cand) {
+        if (n >= max_blocks) break;
+        pool->cache.erase(c.hash);
+        pool->cached[c.block] = 0;
+        pool->ref[c.block] = 0;
+        pool->free_stack.push_back(c.block);
+        ++n;
+    }
+    return n;
+}
+
+int64_t pkv_prefix_cached_blocks(const pkv_pool* pool) { return pool ? (int64_t)pool->cache.size() : -1; }
 
 int32_t pkv_ref_count(const pkv_pool* pool, int64_t block)
 {
@@ -298,6 +507,7 @@ pkv_status pkv_build_step(const pkv_pool* pool, const int64_t* seq_ids, const in
         auto it = pool->seqs.find(seq_ids[i]);
         if (it == pool->seqs.end()) return fail(PKV_E_INVALID, "row %d: unknown sequence %lld", i, (long long)seq_ids[i]);
         const pkv::Seq& s = it->second;
+        if (s.swapped) return fail(PKV_E_INVALID, "row %d: sequence %lld is swapped out", i, (long long)seq_ids[i]);
         if (q_lens[i] < 1 || q_lens[i] > s.len) return fail(PKV_E_INVALID, "row %d: q_len %d outside [1, %lld]", i,
                                                             q_lens[i], (long long)s.len);
         if ((int64_t)s.table.size() > max_blocks)
@@ -352,6 +562,47 @@ pkv_status pkv_kv_append(pkv_pool* pool, int32_t layer, const void* k, const voi
     if (!dg.ok) return fail(PKV_E_DEVICE, "cannot select the pool's device");
     cudaError_t e = launch_append_any(pool, layer, k, v, slot_mapping, num_tokens, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PKV_OK : pkv::cuda_fail(e, "kv_append launch");
+}
+
+pkv_status pkv_copy_blocks(pkv_pool* pool, const int32_t* pairs, int32_t n, void* stream)
+{
+    if (pkv_status s = check_device_pool(pool)) return s;
+    if (n < 0) return fail(PKV_E_INVALID, "n < 0");
+    if (n == 0) return PKV_OK;
+    if (!pairs || !aligned(pairs, 4)) return fail(PKV_E_INVALID, "pairs NULL or unaligned");
+    DeviceGuard dg(pool->device);
+    if (!dg.ok) return fail(PKV_E_DEVICE, "cannot select the pool's device");
+    cudaError_t e = pkv::launch_copy_blocks(pool->geom, pairs, n, pool->status_dev, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PKV_OK : pkv::cuda_fail(e, "copy_blocks launch");
+}
+
+static pkv_status swap_blocks(pkv_pool* pool, const int32_t* blocks, int32_t n, void* host, bool to_host, void* stream)
+{
+    if (pkv_status s = check_device_pool(pool)) return s;
+    if (n < 0) return fail(PKV_E_INVALID, "n < 0");
+    if (n == 0) return PKV_OK;
+    if (!blocks || !host || !aligned(blocks, 4) || !aligned(host, 16))
+        return fail(PKV_E_INVALID, "blocks or host buffer NULL or unaligned (host: 16 bytes)");
+    cudaPointerAttributes attr;
+    if (cudaPointerGetAttributes(&attr, host) != cudaSuccess || attr.type != cudaMemoryTypeHost || !attr.devicePointer) {
+        cudaGetLastError();
+        return fail(PKV_E_INVALID, "host buffer is not page-locked host memory the device can address");
+    }
+    DeviceGuard dg(pool->device);
+    if (!dg.ok) return fail(PKV_E_DEVICE, "cannot select the pool's device");
+    cudaError_t e = pkv::launch_swap_blocks(pool->geom, blocks, n, attr.devicePointer, to_host, pool->status_dev,
+                                            static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PKV_OK : pkv::cuda_fail(e, "swap launch");
+}
+
+pkv_status pkv_swap_blocks_out(pkv_pool* pool, const int32_t* blocks, int32_t n, void* host_dst, void* stream)
+{
+    return swap_blocks(pool, blocks, n, host_dst, true, stream);
+}
+
+pkv_status pkv_swap_blocks_in(pkv_pool* pool, const int32_t* blocks, int32_t n, const void* host_src, void* stream)
+{
+    return swap_blocks(pool, blocks, n, const_cast<void*>(host_src), false, stream);
 }
 
 size_t pkv_decode_workspace_bytes(const pkv_pool* pool, int32_t num_seqs, int32_t max_blocks)

@@ -27,6 +27,14 @@ constexpr int kMaxPartitionsPerRow = 4096;  // the decode kernel merges at most 
 struct Seq {
     std::vector<int32_t> table;
     int64_t len = 0;
+    bool swapped = false;  // blocks given back; the contents live in a caller's host buffer
+};
+
+// One prefix-cache entry: the block holding a full block of tokens whose chained hash is the key.
+struct CacheEntry {
+    int32_t block;
+    uint64_t last_use;
+    int64_t depth;  // position of the block in its chain
 };
 
 // Geometry of the device pool in bytes, for the kernels.
@@ -71,6 +79,9 @@ struct pkv_pool {
     std::vector<int32_t> ref;
     std::vector<int32_t> free_stack;  // back() is handed out next
     std::unordered_map<int64_t, pkv::Seq> seqs;
+    std::unordered_map<uint64_t, pkv::CacheEntry> cache;  // prefix cache: chained hash -> block
+    std::vector<char> cached;                              // [num_blocks] block is in the cache
+    uint64_t clock = 0;
 };
 
 namespace pkv {
@@ -111,6 +122,12 @@ cudaError_t launch_decode_group(const PoolGeom& g, const TensorMap128& kv_tmap, 
                                 const int32_t* tables, int max_blocks, const int32_t* ctx_lens, int num_seqs,
                                 float scale, void* out, const DecodeWs& ws, int partition_tokens, const void* k_new,
                                 const void* v_new, const int64_t* slots, unsigned int* status, cudaStream_t stream);
+// pkv_blocks.cu: whole-block copies inside the pool (copy-on-write) and to / from host memory (swap).
+cudaError_t launch_copy_blocks(const PoolGeom& g, const int32_t* pairs, int n, unsigned int* status,
+                               cudaStream_t stream);
+cudaError_t launch_swap_blocks(const PoolGeom& g, const int32_t* blocks, int n, void* host, bool to_host,
+                               unsigned int* status, cudaStream_t stream);
+
 cudaError_t launch_wait_probe(uint64_t timeout_ns, unsigned int* status, cudaStream_t stream);
 
 // pkv_prefill.cu

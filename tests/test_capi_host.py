@@ -83,6 +83,83 @@ def test_int8_pool_bytes_and_refusals(pkv):
     assert p.decode_workspace_bytes(32, 300) == pkv.Pool(None, 64, num_heads=32).decode_workspace_bytes(32, 300)
 
 
+def test_block_hashes_match_the_oracle(pkv):
+    rng = np.random.default_rng(7)
+    for n in [0, 15, 16, 17, 160, 1203]:
+        t = rng.integers(-2**31, 2**31 - 1, n, dtype=np.int64).astype(np.int32)
+        assert np.array_equal(pkv.block_hashes(t), oracle.block_hashes(t))
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_fork_cow_swap_and_prefix_cache_match_the_oracle(pkv, seed):
+    # the library's block manager against the oracle's restatement, operation by operation
+    rng = np.random.default_rng(100 + seed)
+    N = 40
+    order = rng.permutation(N)
+    p = pkv.Pool(None, N, num_layers=1, free_order=order)
+    bm = blockmgr.BlockManager(N, free_order=order)
+    seqs = list(range(8))
+    toks = {s: rng.integers(0, 7, 1000).astype(np.int32) for s in seqs}
+    for _ in range(600):
+        op = int(rng.integers(0, 10))
+        s = int(rng.choice(seqs))
+        if op <= 1:
+            n = bm.lens.get(s, 0) + int(rng.integers(0, 40))
+            assert p.seq_grow(s, n) == bm.grow(s, n)
+        elif op == 2:
+            assert p.seq_free(s) == bm.free_seq(s)
+        elif op == 3:
+            d = int(rng.choice(seqs))
+            assert p.seq_fork(d, s) == bm.fork(d, s)
+            if d in bm.tables:
+                toks[d] = toks[s].copy()
+        elif op == 4:
+            assert p.seq_cow(s) == bm.cow_last(s)
+        elif op == 5:
+            st, blocks = p.seq_swap_out(s)
+            st2, blocks2 = bm.swap_out(s)
+            assert st == st2 and (st != 0 or list(blocks) == blocks2)
+        elif op == 6:
+            st, blocks = p.seq_swap_in(s)
+            st2, blocks2 = bm.swap_in(s)
+            assert st == st2 and (st != 0 or list(blocks) == blocks2)
+        elif op == 7 and s in bm.tables and s not in bm.swapped:
+            h = oracle.block_hashes(toks[s][:bm.lens[s] // 16 * 16])
+            assert p.prefix_register(s, h) == bm.prefix_register(s, h)
+        elif op == 8:
+            h = oracle.block_hashes(toks[s][:int(rng.integers(0, 300))])
+            assert p.prefix_match(h) == bm.prefix_match(h)
+            if s not in bm.tables:
+                assert p.seq_attach_prefix(s, h) == bm.attach_prefix(s, h)
+        else:
+            k = int(rng.integers(0, 3))
+            assert p.prefix_evict(k) == bm.prefix_evict(k)
+        _compare(p, bm, seqs)
+        assert p.prefix_cached_blocks() == len(bm.cache)
+    # swapped sequences refuse growth and steps; freeing everything returns every block
+    for s in seqs:
+        assert p.seq_free(s) == bm.free_seq(s)
+    assert p.prefix_evict(N) == bm.prefix_evict(N)
+    assert p.free_blocks() == N == bm.free_blocks()
+
+
+def test_swap_out_capacity_and_state_rules(pkv):
+    p = pkv.Pool(None, 8, num_layers=1)
+    assert p.seq_grow(0, 40) == pkv.PKV_OK
+    lib = pkv.load()
+    n = ctypes.c_int64()
+    small = np.zeros(2, np.int32)
+    assert lib.pkv_seq_swap_out(p.handle, 0, small.ctypes.data, 2, ctypes.byref(n)) == pkv.PKV_E_INVALID
+    assert n.value == 3 and p.free_blocks() == 5          # refused: nothing changed
+    st, blocks = p.seq_swap_out(0)
+    assert st == pkv.PKV_OK and len(blocks) == 3 and p.free_blocks() == 8 and p.seq_len(0) == 40
+    assert p.seq_grow(0, 41) == pkv.PKV_E_INVALID
+    assert p.build_step([0], [1], 4)[0] == pkv.PKV_E_INVALID
+    assert p.seq_swap_out(0)[0] == pkv.PKV_E_INVALID
+    st, blocks = p.seq_swap_in(0)
+    assert st == pkv.PKV_OK and len(blocks) == 3 and p.free_blocks() == 5
+
+
 def test_free_order_must_be_a_permutation(pkv):
     with pytest.raises(pkv.PkvError):
         pkv.Pool(None, 4, num_layers=1, free_order=[0, 1, 1, 2])
