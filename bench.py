@@ -14,7 +14,9 @@ Other workloads (--config): long_decode (13 x 8,192), shared_prefix_decode
 (64 rows over 125 shared blocks), mixed_prefill (a 4,000-token prompt in
 512-token chunks next to 31 decode rows; one step = the whole 8-chunk
 schedule, i.e. 8 iterations), gqa_decode (32 rows x 2,300 tokens, 8 K/V heads
-serving 32 query heads: 9.65 GB of K/V per step), average_decode_int8 (the
+serving 32 query heads: 9.65 GB of K/V per step), shared_prefix_cascade (the
+shared-prefix workload through cascade decode: the 125 shared blocks are read
+once per layer for all 64 rows; roofline on unique bytes), average_decode_int8 (the
 headline workload over an 8-bit pool: INT8 codes plus one FP32 scale per
 128-value row, 132 bytes per row instead of 256), swap_blocks (a preempted
 batch's 384 scattered 8 MB blocks swapped out to page-locked host memory and
@@ -57,7 +59,7 @@ def _iterations(config: str, seed: int = 0):
         return [workloads.average_decode(seed)]
     if config == "long_decode":
         return [workloads.long_decode(seed)]
-    if config == "shared_prefix_decode":
+    if config in ("shared_prefix_decode", "shared_prefix_cascade"):
         return [workloads.shared_prefix_decode(seed)]
     if config == "gqa_decode":
         return [workloads.gqa_decode(seed)]
@@ -77,6 +79,9 @@ CONFIG_TEXT = {
                      "of context U{100..2000} advancing one token per iteration, 32 layers",
     "average_decode_int8": "the average_decode workload over an 8-bit pool (INT8 codes, one FP32 scale per "
                            "(token, head) row of K or V; 2,112-byte tiles), 7,152 blocks (30.9 GB)",
+    "shared_prefix_cascade": "64 rows sharing 125 ref-counted prefix blocks + 1..300 private tokens, 32 layers; "
+                             "per layer kv_append of the new tokens then cascade decode (shared partitions once "
+                             "per group on the tensor cores, the rest per row)",
     "swap_blocks": "swap-out then swap-in of 384 scattered blocks (8,388,608 B each, 3.2 GB) of a 1,024-block "
                    "pool to one page-locked host buffer, one launch each way",
     "gqa_decode": "batch-32 decode at 2,300 context tokens per row, 32 layers, 8 K/V heads serving 32 query heads "
@@ -91,6 +96,7 @@ KERNEL_SOURCES = {
     "decode_attn": ["pkv_kernels.cu", "ptx.cuh", "pkv_internal.h"],
     "decode_group_attn": ["pkv_decode_group.cu", "pkv_kernels.cu", "ptx.cuh", "pkv_internal.h"],
     "decode_i8_attn": ["pkv_int8.cu", "ptx.cuh", "pkv_internal.h"],
+    "decode_cascade_attn": ["pkv_decode_group.cu", "pkv_kernels.cu", "ptx.cuh", "pkv_internal.h"],
     "prefill_attn": ["pkv_prefill.cu", "ptx.cuh", "pkv_internal.h"],
 }
 
@@ -338,10 +344,25 @@ def run_ours(args):
     steps = [StepData(torch, pkv, pool, wl, m, L, dev, gen) for wl, m in zip(iters, _metadata(pkv, iters))]
     wspace = torch.empty(max(max(s.ws_bytes for s in steps), 256), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
+    cascade = args.config == "shared_prefix_cascade"
+    if cascade:
+        s0 = steps[0]
+        need = pool.decode_cascade_workspace_bytes(s0.B, s0.desc.max_blocks)
+        if need > wspace.numel():
+            wspace = torch.empty(need, dtype=torch.uint8, device=dev)
+        gs, gb, widest = pkv.cascade_groups(s0.host[0].numpy(), s0.host[1].numpy())
+        groups = (torch.from_numpy(gs).to(dev), torch.from_numpy(gb).to(dev), widest)
 
     def step(strm=None):
+        strm = strm if strm is not None else stream
         for s in steps:
-            pool.step(s.desc, wspace, strm if strm is not None else stream)
+            if cascade:
+                tables_d, ctx_d, _, slots_d = s.dev
+                for l in range(L):
+                    pool.kv_append(l, s.k[l], s.v[l], slots_d, strm)
+                    pool.decode_attn_cascade(l, s.q[l], tables_d, ctx_d, groups, SCALE, s.out[l], wspace, strm)
+            else:
+                pool.step(s.desc, wspace, strm)
 
     def check_status():
         st, flags = pool.get_status(stream)
@@ -376,7 +397,7 @@ def run_ours(args):
     launches_step = 0
     for s in steps:
         # per layer: decode (it also appends the decode rows' K/V); kv_append + prefill for chunk rows
-        per_layer = (1 if s.B else 0) + (2 if s.max_q else 0)
+        per_layer = (1 if s.B else 0) + (2 if s.max_q else 0) + (2 if cascade else 0)
         launches_step += per_layer * L
 
     sampler = ClockSampler(_gpu_id(torch, local))
@@ -407,6 +428,14 @@ def run_ours(args):
         for s in steps:
             tables_d, ctx_d, qs_d, slots_d = s.dev
             for l in range(L):
+                if cascade:
+                    pool.kv_append(l, s.k[l], s.v[l], slots_d, stream)
+                    a, b = ev(), ev()
+                    a.record(stream)
+                    pool.decode_attn_cascade(l, s.q[l], tables_d, ctx_d, groups, SCALE, s.out[l], wspace, stream)
+                    b.record(stream)
+                    dec_ev.append((a, b, s))
+                    continue
                 if s.layer_desc is not None:
                     # decode-only: the one-layer step is exactly the fused decode+append launch of the full step
                     a, b = ev(), ev()
@@ -448,7 +477,10 @@ def run_ours(args):
         for s, io, oh in zip(steps, host_io, outs_h):
             for src, dst in io:
                 dst.copy_(src, non_blocking=True)
-            pool.step(s.desc, wspace, stream)
+            if cascade:
+                step()
+            else:
+                pool.step(s.desc, wspace, stream)
             oh.copy_(s.out, non_blocking=True)
     e5.record(stream)
     torch.cuda.synchronize(dev)
@@ -478,6 +510,19 @@ def run_ours(args):
     dec_src = "decode_attn" if Hq == H else "decode_group_attn"
     if dtype == "int8":
         dec_kernel, dec_src = "decode_i8_kernel (INT8 codes dequantised in the loaders)", "decode_i8_attn"
+    unique_step = None
+    if args.config in ("shared_prefix_decode", "shared_prefix_cascade"):
+        # K/V bytes a layer must read at least once: the shared prefix once, then each row's own tokens
+        w0 = steps[0].wl
+        pre = int(w0.meta["prefix_blocks"]) * 16
+        unique_tok = pre + int((w0.ctx_lens[:w0.num_decode].astype(np.int64) - pre).sum())
+        unique_step = unique_tok * 2 * H * row_bytes(dtype) * L
+    if cascade:
+        dec_kernel = ("cascade decode: decode_group_kernel<true, true> (shared partitions, 16 rows per CTA, "
+                      "mma.sync) then decode_kernel (the rest, merge)")
+        dec_src = "decode_cascade_attn"
+        # the roofline of a cascade launch: unique bytes + q and out
+        dec_bytes_launch = unique_step / L / len(steps) + sum(2 * s.B * Hq * HEAD_DIM * 2 for s in steps) / len(steps)
     rooflines = {}
     if n_dec:
         ach = dec_bytes_launch / (dec_ms / n_dec * 1e-3) / 1e9
@@ -537,6 +582,10 @@ def run_ours(args):
     }
     if has_decode:
         result["hbm_frac_of_measured_peak"] = round(value / hbm_peak, 4)
+    if unique_step:
+        result["unique_kv_bytes_per_step"] = unique_step
+        result["unique_gbs"] = round(unique_step * K * ws / (t_ms * 1e-3) / 1e9, 1)
+        result["unique_frac_of_measured_peak"] = round(unique_step * K * ws / (t_ms * 1e-3) / 1e9 / hbm_peak, 4)
     if has_prefill:
         result["prefill_tflops"] = round(flops_step * K * ws / (t_ms * 1e-3) / 1e12, 1)
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
@@ -819,7 +868,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", default="average_decode",
                     choices=["average_decode", "long_decode", "shared_prefix_decode", "mixed_prefill", "gqa_decode",
-                             "average_decode_int8", "swap_blocks"])
+                             "average_decode_int8", "swap_blocks", "shared_prefix_cascade"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="launch each step directly instead of replaying a CUDA graph")

@@ -252,6 +252,42 @@ pkv_status pkv_decode_attn(pkv_pool* pool, int32_t layer, const void* q, const i
                            int32_t max_blocks, const int32_t* ctx_lens, int32_t num_seqs, float scale, void* out,
                            void* workspace, size_t workspace_bytes, void* stream);
 
+/* Cascade decode for rows that share a prompt prefix ("The inference engine"
+ * (wpnews), "Paging turns variable sequences into block tables": sequences
+ * may point at the same immutable prefix blocks). Same inputs and result as
+ * pkv_decode_attn (within the attention tolerance; the shared part runs on
+ * the tensor cores with the softmax weights rounded to FP16), plus a grouping
+ * of the rows: rows [group_start[i], group_start[i+1]) (device int32,
+ * num_groups + 1 entries, group_start[num_groups] = num_seqs) share their first
+ * group_blocks[i] table entries (device int32), which must be the same
+ * physical blocks, full, and below every row's newest token. Every split-K
+ * partition wholly inside a group's shared prefix is computed once for up to
+ * 16 rows at a time, so its K/V tiles are read from memory once per group
+ * instead of once per row; the rest of each row runs as in pkv_decode_attn,
+ * which merges all partitions. max_group_rows = the largest group.
+ * FP16 pools with num_q_heads == num_heads. No append: call pkv_kv_append
+ * first. Partition plan: a row's shared prefix [0, S) and the rest [S, ctx)
+ * are each cut into partitions of partition_tokens (so a row can have one
+ * partition more than in pkv_decode_attn); results are deterministic for a
+ * given grouping. The workspace must hold pkv_decode_cascade_workspace_bytes. */
+pkv_status pkv_decode_attn_cascade(pkv_pool* pool, int32_t layer, const void* q, const int32_t* block_tables,
+                                   int32_t max_blocks, const int32_t* ctx_lens, int32_t num_seqs,
+                                   const int32_t* group_start, const int32_t* group_blocks, int32_t num_groups,
+                                   int32_t max_group_rows, float scale, void* out, void* workspace,
+                                   size_t workspace_bytes, void* stream);
+
+size_t pkv_decode_cascade_workspace_bytes(const pkv_pool* pool, int32_t num_seqs, int32_t max_blocks);
+
+/* Host helper for the grouping: maximal runs of consecutive rows of host
+ * block_tables [num_seqs, max_blocks] / ctx_lens that share leading blocks
+ * (the first two rows' common prefix, limited to blocks wholly below each
+ * row's newest token); runs shorter than min_rows become single rows with no
+ * shared prefix. Writes group_start [num_groups + 1] and group_blocks
+ * [num_groups] (host, capacity num_seqs + 1 and num_seqs). */
+pkv_status pkv_cascade_groups(const int32_t* block_tables, const int32_t* ctx_lens, int32_t num_seqs,
+                              int32_t max_blocks, int32_t min_rows, int32_t* group_start, int32_t* group_blocks,
+                              int32_t* num_groups, int32_t* max_group_rows);
+
 /* Chunked causal prefill: sequence s owns query tokens
  * [q_start_loc[s], q_start_loc[s+1]) of q ([num_tokens, num_q_heads, 128] FP16);
  * query i sits at position ctx_lens[s] - q_len + i and attends keys 0..that

@@ -75,6 +75,9 @@ SIGNATURES = {
     "pkv_decode_attn": (_i32, [_P, _i32, _P, _P, _i32, _P, _i32, _f32, _P, _P, _sz, _P]),
     "pkv_prefill_attn": (_i32, [_P, _i32, _P, _P, _P, _i32, _P, _i32, _i32, _f32, _P, _P]),
     "pkv_decode_attn_noalloc": (_i32, [_P, _i32, _P, _P, _i32, _P, _i32, _f32, _P, _P]),
+    "pkv_decode_attn_cascade": (_i32, [_P, _i32, _P, _P, _i32, _P, _i32, _P, _P, _i32, _i32, _f32, _P, _P, _sz, _P]),
+    "pkv_decode_cascade_workspace_bytes": (_sz, [_P, _i32, _i32]),
+    "pkv_cascade_groups": (_i32, [_P, _P, _i32, _i32, _i32, _P, _P, _c.POINTER(_i32), _c.POINTER(_i32)]),
     "pkv_step_workspace_bytes": (_sz, [_P, _SD]),
     "pkv_step": (_i32, [_P, _SD, _P, _sz, _P]),
     "pkv_get_status": (_i32, [_P, _P, _c.POINTER(_u32)]),
@@ -303,6 +306,19 @@ class Pool:
                                               int(block_tables.shape[1]), _ptr(ctx_lens), int(ctx_lens.shape[0]),
                                               float(scale), _ptr(out), _stream(stream)))
 
+    def decode_cascade_workspace_bytes(self, num_seqs: int, max_blocks: int) -> int:
+        return load().pkv_decode_cascade_workspace_bytes(self.handle, num_seqs, max_blocks)
+
+    def decode_attn_cascade(self, layer: int, q, block_tables, ctx_lens, groups, scale: float, out, workspace=None,
+                            stream=None) -> None:
+        """groups = (group_start device int32 [G+1], group_blocks device int32 [G], max_group_rows)."""
+        gs, gb, widest = groups
+        ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+        _check(load().pkv_decode_attn_cascade(self.handle, layer, _ptr(q), _ptr(block_tables),
+                                              int(block_tables.shape[1]), _ptr(ctx_lens), int(ctx_lens.shape[0]),
+                                              _ptr(gs), _ptr(gb), int(gb.shape[0]), int(widest), float(scale),
+                                              _ptr(out), _ptr(workspace), ws_bytes, _stream(stream)))
+
     def prefill_attn(self, layer: int, q, q_start_loc, block_tables, ctx_lens, max_q_len: int, scale: float, out,
                      stream=None) -> None:
         _check(load().pkv_prefill_attn(self.handle, layer, _ptr(q), _ptr(q_start_loc), _ptr(block_tables),
@@ -324,6 +340,20 @@ class Pool:
 
     def debug_wait_probe(self, timeout_ns: int, stream=None) -> None:
         _check(load().pkv_debug_wait_probe(self.handle, int(timeout_ns), _stream(stream)))
+
+
+def cascade_groups(tables, ctx_lens, min_rows: int = 2):
+    """(group_start int32 [G+1], group_blocks int32 [G], max_group_rows) from host tables / lengths."""
+    import numpy as np
+    t = np.ascontiguousarray(tables, np.int32)
+    c = np.ascontiguousarray(ctx_lens, np.int32)
+    B = t.shape[0]
+    gs = np.zeros(B + 1, np.int32)
+    gb = np.zeros(max(B, 1), np.int32)
+    G, W = _i32(), _i32()
+    _check(load().pkv_cascade_groups(t.ctypes.data, c.ctypes.data, B, t.shape[1], int(min_rows), gs.ctypes.data,
+                                     gb.ctypes.data, _c.byref(G), _c.byref(W)))
+    return gs[:G.value + 1], gb[:G.value], W.value
 
 
 def block_hashes(tokens):

@@ -39,6 +39,16 @@
 // run first. Rows of a row's last block past ctx_len are zeroed in shared
 // memory before P V: P is zero there, but the pool may hold anything (even
 // NaN) in unwritten slots, and 0 x NaN would poison the tensor-core sum.
+//
+// Cascade mode (CASCADE = true, pools with one query head per K/V head): the
+// MMA rows are up to 16 batch rows of a group that share their leading
+// blocks (a shared prompt prefix: "The inference engine" (wpnews), "Paging
+// turns variable sequences into block tables": sequences may point at the
+// same immutable prefix blocks), all for one head. A CTA handles one split-K
+// partition lying wholly inside the shared prefix, so each shared K/V tile is
+// read from memory once per group instead of once per row; it writes each
+// row's partial and counts it. The one-head kernel then computes the rows'
+// remaining partitions and merges all of them.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_fp16.h>
@@ -93,12 +103,17 @@ struct GroupArgs {
     float* ws_ml;      // [B][num_q_heads][max_parts][2]
     unsigned int* counters;  // [B][num_kv_heads * slices], zero between launches
     int max_parts;
+    int ws_parts;            // partial slots per (row, query head)
     int part_tokens;
     const __half* k_new;     // [B][num_kv_heads][128] when append
     const __half* v_new;
     const int64_t* slots;    // [B] when append
     int append;
     unsigned int* status;
+    // cascade mode: rows [group_start[i], group_start[i+1]) share their first group_blocks[i] blocks
+    const int32_t* group_start;
+    const int32_t* group_blocks;
+    int max_slices;          // ceil(largest group / 16)
 };
 
 // Byte offset of 16-byte chunk ch (dimensions 8ch .. 8ch+7) of token t in a
@@ -117,27 +132,51 @@ __device__ __forceinline__ unsigned int group_atomic_add_acq_rel(unsigned int* p
     return old;
 }
 
-// ROWS16: some query head of the CTA sits in fragment rows 8..15 (R > 8).
-template <bool ROWS16>
+// ROWS16: some row of the CTA sits in fragment rows 8..15 (R > 8).
+template <bool ROWS16, bool CASCADE>
 __global__ void __launch_bounds__(kGWarps * 32) decode_group_kernel(const __grid_constant__ CUtensorMap tmap,
                                                                      const GroupArgs a)
 {
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     const uint32_t sb = smem_u32(smem);
-    const int p = blockIdx.x, r = blockIdx.z;
-    const int kvh = blockIdx.y / a.slices, c = blockIdx.y % a.slices;
+    const int p = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, tq = lane & 3;  // fragment row and column pair of this lane
-    const int h0 = kvh * a.group + c * a.rows;
-
-    const int ctx = __ldg(a.ctx_lens + r);
-    if (ctx < 1 || ctx > a.max_blocks * kBlockSize) {
-        if (p == 0 && blockIdx.y == 0 && threadIdx.x == 0) atomicOr(a.status, PKV_DEV_BAD_CTX);
-        return;
+    // The CTA's rows: query heads h0 .. h0 + R - 1 of row r, or (cascade) rows r .. r + R - 1 of one group,
+    // head h0. Row i's query is q + qoff + i * qstride and its output / partial index rh0 + i * rstride.
+    int r, kvh, c, h0, R, ctx, nparts;
+    int64_t qstride, rstride;
+    if (CASCADE) {
+        const int grp = blockIdx.z / a.max_slices, sl = blockIdx.z % a.max_slices;
+        const int row0 = __ldg(a.group_start + grp), row_end = __ldg(a.group_start + grp + 1);
+        r = row0 + sl * kGRows;
+        R = min(kGRows, row_end - r);
+        if (R <= 0) return;
+        kvh = blockIdx.y;
+        c = 0;
+        h0 = kvh;
+        ctx = __ldg(a.group_blocks + grp) * kBlockSize;  // the shared prefix: full blocks, valid for every row
+        nparts = (ctx + a.part_tokens - 1) / a.part_tokens;  // the prefix partitioned on its own
+        if (p >= nparts) return;
+        qstride = (int64_t)a.num_q_heads * kHeadDim;
+        rstride = a.num_q_heads;
+    } else {
+        r = blockIdx.z;
+        kvh = blockIdx.y / a.slices;
+        c = blockIdx.y % a.slices;
+        h0 = kvh * a.group + c * a.rows;
+        R = a.rows;
+        ctx = __ldg(a.ctx_lens + r);
+        if (ctx < 1 || ctx > a.max_blocks * kBlockSize) {
+            if (p == 0 && blockIdx.y == 0 && threadIdx.x == 0) atomicOr(a.status, PKV_DEV_BAD_CTX);
+            return;
+        }
+        nparts = (ctx + a.part_tokens - 1) / a.part_tokens;
+        if (p >= nparts) return;
+        qstride = kHeadDim;
+        rstride = 1;
     }
-    const int nparts = (ctx + a.part_tokens - 1) / a.part_tokens;
-    if (p >= nparts) return;
     const int blk_lo = p * a.part_tokens / kBlockSize;
     const int blk_hi = (min((p + 1) * a.part_tokens, ctx) + kBlockSize - 1) / kBlockSize;
     const int count = blk_hi - blk_lo;  // <= kGMaxBlocks (partition_tokens <= 2,048, a multiple of 64)
@@ -180,7 +219,7 @@ __global__ void __launch_bounds__(kGWarps * 32) decode_group_kernel(const __grid
     const int new_t = (ctx - 1) % kBlockSize, new_i = (ctx - 1) / kBlockSize - blk_lo;
     int patch_li = -1;
     uint4 patch = make_uint4(0, 0, 0, 0);  // lanes 0-15: K chunk `lane`, lanes 16-31: V chunk `lane - 16`
-    if (a.append && p == nparts - 1) {
+    if (!CASCADE && a.append && p == nparts - 1) {
         const int64_t slot = __ldg(a.slots + r);
         const int32_t tb = __ldg(trow + (ctx - 1) / kBlockSize);
         const bool consistent =
@@ -205,9 +244,10 @@ __global__ void __launch_bounds__(kGWarps * 32) decode_group_kernel(const __grid
     // Q as the A operand: rows = the CTA's query heads (zero past R), k = dims.
     uint32_t qa[8][4];
     {
-        const uint32_t* qlo = reinterpret_cast<const uint32_t*>(a.q + ((int64_t)r * a.num_q_heads + h0 + g) * kHeadDim);
-        const uint32_t* qhi = qlo + 8 * kHeadDim / 2;
-        const bool lo_ok = g < a.rows, hi_ok = ROWS16 && g + 8 < a.rows;
+        const __half* q0 = a.q + ((int64_t)r * a.num_q_heads + h0) * kHeadDim;
+        const uint32_t* qlo = reinterpret_cast<const uint32_t*>(q0 + g * qstride);
+        const uint32_t* qhi = reinterpret_cast<const uint32_t*>(q0 + (g + 8) * qstride);
+        const bool lo_ok = g < R, hi_ok = ROWS16 && g + 8 < R;
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
             qa[ks][0] = lo_ok ? __ldg(qlo + 8 * ks + tq) : 0u;
@@ -355,7 +395,7 @@ __global__ void __launch_bounds__(kGWarps * 32) decode_group_kernel(const __grid
     const float* mo = reinterpret_cast<const float*>(smem + kGSmMergeO);
     const float* mml = reinterpret_cast<const float*>(smem + kGSmMergeML);
     const int64_t rh0 = (int64_t)r * a.num_q_heads + h0;
-    for (int row = 0; row < a.rows; ++row) {
+    for (int row = 0; row < R; ++row) {
         float M = -INFINITY;
 #pragma unroll
         for (int w = 0; w < kGWarps; ++w) M = fmaxf(M, mml[(w * kGRows + row) * 2]);
@@ -366,16 +406,25 @@ __global__ void __launch_bounds__(kGWarps * 32) decode_group_kernel(const __grid
             L = fmaf(wt, mml[(w * kGRows + row) * 2 + 1], L);
             O = fmaf(wt, mo[(w * kGRows + row) * kGMergeStride + d], O);
         }
-        if (nparts == 1) {
+        if (!CASCADE && nparts == 1) {
             a.out[(rh0 + row) * kHeadDim + d] = __float2half_rn(O * (1.f / L));
         } else {
-            const int64_t slot = (rh0 + row) * a.max_parts + p;
+            const int64_t slot = (rh0 + row * rstride) * a.ws_parts + p;
             a.ws_o[slot * kHeadDim + d] = O;
             if (d == 0) {
                 a.ws_ml[slot * 2] = M;
                 a.ws_ml[slot * 2 + 1] = L;
             }
         }
+    }
+    if (CASCADE) {
+        // count the partials; the one-head kernel's last partition of each (row, head) merges them
+        __syncthreads();
+        if (threadIdx.x < R) {
+            __threadfence();
+            atomicAdd(a.counters + rh0 + threadIdx.x * rstride, 1u);
+        }
+        return;
     }
     if (nparts == 1) return;
 
@@ -386,8 +435,8 @@ __global__ void __launch_bounds__(kGWarps * 32) decode_group_kernel(const __grid
     if (threadIdx.x == 0) *flag = group_atomic_add_acq_rel(counter, 1u) == (unsigned int)(nparts - 1);
     __syncthreads();
     if (!*flag) return;
-    for (int row = 0; row < a.rows; ++row) {
-        const int64_t base = (rh0 + row) * a.max_parts;
+    for (int row = 0; row < R; ++row) {
+        const int64_t base = (rh0 + row) * a.ws_parts;
         float M = -INFINITY;
         for (int q = 0; q < nparts; ++q) M = fmaxf(M, __ldcg(a.ws_ml + (base + q) * 2));
         float L = 0.f, O = 0.f;
@@ -402,20 +451,19 @@ __global__ void __launch_bounds__(kGWarps * 32) decode_group_kernel(const __grid
     if (threadIdx.x == 0) *counter = 0u;
 }
 
-template <bool ROWS16>
-cudaError_t launch_group(const CUtensorMap& tmap, const GroupArgs& a, int num_seqs, cudaStream_t stream)
+template <bool ROWS16, bool CASCADE>
+cudaError_t launch_group(const CUtensorMap& tmap, const GroupArgs& a, dim3 grid, cudaStream_t stream)
 {
     static bool attr_set[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 64 && !attr_set[dev]) {
-        cudaError_t e =
-            cudaFuncSetAttribute(decode_group_kernel<ROWS16>, cudaFuncAttributeMaxDynamicSharedMemorySize, kGSmAlloc);
+        cudaError_t e = cudaFuncSetAttribute(decode_group_kernel<ROWS16, CASCADE>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kGSmAlloc);
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
-    dim3 grid(a.max_parts, a.num_kv_heads * a.slices, num_seqs);
-    decode_group_kernel<ROWS16><<<grid, kGWarps * 32, kGSmAlloc, stream>>>(tmap, a);
+    decode_group_kernel<ROWS16, CASCADE><<<grid, kGWarps * 32, kGSmAlloc, stream>>>(tmap, a);
     return cudaGetLastError();
 }
 
@@ -488,16 +536,62 @@ cudaError_t launch_decode_group(const PoolGeom& g, const TensorMap128& kv_tmap, 
     a.ws_ml = ws.ml;
     a.counters = ws.counters;
     a.max_parts = decode_max_parts(max_blocks, partition_tokens);
+    a.ws_parts = ws.parts;
     a.part_tokens = partition_tokens;
     a.k_new = static_cast<const __half*>(k_new);
     a.v_new = static_cast<const __half*>(v_new);
     a.slots = slots;
     a.append = k_new != nullptr;
     a.status = status;
+    a.group_start = a.group_blocks = nullptr;
+    a.max_slices = 0;
     CUtensorMap tmap;
     static_assert(sizeof(tmap) == sizeof(kv_tmap.bytes), "tensor map size");
     memcpy(&tmap, kv_tmap.bytes, sizeof(tmap));
-    return a.rows > 8 ? launch_group<true>(tmap, a, num_seqs, stream) : launch_group<false>(tmap, a, num_seqs, stream);
+    const dim3 grid(a.max_parts, a.num_kv_heads * a.slices, num_seqs);
+    return a.rows > 8 ? launch_group<true, false>(tmap, a, grid, stream)
+                      : launch_group<false, false>(tmap, a, grid, stream);
+}
+
+cudaError_t launch_decode_shared_prefix(const PoolGeom& g, const TensorMap128& kv_tmap, int layer, const void* q,
+                                        const int32_t* tables, int max_blocks, int num_seqs,
+                                        const int32_t* group_start, const int32_t* group_blocks, int num_groups,
+                                        int max_group_rows, float scale, const DecodeWs& ws, int partition_tokens,
+                                        unsigned int* status, cudaStream_t stream)
+{
+    if (num_groups == 0) return cudaSuccess;
+    GroupArgs a;
+    memset(&a, 0, sizeof(a));
+    a.q = static_cast<const __half*>(q);
+    a.tables = tables;
+    a.max_blocks = max_blocks;
+    a.pool = const_cast<char*>(g.base);
+    a.block_bytes = g.block_bytes;
+    a.head_off = (int64_t)layer * g.layer_bytes;
+    a.kv_bytes = g.kv_bytes;
+    a.num_blocks = g.num_blocks;
+    a.layer = layer;
+    a.num_kv_heads = g.num_heads;
+    a.num_q_heads = g.num_q_heads;
+    a.group = 1;
+    a.slices = 1;
+    a.rows = kGRows;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    a.ws_o = ws.o;
+    a.ws_ml = ws.ml;
+    a.counters = ws.counters;
+    a.max_parts = decode_max_parts(max_blocks, partition_tokens);
+    a.ws_parts = ws.parts;
+    a.part_tokens = partition_tokens;
+    a.status = status;
+    a.group_start = group_start;
+    a.group_blocks = group_blocks;
+    a.max_slices = (max_group_rows + kGRows - 1) / kGRows;
+    (void)num_seqs;
+    CUtensorMap tmap;
+    memcpy(&tmap, kv_tmap.bytes, sizeof(tmap));
+    const dim3 grid(a.max_parts, g.num_heads, num_groups * a.max_slices);
+    return launch_group<true, true>(tmap, a, grid, stream);
 }
 
 }  // namespace pkv

@@ -633,10 +633,10 @@ static cudaError_t launch_decode_any(const pkv_pool* pool, int32_t layer, const 
                                      scale, out, w,
                                      pool->partition_tokens, k_new, v_new, slots, pool->status_dev, s);
     }
-    if (pool->geom.group == 1)
-        return pkv::launch_decode(pool->geom, layer, q, tables, max_blocks, ctx_lens, num_seqs, scale, out, ws,
-                                  pool->partition_tokens, k_new, v_new, slots, pool->status_dev, s);
     const pkv::DecodeWs w = pkv::decode_ws(pool->geom, ws, num_seqs, max_blocks, pool->partition_tokens);
+    if (pool->geom.group == 1)
+        return pkv::launch_decode(pool->geom, layer, q, tables, max_blocks, ctx_lens, num_seqs, scale, out, w,
+                                  pool->partition_tokens, k_new, v_new, slots, pool->status_dev, s);
     return pkv::launch_decode_group(pool->geom, pool->tile_tmap, layer, q, tables, max_blocks, ctx_lens, num_seqs, scale,
                                     out, w, pool->partition_tokens, k_new, v_new, slots, pool->status_dev, s);
 }
@@ -684,6 +684,92 @@ pkv_status pkv_decode_attn(pkv_pool* pool, int32_t layer, const void* q, const i
     e = launch_decode_any(pool, layer, q, block_tables, max_blocks, ctx_lens, num_seqs, scale, out, workspace, nullptr,
                           nullptr, nullptr, s);
     return e == cudaSuccess ? PKV_OK : pkv::cuda_fail(e, "decode launch");
+}
+
+pkv_status pkv_cascade_groups(const int32_t* tables, const int32_t* ctx_lens, int32_t num_seqs, int32_t max_blocks,
+                              int32_t min_rows, int32_t* group_start, int32_t* group_blocks, int32_t* num_groups,
+                              int32_t* max_group_rows)
+{
+    if (num_seqs < 0 || max_blocks < 1 || min_rows < 1 || !num_groups || !max_group_rows)
+        return fail(PKV_E_INVALID, "bad sizes or NULL output");
+    if (num_seqs > 0 && (!tables || !ctx_lens || !group_start || !group_blocks)) return fail(PKV_E_INVALID, "NULL array");
+    // blocks of row i that lie wholly before its newest token (a shared block never holds one)
+    auto full = [&](int32_t i) { return std::max(0, std::min(max_blocks, (ctx_lens[i] - 1) / pkv::kBlockSize)); };
+    auto lcp = [&](int32_t i, int32_t j, int32_t limit) {
+        int32_t k = 0;
+        const int32_t* a = tables + (int64_t)i * max_blocks;
+        const int32_t* b = tables + (int64_t)j * max_blocks;
+        while (k < limit && a[k] == b[k] && a[k] >= 0) ++k;
+        return k;
+    };
+    int32_t G = 0, widest = 0;
+    for (int32_t i = 0; i < num_seqs;) {
+        int32_t j = i + 1, cp = 0;
+        if (j < num_seqs) cp = lcp(i, j, std::min(full(i), full(j)));
+        if (cp > 0)
+            while (j < num_seqs && lcp(i, j, std::min(cp, full(j))) >= cp) ++j;
+        if (cp == 0 || j - i < min_rows) {
+            j = i + 1;
+            cp = 0;
+        }
+        group_start[G] = i;
+        group_blocks[G] = cp;
+        widest = std::max(widest, j - i);
+        ++G;
+        i = j;
+    }
+    if (num_seqs > 0) group_start[G] = num_seqs;
+    else group_start[0] = 0;
+    *num_groups = G;
+    *max_group_rows = widest;
+    return PKV_OK;
+}
+
+pkv_status pkv_decode_attn_cascade(pkv_pool* pool, int32_t layer, const void* q, const int32_t* block_tables,
+                                   int32_t max_blocks, const int32_t* ctx_lens, int32_t num_seqs,
+                                   const int32_t* group_start, const int32_t* group_blocks, int32_t num_groups,
+                                   int32_t max_group_rows, float scale, void* out, void* workspace,
+                                   size_t workspace_bytes, void* stream)
+{
+    if (pkv_status s = check_decode(pool, layer, q, block_tables, max_blocks, ctx_lens, num_seqs, out, workspace,
+                                    workspace_bytes))
+        return s;
+    if (num_seqs == 0) return PKV_OK;
+    const size_t need = pkv::decode_workspace_bytes(num_seqs, pool->desc.num_q_heads, max_blocks,
+                                                    pool->partition_tokens, 1);
+    if (!workspace || workspace_bytes < need || !aligned(workspace, 256))
+        return fail(PKV_E_INVALID, "cascade workspace NULL, unaligned or below %zu bytes", need);
+    if (pool->geom.group != 1 || pool->geom.dtype != PKV_DTYPE_FP16)
+        return fail(PKV_E_INVALID, "cascade decode is built for FP16 pools with one query head per K/V head");
+    if (!pool->tile_tmap_ok) return fail(PKV_E_DEVICE, "TMA descriptor for the pool could not be encoded");
+    if (num_groups < 1 || num_groups > num_seqs || max_group_rows < 1 || max_group_rows > num_seqs || !group_start ||
+        !group_blocks || !aligned(group_start, 4) || !aligned(group_blocks, 4))
+        return fail(PKV_E_INVALID, "bad group description");
+    if ((int64_t)num_groups * ((max_group_rows + 15) / 16) > 65535)
+        return fail(PKV_E_INVALID, "too many groups x 16-row slices (%d x %d) for one launch", num_groups,
+                    (max_group_rows + 15) / 16);
+    DeviceGuard dg(pool->device);
+    if (!dg.ok) return fail(PKV_E_DEVICE, "cannot select the pool's device");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // one partial slot more per row than the plain plan: the shared prefix and the rest are partitioned apart
+    cudaError_t e =
+        pkv::clear_decode_counters(pool->geom, num_seqs, max_blocks, pool->partition_tokens, workspace, s, 1);
+    if (e != cudaSuccess) return pkv::cuda_fail(e, "clear decode counters");
+    const pkv::DecodeWs w = pkv::decode_ws(pool->geom, workspace, num_seqs, max_blocks, pool->partition_tokens, 1);
+    e = pkv::launch_decode_shared_prefix(pool->geom, pool->tile_tmap, layer, q, block_tables, max_blocks, num_seqs,
+                                         group_start, group_blocks, num_groups, max_group_rows, scale, w,
+                                         pool->partition_tokens, pool->status_dev, s);
+    if (e != cudaSuccess) return pkv::cuda_fail(e, "cascade (shared prefix) launch");
+    e = pkv::launch_decode(pool->geom, layer, q, block_tables, max_blocks, ctx_lens, num_seqs, scale, out, w,
+                           pool->partition_tokens, nullptr, nullptr, nullptr, pool->status_dev, s, group_start,
+                           group_blocks, num_groups);
+    return e == cudaSuccess ? PKV_OK : pkv::cuda_fail(e, "cascade decode launch");
+}
+
+size_t pkv_decode_cascade_workspace_bytes(const pkv_pool* pool, int32_t num_seqs, int32_t max_blocks)
+{
+    if (!pool || num_seqs < 0 || max_blocks < 1) return 0;
+    return pkv::decode_workspace_bytes(num_seqs, pool->desc.num_q_heads, max_blocks, pool->partition_tokens, 1);
 }
 
 pkv_status pkv_prefill_attn(pkv_pool* pool, int32_t layer, const void* q, const int32_t* q_start_loc,

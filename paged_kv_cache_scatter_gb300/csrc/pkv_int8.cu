@@ -153,6 +153,7 @@ struct I8Args {
     float* ws_ml;
     unsigned int* counters;  // [B][num_kv_heads * slices]
     int max_parts;
+    int ws_parts;
     int part_tokens;
     const __half* k_new;     // [B][num_kv_heads][128] when append
     const __half* v_new;
@@ -473,7 +474,7 @@ __global__ void __launch_bounds__(kQWarps * 32) decode_i8_kernel(const __grid_co
         if (nparts == 1) {
             a.out[(rh0 + row) * kHeadDim + d] = __float2half_rn(O * (1.f / L));
         } else {
-            const int64_t slot = (rh0 + row) * a.max_parts + p;
+            const int64_t slot = (rh0 + row) * a.ws_parts + p;
             a.ws_o[slot * kHeadDim + d] = O;
             if (d == 0) {
                 a.ws_ml[slot * 2] = M;
@@ -490,7 +491,7 @@ __global__ void __launch_bounds__(kQWarps * 32) decode_i8_kernel(const __grid_co
     __syncthreads();
     if (!*flag) return;
     for (int row = 0; row < a.rows; ++row) {
-        const int64_t base = (rh0 + row) * a.max_parts;
+        const int64_t base = (rh0 + row) * a.ws_parts;
         float M = -INFINITY;
         for (int q = 0; q < nparts; ++q) M = fmaxf(M, __ldcg(a.ws_ml + (base + q) * 2));
         float L = 0.f, O = 0.f;
@@ -599,6 +600,7 @@ cudaError_t launch_decode_i8(const PoolGeom& g, const TensorMap128& i8_tmap, int
     a.ws_ml = ws.ml;
     a.counters = ws.counters;
     a.max_parts = decode_max_parts(max_blocks, partition_tokens);
+    a.ws_parts = ws.parts;
     a.part_tokens = partition_tokens;
     a.k_new = static_cast<const __half*>(k_new);
     a.v_new = static_cast<const __half*>(v_new);

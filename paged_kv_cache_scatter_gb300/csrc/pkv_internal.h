@@ -54,9 +54,10 @@ struct PoolGeom {
 
 // Split-K scratch of one decode launch, carved from the caller's workspace.
 struct DecodeWs {
-    float* o;                // [B][num_q_heads][max_parts][128] un-normalised partial outputs
-    float* ml;               // [B][num_q_heads][max_parts][2] partial max and sum
+    float* o;                // [B][num_q_heads][parts][128] un-normalised partial outputs
+    float* ml;               // [B][num_q_heads][parts][2] partial max and sum
     unsigned int* counters;  // [B][num_q_heads] arrival counters, zero between launches
+    int parts;               // partial slots per (row, query head)
 };
 
 struct alignas(64) TensorMap128 {
@@ -94,17 +95,23 @@ cudaError_t status_word(int device, unsigned int** out);
 cudaError_t launch_kv_append(const PoolGeom& g, int layer, const void* k, const void* v, const int64_t* slots,
                              int num_tokens, unsigned int* status, cudaStream_t stream);
 int decode_max_parts(int max_blocks, int partition_tokens);
-size_t decode_workspace_bytes(int num_seqs, int num_q_heads, int max_blocks, int partition_tokens);
-DecodeWs decode_ws(const PoolGeom& g, void* ws, int num_seqs, int max_blocks, int partition_tokens);
+// extra_parts: partial slots beyond the plain plan's (cascade decode needs one more per row).
+size_t decode_workspace_bytes(int num_seqs, int num_q_heads, int max_blocks, int partition_tokens,
+                              int extra_parts = 0);
+DecodeWs decode_ws(const PoolGeom& g, void* ws, int num_seqs, int max_blocks, int partition_tokens,
+                   int extra_parts = 0);
 // Zero the split-K counters of a decode workspace (they return to zero after every
 // completed launch; this covers the first use and any launch that stopped early).
 cudaError_t clear_decode_counters(const PoolGeom& g, int num_seqs, int max_blocks, int partition_tokens, void* ws,
-                                  cudaStream_t stream);
+                                  cudaStream_t stream, int extra_parts = 0);
 // k_new/v_new/slots non-NULL: the decode rows' kv_append is done by the same kernel.
+// group_start/group_blocks (num_groups > 0): skip each row's partitions inside its group's shared prefix
+// (launch_decode_shared_prefix computed them).
 cudaError_t launch_decode(const PoolGeom& g, int layer, const void* q, const int32_t* tables, int max_blocks,
-                          const int32_t* ctx_lens, int num_seqs, float scale, void* out, void* ws,
+                          const int32_t* ctx_lens, int num_seqs, float scale, void* out, const DecodeWs& ws,
                           int partition_tokens, const void* k_new, const void* v_new, const int64_t* slots,
-                          unsigned int* status, cudaStream_t stream);
+                          unsigned int* status, cudaStream_t stream, const int32_t* group_start = nullptr,
+                          const int32_t* group_blocks = nullptr, int num_groups = 0);
 
 // pkv_int8.cu: the 8-bit cache (quantising kv_append; decode that dequantises in its loaders).
 cudaError_t launch_kv_append_i8(const PoolGeom& g, int layer, const void* k, const void* v, const int64_t* slots,
@@ -118,6 +125,12 @@ cudaError_t launch_decode_i8(const PoolGeom& g, const TensorMap128& i8_tmap, int
 // pkv_decode_group.cu: decode attention for pools whose K/V heads serve groups of query heads.
 bool encode_tile_tmap(const PoolGeom& g, TensorMap128* out, std::string* err);
 int decode_group_slices(int group);
+// Cascade: the partitions wholly inside each group's shared prefix, for every row of the group at once.
+cudaError_t launch_decode_shared_prefix(const PoolGeom& g, const TensorMap128& kv_tmap, int layer, const void* q,
+                                        const int32_t* tables, int max_blocks, int num_seqs,
+                                        const int32_t* group_start, const int32_t* group_blocks, int num_groups,
+                                        int max_group_rows, float scale, const DecodeWs& ws, int partition_tokens,
+                                        unsigned int* status, cudaStream_t stream);
 cudaError_t launch_decode_group(const PoolGeom& g, const TensorMap128& kv_tmap, int layer, const void* q,
                                 const int32_t* tables, int max_blocks, const int32_t* ctx_lens, int num_seqs,
                                 float scale, void* out, const DecodeWs& ws, int partition_tokens, const void* k_new,

@@ -130,12 +130,17 @@ struct DecodeArgs {
     float* ws_ml;           // [B][H][max_parts][2]
     unsigned int* counters; // [B][H], zero between launches
     int max_parts;
+    int ws_parts;           // partial slots per (row, head)
     int part_tokens;
     const __half* k_new;    // [B][H][128] when append
     const __half* v_new;
     const int64_t* slots;   // [B] when append
     int append;
     unsigned int* status;
+    // cascade: a row's partitions wholly inside its group's shared prefix were computed already
+    const int32_t* group_start;   // [num_groups + 1] or NULL
+    const int32_t* group_blocks;  // [num_groups]
+    int num_groups;
 };
 
 template <int WARPS, int STAGES>
@@ -174,10 +179,25 @@ __global__ void __launch_bounds__(WARPS * 32) decode_kernel(const DecodeArgs a)
         if (p == 0 && h == 0 && threadIdx.x == 0) atomicOr(a.status, PKV_DEV_BAD_CTX);
         return;
     }
-    const int nparts = (ctx + a.part_tokens - 1) / a.part_tokens;
-    if (p >= nparts) return;
-    const int blk_lo = (p * a.part_tokens) >> 4;
-    const int blk_hi = (min((p + 1) * a.part_tokens, ctx) + 15) >> 4;
+    // Partition plan: keys [0, ctx) in partitions of part_tokens. Cascade: keys [0, S) of the row's group's
+    // shared prefix are partitioned on their own (computed already, slots 0 .. nsh-1); this CTA takes
+    // partition p of [S, ctx), slot nsh + p.
+    int S = 0;
+    if (a.group_start) {  // the row's group, by binary search over the group starts
+        int lo = 0, hi = a.num_groups - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (__ldg(a.group_start + mid) <= r) lo = mid; else hi = mid - 1;
+        }
+        S = __ldg(a.group_blocks + lo) * kBlockSize;
+    }
+    const int nsh = (S + a.part_tokens - 1) / a.part_tokens;
+    const int tok_lo = S + p * a.part_tokens;
+    if (tok_lo >= ctx) return;
+    const int nparts = nsh + (ctx - S + a.part_tokens - 1) / a.part_tokens;
+    const int slot_p = nsh + p;
+    const int blk_lo = tok_lo >> 4;
+    const int blk_hi = (min(tok_lo + a.part_tokens, ctx) + 15) >> 4;
     const int nblk = blk_hi - blk_lo;
     int count = nblk > warp ? (nblk - warp + WARPS - 1) / WARPS : 0;  // <= 32 by construction
 
@@ -227,7 +247,7 @@ __global__ void __launch_bounds__(WARPS * 32) decode_kernel(const DecodeArgs a)
     const int last_local = ((ctx - 1) >> 4) - blk_lo;
     int patch_iter = -1;  // iteration of this warp that streams the new token's block
     uint4 knew = make_uint4(0, 0, 0, 0), vnew = make_uint4(0, 0, 0, 0);
-    if (a.append && p == nparts - 1) {
+    if (a.append && slot_p == nparts - 1) {
         const int64_t slot = __ldg(a.slots + r);
         const int32_t tb = __ldg(trow + ((ctx - 1) >> 4));
         const bool consistent = slot == (int64_t)tb * kBlockSize + ((ctx - 1) & 15) && tb >= 0 &&
@@ -391,7 +411,7 @@ __global__ void __launch_bounds__(WARPS * 32) decode_kernel(const DecodeArgs a)
         }
         return;
     }
-    const int64_t slot = rh * a.max_parts + p;
+    const int64_t slot = rh * a.ws_parts + slot_p;
     for (int d = threadIdx.x; d < kHeadDim; d += WARPS * 32) {
         float O = 0.f;
 #pragma unroll
@@ -411,7 +431,7 @@ __global__ void __launch_bounds__(WARPS * 32) decode_kernel(const DecodeArgs a)
     if (threadIdx.x == 0) *flag = atomic_add_acq_rel_gpu(a.counters + rh, 1u) == (unsigned int)(nparts - 1);
     __syncthreads();
     if (!*flag) return;
-    const int64_t base = rh * a.max_parts;
+    const int64_t base = rh * a.ws_parts;
     float* s_w = reinterpret_cast<float*>(smem);  // the rings are idle now
     float* s_l = s_w + kMaxMergeParts;
     for (int q = threadIdx.x; q < nparts; q += WARPS * 32) {
@@ -446,9 +466,8 @@ struct WsLayout {
     size_t o_bytes, ml_off, ctr_off, total;
 };
 
-WsLayout ws_layout(int num_seqs, int num_q_heads, int max_blocks, int partition_tokens)
+WsLayout ws_layout(int num_seqs, int num_q_heads, int64_t parts)
 {
-    const int64_t parts = decode_max_parts(max_blocks, partition_tokens);
     const int64_t slots = (int64_t)num_seqs * num_q_heads * parts;
     WsLayout w;
     w.o_bytes = ((size_t)slots * kHeadDim * sizeof(float) + 255) & ~(size_t)255;
@@ -459,17 +478,19 @@ WsLayout ws_layout(int num_seqs, int num_q_heads, int max_blocks, int partition_
 }
 }  // namespace
 
-size_t decode_workspace_bytes(int num_seqs, int num_q_heads, int max_blocks, int partition_tokens)
+size_t decode_workspace_bytes(int num_seqs, int num_q_heads, int max_blocks, int partition_tokens, int extra_parts)
 {
-    if (decode_max_parts(max_blocks, partition_tokens) <= 1) return 256;
-    return ws_layout(num_seqs, num_q_heads, max_blocks, partition_tokens).total;
+    const int parts = decode_max_parts(max_blocks, partition_tokens) + extra_parts;
+    if (parts <= 1) return 256;
+    return ws_layout(num_seqs, num_q_heads, parts).total;
 }
 
-DecodeWs decode_ws(const PoolGeom& g, void* ws, int num_seqs, int max_blocks, int partition_tokens)
+DecodeWs decode_ws(const PoolGeom& g, void* ws, int num_seqs, int max_blocks, int partition_tokens, int extra_parts)
 {
-    DecodeWs d{nullptr, nullptr, nullptr};
-    if (decode_max_parts(max_blocks, partition_tokens) <= 1) return d;
-    const WsLayout w = ws_layout(num_seqs, g.num_q_heads, max_blocks, partition_tokens);
+    const int parts = decode_max_parts(max_blocks, partition_tokens) + extra_parts;
+    DecodeWs d{nullptr, nullptr, nullptr, parts};
+    if (parts <= 1) return d;
+    const WsLayout w = ws_layout(num_seqs, g.num_q_heads, parts);
     d.o = static_cast<float*>(ws);
     d.ml = reinterpret_cast<float*>(static_cast<char*>(ws) + w.ml_off);
     d.counters = reinterpret_cast<unsigned int*>(static_cast<char*>(ws) + w.ctr_off);
@@ -477,18 +498,20 @@ DecodeWs decode_ws(const PoolGeom& g, void* ws, int num_seqs, int max_blocks, in
 }
 
 cudaError_t clear_decode_counters(const PoolGeom& g, int num_seqs, int max_blocks, int partition_tokens, void* ws,
-                                  cudaStream_t stream)
+                                  cudaStream_t stream, int extra_parts)
 {
-    if (num_seqs == 0 || decode_max_parts(max_blocks, partition_tokens) <= 1) return cudaSuccess;
-    const WsLayout w = ws_layout(num_seqs, g.num_q_heads, max_blocks, partition_tokens);
+    const int parts = decode_max_parts(max_blocks, partition_tokens) + extra_parts;
+    if (num_seqs == 0 || parts <= 1) return cudaSuccess;
+    const WsLayout w = ws_layout(num_seqs, g.num_q_heads, parts);
     return cudaMemsetAsync(static_cast<char*>(ws) + w.ctr_off, 0,
                            (size_t)num_seqs * g.num_q_heads * sizeof(unsigned int), stream);
 }
 
 cudaError_t launch_decode(const PoolGeom& g, int layer, const void* q, const int32_t* tables, int max_blocks,
-                          const int32_t* ctx_lens, int num_seqs, float scale, void* out, void* ws,
+                          const int32_t* ctx_lens, int num_seqs, float scale, void* out, const DecodeWs& w,
                           int partition_tokens, const void* k_new, const void* v_new, const int64_t* slots,
-                          unsigned int* status, cudaStream_t stream)
+                          unsigned int* status, cudaStream_t stream, const int32_t* group_start,
+                          const int32_t* group_blocks, int num_groups)
 {
     if (num_seqs == 0) return cudaSuccess;
     using Lay = DecodeLayout<kDecodeWarps, kDecodeStages>;
@@ -521,7 +544,10 @@ cudaError_t launch_decode(const PoolGeom& g, int layer, const void* q, const int
     a.slots = slots;
     a.append = k_new != nullptr;
     a.status = status;
-    const DecodeWs w = decode_ws(g, ws, num_seqs, max_blocks, partition_tokens);
+    a.group_start = num_groups > 0 ? group_start : nullptr;
+    a.group_blocks = group_blocks;
+    a.num_groups = num_groups;
+    a.ws_parts = w.parts;
     a.ws_o = w.o;
     a.ws_ml = w.ml;
     a.counters = w.counters;

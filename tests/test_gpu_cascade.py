@@ -1,0 +1,120 @@
+"""GPU parity of cascade decode (rows sharing a prompt prefix read the shared blocks once per group)
+against the oracle, and against the plain decode kernel, on the shared-prefix workload shape.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from tests import _gpu as G
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def pkv():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    return G.lib()
+
+
+def _groups_wl(seed, sizes, prefix_blocks, max_private=120, num_layers=1):
+    """Rows in consecutive groups; group i's rows share prefix_blocks[i] blocks, then 1..max_private own tokens."""
+    rng = np.random.default_rng(seed)
+    rows, ctx = [], []
+    nb_total = sum(prefix_blocks) + sum(sizes) * (-(-max_private // 16)) + 16
+    perm = rng.permutation(nb_total).astype(np.int32)
+    cur = 0
+    width = max(prefix_blocks) + (-(-max_private // 16)) + 1
+    for n, pb in zip(sizes, prefix_blocks):
+        shared = perm[cur:cur + pb]
+        cur += pb
+        for _ in range(n):
+            u = int(rng.integers(1, max_private + 1))
+            own = -(-u // 16)
+            t = np.full(width, -1, np.int32)
+            t[:pb] = shared
+            t[pb:pb + own] = perm[cur:cur + own]
+            cur += own
+            rows.append(t)
+            ctx.append(pb * 16 + u)
+    tables = np.stack(rows)
+    ctx = np.array(ctx, np.int32)
+    return workloads.Workload(f"groups{seed}", num_layers, nb_total, tables, ctx, np.ones(len(ctx), np.int32), seed)
+
+
+def run_cascade(pkv, wl, partition, check_plain=True):
+    H = 32
+    pool = G.device_pool(wl.num_blocks, wl.num_layers, H, seed=wl.seed)
+    host = G.to_bits(pool).reshape(pool.shape).copy()
+    p = pkv.Pool(pool, wl.num_blocks, num_layers=wl.num_layers, num_heads=H, partition_tokens=partition)
+    tables_d, ctx_d, _, slots_d, slots = G.step_metadata(wl)
+    q, k, v = G.new_token_inputs(wl, 0)
+    p.kv_append(0, k, v, slots_d)
+    g = oracle.geom(wl.num_blocks, wl.num_layers, H)
+    assert oracle.kv_append(host, g, 0, G.to_bits(k), G.to_bits(v), slots) == -1
+    gs, gb, widest = pkv.cascade_groups(wl.block_tables, wl.ctx_lens)
+    groups = (torch.from_numpy(gs).cuda(), torch.from_numpy(gb).cuda(), widest)
+    ws = torch.empty(max(p.decode_cascade_workspace_bytes(wl.num_seqs, wl.max_blocks), 256), dtype=torch.uint8,
+                     device="cuda")
+    assert p.decode_cascade_workspace_bytes(wl.num_seqs, wl.max_blocks) >= p.decode_workspace_bytes(wl.num_seqs,
+                                                                                                     wl.max_blocks)
+    out = torch.full_like(q, float("nan"))
+    p.decode_attn_cascade(0, q, tables_d, ctx_d, groups, G.SCALE, out, ws)
+    assert p.get_status() == (pkv.PKV_OK, 0)
+    ref, _ = oracle.decode_attn(host, g, 0, G.to_bits(q), wl.block_tables, wl.ctx_lens, G.SCALE)
+    G.assert_close(out, ref, f"cascade, partition {partition}")
+    again = torch.full_like(q, float("nan"))
+    p.decode_attn_cascade(0, q, tables_d, ctx_d, groups, G.SCALE, again, ws)
+    assert torch.equal(out, again)                      # deterministic for a given grouping
+    if check_plain:
+        plain = torch.empty_like(q)
+        p.decode_attn(0, q, tables_d, ctx_d, G.SCALE, plain, ws)   # the counters were left at zero
+        assert p.get_status() == (pkv.PKV_OK, 0)
+        G.assert_close(plain, ref, "plain decode after cascade")
+    return gs, gb
+
+
+@pytest.mark.parametrize("partition", [64, 256, 1024])
+def test_cascade_groups_of_many_sizes(pkv, partition):
+    # groups of 1, 5, 16, 17 (two row slices) and 40 rows; shared prefixes of 3 to 70 blocks
+    wl = _groups_wl(1, [1, 5, 16, 17, 40], [3, 70, 20, 5, 64])
+    gs, gb = run_cascade(pkv, wl, partition)
+    assert list(np.diff(gs)) == [1, 5, 16, 17, 40] and list(gb) == [0, 70, 20, 5, 64]
+
+
+def test_cascade_shared_prefix_config(pkv):
+    # the shared-prefix workload's shape: 64 rows over 125 shared blocks + 1..300 private tokens (one layer)
+    wl = workloads.shared_prefix_decode(0, num_layers=1, num_blocks=1500)
+    gs, gb = run_cascade(pkv, wl, 0)
+    assert list(gb) == [125] and list(gs) == [0, 64]
+
+
+def test_cascade_without_sharing_equals_plain_decode(pkv):
+    wl = workloads.random_step(3, num_seqs=7, max_ctx=900, num_blocks=500, num_layers=1)
+    gs, gb = run_cascade(pkv, wl, 64)
+    assert not gb.any()
+
+
+def test_cascade_refuses_bad_groups_and_pools(pkv):
+    wl = _groups_wl(4, [4], [10])
+    pool = G.device_pool(wl.num_blocks, 1, 32, seed=4)
+    p = pkv.Pool(pool, wl.num_blocks, num_layers=1)
+    tables_d, ctx_d, _, _, _ = G.step_metadata(wl)
+    q = torch.zeros(4, 32, 128, dtype=torch.float16, device="cuda")
+    ws = torch.empty(p.decode_cascade_workspace_bytes(4, wl.max_blocks), dtype=torch.uint8, device="cuda")
+    small = torch.empty(p.decode_workspace_bytes(4, wl.max_blocks), dtype=torch.uint8, device="cuda")
+    ok = (torch.tensor([0, 4], dtype=torch.int32, device="cuda"), torch.tensor([10], dtype=torch.int32, device="cuda"),
+          4)
+    with pytest.raises(pkv.PkvError):                      # the plain decode's workspace is one slot short
+        p.decode_attn_cascade(0, q, tables_d, ctx_d, ok, G.SCALE, q, small)
+    bad = (torch.tensor([0, 4], dtype=torch.int32, device="cuda"), torch.tensor([10], dtype=torch.int32, device="cuda"),
+           9)                                              # max_group_rows above num_seqs
+    with pytest.raises(pkv.PkvError):
+        p.decode_attn_cascade(0, q, tables_d, ctx_d, bad, G.SCALE, q, ws)
+    pg = pkv.Pool(G.device_pool(wl.num_blocks, 1, 8, seed=4), wl.num_blocks, num_layers=1, num_heads=8,
+                  num_q_heads=32)
+    good = (bad[0], bad[1], 4)
+    with pytest.raises(pkv.PkvError):
+        pg.decode_attn_cascade(0, q, tables_d, ctx_d, good, G.SCALE, q, ws)
