@@ -215,6 +215,10 @@ __global__ void __launch_bounds__(kGWarps * 32) decode_group_kernel(const __grid
     if (lane == 0)
         for (int li = 0; li < issued; ++li) issue(li);
 
+    // Only lengths, tables and this layer's K/V were read so far; with a programmatic dependency on the
+    // previous layer's kernel, wait for it before reading q or the new K/V and touching the workspace.
+    pdl_wait();
+
     // The new token (position ctx - 1) is the last token of the partition's last block.
     const int new_t = (ctx - 1) % kBlockSize, new_i = (ctx - 1) / kBlockSize - blk_lo;
     int patch_li = -1;
@@ -353,6 +357,7 @@ __global__ void __launch_bounds__(kGWarps * 32) decode_group_kernel(const __grid
             ++issued;
         }
     }
+    pdl_trigger();
     if (!ok) {
         if (lane == 0) {
             atomicOr(a.status, PKV_DEV_TIMEOUT);
@@ -452,7 +457,8 @@ __global__ void __launch_bounds__(kGWarps * 32) decode_group_kernel(const __grid
 }
 
 template <bool ROWS16, bool CASCADE>
-cudaError_t launch_group(const CUtensorMap& tmap, const GroupArgs& a, dim3 grid, cudaStream_t stream)
+cudaError_t launch_group(const CUtensorMap& tmap, const GroupArgs& a, dim3 grid, cudaStream_t stream,
+                         bool pdl = false)
 {
     static bool attr_set[64] = {};
     int dev = 0;
@@ -463,8 +469,17 @@ cudaError_t launch_group(const CUtensorMap& tmap, const GroupArgs& a, dim3 grid,
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
-    decode_group_kernel<ROWS16, CASCADE><<<grid, kGWarps * 32, kGSmAlloc, stream>>>(tmap, a);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kGWarps * 32);
+    cfg.dynamicSmemBytes = kGSmAlloc;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, decode_group_kernel<ROWS16, CASCADE>, tmap, a);
 }
 
 }  // namespace
@@ -511,7 +526,8 @@ int decode_group_slices(int group)
 cudaError_t launch_decode_group(const PoolGeom& g, const TensorMap128& kv_tmap, int layer, const void* q,
                                 const int32_t* tables, int max_blocks, const int32_t* ctx_lens, int num_seqs,
                                 float scale, void* out, const DecodeWs& ws, int partition_tokens, const void* k_new,
-                                const void* v_new, const int64_t* slots, unsigned int* status, cudaStream_t stream)
+                                const void* v_new, const int64_t* slots, unsigned int* status, cudaStream_t stream,
+                                bool pdl)
 {
     if (num_seqs == 0) return cudaSuccess;
     GroupArgs a;
@@ -549,8 +565,8 @@ cudaError_t launch_decode_group(const PoolGeom& g, const TensorMap128& kv_tmap, 
     static_assert(sizeof(tmap) == sizeof(kv_tmap.bytes), "tensor map size");
     memcpy(&tmap, kv_tmap.bytes, sizeof(tmap));
     const dim3 grid(a.max_parts, a.num_kv_heads * a.slices, num_seqs);
-    return a.rows > 8 ? launch_group<true, false>(tmap, a, grid, stream)
-                      : launch_group<false, false>(tmap, a, grid, stream);
+    return a.rows > 8 ? launch_group<true, false>(tmap, a, grid, stream, pdl)
+                      : launch_group<false, false>(tmap, a, grid, stream, pdl);
 }
 
 cudaError_t launch_decode_shared_prefix(const PoolGeom& g, const TensorMap128& kv_tmap, int layer, const void* q,

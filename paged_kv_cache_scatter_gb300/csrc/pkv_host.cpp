@@ -625,20 +625,21 @@ static cudaError_t launch_append_any(const pkv_pool* pool, int32_t layer, const 
 static cudaError_t launch_decode_any(const pkv_pool* pool, int32_t layer, const void* q, const int32_t* tables,
                                      int32_t max_blocks, const int32_t* ctx_lens, int32_t num_seqs, float scale,
                                      void* out, void* ws, const void* k_new, const void* v_new, const int64_t* slots,
-                                     cudaStream_t s)
+                                     cudaStream_t s, bool pdl = false)
 {
     if (pool->geom.dtype == PKV_DTYPE_INT8) {
         const pkv::DecodeWs w = pkv::decode_ws(pool->geom, ws, num_seqs, max_blocks, pool->partition_tokens);
         return pkv::launch_decode_i8(pool->geom, pool->tile_tmap, layer, q, tables, max_blocks, ctx_lens, num_seqs,
-                                     scale, out, w,
-                                     pool->partition_tokens, k_new, v_new, slots, pool->status_dev, s);
+                                     scale, out, w, pool->partition_tokens, k_new, v_new, slots, pool->status_dev, s,
+                                     pdl);
     }
     const pkv::DecodeWs w = pkv::decode_ws(pool->geom, ws, num_seqs, max_blocks, pool->partition_tokens);
     if (pool->geom.group == 1)
         return pkv::launch_decode(pool->geom, layer, q, tables, max_blocks, ctx_lens, num_seqs, scale, out, w,
-                                  pool->partition_tokens, k_new, v_new, slots, pool->status_dev, s);
+                                  pool->partition_tokens, k_new, v_new, slots, pool->status_dev, s, nullptr, nullptr, 0,
+                                  pdl);
     return pkv::launch_decode_group(pool->geom, pool->tile_tmap, layer, q, tables, max_blocks, ctx_lens, num_seqs, scale,
-                                    out, w, pool->partition_tokens, k_new, v_new, slots, pool->status_dev, s);
+                                    out, w, pool->partition_tokens, k_new, v_new, slots, pool->status_dev, s, pdl);
 }
 
 static pkv_status check_decode(pkv_pool* pool, int32_t layer, const void* q, const int32_t* tables, int32_t max_blocks,
@@ -848,8 +849,9 @@ pkv_status pkv_step(pkv_pool* pool, const pkv_step_desc* st, void* workspace, si
             if (e != cudaSuccess) return pkv::cuda_fail(e, "kv_append launch");
         }
         if (B > 0) {
+            // decode-only steps: every layer after the first overlaps its prologue with the previous layer
             e = launch_decode_any(pool, layer, ql, st->block_tables, st->max_blocks, st->ctx_lens, B, st->scale, ol,
-                                  workspace, kl, vl, st->slot_mapping, s);
+                                  workspace, kl, vl, st->slot_mapping, s, P == 0 && i > 0);
             if (e != cudaSuccess) return pkv::cuda_fail(e, "decode launch");
         }
         if (P > 0) {

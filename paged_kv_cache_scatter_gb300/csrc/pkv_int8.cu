@@ -244,6 +244,10 @@ __global__ void __launch_bounds__(kQWarps * 32) decode_i8_kernel(const __grid_co
     if (lane == 0)
         for (int li = 0; li < issued; ++li) issue(li);
 
+    // Only lengths, tables and this layer's codes were read so far; with a programmatic dependency on the
+    // previous layer's kernel, wait for it before reading q or the new K/V and touching the workspace.
+    pdl_wait();
+
     // The new token: quantised here by the warp that streams its block, and stored by c == 0's warp 0.
     const int new_t = (ctx - 1) % kBlockSize, new_i = (ctx - 1) / kBlockSize - blk_lo;
     int patch_li = -1;
@@ -416,6 +420,7 @@ __global__ void __launch_bounds__(kQWarps * 32) decode_i8_kernel(const __grid_co
             ++issued;
         }
     }
+    pdl_trigger();
     if (!ok) {
         if (lane == 0) {
             atomicOr(a.status, PKV_DEV_TIMEOUT);
@@ -507,7 +512,7 @@ __global__ void __launch_bounds__(kQWarps * 32) decode_i8_kernel(const __grid_co
 }
 
 template <bool ROWS16>
-cudaError_t launch_i8(const CUtensorMap& tmap, const I8Args& a, int num_seqs, cudaStream_t stream)
+cudaError_t launch_i8(const CUtensorMap& tmap, const I8Args& a, int num_seqs, cudaStream_t stream, bool pdl)
 {
     static bool attr_set[64] = {};
     int dev = 0;
@@ -518,9 +523,17 @@ cudaError_t launch_i8(const CUtensorMap& tmap, const I8Args& a, int num_seqs, cu
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
-    dim3 grid(a.max_parts, a.num_kv_heads * a.slices, num_seqs);
-    decode_i8_kernel<ROWS16><<<grid, kQWarps * 32, kQSmAlloc, stream>>>(tmap, a);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(a.max_parts, a.num_kv_heads * a.slices, num_seqs);
+    cfg.blockDim = dim3(kQWarps * 32);
+    cfg.dynamicSmemBytes = kQSmAlloc;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, decode_i8_kernel<ROWS16>, tmap, a);
 }
 
 }  // namespace
@@ -575,7 +588,8 @@ bool encode_i8_tmap(const PoolGeom& g, TensorMap128* out, std::string* err)
 cudaError_t launch_decode_i8(const PoolGeom& g, const TensorMap128& i8_tmap, int layer, const void* q,
                              const int32_t* tables, int max_blocks, const int32_t* ctx_lens, int num_seqs,
                              float scale, void* out, const DecodeWs& ws, int partition_tokens, const void* k_new,
-                             const void* v_new, const int64_t* slots, unsigned int* status, cudaStream_t stream)
+                             const void* v_new, const int64_t* slots, unsigned int* status, cudaStream_t stream,
+                             bool pdl)
 {
     if (num_seqs == 0) return cudaSuccess;
     I8Args a;
@@ -610,7 +624,8 @@ cudaError_t launch_decode_i8(const PoolGeom& g, const TensorMap128& i8_tmap, int
     CUtensorMap tmap;
     static_assert(sizeof(tmap) == sizeof(i8_tmap.bytes), "tensor map size");
     memcpy(&tmap, i8_tmap.bytes, sizeof(tmap));
-    return a.rows > 8 ? launch_i8<true>(tmap, a, num_seqs, stream) : launch_i8<false>(tmap, a, num_seqs, stream);
+    return a.rows > 8 ? launch_i8<true>(tmap, a, num_seqs, stream, pdl)
+                      : launch_i8<false>(tmap, a, num_seqs, stream, pdl);
 }
 
 }  // namespace pkv

@@ -111,7 +111,9 @@ cudaError_t launch_decode(const PoolGeom& g, int layer, const void* q, const int
                           const int32_t* ctx_lens, int num_seqs, float scale, void* out, const DecodeWs& ws,
                           int partition_tokens, const void* k_new, const void* v_new, const int64_t* slots,
                           unsigned int* status, cudaStream_t stream, const int32_t* group_start = nullptr,
-                          const int32_t* group_blocks = nullptr, int num_groups = 0);
+                          const int32_t* group_blocks = nullptr, int num_groups = 0, bool pdl = false);
+// pdl: launched with a programmatic dependency on the stream's previous kernel (the previous layer's decode
+// in a decode-only pkv_step): its CTAs load lengths, tables and K/V tiles, then wait for that kernel.
 
 // pkv_int8.cu: the 8-bit cache (quantising kv_append; decode that dequantises in its loaders).
 cudaError_t launch_kv_append_i8(const PoolGeom& g, int layer, const void* k, const void* v, const int64_t* slots,
@@ -120,7 +122,8 @@ bool encode_i8_tmap(const PoolGeom& g, TensorMap128* out, std::string* err);
 cudaError_t launch_decode_i8(const PoolGeom& g, const TensorMap128& i8_tmap, int layer, const void* q,
                              const int32_t* tables, int max_blocks, const int32_t* ctx_lens, int num_seqs,
                              float scale, void* out, const DecodeWs& ws, int partition_tokens, const void* k_new,
-                             const void* v_new, const int64_t* slots, unsigned int* status, cudaStream_t stream);
+                             const void* v_new, const int64_t* slots, unsigned int* status, cudaStream_t stream,
+                             bool pdl = false);
 
 // pkv_decode_group.cu: decode attention for pools whose K/V heads serve groups of query heads.
 bool encode_tile_tmap(const PoolGeom& g, TensorMap128* out, std::string* err);
@@ -134,7 +137,8 @@ cudaError_t launch_decode_shared_prefix(const PoolGeom& g, const TensorMap128& k
 cudaError_t launch_decode_group(const PoolGeom& g, const TensorMap128& kv_tmap, int layer, const void* q,
                                 const int32_t* tables, int max_blocks, const int32_t* ctx_lens, int num_seqs,
                                 float scale, void* out, const DecodeWs& ws, int partition_tokens, const void* k_new,
-                                const void* v_new, const int64_t* slots, unsigned int* status, cudaStream_t stream);
+                                const void* v_new, const int64_t* slots, unsigned int* status, cudaStream_t stream,
+                                bool pdl = false);
 // pkv_blocks.cu: whole-block copies inside the pool (copy-on-write) and to / from host memory (swap).
 cudaError_t launch_copy_blocks(const PoolGeom& g, const int32_t* pairs, int n, unsigned int* status,
                                cudaStream_t stream);

@@ -243,6 +243,11 @@ __global__ void __launch_bounds__(WARPS * 32) decode_kernel(const DecodeArgs a)
         }
     }
 
+    // Everything above reads only what the step's earlier layers never write (lengths, tables, this
+    // layer's K/V). With a programmatic dependency on the previous layer's kernel, wait for it here, before
+    // reading q or the new K/V and before touching the workspace or the output.
+    pdl_wait();
+
     // The new token (position ctx - 1) lives in this partition's last block.
     const int last_local = ((ctx - 1) >> 4) - blk_lo;
     int patch_iter = -1;  // iteration of this warp that streams the new token's block
@@ -367,6 +372,7 @@ __global__ void __launch_bounds__(WARPS * 32) decode_kernel(const DecodeArgs a)
             }
         }
     }
+    pdl_trigger();  // the next layer's CTAs may start their prologue as this grid drains
     if (timed_out) {
         // Give the copies still in flight into this warp's ring a bounded
         // chance to land before the shared memory is reused or released.
@@ -511,7 +517,7 @@ cudaError_t launch_decode(const PoolGeom& g, int layer, const void* q, const int
                           const int32_t* ctx_lens, int num_seqs, float scale, void* out, const DecodeWs& w,
                           int partition_tokens, const void* k_new, const void* v_new, const int64_t* slots,
                           unsigned int* status, cudaStream_t stream, const int32_t* group_start,
-                          const int32_t* group_blocks, int num_groups)
+                          const int32_t* group_blocks, int num_groups, bool pdl)
 {
     if (num_seqs == 0) return cudaSuccess;
     using Lay = DecodeLayout<kDecodeWarps, kDecodeStages>;
@@ -551,9 +557,17 @@ cudaError_t launch_decode(const PoolGeom& g, int layer, const void* q, const int
     a.ws_o = w.o;
     a.ws_ml = w.ml;
     a.counters = w.counters;
-    dim3 grid(a.max_parts, g.num_heads, num_seqs);
-    decode_kernel<kDecodeWarps, kDecodeStages><<<grid, kDecodeWarps * 32, Lay::kBytes, stream>>>(a);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(a.max_parts, g.num_heads, num_seqs);
+    cfg.blockDim = dim3(kDecodeWarps * 32);
+    cfg.dynamicSmemBytes = Lay::kBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, decode_kernel<kDecodeWarps, kDecodeStages>, a);
 }
 
 // ======================================================================

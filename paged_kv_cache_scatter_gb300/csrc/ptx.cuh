@@ -158,6 +158,15 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi)
     return *reinterpret_cast<const uint32_t*>(&h);
 }
 
+// ------------------------------------------------- programmatic dependent launch
+
+// Block until the grids this one depends on have completed and their writes are visible
+// (a no-op when the grid was launched without a programmatic dependency).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Let the dependent grid be scheduled once every CTA of this grid has signalled or exited.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" :::); }
+
 // ---------------------------------------------------------------- helpers
 
 __device__ __forceinline__ void half8_to_float(const uint4& raw, float* f)
