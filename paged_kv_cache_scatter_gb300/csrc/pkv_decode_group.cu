@@ -396,11 +396,14 @@ __global__ void __launch_bounds__(kGWarps * 32) decode_group_kernel(const __grid
         }
     }
     __syncthreads();
-    const int d = threadIdx.x;  // 128 threads: one output dimension each
+    // thread t merges output dimension t % 128 of rows t / 128, t / 128 + kRowStep, ...
+    constexpr int kRowStep = kGWarps * 32 / kHeadDim;
+    static_assert(kGWarps * 32 % kHeadDim == 0, "whole rows per pass");
+    const int d = threadIdx.x % kHeadDim, row0 = threadIdx.x / kHeadDim;
     const float* mo = reinterpret_cast<const float*>(smem + kGSmMergeO);
     const float* mml = reinterpret_cast<const float*>(smem + kGSmMergeML);
     const int64_t rh0 = (int64_t)r * a.num_q_heads + h0;
-    for (int row = 0; row < R; ++row) {
+    for (int row = row0; row < R; row += kRowStep) {
         float M = -INFINITY;
 #pragma unroll
         for (int w = 0; w < kGWarps; ++w) M = fmaxf(M, mml[(w * kGRows + row) * 2]);
@@ -440,7 +443,7 @@ __global__ void __launch_bounds__(kGWarps * 32) decode_group_kernel(const __grid
     if (threadIdx.x == 0) *flag = group_atomic_add_acq_rel(counter, 1u) == (unsigned int)(nparts - 1);
     __syncthreads();
     if (!*flag) return;
-    for (int row = 0; row < R; ++row) {
+    for (int row = row0; row < R; row += kRowStep) {
         const int64_t base = (rh0 + row) * a.ws_parts;
         float M = -INFINITY;
         for (int q = 0; q < nparts; ++q) M = fmaxf(M, __ldcg(a.ws_ml + (base + q) * 2));
