@@ -168,12 +168,20 @@ __device__ __forceinline__ uint32_t code_off(int t, int b)
     return (uint32_t)(t * 128 + ((((b >> 4) ^ (t & 7))) << 4) + (b & 15));
 }
 
-// Two biased code bytes (byte + 128) selected by `sel` into a half2 of the codes, exactly.
+// Two biased code bytes (code + 128) selected by `sel` into a half2 of code + 1,152, exactly (the byte
+// under an FP16 exponent of 1,024). The MMAs run on these biased values; the bias comes off once per
+// score (1,152 * sum(q)) and once per output row (1,152 * sum of the FP16 weights), so no per-value
+// subtraction is needed.
+constexpr float kCodeBias = 1152.f;
 __device__ __forceinline__ uint32_t codes2_to_half2(uint32_t biased, uint32_t sel)
 {
-    const uint32_t h = __byte_perm(biased, 0x64646464u, sel);  // halves 1024 + byte
-    const __half2 r = __hsub2(*reinterpret_cast<const __half2*>(&h), __half2half2(__ushort_as_half(0x6480)));
-    return *reinterpret_cast<const uint32_t*>(&r);
+    return __byte_perm(biased, 0x64646464u, sel);
+}
+
+__device__ __forceinline__ float half2_sum(uint32_t h)
+{
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h));
+    return f.x + f.y;
 }
 
 __device__ __forceinline__ unsigned int q_atomic_add_acq_rel(unsigned int* p, unsigned int v)
@@ -292,11 +300,27 @@ __global__ void __launch_bounds__(kQWarps * 32) decode_i8_kernel(const __grid_co
             qa[j][3] = hi_ok ? __ldg(qhi + 8 * j + 2 * tq + 1) : 0u;
         }
     }
+    // the scores' bias: 1,152 * sum(q) of rows g and g + 8 (q * 1,152 is exact in FP32)
+    float bias_lo = 0.f, bias_hi = 0.f;
+    {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            bias_lo += half2_sum(qa[j][0]) + half2_sum(qa[j][2]);
+            if (ROWS16) bias_hi += half2_sum(qa[j][1]) + half2_sum(qa[j][3]);
+        }
+        bias_lo += __shfl_xor_sync(0xffffffffu, bias_lo, 1);
+        bias_lo += __shfl_xor_sync(0xffffffffu, bias_lo, 2);
+        bias_hi += __shfl_xor_sync(0xffffffffu, bias_hi, 1);
+        bias_hi += __shfl_xor_sync(0xffffffffu, bias_hi, 2);
+        bias_lo *= kCodeBias;
+        bias_hi *= kCodeBias;
+    }
 
     float o[16][4];
 #pragma unroll
     for (int nt = 0; nt < 16; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
     float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.f, l_hi = 0.f;
+    float w_lo = 0.f, w_hi = 0.f;  // running sums of the FP16 weights the P V MMAs saw (this lane's tokens)
     const int mi = lane >> 3, rr = lane & 7;
     bool ok = true;
     for (int li = 0; li < nloc; ++li) {
@@ -348,8 +372,9 @@ __global__ void __launch_bounds__(kQWarps * 32) decode_i8_kernel(const __grid_co
         for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
             for (int e = 0; e < 4; ++e)
-                sv[nt][e] = (nt * 8 + 2 * tq + (e & 1) < nvalid) ? sacc[nt][e] * ksc[nt][e & 1] * a.scale_log2
-                                                                : -INFINITY;
+                sv[nt][e] = (nt * 8 + 2 * tq + (e & 1) < nvalid)
+                                ? (sacc[nt][e] - (e < 2 ? bias_lo : bias_hi)) * ksc[nt][e & 1] * a.scale_log2
+                                : -INFINITY;
         float mx = fmaxf(fmaxf(sv[0][0], sv[0][1]), fmaxf(sv[1][0], sv[1][1]));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
@@ -389,13 +414,18 @@ __global__ void __launch_bounds__(kQWarps * 32) decode_i8_kernel(const __grid_co
                 pw[nt][e] = (nt * 8 + 2 * tq + (e & 1) < nvalid) ? pr[nt][e] * vsc[nt][e & 1] : 0.f;
         const uint32_t pa[4] = {pack_half2(pw[0][0], pw[0][1]), pack_half2(pw[0][2], pw[0][3]),
                                 pack_half2(pw[1][0], pw[1][1]), pack_half2(pw[1][2], pw[1][3])};
+        w_lo = w_lo * al_lo + (half2_sum(pa[0]) + half2_sum(pa[2]));
+        if (ROWS16) w_hi = w_hi * al_hi + (half2_sum(pa[1]) + half2_sum(pa[3]));
+        // rescale O only when some row's running max rose in this block (alpha is exactly 1 otherwise)
+        if (__any_sync(0xffffffffu, al_lo != 1.f || (ROWS16 && al_hi != 1.f))) {
 #pragma unroll
-        for (int nt = 0; nt < 16; ++nt) {
-            o[nt][0] *= al_lo;
-            o[nt][1] *= al_lo;
-            if (ROWS16) {
-                o[nt][2] *= al_hi;
-                o[nt][3] *= al_hi;
+            for (int nt = 0; nt < 16; ++nt) {
+                o[nt][0] *= al_lo;
+                o[nt][1] *= al_lo;
+                if (ROWS16) {
+                    o[nt][2] *= al_hi;
+                    o[nt][3] *= al_hi;
+                }
             }
         }
         // O += P' C_V over chunk pairs; matrices (tokens 0-7 | 8-15) x (chunk cc | cc+1), transposed:
@@ -431,9 +461,23 @@ __global__ void __launch_bounds__(kQWarps * 32) decode_i8_kernel(const __grid_co
     }
     l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 1);
     l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 2);
+    w_lo += __shfl_xor_sync(0xffffffffu, w_lo, 1);
+    w_lo += __shfl_xor_sync(0xffffffffu, w_lo, 2);
     if (ROWS16) {
         l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 1);
         l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 2);
+        w_hi += __shfl_xor_sync(0xffffffffu, w_hi, 1);
+        w_hi += __shfl_xor_sync(0xffffffffu, w_hi, 2);
+    }
+    // take the codes' bias off the outputs: sum over tokens of weight * 1,152, the same for every dimension
+#pragma unroll
+    for (int nt = 0; nt < 16; ++nt) {
+        o[nt][0] -= kCodeBias * w_lo;
+        o[nt][1] -= kCodeBias * w_lo;
+        if (ROWS16) {
+            o[nt][2] -= kCodeBias * w_hi;
+            o[nt][3] -= kCodeBias * w_hi;
+        }
     }
 
     // ---- merge the four warps (warp order); O tile nt = 2 * chunk + parity holds dims 16 chunk + 4tq + 2e + parity
