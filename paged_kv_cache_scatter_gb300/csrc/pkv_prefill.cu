@@ -473,13 +473,19 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             // diagonal tile or padding row: keys past the row's position count as -inf
             const bool diag = !valid || key0 + kKeys - 1 > p0;
             const int nvis = valid ? pos - key0 + 1 : 0;
-            // all of S_j in registers with one load: its buffer is free for S_{j+2} at once
+            // all of S_j in registers, in two halves: the first half's max is taken while the second
+            // half is still on its way from tensor memory; then the buffer is free for S_{j+2}
             uint32_t sr[kKeys];
-            tc_ld128(ts, sr);
+            tc_ld64_issue(ts, sr);
+            tc_wait_ld64(sr);
+            tc_ld64_issue(ts + 64, sr + 64);
+            if (diag) mask_tail<64>(sr, nvis);
+            float mx = max64(sr);
+            tc_wait_ld64(sr + 64);
             tc_fence_before();
             mbar_arrive(bar(S_FREE + sbuf));
-            if (diag) mask_tail<kKeys>(sr, nvis);
-            const float m_tile = fmaxf(max64(sr), max64(sr + 64)) * a.scale_log2;
+            if (diag) mask_tail<64>(sr + 64, nvis - 64);
+            const float m_tile = fmaxf(mx, max64(sr + 64)) * a.scale_log2;
             const bool raise = m_tile > m_used + kRescaleThreshold;  // false while the row has seen no key
             if (j > 0 && __any_sync(0xffffffffu, raise)) {
                 // the previous P V product must have landed before O is rescaled
