@@ -421,49 +421,76 @@ def run_ours(args):
         dist.barrier()
     t_ms = e0.elapsed_time(e1)
 
-    # ---- timed region 2: the same work call by call, events around every attention call
-    dec_ev, pre_ev = [], []
+    # ---- timed region 2: each attention kernel alone. With graphs (the default), one CUDA graph per iteration
+    # and kernel holds that kernel's launches for all layers, replayed between two events: per-launch time =
+    # elapsed / layers, the kernel back to back with itself as the step graph runs it. (Events around single
+    # stream launches would also time the stream's launch gaps, several microseconds per launch on this
+    # platform.) With --no-graph: events around every call.
+    def launch_dec(s, l, strm):
+        tables_d, ctx_d, qs_d, slots_d = s.dev
+        if cascade:
+            pool.decode_attn_cascade(l, s.q[l], tables_d, ctx_d, groups, SCALE, s.out[l], wspace, strm)
+        elif s.layer_desc is not None:
+            # decode-only: the one-layer step is exactly the fused decode+append launch of the full step
+            pool.step(s.layer_desc[l], wspace, strm)
+        else:
+            pool.decode_attn(l, s.q[l, :s.B], tables_d[:s.B], ctx_d[:s.B], SCALE, s.out[l, :s.B], wspace, strm)
+
+    def launch_pre(s, l, strm):
+        tables_d, ctx_d, qs_d, slots_d = s.dev
+        pool.prefill_attn(l, s.q[l], qs_d[s.B:], tables_d[s.B:], ctx_d[s.B:], s.max_q, SCALE, s.out[l], strm)
+
+    dec_ev, pre_ev = [], []  # (start event, end event, iteration, launches between them)
     torch.cuda.synchronize(dev)
-    for _ in range(args.steps):
+    if graph is not None:
+        kgraphs = []
         for s in steps:
-            tables_d, ctx_d, qs_d, slots_d = s.dev
-            for l in range(L):
-                if cascade:
-                    pool.kv_append(l, s.k[l], s.v[l], slots_d, stream)
+            pair = []
+            for use, fn in ((bool(s.B) or cascade, launch_dec), (bool(s.max_q), launch_pre)):
+                g = None
+                if use:
+                    g = torch.cuda.CUDAGraph()
+                    cap = torch.cuda.Stream(dev)
+                    cap.wait_stream(stream)
+                    with torch.cuda.graph(g, stream=cap, capture_error_mode="thread_local"):
+                        for l in range(L):
+                            fn(s, l, torch.cuda.current_stream(dev))
+                pair.append(g)
+            kgraphs.append(pair)
+        torch.cuda.synchronize(dev)
+        for s, (gd, gp) in zip(steps, kgraphs):  # one untimed replay each
+            for g in (gd, gp):
+                if g is not None:
+                    g.replay()
+        torch.cuda.synchronize(dev)
+        for _ in range(args.steps):
+            for s, (gd, gp) in zip(steps, kgraphs):
+                for g, lst in ((gd, dec_ev), (gp, pre_ev)):
+                    if g is None:
+                        continue
                     a, b = ev(), ev()
                     a.record(stream)
-                    pool.decode_attn_cascade(l, s.q[l], tables_d, ctx_d, groups, SCALE, s.out[l], wspace, stream)
+                    g.replay()
                     b.record(stream)
-                    dec_ev.append((a, b, s))
-                    continue
-                if s.layer_desc is not None:
-                    # decode-only: the one-layer step is exactly the fused decode+append launch of the full step
-                    a, b = ev(), ev()
-                    a.record(stream)
-                    pool.step(s.layer_desc[l], wspace, stream)
-                    b.record(stream)
-                    dec_ev.append((a, b, s))
-                    continue
-                pool.kv_append(l, s.k[l], s.v[l], slots_d, stream)
-                if s.B:
-                    a, b = ev(), ev()
-                    a.record(stream)
-                    pool.decode_attn(l, s.q[l, :s.B], tables_d[:s.B], ctx_d[:s.B], SCALE, s.out[l, :s.B], wspace,
-                                     stream)
-                    b.record(stream)
-                    dec_ev.append((a, b, s))
-                if s.max_q:
-                    a, b = ev(), ev()
-                    a.record(stream)
-                    pool.prefill_attn(l, s.q[l], qs_d[s.B:], tables_d[s.B:], ctx_d[s.B:], s.max_q, SCALE, s.out[l],
-                                      stream)
-                    b.record(stream)
-                    pre_ev.append((a, b, s))
+                    lst.append((a, b, s, L))
+    else:
+        for _ in range(args.steps):
+            for s in steps:
+                for l in range(L):
+                    if cascade or s.layer_desc is None:  # a decode-only layer step appends inside its launch
+                        pool.kv_append(l, s.k[l], s.v[l], s.dev[3], stream)
+                    for use, fn, lst in ((bool(s.B) or cascade, launch_dec, dec_ev), (bool(s.max_q), launch_pre, pre_ev)):
+                        if use:
+                            a, b = ev(), ev()
+                            a.record(stream)
+                            fn(s, l, stream)
+                            b.record(stream)
+                            lst.append((a, b, s, 1))
     torch.cuda.synchronize(dev)
     clocks = sampler.stop()
     check_status()
-    dec_ms = sum(a.elapsed_time(b) for a, b, _ in dec_ev)
-    pre_ms = sum(a.elapsed_time(b) for a, b, _ in pre_ev)
+    dec_ms = sum(a.elapsed_time(b) for a, b, _, _ in dec_ev)
+    pre_ms = sum(a.elapsed_time(b) for a, b, _, _ in pre_ev)
 
     # ---- end to end: host buffers in, host result out, every step
     host_io = []
@@ -503,7 +530,8 @@ def run_ours(args):
         value = flops_step * K * ws / (t_ms * 1e-3) / 1e12
         unit = "TFLOP/s"
         e2e_value = flops_step * K * ws / (e2e_ms * 1e-3) / 1e12
-    n_dec = len(dec_ev)
+    n_dec = sum(n for *_, n in dec_ev)
+    n_pre = sum(n for *_, n in pre_ev)
     # K/V context read + q read + out written, per launch
     dec_bytes_launch = (kv_step / L / len(steps)) + sum(2 * s.B * Hq * HEAD_DIM * 2 for s in steps) / len(steps)
     dec_kernel = "decode_kernel" if Hq == H else "decode_group_kernel (mma.sync m16n8k16, one K/V read per group)"
@@ -528,24 +556,28 @@ def run_ours(args):
         ach = dec_bytes_launch / (dec_ms / n_dec * 1e-3) / 1e9
         rooflines["decode"] = {"bound": "hbm",
                                "kernel": dec_kernel + " (with its split-K merge; decode-only steps: also the "
-                                         "decode rows' kv_append), timed per launch incl. the workspace counter clear",
+                                         "decode rows' kv_append), incl. the workspace counter clear",
                                "achieved": round(ach, 1), "peak": hbm_peak, "peak_kind": peak_kind, "unit": "GB/s",
                                "frac": round(ach / hbm_peak, 4),
                                "traffic": _traffic(dec_src, args.config),
                                "algorithmic_bytes_per_launch": int(dec_bytes_launch),
                                "avg_launch_us": round(dec_ms / n_dec * 1e3, 2)}
     if pre_ev:
-        fl = 4 * HEAD_DIM * Hq * sum(prefill_pairs(s.wl) for _, _, s in pre_ev)
+        fl = 4 * HEAD_DIM * Hq * sum(prefill_pairs(s.wl) * n for _, _, s, n in pre_ev)
         ach = fl / (pre_ms * 1e-3) / 1e12
         rooflines["prefill"] = {"bound": "tensor", "kernel": "prefill_kernel (tcgen05)", "achieved": round(ach, 1),
                                 "peak": tf_peak, "peak_kind": peak_kind + " bf16 dense (fp16 runs at the same rate)",
                                 "unit": "TFLOP/s", "frac": round(ach / tf_peak, 4),
                                 "traffic": _traffic("prefill_attn", args.config),
-                                "algorithmic_flops_per_launch": int(fl / len(pre_ev)),
-                                "avg_launch_us": round(pre_ms / len(pre_ev) * 1e3, 2),
-                                "per_chunk_us": [round(sum(a.elapsed_time(b) for a, b, s2 in pre_ev if s2 is s)
-                                                       / max(1, sum(1 for *_, s2 in pre_ev if s2 is s)) * 1e3, 2)
+                                "algorithmic_flops_per_launch": int(fl / n_pre),
+                                "avg_launch_us": round(pre_ms / n_pre * 1e3, 2),
+                                "per_chunk_us": [round(sum(a.elapsed_time(b) for a, b, s2, _ in pre_ev if s2 is s)
+                                                       / max(1, sum(n for _, _, s2, n in pre_ev if s2 is s)) * 1e3, 2)
                                                  for s in steps if s.max_q]}
+    kernel_timing = ("CUDA events around a graph of one kernel's launches for all layers, per-launch = elapsed / "
+                     "layers" if graph is not None else "CUDA events around every launch")
+    for r in rooflines.values():
+        r["timing"] = kernel_timing
     dominant = "decode" if (dec_ms >= pre_ms and n_dec) else "prefill"
 
     result = {

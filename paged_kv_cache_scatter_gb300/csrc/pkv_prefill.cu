@@ -12,28 +12,38 @@
 // pool, 128 at a time (8 blocks).
 //
 // Tiles are 128 keys: an M=128 N=128 QK^T product keeps the tensor core at
-// its full rate (N=64 runs it at about half). Tensor memory holds two S
-// buffers, two P buffers (FP16) and O. The softmax frees S buffer j%2 as soon
-// as it has read S_j, so S_{j+2} is computed while the softmax still works on
-// S_j and never waits for a P V product; P_j goes to P buffer j%2, which
-// P_{j-2} V_{j-2} (two softmax periods earlier) has finished reading, and
-// O += P_j V_j reads it from tensor memory (no shared-memory round trip).
+// its full rate (N=64 runs it at about half). Tensor memory holds three S
+// buffers and O (all 512 columns). The softmax reads S_j into registers and
+// writes P_j (FP16) over the first 64 columns of S_j's own buffer, where
+// O += P_j V_j reads it (no shared-memory round trip). S_{j+2} goes to the
+// buffer of P_{j-1}, so the only wait before it is for P_{j-1} V_{j-1}. S and
+// P V are issued by two warps of their own: each waits only for its own
+// operands, and while one waits the other's MMAs keep the tensor core's queue
+// filled (a single issuer stalls the tensor core at every wait; its queue
+// holds only a couple of MMAs).
 //
-// Warp roles (256 threads; up to 255 registers a thread, so that a softmax
-// thread keeps its row's 128 S values in registers):
-//   warps 0-2    TMA producers: K low 64 dims (lanes 0-7), K high (lanes
-//                0-7), V both halves (lanes 0-15); each lane copies one 2 KB
-//                box (one block's 16 rows of one 64-dim half) of every
-//                128-key tile into a 3-stage ring. Three issuing warps keep
-//                the copy engine's request rate off the critical path; they
-//                sleep between polls while they wait for a free slot.
-//   warp 3       MMA issuer (one elected lane; the warp owns the TMEM
-//                allocation): S_j = Q K_j^T (A and B from shared memory),
-//                O += P_j V_j (P from tensor memory); completion by
-//                tcgen05.commit. Order: S_0, S_1, then S_{j+2}, P_j V_j.
+// Warp roles (384 threads, three warpgroups; the producer and issuer
+// warpgroups hand registers to the softmax warpgroup with setmaxnreg, so that a
+// softmax thread keeps its row's 128 S values in registers):
+//   warps 0-3    TMA producers of K's 64-dim halves 0, 1 and V's halves 0, 1:
+//                lane b < 8 copies one 2 KB box (block b's 16 rows of the
+//                warp's half) of every 128-key tile into a 3-stage ring. A
+//                warp issues its TMA copies one after another, a few hundred
+//                cycles each, so a tile's 32 boxes need four issuing warps
+//                to arrive about as fast as the tensor core consumes them
+//                (one warp: ~2,400 cycles per 64 KB tile; four: ~1,150).
+//                They sleep between polls while they wait for a free slot.
+//   warp 8       S issuer (the warp runs the loop, one elected lane issues;
+//                the warp owns the TMEM allocation): S_j = Q K_j^T, A and B
+//                from shared memory, into S buffer j%3 once K_j has landed
+//                and P_{j-3} V_{j-3} has read that buffer; tcgen05.commit
+//                signals S_j done and K_j's ring slot free.
+//   warp 9       P V issuer: O += P_j V_j, P from tensor memory, once the
+//                softmax has written P_j and V_j has landed; commits signal
+//                the product done and V_j's ring slot free.
 //   warps 4-7    softmax: thread r owns query row r (TMEM lane r). Per tile it
-//                loads its 128 S values into registers (freeing the S
-//                buffer), takes the row max, and writes P =
+//                loads its 128 S values into registers, takes the row max,
+//                and writes P =
 //                2^(s*scale*log2e - m) by quarters while adding to the
 //                running sum. The running max m is only raised when the
 //                tile's max exceeds it by more than 8 (a factor 256, far
@@ -95,12 +105,17 @@ constexpr int kRows = 128;            // query rows per CTA (MMA M)
 constexpr int kKeys = 128;            // keys per tile (8 blocks)
 constexpr int kBlocksPerTile = kKeys / kBlockSize;
 constexpr int kStages = 3;            // K and V ring depth
-constexpr int kBufs = 2;              // S buffers and P buffers in tensor memory
-constexpr int kProducerWarps = 3;     // K low, K high, V
-constexpr int kMmaWarp = 3;           // also owns the TMEM allocation
+constexpr int kBufs = 3;              // S buffers in tensor memory (P_j overwrites S_j's)
+constexpr int kProducerWarps = 4;     // K low, K high, V low, V high
 constexpr int kFirstSoftmaxWarp = 4;
 constexpr int kSoftmaxThreads = 128;
-constexpr int kThreads = (kFirstSoftmaxWarp + 4) * 32;  // 256
+constexpr int kMmaWarp = 8;           // S issuer; also owns the TMEM allocation
+constexpr int kPvWarp = 9;            // P V issuer
+constexpr int kThreads = 384;         // warps 10, 11 only fill the third warpgroup
+constexpr int kLaunchRegs = 65536 / kThreads / 8 * 8;  // 168: what ptxas allows a thread at launch
+constexpr int kSideRegs = 64;         // producer and issuer warpgroups
+constexpr int kSoftmaxRegs = 200;     // softmax warpgroup
+static_assert(2 * 128 * kSideRegs + 128 * kSoftmaxRegs <= kThreads * kLaunchRegs, "register split");
 constexpr int kQBytes = kRows * kHeadDim * 2;        // 32 KB
 constexpr int kQSlab = kQBytes / 2;                  // 16 KB: 128 rows x 64 halves
 constexpr int kTileOpBytes = kKeys * kHeadDim * 2;   // 32 KB: one 128-key K or V tile
@@ -113,18 +128,18 @@ constexpr int kSmKRing = kQBytes;                             // [stage] K tiles
 constexpr int kSmVRing = kSmKRing + kStages * kTileOpBytes;   // [stage] V tiles
 constexpr int kSmBars = kSmVRing + kStages * kTileOpBytes;
 enum Bar {
-    K_FULL = 0,                   // count 2: the two K producers arm it
+    K_FULL = 0,                   // count 2: the K low and K high producers arm it
     V_FULL = K_FULL + kStages,
     K_EMPTY = V_FULL + kStages,
     V_EMPTY = K_EMPTY + kStages,
     S_FULL = V_EMPTY + kStages,   // [kBufs] per S buffer
-    S_FREE = S_FULL + kBufs,      // [kBufs] count kSoftmaxThreads: the softmax has read the S buffer
-    P_FULL = S_FREE + kBufs,      // [kBufs] count kSoftmaxThreads
+    P_FULL = S_FULL + kBufs,      // [kBufs] count kSoftmaxThreads: P written over the buffer's S
     PV_DONE = P_FULL + kBufs,     // [kBufs]
     V_FIXED = PV_DONE + kBufs,    // the last tile's V rows past the last position are zeroed
     Q_READY = V_FIXED + 1,        // count kSoftmaxThreads
-    MMA_DONE = Q_READY + 1,
-    NUM_BARS = MMA_DONE + 1
+    S_ALL_DONE = Q_READY + 1,     // every S MMA finished (before the CTA frees tensor memory)
+    PV_ALL_DONE = S_ALL_DONE + 1, // every P V MMA finished
+    NUM_BARS = PV_ALL_DONE + 1
 };
 constexpr int kSmTmemSlot = kSmBars + NUM_BARS * 8;
 constexpr int kSmAbort = kSmTmemSlot + 4;
@@ -132,14 +147,12 @@ constexpr int kSmBytes = kSmAbort + 12;
 constexpr int kSmAlloc = kSmBytes + 1024;  // slack to align the base
 static_assert(kSmAlloc <= 227 * 1024, "shared memory per CTA");
 
-// TMEM columns: S buffers 0, 1 (128 fp32 columns each), P buffers 0, 1
-// (64 columns each, FP16 two per column), O (128): all 512.
+// TMEM columns: S buffers 0, 1, 2 (128 fp32 columns each; P, FP16 two per
+// column, takes the first 64 of its S buffer), O (128): all 512.
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;
 constexpr uint32_t kSBufCols = 128;
-constexpr uint32_t kColP = kBufs * kSBufCols;
-constexpr uint32_t kPBufCols = 64;
-constexpr uint32_t kColO = kColP + kBufs * kPBufCols;
+constexpr uint32_t kColO = kBufs * kSBufCols;
 static_assert(kColO + 128 <= kTmemCols, "tensor memory columns");
 
 // Instruction descriptors, kind::f16: D = F32 (bit 4), A = B = F16,
@@ -180,17 +193,6 @@ __device__ __forceinline__ bool flag_wait(uint32_t bar, uint32_t parity, volatil
         *abort = 1;
     }
     return ok;
-}
-
-// Bounded wait of a single thread (the MMA issuer's lane runs its loop alone).
-__device__ __forceinline__ bool lane_wait(uint32_t bar, uint32_t parity, volatile int* abort, unsigned int* status)
-{
-    if (mbar_try_wait(bar, parity)) return true;
-    if (*abort) return false;
-    if (mbar_wait(bar, parity)) return true;
-    atomicOr(status, PKV_DEV_TIMEOUT);
-    *abort = 1;
-    return false;
 }
 
 // Bounded wait of a warp off the critical path (a producer waiting for a free ring slot): lane 0
@@ -294,19 +296,19 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) {
             mbar_init(bar(K_FULL + i), 2);
-            mbar_init(bar(V_FULL + i), 1);
+            mbar_init(bar(V_FULL + i), 2);
             mbar_init(bar(K_EMPTY + i), 1);
             mbar_init(bar(V_EMPTY + i), 1);
         }
         for (int i = 0; i < kBufs; ++i) {
             mbar_init(bar(S_FULL + i), 1);
-            mbar_init(bar(S_FREE + i), kSoftmaxThreads);
             mbar_init(bar(P_FULL + i), kSoftmaxThreads);
             mbar_init(bar(PV_DONE + i), 1);
         }
         mbar_init(bar(V_FIXED), 1);
         mbar_init(bar(Q_READY), kSoftmaxThreads);
-        mbar_init(bar(MMA_DONE), 1);
+        mbar_init(bar(S_ALL_DONE), 1);
+        mbar_init(bar(PV_ALL_DONE), 1);
         *abort = 0;
         fence_mbar_init();
     }
@@ -319,12 +321,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kSmTmemSlot);
 
+    // Each warpgroup sets its register budget at the top of its own branch (the same instruction in all
+    // four of its warps), so that ptxas allocates each role's code with that role's budget.
     if (warp < kProducerWarps) {
-        // ================================================= TMA producers: warps 0, 1 copy K's 64-dim half 0, 1
-        // (lane b < 8: block b of each tile), warp 2 copies V (lane < 16: block lane % 8, half lane / 8).
-        const int kv = warp == 2;
-        const int b = lane & (kBlocksPerTile - 1), half = kv ? lane / kBlocksPerTile : warp;
-        const bool copier = lane < (kv ? 2 : 1) * kBlocksPerTile;
+        regs_dec<kSideRegs>();
+        // ================================================= TMA producers: warp 0 copies K's 64-dim half 0,
+        // warp 1 K's half 1, warps 2, 3 V's halves (lane < 8: block lane of each tile).
+        const int kv = warp >> 1;
+        const int b = lane & (kBlocksPerTile - 1), half = warp & 1;
+        const bool copier = lane < kBlocksPerTile;
         const uint32_t ring = sb + (kv ? kSmVRing : kSmKRing) + half * kTileSlab;
         const uint32_t full0 = bar(kv ? V_FULL : K_FULL);
         const uint32_t empty0 = bar(kv ? V_EMPTY : K_EMPTY);
@@ -352,7 +357,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                     stop = true;
                     break;
                 }
-                if (lane == 0) mbar_arrive_expect_tx(full0 + 8 * st, nb * (kv ? kTileBytes : kTileBytes / 2));
+                if (lane == 0) mbar_arrive_expect_tx(full0 + 8 * st, nb * (kTileBytes / 2));
                 __syncwarp();
                 if (copier && b < nb)
                     tma_load_5d(ring + st * kTileOpBytes + b * 2048, &tmap, half * 64, 0, kv * a.num_heads + h / a.group,
@@ -362,7 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                 idq[u] = copier && i + kIdAhead < n && blk < nblk ? __ldg(trow + blk) : 0;
             }
         }
-        if (kv && !stop) {
+        if (warp == 2 && !stop) {
             // The last tile: keys past the last row's position may hold anything (even NaN), and rows of
             // blocks past the table's end were not copied at all. Zero those V rows (both halves, once they
             // have landed) so that P = 0 times V stays 0 in the tensor core, then release the tile.
@@ -383,53 +388,58 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         // copies still in flight (after an abort) must land before the CTA exits
         for (int i = (issued > kStages ? issued - kStages : 0); i < issued; ++i)
             mbar_wait(full0 + 8 * (i % kStages), (uint32_t)(i / kStages) & 1u);
-    } else if (warp == kMmaWarp) {
-        // ================================================= MMA issuer: lane 0 alone runs the loop, with
-        // single-thread waits (no warp vote between MMA groups, so the tensor pipe drains less between them).
-        // Order: S_0, S_1, then per tile j: S_{j+2} (once the softmax has read S_j), P_j V_j.
-        if (lane == 0) {
-            // base descriptors; each MMA adds a constant offset (one 64-bit add instead of building a descriptor)
-            const uint64_t dq = sw128_desc(sb + kSmQ, 16, 1024);
-            const uint64_t dk = sw128_desc(sb + kSmKRing, 16, 1024);
-            const uint64_t dv = sw128_desc(sb + kSmVRing, kTileSlab, 1024);
-            bool ok = true;
-            auto issue_s = [&](int j) {
-                const int ks = j % kStages, sbuf = j % kBufs;
-                ok = ok && (j > 0 || lane_wait(bar(Q_READY), 0, abort, a.status)) &&
-                     lane_wait(bar(K_FULL + ks), (uint32_t)(j / kStages) & 1u, abort, a.status) &&
-                     (j < kBufs ||
-                      lane_wait(bar(S_FREE + sbuf), (uint32_t)((j - kBufs) / kBufs) & 1u, abort, a.status));
-                if (!ok) return;
-                tc_fence_after();
+    } else if (warp >= kMmaWarp) {
+        regs_dec<kSideRegs>();
+        if (warp == kMmaWarp) {
+        // ================================================= S issuer: the whole warp runs the loop (warp-uniform
+        // waits and descriptors) and one elected lane issues each MMA and commit.
+        // base descriptors; each MMA adds a constant offset (one 64-bit add instead of building a descriptor)
+        const uint64_t dq = sw128_desc(sb + kSmQ, 16, 1024);
+        const uint64_t dk = sw128_desc(sb + kSmKRing, 16, 1024);
+        for (int j = 0; j < n; ++j) {
+            const int ks = j % kStages, sbuf = j % kBufs;
+            const bool ok = (j > 0 || flag_wait(bar(Q_READY), 0, abort, a.status)) &&
+                            flag_wait(bar(K_FULL + ks), (uint32_t)(j / kStages) & 1u, abort, a.status) &&
+                            // S buffer j%3 last held P_{j-3}, which P_{j-3} V_{j-3} must have read
+                            (j < kBufs ||
+                             flag_wait(bar(PV_DONE + sbuf), (uint32_t)((j - kBufs) / kBufs) & 1u, abort, a.status));
+            if (!ok) break;
+            tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    tc_mma_f16(tmem + kColS + sbuf * kSBufCols, desc_add(dq, (kk >> 2) * kQSlab + (kk & 3) * 32),
-                               desc_add(dk, ks * kTileOpBytes + (kk >> 2) * kTileSlab + (kk & 3) * 32), kIdescS, kk > 0);
-                tc_commit(bar(S_FULL + sbuf));
-                tc_commit(bar(K_EMPTY + ks));
-            };
-            for (int j = 0; j < kBufs && j < n; ++j) issue_s(j);
-            for (int j = 0; j < n && ok; ++j) {
-                if (j + kBufs < n) issue_s(j + kBufs);
-                const int vs = j % kStages, pbuf = j % kBufs;
-                ok = ok && lane_wait(bar(P_FULL + pbuf), (uint32_t)(j / kBufs) & 1u, abort, a.status) &&
-                     (j == n - 1 ? lane_wait(bar(V_FIXED), 0, abort, a.status)
-                                 : lane_wait(bar(V_FULL + vs), (uint32_t)(j / kStages) & 1u, abort, a.status));
-                if (!ok) break;
-                tc_fence_after();
-                const uint32_t pcol = tmem + kColP + pbuf * kPBufCols;
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    tc_mma_f16_ts(tmem + kColO, pcol + kk * 8, desc_add(dv, vs * kTileOpBytes + kk * 2048), kIdescPV,
-                                  (j > 0 || kk > 0) ? 1u : 0u);
-                tc_commit(bar(PV_DONE + pbuf));
-                tc_commit(bar(V_EMPTY + vs));
-            }
-            tc_commit(bar(MMA_DONE));
-            mbar_wait(bar(MMA_DONE), 0);
+            for (int kk = 0; kk < 8; ++kk)
+                tc_mma_f16_warp(tmem + kColS + sbuf * kSBufCols, desc_add(dq, (kk >> 2) * kQSlab + (kk & 3) * 32),
+                                desc_add(dk, ks * kTileOpBytes + (kk >> 2) * kTileSlab + (kk & 3) * 32), kIdescS, kk > 0);
+            tc_commit_warp(bar(S_FULL + sbuf));
+            tc_commit_warp(bar(K_EMPTY + ks));
         }
+        // every MMA this warp issued must have finished before the CTA frees its tensor memory and exits
+        tc_commit_warp(bar(S_ALL_DONE));
+        mbar_wait(bar(S_ALL_DONE), 0);
         __syncwarp();
+        } else if (warp == kPvWarp) {
+        // ================================================= P V issuer, in the same style
+        const uint64_t dv = sw128_desc(sb + kSmVRing, kTileSlab, 1024);
+        for (int j = 0; j < n; ++j) {
+            const int vs = j % kStages, pbuf = j % kBufs;
+            const bool ok = flag_wait(bar(P_FULL + pbuf), (uint32_t)(j / kBufs) & 1u, abort, a.status) &&
+                            (j == n - 1 ? flag_wait(bar(V_FIXED), 0, abort, a.status)
+                                        : flag_wait(bar(V_FULL + vs), (uint32_t)(j / kStages) & 1u, abort, a.status));
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t pcol = tmem + kColS + pbuf * kSBufCols;
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+                tc_mma_f16_ts_warp(tmem + kColO, pcol + kk * 8, desc_add(dv, vs * kTileOpBytes + kk * 2048), kIdescPV,
+                                   (j > 0 || kk > 0) ? 1u : 0u);
+            tc_commit_warp(bar(PV_DONE + pbuf));
+            tc_commit_warp(bar(V_EMPTY + vs));
+        }
+        tc_commit_warp(bar(PV_ALL_DONE));
+        mbar_wait(bar(PV_ALL_DONE), 0);
+        __syncwarp();
+        }
     } else {
+        regs_inc<kSoftmaxRegs>();
         // ================================================= softmax: thread = query row
         const int qtr = warp & 3;
         const int row = qtr * 32 + lane;
@@ -470,11 +480,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             tc_fence_after();
             const uint32_t ts = tl + kColS + sbuf * kSBufCols;
             const int key0 = j * kKeys;
-            // diagonal tile or padding row: keys past the row's position count as -inf
-            const bool diag = !valid || key0 + kKeys - 1 > p0;
-            const int nvis = valid ? pos - key0 + 1 : 0;
+            // diagonal tile: keys past the row's position count as -inf. Padding rows (past the chunk's last
+            // query) are left unmasked: their Q is zero, their O is never written and rows do not mix in the
+            // MMAs, so whatever they compute (even NaN from a key past the context) stays in them; masking
+            // them on every tile would slow their warps, and every tile waits for the slowest softmax warp.
+            const bool diag = valid && key0 + kKeys - 1 > p0;
+            const int nvis = pos - key0 + 1;
             // all of S_j in registers, in two halves: the first half's max is taken while the second
-            // half is still on its way from tensor memory; then the buffer is free for S_{j+2}
+            // half is still on its way from tensor memory
             uint32_t sr[kKeys];
             tc_ld64_issue(ts, sr);
             tc_wait_ld64(sr);
@@ -482,8 +495,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             if (diag) mask_tail<64>(sr, nvis);
             float mx = max64(sr);
             tc_wait_ld64(sr + 64);
-            tc_fence_before();
-            mbar_arrive(bar(S_FREE + sbuf));
             if (diag) mask_tail<64>(sr + 64, nvis - 64);
             const float m_tile = fmaxf(mx, max64(sr + 64)) * a.scale_log2;
             const bool raise = m_tile > m_used + kRescaleThreshold;  // false while the row has seen no key
@@ -509,13 +520,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             if (raise) m_used = m_tile;
             // rows that have seen no visible key keep p = 0 (exp2(-inf - -inf) would be NaN)
             const float m_sub = m_used == -INFINITY ? 0.f : m_used;
-            // P_j goes to P buffer j%2, free once P_{j-2} V_{j-2} is done
-            if (j >= kBufs &&
-                !flag_wait(bar(PV_DONE + sbuf), (uint32_t)((j - kBufs) / kBufs) & 1u, abort, a.status)) {
-                ok = false;
-                break;
-            }
-            const uint32_t tp = tl + kColP + sbuf * kPBufCols;
+            // P_j goes over the S_j just read (no MMA touches this buffer until P_j V_j)
+            const uint32_t tp = ts;
             // quarters of 32 keys: P of keys 32q.. goes to P columns 16q.., stored without waiting
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
