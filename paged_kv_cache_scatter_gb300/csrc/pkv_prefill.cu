@@ -27,7 +27,7 @@
 // softmax thread keeps its row's 128 S values in registers):
 //   warps 0-3    TMA producers of K's 64-dim halves 0, 1 and V's halves 0, 1:
 //                lane b < 8 copies one 2 KB box (block b's 16 rows of the
-//                warp's half) of every 128-key tile into a 3-stage ring. A
+//                warp's half) of every 128-key tile into its 3-stage ring. A
 //                warp issues its TMA copies one after another, a few hundred
 //                cycles each, so a tile's 32 boxes need four issuing warps
 //                to arrive about as fast as the tensor core consumes them
@@ -104,7 +104,8 @@ namespace {
 constexpr int kRows = 128;            // query rows per CTA (MMA M)
 constexpr int kKeys = 128;            // keys per tile (8 blocks)
 constexpr int kBlocksPerTile = kKeys / kBlockSize;
-constexpr int kStages = 3;            // K and V ring depth
+constexpr int kStagesK = 3;           // K ring depth (4 K + 2 V stages in the same space measured the same)
+constexpr int kStagesV = 3;           // V ring depth
 constexpr int kBufs = 3;              // S buffers in tensor memory (P_j overwrites S_j's)
 constexpr int kProducerWarps = 4;     // K low, K high, V low, V high
 constexpr int kFirstSoftmaxWarp = 4;
@@ -125,14 +126,14 @@ constexpr float kRescaleThreshold = 8.f;             // log2 of the largest un-r
 // shared-memory map (offsets from a 1,024-byte aligned base)
 constexpr int kSmQ = 0;
 constexpr int kSmKRing = kQBytes;                             // [stage] K tiles
-constexpr int kSmVRing = kSmKRing + kStages * kTileOpBytes;   // [stage] V tiles
-constexpr int kSmBars = kSmVRing + kStages * kTileOpBytes;
+constexpr int kSmVRing = kSmKRing + kStagesK * kTileOpBytes;  // [stage] V tiles
+constexpr int kSmBars = kSmVRing + kStagesV * kTileOpBytes;
 enum Bar {
     K_FULL = 0,                   // count 2: the K low and K high producers arm it
-    V_FULL = K_FULL + kStages,
-    K_EMPTY = V_FULL + kStages,
-    V_EMPTY = K_EMPTY + kStages,
-    S_FULL = V_EMPTY + kStages,   // [kBufs] per S buffer
+    V_FULL = K_FULL + kStagesK,
+    K_EMPTY = V_FULL + kStagesV,
+    V_EMPTY = K_EMPTY + kStagesK,
+    S_FULL = V_EMPTY + kStagesV,  // [kBufs] per S buffer
     P_FULL = S_FULL + kBufs,      // [kBufs] count kSoftmaxThreads: P written over the buffer's S
     PV_DONE = P_FULL + kBufs,     // [kBufs]
     V_FIXED = PV_DONE + kBufs,    // the last tile's V rows past the last position are zeroed
@@ -294,10 +295,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
     volatile int* abort = reinterpret_cast<volatile int*>(smem + kSmAbort);
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kStages; ++i) {
+        for (int i = 0; i < kStagesK; ++i) {
             mbar_init(bar(K_FULL + i), 2);
-            mbar_init(bar(V_FULL + i), 2);
             mbar_init(bar(K_EMPTY + i), 1);
+        }
+        for (int i = 0; i < kStagesV; ++i) {
+            mbar_init(bar(V_FULL + i), 2);
             mbar_init(bar(V_EMPTY + i), 1);
         }
         for (int i = 0; i < kBufs; ++i) {
@@ -343,6 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             const int blk = kBlocksPerTile * u + b;
             idq[u] = copier && u < n && blk < nblk ? __ldg(trow + blk) : 0;
         }
+        const int stages = kv ? kStagesV : kStagesK;
         int issued = 0;
         bool stop = false;
         for (int i0 = 0; i0 < n && !stop; i0 += kIdAhead) {
@@ -350,10 +354,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             for (int u = 0; u < kIdAhead; ++u) {
                 const int i = i0 + u;
                 if (i >= n) break;
-                const int st = i % kStages;
-                const uint32_t ph = (uint32_t)(i / kStages) & 1u;
+                const int st = i % stages;
+                const uint32_t ph = (uint32_t)(i / stages) & 1u;
                 const int nb = min(kBlocksPerTile, nblk - kBlocksPerTile * i);
-                if (i >= kStages && !lazy_wait(empty0 + 8 * st, ph ^ 1u, abort, a.status)) {
+                if (i >= stages && !lazy_wait(empty0 + 8 * st, ph ^ 1u, abort, a.status)) {
                     stop = true;
                     break;
                 }
@@ -371,8 +375,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             // The last tile: keys past the last row's position may hold anything (even NaN), and rows of
             // blocks past the table's end were not copied at all. Zero those V rows (both halves, once they
             // have landed) so that P = 0 times V stays 0 in the tensor core, then release the tile.
-            const int i = n - 1, st = i % kStages;
-            if (flag_wait(full0 + 8 * st, (uint32_t)(i / kStages) & 1u, abort, a.status)) {
+            const int i = n - 1, st = i % kStagesV;
+            if (flag_wait(full0 + 8 * st, (uint32_t)(i / kStagesV) & 1u, abort, a.status)) {
                 const uint32_t vt = sb + kSmVRing + st * kTileOpBytes;
                 const int first = pos_max + 1 - (n - 1) * kKeys;
                 for (int c = first * 8 + lane; c < kKeys * 8; c += 32) {
@@ -386,8 +390,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             }
         }
         // copies still in flight (after an abort) must land before the CTA exits
-        for (int i = (issued > kStages ? issued - kStages : 0); i < issued; ++i)
-            mbar_wait(full0 + 8 * (i % kStages), (uint32_t)(i / kStages) & 1u);
+        for (int i = (issued > stages ? issued - stages : 0); i < issued; ++i)
+            mbar_wait(full0 + 8 * (i % stages), (uint32_t)(i / stages) & 1u);
     } else if (warp >= kMmaWarp) {
         regs_dec<kSideRegs>();
         if (warp == kMmaWarp) {
@@ -397,9 +401,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         const uint64_t dq = sw128_desc(sb + kSmQ, 16, 1024);
         const uint64_t dk = sw128_desc(sb + kSmKRing, 16, 1024);
         for (int j = 0; j < n; ++j) {
-            const int ks = j % kStages, sbuf = j % kBufs;
+            const int ks = j % kStagesK, sbuf = j % kBufs;
             const bool ok = (j > 0 || flag_wait(bar(Q_READY), 0, abort, a.status)) &&
-                            flag_wait(bar(K_FULL + ks), (uint32_t)(j / kStages) & 1u, abort, a.status) &&
+                            flag_wait(bar(K_FULL + ks), (uint32_t)(j / kStagesK) & 1u, abort, a.status) &&
                             // S buffer j%3 last held P_{j-3}, which P_{j-3} V_{j-3} must have read
                             (j < kBufs ||
                              flag_wait(bar(PV_DONE + sbuf), (uint32_t)((j - kBufs) / kBufs) & 1u, abort, a.status));
@@ -420,10 +424,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         // ================================================= P V issuer, in the same style
         const uint64_t dv = sw128_desc(sb + kSmVRing, kTileSlab, 1024);
         for (int j = 0; j < n; ++j) {
-            const int vs = j % kStages, pbuf = j % kBufs;
+            const int vs = j % kStagesV, pbuf = j % kBufs;
             const bool ok = flag_wait(bar(P_FULL + pbuf), (uint32_t)(j / kBufs) & 1u, abort, a.status) &&
                             (j == n - 1 ? flag_wait(bar(V_FIXED), 0, abort, a.status)
-                                        : flag_wait(bar(V_FULL + vs), (uint32_t)(j / kStages) & 1u, abort, a.status));
+                                        : flag_wait(bar(V_FULL + vs), (uint32_t)(j / kStagesV) & 1u, abort, a.status));
             if (!ok) break;
             tc_fence_after();
             const uint32_t pcol = tmem + kColS + pbuf * kSBufCols;
