@@ -58,8 +58,11 @@ typedef enum pkv_status {
  * single precision; attention reads code * scale. kv_append quantises,
  * decode attention dequantises in its loaders (tensor cores: codes become
  * FP16 exactly, the K scale multiplies the scores, the V scale folds into the
- * softmax weights, which are rounded to FP16). Prefill attention over an INT8
- * pool is not built (PKV_E_INVALID). */
+ * softmax weights, which are rounded to FP16). Prefill attention dequantises
+ * in its loaders too: each 128-key tile's codes and scales arrive by TMA and
+ * become FP16 code * scale in shared memory (the scale applied as an FP16
+ * pair hi + lo, so the product's rounding to FP16 is the only one) before the
+ * tensor cores read them. */
 enum { PKV_DTYPE_FP16 = 0, PKV_DTYPE_INT8 = 1 };
 
 /* Bits of the sticky device error word (pkv_get_status). */

@@ -784,8 +784,8 @@ pkv_status pkv_prefill_attn(pkv_pool* pool, int32_t layer, const void* q, const 
     if (num_seqs > 65535) return fail(PKV_E_INVALID, "num_seqs above 65,535");
     if (!q || !q_start_loc || !block_tables || !ctx_lens || !out) return fail(PKV_E_INVALID, "NULL argument");
     if (!aligned(q, 16) || !aligned(out, 16)) return fail(PKV_E_INVALID, "q/out must be 16-byte aligned");
-    if (pool->geom.dtype == PKV_DTYPE_INT8) return fail(PKV_E_INVALID, "prefill over an INT8 pool is not built");
-    if (!pool->kv_tmap_ok) return fail(PKV_E_DEVICE, "TMA descriptor for the pool could not be encoded");
+    if (!(pool->geom.dtype == PKV_DTYPE_INT8 ? pool->tile_tmap_ok : pool->kv_tmap_ok))
+        return fail(PKV_E_DEVICE, "TMA descriptor for the pool could not be encoded");
     DeviceGuard dg(pool->device);
     if (!dg.ok) return fail(PKV_E_DEVICE, "cannot select the pool's device");
     cudaError_t e = pkv::launch_prefill(pool, layer, q, q_start_loc, block_tables, max_blocks, ctx_lens, num_seqs,
@@ -817,8 +817,6 @@ pkv_status pkv_step(pkv_pool* pool, const pkv_step_desc* st, void* workspace, si
     if (!st->block_tables || !st->ctx_lens || !st->slot_mapping || !st->q || !st->k || !st->v || !st->out)
         return fail(PKV_E_INVALID, "NULL step array");
     if (P > 0 && !st->q_start_loc) return fail(PKV_E_INVALID, "prefill rows need q_start_loc");
-    if (P > 0 && pool->geom.dtype == PKV_DTYPE_INT8)
-        return fail(PKV_E_INVALID, "prefill over an INT8 pool is not built");
     if (st->q_layer_stride % 8 || st->k_layer_stride % 8 || st->v_layer_stride % 8 || st->out_layer_stride % 8)
         return fail(PKV_E_INVALID, "layer strides must be multiples of 8 elements");
     const int64_t tok = (int64_t)pool->desc.num_heads * pkv::kHeadDim * 2;  // bytes of one token's k or v row

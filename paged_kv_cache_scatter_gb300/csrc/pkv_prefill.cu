@@ -104,49 +104,65 @@ namespace {
 constexpr int kRows = 128;            // query rows per CTA (MMA M)
 constexpr int kKeys = 128;            // keys per tile (8 blocks)
 constexpr int kBlocksPerTile = kKeys / kBlockSize;
-constexpr int kStagesK = 3;           // K ring depth (4 K + 2 V stages in the same space measured the same)
-constexpr int kStagesV = 3;           // V ring depth
 constexpr int kBufs = 3;              // S buffers in tensor memory (P_j overwrites S_j's)
-constexpr int kProducerWarps = 4;     // K low, K high, V low, V high
+constexpr int kProducerWarps = 4;
 constexpr int kFirstSoftmaxWarp = 4;
 constexpr int kSoftmaxThreads = 128;
 constexpr int kMmaWarp = 8;           // S issuer; also owns the TMEM allocation
 constexpr int kPvWarp = 9;            // P V issuer
-constexpr int kThreads = 384;         // warps 10, 11 only fill the third warpgroup
-constexpr int kLaunchRegs = 65536 / kThreads / 8 * 8;  // 168: what ptxas allows a thread at launch
-constexpr int kSideRegs = 64;         // producer and issuer warpgroups
-constexpr int kSoftmaxRegs = 200;     // softmax warpgroup
-static_assert(2 * 128 * kSideRegs + 128 * kSoftmaxRegs <= kThreads * kLaunchRegs, "register split");
+constexpr int kFirstConvWarp = 12;    // 8-bit pools: warps 12-15 turn codes into FP16 operand tiles
 constexpr int kQBytes = kRows * kHeadDim * 2;        // 32 KB
 constexpr int kQSlab = kQBytes / 2;                  // 16 KB: 128 rows x 64 halves
 constexpr int kTileOpBytes = kKeys * kHeadDim * 2;   // 32 KB: one 128-key K or V tile
 constexpr int kTileSlab = kTileOpBytes / 2;          // 16 KB: 128 rows x 64 halves
+constexpr int kScaleStage = 2 * kKeys * 4;           // 8-bit pools: a tile's 128 K then 128 V row scales (FP32)
+constexpr int kScaleStages = 6;                      // 8-bit pools: scale ring depth (held until the softmax is done)
+constexpr int kCodesBytes = kBlockSize * kHeadDim;   // 8-bit pools: one (block, layer, K|V, head) tile's codes
 constexpr float kRescaleThreshold = 8.f;             // log2 of the largest un-rescaled P (256)
 
-// shared-memory map (offsets from a 1,024-byte aligned base)
-constexpr int kSmQ = 0;
-constexpr int kSmKRing = kQBytes;                             // [stage] K tiles
-constexpr int kSmVRing = kSmKRing + kStagesK * kTileOpBytes;  // [stage] V tiles
-constexpr int kSmBars = kSmVRing + kStagesV * kTileOpBytes;
-enum Bar {
-    K_FULL = 0,                   // count 2: the K low and K high producers arm it
-    V_FULL = K_FULL + kStagesK,
-    K_EMPTY = V_FULL + kStagesV,
-    V_EMPTY = K_EMPTY + kStagesK,
-    S_FULL = V_EMPTY + kStagesV,  // [kBufs] per S buffer
-    P_FULL = S_FULL + kBufs,      // [kBufs] count kSoftmaxThreads: P written over the buffer's S
-    PV_DONE = P_FULL + kBufs,     // [kBufs]
-    V_FIXED = PV_DONE + kBufs,    // the last tile's V rows past the last position are zeroed
-    Q_READY = V_FIXED + 1,        // count kSoftmaxThreads
-    S_ALL_DONE = Q_READY + 1,     // every S MMA finished (before the CTA frees tensor memory)
-    PV_ALL_DONE = S_ALL_DONE + 1, // every P V MMA finished
-    NUM_BARS = PV_ALL_DONE + 1
+// Per pool element type: ring depths, threads, register split and the shared-memory map.
+// FP16 pools: 12 warps (producers, softmax, issuers + 2 idle). 8-bit pools: a fourth warpgroup
+// converts codes, the V ring has 2 stages, and the row scales have a ring of their own.
+template <bool kI8>
+struct Cfg {
+    static constexpr int kStagesK = 3;           // K ring depth (4 K + 2 V stages in the same space measured the same)
+    static constexpr int kStagesV = kI8 ? 2 : 3; // V ring depth
+    static constexpr int kThreads = kI8 ? 512 : 384;
+    static constexpr int kLaunchRegs = 65536 / kThreads / 8 * 8;  // what ptxas allows a thread at launch
+    static constexpr int kSideRegs = kI8 ? 56 : 64;               // producer and issuer warpgroups
+    static constexpr int kConvRegs = 96;                          // converter warpgroup (8-bit pools)
+    static constexpr int kSoftmaxRegs = 200;                      // softmax warpgroup
+    static_assert(2 * 128 * kSideRegs + 128 * kSoftmaxRegs + (kI8 ? 128 * kConvRegs : 0) <= kThreads * kLaunchRegs,
+                  "register split");
+    // shared-memory map (offsets from a 1,024-byte aligned base)
+    static constexpr int kSmQ = 0;
+    static constexpr int kSmKRing = kQBytes;                             // [stage] K tiles
+    static constexpr int kSmVRing = kSmKRing + kStagesK * kTileOpBytes;  // [stage] V tiles
+    static constexpr int kSmScales = kSmVRing + kStagesV * kTileOpBytes; // 8-bit: [stage][K 128, V 128] f32
+    static constexpr int kSmBars = kSmScales + (kI8 ? kScaleStages * kScaleStage : 0);
+    // barriers
+    static constexpr int K_FULL = 0;                     // count 2 (FP16: two half-tile producers) or 1 (8-bit codes)
+    static constexpr int V_FULL = K_FULL + kStagesK;
+    static constexpr int K_EMPTY = V_FULL + kStagesV;
+    static constexpr int V_EMPTY = K_EMPTY + kStagesK;
+    static constexpr int K_CONV = V_EMPTY + kStagesV;    // 8-bit: count 4, the converter warps
+    static constexpr int V_CONV = K_CONV + kStagesK;
+    static constexpr int SC_FULL = V_CONV + kStagesV;    // 8-bit: [kScaleStages] count 2, the two scale producers
+    static constexpr int SC_FREE = SC_FULL + kScaleStages;  // 8-bit: [kScaleStages] count 4, the softmax warps
+    static constexpr int S_FULL = SC_FREE + kScaleStages;   // [kBufs] per S buffer
+    static constexpr int P_FULL = S_FULL + kBufs;        // [kBufs] count kSoftmaxThreads: P written over the buffer's S
+    static constexpr int PV_DONE = P_FULL + kBufs;       // [kBufs]
+    static constexpr int V_FIXED = PV_DONE + kBufs;      // FP16: the last tile's V rows past the last position zeroed
+    static constexpr int Q_READY = V_FIXED + 1;          // count kSoftmaxThreads
+    static constexpr int S_ALL_DONE = Q_READY + 1;       // every S MMA finished (before the CTA frees tensor memory)
+    static constexpr int PV_ALL_DONE = S_ALL_DONE + 1;   // every P V MMA finished
+    static constexpr int NUM_BARS = PV_ALL_DONE + 1;
+    static constexpr int kSmTmemSlot = kSmBars + NUM_BARS * 8;
+    static constexpr int kSmAbort = kSmTmemSlot + 4;
+    static constexpr int kSmBytes = kSmAbort + 12;
+    static constexpr int kSmAlloc = kSmBytes + 1024;  // slack to align the base
+    static_assert(kSmAlloc <= 227 * 1024, "shared memory per CTA");
 };
-constexpr int kSmTmemSlot = kSmBars + NUM_BARS * 8;
-constexpr int kSmAbort = kSmTmemSlot + 4;
-constexpr int kSmBytes = kSmAbort + 12;
-constexpr int kSmAlloc = kSmBytes + 1024;  // slack to align the base
-static_assert(kSmAlloc <= 227 * 1024, "shared memory per CTA");
 
 // TMEM columns: S buffers 0, 1, 2 (128 fp32 columns each; P, FP16 two per
 // column, takes the first 64 of its S buffer), O (128): all 512.
@@ -168,6 +184,10 @@ struct PrefillArgs {
     const int32_t* q_start;  // [S + 1]
     const int32_t* tables;   // [S][max_blocks]
     const int32_t* ctx_lens; // [S]
+    const char* base;        // 8-bit pools: the pool, for the row scales of a tile
+    int64_t block_bytes;
+    int64_t layer_bytes;
+    int64_t tile_bytes;
     int max_blocks;
     int num_heads;     // K/V heads of the pool
     int num_q_heads;   // query heads: q and out rows are [num_q_heads][128]
@@ -256,9 +276,104 @@ __device__ __forceinline__ void softmax_quarter(uint32_t* s, float scale_log2, f
     l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
 }
 
-__global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ CUtensorMap tmap,
-                                                               const PrefillArgs a)
+// 8-bit pools: one key row r of a 128-key operand tile. Its 128 codes sit in the tile's second slab, row r,
+// 16-byte chunks in 128-byte swizzle (dims 16c..16c+15 in chunk c ^ (r % 8)); the row becomes the codes as
+// FP16 (exact: |code| <= 127) in both slabs (dims 0-63, 64-127), in the same swizzle, in place: this thread
+// alone reads or writes row r, and it reads every chunk first. A code c becomes FP16 c via the byte
+// pattern 0x64XX = 1024 + XX with XX = c + 128, less 1152. The row scales are applied by the softmax
+// (K's to the scores, V's to the weights P), so no value is rounded here. Rows past the last query
+// position (or of blocks not copied) become zeros: keys there may hold anything.
+__device__ __forceinline__ void convert_code_row(uint32_t tile, int r, bool valid)
 {
+    const uint32_t s0 = tile + r * 128, s1 = tile + kTileSlab + r * 128;
+    const uint32_t sw = (uint32_t)(r & 7);
+    if (!valid) {
+        const uint4 z = make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            st_shared_v4(s0 + (c << 4), z);
+            st_shared_v4(s1 + (c << 4), z);
+        }
+        return;
+    }
+    uint4 cw[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) cw[c] = ld_shared_v4(s1 + (((uint32_t)c ^ sw) << 4));
+    const __half2 bias = __float2half2_rn(1152.f);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        const uint32_t w[4] = {cw[c].x, cw[c].y, cw[c].z, cw[c].w};
+        uint32_t o[8];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const uint32_t u = w[k] ^ 0x80808080u;
+#pragma unroll
+            for (int hlf = 0; hlf < 2; ++hlf) {
+                const uint32_t bits = __byte_perm(u, 0x64646464u, hlf ? 0x4342u : 0x4140u);
+                const __half2 x = __hsub2(*reinterpret_cast<const __half2*>(&bits), bias);
+                o[2 * k + hlf] = *reinterpret_cast<const uint32_t*>(&x);
+            }
+        }
+        const uint32_t dst = (c >> 2) ? s1 : s0;
+        const uint32_t ch = (uint32_t)(2 * (c & 3));
+        st_shared_v4(dst + ((ch ^ sw) << 4), make_uint4(o[0], o[1], o[2], o[3]));
+        st_shared_v4(dst + (((ch + 1) ^ sw) << 4), make_uint4(o[4], o[5], o[6], o[7]));
+    }
+}
+
+// 8-bit pools: N scores times their keys' row scales (FP32, from shared memory, the same for every row).
+template <int N>
+__device__ __forceinline__ void scale_columns(uint32_t* s, uint32_t scales)
+{
+#pragma unroll
+    for (int e = 0; e < N; e += 4) {
+        const uint4 k4 = ld_shared_v4(scales + e * 4);
+        s[e] = __float_as_uint(__uint_as_float(s[e]) * __uint_as_float(k4.x));
+        s[e + 1] = __float_as_uint(__uint_as_float(s[e + 1]) * __uint_as_float(k4.y));
+        s[e + 2] = __float_as_uint(__uint_as_float(s[e + 2]) * __uint_as_float(k4.z));
+        s[e + 3] = __float_as_uint(__uint_as_float(s[e + 3]) * __uint_as_float(k4.w));
+    }
+}
+
+// 8-bit pools: softmax_quarter with each weight times its key's V row scale before the rounding to FP16
+// (O accumulates P' codes_V = P V); the running sum takes the unscaled weights. kTail (the last tile): keys
+// e >= nkeys lie past the last query position, where the scale bytes may be anything (NaN, inf); their
+// weights are 0 and take scale 0, so that 0 times such a scale never reaches the P V product.
+template <bool kTail>
+__device__ __forceinline__ void softmax_quarter_vscaled(uint32_t* s, float scale_log2, float m_sub, float& l,
+                                                        uint32_t vscales, int nkeys)
+{
+    float ls[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) ls[u] = 0.f;
+#pragma unroll
+    for (int e = 0; e < 32; e += 4) {
+        const uint4 v4 = ld_shared_v4(vscales + e * 4);
+        float vs[4] = {__uint_as_float(v4.x), __uint_as_float(v4.y), __uint_as_float(v4.z), __uint_as_float(v4.w)};
+        if (kTail) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) vs[u] = e + u < nkeys ? vs[u] : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; u += 2) {
+            const float pa = ex2(fmaf(__uint_as_float(s[e + u]), scale_log2, -m_sub));
+            const float pb = ex2(fmaf(__uint_as_float(s[e + u + 1]), scale_log2, -m_sub));
+            ls[u] += pa;
+            ls[u + 1] += pb;
+            const __half2 hp = __floats2half2_rn(pa * vs[u], pb * vs[u + 1]);
+            s[(e + u) >> 1] = *reinterpret_cast<const uint32_t*>(&hp);
+        }
+    }
+    l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+}
+
+// tmap: FP16 pools, 2 KB boxes of one block's 16 rows of one 64-dim half; 8-bit pools, a 2 KB box of one
+// tile's codes (16 rows of 128).
+template <bool kI8>
+__global__ void __launch_bounds__(Cfg<kI8>::kThreads, 1) prefill_kernel(const __grid_constant__ CUtensorMap tmap,
+                                                                         const PrefillArgs a)
+{
+    using C = Cfg<kI8>;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     const uint32_t sb = smem_u32(smem);
@@ -282,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     const int nblk = pos_max / kBlockSize + 1;
     const int32_t* trow = a.tables + (int64_t)s * a.max_blocks;
     bool bad = false;
-    for (int b = threadIdx.x; b < nblk; b += kThreads) {
+    for (int b = threadIdx.x; b < nblk; b += C::kThreads) {
         const int id = __ldg(trow + b);
         bad |= id < 0 || (int64_t)id >= a.num_blocks;
     }
@@ -291,51 +406,63 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         return;
     }
 
-    const uint32_t bars = sb + kSmBars;
+    const uint32_t bars = sb + C::kSmBars;
     auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
-    volatile int* abort = reinterpret_cast<volatile int*>(smem + kSmAbort);
+    volatile int* abort = reinterpret_cast<volatile int*>(smem + C::kSmAbort);
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kStagesK; ++i) {
-            mbar_init(bar(K_FULL + i), 2);
-            mbar_init(bar(K_EMPTY + i), 1);
+        for (int i = 0; i < C::kStagesK; ++i) {
+            mbar_init(bar(C::K_FULL + i), kI8 ? 1 : 2);
+            mbar_init(bar(C::K_EMPTY + i), 1);
+            mbar_init(bar(C::K_CONV + i), 4);
         }
-        for (int i = 0; i < kStagesV; ++i) {
-            mbar_init(bar(V_FULL + i), 2);
-            mbar_init(bar(V_EMPTY + i), 1);
+        for (int i = 0; i < C::kStagesV; ++i) {
+            mbar_init(bar(C::V_FULL + i), kI8 ? 1 : 2);
+            mbar_init(bar(C::V_EMPTY + i), 1);
+            mbar_init(bar(C::V_CONV + i), 4);
+        }
+        for (int i = 0; i < kScaleStages; ++i) {
+            mbar_init(bar(C::SC_FULL + i), 2);
+            mbar_init(bar(C::SC_FREE + i), 4);
         }
         for (int i = 0; i < kBufs; ++i) {
-            mbar_init(bar(S_FULL + i), 1);
-            mbar_init(bar(P_FULL + i), kSoftmaxThreads);
-            mbar_init(bar(PV_DONE + i), 1);
+            mbar_init(bar(C::S_FULL + i), 1);
+            mbar_init(bar(C::P_FULL + i), kSoftmaxThreads);
+            mbar_init(bar(C::PV_DONE + i), 1);
         }
-        mbar_init(bar(V_FIXED), 1);
-        mbar_init(bar(Q_READY), kSoftmaxThreads);
-        mbar_init(bar(S_ALL_DONE), 1);
-        mbar_init(bar(PV_ALL_DONE), 1);
+        mbar_init(bar(C::V_FIXED), 1);
+        mbar_init(bar(C::Q_READY), kSoftmaxThreads);
+        mbar_init(bar(C::S_ALL_DONE), 1);
+        mbar_init(bar(C::PV_ALL_DONE), 1);
         *abort = 0;
         fence_mbar_init();
     }
     if (warp == kMmaWarp) {
-        tmem_alloc(sb + kSmTmemSlot, kTmemCols);
+        tmem_alloc(sb + C::kSmTmemSlot, kTmemCols);
         tmem_relinquish();
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kSmTmemSlot);
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + C::kSmTmemSlot);
 
     // Each warpgroup sets its register budget at the top of its own branch (the same instruction in all
     // four of its warps), so that ptxas allocates each role's code with that role's budget.
     if (warp < kProducerWarps) {
-        regs_dec<kSideRegs>();
-        // ================================================= TMA producers: warp 0 copies K's 64-dim half 0,
-        // warp 1 K's half 1, warps 2, 3 V's halves (lane < 8: block lane of each tile).
+        regs_dec<C::kSideRegs>();
+        // ================================================= TMA producers (lane < 8: block lane of each tile).
+        // FP16: warp 0 copies K's 64-dim half 0, warp 1 K's half 1, warps 2, 3 V's halves.
+        // 8-bit: warps 0, 2 K's and V's codes (into the tile's second slab); warps 1, 3 K's and V's row
+        // scales into the scale ring, whose stages the softmax releases once it is done with the tile.
         const int kv = warp >> 1;
         const int b = lane & (kBlocksPerTile - 1), half = warp & 1;
         const bool copier = lane < kBlocksPerTile;
-        const uint32_t ring = sb + (kv ? kSmVRing : kSmKRing) + half * kTileSlab;
-        const uint32_t full0 = bar(kv ? V_FULL : K_FULL);
-        const uint32_t empty0 = bar(kv ? V_EMPTY : K_EMPTY);
+        const bool scales = kI8 && half;
+        const int kvh = kv * a.num_heads + h / a.group;
+        const uint32_t ring = sb + (kv ? C::kSmVRing : C::kSmKRing) + ((kI8 || half) ? kTileSlab : 0);
+        const uint32_t scale_ring = sb + C::kSmScales + kv * kKeys * 4;
+        const uint32_t full0 = bar(scales ? C::SC_FULL : kv ? C::V_FULL : C::K_FULL);
+        const uint32_t empty0 = bar(scales ? C::SC_FREE : kv ? C::V_EMPTY : C::K_EMPTY);
+        const uint32_t box_bytes = kI8 ? (half ? 4 * kBlockSize : kCodesBytes) : kTileBytes / 2;
         if (lane == 0) prefetch_tmap(&tmap);
         // Block ids of tile i come from a register queue filled kIdAhead tiles in advance, so that
         // the table reads' latency never sits between two tiles' copies.
@@ -346,7 +473,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             const int blk = kBlocksPerTile * u + b;
             idq[u] = copier && u < n && blk < nblk ? __ldg(trow + blk) : 0;
         }
-        const int stages = kv ? kStagesV : kStagesK;
+        const int stages = scales ? kScaleStages : kv ? C::kStagesV : C::kStagesK;
         int issued = 0;
         bool stop = false;
         for (int i0 = 0; i0 < n && !stop; i0 += kIdAhead) {
@@ -361,23 +488,33 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                     stop = true;
                     break;
                 }
-                if (lane == 0) mbar_arrive_expect_tx(full0 + 8 * st, nb * (kTileBytes / 2));
+                if (lane == 0) mbar_arrive_expect_tx(full0 + 8 * st, nb * box_bytes);
                 __syncwarp();
-                if (copier && b < nb)
-                    tma_load_5d(ring + st * kTileOpBytes + b * 2048, &tmap, half * 64, 0, kv * a.num_heads + h / a.group,
-                                a.layer, idq[u], full0 + 8 * st);
+                if (copier && b < nb) {
+                    if (!kI8)
+                        tma_load_5d(ring + st * kTileOpBytes + b * 2048, &tmap, half * 64, 0, kvh, a.layer, idq[u],
+                                    full0 + 8 * st);
+                    else if (!half)
+                        tma_load_5d(ring + st * kTileOpBytes + b * kCodesBytes, &tmap, 0, 0, kvh, a.layer, idq[u],
+                                    full0 + 8 * st);
+                    else
+                        bulk_g2s(scale_ring + st * kScaleStage + b * 4 * kBlockSize,
+                                 a.base + (int64_t)idq[u] * a.block_bytes + (int64_t)a.layer * a.layer_bytes +
+                                     (int64_t)kvh * a.tile_bytes + kCodesBytes,
+                                 4 * kBlockSize, full0 + 8 * st);
+                }
                 issued = i + 1;
                 const int blk = kBlocksPerTile * (i + kIdAhead) + b;  // refill this slot with tile i + kIdAhead
                 idq[u] = copier && i + kIdAhead < n && blk < nblk ? __ldg(trow + blk) : 0;
             }
         }
-        if (warp == 2 && !stop) {
+        if (!kI8 && warp == 2 && !stop) {
             // The last tile: keys past the last row's position may hold anything (even NaN), and rows of
             // blocks past the table's end were not copied at all. Zero those V rows (both halves, once they
             // have landed) so that P = 0 times V stays 0 in the tensor core, then release the tile.
-            const int i = n - 1, st = i % kStagesV;
-            if (flag_wait(full0 + 8 * st, (uint32_t)(i / kStagesV) & 1u, abort, a.status)) {
-                const uint32_t vt = sb + kSmVRing + st * kTileOpBytes;
+            const int i = n - 1, st = i % C::kStagesV;
+            if (flag_wait(full0 + 8 * st, (uint32_t)(i / C::kStagesV) & 1u, abort, a.status)) {
+                const uint32_t vt = sb + C::kSmVRing + st * kTileOpBytes;
                 const int first = pos_max + 1 - (n - 1) * kKeys;
                 for (int c = first * 8 + lane; c < kKeys * 8; c += 32) {
                     const int r = c >> 3, ch = c & 7;
@@ -386,48 +523,53 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar(V_FIXED));
+                if (lane == 0) mbar_arrive(bar(C::V_FIXED));
             }
         }
         // copies still in flight (after an abort) must land before the CTA exits
         for (int i = (issued > stages ? issued - stages : 0); i < issued; ++i)
             mbar_wait(full0 + 8 * (i % stages), (uint32_t)(i / stages) & 1u);
-    } else if (warp >= kMmaWarp) {
-        regs_dec<kSideRegs>();
+    } else if (warp >= kMmaWarp && warp < kMmaWarp + 4) {
+        regs_dec<C::kSideRegs>();
         if (warp == kMmaWarp) {
         // ================================================= S issuer: the whole warp runs the loop (warp-uniform
         // waits and descriptors) and one elected lane issues each MMA and commit.
         // base descriptors; each MMA adds a constant offset (one 64-bit add instead of building a descriptor)
-        const uint64_t dq = sw128_desc(sb + kSmQ, 16, 1024);
-        const uint64_t dk = sw128_desc(sb + kSmKRing, 16, 1024);
+        const uint64_t dq = sw128_desc(sb + C::kSmQ, 16, 1024);
+        const uint64_t dk = sw128_desc(sb + C::kSmKRing, 16, 1024);
         for (int j = 0; j < n; ++j) {
-            const int ks = j % kStagesK, sbuf = j % kBufs;
-            const bool ok = (j > 0 || flag_wait(bar(Q_READY), 0, abort, a.status)) &&
-                            flag_wait(bar(K_FULL + ks), (uint32_t)(j / kStagesK) & 1u, abort, a.status) &&
+            const int ks = j % C::kStagesK, sbuf = j % kBufs;
+            // K_j landed (FP16) or converted (8-bit)
+            const bool ok = (j > 0 || flag_wait(bar(C::Q_READY), 0, abort, a.status)) &&
+                            flag_wait(bar((kI8 ? C::K_CONV : C::K_FULL) + ks), (uint32_t)(j / C::kStagesK) & 1u, abort,
+                                      a.status) &&
                             // S buffer j%3 last held P_{j-3}, which P_{j-3} V_{j-3} must have read
-                            (j < kBufs ||
-                             flag_wait(bar(PV_DONE + sbuf), (uint32_t)((j - kBufs) / kBufs) & 1u, abort, a.status));
+                            (j < kBufs || flag_wait(bar(C::PV_DONE + sbuf), (uint32_t)((j - kBufs) / kBufs) & 1u, abort,
+                                                    a.status));
             if (!ok) break;
             tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
                 tc_mma_f16_warp(tmem + kColS + sbuf * kSBufCols, desc_add(dq, (kk >> 2) * kQSlab + (kk & 3) * 32),
                                 desc_add(dk, ks * kTileOpBytes + (kk >> 2) * kTileSlab + (kk & 3) * 32), kIdescS, kk > 0);
-            tc_commit_warp(bar(S_FULL + sbuf));
-            tc_commit_warp(bar(K_EMPTY + ks));
+            tc_commit_warp(bar(C::S_FULL + sbuf));
+            tc_commit_warp(bar(C::K_EMPTY + ks));
         }
         // every MMA this warp issued must have finished before the CTA frees its tensor memory and exits
-        tc_commit_warp(bar(S_ALL_DONE));
-        mbar_wait(bar(S_ALL_DONE), 0);
+        tc_commit_warp(bar(C::S_ALL_DONE));
+        mbar_wait(bar(C::S_ALL_DONE), 0);
         __syncwarp();
         } else if (warp == kPvWarp) {
         // ================================================= P V issuer, in the same style
-        const uint64_t dv = sw128_desc(sb + kSmVRing, kTileSlab, 1024);
+        const uint64_t dv = sw128_desc(sb + C::kSmVRing, kTileSlab, 1024);
         for (int j = 0; j < n; ++j) {
-            const int vs = j % kStagesV, pbuf = j % kBufs;
-            const bool ok = flag_wait(bar(P_FULL + pbuf), (uint32_t)(j / kBufs) & 1u, abort, a.status) &&
-                            (j == n - 1 ? flag_wait(bar(V_FIXED), 0, abort, a.status)
-                                        : flag_wait(bar(V_FULL + vs), (uint32_t)(j / kStagesV) & 1u, abort, a.status));
+            const int vs = j % C::kStagesV, pbuf = j % kBufs;
+            // V_j converted (8-bit), landed (FP16), or for the last FP16 tile: landed and its tail zeroed
+            const bool ok =
+                flag_wait(bar(C::P_FULL + pbuf), (uint32_t)(j / kBufs) & 1u, abort, a.status) &&
+                (kI8 ? flag_wait(bar(C::V_CONV + vs), (uint32_t)(j / C::kStagesV) & 1u, abort, a.status)
+                     : j == n - 1 ? flag_wait(bar(C::V_FIXED), 0, abort, a.status)
+                                  : flag_wait(bar(C::V_FULL + vs), (uint32_t)(j / C::kStagesV) & 1u, abort, a.status));
             if (!ok) break;
             tc_fence_after();
             const uint32_t pcol = tmem + kColS + pbuf * kSBufCols;
@@ -435,15 +577,37 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             for (int kk = 0; kk < 8; ++kk)
                 tc_mma_f16_ts_warp(tmem + kColO, pcol + kk * 8, desc_add(dv, vs * kTileOpBytes + kk * 2048), kIdescPV,
                                    (j > 0 || kk > 0) ? 1u : 0u);
-            tc_commit_warp(bar(PV_DONE + pbuf));
-            tc_commit_warp(bar(V_EMPTY + vs));
+            tc_commit_warp(bar(C::PV_DONE + pbuf));
+            tc_commit_warp(bar(C::V_EMPTY + vs));
         }
-        tc_commit_warp(bar(PV_ALL_DONE));
-        mbar_wait(bar(PV_ALL_DONE), 0);
+        tc_commit_warp(bar(C::PV_ALL_DONE));
+        mbar_wait(bar(C::PV_ALL_DONE), 0);
         __syncwarp();
         }
-    } else {
-        regs_inc<kSoftmaxRegs>();
+    } else if (warp >= kFirstConvWarp) {
+        regs_dec<C::kConvRegs>();
+        // ================================================= 8-bit pools: code -> FP16 conversion, thread = key row
+        // of the tile. K runs two tiles ahead of V, as S runs two tiles ahead of P V: K_i, then V_{i-2}.
+        const int r = threadIdx.x - kFirstConvWarp * 32;
+        bool ok = true;
+        for (int i = 0; i < n + 2 && ok; ++i) {
+#pragma unroll
+            for (int kv = 0; kv < 2; ++kv) {
+                const int j = kv ? i - 2 : i;
+                if (j < 0 || j >= n) continue;
+                const int stages = kv ? C::kStagesV : C::kStagesK, st = j % stages;
+                if (!flag_wait(bar((kv ? C::V_FULL : C::K_FULL) + st), (uint32_t)(j / stages) & 1u, abort, a.status)) {
+                    ok = false;
+                    break;
+                }
+                convert_code_row(sb + (kv ? C::kSmVRing : C::kSmKRing) + st * kTileOpBytes, r, j * kKeys + r <= pos_max);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar((kv ? C::V_CONV : C::K_CONV) + st));
+            }
+        }
+    } else if (warp >= kFirstSoftmaxWarp && warp < kFirstSoftmaxWarp + 4) {
+        regs_inc<C::kSoftmaxRegs>();
         // ================================================= softmax: thread = query row
         const int qtr = warp & 3;
         const int row = qtr * 32 + lane;
@@ -468,22 +632,31 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
 #pragma unroll
             for (int u = 0; u < kPer; ++u) {
                 const int c = t + u * kSoftmaxThreads, r = c >> 4, ch = c & 15;
-                st_shared_v4(sb + kSmQ + (ch >> 3) * kQSlab + r * 128 + (((ch & 7) ^ (r & 7)) << 4), v[u]);
+                st_shared_v4(sb + C::kSmQ + (ch >> 3) * kQSlab + r * 128 + (((ch & 7) ^ (r & 7)) << 4), v[u]);
             }
             fence_proxy_async_smem();
-            mbar_arrive(bar(Q_READY));
+            mbar_arrive(bar(C::Q_READY));
         }
         float m_used = -INFINITY, l = 0.f;
         bool ok = true;
         for (int j = 0; j < n; ++j) {
             const int sbuf = j % kBufs;
-            if (!flag_wait(bar(S_FULL + sbuf), (uint32_t)(j / kBufs) & 1u, abort, a.status)) {
+            if (!flag_wait(bar(C::S_FULL + sbuf), (uint32_t)(j / kBufs) & 1u, abort, a.status)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
             const uint32_t ts = tl + kColS + sbuf * kSBufCols;
             const int key0 = j * kKeys;
+            // 8-bit pools: this tile's K and V row scales (stage j % 6 of the scale ring)
+            const uint32_t ksc = sb + C::kSmScales + (j % kScaleStages) * kScaleStage, vsc = ksc + kKeys * 4;
+            if constexpr (kI8) {
+                if (!flag_wait(bar(C::SC_FULL + j % kScaleStages), (uint32_t)(j / kScaleStages) & 1u, abort,
+                               a.status)) {
+                    ok = false;
+                    break;
+                }
+            }
             // diagonal tile: keys past the row's position count as -inf. Padding rows (past the chunk's last
             // query) are left unmasked: their Q is zero, their O is never written and rows do not mix in the
             // MMAs, so whatever they compute (even NaN from a key past the context) stays in them; masking
@@ -496,15 +669,17 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             tc_ld64_issue(ts, sr);
             tc_wait_ld64(sr);
             tc_ld64_issue(ts + 64, sr + 64);
+            if constexpr (kI8) scale_columns<64>(sr, ksc);
             if (diag) mask_tail<64>(sr, nvis);
             float mx = max64(sr);
             tc_wait_ld64(sr + 64);
+            if constexpr (kI8) scale_columns<64>(sr + 64, ksc + 64 * 4);
             if (diag) mask_tail<64>(sr + 64, nvis - 64);
             const float m_tile = fmaxf(mx, max64(sr + 64)) * a.scale_log2;
             const bool raise = m_tile > m_used + kRescaleThreshold;  // false while the row has seen no key
             if (j > 0 && __any_sync(0xffffffffu, raise)) {
                 // the previous P V product must have landed before O is rescaled
-                if (!flag_wait(bar(PV_DONE + (j - 1) % kBufs), (uint32_t)((j - 1) / kBufs) & 1u, abort,
+                if (!flag_wait(bar(C::PV_DONE + (j - 1) % kBufs), (uint32_t)((j - 1) / kBufs) & 1u, abort,
                                a.status)) {
                     ok = false;
                     break;
@@ -529,15 +704,26 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             // quarters of 32 keys: P of keys 32q.. goes to P columns 16q.., stored without waiting
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                softmax_quarter(sr + q * 32, a.scale_log2, m_sub, l);
+                if constexpr (kI8) {
+                    if (j == n - 1)  // keys 0..pos_max - key0 of this tile lie at or before the last position
+                        softmax_quarter_vscaled<true>(sr + q * 32, a.scale_log2, m_sub, l, vsc + q * 32 * 4,
+                                                      pos_max - key0 + 1 - q * 32);
+                    else
+                        softmax_quarter_vscaled<false>(sr + q * 32, a.scale_log2, m_sub, l, vsc + q * 32 * 4, 0);
+                } else
+                    softmax_quarter(sr + q * 32, a.scale_log2, m_sub, l);
                 tc_st16_async(tp + q * 16, sr + q * 32);
             }
             tc_wait_st();
             tc_fence_before();
-            mbar_arrive(bar(P_FULL + sbuf));
+            mbar_arrive(bar(C::P_FULL + sbuf));
+            if constexpr (kI8) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(C::SC_FREE + j % kScaleStages));  // done with this tile's scales
+            }
         }
         // ---- epilogue: O / l -> FP16 (each row's 256 B written by its thread)
-        if (ok && flag_wait(bar(PV_DONE + (n - 1) % kBufs), (uint32_t)((n - 1) / kBufs) & 1u, abort, a.status)) {
+        if (ok && flag_wait(bar(C::PV_DONE + (n - 1) % kBufs), (uint32_t)((n - 1) / kBufs) & 1u, abort, a.status)) {
             tc_fence_after();
             const float inv = 1.f / l;
             uint4* dst =
@@ -574,13 +760,17 @@ cudaError_t launch_prefill(const pkv_pool* pool, int layer, const void* q, const
                            const int32_t* tables, int max_blocks, const int32_t* ctx_lens, int num_seqs, int max_q_len,
                            float scale, void* out, cudaStream_t stream)
 {
-    static bool attr_set[64] = {};
+    const bool i8 = pool->geom.dtype == PKV_DTYPE_INT8;
+    static bool attr_set[2][64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
-    if (dev < 64 && !attr_set[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmAlloc);
+    if (dev < 64 && !attr_set[i8][dev]) {
+        cudaError_t e = i8 ? cudaFuncSetAttribute(prefill_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                  Cfg<true>::kSmAlloc)
+                           : cudaFuncSetAttribute(prefill_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                  Cfg<false>::kSmAlloc);
         if (e != cudaSuccess) return e;
-        attr_set[dev] = true;
+        attr_set[i8][dev] = true;
     }
     PrefillArgs a;
     a.q = static_cast<const __half*>(q);
@@ -588,6 +778,10 @@ cudaError_t launch_prefill(const pkv_pool* pool, int layer, const void* q, const
     a.q_start = q_start;
     a.tables = tables;
     a.ctx_lens = ctx_lens;
+    a.base = pool->geom.base;
+    a.block_bytes = pool->geom.block_bytes;
+    a.layer_bytes = pool->geom.layer_bytes;
+    a.tile_bytes = pool->geom.tile_bytes;
     a.max_blocks = max_blocks;
     a.num_heads = pool->geom.num_heads;
     a.num_q_heads = pool->geom.num_q_heads;
@@ -599,9 +793,12 @@ cudaError_t launch_prefill(const pkv_pool* pool, int layer, const void* q, const
     a.status = pool->status_dev;
     CUtensorMap tmap;
     static_assert(sizeof(tmap) == sizeof(pool->kv_tmap.bytes), "tensor map size");
-    memcpy(&tmap, pool->kv_tmap.bytes, sizeof(tmap));
+    memcpy(&tmap, (i8 ? pool->tile_tmap : pool->kv_tmap).bytes, sizeof(tmap));
     dim3 grid((max_q_len + kRows - 1) / kRows, pool->geom.num_q_heads, num_seqs);
-    prefill_kernel<<<grid, kThreads, kSmAlloc, stream>>>(tmap, a);
+    if (i8)
+        prefill_kernel<true><<<grid, Cfg<true>::kThreads, Cfg<true>::kSmAlloc, stream>>>(tmap, a);
+    else
+        prefill_kernel<false><<<grid, Cfg<false>::kThreads, Cfg<false>::kSmAlloc, stream>>>(tmap, a);
     return cudaGetLastError();
 }
 
