@@ -63,7 +63,7 @@ def _iterations(config: str, seed: int = 0):
         return [workloads.shared_prefix_decode(seed)]
     if config == "gqa_decode":
         return [workloads.gqa_decode(seed)]
-    if config == "mixed_prefill":
+    if config in ("mixed_prefill", "mixed_prefill_int8"):
         first = workloads.mixed_prefill(0, seed=seed)
         return [workloads.mixed_prefill(c, seed=seed) for c in range(first.meta["num_chunks"])]
     raise KeyError(config)
@@ -77,6 +77,8 @@ CONFIG_TEXT = {
     "shared_prefix_decode": "64 rows sharing 125 ref-counted prefix blocks + 1..300 private tokens, 32 layers",
     "mixed_prefill": "one 4,000-token prompt prefilled in 512-token chunks (8 iterations) next to 31 decode rows "
                      "of context U{100..2000} advancing one token per iteration, 32 layers",
+    "mixed_prefill_int8": "the mixed_prefill schedule over an 8-bit pool (INT8 codes, one FP32 scale per (token, "
+                          "head) row of K or V): decode rows and prefill chunks both read codes and scales",
     "average_decode_int8": "the average_decode workload over an 8-bit pool (INT8 codes, one FP32 scale per "
                            "(token, head) row of K or V; 2,112-byte tiles), 7,152 blocks (30.9 GB)",
     "shared_prefix_cascade": "64 rows sharing 125 ref-counted prefix blocks + 1..300 private tokens, 32 layers; "
@@ -89,7 +91,7 @@ CONFIG_TEXT = {
                   "kv_append of 1 token per row",
 }
 
-CONFIG_DTYPE = {"average_decode_int8": "int8"}
+CONFIG_DTYPE = {"average_decode_int8": "int8", "mixed_prefill_int8": "int8"}
 SWAP_BLOCKS, SWAP_POOL = 384, 1024
 
 KERNEL_SOURCES = {
@@ -565,7 +567,9 @@ def run_ours(args):
     if pre_ev:
         fl = 4 * HEAD_DIM * Hq * sum(prefill_pairs(s.wl) * n for _, _, s, n in pre_ev)
         ach = fl / (pre_ms * 1e-3) / 1e12
-        rooflines["prefill"] = {"bound": "tensor", "kernel": "prefill_kernel (tcgen05)", "achieved": round(ach, 1),
+        pre_kernel = ("prefill_kernel<8-bit> (tcgen05; codes by TMA become FP16 in shared memory, row scales "
+                      "applied in the softmax)" if dtype == "int8" else "prefill_kernel (tcgen05)")
+        rooflines["prefill"] = {"bound": "tensor", "kernel": pre_kernel, "achieved": round(ach, 1),
                                 "peak": tf_peak, "peak_kind": peak_kind + " bf16 dense (fp16 runs at the same rate)",
                                 "unit": "TFLOP/s", "frac": round(ach / tf_peak, 4),
                                 "traffic": _traffic("prefill_attn", args.config),
@@ -900,7 +904,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", default="average_decode",
                     choices=["average_decode", "long_decode", "shared_prefix_decode", "mixed_prefill", "gqa_decode",
-                             "average_decode_int8", "swap_blocks", "shared_prefix_cascade"])
+                             "average_decode_int8", "mixed_prefill_int8", "swap_blocks", "shared_prefix_cascade"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="launch each step directly instead of replaying a CUDA graph")

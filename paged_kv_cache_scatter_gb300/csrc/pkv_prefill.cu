@@ -145,7 +145,7 @@ struct Cfg {
     static constexpr int V_FULL = K_FULL + kStagesK;
     static constexpr int K_EMPTY = V_FULL + kStagesV;
     static constexpr int V_EMPTY = K_EMPTY + kStagesK;
-    static constexpr int K_CONV = V_EMPTY + kStagesV;    // 8-bit: count 4, the converter warps
+    static constexpr int K_CONV = V_EMPTY + kStagesV;    // 8-bit: count 2, the K (or V) converter warps
     static constexpr int V_CONV = K_CONV + kStagesK;
     static constexpr int SC_FULL = V_CONV + kStagesV;    // 8-bit: [kScaleStages] count 2, the two scale producers
     static constexpr int SC_FREE = SC_FULL + kScaleStages;  // 8-bit: [kScaleStages] count 4, the softmax warps
@@ -322,16 +322,18 @@ __device__ __forceinline__ void convert_code_row(uint32_t tile, int r, bool vali
 }
 
 // 8-bit pools: N scores times their keys' row scales (FP32, from shared memory, the same for every row).
+// The scales are read through an ordinary pointer, not an asm load, so that the compiler can issue the
+// reads ahead of the arithmetic (they are fenced only by the barrier waits, which clobber memory).
 template <int N>
-__device__ __forceinline__ void scale_columns(uint32_t* s, uint32_t scales)
+__device__ __forceinline__ void scale_columns(uint32_t* s, const float4* scales)
 {
 #pragma unroll
     for (int e = 0; e < N; e += 4) {
-        const uint4 k4 = ld_shared_v4(scales + e * 4);
-        s[e] = __float_as_uint(__uint_as_float(s[e]) * __uint_as_float(k4.x));
-        s[e + 1] = __float_as_uint(__uint_as_float(s[e + 1]) * __uint_as_float(k4.y));
-        s[e + 2] = __float_as_uint(__uint_as_float(s[e + 2]) * __uint_as_float(k4.z));
-        s[e + 3] = __float_as_uint(__uint_as_float(s[e + 3]) * __uint_as_float(k4.w));
+        const float4 k4 = scales[e / 4];
+        s[e] = __float_as_uint(__uint_as_float(s[e]) * k4.x);
+        s[e + 1] = __float_as_uint(__uint_as_float(s[e + 1]) * k4.y);
+        s[e + 2] = __float_as_uint(__uint_as_float(s[e + 2]) * k4.z);
+        s[e + 3] = __float_as_uint(__uint_as_float(s[e + 3]) * k4.w);
     }
 }
 
@@ -341,15 +343,15 @@ __device__ __forceinline__ void scale_columns(uint32_t* s, uint32_t scales)
 // weights are 0 and take scale 0, so that 0 times such a scale never reaches the P V product.
 template <bool kTail>
 __device__ __forceinline__ void softmax_quarter_vscaled(uint32_t* s, float scale_log2, float m_sub, float& l,
-                                                        uint32_t vscales, int nkeys)
+                                                        const float4* vscales, int nkeys)
 {
     float ls[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) ls[u] = 0.f;
 #pragma unroll
     for (int e = 0; e < 32; e += 4) {
-        const uint4 v4 = ld_shared_v4(vscales + e * 4);
-        float vs[4] = {__uint_as_float(v4.x), __uint_as_float(v4.y), __uint_as_float(v4.z), __uint_as_float(v4.w)};
+        const float4 v4 = vscales[e / 4];
+        float vs[4] = {v4.x, v4.y, v4.z, v4.w};
         if (kTail) {
 #pragma unroll
             for (int u = 0; u < 4; ++u) vs[u] = e + u < nkeys ? vs[u] : 0.f;
@@ -413,12 +415,12 @@ __global__ void __launch_bounds__(Cfg<kI8>::kThreads, 1) prefill_kernel(const __
         for (int i = 0; i < C::kStagesK; ++i) {
             mbar_init(bar(C::K_FULL + i), kI8 ? 1 : 2);
             mbar_init(bar(C::K_EMPTY + i), 1);
-            mbar_init(bar(C::K_CONV + i), 4);
+            mbar_init(bar(C::K_CONV + i), 2);
         }
         for (int i = 0; i < C::kStagesV; ++i) {
             mbar_init(bar(C::V_FULL + i), kI8 ? 1 : 2);
             mbar_init(bar(C::V_EMPTY + i), 1);
-            mbar_init(bar(C::V_CONV + i), 4);
+            mbar_init(bar(C::V_CONV + i), 2);
         }
         for (int i = 0; i < kScaleStages; ++i) {
             mbar_init(bar(C::SC_FULL + i), 2);
@@ -586,25 +588,24 @@ __global__ void __launch_bounds__(Cfg<kI8>::kThreads, 1) prefill_kernel(const __
         }
     } else if (warp >= kFirstConvWarp) {
         regs_dec<C::kConvRegs>();
-        // ================================================= 8-bit pools: code -> FP16 conversion, thread = key row
-        // of the tile. K runs two tiles ahead of V, as S runs two tiles ahead of P V: K_i, then V_{i-2}.
-        const int r = threadIdx.x - kFirstConvWarp * 32;
-        bool ok = true;
-        for (int i = 0; i < n + 2 && ok; ++i) {
+        // ================================================= 8-bit pools: code -> FP16 conversion. Warps 12, 13
+        // convert K tiles and warps 14, 15 V tiles, two key rows per thread, as two independent streams (K is
+        // needed two tiles before V: one stream doing both would hold K back behind V). Thread i takes rows i
+        // and i + 64, so a warp's 32 rows cover all eight swizzle phases (no bank conflicts).
+        const int kv = (warp - kFirstConvWarp) >> 1;
+        const int r0 = threadIdx.x - (kFirstConvWarp + 2 * kv) * 32;  // rows r0, r0 + 64
+        const int stages = kv ? C::kStagesV : C::kStagesK;
+        const uint32_t full0 = bar(kv ? C::V_FULL : C::K_FULL), conv0 = bar(kv ? C::V_CONV : C::K_CONV);
+        const uint32_t ring = sb + (kv ? C::kSmVRing : C::kSmKRing);
+        for (int j = 0; j < n; ++j) {
+            const int st = j % stages;
+            if (!flag_wait(full0 + 8 * st, (uint32_t)(j / stages) & 1u, abort, a.status)) break;
 #pragma unroll
-            for (int kv = 0; kv < 2; ++kv) {
-                const int j = kv ? i - 2 : i;
-                if (j < 0 || j >= n) continue;
-                const int stages = kv ? C::kStagesV : C::kStagesK, st = j % stages;
-                if (!flag_wait(bar((kv ? C::V_FULL : C::K_FULL) + st), (uint32_t)(j / stages) & 1u, abort, a.status)) {
-                    ok = false;
-                    break;
-                }
-                convert_code_row(sb + (kv ? C::kSmVRing : C::kSmKRing) + st * kTileOpBytes, r, j * kKeys + r <= pos_max);
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar((kv ? C::V_CONV : C::K_CONV) + st));
-            }
+            for (int u = 0; u < 2; ++u)
+                convert_code_row(ring + st * kTileOpBytes, r0 + 64 * u, j * kKeys + r0 + 64 * u <= pos_max);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(conv0 + 8 * st);
         }
     } else if (warp >= kFirstSoftmaxWarp && warp < kFirstSoftmaxWarp + 4) {
         regs_inc<C::kSoftmaxRegs>();
@@ -649,7 +650,8 @@ __global__ void __launch_bounds__(Cfg<kI8>::kThreads, 1) prefill_kernel(const __
             const uint32_t ts = tl + kColS + sbuf * kSBufCols;
             const int key0 = j * kKeys;
             // 8-bit pools: this tile's K and V row scales (stage j % 6 of the scale ring)
-            const uint32_t ksc = sb + C::kSmScales + (j % kScaleStages) * kScaleStage, vsc = ksc + kKeys * 4;
+            const float4* ksc = reinterpret_cast<const float4*>(smem + C::kSmScales + (j % kScaleStages) * kScaleStage);
+            const float4* vsc = ksc + kKeys / 4;
             if constexpr (kI8) {
                 if (!flag_wait(bar(C::SC_FULL + j % kScaleStages), (uint32_t)(j / kScaleStages) & 1u, abort,
                                a.status)) {
@@ -673,7 +675,7 @@ __global__ void __launch_bounds__(Cfg<kI8>::kThreads, 1) prefill_kernel(const __
             if (diag) mask_tail<64>(sr, nvis);
             float mx = max64(sr);
             tc_wait_ld64(sr + 64);
-            if constexpr (kI8) scale_columns<64>(sr + 64, ksc + 64 * 4);
+            if constexpr (kI8) scale_columns<64>(sr + 64, ksc + 16);
             if (diag) mask_tail<64>(sr + 64, nvis - 64);
             const float m_tile = fmaxf(mx, max64(sr + 64)) * a.scale_log2;
             const bool raise = m_tile > m_used + kRescaleThreshold;  // false while the row has seen no key
@@ -706,10 +708,10 @@ __global__ void __launch_bounds__(Cfg<kI8>::kThreads, 1) prefill_kernel(const __
             for (int q = 0; q < 4; ++q) {
                 if constexpr (kI8) {
                     if (j == n - 1)  // keys 0..pos_max - key0 of this tile lie at or before the last position
-                        softmax_quarter_vscaled<true>(sr + q * 32, a.scale_log2, m_sub, l, vsc + q * 32 * 4,
+                        softmax_quarter_vscaled<true>(sr + q * 32, a.scale_log2, m_sub, l, vsc + q * 8,
                                                       pos_max - key0 + 1 - q * 32);
                     else
-                        softmax_quarter_vscaled<false>(sr + q * 32, a.scale_log2, m_sub, l, vsc + q * 32 * 4, 0);
+                        softmax_quarter_vscaled<false>(sr + q * 32, a.scale_log2, m_sub, l, vsc + q * 8, 0);
                 } else
                     softmax_quarter(sr + q * 32, a.scale_log2, m_sub, l);
                 tc_st16_async(tp + q * 16, sr + q * 32);

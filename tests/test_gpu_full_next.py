@@ -1,5 +1,6 @@
-"""Parity at full size for the grouped-head, 8-bit and cascade paths, in the launch configuration bench.py
-times (pkv_step over 32 layers; cascade: kv_append + pkv_decode_attn_cascade per layer).
+"""Parity at full size for the grouped-head, 8-bit (decode and chunked prefill) and cascade paths, in the
+launch configuration bench.py times (pkv_step over 32 layers; cascade: kv_append + pkv_decode_attn_cascade per
+layer).
 
 Sampled (layer, row) outputs are checked against the oracle, which gets host copies of the row's blocks
 taken before the step plus its own append of the row's new token; every new token's stored K/V (FP16
@@ -148,4 +149,69 @@ def test_full_shared_prefix_cascade(pkv):
     g = oracle.geom(N, L, H)
     _check_rows(wl, g, copies, G.to_bits(q), G.to_bits(k), G.to_bits(v), out, H)
     del pool_t
+    torch.cuda.empty_cache()
+
+
+def test_full_int8_mixed_chunked_prefill(pkv):
+    """The 8-chunk schedule of a 4,000-token prompt next to 31 decode rows over an 8-bit pool (30.9 GB),
+    through pkv_step as bench.py times it: after every chunk the prompt's stored codes and scales equal the
+    oracle's own append; sampled prompt rows (chunks 0, 1, 6, 7) and decode rows against the oracle."""
+    first = workloads.mixed_prefill(0)
+    H, N = first.num_heads, first.num_blocks
+    nchunks = first.meta["num_chunks"]
+    P = first.num_seqs - 1                    # the prompt row
+    pool_t = torch.empty(pkv.Pool.bytes_needed(N, L, H, "int8"), dtype=torch.uint8, device="cuda")
+    workloads.fill_int8_tiles_(pool_t, workloads.value_seed(0, "pool"))
+    tiles = pool_t.view(N, L, 2, H, 2112)
+    p = pkv.Pool(pool_t, N, num_layers=L, num_heads=H, dtype="int8")
+    layers, dec_rows = (0, 31), (0, 30)
+    prompt_nb = -(-first.meta["prompt_len"] // 16)
+    prompt_ids = torch.from_numpy(first.block_tables[P, :prompt_nb].astype(np.int64)).cuda()
+    mini = {l: tiles.index_select(0, prompt_ids)[:, l].contiguous().cpu().numpy().reshape(-1).copy()
+            for l in layers}
+    dec_nb = {r: -(-int(first.ctx_lens[r] + nchunks - 1) // 16) for r in dec_rows}
+    dec_mini = {(l, r): tiles.index_select(0, torch.from_numpy(first.block_tables[r, :dec_nb[r]].astype(
+                np.int64)).cuda())[:, l].contiguous().cpu().numpy().reshape(-1).copy()
+                for l in layers for r in dec_rows}
+    g = oracle.geom(prompt_nb, 1, H, dtype=oracle.INT8)
+    table = np.arange(prompt_nb, dtype=np.int32)[None]
+    rng = np.random.default_rng(9)
+    for c in range(nchunks):
+        wl = workloads.mixed_prefill(c)
+        T, B = wl.num_tokens, wl.num_decode
+        start, end = wl.meta["chunk_start"], wl.meta["chunk_end"]
+        tables_d, ctx_d, qs_d, slots_d, slots = G.step_metadata(wl)
+        q, k, v = _inputs(T, H, H, 40 + c)
+        out = torch.full_like(q, float("nan"))
+        sd = pkv.make_step_desc(num_decode=B, num_prefill=1, num_tokens=T, max_q_len=end - start,
+                                max_blocks=wl.max_blocks, first_layer=0, num_layers=L, scale=G.SCALE,
+                                block_tables=tables_d, ctx_lens=ctx_d, q_start_loc=qs_d, slot_mapping=slots_d,
+                                q=q, k=k, v=v, out=out, q_layer_stride=T * H * 128, k_layer_stride=T * H * 128,
+                                v_layer_stride=T * H * 128, out_layer_stride=T * H * 128)
+        ws = torch.empty(max(p.step_workspace_bytes(sd), 256), dtype=torch.uint8, device="cuda")
+        p.step(sd, ws)
+        assert p.get_status() == (pkv.PKV_OK, 0), f"chunk {c}"
+        qb, kb, vb = G.to_bits(q), G.to_bits(k), G.to_bits(v)
+        for l in layers:
+            pos = np.arange(start, end, dtype=np.int64)
+            assert oracle.kv_append(mini[l], g, 0, kb[l, B:], vb[l, B:], pos) == -1
+            got = tiles.index_select(0, prompt_ids)[:, l].contiguous().cpu().numpy().reshape(-1)
+            assert np.array_equal(got, mini[l]), f"chunk {c} layer {l}: prompt codes/scales differ"
+            for r in dec_rows:
+                ctx = int(wl.ctx_lens[r])
+                gd = oracle.geom(dec_nb[r], 1, H, dtype=oracle.INT8)
+                assert oracle.kv_append(dec_mini[(l, r)], gd, 0, kb[l, r][None], vb[l, r][None],
+                                        np.array([ctx - 1], np.int64)) == -1
+                ref, _ = oracle.decode_attn(dec_mini[(l, r)], gd, 0, qb[l, r][None],
+                                            np.arange(dec_nb[r], dtype=np.int32)[None], np.array([ctx], np.int32),
+                                            G.SCALE)
+                G.assert_close(out[l, r], ref[0], f"chunk {c} layer {l} decode row {r}")
+            if c not in (0, 1, 6, 7):
+                continue
+            picks = sorted(set([0, end - start - 1] + rng.integers(0, end - start, 14).tolist()))
+            for i in picks:
+                ref, _ = oracle.decode_attn(mini[l], g, 0, qb[l, B + i][None], table,
+                                            np.array([start + i + 1], np.int32), G.SCALE)
+                G.assert_close(out[l, B + i], ref[0], f"chunk {c} layer {l} prefill row {i}")
+    del pool_t, tiles
     torch.cuda.empty_cache()
