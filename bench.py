@@ -63,9 +63,13 @@ def _iterations(config: str, seed: int = 0):
         return [workloads.shared_prefix_decode(seed)]
     if config == "gqa_decode":
         return [workloads.gqa_decode(seed)]
-    if config in ("mixed_prefill", "mixed_prefill_int8"):
+    if config in ("mixed_prefill", "mixed_prefill_int8", "mixed_prefill_gqa"):
         first = workloads.mixed_prefill(0, seed=seed)
-        return [workloads.mixed_prefill(c, seed=seed) for c in range(first.meta["num_chunks"])]
+        its = [workloads.mixed_prefill(c, seed=seed) for c in range(first.meta["num_chunks"])]
+        if config == "mixed_prefill_gqa":
+            for w in its:
+                w.num_heads, w.num_q_heads = workloads.GQA_KV_HEADS, workloads.NUM_HEADS
+        return its
     raise KeyError(config)
 
 
@@ -77,6 +81,8 @@ CONFIG_TEXT = {
     "shared_prefix_decode": "64 rows sharing 125 ref-counted prefix blocks + 1..300 private tokens, 32 layers",
     "mixed_prefill": "one 4,000-token prompt prefilled in 512-token chunks (8 iterations) next to 31 decode rows "
                      "of context U{100..2000} advancing one token per iteration, 32 layers",
+    "mixed_prefill_gqa": "the mixed_prefill schedule with 8 K/V heads serving 32 query heads (grouped-query "
+                         "attention): a prefill CTA takes 32 tokens of a K/V head's 4 query heads as its 128 rows",
     "mixed_prefill_int8": "the mixed_prefill schedule over an 8-bit pool (INT8 codes, one FP32 scale per (token, "
                           "head) row of K or V): decode rows and prefill chunks both read codes and scales",
     "average_decode_int8": "the average_decode workload over an 8-bit pool (INT8 codes, one FP32 scale per "
@@ -904,7 +910,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", default="average_decode",
                     choices=["average_decode", "long_decode", "shared_prefix_decode", "mixed_prefill", "gqa_decode",
-                             "average_decode_int8", "mixed_prefill_int8", "swap_blocks", "shared_prefix_cascade"])
+                             "average_decode_int8", "mixed_prefill_int8", "mixed_prefill_gqa", "swap_blocks",
+                             "shared_prefix_cascade"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="launch each step directly instead of replaying a CUDA graph")

@@ -192,6 +192,8 @@ struct PrefillArgs {
     int num_heads;     // K/V heads of the pool
     int num_q_heads;   // query heads: q and out rows are [num_q_heads][128]
     int group;         // query heads per K/V head; query head h reads K/V head h / group
+    int hpc;           // query heads per CTA: the group (group <= 128) or 1
+    int tok;           // query tokens per CTA: 128 / hpc; MMA row r is token r % tok of head r / tok
     int layer;
     int max_q_len;
     int64_t num_blocks;
@@ -379,7 +381,10 @@ __global__ void __launch_bounds__(Cfg<kI8>::kThreads, 1) prefill_kernel(const __
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     const uint32_t sb = smem_u32(smem);
-    const int qt = blockIdx.x, h = blockIdx.y, s = blockIdx.z;
+    // CTA = (tile of `tok` query tokens, group of `hpc` query heads sharing one K/V head, sequence). Its 128
+    // MMA rows are (head r / tok, token r % tok): the group's K/V tiles are gathered once for all its heads.
+    const int qt = blockIdx.x, s = blockIdx.z;
+    const int hq0 = blockIdx.y * a.hpc, hkv = hq0 / a.group;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     // ---- validate this sequence's metadata (all threads agree)
@@ -387,14 +392,14 @@ __global__ void __launch_bounds__(Cfg<kI8>::kThreads, 1) prefill_kernel(const __
     const int qlen = __ldg(a.q_start + s + 1) - q0;
     const int ctx = __ldg(a.ctx_lens + s);
     if (q0 < 0 || qlen < 1 || qlen > ctx || qlen > a.max_q_len || ctx > a.max_blocks * kBlockSize) {
-        if (qt == 0 && h == 0 && threadIdx.x == 0)
+        if (qt == 0 && blockIdx.y == 0 && threadIdx.x == 0)
             atomicOr(a.status, ctx > a.max_blocks * kBlockSize ? PKV_DEV_BAD_CTX : PKV_DEV_BAD_QLEN);
         return;
     }
-    if (qt * kRows >= qlen) return;
-    const int rows = min(kRows, qlen - qt * kRows);
-    const int p0 = ctx - qlen + qt * kRows;  // position of row 0
-    const int pos_max = p0 + rows - 1;
+    if (qt * a.tok >= qlen) return;
+    const int ntok = min(a.tok, qlen - qt * a.tok);  // this CTA's query tokens
+    const int p0 = ctx - qlen + qt * a.tok;           // position of its first token
+    const int pos_max = p0 + ntok - 1;
     const int n = pos_max / kKeys + 1;       // 128-key tiles
     const int nblk = pos_max / kBlockSize + 1;
     const int32_t* trow = a.tables + (int64_t)s * a.max_blocks;
@@ -459,7 +464,7 @@ __global__ void __launch_bounds__(Cfg<kI8>::kThreads, 1) prefill_kernel(const __
         const int b = lane & (kBlocksPerTile - 1), half = warp & 1;
         const bool copier = lane < kBlocksPerTile;
         const bool scales = kI8 && half;
-        const int kvh = kv * a.num_heads + h / a.group;
+        const int kvh = kv * a.num_heads + hkv;
         const uint32_t ring = sb + (kv ? C::kSmVRing : C::kSmKRing) + ((kI8 || half) ? kTileSlab : 0);
         const uint32_t scale_ring = sb + C::kSmScales + kv * kKeys * 4;
         const uint32_t full0 = bar(scales ? C::SC_FULL : kv ? C::V_FULL : C::K_FULL);
@@ -612,8 +617,9 @@ __global__ void __launch_bounds__(Cfg<kI8>::kThreads, 1) prefill_kernel(const __
         // ================================================= softmax: thread = query row
         const int qtr = warp & 3;
         const int row = qtr * 32 + lane;
-        const bool valid = row < rows;
-        const int pos = p0 + row;
+        const int rhead = row / a.tok, rtok = row % a.tok;
+        const bool valid = rhead < a.hpc && rtok < ntok;  // else a padding row (zero Q, never written)
+        const int pos = p0 + rtok;
         const uint32_t tl = tmem + ((uint32_t)(qtr * 32) << 16);
         {
             // ---- Q tile -> shared memory (swizzled, K-major), rows past the chunk zero, while the
@@ -624,10 +630,11 @@ __global__ void __launch_bounds__(Cfg<kI8>::kThreads, 1) prefill_kernel(const __
 #pragma unroll
             for (int u = 0; u < kPer; ++u) {
                 const int c = t + u * kSoftmaxThreads, r = c >> 4, ch = c & 15;
+                const int hh = r / a.tok, tt = r % a.tok;
                 v[u] = make_uint4(0, 0, 0, 0);
-                if (r < rows)
+                if (hh < a.hpc && tt < ntok)
                     v[u] = __ldg(reinterpret_cast<const uint4*>(
-                                     a.q + ((int64_t)(q0 + qt * kRows + r) * a.num_q_heads + h) * kHeadDim) +
+                                     a.q + ((int64_t)(q0 + qt * a.tok + tt) * a.num_q_heads + hq0 + hh) * kHeadDim) +
                                  ch);
             }
 #pragma unroll
@@ -729,7 +736,8 @@ __global__ void __launch_bounds__(Cfg<kI8>::kThreads, 1) prefill_kernel(const __
             tc_fence_after();
             const float inv = 1.f / l;
             uint4* dst =
-                reinterpret_cast<uint4*>(a.out + ((int64_t)(q0 + qt * kRows + row) * a.num_q_heads + h) * kHeadDim);
+                reinterpret_cast<uint4*>(a.out + ((int64_t)(q0 + qt * a.tok + rtok) * a.num_q_heads + hq0 + rhead) *
+                                         kHeadDim);
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 float o[32];
@@ -788,6 +796,8 @@ cudaError_t launch_prefill(const pkv_pool* pool, int layer, const void* q, const
     a.num_heads = pool->geom.num_heads;
     a.num_q_heads = pool->geom.num_q_heads;
     a.group = pool->geom.group;
+    a.hpc = pool->geom.group <= kRows ? pool->geom.group : 1;
+    a.tok = kRows / a.hpc;
     a.layer = layer;
     a.max_q_len = max_q_len;
     a.num_blocks = pool->geom.num_blocks;
@@ -796,7 +806,7 @@ cudaError_t launch_prefill(const pkv_pool* pool, int layer, const void* q, const
     CUtensorMap tmap;
     static_assert(sizeof(tmap) == sizeof(pool->kv_tmap.bytes), "tensor map size");
     memcpy(&tmap, (i8 ? pool->tile_tmap : pool->kv_tmap).bytes, sizeof(tmap));
-    dim3 grid((max_q_len + kRows - 1) / kRows, pool->geom.num_q_heads, num_seqs);
+    dim3 grid((max_q_len + a.tok - 1) / a.tok, pool->geom.num_q_heads / a.hpc, num_seqs);
     if (i8)
         prefill_kernel<true><<<grid, Cfg<true>::kThreads, Cfg<true>::kSmAlloc, stream>>>(tmap, a);
     else
