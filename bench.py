@@ -21,7 +21,8 @@ headline workload over an 8-bit pool: INT8 codes plus one FP32 scale per
 128-value row, 132 bytes per row instead of 256), swap_blocks (a preempted
 batch's 384 scattered 8 MB blocks swapped out to page-locked host memory and
 back in one launch each; its roofline is a contiguous cudaMemcpyAsync of the
-same bytes measured in the same run).
+same bytes measured in the same run), mixed_prefill_int8 and mixed_prefill_gqa (the
+chunk schedule over an 8-bit pool, and with 8 K/V heads serving 32 query heads).
 
 Rank 0 prints one JSON line. Under torchrun (N > 1) every rank runs its own
 replica (weak scaling, no collective on the data path); `value` adds all
