@@ -403,10 +403,31 @@ __global__ void __launch_bounds__(Cfg<kI8>::kThreads, 1) prefill_kernel(const __
     const int n = pos_max / kKeys + 1;       // 128-key tiles
     const int nblk = pos_max / kBlockSize + 1;
     const int32_t* trow = a.tables + (int64_t)s * a.max_blocks;
+    // The first S waits on two cold reads, Q and the first K tile: start both into L2 now (prefetch hints
+    // through the load path, not the copy engine, whose queue the first tile's boxes need). Q: a line
+    // (128 B) per thread; the first tile's K and V tiles: their lines spread over the CTA.
+    {
+        const int lines_per_tok = a.hpc * 2;  // hpc rows of 256 B
+        for (int i = threadIdx.x; i < ntok * lines_per_tok; i += C::kThreads)
+            prefetch_l2(a.q + ((int64_t)(q0 + qt * a.tok + i / lines_per_tok) * a.num_q_heads + hq0) * kHeadDim +
+                        (i % lines_per_tok) * 64);
+    }
     bool bad = false;
+    const int lines_per_tile = (int)(a.tile_bytes / 128);
     for (int b = threadIdx.x; b < nblk; b += C::kThreads) {
         const int id = __ldg(trow + b);
         bad |= id < 0 || (int64_t)id >= a.num_blocks;
+    }
+    if (threadIdx.x < kBlocksPerTile * 2 * 32) {  // block b of the first tile, K or V, 32 lines apart
+        const int b = threadIdx.x / 64, kvl = (threadIdx.x / 32) & 1, l0 = threadIdx.x & 31;
+        if (b < nblk) {
+            const int id = __ldg(trow + b);
+            if (id >= 0 && (int64_t)id < a.num_blocks) {
+                const char* t = a.base + (int64_t)id * a.block_bytes + (int64_t)a.layer * a.layer_bytes +
+                                (int64_t)(kvl * a.num_heads + hkv) * a.tile_bytes;
+                for (int l = l0; l < lines_per_tile; l += 32) prefetch_l2(t + l * 128);
+            }
+        }
     }
     if (__syncthreads_or(bad)) {
         if (threadIdx.x == 0) atomicOr(a.status, PKV_DEV_BAD_BLOCK);
@@ -483,6 +504,11 @@ __global__ void __launch_bounds__(Cfg<kI8>::kThreads, 1) prefill_kernel(const __
         const int stages = scales ? kScaleStages : kv ? C::kStagesV : C::kStagesK;
         int issued = 0;
         bool stop = false;
+        // The copy engine serves boxes in issue order and P_0 V_0 comes a whole softmax period after S_0:
+        // V's producers start once S_0 is done (so K_0 has landed), so that K_0's boxes are not queued
+        // behind V_0's. (S_FULL of buffer 0 cannot complete a second phase before P_0 V_0, which needs V_0,
+        // so this wait cannot miss its phase; K_FULL of stage 0 could, via K_3.)
+        if (kv && !scales && !flag_wait(bar(C::S_FULL), 0, abort, a.status)) stop = true;
         for (int i0 = 0; i0 < n && !stop; i0 += kIdAhead) {
 #pragma unroll
             for (int u = 0; u < kIdAhead; ++u) {

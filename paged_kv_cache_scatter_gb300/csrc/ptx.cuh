@@ -94,6 +94,12 @@ __device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity, u
 
 // ------------------------------------------------------- bulk async copies
 
+// Hint: bring the line holding `p` into L2 (through the load path, not the copy engine).
+__device__ __forceinline__ void prefetch_l2(const void* p)
+{
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 // 1-D bulk copy global -> shared; completes `bytes` of transaction on `bar`.
 // dst and src 16-byte aligned, bytes a multiple of 16.
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar)
