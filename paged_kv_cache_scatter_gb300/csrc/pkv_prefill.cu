@@ -247,35 +247,34 @@ __device__ __forceinline__ void mask_tail(uint32_t* s, int nvis)
         if (e >= nvis) s[e] = __float_as_uint(-INFINITY);
 }
 
-// Max of 64 S values.
+// Max of 64 S values: three-input maxima, eight independent chains.
 __device__ __forceinline__ float max64(const uint32_t* sr)
 {
+    auto f = [&](int e) { return __uint_as_float(sr[e]); };
     float mxs[8];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) mxs[u] = __uint_as_float(sr[u]);
+    for (int u = 0; u < 8; ++u) mxs[u] = fmax3(f(3 * u), f(3 * u + 1), f(3 * u + 2));  // values 0..23
 #pragma unroll
-    for (int e = 8; e < 64; ++e) mxs[e & 7] = fmaxf(mxs[e & 7], __uint_as_float(sr[e]));
-    return fmaxf(fmaxf(fmaxf(mxs[0], mxs[1]), fmaxf(mxs[2], mxs[3])),
-                 fmaxf(fmaxf(mxs[4], mxs[5]), fmaxf(mxs[6], mxs[7])));
+    for (int i = 0; i < 20; ++i) mxs[i & 7] = fmax3(mxs[i & 7], f(24 + 2 * i), f(25 + 2 * i));  // 24..63
+    return fmax3(fmax3(mxs[0], mxs[1], mxs[2]), fmax3(mxs[3], mxs[4], mxs[5]), fmaxf(mxs[6], mxs[7]));
 }
 
 // Softmax of a quarter tile: 32 S values -> P = 2^(s*scale - m) as 16 FP16 pairs, written in place over
 // s[0..15] (pair e/2 lands on a value already read); the sum is added to l. An s of -inf gives p = 0.
+// The exponents and the sums go two at a time (f32x2 FMA and add); the 2^x stay scalar.
 __device__ __forceinline__ void softmax_quarter(uint32_t* s, float scale_log2, float m_sub, float& l)
 {
-    float ls[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) ls[u] = 0.f;
+    const uint64_t sc2 = f32x2_pack(scale_log2, scale_log2), nm2 = f32x2_pack(-m_sub, -m_sub);
+    uint64_t acc[2] = {f32x2_pack(0.f, 0.f), f32x2_pack(0.f, 0.f)};
 #pragma unroll
     for (int e = 0; e < 32; e += 2) {
-        const float pa = ex2(fmaf(__uint_as_float(s[e]), scale_log2, -m_sub));
-        const float pb = ex2(fmaf(__uint_as_float(s[e + 1]), scale_log2, -m_sub));
-        ls[e & 3] += pa;
-        ls[(e + 1) & 3] += pb;
-        const __half2 hp = __floats2half2_rn(pa, pb);
-        s[e >> 1] = *reinterpret_cast<const uint32_t*>(&hp);
+        const float2 x = f32x2_unpack(fma_f32x2(f32x2_pack(__uint_as_float(s[e]), __uint_as_float(s[e + 1])), sc2, nm2));
+        const float pa = ex2(x.x), pb = ex2(x.y);
+        acc[(e >> 1) & 1] = add_f32x2(acc[(e >> 1) & 1], f32x2_pack(pa, pb));
+        s[e >> 1] = pack_half2(pa, pb);
     }
-    l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+    const float2 a0 = f32x2_unpack(acc[0]), a1 = f32x2_unpack(acc[1]);
+    l += (a0.x + a0.y) + (a1.x + a1.y);
 }
 
 // 8-bit pools: one key row r of a 128-key operand tile. Its 128 codes sit in the tile's second slab, row r,
