@@ -386,6 +386,12 @@ __global__ void __launch_bounds__(Cfg<kI8>::kThreads, 1) prefill_kernel(const __
     const int hq0 = blockIdx.y * a.hpc, hkv = hq0 / a.group;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+    // Launched with a programmatic dependency on the stream's previous kernel: this grid's CTAs may be
+    // placed on SMs that kernel has left (or never used) before it ends, and wait here for its results.
+    // Nothing in global memory is read before this point, so any earlier kernel may produce the inputs.
+    pdl_trigger();
+    pdl_wait();
+
     // ---- validate this sequence's metadata (all threads agree)
     const int q0 = __ldg(a.q_start + s);
     const int qlen = __ldg(a.q_start + s + 1) - q0;
@@ -831,12 +837,18 @@ cudaError_t launch_prefill(const pkv_pool* pool, int layer, const void* q, const
     CUtensorMap tmap;
     static_assert(sizeof(tmap) == sizeof(pool->kv_tmap.bytes), "tensor map size");
     memcpy(&tmap, (i8 ? pool->tile_tmap : pool->kv_tmap).bytes, sizeof(tmap));
-    dim3 grid((max_q_len + a.tok - 1) / a.tok, pool->geom.num_q_heads / a.hpc, num_seqs);
-    if (i8)
-        prefill_kernel<true><<<grid, Cfg<true>::kThreads, Cfg<true>::kSmAlloc, stream>>>(tmap, a);
-    else
-        prefill_kernel<false><<<grid, Cfg<false>::kThreads, Cfg<false>::kSmAlloc, stream>>>(tmap, a);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((max_q_len + a.tok - 1) / a.tok, pool->geom.num_q_heads / a.hpc, num_seqs);
+    cfg.blockDim = dim3(i8 ? Cfg<true>::kThreads : Cfg<false>::kThreads);
+    cfg.dynamicSmemBytes = i8 ? Cfg<true>::kSmAlloc : Cfg<false>::kSmAlloc;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return i8 ? cudaLaunchKernelEx(&cfg, prefill_kernel<true>, tmap, a)
+              : cudaLaunchKernelEx(&cfg, prefill_kernel<false>, tmap, a);
 }
 
 }  // namespace pkv
