@@ -145,7 +145,7 @@ __global__ void __launch_bounds__(kGWarps * 32) decode_group_kernel(const __grid
     const int g = lane >> 2, tq = lane & 3;  // fragment row and column pair of this lane
     // The CTA's rows: query heads h0 .. h0 + R - 1 of row r, or (cascade) rows r .. r + R - 1 of one group,
     // head h0. Row i's query is q + qoff + i * qstride and its output / partial index rh0 + i * rstride.
-    int r, kvh, c, h0, R, ctx, nparts;
+    int r, kvh, c, h0, R, ctx, nparts, span;
     int64_t qstride, rstride;
     if (CASCADE) {
         const int grp = blockIdx.z / a.max_slices, sl = blockIdx.z % a.max_slices;
@@ -157,7 +157,8 @@ __global__ void __launch_bounds__(kGWarps * 32) decode_group_kernel(const __grid
         c = 0;
         h0 = kvh;
         ctx = __ldg(a.group_blocks + grp) * kBlockSize;  // the shared prefix: full blocks, valid for every row
-        nparts = (ctx + a.part_tokens - 1) / a.part_tokens;  // the prefix partitioned on its own
+        span = a.part_tokens;
+        nparts = (ctx + span - 1) / span;  // the prefix partitioned on its own
         if (p >= nparts) return;
         qstride = (int64_t)a.num_q_heads * kHeadDim;
         rstride = a.num_q_heads;
@@ -172,13 +173,18 @@ __global__ void __launch_bounds__(kGWarps * 32) decode_group_kernel(const __grid
             if (p == 0 && blockIdx.y == 0 && threadIdx.x == 0) atomicOr(a.status, PKV_DEV_BAD_CTX);
             return;
         }
-        nparts = (ctx + a.part_tokens - 1) / a.part_tokens;
+        // As few partitions as part_tokens allows, of equal length in whole blocks (a row of 2,300 keys: 768,
+        // 768, 764 rather than 1,024, 1,024, 252), so that no short partition's CTA trails the launch. The plan
+        // depends only on ctx and part_tokens: a row's result is the same in any batch.
+        const int np = (ctx + a.part_tokens - 1) / a.part_tokens;
+        span = ((ctx + np - 1) / np + kBlockSize - 1) / kBlockSize * kBlockSize;  // <= part_tokens
+        nparts = (ctx + span - 1) / span;                                       // <= np
         if (p >= nparts) return;
         qstride = kHeadDim;
         rstride = 1;
     }
-    const int blk_lo = p * a.part_tokens / kBlockSize;
-    const int blk_hi = (min((p + 1) * a.part_tokens, ctx) + kBlockSize - 1) / kBlockSize;
+    const int blk_lo = p * span / kBlockSize;
+    const int blk_hi = (min((p + 1) * span, ctx) + kBlockSize - 1) / kBlockSize;
     const int count = blk_hi - blk_lo;  // <= kGMaxBlocks (partition_tokens <= 2,048, a multiple of 64)
 
     int32_t* ids = reinterpret_cast<int32_t*>(smem + kGSmIds);

@@ -179,7 +179,7 @@ __global__ void __launch_bounds__(WARPS * 32) decode_kernel(const DecodeArgs a)
         if (p == 0 && h == 0 && threadIdx.x == 0) atomicOr(a.status, PKV_DEV_BAD_CTX);
         return;
     }
-    // Partition plan: keys [0, ctx) in partitions of part_tokens. Cascade: keys [0, S) of the row's group's
+    // Partition plan: keys [0, ctx) in partitions of at most part_tokens. Cascade: keys [0, S) of the row's group's
     // shared prefix are partitioned on their own (computed already, slots 0 .. nsh-1); this CTA takes
     // partition p of [S, ctx), slot nsh + p.
     int S = 0;
@@ -191,13 +191,17 @@ __global__ void __launch_bounds__(WARPS * 32) decode_kernel(const DecodeArgs a)
         }
         S = __ldg(a.group_blocks + lo) * kBlockSize;
     }
+    // [S, ctx) goes into as few partitions as part_tokens allows, of equal length in whole blocks (1,043 keys:
+    // 528 + 515, not 1,024 + 19), so that no short partition's CTA trails the launch.
     const int nsh = (S + a.part_tokens - 1) / a.part_tokens;
-    const int tok_lo = S + p * a.part_tokens;
+    const int np = (ctx - S + a.part_tokens - 1) / a.part_tokens;
+    const int span = ((ctx - S + np - 1) / np + kBlockSize - 1) / kBlockSize * kBlockSize;
+    const int tok_lo = S + p * span;
     if (tok_lo >= ctx) return;
-    const int nparts = nsh + (ctx - S + a.part_tokens - 1) / a.part_tokens;
+    const int nparts = nsh + (ctx - S + span - 1) / span;
     const int slot_p = nsh + p;
     const int blk_lo = tok_lo >> 4;
-    const int blk_hi = (min(tok_lo + a.part_tokens, ctx) + 15) >> 4;
+    const int blk_hi = (min(tok_lo + span, ctx) + 15) >> 4;
     const int nblk = blk_hi - blk_lo;
     int count = nblk > warp ? (nblk - warp + WARPS - 1) / WARPS : 0;  // <= 32 by construction
 
