@@ -418,17 +418,20 @@ def run_ours(args):
     sampler.start()
     time.sleep(0.3)
     e0, e1 = ev(), ev()
+    marks = [ev() for _ in range(args.steps)]  # one event after each step: the per-step distribution
     e0.record(stream)
-    for _ in range(args.steps):
+    for i in range(args.steps):
         if graph is not None:
             graph.replay()
         else:
             step()
+        marks[i].record(stream)
     e1.record(stream)
     torch.cuda.synchronize(dev)
     if ws > 1:
         dist.barrier()
     t_ms = e0.elapsed_time(e1)
+    step_times = [(e0 if i == 0 else marks[i - 1]).elapsed_time(marks[i]) for i in range(args.steps)]
 
     # ---- timed region 2: each attention kernel alone. With graphs (the default), one CUDA graph per iteration
     # and kernel holds that kernel's launches for all layers, replayed between two events: per-launch time =
@@ -599,6 +602,9 @@ def run_ours(args):
         "steps": K,
         "warmup": args.warmup,
         "ms_per_step": round(t_ms / K, 4),
+        "step_ms": {"p10": round(float(np.percentile(step_times, 10)), 4),
+                    "median": round(float(np.median(step_times)), 4),
+                    "p90": round(float(np.percentile(step_times, 90)), 4)},
         "us_per_iteration": round(t_ms / K / len(steps) * 1e3, 1),
         "attention_tokens_per_s": round(tokens_step * K * ws / (t_ms * 1e-3), 1),
         "higher_is_better": True,
