@@ -101,6 +101,17 @@ def test_random_ragged_decode(pkv, seed, partition):
     _run_decode_case(pkv, wl, partition, layers=(1,))
 
 
+@pytest.mark.parametrize("partition,ctxs", [(0, [1024, 1025, 1040, 1041, 2047, 2048, 2049, 3073]),
+                                            (64, [64, 65, 80, 127, 128, 129, 1000, 3073])])
+def test_decode_equal_partition_boundaries(pkv, partition, ctxs):
+    # Contexts on and next to the partition bounds (0 = the library's 1,024): a row's keys go into the fewest
+    # partitions of at most that many keys, of equal length in whole blocks, which must cover [0, ctx) once.
+    wl = workloads.random_step(13, num_seqs=len(ctxs), max_ctx=3100, min_ctx=3100,
+                               num_blocks=len(ctxs) * 194 + 8, num_layers=1)
+    wl.ctx_lens[:] = ctxs
+    _run_decode_case(pkv, wl, partition)
+
+
 def test_decode_long_rows_many_partitions(pkv):
     wl = workloads.random_step(7, num_seqs=3, max_ctx=4200, min_ctx=3000, num_blocks=800, num_layers=1)
     _run_decode_case(pkv, wl, partition=64)

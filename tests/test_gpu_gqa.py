@@ -128,6 +128,15 @@ def test_gqa_fused_append_equals_separate(pkv):
     assert torch.equal(a, b)
 
 
+@pytest.mark.parametrize("partition,ctxs", [(0, [1024, 1025, 1041, 2047, 2049, 2300, 3073]),
+                                            (64, [64, 65, 127, 129, 1000, 2300, 3073])])
+def test_gqa_equal_partition_boundaries(pkv, partition, ctxs):
+    # Equal-length partitions at and next to the bounds, with the decode rows' append fused into the last one.
+    wl = _decode_wl(17, 8, num_seqs=len(ctxs), max_ctx=3100, min_ctx=3100, num_layers=1, edges=False)
+    wl.ctx_lens[:] = ctxs
+    run_gqa(pkv, wl, 32, partition=partition, use_step=True)
+
+
 def test_gqa_long_rows_many_partitions(pkv):
     wl = _decode_wl(7, 8, num_seqs=3, max_ctx=4200, min_ctx=3000, num_layers=1, edges=False)
     assert wl.ctx_lens.min() >= 3000
