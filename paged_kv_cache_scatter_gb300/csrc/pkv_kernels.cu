@@ -110,6 +110,7 @@ cudaError_t launch_kv_append(const PoolGeom& g, int layer, const void* k, const 
 
 constexpr int kDecodeWarps = 4;
 constexpr int kDecodeStages = 2;
+constexpr int kCascadeWarps = 2;  // cascade decode's private-key launch
 constexpr int kStageBytes = 2 * kTileBytes;
 constexpr int kMaxMergeParts = kMaxPartitionsPerRow;  // s_w and s_l of the merge fit in the idle rings
 
@@ -524,13 +525,21 @@ cudaError_t launch_decode(const PoolGeom& g, int layer, const void* q, const int
                           const int32_t* group_blocks, int num_groups, bool pdl)
 {
     if (num_seqs == 0) return cudaSuccess;
+    // Cascade decode's private keys are a few hundred per row: CTAs of two warps (half the shared memory, so
+    // twice as many resident per SM) overlap more of their start-up with each other's streaming.
+    // (A warp's lanes hold its block ids, at most 32: two warps cover partitions of up to 1,024 keys.)
+    const bool cascade = num_groups > 0 && partition_tokens <= 32 * kCascadeWarps * kBlockSize;
     using Lay = DecodeLayout<kDecodeWarps, kDecodeStages>;
+    using LayC = DecodeLayout<kCascadeWarps, kDecodeStages>;
     static bool attr_set[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 64 && !attr_set[dev]) {
         cudaError_t e = cudaFuncSetAttribute(decode_kernel<kDecodeWarps, kDecodeStages>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kBytes);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(decode_kernel<kCascadeWarps, kDecodeStages>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, LayC::kBytes);
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
@@ -563,15 +572,16 @@ cudaError_t launch_decode(const PoolGeom& g, int layer, const void* q, const int
     a.counters = w.counters;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(a.max_parts, g.num_heads, num_seqs);
-    cfg.blockDim = dim3(kDecodeWarps * 32);
-    cfg.dynamicSmemBytes = Lay::kBytes;
+    cfg.blockDim = dim3((cascade ? kCascadeWarps : kDecodeWarps) * 32);
+    cfg.dynamicSmemBytes = cascade ? LayC::kBytes : Lay::kBytes;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, decode_kernel<kDecodeWarps, kDecodeStages>, a);
+    return cascade ? cudaLaunchKernelEx(&cfg, decode_kernel<kCascadeWarps, kDecodeStages>, a)
+                   : cudaLaunchKernelEx(&cfg, decode_kernel<kDecodeWarps, kDecodeStages>, a);
 }
 
 // ======================================================================
