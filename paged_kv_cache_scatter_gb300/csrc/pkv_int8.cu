@@ -191,9 +191,13 @@ __device__ __forceinline__ unsigned int q_atomic_add_acq_rel(unsigned int* p, un
     return old;
 }
 
+// Up to 8 query heads per CTA: four CTAs per SM (at most 128 registers a thread; shared memory allows more): an
+// 8-bit CTA carries half the bytes of an FP16 one, so more of them in flight cover more of each other's start-up
+// (+4 % on the batch-32 step against three per SM, a few spilled registers included). 16 query heads per CTA
+// need more registers: three per SM.
 template <bool ROWS16>
-__global__ void __launch_bounds__(kQWarps * 32) decode_i8_kernel(const __grid_constant__ CUtensorMap tmap,
-                                                                 const I8Args a)
+__global__ void __launch_bounds__(kQWarps * 32, ROWS16 ? 3 : 4)
+    decode_i8_kernel(const __grid_constant__ CUtensorMap tmap, const I8Args a)
 {
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
