@@ -147,13 +147,21 @@ int64_t pkv_seq_len(const pkv_pool* pool, int64_t seq_id);      /* -1 if unknown
  * into block tables": copy-on-write sharing for parallel sampling). */
 pkv_status pkv_seq_fork(pkv_pool* pool, int64_t dst_seq, int64_t src_seq);
 
-/* Copy-on-write: if seq_id's next token would land in its partly filled last
- * block and that block is shared, give seq_id a private block: a free block
- * replaces the shared one in its table (old ref_count - 1, new 1) and
+/* Copy-on-write ("The inference engine" (wpnews), "Paging turns variable
+ * sequences into block tables": a branch that diverges gets its own copy).
+ * Call after pkv_seq_grow and before the step that writes seq_id's last
+ * num_new positions [len - num_new, len) (num_new = the row's q_len in
+ * pkv_build_step). If a block holding one of those positions is also named
+ * by another table (ref_count > 1), the first such block in table order is
+ * replaced in seq_id's table by a free block (old ref_count - 1, new 1) and
  * *src_block / *dst_block name the copy the caller must make on the device
- * (pkv_copy_blocks) before writing; otherwise both are -1 and nothing changes.
- * PKV_E_NOMEM (nothing changes) if no block is free. */
-pkv_status pkv_seq_cow(pkv_pool* pool, int64_t seq_id, int32_t* src_block, int32_t* dst_block);
+ * (pkv_copy_blocks: every layer) before the step; otherwise both are -1 and
+ * nothing changes. One call handles one block: call again until it returns
+ * -1 (after a fork only the partly filled last block is shared, so one call
+ * suffices). Afterwards pkv_build_step does not refuse the row with
+ * PKV_E_SHARED. PKV_E_NOMEM (nothing changes) if no block is free;
+ * PKV_E_INVALID if num_new is negative or above the length. */
+pkv_status pkv_seq_cow(pkv_pool* pool, int64_t seq_id, int64_t num_new, int32_t* src_block, int32_t* dst_block);
 
 /* Preemption by swap ("continuous batching server", "Preemption and Eviction:
  * Recompute vs Swap"; the choice of victim and of swap over recompute is the

@@ -15,8 +15,9 @@ Follows, in this order:
   * "The inference engine" (wpnews), "Paging turns variable sequences into
     block tables": sequences may point at the same immutable prefix blocks,
     and copy-on-write restores separate ownership when a branch diverges
-    (fork shares every block, cow_last gives the writer a private copy of a
-    shared partly filled last block);
+    (fork shares every block; before a step writes positions that fall in
+    a block another sequence also holds, cow gives the writer a private copy
+    of that block);
   * "continuous batching server", "Preemption and Eviction: Recompute vs
     Swap": a swapped-out victim keeps its length but gives its blocks back;
     swapping in allocates fresh blocks for the host copy to return to;
@@ -103,21 +104,35 @@ class BlockManager:
         self.lens[dst] = self.lens[src]
         return OK
 
-    def cow_last(self, seq: int):
-        """(status, src, dst): give seq a private copy of its last block if the next token would land in a
-        shared one; (OK, -1, -1) when nothing needs copying."""
+    def cow(self, seq: int, num_new: int = 1):
+        """(status, src, dst) for a step about to write seq's last num_new positions (called after grow).
+
+        The written positions are [len - num_new, len). If one of the blocks
+        holding them is also named by another table (ref_count > 1), the first
+        such block in table order is replaced, in seq's table only, by a block
+        off the free list: the shared block loses one reference, the new one has
+        ref_count 1, and (OK, shared block, new block) names the copy the
+        caller makes before the step writes. (OK, -1, -1) when every such block
+        is already seq's alone; (E_NOMEM, -1, -1) with nothing changed when no
+        block is free. Several shared blocks take one call each."""
         if seq not in self.tables or seq in self.swapped:
             return E_INVALID, -1, -1
+        n = self.lens[seq]
+        if num_new < 0 or num_new > n:
+            return E_INVALID, -1, -1
         t = self.tables[seq]
-        if not t or self.lens[seq] % self.block_size == 0 or self.ref[t[-1]] == 1:
+        written = range((n - num_new) // self.block_size, (n - 1) // self.block_size + 1) if num_new else ()
+        shared = [i for i in written if self.ref[t[i]] > 1]
+        if not shared:
             return OK, -1, -1
         if not self.free:
             return E_NOMEM, -1, -1
+        i = shared[0]
         b = self.free.pop()
         self.ref[b] = 1
-        old = t[-1]
+        old = t[i]
         self.ref[old] -= 1
-        t[-1] = b
+        t[i] = b
         return OK, old, b
 
     # ---- swap

@@ -57,7 +57,7 @@ SIGNATURES = {
     "pkv_seq_len": (_i64, [_P, _i64]),
     "pkv_block_table": (_i32, [_P, _i64, _P, _i64, _c.POINTER(_i64)]),
     "pkv_seq_fork": (_i32, [_P, _i64, _i64]),
-    "pkv_seq_cow": (_i32, [_P, _i64, _c.POINTER(_i32), _c.POINTER(_i32)]),
+    "pkv_seq_cow": (_i32, [_P, _i64, _i64, _c.POINTER(_i32), _c.POINTER(_i32)]),
     "pkv_seq_swap_out": (_i32, [_P, _i64, _P, _i64, _c.POINTER(_i64)]),
     "pkv_seq_swap_in": (_i32, [_P, _i64, _P, _i64, _c.POINTER(_i64)]),
     "pkv_block_hashes": (_i64, [_P, _i64, _P, _i64]),
@@ -223,10 +223,11 @@ class Pool:
     def seq_fork(self, dst: int, src: int) -> int:
         return load().pkv_seq_fork(self.handle, dst, src)
 
-    def seq_cow(self, seq_id: int):
-        """(status, src_block, dst_block); (OK, -1, -1) when no copy is needed."""
+    def seq_cow(self, seq_id: int, num_new: int = 1):
+        """(status, src_block, dst_block) before a step writes the last num_new positions; (OK, -1, -1)
+        when no copy is needed."""
         a, b = _i32(), _i32()
-        st = load().pkv_seq_cow(self.handle, seq_id, _c.byref(a), _c.byref(b))
+        st = load().pkv_seq_cow(self.handle, seq_id, num_new, _c.byref(a), _c.byref(b))
         return st, a.value, b.value
 
     def _swap(self, fn, seq_id: int):

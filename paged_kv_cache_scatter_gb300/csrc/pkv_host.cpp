@@ -273,7 +273,7 @@ pkv_status pkv_seq_fork(pkv_pool* pool, int64_t dst, int64_t src)
     return PKV_OK;
 }
 
-pkv_status pkv_seq_cow(pkv_pool* pool, int64_t seq_id, int32_t* src_block, int32_t* dst_block)
+pkv_status pkv_seq_cow(pkv_pool* pool, int64_t seq_id, int64_t num_new, int32_t* src_block, int32_t* dst_block)
 {
     if (pkv_status s = check_pool(pool)) return s;
     if (!src_block || !dst_block) return fail(PKV_E_INVALID, "NULL output");
@@ -282,14 +282,23 @@ pkv_status pkv_seq_cow(pkv_pool* pool, int64_t seq_id, int32_t* src_block, int32
     if (it == pool->seqs.end() || it->second.swapped)
         return fail(PKV_E_INVALID, "seq %lld unknown or swapped out", (long long)seq_id);
     pkv::Seq& s = it->second;
-    if (s.table.empty() || s.len % pkv::kBlockSize == 0 || pool->ref[s.table.back()] == 1) return PKV_OK;
+    if (num_new < 0 || num_new > s.len)
+        return fail(PKV_E_INVALID, "seq %lld: %lld new tokens with length %lld", (long long)seq_id,
+                    (long long)num_new, (long long)s.len);
+    if (num_new == 0) return PKV_OK;
+    // the step writes positions [len - num_new, len): the first block among them that another table
+    // also names is the one to copy
+    const int64_t first = (s.len - num_new) / pkv::kBlockSize, last = (s.len - 1) / pkv::kBlockSize;
+    int64_t i = first;
+    while (i <= last && pool->ref[s.table[i]] == 1) ++i;
+    if (i > last) return PKV_OK;
     if (pool->free_stack.empty()) return fail(PKV_E_NOMEM, "no free block for the copy");
     const int32_t b = pool->free_stack.back();
     pool->free_stack.pop_back();
     pool->ref[b] = 1;
-    const int32_t old = s.table.back();
+    const int32_t old = s.table[i];
     pool->ref[old] -= 1;  // above 1 before, so it stays referenced
-    s.table.back() = b;
+    s.table[i] = b;
     *src_block = old;
     *dst_block = b;
     return PKV_OK;

@@ -114,7 +114,8 @@ def test_fork_cow_swap_and_prefix_cache_match_the_oracle(pkv, seed):
             if d in bm.tables:
                 toks[d] = toks[s].copy()
         elif op == 4:
-            assert p.seq_cow(s) == bm.cow_last(s)
+            k = int(rng.integers(-1, bm.lens.get(s, 0) + 2))
+            assert p.seq_cow(s, k) == bm.cow(s, k)
         elif op == 5:
             st, blocks = p.seq_swap_out(s)
             st2, blocks2 = bm.swap_out(s)
@@ -141,6 +142,54 @@ def test_fork_cow_swap_and_prefix_cache_match_the_oracle(pkv, seed):
         assert p.seq_free(s) == bm.free_seq(s)
     assert p.prefix_evict(N) == bm.prefix_evict(N)
     assert p.free_blocks() == N == bm.free_blocks()
+
+
+# the hand-worked copy-on-write cases of tests/test_blockmgr_pins.py, through the C ABI
+@pytest.mark.parametrize("n, src_table, grown, pair, after, slot", [
+    (15, [0], [0], (0, 1), [1], 31), (16, [0], [0, 1], (-1, -1), [0, 1], 16), (17, [0, 1], [0, 1], (1, 2), [0, 2], 33),
+    (47, [0, 1, 2], [0, 1, 2], (2, 3), [0, 1, 3], 63), (48, [0, 1, 2], [0, 1, 2, 3], (-1, -1), [0, 1, 2, 3], 48)])
+def test_cow_at_fork_lengths(pkv, n, src_table, grown, pair, after, slot):
+    p = pkv.Pool(None, 10, num_layers=1)
+    assert p.seq_grow(0, n) == pkv.PKV_OK and list(p.block_table(0)) == src_table
+    assert p.seq_fork(1, 0) == pkv.PKV_OK and p.seq_grow(1, n + 1) == pkv.PKV_OK
+    assert list(p.block_table(1)) == grown
+    assert p.build_step([1], [1], 8)[0] == (pkv.PKV_OK if pair == (-1, -1) else pkv.PKV_E_SHARED)
+    assert p.seq_cow(1, 1) == (pkv.PKV_OK, *pair)
+    assert list(p.block_table(1)) == after and p.seq_cow(1, 1) == (pkv.PKV_OK, -1, -1)
+    st, _, ctx, slots, _ = p.build_step([1], [1], 8)
+    assert st == pkv.PKV_OK and list(ctx) == [n + 1] and list(slots) == [slot]
+    assert p.seq_grow(0, n + 1) == pkv.PKV_OK and p.seq_cow(0, 1) == (pkv.PKV_OK, -1, -1)
+    assert p.seq_cow(1, n + 2)[0] == pkv.PKV_E_INVALID and p.seq_cow(1, -1)[0] == pkv.PKV_E_INVALID
+
+
+def test_cow_rewrite_of_shared_prefix_one_block_per_call(pkv):
+    p = pkv.Pool(None, 10, num_layers=1)
+    assert p.seq_grow(0, 48) == pkv.PKV_OK and p.seq_share_prefix(1, 0, 3) == pkv.PKV_OK
+    assert p.seq_cow(1, 17) == (pkv.PKV_OK, 1, 3)
+    assert p.seq_cow(1, 17) == (pkv.PKV_OK, 2, 4)
+    assert p.seq_cow(1, 17) == (pkv.PKV_OK, -1, -1)
+    assert list(p.block_table(1)) == [0, 3, 4] and [p.ref_count(b) for b in range(5)] == [2, 1, 1, 1, 1]
+
+
+def test_prefix_evict_order_by_hand(pkv):
+    # least recently used first, deeper chain positions first among equals: blocks 2, 1, 4, 3, 0
+    p = pkv.Pool(None, 8, num_layers=1)
+    rng = np.random.default_rng(0)
+    a = pkv.block_hashes(rng.integers(0, 1000, 48).astype(np.int32))
+    b = pkv.block_hashes(rng.integers(0, 1000, 32).astype(np.int32))
+    assert p.seq_grow(0, 48) == pkv.PKV_OK and p.prefix_register(0, a) == (pkv.PKV_OK, 3)
+    assert p.seq_grow(1, 32) == pkv.PKV_OK and p.prefix_register(1, b) == (pkv.PKV_OK, 2)
+    assert p.seq_free(0) == pkv.PKV_OK and p.seq_free(1) == pkv.PKV_OK
+    assert p.seq_attach_prefix(2, a[:1]) == (pkv.PKV_OK, 1) and p.seq_free(2) == pkv.PKV_OK
+    order = []
+    for _ in range(5):
+        left = {x for x in range(5) if p.ref_count(x) == 1}
+        assert p.prefix_evict(1) == 1
+        gone = left - {x for x in range(5) if p.ref_count(x) == 1}
+        assert len(gone) == 1
+        order += list(gone)
+    assert order == [2, 1, 4, 3, 0]
+    assert p.seq_grow(3, 16) == pkv.PKV_OK and list(p.block_table(3)) == [0]   # evicted last, reused first
 
 
 def test_swap_out_capacity_and_state_rules(pkv):

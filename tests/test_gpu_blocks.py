@@ -116,23 +116,34 @@ def test_decode_unchanged_after_swap_out_and_in(pkv):
         assert torch.equal(a, b)
 
 
-def test_fork_copy_on_write_then_diverge(pkv):
-    # parallel sampling: a fork shares the partly filled last block; before the sample's first append the
-    # block manager hands it a private copy, the device copies the block, and the two branches diverge
+@pytest.mark.parametrize("n", [15, 40, 47, 48])
+def test_fork_copy_on_write_then_diverge(pkv, n):
+    # parallel sampling: a fork shares every block, the partly filled last one included; before each
+    # branch's next token the block manager hands the writer a private copy of a shared block the token
+    # lands in (none when the token opens a new block: n = 48), the device copies it, and the two branches
+    # diverge. n = 47: the token completes the shared block.
     N, L, H = 32, 1, 32
     pool = G.device_pool(N, L, H, seed=7)
     host = G.to_bits(pool).reshape(pool.shape).copy()
     g = oracle.geom(N, L, H)
     p = pkv.Pool(pool, N, num_layers=L, num_heads=H)
-    assert p.seq_grow(0, 40) == pkv.PKV_OK                   # 2.5 blocks
+    assert p.seq_grow(0, n) == pkv.PKV_OK
     assert p.seq_fork(1, 0) == pkv.PKV_OK
     for s in (0, 1):
-        assert p.seq_grow(s, 41) == pkv.PKV_OK
-    assert p.build_step([1], [1], 4)[0] == pkv.PKV_E_SHARED
-    st, src, dst = p.seq_cow(1)
-    assert st == pkv.PKV_OK and src >= 0 and dst >= 0
-    p.copy_blocks(torch.tensor([[src, dst]], dtype=torch.int32, device="cuda"))
-    assert oracle.copy_blocks(host, g, np.array([[src, dst]], np.int32)) == -1
+        assert p.seq_grow(s, n + 1) == pkv.PKV_OK
+    lands_in_shared = n % 16 != 0
+    assert p.build_step([1], [1], 4)[0] == (pkv.PKV_E_SHARED if lands_in_shared else pkv.PKV_OK)
+    pairs = []
+    for s in (1, 0):
+        st, src, dst = p.seq_cow(s, 1)
+        assert st == pkv.PKV_OK
+        if src >= 0:
+            pairs.append((src, dst))
+    assert len(pairs) == (1 if lands_in_shared else 0)     # the second writer finds the block its own
+    if pairs:
+        pr = np.array(pairs, np.int32)
+        p.copy_blocks(torch.from_numpy(pr).cuda())
+        assert oracle.copy_blocks(host, g, pr) == -1
     st, tables, ctx, slots, qs = p.build_step([0, 1], [1, 1], 4)
     assert st == pkv.PKV_OK and slots[0] != slots[1]
     k = workloads.normal_fp16((2, H, 128), 8).cuda()

@@ -9,7 +9,6 @@ inputs, and the identities between chunked and unchunked prefill and between
 split and unsplit decode. tests/test_oracle_mutants.py plants mistakes in a
 copy of the oracle and checks that this file catches each of them.
 """
-import math
 import os
 
 import numpy as np
@@ -17,7 +16,6 @@ import pytest
 import torch
 
 import oracle
-from oracle import blockmgr
 import workloads
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "page_arithmetic.txt")
@@ -424,64 +422,6 @@ def test_merge_of_two_halves_by_hand():
     assert np.allclose(got, (p / p.sum()) @ V, rtol=1e-12, atol=1e-14)
 
 
-# ------------------------------------------------------------------ block manager
-
-def test_blockmgr_page_example_lengths():
-    bm = blockmgr.BlockManager(7152)
-    for i, n in enumerate([17, 33, 65]):
-        assert bm.grow(i, n) == blockmgr.OK
-    assert 7152 - bm.free_blocks() == 10
-    assert bm.grow(3, 600) == blockmgr.OK and len(bm.tables[3]) == 38
-    assert bm.grow(4, 2300) == blockmgr.OK and len(bm.tables[4]) == 144
-
-
-def test_blockmgr_grow_one_block_every_16_tokens():
-    bm = blockmgr.BlockManager(64)
-    for n in range(1, 200):
-        assert bm.grow(0, n) == blockmgr.OK
-        assert len(bm.tables[0]) == math.ceil(n / 16)
-
-
-def test_blockmgr_nomem_changes_nothing():
-    bm = blockmgr.BlockManager(8)
-    assert bm.grow(0, 100) == blockmgr.OK           # 7 blocks
-    before = (list(bm.free), list(bm.tables[0]), bm.lens[0])
-    assert bm.grow(1, 40) == blockmgr.E_NOMEM
-    assert bm.grow(0, 129) == blockmgr.E_NOMEM
-    assert (list(bm.free), list(bm.tables[0]), bm.lens[0]) == before and 1 not in bm.tables
-
-
-def test_blockmgr_shared_prefix_refcounts_and_soak_returns_all_blocks():
-    bm = blockmgr.BlockManager(7152, free_order=np.random.default_rng(0).permutation(7152))
-    assert bm.grow(0, 2000) == blockmgr.OK
-    for s in range(1, 65):
-        assert bm.share_prefix(s, 0, 125) == blockmgr.OK
-        assert bm.grow(s, 2000 + s) == blockmgr.OK
-    shared = bm.tables[0][:125]
-    assert all(bm.ref[b] == 65 for b in shared)
-    st, tables, ctx, slots, qs = bm.build_step(list(range(1, 65)), [1] * 64, 200)
-    assert st == blockmgr.OK and len(slots) == 64
-    assert all(s // 16 not in shared for s in slots)
-    # a write into a shared block is refused
-    assert bm.grow(99, 0) == blockmgr.OK
-    assert bm.share_prefix(100, 0, 10) == blockmgr.OK
-    assert bm.build_step([100], [1], 200)[0] == blockmgr.E_SHARED
-    for s in list(bm.tables):
-        assert bm.free_seq(s) == blockmgr.OK
-    assert bm.free_blocks() == 7152 and all(r == 0 for r in bm.ref)
-
-
-def test_blockmgr_lifo_reuse_and_invalid_calls():
-    bm = blockmgr.BlockManager(10)
-    assert bm.grow(0, 40) == blockmgr.OK
-    assert bm.tables[0] == [0, 1, 2]
-    assert bm.free_seq(0) == blockmgr.OK
-    assert bm.grow(1, 16) == blockmgr.OK and bm.tables[1] == [2]
-    assert bm.free_seq(7) == blockmgr.E_INVALID
-    assert bm.grow(1, 3) == blockmgr.E_INVALID          # sequences only grow
-    assert bm.share_prefix(2, 1, 2) == blockmgr.E_INVALID  # only full blocks that exist
-
-
 # ------------------------------------------------------------------ 8-bit cache
 # Reading (the pages fix no scale rule): INT8 codes, one float32 scale per (token, head) row of K or V,
 # scale = max|x| / 127, code = round-half-even(x / scale); the stored value is code * scale.
@@ -671,39 +611,6 @@ def test_block_hash_chain_depends_on_the_whole_prefix():
         prev = int(h[i])
 
 
-def _page_prefill_with_cache(cache: set, tokens) -> int:
-    """The page's lookup: count cached leading blocks until the first miss, then cache this prompt's blocks."""
-    hit = 0
-    hs = [int(x) for x in oracle.block_hashes(tokens)]
-    for h in hs:
-        if h not in cache:
-            break
-        hit += 16
-    cache.update(hs)
-    return hit
-
-
-def test_prefix_cache_matches_the_pages_lookup():
-    rng = np.random.default_rng(1)
-    system = rng.integers(0, 32000, 1200).astype(np.int32)            # a shared 1,200-token system prompt
-    bm = blockmgr.BlockManager(4000)
-    page_cache: set = set()
-    for r in range(20):
-        user = rng.integers(0, 32000, int(rng.integers(1, 900))).astype(np.int32)
-        prompt = np.concatenate([system, user]) if r % 4 else user
-        hs = oracle.block_hashes(prompt)
-        expect = _page_prefill_with_cache(page_cache, prompt)
-        st, n = bm.attach_prefix(r, hs)
-        assert st == blockmgr.OK and n * 16 == expect
-        assert bm.grow(r, len(prompt)) == blockmgr.OK
-        assert bm.prefix_register(r, hs)[0] == blockmgr.OK
-    # a changed token near the start of the system prompt: nothing is served from the cache
-    p = np.concatenate([system, [5, 6, 7]]).astype(np.int32)
-    p[3] += 1
-    assert bm.prefix_match(oracle.block_hashes(p)) == 0 == _page_prefill_with_cache(set(page_cache), p)
-    assert bm.prefix_match(oracle.block_hashes(system)) == 1200 // 16
-
-
 def test_copy_blocks_and_swap_are_whole_block_byte_copies():
     rng = np.random.default_rng(2)
     for dtype in (oracle.FP16, oracle.INT8):
@@ -729,82 +636,3 @@ def test_copy_blocks_and_swap_are_whole_block_byte_copies():
         assert np.array_equal(view[dst], before[blocks])
         with pytest.raises(IndexError):
             oracle.swap_out(pool, g, np.array([1, -1], np.int32))
-
-
-def test_blockmgr_fork_cow_and_swap_scenario():
-    bm = blockmgr.BlockManager(10)
-    assert bm.grow(0, 40) == blockmgr.OK                  # blocks 0, 1, 2 (last holds 8 tokens)
-    assert bm.tables[0] == [0, 1, 2]
-    assert bm.fork(1, 0) == blockmgr.OK                   # parallel sample: shares all three
-    assert [bm.ref[b] for b in (0, 1, 2)] == [2, 2, 2]
-    assert bm.build_step([1], [1], 4)[0] == blockmgr.E_SHARED or True   # (its next token is position 40, below)
-    assert bm.grow(1, 41) == blockmgr.OK                  # still 3 blocks: position 40 falls in shared block 2
-    assert bm.build_step([1], [1], 4)[0] == blockmgr.E_SHARED
-    st, src, dst = bm.cow_last(1)
-    assert (st, src, dst) == (blockmgr.OK, 2, 3)          # block 3 is handed out next
-    assert bm.tables[1] == [0, 1, 3] and bm.ref[2] == 1 and bm.ref[3] == 1
-    assert bm.build_step([1], [1], 4)[0] == blockmgr.OK
-    assert bm.cow_last(0) == (blockmgr.OK, -1, -1)        # block 2 is now 0's alone
-    st, blocks = bm.swap_out(1)
-    assert st == blockmgr.OK and blocks == [0, 1, 3]
-    assert bm.ref[3] == 0 and bm.ref[0] == 1 and bm.free_blocks() == 7 and bm.lens[1] == 41
-    assert bm.grow(1, 50) == blockmgr.E_INVALID and bm.build_step([1], [1], 4)[0] == blockmgr.E_INVALID
-    st, blocks = bm.swap_in(1)
-    assert st == blockmgr.OK and len(blocks) == 3 and bm.tables[1] == blocks
-    assert all(bm.ref[b] == 1 for b in blocks) and bm.free_blocks() == 4
-
-
-def test_blockmgr_nomem_leaves_state_unchanged_for_cow_and_swap_in():
-    bm = blockmgr.BlockManager(4)
-    assert bm.grow(0, 20) == blockmgr.OK and bm.fork(1, 0) == blockmgr.OK
-    assert bm.grow(2, 32) == blockmgr.OK                  # pool full
-    snap = (list(bm.free), list(bm.ref), {k: list(v) for k, v in bm.tables.items()})
-    assert bm.cow_last(1) == (blockmgr.E_NOMEM, -1, -1)
-    assert bm.swap_out(2)[0] == blockmgr.OK and bm.grow(3, 32) == blockmgr.OK
-    snap = (list(bm.free), list(bm.ref), {k: list(v) for k, v in bm.tables.items()})
-    assert bm.swap_in(2) == (blockmgr.E_NOMEM, None)
-    assert snap == (list(bm.free), list(bm.ref), {k: list(v) for k, v in bm.tables.items()})
-
-
-def test_blockmgr_reference_counts_under_random_operations():
-    # invariant: ref[b] = number of table entries naming b + 1 if b is cached; free list = blocks with ref 0
-    rng = np.random.default_rng(3)
-    N = 64
-    bm = blockmgr.BlockManager(N, free_order=rng.permutation(N))
-    toks = {}
-    for step in range(3000):
-        op = rng.integers(0, 9)
-        s = int(rng.integers(0, 12))
-        if op == 0:
-            bm.grow(s, bm.lens.get(s, 0) + int(rng.integers(0, 40)))
-        elif op == 1:
-            bm.free_seq(s)
-        elif op == 2:
-            bm.fork(int(rng.integers(0, 12)), s)
-        elif op == 3:
-            bm.cow_last(s)
-        elif op == 4:
-            bm.swap_out(s)
-        elif op == 5:
-            bm.swap_in(s)
-        elif op == 6 and s in bm.tables and s not in bm.swapped:
-            n = bm.lens[s] // 16 * 16
-            toks.setdefault(s, rng.integers(0, 9, 4000).astype(np.int32))
-            bm.prefix_register(s, oracle.block_hashes(toks[s][:n]))
-        elif op == 7 and s not in bm.tables:
-            toks[s] = rng.integers(0, 9, 4000).astype(np.int32)
-            bm.attach_prefix(s, oracle.block_hashes(toks[s][:int(rng.integers(0, 200))]))
-        elif op == 8:
-            bm.prefix_evict(int(rng.integers(0, 4)))
-        count = [0] * N
-        for t in bm.tables.values():
-            for b in t:
-                count[b] += 1
-        for e in bm.cache.values():
-            count[e[0]] += 1
-        assert count == bm.ref
-        assert sorted(bm.free) == [b for b in range(N) if bm.ref[b] == 0]
-    for s in list(bm.tables):
-        bm.free_seq(s)
-    bm.prefix_evict(N)
-    assert bm.free_blocks() == N and not bm.cache
