@@ -27,8 +27,11 @@
  *     pkv_get_status() reads. No C++ exception crosses this boundary.
  *   - Threads: a pool is not thread-safe; one scheduler thread owns it
  *     ("llm-inference-batching", step 3: one scheduler thread owns the GPU).
- *   - Supported geometry: head_dim 128, block_size 16, FP16, any number of
- *     layers (1..1024) and heads (1..256). Query heads equal K/V heads.
+ *   - Supported geometry: head_dim 128, block_size 16, FP16 or 8-bit
+ *     (PKV_DTYPE_INT8) elements, any number of layers (1..1024) and K/V heads
+ *     (1..256). num_q_heads is a multiple of the K/V heads (grouped-query
+ *     and multi-query attention: query head h reads K/V head
+ *     h / (num_q_heads / num_heads)), at most 1,024.
  */
 #ifndef PKV_H
 #define PKV_H
@@ -58,11 +61,11 @@ typedef enum pkv_status {
  * single precision; attention reads code * scale. kv_append quantises,
  * decode attention dequantises in its loaders (tensor cores: codes become
  * FP16 exactly, the K scale multiplies the scores, the V scale folds into the
- * softmax weights, which are rounded to FP16). Prefill attention dequantises
- * in its loaders too: each 128-key tile's codes and scales arrive by TMA and
- * become FP16 code * scale in shared memory (the scale applied as an FP16
- * pair hi + lo, so the product's rounding to FP16 is the only one) before the
- * tensor cores read them. */
+ * softmax weights, which are rounded to FP16). Prefill attention does the
+ * same: each 128-key tile's codes arrive by TMA and become exact FP16 codes
+ * in shared memory for the tensor cores; the row scales arrive beside them
+ * and are applied in FP32 in the softmax (K scales to the scores, V scales to
+ * the weights before their rounding to FP16), never to the operands. */
 enum { PKV_DTYPE_FP16 = 0, PKV_DTYPE_INT8 = 1 };
 
 /* Bits of the sticky device error word (pkv_get_status). */
@@ -323,18 +326,26 @@ pkv_status pkv_prefill_attn(pkv_pool* pool, int32_t layer, const void* q, const 
  * synchronise the device and stall every stream.
  *
  *   - Limit: the scratch pkv_decode_workspace_bytes(pool, num_seqs,
- *     max_blocks) would report must fit in 16 MiB (with 32 heads and
- *     512-token partitions: num_seqs x ceil(16 x max_blocks / 512) <= ~1,000,
- *     e.g. 32 rows with tables up to 992 blocks). Larger requests are refused
- *     with PKV_E_INVALID and a message, before anything is launched.
+ *     max_blocks) would report must fit in 16 MiB. That is about
+ *     num_seqs x num_q_heads x P x 520 B <= 16 MiB with
+ *     P = ceil(16 x max_blocks / partition_tokens), the pool's partition
+ *     length (1,024 tokens by default): with 32 query heads, num_seqs x P
+ *     <= ~1,000, e.g. 32 rows with tables up to 1,984 blocks at the default,
+ *     or up to 992 blocks for a pool created with 512-token partitions.
+ *     Larger requests are refused with PKV_E_INVALID and a message, before
+ *     anything is launched.
  *   - The first call on a device looks up the array's device address
- *     (cudaGetSymbolAddress, with that device current); make that first call
- *     before any stream capture.
+ *     (cudaGetSymbolAddress, with that device current) and keeps it for the
+ *     rest of the process; make that first call before any stream capture.
+ *     Do not use this entry point on a device after cudaDeviceReset (or any
+ *     other reset of its primary context) in the same process: the kept
+ *     address would be stale.
  *   - Every call on a device shares the one array and overwrites it. Calls
  *     whose kernels overlap on the GPU (other streams, other threads) race
- *     and give wrong results; serialise them. Nothing in it needs clearing
- *     between calls. No cudaMalloc, cudaFree or allocating library routine
- *     is called. */
+ *     and give wrong results; serialise them. Each call clears the array's
+ *     arrival counters on its stream (a memset, not an allocation) before its
+ *     kernel. No cudaMalloc, cudaFree or allocating library routine is
+ *     called. */
 pkv_status pkv_decode_attn_noalloc(pkv_pool* pool, int32_t layer, const void* q, const int32_t* block_tables,
                                    int32_t max_blocks, const int32_t* ctx_lens, int32_t num_seqs, float scale,
                                    void* out, void* stream);

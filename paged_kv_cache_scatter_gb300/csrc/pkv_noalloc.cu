@@ -3,6 +3,8 @@
 // instead of a caller-provided workspace.
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include "pkv_internal.h"
 
 namespace {
@@ -14,13 +16,16 @@ constexpr size_t kScratchBytes = size_t(16) << 20;  // 16 MiB per GPU, held unti
 static __device__ __align__(256) unsigned char g_decode_scratch[kScratchBytes];
 
 constexpr int kMaxDevices = 64;
-void* g_scratch_addr[kMaxDevices] = {};
+// Atomic so that two host threads making their first call on the same device at once do not race: both look
+// the (same) address up and both store it.
+std::atomic<void*> g_scratch_addr[kMaxDevices] = {};
 
 // First call on a device: make it current and look the array's address up.
 pkv_status scratch_for_device(int device, void** out)
 {
     if (device < 0 || device >= kMaxDevices) return pkv::fail(PKV_E_INVALID, "device ordinal %d unsupported", device);
-    if (!g_scratch_addr[device]) {
+    void* cached = g_scratch_addr[device].load(std::memory_order_acquire);
+    if (!cached) {
         int prev = -1;
         cudaError_t e = cudaGetDevice(&prev);
         if (e != cudaSuccess) return pkv::cuda_fail(e, "cudaGetDevice");
@@ -29,9 +34,10 @@ pkv_status scratch_for_device(int device, void** out)
         e = cudaGetSymbolAddress(&p, g_decode_scratch);
         if (prev != device) cudaSetDevice(prev);
         if (e != cudaSuccess || !p) return pkv::cuda_fail(e, "cudaGetSymbolAddress(decode scratch)");
-        g_scratch_addr[device] = p;
+        g_scratch_addr[device].store(p, std::memory_order_release);
+        cached = p;
     }
-    *out = g_scratch_addr[device];
+    *out = cached;
     return PKV_OK;
 }
 
@@ -53,7 +59,8 @@ extern "C" pkv_status pkv_decode_attn_noalloc(pkv_pool* pool, int32_t layer, con
                          num_seqs, max_blocks, need, kScratchBytes);
     void* scratch = nullptr;
     if (pkv_status s = scratch_for_device(pool->device, &scratch)) return s;
-    // The partials are written before they are read, so nothing needs clearing.
+    // pkv_decode_attn clears the scratch's per-(row, head) arrival counters on the stream (a memset, no
+    // allocation) before its kernel; the partial outputs are written before they are read.
     return pkv_decode_attn(pool, layer, q, block_tables, max_blocks, ctx_lens, num_seqs, scale, out, scratch,
                            kScratchBytes, stream);
 }
