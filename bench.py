@@ -255,6 +255,77 @@ def kv_bytes(wl, layers, dtype="fp16") -> int:
 
 # ------------------------------------------------------------------ ours
 
+def prefill_chunk_summary(chunks, hbm_peak, tf_peak, peak_kind):
+    """Roofline of the prefill kernel over a chunk schedule. chunks: (iteration workload, microseconds per
+    launch, query heads, K/V heads, bytes per K/V row) per chunk. Each chunk is held against the tensor peak
+    (FLOPs of its unmasked (q, k) pairs) and the HBM peak (its K/V prefix read once, q read, out written);
+    a chunk whose FLOPs per byte sit below the ridge tf_peak / hbm_peak is HBM-bound."""
+    per, fl_tot, us_tot = [], 0.0, 0.0
+    ridge = tf_peak * 1e12 / (hbm_peak * 1e9)
+    for wl, us, hq, hkv, rb in chunks:
+        fl = 4 * HEAD_DIM * hq * prefill_pairs(wl)
+        B = wl.num_decode
+        by = sum(int(c) * 2 * hkv * rb + 2 * int(q) * hq * HEAD_DIM * 2
+                 for c, q in zip(wl.ctx_lens[B:], wl.q_lens[B:]))
+        tf = fl / (us * 1e-6) / 1e12
+        gbs = by / (us * 1e-6) / 1e9
+        per.append({"chunk": int(wl.meta.get("chunk", len(per))), "us": round(us, 2), "tflops": round(tf, 1),
+                    "frac": round(tf / tf_peak, 4), "gbs": round(gbs, 1), "hbm_frac": round(gbs / hbm_peak, 4),
+                    "bound": "tensor" if fl / by >= ridge else "hbm"})
+        fl_tot += fl
+        us_tot += us
+    agg = fl_tot / (us_tot * 1e-6) / 1e12
+    return {"bound": "tensor", "achieved": round(agg, 1), "peak": tf_peak,
+            "peak_kind": peak_kind + " bf16 dense (fp16 runs at the same rate)", "unit": "TFLOP/s",
+            "frac": round(agg / tf_peak, 4),
+            "aggregate": {"chunks": len(per), "us_per_layer": round(us_tot, 2), "tflops": round(agg, 1),
+                          "frac": round(agg / tf_peak, 4)},
+            "per_chunk": per}
+
+
+def prefill_schedule(torch, pkv, pool, L, dev, gen, steps, stream, hbm_peak, tf_peak, peak_kind):
+    """The prefill kernel alone over the 4,000-token prompt's 8-chunk schedule (the mixed_prefill workload's
+    prefill rows, 32 heads), on this run's pool: per chunk a CUDA graph of its L per-layer launches, replayed
+    `steps` times between two events on the launching stream; per-launch time = elapsed / (steps x L)."""
+    iters = _iterations("mixed_prefill")
+    datas = [StepData(torch, pkv, pool, wl, m, L, dev, gen) for wl, m in zip(iters, _metadata(pkv, iters))]
+    graphs = []
+    for d in datas:
+        tables_d, ctx_d, qs_d, _ = d.dev
+        g = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(stream)
+        with torch.cuda.graph(g, stream=cap, capture_error_mode="thread_local"):
+            for l in range(L):
+                pool.prefill_attn(l, d.q[l], qs_d[d.B:], tables_d[d.B:], ctx_d[d.B:], d.max_q, SCALE, d.out[l],
+                                  torch.cuda.current_stream(dev))
+        graphs.append(g)
+    torch.cuda.synchronize(dev)
+    for g in graphs:
+        g.replay()
+    torch.cuda.synchronize(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in graphs]
+    for (a, b), g in zip(ev, graphs):
+        a.record(stream)
+        for _ in range(steps):
+            g.replay()
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+    st, flags = pool.get_status(stream)
+    if st != pkv.PKV_OK:
+        raise RuntimeError(f"device status {st} flags {flags:#x}")
+    chunks = [(d.wl, a.elapsed_time(b) * 1e3 / (steps * L), d.wl.q_heads, d.wl.num_heads, row_bytes("fp16"))
+              for d, (a, b) in zip(datas, ev)]
+    res = prefill_chunk_summary(chunks, hbm_peak, tf_peak, peak_kind)
+    res["kernel"] = "prefill_kernel (tcgen05)"
+    res["workload"] = ("the mixed_prefill schedule's prefill rows: a 4,000-token prompt in 512-token chunks, "
+                       "32 layers x 32 heads x 128, on this run's 7,152-block pool")
+    res["timing"] = ("CUDA events around a graph of one chunk's prefill launches for all layers, replayed; "
+                     "per-launch = elapsed / (replays x layers)")
+    return res
+
+
+
 class StepData:
     """Device metadata and per-layer tensors of one engine iteration."""
 
@@ -279,7 +350,16 @@ class StepData:
                                        q=self.q, k=self.k, v=self.v, out=self.out, q_layer_stride=qstride,
                                        k_layer_stride=stride, v_layer_stride=stride, out_layer_stride=qstride)
         self.ws_bytes = pool.step_workspace_bytes(self.desc)
-        # one-layer steps (same kernels as the full step) for per-launch timing of decode-only iterations
+        # the iteration's decode rows alone, over all layers, as pkv_step runs them (one counter clear, then the
+        # layers' decode launches chained with programmatic dependencies): the per-kernel timing of decode
+        self.dec_desc = self.desc if wl.num_seqs == B else (
+            pkv.make_step_desc(num_decode=B, num_prefill=0, num_tokens=B, max_q_len=0, max_blocks=tables.shape[1],
+                               first_layer=0, num_layers=layers, scale=SCALE, block_tables=tables_d,
+                               ctx_lens=ctx_d, q_start_loc=qs_d, slot_mapping=slots_d, q=self.q, k=self.k, v=self.v,
+                               out=self.out, q_layer_stride=qstride, k_layer_stride=stride, v_layer_stride=stride,
+                               out_layer_stride=qstride) if B else None)
+        # one-layer steps (same kernels as the full step) for per-launch timing of decode-only iterations without
+        # graphs
         self.layer_desc = [
             pkv.make_step_desc(num_decode=B, num_prefill=0, num_tokens=T, max_q_len=0, max_blocks=tables.shape[1],
                                first_layer=l, num_layers=1, scale=SCALE, block_tables=tables_d, ctx_lens=ctx_d,
@@ -465,8 +545,13 @@ def run_ours(args):
                     cap = torch.cuda.Stream(dev)
                     cap.wait_stream(stream)
                     with torch.cuda.graph(g, stream=cap, capture_error_mode="thread_local"):
-                        for l in range(L):
-                            fn(s, l, torch.cuda.current_stream(dev))
+                        if fn is launch_dec and not cascade:
+                            # all layers' decode launches as pkv_step issues them: one counter clear, then the
+                            # layers chained with programmatic dependencies
+                            pool.step(s.dec_desc, wspace, torch.cuda.current_stream(dev))
+                        else:
+                            for l in range(L):
+                                fn(s, l, torch.cuda.current_stream(dev))
                 pair.append(g)
             kgraphs.append(pair)
         torch.cuda.synchronize(dev)
@@ -499,6 +584,13 @@ def run_ours(args):
                             b.record(stream)
                             lst.append((a, b, s, 1))
     torch.cuda.synchronize(dev)
+    hbm_peak, tf_peak, peak_kind = _peaks()
+    sched_roofline = None
+    if args.config == "average_decode" and not args.no_prefill_schedule and L == wl0.num_layers:
+        # the prefill kernel over the mixed workload's 8-chunk schedule, on this run's pool, inside the clock
+        # record (an extra key of the line: the headline stays decode)
+        sched_roofline = prefill_schedule(torch, pkv, pool, L, dev, gen, args.steps, stream, hbm_peak, tf_peak,
+                                          peak_kind)
     clocks = sampler.stop()
     check_status()
     dec_ms = sum(a.elapsed_time(b) for a, b, _, _ in dec_ev)
@@ -530,7 +622,6 @@ def run_ours(args):
 
     t_ms, e2e_ms = max_over_ranks([t_ms, e2e_ms], dist if ws > 1 else None, dev)
 
-    hbm_peak, tf_peak, peak_kind = _peaks()
     K = args.steps
     if has_decode:
         metric = "decode KV GB/s (KV bytes read per 32-layer iteration / iteration time) at batch 32"
@@ -576,22 +667,24 @@ def run_ours(args):
                                "avg_launch_us": round(dec_ms / n_dec * 1e3, 2)}
     if pre_ev:
         fl = 4 * HEAD_DIM * Hq * sum(prefill_pairs(s.wl) * n for _, _, s, n in pre_ev)
-        ach = fl / (pre_ms * 1e-3) / 1e12
         pre_kernel = ("prefill_kernel<8-bit> (tcgen05; codes by TMA become FP16 in shared memory, row scales "
                       "applied in the softmax)" if dtype == "int8" else "prefill_kernel (tcgen05)")
-        rooflines["prefill"] = {"bound": "tensor", "kernel": pre_kernel, "achieved": round(ach, 1),
-                                "peak": tf_peak, "peak_kind": peak_kind + " bf16 dense (fp16 runs at the same rate)",
-                                "unit": "TFLOP/s", "frac": round(ach / tf_peak, 4),
-                                "traffic": _traffic("prefill_attn", args.config),
-                                "algorithmic_flops_per_launch": int(fl / n_pre),
-                                "avg_launch_us": round(pre_ms / n_pre * 1e3, 2),
-                                "per_chunk_us": [round(sum(a.elapsed_time(b) for a, b, s2, _ in pre_ev if s2 is s)
-                                                       / max(1, sum(n for _, _, s2, n in pre_ev if s2 is s)) * 1e3, 2)
-                                                 for s in steps if s.max_q]}
+        chunks = []
+        for s in steps:
+            if s.max_q:
+                us = (sum(a.elapsed_time(b) for a, b, s2, _ in pre_ev if s2 is s)
+                      / max(1, sum(n for _, _, s2, n in pre_ev if s2 is s)) * 1e3)
+                chunks.append((s.wl, us, Hq, H, row_bytes(dtype)))
+        rooflines["prefill"] = prefill_chunk_summary(chunks, hbm_peak, tf_peak, peak_kind)
+        rooflines["prefill"].update({"kernel": pre_kernel, "traffic": _traffic("prefill_attn", args.config),
+                                     "algorithmic_flops_per_launch": int(fl / n_pre),
+                                     "avg_launch_us": round(pre_ms / n_pre * 1e3, 2)})
     kernel_timing = ("CUDA events around a graph of one kernel's launches for all layers, per-launch = elapsed / "
                      "layers" if graph is not None else "CUDA events around every launch")
     for r in rooflines.values():
         r["timing"] = kernel_timing
+    if sched_roofline is not None:
+        rooflines["prefill"] = sched_roofline
     dominant = "decode" if (dec_ms >= pre_ms and n_dec) else "prefill"
 
     result = {
@@ -922,6 +1015,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="launch each step directly instead of replaying a CUDA graph")
+    ap.add_argument("--no-prefill-schedule", action="store_true",
+                    help="average_decode: skip the extra prefill-kernel timing over the 8-chunk schedule")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--seed", type=int, default=0, help="seed of the workload's length and block draws")
     ap.add_argument("--partition-tokens", type=int, default=0,

@@ -782,9 +782,11 @@ size_t pkv_decode_cascade_workspace_bytes(const pkv_pool* pool, int32_t num_seqs
     return pkv::decode_workspace_bytes(num_seqs, pool->desc.num_q_heads, max_blocks, pool->partition_tokens, 1);
 }
 
-pkv_status pkv_prefill_attn(pkv_pool* pool, int32_t layer, const void* q, const int32_t* q_start_loc,
-                            const int32_t* block_tables, int32_t max_blocks, const int32_t* ctx_lens, int32_t num_seqs,
-                            int32_t max_q_len, float scale, void* out, void* stream)
+// wait_prev: the kernel waits for the stream's previous kernel before reading its inputs (always, except
+// in pkv_step after the decode launch, which writes nothing prefill reads).
+static pkv_status prefill_impl(pkv_pool* pool, int32_t layer, const void* q, const int32_t* q_start_loc,
+                               const int32_t* block_tables, int32_t max_blocks, const int32_t* ctx_lens,
+                               int32_t num_seqs, int32_t max_q_len, float scale, void* out, bool wait_prev, void* stream)
 {
     if (pkv_status s = check_device_pool(pool)) return s;
     if (pkv_status s = check_layer(pool, layer)) return s;
@@ -798,8 +800,16 @@ pkv_status pkv_prefill_attn(pkv_pool* pool, int32_t layer, const void* q, const 
     DeviceGuard dg(pool->device);
     if (!dg.ok) return fail(PKV_E_DEVICE, "cannot select the pool's device");
     cudaError_t e = pkv::launch_prefill(pool, layer, q, q_start_loc, block_tables, max_blocks, ctx_lens, num_seqs,
-                                        max_q_len, scale, out, static_cast<cudaStream_t>(stream));
+                                        max_q_len, scale, out, wait_prev, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PKV_OK : pkv::cuda_fail(e, "prefill launch");
+}
+
+pkv_status pkv_prefill_attn(pkv_pool* pool, int32_t layer, const void* q, const int32_t* q_start_loc,
+                            const int32_t* block_tables, int32_t max_blocks, const int32_t* ctx_lens, int32_t num_seqs,
+                            int32_t max_q_len, float scale, void* out, void* stream)
+{
+    return prefill_impl(pool, layer, q, q_start_loc, block_tables, max_blocks, ctx_lens, num_seqs, max_q_len, scale,
+                        out, true, stream);
 }
 
 // ------------------------------------------------------------------- step
@@ -862,9 +872,12 @@ pkv_status pkv_step(pkv_pool* pool, const pkv_step_desc* st, void* workspace, si
             if (e != cudaSuccess) return pkv::cuda_fail(e, "decode launch");
         }
         if (P > 0) {
-            pkv_status r = pkv_prefill_attn(pool, layer, ql, st->q_start_loc + B,
-                                            st->block_tables + (int64_t)B * st->max_blocks, st->max_blocks,
-                                            st->ctx_lens + B, P, st->max_q_len, st->scale, ol, stream);
+            // After decode rows the prefill launch does not wait for the decode kernel (it writes only the decode
+            // rows' outputs and their own blocks, nothing prefill reads): its CTAs start on the SMs the decode
+            // kernel leaves. Without decode rows it waits for the kv_append launch that wrote the chunk's keys.
+            pkv_status r = prefill_impl(pool, layer, ql, st->q_start_loc + B,
+                                        st->block_tables + (int64_t)B * st->max_blocks, st->max_blocks,
+                                        st->ctx_lens + B, P, st->max_q_len, st->scale, ol, B == 0, stream);
             if (r) return r;
         }
     }

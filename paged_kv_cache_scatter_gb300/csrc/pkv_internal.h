@@ -151,6 +151,6 @@ cudaError_t launch_wait_probe(uint64_t timeout_ns, unsigned int* status, cudaStr
 bool encode_kv_tmap(const PoolGeom& g, TensorMap128* out, std::string* err);
 cudaError_t launch_prefill(const pkv_pool* pool, int layer, const void* q, const int32_t* q_start,
                            const int32_t* tables, int max_blocks, const int32_t* ctx_lens, int num_seqs,
-                           int max_q_len, float scale, void* out, cudaStream_t stream);
+                           int max_q_len, float scale, void* out, bool wait_prev, cudaStream_t stream);
 
 }  // namespace pkv
