@@ -275,11 +275,15 @@ pkv_status pkv_decode_attn(pkv_pool* pool, int32_t layer, const void* q, const i
  * num_groups + 1 entries, group_start[num_groups] = num_seqs) share their first
  * group_blocks[i] table entries (device int32), which must be the same
  * physical blocks, full, and below every row's newest token. Every split-K
- * partition wholly inside a group's shared prefix is computed once for up to
- * 16 rows at a time, so its K/V tiles are read from memory once per group
- * instead of once per row; the rest of each row runs as in pkv_decode_attn,
- * which merges all partitions. max_group_rows = the largest group.
- * FP16 pools with num_q_heads == num_heads. No append: call pkv_kv_append
+ * partition wholly inside a group's shared prefix is computed once for
+ * several rows at a time (a CTA holds 16 query rows: 16 rows of one head over
+ * a pool with one query head per K/V head, 4 rows of 4 query heads for G = 4,
+ * one row's 16 heads from G = 16 up), so its K/V tiles are read from memory
+ * once per group instead of once per row; the rest of each row runs as in
+ * pkv_decode_attn, which merges all partitions. max_group_rows = the largest
+ * group. Every pool kind: FP16 with any G = num_q_heads / num_heads, and
+ * 8-bit (codes dequantised as in pkv_decode_attn; the 8-bit pool keeps its
+ * fixed partitions of partition_tokens). No append: call pkv_kv_append
  * first. Partition plan: a row's shared prefix [0, S) and the rest [S, ctx)
  * are each cut into partitions of partition_tokens (so a row can have one
  * partition more than in pkv_decode_attn); results are deterministic for a

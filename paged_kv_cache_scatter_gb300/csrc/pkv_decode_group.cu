@@ -110,10 +110,13 @@ struct GroupArgs {
     const int64_t* slots;    // [B] when append
     int append;
     unsigned int* status;
-    // cascade mode: rows [group_start[i], group_start[i+1]) share their first group_blocks[i] blocks
+    // cascade: rows [group_start[i], group_start[i+1]) share their first group_blocks[i] blocks. In CASCADE mode
+    // the kernel computes those shared partitions for the group's rows at once; otherwise (group_start set) a
+    // row's partitions cover only the keys after its group's shared prefix.
     const int32_t* group_start;
     const int32_t* group_blocks;
-    int max_slices;          // ceil(largest group / 16)
+    int num_groups;
+    int max_slices;          // CASCADE: ceil(largest group / sequences per CTA)
 };
 
 // Byte offset of 16-byte chunk ch (dimensions 8ch .. 8ch+7) of token t in a
@@ -143,48 +146,63 @@ __global__ void __launch_bounds__(kGWarps * 32) decode_group_kernel(const __grid
     const int p = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, tq = lane & 3;  // fragment row and column pair of this lane
-    // The CTA's rows: query heads h0 .. h0 + R - 1 of row r, or (cascade) rows r .. r + R - 1 of one group,
-    // head h0. Row i's query is q + qoff + i * qstride and its output / partial index rh0 + i * rstride.
-    int r, kvh, c, h0, R, ctx, nparts, span;
-    int64_t qstride, rstride;
+    // The CTA's R fragment rows: query heads h0 .. h0 + hpr - 1 (hpr = a.rows, one slice of K/V head kvh's
+    // group) of rows r .. r + nseq - 1; fragment row f is query head h0 + f % hpr of row r + f / hpr. Normal
+    // mode: one row (nseq = 1). CASCADE: as many rows of one group as 16 fragment rows hold, over the
+    // group's shared prefix, so each shared tile is read once for all of them.
+    const int hpr = a.rows;
+    const int kvh = blockIdx.y / a.slices, c = blockIdx.y % a.slices;
+    const int h0 = kvh * a.group + c * hpr;
+    int r, R, nseq, ctx, nparts, span, tok_lo, slot_p;
     if (CASCADE) {
+        const int spc = kGRows / hpr;  // rows per CTA
         const int grp = blockIdx.z / a.max_slices, sl = blockIdx.z % a.max_slices;
         const int row0 = __ldg(a.group_start + grp), row_end = __ldg(a.group_start + grp + 1);
-        r = row0 + sl * kGRows;
-        R = min(kGRows, row_end - r);
-        if (R <= 0) return;
-        kvh = blockIdx.y;
-        c = 0;
-        h0 = kvh;
+        r = row0 + sl * spc;
+        nseq = min(spc, row_end - r);
+        if (nseq <= 0) return;
+        R = nseq * hpr;
         ctx = __ldg(a.group_blocks + grp) * kBlockSize;  // the shared prefix: full blocks, valid for every row
         span = a.part_tokens;
         nparts = (ctx + span - 1) / span;  // the prefix partitioned on its own
         if (p >= nparts) return;
-        qstride = (int64_t)a.num_q_heads * kHeadDim;
-        rstride = a.num_q_heads;
+        tok_lo = p * span;
+        slot_p = p;
     } else {
         r = blockIdx.z;
-        kvh = blockIdx.y / a.slices;
-        c = blockIdx.y % a.slices;
-        h0 = kvh * a.group + c * a.rows;
-        R = a.rows;
+        nseq = 1;
+        R = hpr;
         ctx = __ldg(a.ctx_lens + r);
         if (ctx < 1 || ctx > a.max_blocks * kBlockSize) {
             if (p == 0 && blockIdx.y == 0 && threadIdx.x == 0) atomicOr(a.status, PKV_DEV_BAD_CTX);
             return;
         }
+        // Cascade's other half: keys [0, S) of the row's group's shared prefix were partitioned on their own
+        // (slots 0 .. nsh - 1, computed already); this CTA takes partition p of [S, ctx), slot nsh + p.
+        int S = 0;
+        if (a.group_start) {  // the row's group, by binary search over the group starts
+            int lo = 0, hi = a.num_groups - 1;
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (__ldg(a.group_start + mid) <= r) lo = mid; else hi = mid - 1;
+            }
+            S = __ldg(a.group_blocks + lo) * kBlockSize;
+        }
         // As few partitions as part_tokens allows, of equal length in whole blocks (a row of 2,300 keys: 768,
         // 768, 764 rather than 1,024, 1,024, 252), so that no short partition's CTA trails the launch. The plan
-        // depends only on ctx and part_tokens: a row's result is the same in any batch.
-        const int np = (ctx + a.part_tokens - 1) / a.part_tokens;
-        span = ((ctx + np - 1) / np + kBlockSize - 1) / kBlockSize * kBlockSize;  // <= part_tokens
-        nparts = (ctx + span - 1) / span;                                       // <= np
-        if (p >= nparts) return;
-        qstride = kHeadDim;
-        rstride = 1;
+        // depends only on ctx, S and part_tokens: a row's result is the same in any batch of the same grouping.
+        const int nsh = (S + a.part_tokens - 1) / a.part_tokens;
+        const int np = (ctx - S + a.part_tokens - 1) / a.part_tokens;
+        span = ((ctx - S + np - 1) / np + kBlockSize - 1) / kBlockSize * kBlockSize;  // <= part_tokens
+        tok_lo = S + p * span;
+        if (tok_lo >= ctx) return;
+        nparts = nsh + (ctx - S + span - 1) / span;
+        slot_p = nsh + p;
     }
-    const int blk_lo = p * span / kBlockSize;
-    const int blk_hi = (min((p + 1) * span, ctx) + kBlockSize - 1) / kBlockSize;
+    // query / output row of fragment row f, as an index of [rows][query heads]
+    auto rh = [&](int f) { return (int64_t)(r + f / hpr) * a.num_q_heads + h0 + f % hpr; };
+    const int blk_lo = tok_lo / kBlockSize;
+    const int blk_hi = (min(tok_lo + span, ctx) + kBlockSize - 1) / kBlockSize;
     const int count = blk_hi - blk_lo;  // <= kGMaxBlocks (partition_tokens <= 2,048, a multiple of 64)
 
     int32_t* ids = reinterpret_cast<int32_t*>(smem + kGSmIds);
@@ -229,7 +247,7 @@ __global__ void __launch_bounds__(kGWarps * 32) decode_group_kernel(const __grid
     const int new_t = (ctx - 1) % kBlockSize, new_i = (ctx - 1) / kBlockSize - blk_lo;
     int patch_li = -1;
     uint4 patch = make_uint4(0, 0, 0, 0);  // lanes 0-15: K chunk `lane`, lanes 16-31: V chunk `lane - 16`
-    if (!CASCADE && a.append && p == nparts - 1) {
+    if (!CASCADE && a.append && slot_p == nparts - 1) {
         const int64_t slot = __ldg(a.slots + r);
         const int32_t tb = __ldg(trow + (ctx - 1) / kBlockSize);
         const bool consistent =
@@ -251,13 +269,12 @@ __global__ void __launch_bounds__(kGWarps * 32) decode_group_kernel(const __grid
         }
     }
 
-    // Q as the A operand: rows = the CTA's query heads (zero past R), k = dims.
+    // Q as the A operand: rows = the CTA's fragment rows (zero past R), k = dims.
     uint32_t qa[8][4];
     {
-        const __half* q0 = a.q + ((int64_t)r * a.num_q_heads + h0) * kHeadDim;
-        const uint32_t* qlo = reinterpret_cast<const uint32_t*>(q0 + g * qstride);
-        const uint32_t* qhi = reinterpret_cast<const uint32_t*>(q0 + (g + 8) * qstride);
         const bool lo_ok = g < R, hi_ok = ROWS16 && g + 8 < R;
+        const uint32_t* qlo = reinterpret_cast<const uint32_t*>(a.q + (lo_ok ? rh(g) : 0) * kHeadDim);
+        const uint32_t* qhi = reinterpret_cast<const uint32_t*>(a.q + (hi_ok ? rh(g + 8) : 0) * kHeadDim);
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
             qa[ks][0] = lo_ok ? __ldg(qlo + 8 * ks + tq) : 0u;
@@ -408,7 +425,6 @@ __global__ void __launch_bounds__(kGWarps * 32) decode_group_kernel(const __grid
     const int d = threadIdx.x % kHeadDim, row0 = threadIdx.x / kHeadDim;
     const float* mo = reinterpret_cast<const float*>(smem + kGSmMergeO);
     const float* mml = reinterpret_cast<const float*>(smem + kGSmMergeML);
-    const int64_t rh0 = (int64_t)r * a.num_q_heads + h0;
     for (int row = row0; row < R; row += kRowStep) {
         float M = -INFINITY;
 #pragma unroll
@@ -421,9 +437,9 @@ __global__ void __launch_bounds__(kGWarps * 32) decode_group_kernel(const __grid
             O = fmaf(wt, mo[(w * kGRows + row) * kGMergeStride + d], O);
         }
         if (!CASCADE && nparts == 1) {
-            a.out[(rh0 + row) * kHeadDim + d] = __float2half_rn(O * (1.f / L));
+            a.out[rh(row) * kHeadDim + d] = __float2half_rn(O * (1.f / L));
         } else {
-            const int64_t slot = (rh0 + row * rstride) * a.ws_parts + p;
+            const int64_t slot = rh(row) * a.ws_parts + slot_p;
             a.ws_o[slot * kHeadDim + d] = O;
             if (d == 0) {
                 a.ws_ml[slot * 2] = M;
@@ -432,11 +448,12 @@ __global__ void __launch_bounds__(kGWarps * 32) decode_group_kernel(const __grid
         }
     }
     if (CASCADE) {
-        // count the partials; the one-head kernel's last partition of each (row, head) merges them
+        // count the partial of each of the CTA's rows (one counter per row, K/V head and slice: the one the
+        // private keys' kernel counts with); the last partition of the row to arrive merges them
         __syncthreads();
-        if (threadIdx.x < R) {
+        if (threadIdx.x < nseq) {
             __threadfence();
-            atomicAdd(a.counters + rh0 + threadIdx.x * rstride, 1u);
+            atomicAdd(a.counters + ((int64_t)(r + threadIdx.x) * a.num_kv_heads + kvh) * a.slices + c, 1u);
         }
         return;
     }
@@ -450,7 +467,7 @@ __global__ void __launch_bounds__(kGWarps * 32) decode_group_kernel(const __grid
     __syncthreads();
     if (!*flag) return;
     for (int row = row0; row < R; row += kRowStep) {
-        const int64_t base = (rh0 + row) * a.ws_parts;
+        const int64_t base = rh(row) * a.ws_parts;
         float M = -INFINITY;
         for (int q = 0; q < nparts; ++q) M = fmaxf(M, __ldcg(a.ws_ml + (base + q) * 2));
         float L = 0.f, O = 0.f;
@@ -459,7 +476,7 @@ __global__ void __launch_bounds__(kGWarps * 32) decode_group_kernel(const __grid
             L = fmaf(wt, __ldcg(a.ws_ml + (base + q) * 2 + 1), L);
             O = fmaf(wt, __ldcg(a.ws_o + (base + q) * kHeadDim + d), O);
         }
-        a.out[(rh0 + row) * kHeadDim + d] = __float2half_rn(O * (1.f / L));
+        a.out[rh(row) * kHeadDim + d] = __float2half_rn(O * (1.f / L));
     }
     __syncthreads();
     if (threadIdx.x == 0) *counter = 0u;
@@ -536,7 +553,7 @@ cudaError_t launch_decode_group(const PoolGeom& g, const TensorMap128& kv_tmap, 
                                 const int32_t* tables, int max_blocks, const int32_t* ctx_lens, int num_seqs,
                                 float scale, void* out, const DecodeWs& ws, int partition_tokens, const void* k_new,
                                 const void* v_new, const int64_t* slots, unsigned int* status, cudaStream_t stream,
-                                bool pdl)
+                                bool pdl, const int32_t* group_start, const int32_t* group_blocks, int num_groups)
 {
     if (num_seqs == 0) return cudaSuccess;
     GroupArgs a;
@@ -568,7 +585,9 @@ cudaError_t launch_decode_group(const PoolGeom& g, const TensorMap128& kv_tmap, 
     a.slots = slots;
     a.append = k_new != nullptr;
     a.status = status;
-    a.group_start = a.group_blocks = nullptr;
+    a.group_start = num_groups > 0 ? group_start : nullptr;
+    a.group_blocks = num_groups > 0 ? group_blocks : nullptr;
+    a.num_groups = num_groups;
     a.max_slices = 0;
     CUtensorMap tmap;
     static_assert(sizeof(tmap) == sizeof(kv_tmap.bytes), "tensor map size");
@@ -598,9 +617,11 @@ cudaError_t launch_decode_shared_prefix(const PoolGeom& g, const TensorMap128& k
     a.layer = layer;
     a.num_kv_heads = g.num_heads;
     a.num_q_heads = g.num_q_heads;
-    a.group = 1;
-    a.slices = 1;
-    a.rows = kGRows;
+    // fragment rows: the a.rows query heads of one slice of a K/V head's group, for as many rows of the
+    // group as 16 fragment rows hold (16 rows of one head each over a pool with one query head per K/V head)
+    a.group = g.group;
+    a.slices = decode_group_slices(g.group);
+    a.rows = g.group / a.slices;
     a.scale_log2 = scale * 1.4426950408889634f;
     a.ws_o = ws.o;
     a.ws_ml = ws.ml;
@@ -611,11 +632,13 @@ cudaError_t launch_decode_shared_prefix(const PoolGeom& g, const TensorMap128& k
     a.status = status;
     a.group_start = group_start;
     a.group_blocks = group_blocks;
-    a.max_slices = (max_group_rows + kGRows - 1) / kGRows;
+    a.num_groups = num_groups;
+    const int rows_per_cta = kGRows / a.rows;
+    a.max_slices = (max_group_rows + rows_per_cta - 1) / rows_per_cta;
     (void)num_seqs;
     CUtensorMap tmap;
     memcpy(&tmap, kv_tmap.bytes, sizeof(tmap));
-    const dim3 grid(a.max_parts, g.num_heads, num_groups * a.max_slices);
+    const dim3 grid(a.max_parts, g.num_heads * a.slices, num_groups * a.max_slices);
     return launch_group<true, true>(tmap, a, grid, stream);
 }
 

@@ -749,15 +749,18 @@ pkv_status pkv_decode_attn_cascade(pkv_pool* pool, int32_t layer, const void* q,
                                                     pool->partition_tokens, 1);
     if (!workspace || workspace_bytes < need || !aligned(workspace, 256))
         return fail(PKV_E_INVALID, "cascade workspace NULL, unaligned or below %zu bytes", need);
-    if (pool->geom.group != 1 || pool->geom.dtype != PKV_DTYPE_FP16)
-        return fail(PKV_E_INVALID, "cascade decode is built for FP16 pools with one query head per K/V head");
     if (!pool->tile_tmap_ok) return fail(PKV_E_DEVICE, "TMA descriptor for the pool could not be encoded");
     if (num_groups < 1 || num_groups > num_seqs || max_group_rows < 1 || max_group_rows > num_seqs || !group_start ||
         !group_blocks || !aligned(group_start, 4) || !aligned(group_blocks, 4))
         return fail(PKV_E_INVALID, "bad group description");
-    if ((int64_t)num_groups * ((max_group_rows + 15) / 16) > 65535)
-        return fail(PKV_E_INVALID, "too many groups x 16-row slices (%d x %d) for one launch", num_groups,
-                    (max_group_rows + 15) / 16);
+    // a shared-prefix CTA holds 16 fragment rows: the query heads of one slice of a K/V head's group for as
+    // many of the group's rows as fit
+    const int slices = pkv::decode_group_slices(pool->geom.group);
+    const int rows_per_cta = 16 / (pool->geom.group / slices);
+    const int64_t row_slices = (max_group_rows + rows_per_cta - 1) / rows_per_cta;
+    if ((int64_t)num_groups * row_slices > 65535)
+        return fail(PKV_E_INVALID, "too many groups x row slices (%d x %lld) for one launch", num_groups,
+                    (long long)row_slices);
     DeviceGuard dg(pool->device);
     if (!dg.ok) return fail(PKV_E_DEVICE, "cannot select the pool's device");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -766,13 +769,27 @@ pkv_status pkv_decode_attn_cascade(pkv_pool* pool, int32_t layer, const void* q,
         pkv::clear_decode_counters(pool->geom, num_seqs, max_blocks, pool->partition_tokens, workspace, s, 1);
     if (e != cudaSuccess) return pkv::cuda_fail(e, "clear decode counters");
     const pkv::DecodeWs w = pkv::decode_ws(pool->geom, workspace, num_seqs, max_blocks, pool->partition_tokens, 1);
-    e = pkv::launch_decode_shared_prefix(pool->geom, pool->tile_tmap, layer, q, block_tables, max_blocks, num_seqs,
-                                         group_start, group_blocks, num_groups, max_group_rows, scale, w,
-                                         pool->partition_tokens, pool->status_dev, s);
+    const bool i8 = pool->geom.dtype == PKV_DTYPE_INT8;
+    // (1) every group's shared prefix, once per group; (2) each row's own keys, whose last partition merges
+    e = i8 ? pkv::launch_decode_i8_shared_prefix(pool->geom, pool->tile_tmap, layer, q, block_tables, max_blocks,
+                                                 group_start, group_blocks, num_groups, max_group_rows, scale, w,
+                                                 pool->partition_tokens, pool->status_dev, s)
+           : pkv::launch_decode_shared_prefix(pool->geom, pool->tile_tmap, layer, q, block_tables, max_blocks,
+                                              num_seqs, group_start, group_blocks, num_groups, max_group_rows, scale,
+                                              w, pool->partition_tokens, pool->status_dev, s);
     if (e != cudaSuccess) return pkv::cuda_fail(e, "cascade (shared prefix) launch");
-    e = pkv::launch_decode(pool->geom, layer, q, block_tables, max_blocks, ctx_lens, num_seqs, scale, out, w,
-                           pool->partition_tokens, nullptr, nullptr, nullptr, pool->status_dev, s, group_start,
-                           group_blocks, num_groups);
+    if (i8)
+        e = pkv::launch_decode_i8(pool->geom, pool->tile_tmap, layer, q, block_tables, max_blocks, ctx_lens, num_seqs,
+                                  scale, out, w, pool->partition_tokens, nullptr, nullptr, nullptr, pool->status_dev,
+                                  s, false, group_start, group_blocks, num_groups);
+    else if (pool->geom.group > 1)
+        e = pkv::launch_decode_group(pool->geom, pool->tile_tmap, layer, q, block_tables, max_blocks, ctx_lens,
+                                     num_seqs, scale, out, w, pool->partition_tokens, nullptr, nullptr, nullptr,
+                                     pool->status_dev, s, false, group_start, group_blocks, num_groups);
+    else
+        e = pkv::launch_decode(pool->geom, layer, q, block_tables, max_blocks, ctx_lens, num_seqs, scale, out, w,
+                               pool->partition_tokens, nullptr, nullptr, nullptr, pool->status_dev, s, group_start,
+                               group_blocks, num_groups);
     return e == cudaSuccess ? PKV_OK : pkv::cuda_fail(e, "cascade decode launch");
 }
 

@@ -160,6 +160,13 @@ struct I8Args {
     const int64_t* slots;
     int append;
     unsigned int* status;
+    // cascade: rows [group_start[i], group_start[i+1]) share their first group_blocks[i] blocks. In CASCADE mode
+    // the kernel computes those shared partitions for the group's rows at once; otherwise (group_start set) a
+    // row's partitions cover only the keys after its group's shared prefix.
+    const int32_t* group_start;
+    const int32_t* group_blocks;
+    int num_groups;
+    int max_slices;          // CASCADE: ceil(largest group / rows per CTA)
 };
 
 // Byte offset of byte b of token t's 128 codes in a swizzled 16 x 128 B code tile.
@@ -195,28 +202,65 @@ __device__ __forceinline__ unsigned int q_atomic_add_acq_rel(unsigned int* p, un
 // 8-bit CTA carries half the bytes of an FP16 one, so more of them in flight cover more of each other's start-up
 // (+4 % on the batch-32 step against three per SM, a few spilled registers included). 16 query heads per CTA
 // need more registers: three per SM.
-template <bool ROWS16>
+template <bool ROWS16, bool CASCADE>
 __global__ void __launch_bounds__(kQWarps * 32, ROWS16 ? 3 : 4)
     decode_i8_kernel(const __grid_constant__ CUtensorMap tmap, const I8Args a)
 {
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     const uint32_t sb = smem_u32(smem);
-    const int p = blockIdx.x, r = blockIdx.z;
+    const int p = blockIdx.x;
     const int kvh = blockIdx.y / a.slices, c = blockIdx.y % a.slices;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, tq = lane & 3;
-    const int h0 = kvh * a.group + c * a.rows;
-
-    const int ctx = __ldg(a.ctx_lens + r);
-    if (ctx < 1 || ctx > a.max_blocks * kBlockSize) {
-        if (p == 0 && blockIdx.y == 0 && threadIdx.x == 0) atomicOr(a.status, PKV_DEV_BAD_CTX);
-        return;
+    // The CTA's R fragment rows: query heads h0 .. h0 + hpr - 1 (hpr = a.rows) of rows r .. r + nseq - 1;
+    // fragment row f is query head h0 + f % hpr of row r + f / hpr. Normal mode: one row. CASCADE: as many
+    // rows of one group as 16 fragment rows hold, over the group's shared prefix.
+    const int hpr = a.rows;
+    const int h0 = kvh * a.group + c * hpr;
+    int r, R, nseq, ctx, nparts, tok_lo, slot_p;
+    if (CASCADE) {
+        const int spc = kQRows / hpr;
+        const int grp = blockIdx.z / a.max_slices, sl = blockIdx.z % a.max_slices;
+        const int row0 = __ldg(a.group_start + grp), row_end = __ldg(a.group_start + grp + 1);
+        r = row0 + sl * spc;
+        nseq = min(spc, row_end - r);
+        if (nseq <= 0) return;
+        R = nseq * hpr;
+        ctx = __ldg(a.group_blocks + grp) * kBlockSize;  // the shared prefix: full blocks, valid for every row
+        nparts = (ctx + a.part_tokens - 1) / a.part_tokens;
+        if (p >= nparts) return;
+        tok_lo = p * a.part_tokens;
+        slot_p = p;
+    } else {
+        r = blockIdx.z;
+        nseq = 1;
+        R = hpr;
+        ctx = __ldg(a.ctx_lens + r);
+        if (ctx < 1 || ctx > a.max_blocks * kBlockSize) {
+            if (p == 0 && blockIdx.y == 0 && threadIdx.x == 0) atomicOr(a.status, PKV_DEV_BAD_CTX);
+            return;
+        }
+        // Cascade's other half: keys [0, S) of the row's group's shared prefix were partitioned on their own
+        // (slots 0 .. nsh - 1); this CTA takes partition p of [S, ctx), slot nsh + p.
+        int S = 0;
+        if (a.group_start) {
+            int lo = 0, hi = a.num_groups - 1;
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (__ldg(a.group_start + mid) <= r) lo = mid; else hi = mid - 1;
+            }
+            S = __ldg(a.group_blocks + lo) * kBlockSize;
+        }
+        const int nsh = (S + a.part_tokens - 1) / a.part_tokens;
+        tok_lo = S + p * a.part_tokens;
+        if (tok_lo >= ctx) return;
+        nparts = nsh + (ctx - S + a.part_tokens - 1) / a.part_tokens;
+        slot_p = nsh + p;
     }
-    const int nparts = (ctx + a.part_tokens - 1) / a.part_tokens;
-    if (p >= nparts) return;
-    const int blk_lo = p * a.part_tokens / kBlockSize;
-    const int blk_hi = (min((p + 1) * a.part_tokens, ctx) + kBlockSize - 1) / kBlockSize;
+    auto rh = [&](int f) { return (int64_t)(r + f / hpr) * a.num_q_heads + h0 + f % hpr; };
+    const int blk_lo = tok_lo / kBlockSize;
+    const int blk_hi = (min(tok_lo + a.part_tokens, ctx) + kBlockSize - 1) / kBlockSize;
     const int count = blk_hi - blk_lo;
 
     int32_t* ids = reinterpret_cast<int32_t*>(smem + kQSmIds);
@@ -265,7 +309,7 @@ __global__ void __launch_bounds__(kQWarps * 32, ROWS16 ? 3 : 4)
     int patch_li = -1;
     uint32_t kcodes = 0, vcodes = 0;
     float kscale = 0.f, vscale = 0.f;
-    if (a.append && p == nparts - 1) {
+    if (!CASCADE && a.append && slot_p == nparts - 1) {
         const int64_t slot = __ldg(a.slots + r);
         const int32_t tb = __ldg(trow + (ctx - 1) / kBlockSize);
         const bool consistent =
@@ -293,9 +337,9 @@ __global__ void __launch_bounds__(kQWarps * 32, ROWS16 ? 3 : 4)
     // register 0 holds dims 16j+4tq, +1 and register 2 holds dims 16j+4tq+2, +3 of row g.
     uint32_t qa[8][4];
     {
-        const uint32_t* qlo = reinterpret_cast<const uint32_t*>(a.q + ((int64_t)r * a.num_q_heads + h0 + g) * kHeadDim);
-        const uint32_t* qhi = qlo + 8 * kHeadDim / 2;
-        const bool lo_ok = g < a.rows, hi_ok = ROWS16 && g + 8 < a.rows;
+        const bool lo_ok = g < R, hi_ok = ROWS16 && g + 8 < R;
+        const uint32_t* qlo = reinterpret_cast<const uint32_t*>(a.q + (lo_ok ? rh(g) : 0) * kHeadDim);
+        const uint32_t* qhi = reinterpret_cast<const uint32_t*>(a.q + (hi_ok ? rh(g + 8) : 0) * kHeadDim);
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             qa[j][0] = lo_ok ? __ldg(qlo + 8 * j + 2 * tq) : 0u;
@@ -512,8 +556,7 @@ __global__ void __launch_bounds__(kQWarps * 32, ROWS16 ? 3 : 4)
     const int d = threadIdx.x;
     const float* mo = reinterpret_cast<const float*>(smem + kQSmMergeO);
     const float* mml = reinterpret_cast<const float*>(smem + kQSmMergeML);
-    const int64_t rh0 = (int64_t)r * a.num_q_heads + h0;
-    for (int row = 0; row < a.rows; ++row) {
+    for (int row = 0; row < R; ++row) {
         float M = -INFINITY;
 #pragma unroll
         for (int w = 0; w < kQWarps; ++w) M = fmaxf(M, mml[(w * kQRows + row) * 2]);
@@ -524,16 +567,26 @@ __global__ void __launch_bounds__(kQWarps * 32, ROWS16 ? 3 : 4)
             L = fmaf(wt, mml[(w * kQRows + row) * 2 + 1], L);
             O = fmaf(wt, mo[(w * kQRows + row) * kQMergeStride + d], O);
         }
-        if (nparts == 1) {
-            a.out[(rh0 + row) * kHeadDim + d] = __float2half_rn(O * (1.f / L));
+        if (!CASCADE && nparts == 1) {
+            a.out[rh(row) * kHeadDim + d] = __float2half_rn(O * (1.f / L));
         } else {
-            const int64_t slot = (rh0 + row) * a.ws_parts + p;
+            const int64_t slot = rh(row) * a.ws_parts + slot_p;
             a.ws_o[slot * kHeadDim + d] = O;
             if (d == 0) {
                 a.ws_ml[slot * 2] = M;
                 a.ws_ml[slot * 2 + 1] = L;
             }
         }
+    }
+    if (CASCADE) {
+        // count the partial of each of the CTA's rows (the counter the private keys' launch counts with); the
+        // last partition of the row to arrive merges them
+        __syncthreads();
+        if (threadIdx.x < nseq) {
+            __threadfence();
+            atomicAdd(a.counters + ((int64_t)(r + threadIdx.x) * a.num_kv_heads + kvh) * a.slices + c, 1u);
+        }
+        return;
     }
     if (nparts == 1) return;
 
@@ -543,8 +596,8 @@ __global__ void __launch_bounds__(kQWarps * 32, ROWS16 ? 3 : 4)
     if (threadIdx.x == 0) *flag = q_atomic_add_acq_rel(counter, 1u) == (unsigned int)(nparts - 1);
     __syncthreads();
     if (!*flag) return;
-    for (int row = 0; row < a.rows; ++row) {
-        const int64_t base = (rh0 + row) * a.ws_parts;
+    for (int row = 0; row < R; ++row) {
+        const int64_t base = rh(row) * a.ws_parts;
         float M = -INFINITY;
         for (int q = 0; q < nparts; ++q) M = fmaxf(M, __ldcg(a.ws_ml + (base + q) * 2));
         float L = 0.f, O = 0.f;
@@ -553,26 +606,26 @@ __global__ void __launch_bounds__(kQWarps * 32, ROWS16 ? 3 : 4)
             L = fmaf(wt, __ldcg(a.ws_ml + (base + q) * 2 + 1), L);
             O = fmaf(wt, __ldcg(a.ws_o + (base + q) * kHeadDim + d), O);
         }
-        a.out[(rh0 + row) * kHeadDim + d] = __float2half_rn(O * (1.f / L));
+        a.out[rh(row) * kHeadDim + d] = __float2half_rn(O * (1.f / L));
     }
     __syncthreads();
     if (threadIdx.x == 0) *counter = 0u;
 }
 
-template <bool ROWS16>
-cudaError_t launch_i8(const CUtensorMap& tmap, const I8Args& a, int num_seqs, cudaStream_t stream, bool pdl)
+template <bool ROWS16, bool CASCADE>
+cudaError_t launch_i8(const CUtensorMap& tmap, const I8Args& a, dim3 grid, cudaStream_t stream, bool pdl)
 {
     static bool attr_set[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 64 && !attr_set[dev]) {
-        cudaError_t e =
-            cudaFuncSetAttribute(decode_i8_kernel<ROWS16>, cudaFuncAttributeMaxDynamicSharedMemorySize, kQSmAlloc);
+        cudaError_t e = cudaFuncSetAttribute(decode_i8_kernel<ROWS16, CASCADE>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kQSmAlloc);
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(a.max_parts, a.num_kv_heads * a.slices, num_seqs);
+    cfg.gridDim = grid;
     cfg.blockDim = dim3(kQWarps * 32);
     cfg.dynamicSmemBytes = kQSmAlloc;
     cfg.stream = stream;
@@ -581,7 +634,7 @@ cudaError_t launch_i8(const CUtensorMap& tmap, const I8Args& a, int num_seqs, cu
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, decode_i8_kernel<ROWS16>, tmap, a);
+    return cudaLaunchKernelEx(&cfg, decode_i8_kernel<ROWS16, CASCADE>, tmap, a);
 }
 
 }  // namespace
@@ -637,10 +690,11 @@ cudaError_t launch_decode_i8(const PoolGeom& g, const TensorMap128& i8_tmap, int
                              const int32_t* tables, int max_blocks, const int32_t* ctx_lens, int num_seqs,
                              float scale, void* out, const DecodeWs& ws, int partition_tokens, const void* k_new,
                              const void* v_new, const int64_t* slots, unsigned int* status, cudaStream_t stream,
-                             bool pdl)
+                             bool pdl, const int32_t* group_start, const int32_t* group_blocks, int num_groups)
 {
     if (num_seqs == 0) return cudaSuccess;
     I8Args a;
+    memset(&a, 0, sizeof(a));
     a.q = static_cast<const __half*>(q);
     a.out = static_cast<__half*>(out);
     a.tables = tables;
@@ -669,11 +723,59 @@ cudaError_t launch_decode_i8(const PoolGeom& g, const TensorMap128& i8_tmap, int
     a.slots = slots;
     a.append = k_new != nullptr;
     a.status = status;
+    a.group_start = num_groups > 0 ? group_start : nullptr;
+    a.group_blocks = num_groups > 0 ? group_blocks : nullptr;
+    a.num_groups = num_groups;
     CUtensorMap tmap;
     static_assert(sizeof(tmap) == sizeof(i8_tmap.bytes), "tensor map size");
     memcpy(&tmap, i8_tmap.bytes, sizeof(tmap));
-    return a.rows > 8 ? launch_i8<true>(tmap, a, num_seqs, stream, pdl)
-                      : launch_i8<false>(tmap, a, num_seqs, stream, pdl);
+    const dim3 grid(a.max_parts, a.num_kv_heads * a.slices, num_seqs);
+    return a.rows > 8 ? launch_i8<true, false>(tmap, a, grid, stream, pdl)
+                      : launch_i8<false, false>(tmap, a, grid, stream, pdl);
+}
+
+cudaError_t launch_decode_i8_shared_prefix(const PoolGeom& g, const TensorMap128& i8_tmap, int layer, const void* q,
+                                           const int32_t* tables, int max_blocks, const int32_t* group_start,
+                                           const int32_t* group_blocks, int num_groups, int max_group_rows,
+                                           float scale, const DecodeWs& ws, int partition_tokens,
+                                           unsigned int* status, cudaStream_t stream)
+{
+    if (num_groups == 0) return cudaSuccess;
+    I8Args a;
+    memset(&a, 0, sizeof(a));
+    a.q = static_cast<const __half*>(q);
+    a.tables = tables;
+    a.max_blocks = max_blocks;
+    a.pool = const_cast<char*>(g.base);
+    a.block_bytes = g.block_bytes;
+    a.head_off = (int64_t)layer * g.layer_bytes;
+    a.kv_bytes = g.kv_bytes;
+    a.num_blocks = g.num_blocks;
+    a.layer = layer;
+    a.num_kv_heads = g.num_heads;
+    a.num_q_heads = g.num_q_heads;
+    // fragment rows: the a.rows query heads of one slice of a K/V head's group, for as many rows of the group
+    // as 16 fragment rows hold
+    a.group = g.group;
+    a.slices = decode_group_slices(g.group);
+    a.rows = g.group / a.slices;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    a.ws_o = ws.o;
+    a.ws_ml = ws.ml;
+    a.counters = ws.counters;
+    a.max_parts = decode_max_parts(max_blocks, partition_tokens);
+    a.ws_parts = ws.parts;
+    a.part_tokens = partition_tokens;
+    a.status = status;
+    a.group_start = group_start;
+    a.group_blocks = group_blocks;
+    a.num_groups = num_groups;
+    const int rows_per_cta = kQRows / a.rows;
+    a.max_slices = (max_group_rows + rows_per_cta - 1) / rows_per_cta;
+    CUtensorMap tmap;
+    memcpy(&tmap, i8_tmap.bytes, sizeof(tmap));
+    const dim3 grid(a.max_parts, g.num_heads * a.slices, num_groups * a.max_slices);
+    return launch_i8<true, true>(tmap, a, grid, stream, false);
 }
 
 }  // namespace pkv

@@ -123,7 +123,15 @@ cudaError_t launch_decode_i8(const PoolGeom& g, const TensorMap128& i8_tmap, int
                              const int32_t* tables, int max_blocks, const int32_t* ctx_lens, int num_seqs,
                              float scale, void* out, const DecodeWs& ws, int partition_tokens, const void* k_new,
                              const void* v_new, const int64_t* slots, unsigned int* status, cudaStream_t stream,
-                             bool pdl = false);
+                             bool pdl = false, const int32_t* group_start = nullptr,
+                             const int32_t* group_blocks = nullptr, int num_groups = 0);
+// Cascade over an 8-bit pool: the partitions wholly inside each group's shared prefix, for every row of the
+// group at once.
+cudaError_t launch_decode_i8_shared_prefix(const PoolGeom& g, const TensorMap128& i8_tmap, int layer, const void* q,
+                                           const int32_t* tables, int max_blocks, const int32_t* group_start,
+                                           const int32_t* group_blocks, int num_groups, int max_group_rows,
+                                           float scale, const DecodeWs& ws, int partition_tokens,
+                                           unsigned int* status, cudaStream_t stream);
 
 // pkv_decode_group.cu: decode attention for pools whose K/V heads serve groups of query heads.
 bool encode_tile_tmap(const PoolGeom& g, TensorMap128* out, std::string* err);
@@ -134,11 +142,14 @@ cudaError_t launch_decode_shared_prefix(const PoolGeom& g, const TensorMap128& k
                                         const int32_t* group_start, const int32_t* group_blocks, int num_groups,
                                         int max_group_rows, float scale, const DecodeWs& ws, int partition_tokens,
                                         unsigned int* status, cudaStream_t stream);
+// group_start/group_blocks (num_groups > 0): skip each row's keys inside its group's shared prefix
+// (launch_decode_shared_prefix computed them).
 cudaError_t launch_decode_group(const PoolGeom& g, const TensorMap128& kv_tmap, int layer, const void* q,
                                 const int32_t* tables, int max_blocks, const int32_t* ctx_lens, int num_seqs,
                                 float scale, void* out, const DecodeWs& ws, int partition_tokens, const void* k_new,
                                 const void* v_new, const int64_t* slots, unsigned int* status, cudaStream_t stream,
-                                bool pdl = false);
+                                bool pdl = false, const int32_t* group_start = nullptr,
+                                const int32_t* group_blocks = nullptr, int num_groups = 0);
 // pkv_blocks.cu: whole-block copies inside the pool (copy-on-write) and to / from host memory (swap).
 cudaError_t launch_copy_blocks(const PoolGeom& g, const int32_t* pairs, int n, unsigned int* status,
                                cudaStream_t stream);

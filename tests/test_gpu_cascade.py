@@ -44,15 +44,24 @@ def _groups_wl(seed, sizes, prefix_blocks, max_private=120, num_layers=1):
     return workloads.Workload(f"groups{seed}", num_layers, nb_total, tables, ctx, np.ones(len(ctx), np.int32), seed)
 
 
-def run_cascade(pkv, wl, partition, check_plain=True):
-    H = 32
-    pool = G.device_pool(wl.num_blocks, wl.num_layers, H, seed=wl.seed)
-    host = G.to_bits(pool).reshape(pool.shape).copy()
-    p = pkv.Pool(pool, wl.num_blocks, num_layers=wl.num_layers, num_heads=H, partition_tokens=partition)
+def run_cascade(pkv, wl, partition, check_plain=True, heads=32, q_heads=None, dtype="fp16"):
+    H, hq = heads, q_heads or heads
+    i8 = dtype == "int8"
+    if i8:
+        pool = G.device_pool_i8(wl.num_blocks, wl.num_layers, H, seed=wl.seed)
+        host = pool.detach().cpu().numpy().reshape(-1).copy()
+    else:
+        pool = G.device_pool(wl.num_blocks, wl.num_layers, H, seed=wl.seed)
+        host = G.to_bits(pool).reshape(pool.shape).copy()
+    p = pkv.Pool(pool, wl.num_blocks, num_layers=wl.num_layers, num_heads=H, partition_tokens=partition,
+                 num_q_heads=hq, dtype=dtype)
     tables_d, ctx_d, _, slots_d, slots = G.step_metadata(wl)
-    q, k, v = G.new_token_inputs(wl, 0)
+    T = wl.num_tokens
+    q = workloads.normal_fp16((T, hq, 128), workloads.value_seed(wl.seed, "q")).cuda()
+    k = workloads.normal_fp16((T, H, 128), workloads.value_seed(wl.seed, "k")).cuda()
+    v = workloads.normal_fp16((T, H, 128), workloads.value_seed(wl.seed, "v")).cuda()
     p.kv_append(0, k, v, slots_d)
-    g = oracle.geom(wl.num_blocks, wl.num_layers, H)
+    g = oracle.geom(wl.num_blocks, wl.num_layers, H, num_q_heads=hq, dtype=oracle.INT8 if i8 else oracle.FP16)
     assert oracle.kv_append(host, g, 0, G.to_bits(k), G.to_bits(v), slots) == -1
     gs, gb, widest = pkv.cascade_groups(wl.block_tables, wl.ctx_lens)
     groups = (torch.from_numpy(gs).cuda(), torch.from_numpy(gb).cuda(), widest)
@@ -64,15 +73,16 @@ def run_cascade(pkv, wl, partition, check_plain=True):
     p.decode_attn_cascade(0, q, tables_d, ctx_d, groups, G.SCALE, out, ws)
     assert p.get_status() == (pkv.PKV_OK, 0)
     ref, _ = oracle.decode_attn(host, g, 0, G.to_bits(q), wl.block_tables, wl.ctx_lens, G.SCALE)
-    G.assert_close(out, ref, f"cascade, partition {partition}")
+    what = f"cascade, partition {partition}, {hq} query / {H} K/V heads, {dtype}"
+    G.assert_close(out, ref, what)
     again = torch.full_like(q, float("nan"))
     p.decode_attn_cascade(0, q, tables_d, ctx_d, groups, G.SCALE, again, ws)
-    assert torch.equal(out, again)                      # deterministic for a given grouping
+    assert torch.equal(out, again), what                # deterministic for a given grouping
     if check_plain:
         plain = torch.empty_like(q)
         p.decode_attn(0, q, tables_d, ctx_d, G.SCALE, plain, ws)   # the counters were left at zero
         assert p.get_status() == (pkv.PKV_OK, 0)
-        G.assert_close(plain, ref, "plain decode after cascade")
+        G.assert_close(plain, ref, "plain decode after " + what)
     return gs, gb
 
 
@@ -113,8 +123,29 @@ def test_cascade_refuses_bad_groups_and_pools(pkv):
            9)                                              # max_group_rows above num_seqs
     with pytest.raises(pkv.PkvError):
         p.decode_attn_cascade(0, q, tables_d, ctx_d, bad, G.SCALE, q, ws)
-    pg = pkv.Pool(G.device_pool(wl.num_blocks, 1, 8, seed=4), wl.num_blocks, num_layers=1, num_heads=8,
-                  num_q_heads=32)
-    good = (bad[0], bad[1], 4)
+    empty = (torch.tensor([0, 4], dtype=torch.int32, device="cuda"),
+             torch.tensor([10], dtype=torch.int32, device="cuda"), 0)          # max_group_rows below 1
     with pytest.raises(pkv.PkvError):
-        pg.decode_attn_cascade(0, q, tables_d, ctx_d, good, G.SCALE, q, ws)
+        p.decode_attn_cascade(0, q, tables_d, ctx_d, empty, G.SCALE, q, ws)
+
+
+# Grouped query heads and 8-bit pools: (K/V heads, query heads, element type). A shared-prefix CTA holds 16 query
+# rows: 4 rows x 4 heads (G = 4), 2 rows x 8 heads (MQA with 8 query heads), 1 row x 12 heads (G = 12), one row's
+# 16-head slice of a 32-head group (G = 32, two slices); 8-bit pools with 1 and 4 query heads per K/V head.
+KINDS = [(8, 32, "fp16"), (1, 8, "fp16"), (4, 48, "fp16"), (2, 64, "fp16"), (32, 32, "int8"), (8, 32, "int8")]
+
+
+@pytest.mark.parametrize("heads,q_heads,dtype", KINDS)
+@pytest.mark.parametrize("partition", [64, 1024])
+def test_cascade_grouped_heads_and_8bit_pools(pkv, heads, q_heads, dtype, partition):
+    wl = _groups_wl(5, [1, 6, 9, 17], [4, 40, 9, 66])
+    gs, gb = run_cascade(pkv, wl, partition, heads=heads, q_heads=q_heads, dtype=dtype)
+    assert list(np.diff(gs)) == [1, 6, 9, 17] and list(gb) == [0, 40, 9, 66]
+
+
+@pytest.mark.parametrize("heads,q_heads,dtype", [(8, 32, "fp16"), (32, 32, "int8"), (8, 32, "int8")])
+def test_cascade_shared_prefix_config_grouped_and_8bit(pkv, heads, q_heads, dtype):
+    # the shared-prefix workload's shape (64 rows over 125 shared blocks) with 8 K/V heads and over an 8-bit pool
+    wl = workloads.shared_prefix_decode(0, num_layers=1, num_blocks=1500)
+    gs, gb = run_cascade(pkv, wl, 0, heads=heads, q_heads=q_heads, dtype=dtype)
+    assert list(gb) == [125] and list(gs) == [0, 64]

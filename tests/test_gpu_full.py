@@ -147,7 +147,7 @@ def test_full_mixed_chunked_prefill(pkv, big_pool):
     first = workloads.mixed_prefill(0)
     nchunks = first.meta["num_chunks"]
     P = first.num_seqs - 1                    # the prompt row
-    layers = (0, 31)
+    layers = (0, 13, 31)
     prompt_nb = -(-first.meta["prompt_len"] // 16)
     prompt_copy = {l: _rows_copy(big_pool, first.block_tables[P], prompt_nb, l) for l in layers}
     dec_rows = (0, 15, 30)
@@ -180,12 +180,13 @@ def test_full_mixed_chunked_prefill(pkv, big_pool):
                 mini = dec_copy[(l, r)].copy()
                 ref = _oracle_row(mini, dec_kv[(l, r)], qb[l, r], ctx, mini.shape[0])
                 G.assert_close(st.out[l, r], ref, f"chunk {c} layer {l} decode row {r}")
-            if c not in (0, 1, 6, 7):
-                continue
             mini = prompt_copy[l].copy()
             assert oracle.kv_append(mini, g, 0, np.concatenate(k_l), np.concatenate(v_l),
                                     np.array(pos_l, np.int64)) == -1
-            picks = sorted(set([0, end - start - 1] + rng.integers(0, end - start, 14).tolist()))
+            # every chunk: both rows at each 128-row query-tile boundary, the chunk's ends and 24 more
+            n_q = end - start
+            bounds = [x for b in range(0, n_q, 128) for x in (b, b + 127)]
+            picks = sorted(set(x for x in [0, n_q - 1] + bounds + rng.integers(0, n_q, 24).tolist() if x < n_q))
             for i in picks:
                 ref, _ = oracle.decode_attn(mini, g, 0, qb[l, B + i][None], table, np.array([start + i + 1], np.int32),
                                             G.SCALE)

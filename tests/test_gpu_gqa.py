@@ -158,6 +158,14 @@ def test_gqa_prefill_one_sequence(pkv, ctx, qlen, hq, h):
     run_gqa(pkv, wl, hq, use_step=False)
 
 
+def test_gqa_prefill_512_row_chunk_over_long_prefix_every_row(pkv):
+    # the schedule's chunk 6 (512 queries after a 3,072-key prefix) with 2 K/V heads serving 8 query heads:
+    # a CTA's 128 rows are 32 tokens of 4 query heads; every row against the oracle
+    wl = _wl([3584], [512], seed=23)
+    wl.num_heads = 2
+    run_gqa(pkv, wl, 8, use_step=False)
+
+
 @pytest.mark.parametrize("seed", [1, 2])
 def test_gqa_mixed_step(pkv, seed):
     rng = np.random.default_rng(seed)

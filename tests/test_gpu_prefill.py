@@ -99,6 +99,21 @@ def test_prefill_one_sequence(pkv, ctx, qlen):
     run_step_case(pkv, _wl([ctx], [qlen], seed=ctx), use_step=False)
 
 
+def test_prefill_512_row_chunk_over_long_prefix_every_row(pkv):
+    # a chunk of 512 queries at positions 3,072..3,583 (the schedule's chunk 6) over its 3,072-key prefix:
+    # every row of every head against the oracle (4 heads keep the oracle's double-precision work small)
+    wl = _wl([3584], [512], seed=21)
+    wl.num_heads = 4
+    run_step_case(pkv, wl, use_step=False)
+
+
+def test_prefill_two_long_chunks_and_a_short_one_every_row(pkv):
+    # several sequences with long prefixes in one call, ragged chunk lengths (a partial last query tile)
+    wl = _wl([3100, 2049, 700], [300, 513, 129], seed=22)
+    wl.num_heads = 2
+    run_step_case(pkv, wl, use_step=False)
+
+
 def test_prefill_several_sequences_one_call(pkv):
     run_step_case(pkv, _wl([200, 37, 513, 140], [200, 5, 260, 2], seed=5), use_step=False)
 
