@@ -60,8 +60,12 @@ def _iterations(config: str, seed: int = 0):
         return [workloads.average_decode(seed)]
     if config == "long_decode":
         return [workloads.long_decode(seed)]
-    if config in ("shared_prefix_decode", "shared_prefix_cascade"):
+    if config in ("shared_prefix_decode", "shared_prefix_cascade", "shared_prefix_cascade_int8"):
         return [workloads.shared_prefix_decode(seed)]
+    if config == "shared_prefix_cascade_gqa":
+        w = workloads.shared_prefix_decode(seed, num_blocks=workloads.GQA_POOL_BLOCKS)
+        w.num_heads, w.num_q_heads = workloads.GQA_KV_HEADS, workloads.NUM_HEADS
+        return [w]
     if config == "gqa_decode":
         return [workloads.gqa_decode(seed)]
     if config in ("mixed_prefill", "mixed_prefill_int8", "mixed_prefill_gqa"):
@@ -88,6 +92,10 @@ CONFIG_TEXT = {
                           "head) row of K or V): decode rows and prefill chunks both read codes and scales",
     "average_decode_int8": "the average_decode workload over an 8-bit pool (INT8 codes, one FP32 scale per "
                            "(token, head) row of K or V; 2,112-byte tiles), 7,152 blocks (30.9 GB)",
+    "shared_prefix_cascade_gqa": "the shared_prefix_cascade workload with 8 K/V heads serving 32 query heads "
+                                 "(28,608-block 60 GB pool): a shared-prefix CTA holds 4 rows x 4 query heads",
+    "shared_prefix_cascade_int8": "the shared_prefix_cascade workload over an 8-bit pool (INT8 codes, one FP32 "
+                                  "scale per (token, head) row of K or V)",
     "shared_prefix_cascade": "64 rows sharing 125 ref-counted prefix blocks + 1..300 private tokens, 32 layers; "
                              "per layer kv_append of the new tokens then cascade decode (shared partitions once "
                              "per group on the tensor cores, the rest per row)",
@@ -98,7 +106,7 @@ CONFIG_TEXT = {
                   "kv_append of 1 token per row",
 }
 
-CONFIG_DTYPE = {"average_decode_int8": "int8", "mixed_prefill_int8": "int8"}
+CONFIG_DTYPE = {"average_decode_int8": "int8", "mixed_prefill_int8": "int8", "shared_prefix_cascade_int8": "int8"}
 SWAP_BLOCKS, SWAP_POOL = 384, 1024
 
 KERNEL_SOURCES = {
@@ -433,7 +441,7 @@ def run_ours(args):
     steps = [StepData(torch, pkv, pool, wl, m, L, dev, gen) for wl, m in zip(iters, _metadata(pkv, iters))]
     wspace = torch.empty(max(max(s.ws_bytes for s in steps), 256), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
-    cascade = args.config == "shared_prefix_cascade"
+    cascade = args.config.startswith("shared_prefix_cascade")
     if cascade:
         s0 = steps[0]
         need = pool.decode_cascade_workspace_bytes(s0.B, s0.desc.max_blocks)
@@ -642,15 +650,22 @@ def run_ours(args):
     if dtype == "int8":
         dec_kernel, dec_src = "decode_i8_kernel (INT8 codes dequantised in the loaders)", "decode_i8_attn"
     unique_step = None
-    if args.config in ("shared_prefix_decode", "shared_prefix_cascade"):
+    if args.config.startswith("shared_prefix"):
         # K/V bytes a layer must read at least once: the shared prefix once, then each row's own tokens
         w0 = steps[0].wl
         pre = int(w0.meta["prefix_blocks"]) * 16
         unique_tok = pre + int((w0.ctx_lens[:w0.num_decode].astype(np.int64) - pre).sum())
         unique_step = unique_tok * 2 * H * row_bytes(dtype) * L
     if cascade:
-        dec_kernel = ("cascade decode: decode_group_kernel<true, true> (shared partitions, 16 rows per CTA, "
-                      "mma.sync) then decode_kernel (the rest, merge)")
+        if dtype == "int8":
+            dec_kernel = ("cascade decode over an 8-bit pool: decode_i8_kernel<true, true> (shared partitions, 16 "
+                          "query rows per CTA, mma.sync) then decode_i8_kernel (the rest, merge)")
+        elif Hq != H:
+            dec_kernel = ("cascade decode, grouped heads: decode_group_kernel<true, true> (shared partitions, 4 rows x "
+                          "4 query heads per CTA, mma.sync) then decode_group_kernel (the rest, merge)")
+        else:
+            dec_kernel = ("cascade decode: decode_group_kernel<true, true> (shared partitions, 16 rows per CTA, "
+                          "mma.sync) then decode_kernel (the rest, merge)")
         dec_src = "decode_cascade_attn"
         # the roofline of a cascade launch: unique bytes + q and out
         dec_bytes_launch = unique_step / L / len(steps) + sum(2 * s.B * Hq * HEAD_DIM * 2 for s in steps) / len(steps)
@@ -1011,7 +1026,7 @@ def main():
     ap.add_argument("--config", default="average_decode",
                     choices=["average_decode", "long_decode", "shared_prefix_decode", "mixed_prefill", "gqa_decode",
                              "average_decode_int8", "mixed_prefill_int8", "mixed_prefill_gqa", "swap_blocks",
-                             "shared_prefix_cascade"])
+                             "shared_prefix_cascade", "shared_prefix_cascade_gqa", "shared_prefix_cascade_int8"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="launch each step directly instead of replaying a CUDA graph")

@@ -400,11 +400,12 @@ typedef struct pkv_step_desc {
 
 size_t pkv_step_workspace_bytes(const pkv_pool* pool, const pkv_step_desc* step);
 
-/* For each layer: kv_append of the prefill tokens, decode attention over the
- * B decode rows (which also appends their K/V), then causal prefill over the
- * P chunks. One clear of the workspace counters per call covers all layers.
- * A layer's prefill launch does not wait for that layer's decode launch (it
- * reads nothing decode writes), so its CTAs start on the SMs decode leaves. */
+/* For each layer: kv_append of the prefill tokens, causal prefill over the
+ * P chunks and decode attention over the B decode rows (which also appends
+ * their K/V). One clear of the workspace counters per call covers all layers.
+ * In a layer with both kinds of rows the prefill launch goes first and the
+ * decode launch does not wait for it (decode reads and writes nothing
+ * prefill touches), so decode CTAs run on the SMs prefill leaves idle. */
 pkv_status pkv_step(pkv_pool* pool, const pkv_step_desc* step, void* workspace, size_t workspace_bytes,
                     void* stream);
 

@@ -109,6 +109,7 @@ struct GroupArgs {
     const __half* v_new;
     const int64_t* slots;    // [B] when append
     int append;
+    int no_wait;             // launched after a kernel whose results it does not read: skip the dependency wait
     unsigned int* status;
     // cascade: rows [group_start[i], group_start[i+1]) share their first group_blocks[i] blocks. In CASCADE mode
     // the kernel computes those shared partitions for the group's rows at once; otherwise (group_start set) a
@@ -241,7 +242,7 @@ __global__ void __launch_bounds__(kGWarps * 32) decode_group_kernel(const __grid
 
     // Only lengths, tables and this layer's K/V were read so far; with a programmatic dependency on the
     // previous layer's kernel, wait for it before reading q or the new K/V and touching the workspace.
-    pdl_wait();
+    if (!a.no_wait) pdl_wait();
 
     // The new token (position ctx - 1) is the last token of the partition's last block.
     const int new_t = (ctx - 1) % kBlockSize, new_i = (ctx - 1) / kBlockSize - blk_lo;
@@ -484,7 +485,7 @@ __global__ void __launch_bounds__(kGWarps * 32) decode_group_kernel(const __grid
 
 template <bool ROWS16, bool CASCADE>
 cudaError_t launch_group(const CUtensorMap& tmap, const GroupArgs& a, dim3 grid, cudaStream_t stream,
-                         bool pdl = false)
+                         int pdl = 0)
 {
     static bool attr_set[64] = {};
     int dev = 0;
@@ -553,10 +554,11 @@ cudaError_t launch_decode_group(const PoolGeom& g, const TensorMap128& kv_tmap, 
                                 const int32_t* tables, int max_blocks, const int32_t* ctx_lens, int num_seqs,
                                 float scale, void* out, const DecodeWs& ws, int partition_tokens, const void* k_new,
                                 const void* v_new, const int64_t* slots, unsigned int* status, cudaStream_t stream,
-                                bool pdl, const int32_t* group_start, const int32_t* group_blocks, int num_groups)
+                                int pdl, const int32_t* group_start, const int32_t* group_blocks, int num_groups)
 {
     if (num_seqs == 0) return cudaSuccess;
     GroupArgs a;
+    memset(&a, 0, sizeof(a));
     a.q = static_cast<const __half*>(q);
     a.out = static_cast<__half*>(out);
     a.tables = tables;
@@ -584,6 +586,7 @@ cudaError_t launch_decode_group(const PoolGeom& g, const TensorMap128& kv_tmap, 
     a.v_new = static_cast<const __half*>(v_new);
     a.slots = slots;
     a.append = k_new != nullptr;
+    a.no_wait = pdl == 2;
     a.status = status;
     a.group_start = num_groups > 0 ? group_start : nullptr;
     a.group_blocks = num_groups > 0 ? group_blocks : nullptr;

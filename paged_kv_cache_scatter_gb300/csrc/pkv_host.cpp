@@ -634,7 +634,7 @@ static cudaError_t launch_append_any(const pkv_pool* pool, int32_t layer, const 
 static cudaError_t launch_decode_any(const pkv_pool* pool, int32_t layer, const void* q, const int32_t* tables,
                                      int32_t max_blocks, const int32_t* ctx_lens, int32_t num_seqs, float scale,
                                      void* out, void* ws, const void* k_new, const void* v_new, const int64_t* slots,
-                                     cudaStream_t s, bool pdl = false)
+                                     cudaStream_t s, int pdl = 0)
 {
     if (pool->geom.dtype == PKV_DTYPE_INT8) {
         const pkv::DecodeWs w = pkv::decode_ws(pool->geom, ws, num_seqs, max_blocks, pool->partition_tokens);
@@ -799,11 +799,9 @@ size_t pkv_decode_cascade_workspace_bytes(const pkv_pool* pool, int32_t num_seqs
     return pkv::decode_workspace_bytes(num_seqs, pool->desc.num_q_heads, max_blocks, pool->partition_tokens, 1);
 }
 
-// wait_prev: the kernel waits for the stream's previous kernel before reading its inputs (always, except
-// in pkv_step after the decode launch, which writes nothing prefill reads).
 static pkv_status prefill_impl(pkv_pool* pool, int32_t layer, const void* q, const int32_t* q_start_loc,
                                const int32_t* block_tables, int32_t max_blocks, const int32_t* ctx_lens,
-                               int32_t num_seqs, int32_t max_q_len, float scale, void* out, bool wait_prev, void* stream)
+                               int32_t num_seqs, int32_t max_q_len, float scale, void* out, void* stream)
 {
     if (pkv_status s = check_device_pool(pool)) return s;
     if (pkv_status s = check_layer(pool, layer)) return s;
@@ -817,7 +815,7 @@ static pkv_status prefill_impl(pkv_pool* pool, int32_t layer, const void* q, con
     DeviceGuard dg(pool->device);
     if (!dg.ok) return fail(PKV_E_DEVICE, "cannot select the pool's device");
     cudaError_t e = pkv::launch_prefill(pool, layer, q, q_start_loc, block_tables, max_blocks, ctx_lens, num_seqs,
-                                        max_q_len, scale, out, wait_prev, static_cast<cudaStream_t>(stream));
+                                        max_q_len, scale, out, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PKV_OK : pkv::cuda_fail(e, "prefill launch");
 }
 
@@ -826,7 +824,7 @@ pkv_status pkv_prefill_attn(pkv_pool* pool, int32_t layer, const void* q, const 
                             int32_t max_q_len, float scale, void* out, void* stream)
 {
     return prefill_impl(pool, layer, q, q_start_loc, block_tables, max_blocks, ctx_lens, num_seqs, max_q_len, scale,
-                        out, true, stream);
+                        out, stream);
 }
 
 // ------------------------------------------------------------------- step
@@ -881,21 +879,24 @@ pkv_status pkv_step(pkv_pool* pool, const pkv_step_desc* st, void* workspace, si
         if (P > 0) {  // the prefill tokens' kv_append; the decode rows append inside the decode kernel
             e = launch_append_any(pool, layer, kl + B * tok, vl + B * tok, st->slot_mapping + B, st->num_tokens - B, s);
             if (e != cudaSuccess) return pkv::cuda_fail(e, "kv_append launch");
-        }
-        if (B > 0) {
-            // decode-only steps: every layer after the first overlaps its prologue with the previous layer
-            e = launch_decode_any(pool, layer, ql, st->block_tables, st->max_blocks, st->ctx_lens, B, st->scale, ol,
-                                  workspace, kl, vl, st->slot_mapping, s, P == 0 && i > 0);
-            if (e != cudaSuccess) return pkv::cuda_fail(e, "decode launch");
-        }
-        if (P > 0) {
-            // After decode rows the prefill launch does not wait for the decode kernel (it writes only the decode
-            // rows' outputs and their own blocks, nothing prefill reads): its CTAs start on the SMs the decode
-            // kernel leaves. Without decode rows it waits for the kv_append launch that wrote the chunk's keys.
+            // Prefill first (it waits for the append that wrote the chunk's keys), then the decode rows, launched
+            // with a programmatic dependency on it but without waiting: decode reads and writes nothing prefill
+            // touches, so its CTAs fill the SMs prefill leaves idle and take the rest as prefill drains. The next
+            // layer's append is an ordinary launch and waits for both.
             pkv_status r = prefill_impl(pool, layer, ql, st->q_start_loc + B,
                                         st->block_tables + (int64_t)B * st->max_blocks, st->max_blocks,
-                                        st->ctx_lens + B, P, st->max_q_len, st->scale, ol, B == 0, stream);
+                                        st->ctx_lens + B, P, st->max_q_len, st->scale, ol, stream);
             if (r) return r;
+            if (B > 0) {
+                e = launch_decode_any(pool, layer, ql, st->block_tables, st->max_blocks, st->ctx_lens, B, st->scale,
+                                      ol, workspace, kl, vl, st->slot_mapping, s, 2);
+                if (e != cudaSuccess) return pkv::cuda_fail(e, "decode launch");
+            }
+        } else {
+            // decode-only steps: every layer after the first overlaps its prologue with the previous layer
+            e = launch_decode_any(pool, layer, ql, st->block_tables, st->max_blocks, st->ctx_lens, B, st->scale, ol,
+                                  workspace, kl, vl, st->slot_mapping, s, i > 0 ? 1 : 0);
+            if (e != cudaSuccess) return pkv::cuda_fail(e, "decode launch");
         }
     }
     return PKV_OK;

@@ -159,6 +159,7 @@ struct I8Args {
     const __half* v_new;
     const int64_t* slots;
     int append;
+    int no_wait;             // launched after a kernel whose results it does not read: skip the dependency wait
     unsigned int* status;
     // cascade: rows [group_start[i], group_start[i+1]) share their first group_blocks[i] blocks. In CASCADE mode
     // the kernel computes those shared partitions for the group's rows at once; otherwise (group_start set) a
@@ -302,7 +303,7 @@ __global__ void __launch_bounds__(kQWarps * 32, ROWS16 ? 3 : 4)
 
     // Only lengths, tables and this layer's codes were read so far; with a programmatic dependency on the
     // previous layer's kernel, wait for it before reading q or the new K/V and touching the workspace.
-    pdl_wait();
+    if (!a.no_wait) pdl_wait();
 
     // The new token: quantised here by the warp that streams its block, and stored by c == 0's warp 0.
     const int new_t = (ctx - 1) % kBlockSize, new_i = (ctx - 1) / kBlockSize - blk_lo;
@@ -613,7 +614,7 @@ __global__ void __launch_bounds__(kQWarps * 32, ROWS16 ? 3 : 4)
 }
 
 template <bool ROWS16, bool CASCADE>
-cudaError_t launch_i8(const CUtensorMap& tmap, const I8Args& a, dim3 grid, cudaStream_t stream, bool pdl)
+cudaError_t launch_i8(const CUtensorMap& tmap, const I8Args& a, dim3 grid, cudaStream_t stream, int pdl)
 {
     static bool attr_set[64] = {};
     int dev = 0;
@@ -690,7 +691,7 @@ cudaError_t launch_decode_i8(const PoolGeom& g, const TensorMap128& i8_tmap, int
                              const int32_t* tables, int max_blocks, const int32_t* ctx_lens, int num_seqs,
                              float scale, void* out, const DecodeWs& ws, int partition_tokens, const void* k_new,
                              const void* v_new, const int64_t* slots, unsigned int* status, cudaStream_t stream,
-                             bool pdl, const int32_t* group_start, const int32_t* group_blocks, int num_groups)
+                             int pdl, const int32_t* group_start, const int32_t* group_blocks, int num_groups)
 {
     if (num_seqs == 0) return cudaSuccess;
     I8Args a;
@@ -722,6 +723,7 @@ cudaError_t launch_decode_i8(const PoolGeom& g, const TensorMap128& i8_tmap, int
     a.v_new = static_cast<const __half*>(v_new);
     a.slots = slots;
     a.append = k_new != nullptr;
+    a.no_wait = pdl == 2;
     a.status = status;
     a.group_start = num_groups > 0 ? group_start : nullptr;
     a.group_blocks = num_groups > 0 ? group_blocks : nullptr;
@@ -775,7 +777,7 @@ cudaError_t launch_decode_i8_shared_prefix(const PoolGeom& g, const TensorMap128
     CUtensorMap tmap;
     memcpy(&tmap, i8_tmap.bytes, sizeof(tmap));
     const dim3 grid(a.max_parts, g.num_heads * a.slices, num_groups * a.max_slices);
-    return launch_i8<true, true>(tmap, a, grid, stream, false);
+    return launch_i8<true, true>(tmap, a, grid, stream, 0);
 }
 
 }  // namespace pkv

@@ -111,9 +111,11 @@ cudaError_t launch_decode(const PoolGeom& g, int layer, const void* q, const int
                           const int32_t* ctx_lens, int num_seqs, float scale, void* out, const DecodeWs& ws,
                           int partition_tokens, const void* k_new, const void* v_new, const int64_t* slots,
                           unsigned int* status, cudaStream_t stream, const int32_t* group_start = nullptr,
-                          const int32_t* group_blocks = nullptr, int num_groups = 0, bool pdl = false);
-// pdl: launched with a programmatic dependency on the stream's previous kernel (the previous layer's decode
-// in a decode-only pkv_step): its CTAs load lengths, tables and K/V tiles, then wait for that kernel.
+                          const int32_t* group_blocks = nullptr, int num_groups = 0, int pdl = 0);
+// pdl: 1 = launched with a programmatic dependency on the stream's previous kernel (the previous layer's
+// decode in a decode-only pkv_step): its CTAs load lengths, tables and K/V tiles, then wait for that kernel;
+// 2 = the same launch without the wait (after a kernel whose results it does not read: the prefill launch of
+// a mixed pkv_step layer), so its CTAs run beside that kernel's.
 
 // pkv_int8.cu: the 8-bit cache (quantising kv_append; decode that dequantises in its loaders).
 cudaError_t launch_kv_append_i8(const PoolGeom& g, int layer, const void* k, const void* v, const int64_t* slots,
@@ -123,7 +125,7 @@ cudaError_t launch_decode_i8(const PoolGeom& g, const TensorMap128& i8_tmap, int
                              const int32_t* tables, int max_blocks, const int32_t* ctx_lens, int num_seqs,
                              float scale, void* out, const DecodeWs& ws, int partition_tokens, const void* k_new,
                              const void* v_new, const int64_t* slots, unsigned int* status, cudaStream_t stream,
-                             bool pdl = false, const int32_t* group_start = nullptr,
+                             int pdl = 0, const int32_t* group_start = nullptr,
                              const int32_t* group_blocks = nullptr, int num_groups = 0);
 // Cascade over an 8-bit pool: the partitions wholly inside each group's shared prefix, for every row of the
 // group at once.
@@ -148,7 +150,7 @@ cudaError_t launch_decode_group(const PoolGeom& g, const TensorMap128& kv_tmap, 
                                 const int32_t* tables, int max_blocks, const int32_t* ctx_lens, int num_seqs,
                                 float scale, void* out, const DecodeWs& ws, int partition_tokens, const void* k_new,
                                 const void* v_new, const int64_t* slots, unsigned int* status, cudaStream_t stream,
-                                bool pdl = false, const int32_t* group_start = nullptr,
+                                int pdl = 0, const int32_t* group_start = nullptr,
                                 const int32_t* group_blocks = nullptr, int num_groups = 0);
 // pkv_blocks.cu: whole-block copies inside the pool (copy-on-write) and to / from host memory (swap).
 cudaError_t launch_copy_blocks(const PoolGeom& g, const int32_t* pairs, int n, unsigned int* status,
@@ -162,6 +164,6 @@ cudaError_t launch_wait_probe(uint64_t timeout_ns, unsigned int* status, cudaStr
 bool encode_kv_tmap(const PoolGeom& g, TensorMap128* out, std::string* err);
 cudaError_t launch_prefill(const pkv_pool* pool, int layer, const void* q, const int32_t* q_start,
                            const int32_t* tables, int max_blocks, const int32_t* ctx_lens, int num_seqs,
-                           int max_q_len, float scale, void* out, bool wait_prev, cudaStream_t stream);
+                           int max_q_len, float scale, void* out, cudaStream_t stream);
 
 }  // namespace pkv

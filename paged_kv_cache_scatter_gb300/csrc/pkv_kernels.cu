@@ -137,6 +137,7 @@ struct DecodeArgs {
     const __half* v_new;
     const int64_t* slots;   // [B] when append
     int append;
+    int no_wait;             // launched after a kernel whose results it does not read: skip the dependency wait
     unsigned int* status;
     // cascade: a row's partitions wholly inside its group's shared prefix were computed already
     const int32_t* group_start;   // [num_groups + 1] or NULL
@@ -251,7 +252,7 @@ __global__ void __launch_bounds__(WARPS * 32) decode_kernel(const DecodeArgs a)
     // Everything above reads only what the step's earlier layers never write (lengths, tables, this
     // layer's K/V). With a programmatic dependency on the previous layer's kernel, wait for it here, before
     // reading q or the new K/V and before touching the workspace or the output.
-    pdl_wait();
+    if (!a.no_wait) pdl_wait();
 
     // The new token (position ctx - 1) lives in this partition's last block.
     const int last_local = ((ctx - 1) >> 4) - blk_lo;
@@ -522,7 +523,7 @@ cudaError_t launch_decode(const PoolGeom& g, int layer, const void* q, const int
                           const int32_t* ctx_lens, int num_seqs, float scale, void* out, const DecodeWs& w,
                           int partition_tokens, const void* k_new, const void* v_new, const int64_t* slots,
                           unsigned int* status, cudaStream_t stream, const int32_t* group_start,
-                          const int32_t* group_blocks, int num_groups, bool pdl)
+                          const int32_t* group_blocks, int num_groups, int pdl)
 {
     if (num_seqs == 0) return cudaSuccess;
     // Cascade decode's private keys are a few hundred per row: CTAs of two warps (half the shared memory, so
@@ -562,6 +563,7 @@ cudaError_t launch_decode(const PoolGeom& g, int layer, const void* q, const int
     a.v_new = static_cast<const __half*>(v_new);
     a.slots = slots;
     a.append = k_new != nullptr;
+    a.no_wait = pdl == 2;
     a.status = status;
     a.group_start = num_groups > 0 ? group_start : nullptr;
     a.group_blocks = group_blocks;

@@ -196,7 +196,6 @@ struct PrefillArgs {
     int tok;           // query tokens per CTA: 128 / hpc; MMA row r is token r % tok of head r / tok
     int layer;
     int max_q_len;
-    int wait_prev;     // wait for the stream's previous kernel before reading any input
     int64_t num_blocks;
     float scale_log2;
     unsigned int* status;
@@ -388,12 +387,11 @@ __global__ void __launch_bounds__(Cfg<kI8>::kThreads, 1) prefill_kernel(const __
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     // Launched with a programmatic dependency on the stream's previous kernel: this grid's CTAs may be
-    // placed on SMs that kernel has left (or never used) before it ends and, with wait_prev, wait here for
-    // its results. Nothing in global memory is read before this point, so any earlier kernel may produce the
-    // inputs. Without wait_prev (pkv_step after its decode launch, which writes nothing this kernel reads)
-    // they go on at once and overlap the decode kernel's last CTAs.
+    // placed on SMs that kernel has left (or never used) before it ends, and wait here for its results.
+    // Nothing in global memory is read before this point, so any earlier kernel may produce the inputs.
+    // (The trigger at the top lets a following decode launch of a mixed pkv_step layer start beside it.)
     pdl_trigger();
-    if (a.wait_prev) pdl_wait();
+    pdl_wait();
 
     // ---- validate this sequence's metadata (all threads agree)
     const int q0 = __ldg(a.q_start + s);
@@ -802,7 +800,7 @@ __global__ void __launch_bounds__(Cfg<kI8>::kThreads, 1) prefill_kernel(const __
 
 cudaError_t launch_prefill(const pkv_pool* pool, int layer, const void* q, const int32_t* q_start,
                            const int32_t* tables, int max_blocks, const int32_t* ctx_lens, int num_seqs, int max_q_len,
-                           float scale, void* out, bool wait_prev, cudaStream_t stream)
+                           float scale, void* out, cudaStream_t stream)
 {
     const bool i8 = pool->geom.dtype == PKV_DTYPE_INT8;
     static bool attr_set[2][64] = {};
@@ -834,7 +832,6 @@ cudaError_t launch_prefill(const pkv_pool* pool, int layer, const void* q, const
     a.tok = kRows / a.hpc;
     a.layer = layer;
     a.max_q_len = max_q_len;
-    a.wait_prev = wait_prev ? 1 : 0;
     a.num_blocks = pool->geom.num_blocks;
     a.scale_log2 = scale * 1.4426950408889634f;
     a.status = pool->status_dev;
