@@ -103,8 +103,14 @@ CONFIG_TEXT = {
                    "pool to one page-locked host buffer, one launch each way",
     "gqa_decode": "batch-32 decode at 2,300 context tokens per row, 32 layers, 8 K/V heads serving 32 query heads "
                   "(grouped-query attention, 131,072 B of K/V per token), 28,608-block (60 GB) shuffled pool, "
-                  "kv_append of 1 token per row",
+                  "kv_append of 1 token per row; pool partition 4,096 tokens (one per row)",
 }
+
+# The pool's split-K partition length per workload (0: the library's default, 1,024 tokens), the best measured
+# on this GB300: the batch-32 MHA rows stream in fewer, longer CTAs at 2,048 (0.951 of HBM peak against 0.926
+# at 1,024); the grouped-head workload's 2,300-token rows take one partition each at 4,096, so its 256 CTAs
+# run in one wave (0.936 against 0.788 at 1,024: 768 CTAs over 456 resident slots).
+CONFIG_PARTITION = {"average_decode": 2048, "long_decode": 2048, "gqa_decode": 4096}
 
 CONFIG_DTYPE = {"average_decode_int8": "int8", "mixed_prefill_int8": "int8", "shared_prefix_cascade_int8": "int8"}
 SWAP_BLOCKS, SWAP_POOL = 384, 1024
@@ -434,6 +440,8 @@ def run_ours(args):
     else:
         pool_t = torch.empty(workloads.pool_shape(wl0.num_blocks, L, H), dtype=torch.float16, device=dev)
         workloads.fill_normal_fp16_(pool_t, workloads.value_seed(wl0.seed, "pool"))
+    if not args.partition_tokens:
+        args.partition_tokens = CONFIG_PARTITION.get(args.config, 0)
     pool = pkv.Pool(pool_t, wl0.num_blocks, num_layers=L, num_heads=H, partition_tokens=args.partition_tokens,
                     num_q_heads=Hq, dtype=dtype)
     gen = torch.Generator(device=dev)

@@ -87,8 +87,10 @@ typedef struct pkv_pool_desc {
     int32_t block_size;   /* must be 16 */
     int32_t dtype;        /* PKV_DTYPE_FP16 or PKV_DTYPE_INT8 */
     int32_t partition_tokens; /* decode split-K partition size in tokens; 0 = default 1024;
-                                 a multiple of 64 in [64, 2048]. Results depend only on a
-                                 row's ctx_len and this value, never on the rest of the batch. */
+                                 a multiple of 64 in [64, 2048] for FP16 pools with one query
+                                 head per K/V head, in [64, 4096] for grouped-head and 8-bit
+                                 pools. Results depend only on a row's ctx_len and this value,
+                                 never on the rest of the batch. */
     void* dev_base;       /* device pointer to the pool, 256-byte aligned; NULL makes a host-only
                              pool (block manager and step metadata only; kernel calls refused) */
     size_t bytes;         /* size of that allocation, >= pkv_pool_bytes(desc) */

@@ -66,7 +66,7 @@ constexpr int kGWarps = 4;                   // warps per CTA
 constexpr int kGStages = 2;                  // ring stages per warp
 constexpr int kGStage = 2 * kTileBytes;      // K tile + V tile of one block (8 KB)
 constexpr int kGRows = 16;                   // query heads per CTA at most (the MMA's M)
-constexpr int kGMaxBlocks = kMaxPartition / kBlockSize;
+constexpr int kGMaxBlocks = kMaxPartitionTiles / kBlockSize;
 constexpr int kGMergeStride = kHeadDim + 4;  // floats per row of the merge scratch (bank-conflict padding)
 
 // shared memory, offsets from a 1,024-byte aligned base
@@ -204,7 +204,7 @@ __global__ void __launch_bounds__(kGWarps * 32) decode_group_kernel(const __grid
     auto rh = [&](int f) { return (int64_t)(r + f / hpr) * a.num_q_heads + h0 + f % hpr; };
     const int blk_lo = tok_lo / kBlockSize;
     const int blk_hi = (min(tok_lo + span, ctx) + kBlockSize - 1) / kBlockSize;
-    const int count = blk_hi - blk_lo;  // <= kGMaxBlocks (partition_tokens <= 2,048, a multiple of 64)
+    const int count = blk_hi - blk_lo;  // <= kGMaxBlocks (partition_tokens <= 4,096, a multiple of 64)
 
     int32_t* ids = reinterpret_cast<int32_t*>(smem + kGSmIds);
     const int32_t* trow = a.tables + (int64_t)r * a.max_blocks;

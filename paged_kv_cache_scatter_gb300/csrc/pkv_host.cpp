@@ -156,8 +156,12 @@ pkv_status pkv_pool_create(const pkv_pool_desc* d, pkv_pool** out)
     if (!host_only && d->bytes < pkv_pool_bytes(d))
         return fail(PKV_E_INVALID, "pool allocation smaller than pkv_pool_bytes()");
     int part = d->partition_tokens ? d->partition_tokens : pkv::kDefaultPartition;
-    if (part % 64 != 0 || part < 64 || part > pkv::kMaxPartition)
-        return fail(PKV_E_INVALID, "partition_tokens must be a multiple of 64 in [64, %d]", pkv::kMaxPartition);
+    // the one-head decode kernel of FP16 pools with one query head per K/V head keeps a partition's block ids
+    // in its lanes (2,048 tokens); the grouped-head and 8-bit kernels keep them in shared memory (4,096)
+    const bool one_head = d->dtype == PKV_DTYPE_FP16 && (d->num_q_heads == 0 || d->num_q_heads == d->num_heads);
+    const int max_part = one_head ? pkv::kMaxPartition : pkv::kMaxPartitionTiles;
+    if (part % 64 != 0 || part < 64 || part > max_part)
+        return fail(PKV_E_INVALID, "partition_tokens must be a multiple of 64 in [64, %d] for this pool", max_part);
 
     pkv_pool* p = new (std::nothrow) pkv_pool;
     if (!p) return fail(PKV_E_NOMEM, "host allocation failed");

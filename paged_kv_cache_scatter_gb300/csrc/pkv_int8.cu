@@ -117,7 +117,7 @@ constexpr int kQStages = 2;
 constexpr int kQStage = 2 * kCodesBytes;  // K codes at 0, V codes at 2,048: both 1 KB aligned for the swizzle
 constexpr int kQScaleStage = 2 * 4 * kBlockSize;  // K scales, then V scales
 constexpr int kQRows = 16;
-constexpr int kQMaxBlocks = kMaxPartition / kBlockSize;
+constexpr int kQMaxBlocks = kMaxPartitionTiles / kBlockSize;
 constexpr int kQMergeStride = kHeadDim + 4;
 
 constexpr int kQSmRing = 0;

@@ -21,7 +21,8 @@ constexpr int kTileBytesI8 = kBlockSize * kHeadDim + 4 * kBlockSize;  // 2,112 B
 // spread over the GPU. Measured on the batch-32 decode workloads (1,024 beat
 // 512, 768 and 1,536 on 4 of 5 length draws).
 constexpr int kDefaultPartition = 1024;
-constexpr int kMaxPartition = 2048;
+constexpr int kMaxPartition = 2048;         // pools whose decode is the one-head kernel (block ids in its lanes)
+constexpr int kMaxPartitionTiles = 4096;    // grouped-head and 8-bit pools (block ids in shared memory)
 constexpr int kMaxPartitionsPerRow = 4096;  // the decode kernel merges at most this many partitions of a row
 
 struct Seq {

@@ -57,6 +57,17 @@ def test_pool_create_refuses_bad_descriptor(pkv, field, value):
     assert pkv.load().pkv_last_error_string()
 
 
+def test_partition_limit_depends_on_the_decode_kernel(pkv):
+    # one-head FP16 pools: up to 2,048 tokens per partition; grouped-head and 8-bit pools: up to 4,096
+    assert pkv.Pool(None, 64, num_heads=32, partition_tokens=2048).handle
+    for kw in ({"num_heads": 8, "num_q_heads": 32}, {"num_heads": 32, "dtype": "int8"}):
+        assert pkv.Pool(None, 64, partition_tokens=4096, **kw).handle
+        with pytest.raises(pkv.PkvError):
+            pkv.Pool(None, 64, partition_tokens=4160, **kw)
+    with pytest.raises(pkv.PkvError):
+        pkv.Pool(None, 64, num_heads=32, partition_tokens=2112)
+
+
 def test_grouped_query_pool_ledger_and_workspace(pkv):
     # "Inference Infrastructure" (seeitflow), KV cache arithmetic: 8 K/V heads x 128 dims x 2 (K and V)
     # x 2 bytes x 32 layers = 131,072 B per token, 2,097,152 B per 16-token block.

@@ -106,8 +106,8 @@ def _oracle_row(mini, layer_tokens, q_row, ctx, nblk):
     return ref[0]
 
 
-def _decode_case(pkv, big_pool, wl, layers, rows, seed):
-    pool = pkv.Pool(big_pool, N_BLOCKS, num_layers=L, num_heads=H)
+def _decode_case(pkv, big_pool, wl, layers, rows, seed, partition=0):
+    pool = pkv.Pool(big_pool, N_BLOCKS, num_layers=L, num_heads=H, partition_tokens=partition)
     st = Step(pkv, pool, wl, seed)
     copies = {}
     for l in layers:
@@ -128,12 +128,14 @@ def _decode_case(pkv, big_pool, wl, layers, rows, seed):
 
 def test_full_average_decode(pkv, big_pool):
     wl = workloads.average_decode(0)
-    _decode_case(pkv, big_pool, wl, layers=(0, 13, 31), rows=range(wl.num_seqs), seed=101)
+    # the pool's partition length bench.py uses for this workload (and the library default)
+    for partition in (2048, 0):
+        _decode_case(pkv, big_pool, wl, layers=(0, 13, 31), rows=range(wl.num_seqs), seed=101, partition=partition)
 
 
 def test_full_long_decode(pkv, big_pool):
     wl = workloads.long_decode(0)
-    _decode_case(pkv, big_pool, wl, layers=(0, 31), rows=(0, 6, 12), seed=102)
+    _decode_case(pkv, big_pool, wl, layers=(0, 31), rows=(0, 6, 12), seed=102, partition=2048)
 
 
 def test_full_shared_prefix_decode(pkv, big_pool):

@@ -60,7 +60,8 @@ def test_full_gqa_decode(pkv):
     H, HQ, N = wl.num_heads, wl.q_heads, wl.num_blocks
     pool_t = torch.empty(workloads.pool_shape(N, L, H), dtype=torch.float16, device="cuda")
     workloads.fill_normal_fp16_(pool_t, workloads.value_seed(0, "pool"))
-    p = pkv.Pool(pool_t, N, num_layers=L, num_heads=H, num_q_heads=HQ)
+    # the pool's partition length bench.py uses for this workload: one 4,096-token partition per 2,300-token row
+    p = pkv.Pool(pool_t, N, num_layers=L, num_heads=H, num_q_heads=HQ, partition_tokens=4096)
     tables_d, ctx_d, qs_d, slots_d, slots = G.step_metadata(wl)
     q, k, v = _inputs(wl.num_tokens, HQ, H, 5)
     out = torch.full_like(q, float("nan"))

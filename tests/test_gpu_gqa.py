@@ -111,7 +111,7 @@ GROUPS = [(32, 8), (32, 1), (8, 1), (48, 4), (64, 2), (6, 2), (40, 8), (16, 8)]
 
 
 @pytest.mark.parametrize("hq,h", GROUPS)
-@pytest.mark.parametrize("partition", [0, 64])
+@pytest.mark.parametrize("partition", [0, 64, 4096])
 def test_gqa_decode_separate_append(pkv, hq, h, partition):
     run_gqa(pkv, _decode_wl(hq + h, h), hq, partition=partition, use_step=False)
 
@@ -129,10 +129,12 @@ def test_gqa_fused_append_equals_separate(pkv):
 
 
 @pytest.mark.parametrize("partition,ctxs", [(0, [1024, 1025, 1041, 2047, 2049, 2300, 3073]),
-                                            (64, [64, 65, 127, 129, 1000, 2300, 3073])])
+                                            (64, [64, 65, 127, 129, 1000, 2300, 3073]),
+                                            (4096, [2300, 4096, 4097, 6000, 8193])])
 def test_gqa_equal_partition_boundaries(pkv, partition, ctxs):
     # Equal-length partitions at and next to the bounds, with the decode rows' append fused into the last one.
-    wl = _decode_wl(17, 8, num_seqs=len(ctxs), max_ctx=3100, min_ctx=3100, num_layers=1, edges=False)
+    top = max(ctxs) + 30
+    wl = _decode_wl(17, 8, num_seqs=len(ctxs), max_ctx=top, min_ctx=top, num_layers=1, edges=False)
     wl.ctx_lens[:] = ctxs
     run_gqa(pkv, wl, 32, partition=partition, use_step=True)
 

@@ -140,7 +140,7 @@ def test_int8_tiny_decode_config(pkv):
 
 
 @pytest.mark.parametrize("seed", [1, 2])
-@pytest.mark.parametrize("partition", [0, 64, 2048])
+@pytest.mark.parametrize("partition", [0, 64, 2048, 4096])
 def test_int8_random_ragged_decode(pkv, seed, partition):
     run_i8(pkv, _wl(seed), partition)
 
