@@ -119,7 +119,7 @@ KERNEL_SOURCES = {
     "decode_attn": ["pkv_kernels.cu", "ptx.cuh", "pkv_internal.h"],
     "decode_group_attn": ["pkv_decode_group.cu", "pkv_kernels.cu", "ptx.cuh", "pkv_internal.h"],
     "decode_i8_attn": ["pkv_int8.cu", "ptx.cuh", "pkv_internal.h"],
-    "decode_cascade_attn": ["pkv_decode_group.cu", "pkv_kernels.cu", "ptx.cuh", "pkv_internal.h"],
+    "decode_cascade_attn": ["pkv_decode_group.cu", "pkv_kernels.cu", "pkv_int8.cu", "ptx.cuh", "pkv_internal.h"],
     "prefill_attn": ["pkv_prefill.cu", "ptx.cuh", "pkv_internal.h"],
 }
 
