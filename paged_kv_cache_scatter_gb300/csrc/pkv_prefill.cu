@@ -331,10 +331,14 @@ __device__ __forceinline__ void scale_columns(uint32_t* s, const float4* scales)
 #pragma unroll
     for (int e = 0; e < N; e += 4) {
         const float4 k4 = scales[e / 4];
-        s[e] = __float_as_uint(__uint_as_float(s[e]) * k4.x);
-        s[e + 1] = __float_as_uint(__uint_as_float(s[e + 1]) * k4.y);
-        s[e + 2] = __float_as_uint(__uint_as_float(s[e + 2]) * k4.z);
-        s[e + 3] = __float_as_uint(__uint_as_float(s[e + 3]) * k4.w);
+        const float2 a = f32x2_unpack(mul_f32x2(f32x2_pack(__uint_as_float(s[e]), __uint_as_float(s[e + 1])),
+                                                f32x2_pack(k4.x, k4.y)));
+        const float2 b = f32x2_unpack(mul_f32x2(f32x2_pack(__uint_as_float(s[e + 2]), __uint_as_float(s[e + 3])),
+                                                f32x2_pack(k4.z, k4.w)));
+        s[e] = __float_as_uint(a.x);
+        s[e + 1] = __float_as_uint(a.y);
+        s[e + 2] = __float_as_uint(b.x);
+        s[e + 3] = __float_as_uint(b.y);
     }
 }
 
@@ -346,9 +350,8 @@ template <bool kTail>
 __device__ __forceinline__ void softmax_quarter_vscaled(uint32_t* s, float scale_log2, float m_sub, float& l,
                                                         const float4* vscales, int nkeys)
 {
-    float ls[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) ls[u] = 0.f;
+    const uint64_t sc2 = f32x2_pack(scale_log2, scale_log2), nm2 = f32x2_pack(-m_sub, -m_sub);
+    uint64_t acc[2] = {f32x2_pack(0.f, 0.f), f32x2_pack(0.f, 0.f)};
 #pragma unroll
     for (int e = 0; e < 32; e += 4) {
         const float4 v4 = vscales[e / 4];
@@ -359,15 +362,16 @@ __device__ __forceinline__ void softmax_quarter_vscaled(uint32_t* s, float scale
         }
 #pragma unroll
         for (int u = 0; u < 4; u += 2) {
-            const float pa = ex2(fmaf(__uint_as_float(s[e + u]), scale_log2, -m_sub));
-            const float pb = ex2(fmaf(__uint_as_float(s[e + u + 1]), scale_log2, -m_sub));
-            ls[u] += pa;
-            ls[u + 1] += pb;
-            const __half2 hp = __floats2half2_rn(pa * vs[u], pb * vs[u + 1]);
-            s[(e + u) >> 1] = *reinterpret_cast<const uint32_t*>(&hp);
+            const float2 x =
+                f32x2_unpack(fma_f32x2(f32x2_pack(__uint_as_float(s[e + u]), __uint_as_float(s[e + u + 1])), sc2, nm2));
+            const uint64_t p2 = f32x2_pack(ex2(x.x), ex2(x.y));
+            acc[u >> 1] = add_f32x2(acc[u >> 1], p2);
+            const float2 pv = f32x2_unpack(mul_f32x2(p2, f32x2_pack(vs[u], vs[u + 1])));
+            s[(e + u) >> 1] = pack_half2(pv.x, pv.y);
         }
     }
-    l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+    const float2 a0 = f32x2_unpack(acc[0]), a1 = f32x2_unpack(acc[1]);
+    l += (a0.x + a0.y) + (a1.x + a1.y);
 }
 
 // tmap: FP16 pools, 2 KB boxes of one block's 16 rows of one 64-dim half; 8-bit pools, a 2 KB box of one
