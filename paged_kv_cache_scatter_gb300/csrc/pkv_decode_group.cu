@@ -307,14 +307,21 @@ __global__ void __launch_bounds__(kGWarps * 32) decode_group_kernel(const __grid
         __syncwarp();
 
         // S = Q K^T: k-step ks covers dims 16ks..16ks+15; matrices (tokens 0-7 | 8-15) x (low | high 8 dims).
+        // even and odd k-steps accumulate apart (two chains of 4 dependent MMAs per tile instead of one of 8),
+        // added at the end
         float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        float sodd[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
             uint32_t b[4];
             ldsm_x4(kt + sw_off(rr + (mi >> 1) * 8, 2 * ks + (mi & 1)), b);
-            mma_16816(sacc[0], qa[ks], b[0], b[1]);
-            mma_16816(sacc[1], qa[ks], b[2], b[3]);
+            mma_16816((ks & 1) ? sodd[0] : sacc[0], qa[ks], b[0], b[1]);
+            mma_16816((ks & 1) ? sodd[1] : sacc[1], qa[ks], b[2], b[3]);
         }
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sacc[nt][e] += sodd[nt][e];
         // fragment element e of tile nt: row g (e < 2) or g + 8, token 8nt + 2tq + (e & 1)
         float sv[2][4];
 #pragma unroll
