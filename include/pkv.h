@@ -253,8 +253,9 @@ size_t pkv_decode_workspace_bytes(const pkv_pool* pool, int32_t num_seqs, int32_
  * attends positions 0..ctx_lens[r]-1 of row r's blocks, including the token
  * appended this step: out = softmax(q K^T * scale) V ("Inference
  * Infrastructure" (seeitflow), the decode steps). Long rows are split into
- * partitions of partition_tokens keys whose softmax statistics are merged
- * exactly ("The inference engine" (wpnews), "IO-aware attention").
+ * the fewest partitions of at most partition_tokens keys, of equal length in
+ * whole blocks, whose softmax statistics are merged exactly ("The inference
+ * engine" (wpnews), "IO-aware attention").
  *   q            device FP16 [num_seqs, num_q_heads, 128]
  *   block_tables device int32 [num_seqs, max_blocks]
  *   ctx_lens     device int32 [num_seqs], 1 <= ctx_len <= 16*max_blocks
@@ -284,12 +285,11 @@ pkv_status pkv_decode_attn(pkv_pool* pool, int32_t layer, const void* q, const i
  * once per group instead of once per row; the rest of each row runs as in
  * pkv_decode_attn, which merges all partitions. max_group_rows = the largest
  * group. Every pool kind: FP16 with any G = num_q_heads / num_heads, and
- * 8-bit (codes dequantised as in pkv_decode_attn; the 8-bit pool keeps its
- * fixed partitions of partition_tokens). No append: call pkv_kv_append
- * first. Partition plan: a row's shared prefix [0, S) and the rest [S, ctx)
- * are each cut into partitions of partition_tokens (so a row can have one
- * partition more than in pkv_decode_attn); results are deterministic for a
- * given grouping. The workspace must hold pkv_decode_cascade_workspace_bytes. */
+ * 8-bit (codes dequantised as in pkv_decode_attn). No append: call
+ * pkv_kv_append first. Partition plan: a row's shared prefix [0, S) is cut
+ * into partitions of partition_tokens, the rest [S, ctx) as pkv_decode_attn
+ * cuts a row (so a row can have one partition more than in pkv_decode_attn);
+ * results are deterministic for a given grouping. The workspace must hold pkv_decode_cascade_workspace_bytes. */
 pkv_status pkv_decode_attn_cascade(pkv_pool* pool, int32_t layer, const void* q, const int32_t* block_tables,
                                    int32_t max_blocks, const int32_t* ctx_lens, int32_t num_seqs,
                                    const int32_t* group_start, const int32_t* group_blocks, int32_t num_groups,

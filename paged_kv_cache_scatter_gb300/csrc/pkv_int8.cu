@@ -94,7 +94,8 @@ __global__ void __launch_bounds__(256) kv_append_i8_kernel(char* __restrict__ po
 // TMA with the 128-byte swizzle and the two 64-byte scale rows by bulk copies
 // into a side array, all on one mbarrier. (Four stages measured slower than
 // two: the rate is not set by the bytes in flight.) Per block a warp runs the attention on the tensor cores with
-// mma.sync m16n8k16 (FP16 operands, FP32 accumulation):
+// mma.sync m16n8k16 (FP16 operands, FP32 accumulation); with up to 8 query heads, in the transposed form described
+// at the kernel (the query heads as the MMA's 8 columns); with more, as follows:
 //   S = Q C_K^T      codes become FP16 exactly (byte + 1024 - 1152), each
 //                    32-bit word of 4 codes feeding one k-step pair; the
 //                    contraction order of the 16 dims in a chunk is permuted
@@ -199,14 +200,22 @@ __device__ __forceinline__ unsigned int q_atomic_add_acq_rel(unsigned int* p, un
     return old;
 }
 
-// Up to 8 query heads per CTA: four CTAs per SM (at most 128 registers a thread; shared memory allows more): an
-// 8-bit CTA carries half the bytes of an FP16 one, so more of them in flight cover more of each other's start-up
-// (+4 % on the batch-32 step against three per SM, a few spilled registers included). 16 query heads per CTA
-// need more registers: three per SM.
+// Up to 8 query heads per CTA: four CTAs per SM (128 registers a thread; the transposed form below fits them
+// without spills, five CTAs at 96 registers spill and ran 7 % slower). An 8-bit CTA carries half the bytes of an
+// FP16 one, so more of them in flight cover more of each other's start-up. 16 fragment rows (up to 16 query
+// heads, or cascade's rows of a group) need more registers: three per SM.
+//
+// Transposed form (kT): with R <= 8 query heads the products run as S^T = C_K Q^T and O^T = C_V^T P'^T, the
+// 16 MMA rows being a block's 16 tokens (for S^T) or 16 dims (for O^T) and the 8 columns the query heads, so a
+// block takes 16 MMAs instead of 32 and O^T 32 accumulators a thread instead of 64. Rows of O^T: in 16-dim
+// chunk c, row g is dim 16c + 2g and row g + 8 dim 16c + 2g + 1 (a transposed ldmatrix of the codes gives
+// token pairs of those two dims in one word). P' moves from S^T's accumulator layout to the B operand's by
+// four shuffles a block.
 template <bool ROWS16, bool CASCADE>
 __global__ void __launch_bounds__(kQWarps * 32, ROWS16 ? 3 : 4)
     decode_i8_kernel(const __grid_constant__ CUtensorMap tmap, const I8Args a)
 {
+    constexpr bool kT = !ROWS16 && !CASCADE;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     const uint32_t sb = smem_u32(smem);
@@ -219,7 +228,7 @@ __global__ void __launch_bounds__(kQWarps * 32, ROWS16 ? 3 : 4)
     // rows of one group as 16 fragment rows hold, over the group's shared prefix.
     const int hpr = a.rows;
     const int h0 = kvh * a.group + c * hpr;
-    int r, R, nseq, ctx, nparts, tok_lo, slot_p;
+    int r, R, nseq, ctx, nparts, tok_lo, slot_p, span = a.part_tokens;
     if (CASCADE) {
         const int spc = kQRows / hpr;
         const int grp = blockIdx.z / a.max_slices, sl = blockIdx.z % a.max_slices;
@@ -253,15 +262,19 @@ __global__ void __launch_bounds__(kQWarps * 32, ROWS16 ? 3 : 4)
             }
             S = __ldg(a.group_blocks + lo) * kBlockSize;
         }
+        // [S, ctx) goes into as few partitions as part_tokens allows, of equal length in whole blocks, so that
+        // no short partition's CTA trails the launch
         const int nsh = (S + a.part_tokens - 1) / a.part_tokens;
-        tok_lo = S + p * a.part_tokens;
+        const int np = (ctx - S + a.part_tokens - 1) / a.part_tokens;
+        span = ((ctx - S + np - 1) / np + kBlockSize - 1) / kBlockSize * kBlockSize;
+        tok_lo = S + p * span;
         if (tok_lo >= ctx) return;
-        nparts = nsh + (ctx - S + a.part_tokens - 1) / a.part_tokens;
+        nparts = nsh + (ctx - S + span - 1) / span;
         slot_p = nsh + p;
     }
     auto rh = [&](int f) { return (int64_t)(r + f / hpr) * a.num_q_heads + h0 + f % hpr; };
     const int blk_lo = tok_lo / kBlockSize;
-    const int blk_hi = (min(tok_lo + a.part_tokens, ctx) + kBlockSize - 1) / kBlockSize;
+    const int blk_hi = (min(tok_lo + span, ctx) + kBlockSize - 1) / kBlockSize;
     const int count = blk_hi - blk_lo;
 
     int32_t* ids = reinterpret_cast<int32_t*>(smem + kQSmIds);
@@ -335,9 +348,27 @@ __global__ void __launch_bounds__(kQWarps * 32, ROWS16 ? 3 : 4)
     }
 
     // q as the A operand in the permuted contraction order: for chunk j (dims 16j..16j+15),
-    // register 0 holds dims 16j+4tq, +1 and register 2 holds dims 16j+4tq+2, +3 of row g.
+    // register 0 holds dims 16j+4tq, +1 and register 2 holds dims 16j+4tq+2, +3 of row g. Transposed form: q as
+    // the B operand, query head g's dims 16j+4tq, +1 (register 0) and 16j+4tq+2, +3 (register 1).
     uint32_t qa[8][4];
-    {
+    uint32_t qb[8][2];
+    float bias_t[2] = {0.f, 0.f};  // transposed form: the scores' bias of query heads 2tq, 2tq+1
+    if constexpr (kT) {
+        const bool q_ok = g < R;
+        const uint2* qrow = reinterpret_cast<const uint2*>(a.q + (q_ok ? rh(g) : 0) * kHeadDim);
+        float sum = 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const uint2 v = q_ok ? __ldg(qrow + 4 * j + tq) : make_uint2(0u, 0u);
+            qb[j][0] = v.x;
+            qb[j][1] = v.y;
+            sum += half2_sum(v.x) + half2_sum(v.y);
+        }
+        sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 2);  // query head g's sum, in each of its four lanes
+        bias_t[0] = kCodeBias * __shfl_sync(0xffffffffu, sum, 8 * tq);
+        bias_t[1] = kCodeBias * __shfl_sync(0xffffffffu, sum, 8 * tq + 4);
+    } else {
         const bool lo_ok = g < R, hi_ok = ROWS16 && g + 8 < R;
         const uint32_t* qlo = reinterpret_cast<const uint32_t*>(a.q + (lo_ok ? rh(g) : 0) * kHeadDim);
         const uint32_t* qhi = reinterpret_cast<const uint32_t*>(a.q + (hi_ok ? rh(g + 8) : 0) * kHeadDim);
@@ -351,7 +382,7 @@ __global__ void __launch_bounds__(kQWarps * 32, ROWS16 ? 3 : 4)
     }
     // the scores' bias: 1,152 * sum(q) of rows g and g + 8 (q * 1,152 is exact in FP32)
     float bias_lo = 0.f, bias_hi = 0.f;
-    {
+    if constexpr (!kT) {
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             bias_lo += half2_sum(qa[j][0]) + half2_sum(qa[j][2]);
@@ -365,9 +396,9 @@ __global__ void __launch_bounds__(kQWarps * 32, ROWS16 ? 3 : 4)
         bias_hi *= kCodeBias;
     }
 
-    float o[16][4];
+    float o[kT ? 8 : 16][4];
 #pragma unroll
-    for (int nt = 0; nt < 16; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+    for (int nt = 0; nt < (kT ? 8 : 16); ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
     float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.f, l_hi = 0.f;
     float w_lo = 0.f, w_hi = 0.f;  // running sums of the FP16 weights the P V MMAs saw (this lane's tokens)
     const int mi = lane >> 3, rr = lane & 7;
@@ -391,6 +422,89 @@ __global__ void __launch_bounds__(kQWarps * 32, ROWS16 ? 3 : 4)
             }
             __syncwarp();
         }
+        if constexpr (kT) {
+            // ---- transposed form: m_lo, l_lo, w_lo belong to query head 2tq, m_hi, l_hi, w_hi to 2tq + 1
+            // S^T = C_K Q^T over chunk pairs; chunks j and j + 1 accumulate apart (shorter MMA chains)
+            float sa[2][4] = {};
+#pragma unroll
+            for (int j = 0; j < 8; j += 2) {
+                uint32_t w[4];
+                ldsm_x4(kt + code_off(rr + (mi & 1) * 8, 16 * (j + (mi >> 1))), w);  // (token g | g + 8) x (j | j+1)
+#pragma unroll
+                for (int jj = 0; jj < 2; ++jj) {
+                    const uint32_t lo = w[2 * jj] ^ 0x80808080u, hi = w[2 * jj + 1] ^ 0x80808080u;
+                    const uint32_t af[4] = {codes2_to_half2(lo, 0x4140u), codes2_to_half2(hi, 0x4140u),
+                                            codes2_to_half2(lo, 0x4342u), codes2_to_half2(hi, 0x4342u)};
+                    mma_16816(sa[jj], af, qb[j + jj][0], qb[j + jj][1]);
+                }
+            }
+            // element e: token g (e < 2) or g + 8, query head 2tq + (e & 1)
+            float ks[2], vs[2];
+            asm volatile("ld.shared.f32 %0, [%1];" : "=f"(ks[0]) : "r"(ks_s + 4 * g));
+            asm volatile("ld.shared.f32 %0, [%1];" : "=f"(ks[1]) : "r"(ks_s + 4 * (g + 8)));
+            asm volatile("ld.shared.f32 %0, [%1];" : "=f"(vs[0]) : "r"(vs_s + 4 * g));
+            asm volatile("ld.shared.f32 %0, [%1];" : "=f"(vs[1]) : "r"(vs_s + 4 * (g + 8)));
+            const bool tv[2] = {g < nvalid, g + 8 < nvalid};
+            float sv[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                sv[e] = tv[e >> 1] ? (sa[0][e] + sa[1][e] - bias_t[e & 1]) * ks[e >> 1] * a.scale_log2 : -INFINITY;
+            float mx0 = fmaxf(sv[0], sv[2]), mx1 = fmaxf(sv[1], sv[3]);
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+            }
+            const float mn0 = fmaxf(m_lo, mx0), mn1 = fmaxf(m_hi, mx1);
+            const float al0 = exp2f(m_lo - mn0), al1 = exp2f(m_hi - mn1);
+            m_lo = mn0;
+            m_hi = mn1;
+            const float p0 = exp2f(sv[0] - mn0), p1 = exp2f(sv[1] - mn1);
+            const float p2 = exp2f(sv[2] - mn0), p3 = exp2f(sv[3] - mn1);
+            l_lo = l_lo * al0 + (p0 + p2);
+            l_hi = l_hi * al1 + (p1 + p3);
+            // P' = P * scale_V, tokens past the context exactly 0; X: token g, Y: token g + 8 (query heads
+            // 2tq, 2tq + 1 in the low and high halves)
+            const uint32_t X = pack_half2(tv[0] ? p0 * vs[0] : 0.f, tv[0] ? p1 * vs[0] : 0.f);
+            const uint32_t Y = pack_half2(tv[1] ? p2 * vs[1] : 0.f, tv[1] ? p3 * vs[1] : 0.f);
+            {
+                const float2 fx = __half22float2(*reinterpret_cast<const __half2*>(&X));
+                const float2 fy = __half22float2(*reinterpret_cast<const __half2*>(&Y));
+                w_lo = w_lo * al0 + (fx.x + fy.x);
+                w_hi = w_hi * al1 + (fx.y + fy.y);
+            }
+            // B operand of P'^T: this lane takes query head g, tokens 2tq, 2tq+1 (b0) and 2tq+8, 2tq+9 (b1),
+            // from the lanes holding tokens 2tq and 2tq + 1 for query heads 2(g/2), 2(g/2) + 1
+            const int src1 = 8 * tq + (g >> 1), src2 = src1 + 4;
+            const uint32_t x1 = __shfl_sync(0xffffffffu, X, src1), x2 = __shfl_sync(0xffffffffu, X, src2);
+            const uint32_t y1 = __shfl_sync(0xffffffffu, Y, src1), y2 = __shfl_sync(0xffffffffu, Y, src2);
+            const uint32_t sel = (g & 1) ? 0x7632u : 0x5410u;
+            const uint32_t pb0 = __byte_perm(x1, x2, sel), pb1 = __byte_perm(y1, y2, sel);
+            // rescale O only when some query head's running max rose in this block
+            if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    o[c][0] *= al0;
+                    o[c][1] *= al1;
+                    o[c][2] *= al0;
+                    o[c][3] *= al1;
+                }
+            }
+            // O^T += C_V^T P'^T over chunk pairs; the word of chunk cc + u holds tokens (2tq, 2tq+1) of dims
+            // (2g, 2g+1) (tokens 0-7 in w[2u], 8-15 in w[2u + 1])
+#pragma unroll
+            for (int cc = 0; cc < 8; cc += 2) {
+                uint32_t w[4];
+                ldsm_x4_t(vt + code_off(rr + (mi & 1) * 8, 16 * (cc + (mi >> 1))), w);
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const uint32_t lo = w[2 * u] ^ 0x80808080u, hi = w[2 * u + 1] ^ 0x80808080u;
+                    const uint32_t af[4] = {codes2_to_half2(lo, 0x4240u), codes2_to_half2(lo, 0x4341u),
+                                            codes2_to_half2(hi, 0x4240u), codes2_to_half2(hi, 0x4341u)};
+                    mma_16816(o[cc + u], af, pb0, pb1);
+                }
+            }
+        } else {
 
         // S = Q C_K^T over chunk pairs (j, j+1); matrices (tokens 0-7 | 8-15) x (chunk j | j+1).
         float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
@@ -490,6 +604,7 @@ __global__ void __launch_bounds__(kQWarps * 32, ROWS16 ? 3 : 4)
                 mma_16816(o[2 * (cc + u) + 1], pa, codes2_to_half2(lo, 0x4341u), codes2_to_half2(hi, 0x4341u));
             }
         }
+        }  // not the transposed form
         __syncwarp();
         if (li + kQStages < nloc) {
             if (lane == 0) {
@@ -508,6 +623,23 @@ __global__ void __launch_bounds__(kQWarps * 32, ROWS16 ? 3 : 4)
         }
         __syncwarp();
     }
+    if constexpr (kT) {
+        // sums over the block's tokens: lanes of the same tq (query heads 2tq, 2tq + 1)
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            l_lo += __shfl_xor_sync(0xffffffffu, l_lo, off);
+            l_hi += __shfl_xor_sync(0xffffffffu, l_hi, off);
+            w_lo += __shfl_xor_sync(0xffffffffu, w_lo, off);
+            w_hi += __shfl_xor_sync(0xffffffffu, w_hi, off);
+        }
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            o[c][0] -= kCodeBias * w_lo;
+            o[c][1] -= kCodeBias * w_hi;
+            o[c][2] -= kCodeBias * w_lo;
+            o[c][3] -= kCodeBias * w_hi;
+        }
+    } else {
     l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 1);
     l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 2);
     w_lo += __shfl_xor_sync(0xffffffffu, w_lo, 1);
@@ -528,12 +660,39 @@ __global__ void __launch_bounds__(kQWarps * 32, ROWS16 ? 3 : 4)
             o[nt][3] -= kCodeBias * w_hi;
         }
     }
+    }  // not the transposed form
 
     // ---- merge the four warps (warp order); O tile nt = 2 * chunk + parity holds dims 16 chunk + 4tq + 2e + parity
     __syncthreads();
     {
         float* mo = reinterpret_cast<float*>(smem + kQSmMergeO) + warp * kQRows * kQMergeStride;
         float* mml = reinterpret_cast<float*>(smem + kQSmMergeML) + warp * kQRows * 2;
+        if constexpr (kT) {
+            // O^T element (chunk c, e): dim 16c + 2g + (e >> 1), query head 2tq + (e & 1)
+            const int h0r = 2 * tq, h1r = 2 * tq + 1;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const int d0 = 16 * c + 2 * g;
+                if (h0r < R) {
+                    mo[h0r * kQMergeStride + d0] = o[c][0];
+                    mo[h0r * kQMergeStride + d0 + 1] = o[c][2];
+                }
+                if (h1r < R) {
+                    mo[h1r * kQMergeStride + d0] = o[c][1];
+                    mo[h1r * kQMergeStride + d0 + 1] = o[c][3];
+                }
+            }
+            if (g == 0) {
+                if (h0r < R) {
+                    mml[2 * h0r] = m_lo;
+                    mml[2 * h0r + 1] = l_lo;
+                }
+                if (h1r < R) {
+                    mml[2 * h1r] = m_hi;
+                    mml[2 * h1r + 1] = l_hi;
+                }
+            }
+        } else {
 #pragma unroll
         for (int nt = 0; nt < 16; ++nt) {
             const int d0 = 16 * (nt >> 1) + 4 * tq + (nt & 1);
@@ -552,6 +711,7 @@ __global__ void __launch_bounds__(kQWarps * 32, ROWS16 ? 3 : 4)
                 mml[2 * (g + 8) + 1] = l_hi;
             }
         }
+        }  // not the transposed form
     }
     __syncthreads();
     const int d = threadIdx.x;
