@@ -110,7 +110,8 @@ CONFIG_TEXT = {
 # on this GB300: the batch-32 MHA rows stream in fewer, longer CTAs at 2,048 (0.951 of HBM peak against 0.926
 # at 1,024); the grouped-head workload's 2,300-token rows take one partition each at 4,096, so its 256 CTAs
 # run in one wave (0.936 against 0.788 at 1,024: 768 CTAs over 456 resident slots).
-CONFIG_PARTITION = {"average_decode": 2048, "long_decode": 2048, "gqa_decode": 4096, "average_decode_int8": 2048}
+CONFIG_PARTITION = {"average_decode": 2048, "long_decode": 2048, "gqa_decode": 4096, "average_decode_int8": 2048,
+                    "shared_prefix_cascade_int8": 768, "shared_prefix_cascade_gqa": 768}
 
 CONFIG_DTYPE = {"average_decode_int8": "int8", "mixed_prefill_int8": "int8", "shared_prefix_cascade_int8": "int8"}
 SWAP_BLOCKS, SWAP_POOL = 384, 1024

@@ -74,7 +74,7 @@ constexpr int kGSmRing = 0;                                       // [warp][stag
 constexpr int kGSmIds = kGSmRing + kGWarps * kGStages * kGStage;  // [kGMaxBlocks] int32
 constexpr int kGSmBars = kGSmIds + kGMaxBlocks * 4;               // [warp][stage] u64
 constexpr int kGSmFlag = kGSmBars + kGWarps * kGStages * 8;
-constexpr int kGSmBytes = kGSmFlag + 16;
+constexpr int kGSmBytes = kGSmFlag + 4 * kGRows;  // the last-arrival flag; cascade: one per row
 constexpr int kGSmAlloc = kGSmBytes + 1024;
 // the warps' merge scratch, over the ring once every copy has landed
 constexpr int kGSmMergeO = 0;                                          // [warp][16][kGMergeStride] f32
@@ -155,6 +155,9 @@ __global__ void __launch_bounds__(kGWarps * 32) decode_group_kernel(const __grid
     const int kvh = blockIdx.y / a.slices, c = blockIdx.y % a.slices;
     const int h0 = kvh * a.group + c * hpr;
     int r, R, nseq, ctx, nparts, span, tok_lo, slot_p;
+    // Cascade: the private keys' launch reads nothing this grid writes except through the split-K counters,
+    // so it may start beside this one at once (whichever partial of a row arrives last merges the row)
+    if (CASCADE) pdl_trigger();
     if (CASCADE) {
         const int spc = kGRows / hpr;  // rows per CTA
         const int grp = blockIdx.z / a.max_slices, sl = blockIdx.z % a.max_slices;
@@ -192,6 +195,10 @@ __global__ void __launch_bounds__(kGWarps * 32) decode_group_kernel(const __grid
         // As few partitions as part_tokens allows, of equal length in whole blocks (a row of 2,300 keys: 768,
         // 768, 764 rather than 1,024, 1,024, 252), so that no short partition's CTA trails the launch. The plan
         // depends only on ctx, S and part_tokens: a row's result is the same in any batch of the same grouping.
+        if (ctx <= S) {  // the group's shared prefix must lie below the row's newest token
+            if (p == 0 && blockIdx.y == 0 && threadIdx.x == 0) atomicOr(a.status, PKV_DEV_BAD_CTX);
+            return;
+        }
         const int nsh = (S + a.part_tokens - 1) / a.part_tokens;
         const int np = (ctx - S + a.part_tokens - 1) / a.part_tokens;
         span = ((ctx - S + np - 1) / np + kBlockSize - 1) / kBlockSize * kBlockSize;  // <= part_tokens
@@ -242,7 +249,9 @@ __global__ void __launch_bounds__(kGWarps * 32) decode_group_kernel(const __grid
 
     // Only lengths, tables and this layer's K/V were read so far; with a programmatic dependency on the
     // previous layer's kernel, wait for it before reading q or the new K/V and touching the workspace.
-    if (!a.no_wait) pdl_wait();
+    // Without the wait (no_wait), one CTA still waits: a cascade's private launch then ends only after the shared
+    // launch it runs beside, so work after the call in the stream finds both done.
+    if (!a.no_wait || (a.group_start && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0)) pdl_wait();
 
     // The new token (position ctx - 1) is the last token of the partition's last block.
     const int new_t = (ctx - 1) % kBlockSize, new_i = (ctx - 1) / kBlockSize - blk_lo;
@@ -307,21 +316,24 @@ __global__ void __launch_bounds__(kGWarps * 32) decode_group_kernel(const __grid
         __syncwarp();
 
         // S = Q K^T: k-step ks covers dims 16ks..16ks+15; matrices (tokens 0-7 | 8-15) x (low | high 8 dims).
-        // even and odd k-steps accumulate apart (two chains of 4 dependent MMAs per tile instead of one of 8),
-        // added at the end
+        // up to 8 query rows: even and odd k-steps accumulate apart (two chains of 4 dependent MMAs per tile
+        // instead of one of 8), added at the end; 16 rows keep one chain (their registers are spoken for)
+        constexpr bool kSplitS = !ROWS16;
         float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
         float sodd[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
             uint32_t b[4];
             ldsm_x4(kt + sw_off(rr + (mi >> 1) * 8, 2 * ks + (mi & 1)), b);
-            mma_16816((ks & 1) ? sodd[0] : sacc[0], qa[ks], b[0], b[1]);
-            mma_16816((ks & 1) ? sodd[1] : sacc[1], qa[ks], b[2], b[3]);
+            mma_16816((kSplitS && (ks & 1)) ? sodd[0] : sacc[0], qa[ks], b[0], b[1]);
+            mma_16816((kSplitS && (ks & 1)) ? sodd[1] : sacc[1], qa[ks], b[2], b[3]);
         }
+        if (kSplitS) {
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
+            for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) sacc[nt][e] += sodd[nt][e];
+                for (int e = 0; e < 4; ++e) sacc[nt][e] += sodd[nt][e];
+        }
         // fragment element e of tile nt: row g (e < 2) or g + 8, token 8nt + 2tq + (e & 1)
         float sv[2][4];
 #pragma unroll
@@ -457,12 +469,44 @@ __global__ void __launch_bounds__(kGWarps * 32) decode_group_kernel(const __grid
     }
     if (CASCADE) {
         // count the partial of each of the CTA's rows (one counter per row, K/V head and slice: the one the
-        // private keys' kernel counts with); the last partition of the row to arrive merges them
+        // private keys' kernel counts with, which may run beside this one); a row whose partials are all in
+        // is merged here, in partition order, by the same arithmetic as the private kernel's merge
+        unsigned int* flags = reinterpret_cast<unsigned int*>(smem + kGSmFlag);
         __syncthreads();
         if (threadIdx.x < nseq) {
-            __threadfence();
-            atomicAdd(a.counters + ((int64_t)(r + threadIdx.x) * a.num_kv_heads + kvh) * a.slices + c, 1u);
+            const int rr = r + threadIdx.x;
+            // the row's partitions: the prefix's nparts, then its private keys cut as the private kernel cuts them
+            const int n = __ldg(a.ctx_lens + rr) - ctx;
+            int npriv = 0;
+            if (n > 0) {
+                const int np = (n + a.part_tokens - 1) / a.part_tokens;
+                const int sp = ((n + np - 1) / np + kBlockSize - 1) / kBlockSize * kBlockSize;
+                npriv = (n + sp - 1) / sp;
+            }
+            const unsigned int total = (unsigned int)(nparts + npriv);
+            unsigned int* cnt = a.counters + ((int64_t)rr * a.num_kv_heads + kvh) * a.slices + c;
+            flags[threadIdx.x] = group_atomic_add_acq_rel(cnt, 1u) == total - 1u ? total : 0u;
         }
+        __syncthreads();
+        for (int row = row0; row < R; row += kRowStep) {
+            const int np_all = (int)flags[row / hpr];
+            if (np_all == 0) continue;
+            const int64_t base = rh(row) * a.ws_parts;
+            float M = -INFINITY;
+            for (int q = 0; q < np_all; ++q) M = fmaxf(M, __ldcg(a.ws_ml + (base + q) * 2));
+            float L = 0.f, O = 0.f;
+            for (int q = 0; q < np_all; ++q) {
+                const float wt = exp2f(__ldcg(a.ws_ml + (base + q) * 2) - M);
+                L = fmaf(wt, __ldcg(a.ws_ml + (base + q) * 2 + 1), L);
+                O = fmaf(wt, __ldcg(a.ws_o + (base + q) * kHeadDim + d), O);
+            }
+            // the private kernel's final step, so that a row's result does not depend on which launch merged it
+            // (pools with one query head per K/V head: decode_kernel divides; grouped heads: this kernel's merge)
+            a.out[rh(row) * kHeadDim + d] = __float2half_rn(a.group == 1 ? O / L : O * (1.f / L));
+        }
+        __syncthreads();
+        if (threadIdx.x < nseq && flags[threadIdx.x])
+            a.counters[((int64_t)(r + threadIdx.x) * a.num_kv_heads + kvh) * a.slices + c] = 0u;
         return;
     }
     if (nparts == 1) return;
@@ -608,15 +652,17 @@ cudaError_t launch_decode_group(const PoolGeom& g, const TensorMap128& kv_tmap, 
 }
 
 cudaError_t launch_decode_shared_prefix(const PoolGeom& g, const TensorMap128& kv_tmap, int layer, const void* q,
-                                        const int32_t* tables, int max_blocks, int num_seqs,
+                                        const int32_t* tables, int max_blocks, const int32_t* ctx_lens, int num_seqs,
                                         const int32_t* group_start, const int32_t* group_blocks, int num_groups,
-                                        int max_group_rows, float scale, const DecodeWs& ws, int partition_tokens,
-                                        unsigned int* status, cudaStream_t stream)
+                                        int max_group_rows, float scale, void* out, const DecodeWs& ws,
+                                        int partition_tokens, unsigned int* status, cudaStream_t stream)
 {
     if (num_groups == 0) return cudaSuccess;
     GroupArgs a;
     memset(&a, 0, sizeof(a));
     a.q = static_cast<const __half*>(q);
+    a.out = static_cast<__half*>(out);
+    a.ctx_lens = ctx_lens;
     a.tables = tables;
     a.max_blocks = max_blocks;
     a.pool = const_cast<char*>(g.base);

@@ -776,24 +776,29 @@ pkv_status pkv_decode_attn_cascade(pkv_pool* pool, int32_t layer, const void* q,
     const bool i8 = pool->geom.dtype == PKV_DTYPE_INT8;
     // (1) every group's shared prefix, once per group; (2) each row's own keys, whose last partition merges
     e = i8 ? pkv::launch_decode_i8_shared_prefix(pool->geom, pool->tile_tmap, layer, q, block_tables, max_blocks,
-                                                 group_start, group_blocks, num_groups, max_group_rows, scale, w,
-                                                 pool->partition_tokens, pool->status_dev, s)
+                                                 ctx_lens, group_start, group_blocks, num_groups, max_group_rows,
+                                                 scale, out, w, pool->partition_tokens, pool->status_dev, s)
            : pkv::launch_decode_shared_prefix(pool->geom, pool->tile_tmap, layer, q, block_tables, max_blocks,
-                                              num_seqs, group_start, group_blocks, num_groups, max_group_rows, scale,
-                                              w, pool->partition_tokens, pool->status_dev, s);
+                                              ctx_lens, num_seqs, group_start, group_blocks, num_groups,
+                                              max_group_rows, scale, out, w, pool->partition_tokens,
+                                              pool->status_dev, s);
     if (e != cudaSuccess) return pkv::cuda_fail(e, "cascade (shared prefix) launch");
+    // the private keys' launch runs beside the shared one (programmatic launch without the dependency wait: it
+    // reads only inputs that were ready before this call); the last partial of each row merges it. Grouped-head
+    // FP16 pools launch it after the shared one instead: beside it, the two kernels' 67 KB CTAs crowd each other
+    // (0.137 against 0.143 of the HBM peak on unique bytes; MHA 0.47 against 0.41, 8-bit 0.25 against 0.23).
     if (i8)
         e = pkv::launch_decode_i8(pool->geom, pool->tile_tmap, layer, q, block_tables, max_blocks, ctx_lens, num_seqs,
                                   scale, out, w, pool->partition_tokens, nullptr, nullptr, nullptr, pool->status_dev,
-                                  s, false, group_start, group_blocks, num_groups);
+                                  s, 2, group_start, group_blocks, num_groups);
     else if (pool->geom.group > 1)
         e = pkv::launch_decode_group(pool->geom, pool->tile_tmap, layer, q, block_tables, max_blocks, ctx_lens,
                                      num_seqs, scale, out, w, pool->partition_tokens, nullptr, nullptr, nullptr,
-                                     pool->status_dev, s, false, group_start, group_blocks, num_groups);
+                                     pool->status_dev, s, 0, group_start, group_blocks, num_groups);
     else
         e = pkv::launch_decode(pool->geom, layer, q, block_tables, max_blocks, ctx_lens, num_seqs, scale, out, w,
                                pool->partition_tokens, nullptr, nullptr, nullptr, pool->status_dev, s, group_start,
-                               group_blocks, num_groups);
+                               group_blocks, num_groups, 2);
     return e == cudaSuccess ? PKV_OK : pkv::cuda_fail(e, "cascade decode launch");
 }
 

@@ -126,7 +126,7 @@ constexpr int kQSmScales = kQSmRing + kQWarps * kQStages * kQStage;  // [warp][s
 constexpr int kQSmIds = kQSmScales + kQWarps * kQStages * kQScaleStage;
 constexpr int kQSmBars = kQSmIds + kQMaxBlocks * 4;
 constexpr int kQSmFlag = kQSmBars + kQWarps * kQStages * 8;
-constexpr int kQSmBytes = kQSmFlag + 16;
+constexpr int kQSmBytes = kQSmFlag + 4 * kQRows;  // the last-arrival flag; cascade: one per row
 constexpr int kQSmAlloc = kQSmBytes + 1024;
 constexpr int kQSmMergeO = 0;
 constexpr int kQSmMergeML = kQWarps * kQRows * kQMergeStride * 4;
@@ -229,6 +229,9 @@ __global__ void __launch_bounds__(kQWarps * 32, ROWS16 ? 3 : 4)
     const int hpr = a.rows;
     const int h0 = kvh * a.group + c * hpr;
     int r, R, nseq, ctx, nparts, tok_lo, slot_p, span = a.part_tokens;
+    // Cascade: the private keys' launch reads nothing this grid writes except through the split-K counters,
+    // so it may start beside this one at once (whichever partial of a row arrives last merges the row)
+    if (CASCADE) pdl_trigger();
     if (CASCADE) {
         const int spc = kQRows / hpr;
         const int grp = blockIdx.z / a.max_slices, sl = blockIdx.z % a.max_slices;
@@ -261,6 +264,10 @@ __global__ void __launch_bounds__(kQWarps * 32, ROWS16 ? 3 : 4)
                 if (__ldg(a.group_start + mid) <= r) lo = mid; else hi = mid - 1;
             }
             S = __ldg(a.group_blocks + lo) * kBlockSize;
+        }
+        if (ctx <= S) {  // the group's shared prefix must lie below the row's newest token
+            if (p == 0 && blockIdx.y == 0 && threadIdx.x == 0) atomicOr(a.status, PKV_DEV_BAD_CTX);
+            return;
         }
         // [S, ctx) goes into as few partitions as part_tokens allows, of equal length in whole blocks, so that
         // no short partition's CTA trails the launch
@@ -316,7 +323,9 @@ __global__ void __launch_bounds__(kQWarps * 32, ROWS16 ? 3 : 4)
 
     // Only lengths, tables and this layer's codes were read so far; with a programmatic dependency on the
     // previous layer's kernel, wait for it before reading q or the new K/V and touching the workspace.
-    if (!a.no_wait) pdl_wait();
+    // Without the wait (no_wait), one CTA still waits: a cascade's private launch then ends only after the shared
+    // launch it runs beside, so work after the call in the stream finds both done.
+    if (!a.no_wait || (a.group_start && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0)) pdl_wait();
 
     // The new token: quantised here by the warp that streams its block, and stored by c == 0's warp 0.
     const int new_t = (ctx - 1) % kBlockSize, new_i = (ctx - 1) / kBlockSize - blk_lo;
@@ -740,13 +749,43 @@ __global__ void __launch_bounds__(kQWarps * 32, ROWS16 ? 3 : 4)
         }
     }
     if (CASCADE) {
-        // count the partial of each of the CTA's rows (the counter the private keys' launch counts with); the
-        // last partition of the row to arrive merges them
+        // count the partial of each of the CTA's rows (the counter the private keys' launch counts with, which
+        // may run beside this one); a row whose partials are all in is merged here, in partition order, by the
+        // same arithmetic as the private kernel's merge
+        unsigned int* flags = reinterpret_cast<unsigned int*>(smem + kQSmFlag);
         __syncthreads();
         if (threadIdx.x < nseq) {
-            __threadfence();
-            atomicAdd(a.counters + ((int64_t)(r + threadIdx.x) * a.num_kv_heads + kvh) * a.slices + c, 1u);
+            const int rr = r + threadIdx.x;
+            // the row's partitions: the prefix's nparts, then its private keys cut as the private kernel cuts them
+            const int n = __ldg(a.ctx_lens + rr) - ctx;
+            int npriv = 0;
+            if (n > 0) {
+                const int np = (n + a.part_tokens - 1) / a.part_tokens;
+                const int sp = ((n + np - 1) / np + kBlockSize - 1) / kBlockSize * kBlockSize;
+                npriv = (n + sp - 1) / sp;
+            }
+            const unsigned int total = (unsigned int)(nparts + npriv);
+            unsigned int* cnt = a.counters + ((int64_t)rr * a.num_kv_heads + kvh) * a.slices + c;
+            flags[threadIdx.x] = q_atomic_add_acq_rel(cnt, 1u) == total - 1u ? total : 0u;
         }
+        __syncthreads();
+        for (int row = 0; row < R; ++row) {
+            const int np_all = (int)flags[row / hpr];
+            if (np_all == 0) continue;
+            const int64_t base = rh(row) * a.ws_parts;
+            float M = -INFINITY;
+            for (int q = 0; q < np_all; ++q) M = fmaxf(M, __ldcg(a.ws_ml + (base + q) * 2));
+            float L = 0.f, O = 0.f;
+            for (int q = 0; q < np_all; ++q) {
+                const float wt = exp2f(__ldcg(a.ws_ml + (base + q) * 2) - M);
+                L = fmaf(wt, __ldcg(a.ws_ml + (base + q) * 2 + 1), L);
+                O = fmaf(wt, __ldcg(a.ws_o + (base + q) * kHeadDim + d), O);
+            }
+            a.out[rh(row) * kHeadDim + d] = __float2half_rn(O * (1.f / L));
+        }
+        __syncthreads();
+        if (threadIdx.x < nseq && flags[threadIdx.x])
+            a.counters[((int64_t)(r + threadIdx.x) * a.num_kv_heads + kvh) * a.slices + c] = 0u;
         return;
     }
     if (nparts == 1) return;
@@ -897,15 +936,17 @@ cudaError_t launch_decode_i8(const PoolGeom& g, const TensorMap128& i8_tmap, int
 }
 
 cudaError_t launch_decode_i8_shared_prefix(const PoolGeom& g, const TensorMap128& i8_tmap, int layer, const void* q,
-                                           const int32_t* tables, int max_blocks, const int32_t* group_start,
-                                           const int32_t* group_blocks, int num_groups, int max_group_rows,
-                                           float scale, const DecodeWs& ws, int partition_tokens,
-                                           unsigned int* status, cudaStream_t stream)
+                                           const int32_t* tables, int max_blocks, const int32_t* ctx_lens,
+                                           const int32_t* group_start, const int32_t* group_blocks, int num_groups,
+                                           int max_group_rows, float scale, void* out, const DecodeWs& ws,
+                                           int partition_tokens, unsigned int* status, cudaStream_t stream)
 {
     if (num_groups == 0) return cudaSuccess;
     I8Args a;
     memset(&a, 0, sizeof(a));
     a.q = static_cast<const __half*>(q);
+    a.out = static_cast<__half*>(out);
+    a.ctx_lens = ctx_lens;
     a.tables = tables;
     a.max_blocks = max_blocks;
     a.pool = const_cast<char*>(g.base);

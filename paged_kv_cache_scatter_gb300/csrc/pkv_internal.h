@@ -129,22 +129,24 @@ cudaError_t launch_decode_i8(const PoolGeom& g, const TensorMap128& i8_tmap, int
                              int pdl = 0, const int32_t* group_start = nullptr,
                              const int32_t* group_blocks = nullptr, int num_groups = 0);
 // Cascade over an 8-bit pool: the partitions wholly inside each group's shared prefix, for every row of the
-// group at once.
+// group at once (merging, as launch_decode_shared_prefix, the rows whose partials it completes).
 cudaError_t launch_decode_i8_shared_prefix(const PoolGeom& g, const TensorMap128& i8_tmap, int layer, const void* q,
-                                           const int32_t* tables, int max_blocks, const int32_t* group_start,
-                                           const int32_t* group_blocks, int num_groups, int max_group_rows,
-                                           float scale, const DecodeWs& ws, int partition_tokens,
-                                           unsigned int* status, cudaStream_t stream);
+                                           const int32_t* tables, int max_blocks, const int32_t* ctx_lens,
+                                           const int32_t* group_start, const int32_t* group_blocks, int num_groups,
+                                           int max_group_rows, float scale, void* out, const DecodeWs& ws,
+                                           int partition_tokens, unsigned int* status, cudaStream_t stream);
 
 // pkv_decode_group.cu: decode attention for pools whose K/V heads serve groups of query heads.
 bool encode_tile_tmap(const PoolGeom& g, TensorMap128* out, std::string* err);
 int decode_group_slices(int group);
-// Cascade: the partitions wholly inside each group's shared prefix, for every row of the group at once.
+// Cascade: the partitions wholly inside each group's shared prefix, for every row of the group at once. The
+// private keys' launch may run beside it (launched with pdl = 2): whichever partial of a row arrives last merges
+// the row into out, so both launches know every row's partition plan (ctx_lens).
 cudaError_t launch_decode_shared_prefix(const PoolGeom& g, const TensorMap128& kv_tmap, int layer, const void* q,
-                                        const int32_t* tables, int max_blocks, int num_seqs,
+                                        const int32_t* tables, int max_blocks, const int32_t* ctx_lens, int num_seqs,
                                         const int32_t* group_start, const int32_t* group_blocks, int num_groups,
-                                        int max_group_rows, float scale, const DecodeWs& ws, int partition_tokens,
-                                        unsigned int* status, cudaStream_t stream);
+                                        int max_group_rows, float scale, void* out, const DecodeWs& ws,
+                                        int partition_tokens, unsigned int* status, cudaStream_t stream);
 // group_start/group_blocks (num_groups > 0): skip each row's keys inside its group's shared prefix
 // (launch_decode_shared_prefix computed them).
 cudaError_t launch_decode_group(const PoolGeom& g, const TensorMap128& kv_tmap, int layer, const void* q,

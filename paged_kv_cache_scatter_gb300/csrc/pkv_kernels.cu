@@ -195,6 +195,10 @@ __global__ void __launch_bounds__(WARPS * 32) decode_kernel(const DecodeArgs a)
     }
     // [S, ctx) goes into as few partitions as part_tokens allows, of equal length in whole blocks (1,043 keys:
     // 528 + 515, not 1,024 + 19), so that no short partition's CTA trails the launch.
+    if (ctx <= S) {  // the group's shared prefix must lie below the row's newest token
+        if (p == 0 && h == 0 && threadIdx.x == 0) atomicOr(a.status, PKV_DEV_BAD_CTX);
+        return;
+    }
     const int nsh = (S + a.part_tokens - 1) / a.part_tokens;
     const int np = (ctx - S + a.part_tokens - 1) / a.part_tokens;
     const int span = ((ctx - S + np - 1) / np + kBlockSize - 1) / kBlockSize * kBlockSize;
@@ -252,7 +256,9 @@ __global__ void __launch_bounds__(WARPS * 32) decode_kernel(const DecodeArgs a)
     // Everything above reads only what the step's earlier layers never write (lengths, tables, this
     // layer's K/V). With a programmatic dependency on the previous layer's kernel, wait for it here, before
     // reading q or the new K/V and before touching the workspace or the output.
-    if (!a.no_wait) pdl_wait();
+    // Without the wait (no_wait), one CTA still waits: a cascade's private launch then ends only after the shared
+    // launch it runs beside, so work after the call in the stream finds both done.
+    if (!a.no_wait || (a.group_start && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0)) pdl_wait();
 
     // The new token (position ctx - 1) lives in this partition's last block.
     const int last_local = ((ctx - 1) >> 4) - blk_lo;
