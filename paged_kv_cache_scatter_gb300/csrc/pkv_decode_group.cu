@@ -176,11 +176,9 @@ __global__ void __launch_bounds__(kGWarps * 32) decode_group_kernel(const __grid
         r = blockIdx.z;
         nseq = 1;
         R = hpr;
+        // the row's length and (cascade) its group's shared prefix: independent loads, both issued before
+        // either is used (one memory round trip for a short cascade row's CTA, not two)
         ctx = __ldg(a.ctx_lens + r);
-        if (ctx < 1 || ctx > a.max_blocks * kBlockSize) {
-            if (p == 0 && blockIdx.y == 0 && threadIdx.x == 0) atomicOr(a.status, PKV_DEV_BAD_CTX);
-            return;
-        }
         // Cascade's other half: keys [0, S) of the row's group's shared prefix were partitioned on their own
         // (slots 0 .. nsh - 1, computed already); this CTA takes partition p of [S, ctx), slot nsh + p.
         int S = 0;
@@ -191,6 +189,10 @@ __global__ void __launch_bounds__(kGWarps * 32) decode_group_kernel(const __grid
                 if (__ldg(a.group_start + mid) <= r) lo = mid; else hi = mid - 1;
             }
             S = __ldg(a.group_blocks + lo) * kBlockSize;
+        }
+        if (ctx < 1 || ctx > a.max_blocks * kBlockSize) {
+            if (p == 0 && blockIdx.y == 0 && threadIdx.x == 0) atomicOr(a.status, PKV_DEV_BAD_CTX);
+            return;
         }
         // As few partitions as part_tokens allows, of equal length in whole blocks (a row of 2,300 keys: 768,
         // 768, 764 rather than 1,024, 1,024, 252), so that no short partition's CTA trails the launch. The plan

@@ -254,11 +254,9 @@ __global__ void __launch_bounds__(kQWarps * 32, ROWS16 ? 3 : 4)
         r = a.part_z ? blockIdx.y : blockIdx.z;
         nseq = 1;
         R = hpr;
+        // the row's length and (cascade) its group's shared prefix: independent loads, both issued before
+        // either is used (one memory round trip for a short cascade row's CTA, not two)
         ctx = __ldg(a.ctx_lens + r);
-        if (ctx < 1 || ctx > a.max_blocks * kBlockSize) {
-            if (p == 0 && blockIdx.y == 0 && threadIdx.x == 0) atomicOr(a.status, PKV_DEV_BAD_CTX);
-            return;
-        }
         // Cascade's other half: keys [0, S) of the row's group's shared prefix were partitioned on their own
         // (slots 0 .. nsh - 1); this CTA takes partition p of [S, ctx), slot nsh + p.
         int S = 0;
@@ -269,6 +267,10 @@ __global__ void __launch_bounds__(kQWarps * 32, ROWS16 ? 3 : 4)
                 if (__ldg(a.group_start + mid) <= r) lo = mid; else hi = mid - 1;
             }
             S = __ldg(a.group_blocks + lo) * kBlockSize;
+        }
+        if (ctx < 1 || ctx > a.max_blocks * kBlockSize) {
+            if (p == 0 && blockIdx.y == 0 && threadIdx.x == 0) atomicOr(a.status, PKV_DEV_BAD_CTX);
+            return;
         }
         if (ctx <= S) {  // the group's shared prefix must lie below the row's newest token
             if (p == 0 && blockIdx.y == 0 && threadIdx.x == 0) atomicOr(a.status, PKV_DEV_BAD_CTX);

@@ -176,11 +176,9 @@ __global__ void __launch_bounds__(WARPS * 32) decode_kernel(const DecodeArgs a)
     const int p = blockIdx.x, h = blockIdx.y, r = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+    // The row's length and (cascade) its group's shared prefix are independent loads: both are issued before
+    // either is used, so a short cascade row's CTA waits for one memory round trip here, not two.
     const int ctx = __ldg(a.ctx_lens + r);
-    if (ctx < 1 || ctx > a.max_blocks * kBlockSize) {
-        if (p == 0 && h == 0 && threadIdx.x == 0) atomicOr(a.status, PKV_DEV_BAD_CTX);
-        return;
-    }
     // Partition plan: keys [0, ctx) in partitions of at most part_tokens. Cascade: keys [0, S) of the row's group's
     // shared prefix are partitioned on their own (computed already, slots 0 .. nsh-1); this CTA takes
     // partition p of [S, ctx), slot nsh + p.
@@ -192,6 +190,10 @@ __global__ void __launch_bounds__(WARPS * 32) decode_kernel(const DecodeArgs a)
             if (__ldg(a.group_start + mid) <= r) lo = mid; else hi = mid - 1;
         }
         S = __ldg(a.group_blocks + lo) * kBlockSize;
+    }
+    if (ctx < 1 || ctx > a.max_blocks * kBlockSize) {
+        if (p == 0 && h == 0 && threadIdx.x == 0) atomicOr(a.status, PKV_DEV_BAD_CTX);
+        return;
     }
     // [S, ctx) goes into as few partitions as part_tokens allows, of equal length in whole blocks (1,043 keys:
     // 528 + 515, not 1,024 + 19), so that no short partition's CTA trails the launch.

@@ -131,8 +131,10 @@ def test_cascade_refuses_bad_groups_and_pools(pkv):
 
 # Grouped query heads and 8-bit pools: (K/V heads, query heads, element type). A shared-prefix CTA holds 16 query
 # rows: 4 rows x 4 heads (G = 4), 2 rows x 8 heads (MQA with 8 query heads), 1 row x 12 heads (G = 12), one row's
-# 16-head slice of a 32-head group (G = 32, two slices); 8-bit pools with 1 and 4 query heads per K/V head.
-KINDS = [(8, 32, "fp16"), (1, 8, "fp16"), (4, 48, "fp16"), (2, 64, "fp16"), (32, 32, "int8"), (8, 32, "int8")]
+# 16-head slice of a 32-head group (G = 32, two slices); 8-bit pools with 1, 4 and 7 query heads per K/V head
+# (G = 7: 2 rows x 7 heads in a shared-prefix CTA, an odd column count in the private keys' transposed form).
+KINDS = [(8, 32, "fp16"), (1, 8, "fp16"), (4, 48, "fp16"), (2, 64, "fp16"), (32, 32, "int8"), (8, 32, "int8"),
+         (2, 14, "int8")]
 
 
 @pytest.mark.parametrize("heads,q_heads,dtype", KINDS)

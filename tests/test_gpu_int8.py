@@ -203,8 +203,10 @@ def test_int8_close_to_fp16_decode(pkv):
     assert 0 < err < 0.02, err
 
 
-# (query heads, K/V heads): G = 4, MQA, G = 12 (fragment rows past 8), G = 32 (two slices), G = 3
-@pytest.mark.parametrize("hq,h", [(32, 8), (16, 1), (48, 4), (64, 2), (6, 2)])
+# (query heads, K/V heads): G = 4, MQA, G = 12 (fragment rows past 8), G = 32 (two slices), G = 3; and G = 2, 5,
+# 7, 8: up to 8 query heads a CTA take the transposed form (query heads as the MMA's 8 columns), odd counts
+# leaving a column pair half used
+@pytest.mark.parametrize("hq,h", [(32, 8), (16, 1), (48, 4), (64, 2), (6, 2), (8, 4), (20, 4), (14, 2), (16, 2)])
 @pytest.mark.parametrize("use_step", [False, True])
 def test_int8_grouped_query_heads(pkv, hq, h, use_step):
     wl = _wl(hq + h, num_seqs=7, max_ctx=1300)
