@@ -129,7 +129,7 @@ struct Cfg {
     static constexpr int kStagesV = kI8 ? 2 : 3; // V ring depth
     static constexpr int kThreads = kI8 ? 512 : 384;
     static constexpr int kLaunchRegs = 65536 / kThreads / 8 * 8;  // what ptxas allows a thread at launch
-    static constexpr int kSideRegs = kI8 ? 56 : 64;               // producer and issuer warpgroups
+    static constexpr int kSideRegs = 64;                          // producer and issuer warpgroups
     static constexpr int kConvRegs = 96;                          // converter warpgroup (8-bit pools)
     static constexpr int kSoftmaxRegs = 200;                      // softmax warpgroup
     static_assert(2 * 128 * kSideRegs + 128 * kSoftmaxRegs + (kI8 ? 128 * kConvRegs : 0) <= kThreads * kLaunchRegs,
@@ -152,7 +152,8 @@ struct Cfg {
     static constexpr int S_FULL = SC_FREE + kScaleStages;   // [kBufs] per S buffer
     static constexpr int P_FULL = S_FULL + kBufs;        // [kBufs] count kSoftmaxThreads: P written over the buffer's S
     static constexpr int PV_DONE = P_FULL + kBufs;       // [kBufs]
-    static constexpr int V_FIXED = PV_DONE + kBufs;      // FP16: the last tile's V rows past the last position zeroed
+    static constexpr int V_FIXED = PV_DONE + kBufs;      // the last tile's V rows (FP16) or V scales (8-bit, count
+                                                         // kSoftmaxThreads) past the last position zeroed
     static constexpr int Q_READY = V_FIXED + 1;          // count kSoftmaxThreads
     static constexpr int S_ALL_DONE = Q_READY + 1;       // every S MMA finished (before the CTA frees tensor memory)
     static constexpr int PV_ALL_DONE = S_ALL_DONE + 1;   // every P V MMA finished
@@ -343,23 +344,18 @@ __device__ __forceinline__ void scale_columns(uint32_t* s, const float4* scales)
 }
 
 // 8-bit pools: softmax_quarter with each weight times its key's V row scale before the rounding to FP16
-// (O accumulates P' codes_V = P V); the running sum takes the unscaled weights. kTail (the last tile): keys
-// e >= nkeys lie past the last query position, where the scale bytes may be anything (NaN, inf); their
-// weights are 0 and take scale 0, so that 0 times such a scale never reaches the P V product.
-template <bool kTail>
+// (O accumulates P' codes_V = P V); the running sum takes the unscaled weights. Keys past the last query
+// position (the last tile) have their V scale set to 0 first, so that 0 times a garbage scale never reaches
+// the P V product.
 __device__ __forceinline__ void softmax_quarter_vscaled(uint32_t* s, float scale_log2, float m_sub, float& l,
-                                                        const float4* vscales, int nkeys)
+                                                        const float4* vscales)
 {
     const uint64_t sc2 = f32x2_pack(scale_log2, scale_log2), nm2 = f32x2_pack(-m_sub, -m_sub);
     uint64_t acc[2] = {f32x2_pack(0.f, 0.f), f32x2_pack(0.f, 0.f)};
 #pragma unroll
     for (int e = 0; e < 32; e += 4) {
         const float4 v4 = vscales[e / 4];
-        float vs[4] = {v4.x, v4.y, v4.z, v4.w};
-        if (kTail) {
-#pragma unroll
-            for (int u = 0; u < 4; ++u) vs[u] = e + u < nkeys ? vs[u] : 0.f;
-        }
+        const float vs[4] = {v4.x, v4.y, v4.z, v4.w};
 #pragma unroll
         for (int u = 0; u < 4; u += 2) {
             const float2 x =
@@ -467,7 +463,7 @@ __global__ void __launch_bounds__(Cfg<kI8>::kThreads, 1) prefill_kernel(const __
             mbar_init(bar(C::P_FULL + i), kSoftmaxThreads);
             mbar_init(bar(C::PV_DONE + i), 1);
         }
-        mbar_init(bar(C::V_FIXED), 1);
+        mbar_init(bar(C::V_FIXED), kI8 ? kSoftmaxThreads : 1);
         mbar_init(bar(C::Q_READY), kSoftmaxThreads);
         mbar_init(bar(C::S_ALL_DONE), 1);
         mbar_init(bar(C::PV_ALL_DONE), 1);
@@ -701,6 +697,18 @@ __global__ void __launch_bounds__(Cfg<kI8>::kThreads, 1) prefill_kernel(const __
                     ok = false;
                     break;
                 }
+                if (j == n - 1) {
+                    // the last tile: keys past the last query position take V scale 0 (their scale bytes may be
+                    // anything, even NaN, and their weights are 0), written by the softmax threads, one key each,
+                    // before any of them reads the scales
+                    const int t = threadIdx.x - kFirstSoftmaxWarp * 32;
+                    if (key0 + t > pos_max) const_cast<float*>(reinterpret_cast<const float*>(vsc))[t] = 0.f;
+                    mbar_arrive(bar(C::V_FIXED));
+                    if (!flag_wait(bar(C::V_FIXED), 0, abort, a.status)) {
+                        ok = false;
+                        break;
+                    }
+                }
             }
             // diagonal tile: keys past the row's position count as -inf. Padding rows (past the chunk's last
             // query) are left unmasked: their Q is zero, their O is never written and rows do not mix in the
@@ -749,13 +757,9 @@ __global__ void __launch_bounds__(Cfg<kI8>::kThreads, 1) prefill_kernel(const __
             // quarters of 32 keys: P of keys 32q.. goes to P columns 16q.., stored without waiting
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                if constexpr (kI8) {
-                    if (j == n - 1)  // keys 0..pos_max - key0 of this tile lie at or before the last position
-                        softmax_quarter_vscaled<true>(sr + q * 32, a.scale_log2, m_sub, l, vsc + q * 8,
-                                                      pos_max - key0 + 1 - q * 32);
-                    else
-                        softmax_quarter_vscaled<false>(sr + q * 32, a.scale_log2, m_sub, l, vsc + q * 8, 0);
-                } else
+                if constexpr (kI8)
+                    softmax_quarter_vscaled(sr + q * 32, a.scale_log2, m_sub, l, vsc + q * 8);
+                else
                     softmax_quarter(sr + q * 32, a.scale_log2, m_sub, l);
                 tc_st16_async(tp + q * 16, sr + q * 32);
             }
