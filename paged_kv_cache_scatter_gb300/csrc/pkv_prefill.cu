@@ -637,7 +637,9 @@ __global__ void __launch_bounds__(Cfg<kI8>::kThreads, 1) prefill_kernel(const __
         for (int j = 0; j < n; ++j) {
             const int st = j % stages;
             if (!flag_wait(full0 + 8 * st, (uint32_t)(j / stages) & 1u, abort, a.status)) break;
-#pragma unroll
+            // the two rows one after the other: one copy of the conversion code (these warps share their
+            // schedulers' instruction caches with the softmax warps)
+#pragma unroll 1
             for (int u = 0; u < 2; ++u)
                 convert_code_row(ring + st * kTileOpBytes, r0 + 64 * u, j * kKeys + r0 + 64 * u <= pos_max);
             fence_proxy_async_smem();
