@@ -151,3 +151,35 @@ def test_cascade_shared_prefix_config_grouped_and_8bit(pkv, heads, q_heads, dtyp
     wl = workloads.shared_prefix_decode(0, num_layers=1, num_blocks=1500)
     gs, gb = run_cascade(pkv, wl, 0, heads=heads, q_heads=q_heads, dtype=dtype)
     assert list(gb) == [125] and list(gs) == [0, 64]
+
+
+@pytest.mark.parametrize("heads,q_heads,dtype", [(32, 32, "fp16"), (32, 32, "int8")])
+def test_cascade_back_to_back_calls_are_bit_identical(pkv, heads, q_heads, dtype):
+    # The shared-prefix and private-key launches run side by side (FP16 with one query head per K/V head, and
+    # 8-bit pools), and whichever partial of a row arrives last merges it. Twelve calls back to back on one
+    # stream, reusing one workspace: every output must be bit-identical (the merge is the same arithmetic
+    # whichever launch does it), and no call may see the previous call's launches still running (its counter
+    # clear would otherwise race their arrivals: rows merged twice, or never).
+    wl = workloads.shared_prefix_decode(1, num_layers=1, num_blocks=1500)
+    i8 = dtype == "int8"
+    pool = (G.device_pool_i8 if i8 else G.device_pool)(wl.num_blocks, 1, heads, seed=wl.seed)
+    p = pkv.Pool(pool, wl.num_blocks, num_layers=1, num_heads=heads, num_q_heads=q_heads, dtype=dtype)
+    tables_d, ctx_d, _, _, _ = G.step_metadata(wl)
+    q = workloads.normal_fp16((wl.num_tokens, q_heads, 128), workloads.value_seed(wl.seed, "q")).cuda()
+    gs, gb, widest = pkv.cascade_groups(wl.block_tables, wl.ctx_lens)
+    groups = (torch.from_numpy(gs).cuda(), torch.from_numpy(gb).cuda(), widest)
+    ws = torch.empty(max(p.decode_cascade_workspace_bytes(wl.num_seqs, wl.max_blocks), 256), dtype=torch.uint8,
+                     device="cuda")
+    outs = [torch.full_like(q, float("nan")) for _ in range(12)]
+    for o in outs:
+        p.decode_attn_cascade(0, q, tables_d, ctx_d, groups, G.SCALE, o, ws)
+    assert p.get_status() == (pkv.PKV_OK, 0)
+    assert not torch.isnan(outs[0]).any()
+    for i, o in enumerate(outs[1:], 1):
+        assert torch.equal(o, outs[0]), f"call {i} differs from call 0"
+    plain = torch.empty_like(q)
+    p.decode_attn(0, q, tables_d, ctx_d, G.SCALE, plain, ws)  # the counters were left at zero
+    assert p.get_status() == (pkv.PKV_OK, 0)
+    # both lie within the attention tolerance of the same exact result, so within twice it of each other
+    d, ref = (plain.double() - outs[0].double()).abs(), plain.double().abs()
+    assert bool((d <= 2 * (2e-3 + 1e-2 * ref)).all()), d.max().item()
