@@ -616,17 +616,24 @@ def run_ours(args):
     # ---- end to end: host buffers in, host result out, every step. As a serving loop runs it: two sets of
     # device buffers, the next step's host-to-device copies (one stream) and this step's result read back (a
     # second stream) run beside the step's kernels, ordered by events (a set's inputs are overwritten only once
-    # the step that used them and its read-back are done). The cascade configs copy, step and read back in turn.
+    # the step that used them and its read-back are done).
     host_io = []
     for s in steps:
         host_io.append([(x.cpu().pin_memory(), x) for x in (s.q, s.k, s.v)] + list(zip(s.host, s.dev)))
     outs_h = [torch.empty(s.out.shape, dtype=s.out.dtype).pin_memory() for s in steps]
-    if cascade:
-        sets = None
-    else:
-        twins = [StepData(torch, pkv, pool, s.wl, m, L, dev, gen) for s, m in zip(steps, _metadata(pkv, iters))]
-        sets = [[(s, [(src, dst) for (src, _), dst in zip(io, [s.q, s.k, s.v] + list(s.dev))], oh)
-                 for s, io, oh in zip(st, host_io, outs_h)] for st in (steps, twins)]
+    twins = [StepData(torch, pkv, pool, s.wl, m, L, dev, gen) for s, m in zip(steps, _metadata(pkv, iters))]
+    sets = [[(s, [(src, dst) for (src, _), dst in zip(io, [s.q, s.k, s.v] + list(s.dev))], oh)
+             for s, io, oh in zip(st, host_io, outs_h)] for st in (steps, twins)]
+
+    def run_unit(t):  # one iteration of the step on one buffer set
+        if cascade:
+            tables_d, ctx_d, _, slots_d = t.dev
+            for l in range(L):
+                pool.kv_append(l, t.k[l], t.v[l], slots_d, stream)
+                pool.decode_attn_cascade(l, t.q[l], tables_d, ctx_d, groups, SCALE, t.out[l], wspace, stream)
+        else:
+            pool.step(t.desc, wspace, stream)
+
     h2d_s, d2h_s = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     n_units = 2 * len(steps)
     in_ready = [ev() for _ in range(n_units)]
@@ -639,13 +646,7 @@ def run_ours(args):
     d2h_s.wait_stream(stream)
     k = 0
     for _ in range(args.steps):
-        for si, (s, io, oh) in enumerate(zip(steps, host_io, outs_h)):
-            if cascade:
-                for src, dst in io:
-                    dst.copy_(src, non_blocking=True)
-                step()
-                oh.copy_(s.out, non_blocking=True)
-                continue
+        for si in range(len(steps)):
             u = (k % 2) * len(steps) + si  # buffer set k % 2 of iteration si
             t, tio, toh = sets[k % 2][si]
             h2d_s.wait_event(done[u])  # the set's previous step is done with its inputs
@@ -655,7 +656,7 @@ def run_ours(args):
             in_ready[u].record(h2d_s)
             stream.wait_event(in_ready[u])
             stream.wait_event(read[u])  # its previous result has been read back
-            pool.step(t.desc, wspace, stream)
+            run_unit(t)
             done[u].record(stream)
             d2h_s.wait_event(done[u])
             with torch.cuda.stream(d2h_s):
@@ -779,10 +780,9 @@ def run_ours(args):
         "rooflines": rooflines,
         "e2e": {"value": round(e2e_value, 1), "unit": unit, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_ms / K, 4),
-                "how": ("pkv_step with every step's inputs copied from pinned host memory and its result read back "
-                        "inside the timed region; " + ("copies, step and read-back in turn" if cascade else
-                        "the next step's copies and this step's read-back on two streams of their own beside the "
-                        "step's kernels (two sets of device buffers)"))},
+                "how": ("the step with every step's inputs copied from pinned host memory and its result read back "
+                        "inside the timed region; the next step's copies and this step's read-back on two streams "
+                        "of their own beside the step's kernels (two sets of device buffers)")},
     }
     if has_decode:
         result["hbm_frac_of_measured_peak"] = round(value / hbm_peak, 4)
