@@ -391,6 +391,24 @@ __global__ void __launch_bounds__(Cfg<kI8>::kThreads, 1) prefill_kernel(const __
     // Nothing in global memory is read before this point, so any earlier kernel may produce the inputs.
     // (The trigger at the top lets a following decode launch of a mixed pkv_step layer start beside it.)
     pdl_trigger();
+    // Before the dependency wait, a hint only: the first tile's K and V lines into L2, from this CTA's metadata
+    // as it reads now (everything is read again after the wait; only block ids inside the pool give addresses,
+    // and a stale value costs at most a wasted prefetch). The lines then come from L2 once the wait is over.
+    if (threadIdx.x < kBlocksPerTile * 2 * 32) {
+        const int q0e = __ldg(a.q_start + s), qle = __ldg(a.q_start + s + 1) - q0e, ctxe = __ldg(a.ctx_lens + s);
+        if (qle >= 1 && qle <= ctxe && ctxe <= a.max_blocks * kBlockSize && qt * a.tok < qle) {
+            const int pme = ctxe - qle + qt * a.tok + min(a.tok, qle - qt * a.tok) - 1;  // last position
+            const int b = threadIdx.x / 64, kvl = (threadIdx.x / 32) & 1, l0 = threadIdx.x & 31;
+            if (b <= pme / kBlockSize) {
+                const int id = __ldg(a.tables + (int64_t)s * a.max_blocks + b);
+                if (id >= 0 && (int64_t)id < a.num_blocks) {
+                    const char* t = a.base + (int64_t)id * a.block_bytes + (int64_t)a.layer * a.layer_bytes +
+                                    (int64_t)(kvl * a.num_heads + hkv) * a.tile_bytes;
+                    for (int l = l0; l < (int)(a.tile_bytes / 128); l += 32) prefetch_l2(t + l * 128);
+                }
+            }
+        }
+    }
     pdl_wait();
 
     // ---- validate this sequence's metadata (all threads agree)
@@ -409,9 +427,9 @@ __global__ void __launch_bounds__(Cfg<kI8>::kThreads, 1) prefill_kernel(const __
     const int n = pos_max / kKeys + 1;       // 128-key tiles
     const int nblk = pos_max / kBlockSize + 1;
     const int32_t* trow = a.tables + (int64_t)s * a.max_blocks;
-    // The first S waits on two cold reads, Q and the first K tile: start both into L2 now (prefetch hints
-    // through the load path, not the copy engine, whose queue the first tile's boxes need). Q: a line
-    // (128 B) per thread; the first tile's K and V tiles: their lines spread over the CTA.
+    // The first S waits on two cold reads, Q and the first K tile (already on its way into L2, above): start Q
+    // into L2 now (prefetch hints through the load path, not the copy engine, whose queue the first tile's boxes
+    // need), a line (128 B) per thread.
     {
         const int lines_per_tok = a.hpc * 2;  // hpc rows of 256 B
         for (int i = threadIdx.x; i < ntok * lines_per_tok; i += C::kThreads)
@@ -419,21 +437,9 @@ __global__ void __launch_bounds__(Cfg<kI8>::kThreads, 1) prefill_kernel(const __
                         (i % lines_per_tok) * 64);
     }
     bool bad = false;
-    const int lines_per_tile = (int)(a.tile_bytes / 128);
     for (int b = threadIdx.x; b < nblk; b += C::kThreads) {
         const int id = __ldg(trow + b);
         bad |= id < 0 || (int64_t)id >= a.num_blocks;
-    }
-    if (threadIdx.x < kBlocksPerTile * 2 * 32) {  // block b of the first tile, K or V, 32 lines apart
-        const int b = threadIdx.x / 64, kvl = (threadIdx.x / 32) & 1, l0 = threadIdx.x & 31;
-        if (b < nblk) {
-            const int id = __ldg(trow + b);
-            if (id >= 0 && (int64_t)id < a.num_blocks) {
-                const char* t = a.base + (int64_t)id * a.block_bytes + (int64_t)a.layer * a.layer_bytes +
-                                (int64_t)(kvl * a.num_heads + hkv) * a.tile_bytes;
-                for (int l = l0; l < lines_per_tile; l += 32) prefetch_l2(t + l * 128);
-            }
-        }
     }
     if (__syncthreads_or(bad)) {
         if (threadIdx.x == 0) atomicOr(a.status, PKV_DEV_BAD_BLOCK);
