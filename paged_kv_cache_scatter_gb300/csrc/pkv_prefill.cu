@@ -394,13 +394,15 @@ __global__ void __launch_bounds__(Cfg<kI8>::kThreads, 1) prefill_kernel(const __
     // Before the dependency wait, a hint only: the first tile's K and V lines into L2, from this CTA's metadata
     // as it reads now (everything is read again after the wait; only block ids inside the pool give addresses,
     // and a stale value costs at most a wasted prefetch). The lines then come from L2 once the wait is over.
+    // These reads bypass L1 (ld.global.cg), so that no line read before the wait, which the previous kernel
+    // may still write, can serve a read after it.
     if (threadIdx.x < kBlocksPerTile * 2 * 32) {
-        const int q0e = __ldg(a.q_start + s), qle = __ldg(a.q_start + s + 1) - q0e, ctxe = __ldg(a.ctx_lens + s);
+        const int q0e = __ldcg(a.q_start + s), qle = __ldcg(a.q_start + s + 1) - q0e, ctxe = __ldcg(a.ctx_lens + s);
         if (qle >= 1 && qle <= ctxe && ctxe <= a.max_blocks * kBlockSize && qt * a.tok < qle) {
             const int pme = ctxe - qle + qt * a.tok + min(a.tok, qle - qt * a.tok) - 1;  // last position
             const int b = threadIdx.x / 64, kvl = (threadIdx.x / 32) & 1, l0 = threadIdx.x & 31;
             if (b <= pme / kBlockSize) {
-                const int id = __ldg(a.tables + (int64_t)s * a.max_blocks + b);
+                const int id = __ldcg(a.tables + (int64_t)s * a.max_blocks + b);
                 if (id >= 0 && (int64_t)id < a.num_blocks) {
                     const char* t = a.base + (int64_t)id * a.block_bytes + (int64_t)a.layer * a.layer_bytes +
                                     (int64_t)(kvl * a.num_heads + hkv) * a.tile_bytes;
