@@ -276,6 +276,7 @@ def prefill_chunk_summary(chunks, hbm_peak, tf_peak, peak_kind):
     (FLOPs of its unmasked (q, k) pairs) and the HBM peak (its K/V prefix read once, q read, out written);
     a chunk whose FLOPs per byte sit below the ridge tf_peak / hbm_peak is HBM-bound."""
     per, fl_tot, us_tot = [], 0.0, 0.0
+    fl_t, us_t = 0.0, 0.0  # the tensor-bound chunks only
     ridge = tf_peak * 1e12 / (hbm_peak * 1e9)
     for wl, us, hq, hkv, rb in chunks:
         fl = 4 * HEAD_DIM * hq * prefill_pairs(wl)
@@ -289,12 +290,20 @@ def prefill_chunk_summary(chunks, hbm_peak, tf_peak, peak_kind):
                     "bound": "tensor" if fl / by >= ridge else "hbm"})
         fl_tot += fl
         us_tot += us
+        if fl / by >= ridge:
+            fl_t += fl
+            us_t += us
     agg = fl_tot / (us_tot * 1e-6) / 1e12
+    agg_t = fl_t / (us_t * 1e-6) / 1e12 if us_t > 0 else None
     return {"bound": "tensor", "achieved": round(agg, 1), "peak": tf_peak,
             "peak_kind": peak_kind + " bf16 dense (fp16 runs at the same rate)", "unit": "TFLOP/s",
             "frac": round(agg / tf_peak, 4),
             "aggregate": {"chunks": len(per), "us_per_layer": round(us_tot, 2), "tflops": round(agg, 1),
                           "frac": round(agg / tf_peak, 4)},
+            "aggregate_tensor_bound": {"chunks": sum(1 for c in per if c["bound"] == "tensor"),
+                                       "us_per_layer": round(us_t, 2),
+                                       "tflops": round(agg_t, 1) if agg_t is not None else None,
+                                       "frac": round(agg_t / tf_peak, 4) if agg_t is not None else None},
             "per_chunk": per}
 
 
