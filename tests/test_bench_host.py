@@ -75,3 +75,18 @@ def test_every_workload_fits_the_pool_and_tables_are_disjoint():
     sp = workloads.shared_prefix_decode(0)
     assert (sp.block_tables[:, :125] == sp.block_tables[0, :125]).all()
     assert ((sp.ctx_lens >= 2001) & (sp.ctx_lens <= 2300)).all()
+
+
+def test_prefill_chunk_roofline_splits_hbm_and_tensor_bound_chunks():
+    # the 4,000-token prompt's 8 chunks at the same time each: the first two chunks' FLOPs per byte sit below
+    # the ridge (1,946.2 TFLOP/s over 6,783.5 GB/s = 287 FLOP/B), the rest above it
+    its = [workloads.mixed_prefill(c) for c in range(8)]
+    r = bench.prefill_chunk_summary([(w, 20.0, 32, 32, 256) for w in its], 6783.5, 1946.2, "measured")
+    assert [c["bound"] for c in r["per_chunk"]] == ["hbm"] * 2 + ["tensor"] * 6
+    # chunk c (c < 7) has 512 queries at positions 512c .. 512c + 511: 512 x 512c + 512 x 513 / 2 pairs;
+    # chunk 7 has 416 queries at 3,584 .. 3,999
+    pairs = [512 * 512 * c + 512 * 513 // 2 for c in range(7)] + [416 * 3584 + 416 * 417 // 2]
+    flops = [4 * 128 * 32 * p for p in pairs]
+    assert r["aggregate"]["tflops"] == pytest.approx(sum(flops) / (8 * 20e-6) / 1e12, abs=0.1)
+    assert r["aggregate_tensor_bound"]["chunks"] == 6
+    assert r["aggregate_tensor_bound"]["tflops"] == pytest.approx(sum(flops[2:]) / (6 * 20e-6) / 1e12, abs=0.1)
