@@ -735,6 +735,14 @@ __global__ void __launch_bounds__(Cfg<kI8>::kThreads, 1) prefill_kernel(const __
             if constexpr (kI8) scale_columns<64>(sr, ksc);
             if (diag) mask_tail<64>(sr, nvis);
             float mx = max64(sr);
+            if (j > 0) {
+                // P_{j-1}, stored at the end of the previous tile: its stores have had this tile's first load and
+                // max to complete, so the wait here costs the softmax nothing (P_{j-1} V_{j-1} has slack: its S
+                // buffer is next needed two tiles on)
+                tc_wait_st();
+                tc_fence_before();
+                mbar_arrive(bar(C::P_FULL + (j - 1) % kBufs));
+            }
             tc_wait_ld64(sr + 64);
             if constexpr (kI8) scale_columns<64>(sr + 64, ksc + 16);
             if (diag) mask_tail<64>(sr + 64, nvis - 64);
@@ -773,13 +781,16 @@ __global__ void __launch_bounds__(Cfg<kI8>::kThreads, 1) prefill_kernel(const __
                     softmax_quarter(sr + q * 32, a.scale_log2, m_sub, l);
                 tc_st16_async(tp + q * 16, sr + q * 32);
             }
-            tc_wait_st();
-            tc_fence_before();
-            mbar_arrive(bar(C::P_FULL + sbuf));
             if constexpr (kI8) {
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(C::SC_FREE + j % kScaleStages));  // done with this tile's scales
             }
+        }
+        // the last tile's P (or, after a failed wait, no store of this thread left in flight)
+        tc_wait_st();
+        if (ok) {
+            tc_fence_before();
+            mbar_arrive(bar(C::P_FULL + (n - 1) % kBufs));
         }
         // ---- epilogue: O / l -> FP16 (each row's 256 B written by its thread)
         if (ok && flag_wait(bar(C::PV_DONE + (n - 1) % kBufs), (uint32_t)((n - 1) / kBufs) & 1u, abort, a.status)) {
