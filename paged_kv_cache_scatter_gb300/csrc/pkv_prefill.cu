@@ -49,7 +49,9 @@
 //                tile's max exceeds it by more than 8 (a factor 256, far
 //                inside FP16/FP32 range); then the row's O and sum are
 //                rescaled once the previous P V product has landed. The
-//                result is exact up to rounding.
+//                result is exact up to rounding. P_j is signalled to the
+//                P V issuer from tile j+1, after that tile's first S load
+//                (by then P_j's stores have completed without a stall).
 // Shared-memory operands use the 128-byte swizzle: rows of 128 B (64 halves),
 // two slabs per 128-wide operand, 8-row groups 1,024 B apart.
 #include <cuda.h>
