@@ -90,3 +90,11 @@ def test_prefill_chunk_roofline_splits_hbm_and_tensor_bound_chunks():
     assert r["aggregate"]["tflops"] == pytest.approx(sum(flops) / (8 * 20e-6) / 1e12, abs=0.1)
     assert r["aggregate_tensor_bound"]["chunks"] == 6
     assert r["aggregate_tensor_bound"]["tflops"] == pytest.approx(sum(flops[2:]) / (6 * 20e-6) / 1e12, abs=0.1)
+
+
+def test_kernel_source_hash_ignores_comments_but_not_code():
+    a = "int f(int x) {\n    // the sum\n    return x + 1;  /* one */\n}\n"
+    b = "int f(int x) {\n\n    return x + 1;\n}\n/* a longer\n   comment */\n"
+    c = "int f(int x) {\n    return x + 2;\n}\n"
+    assert bench._code_only(a) == bench._code_only(b)
+    assert bench._code_only(a) != bench._code_only(c)
