@@ -398,18 +398,17 @@ __global__ void __launch_bounds__(Cfg<kI8>::kThreads, 1) prefill_kernel(const __
     // and a stale value costs at most a wasted prefetch). The lines then come from L2 once the wait is over.
     // These reads bypass L1 (ld.global.cg), so that no line read before the wait, which the previous kernel
     // may still write, can serve a read after it.
-    if (threadIdx.x < kBlocksPerTile * 2 * 32) {
+    if (warp == kMmaWarp && lane < kBlocksPerTile * 2) {
         const int q0e = __ldcg(a.q_start + s), qle = __ldcg(a.q_start + s + 1) - q0e, ctxe = __ldcg(a.ctx_lens + s);
         if (qle >= 1 && qle <= ctxe && ctxe <= a.max_blocks * kBlockSize && qt * a.tok < qle) {
             const int pme = ctxe - qle + qt * a.tok + min(a.tok, qle - qt * a.tok) - 1;  // last position
-            const int b = threadIdx.x / 64, kvl = (threadIdx.x / 32) & 1, l0 = threadIdx.x & 31;
+            const int b = lane >> 1, kvl = lane & 1;  // a lane per (block, K|V) tile of 4 KB
             if (b <= pme / kBlockSize) {
                 const int id = __ldcg(a.tables + (int64_t)s * a.max_blocks + b);
-                if (id >= 0 && (int64_t)id < a.num_blocks) {
-                    const char* t = a.base + (int64_t)id * a.block_bytes + (int64_t)a.layer * a.layer_bytes +
-                                    (int64_t)(kvl * a.num_heads + hkv) * a.tile_bytes;
-                    for (int l = l0; l < (int)(a.tile_bytes / 128); l += 32) prefetch_l2(t + l * 128);
-                }
+                if (id >= 0 && (int64_t)id < a.num_blocks)
+                    bulk_prefetch_l2(a.base + (int64_t)id * a.block_bytes + (int64_t)a.layer * a.layer_bytes +
+                                         (int64_t)(kvl * a.num_heads + hkv) * a.tile_bytes,
+                                     (uint32_t)a.tile_bytes);
             }
         }
     }

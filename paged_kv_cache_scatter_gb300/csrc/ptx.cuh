@@ -94,6 +94,12 @@ __device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity, u
 
 // ------------------------------------------------------- bulk async copies
 
+// Hint: bring `bytes` (a multiple of 16) from the 16-byte aligned `p` on into L2, through the copy engine.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* p, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 // Hint: bring the line holding `p` into L2 (through the load path, not the copy engine).
 __device__ __forceinline__ void prefetch_l2(const void* p)
 {
