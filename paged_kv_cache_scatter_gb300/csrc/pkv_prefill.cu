@@ -878,7 +878,8 @@ cudaError_t launch_prefill(const pkv_pool* pool, int layer, const void* q, const
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     // FP16 pools launch with the programmatic dependency (+1 % per chunk call); the 8-bit kernel measured
-    // 15 % slower per tile with it (270 against 317 TFLOP/s on the 8-chunk schedule) and launches without.
+    // slower per tile with it (270 against 317 TFLOP/s on the 8-chunk schedule; 462 against 483 with the
+    // current kernel: chunk 0 faster, every later chunk slower) and launches without.
     cfg.numAttrs = i8 ? 0 : 1;
     return i8 ? cudaLaunchKernelEx(&cfg, prefill_kernel<true>, tmap, a)
               : cudaLaunchKernelEx(&cfg, prefill_kernel<false>, tmap, a);
