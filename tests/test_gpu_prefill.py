@@ -147,6 +147,23 @@ def test_mixed_step_decode_rows_and_prefill_chunk(pkv, seed):
     run_step_case(pkv, _wl(ctx, qlen, num_layers=2, seed=seed))
 
 
+@pytest.mark.parametrize("seed", [11, 12, 13, 14])
+def test_mixed_step_random_ragged_batches(pkv, seed):
+    # random batches: 0-3 decode rows, then 1-4 prefill rows of random context (1..1,500) and chunk length
+    # (2..min(context, 300)), so query tiles end anywhere and chunks start inside blocks; 8 heads
+    rng = np.random.default_rng(seed)
+    nd, npf = int(rng.integers(0, 4)), int(rng.integers(1, 5))
+    ctx = rng.integers(1, 1500, nd).tolist()
+    qlen = [1] * nd
+    for _ in range(npf):
+        c = int(rng.integers(2, 1501))
+        ctx.append(c)
+        qlen.append(int(rng.integers(2, min(c, 300) + 1)))
+    wl = _wl(ctx, qlen, num_layers=2, seed=seed)
+    wl.num_heads = 8
+    run_step_case(pkv, wl)
+
+
 def test_mixed_chunk_schedule_small(pkv):
     # the chunked-prefill schedule of a 700-token prompt in 256-token chunks next to 5 decode rows
     for chunk in range(3):
