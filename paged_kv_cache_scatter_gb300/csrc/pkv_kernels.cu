@@ -37,6 +37,10 @@ cudaError_t status_word(int device, unsigned int** out)
 // head is 256 B (16 chunks) and lands at tile offset (slot % 16) * 256 of
 // its block's (layer, K, head) tile; V likewise in the V half.
 // "llm-inference-batching", step 7: new keys and values are appended.
+// Grid (chunk blocks, tokens): a block's threads are chunks c = K|V x heads x
+// 16 + head x 16 + chunk of one token (blockIdx.y, plus multiples of
+// gridDim.y past 65,535 tokens), so no thread divides by a runtime value; the
+// new row's load does not depend on the slot and is issued beside it.
 
 __global__ void __launch_bounds__(256) kv_append_kernel(char* __restrict__ pool, int64_t block_bytes,
                                                         int64_t layer_off, int64_t kv_bytes, int num_heads,
@@ -44,34 +48,33 @@ __global__ void __launch_bounds__(256) kv_append_kernel(char* __restrict__ pool,
                                                         const int64_t* __restrict__ slots, int num_tokens,
                                                         int64_t num_slots, unsigned int* status)
 {
-    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    const int64_t per_token = 2LL * num_heads * 16;
-    if (i >= per_token * num_tokens) return;
-    const int tok = (int)(i / per_token);
-    const int rem = (int)(i - (int64_t)tok * per_token);
-    const int kv = rem / (num_heads * 16);
-    const int h = (rem / 16) % num_heads;
-    const int chunk = rem & 15;
-    const int64_t slot = __ldg(slots + tok);
-    if (slot < 0 || slot >= num_slots) {
-        if (rem == 0) atomicOr(status, PKV_DEV_BAD_SLOT);
-        return;
+    const int hc = num_heads * 16;  // chunks of one token's K (or V) rows
+    const int c = blockIdx.x * blockDim.x + threadIdx.x;
+    if (c >= 2 * hc) return;
+    const int kv = c >= hc;
+    const int h = (c - kv * hc) >> 4, chunk = c & 15;
+    for (int tok = blockIdx.y; tok < num_tokens; tok += gridDim.y) {
+        const int64_t slot = __ldg(slots + tok);
+        const uint4 val = __ldg((kv ? v : k) + ((int64_t)tok * num_heads + h) * 16 + chunk);
+        if (slot < 0 || slot >= num_slots) {
+            if (c == 0) atomicOr(status, PKV_DEV_BAD_SLOT);
+            continue;
+        }
+        const int64_t blk = slot >> 4;
+        const int t = (int)(slot & 15);
+        *reinterpret_cast<uint4*>(pool + blk * block_bytes + layer_off + kv * kv_bytes + (int64_t)h * kTileBytes +
+                                  t * 256 + chunk * 16) = val;
     }
-    const int64_t blk = slot >> 4;
-    const int t = (int)(slot & 15);
-    char* dst = pool + blk * block_bytes + layer_off + kv * kv_bytes + (int64_t)h * kTileBytes + t * 256 + chunk * 16;
-    const uint4* src = (kv ? v : k) + ((int64_t)tok * num_heads + h) * 16 + chunk;
-    *reinterpret_cast<uint4*>(dst) = __ldg(src);
 }
 
 cudaError_t launch_kv_append(const PoolGeom& g, int layer, const void* k, const void* v, const int64_t* slots,
                              int num_tokens, unsigned int* status, cudaStream_t stream)
 {
     if (num_tokens == 0) return cudaSuccess;
-    const int64_t total = 2LL * g.num_heads * 16 * num_tokens;
-    const int threads = 256;
-    const int64_t blocks = (total + threads - 1) / threads;
-    kv_append_kernel<<<(unsigned)blocks, threads, 0, stream>>>(
+    const int chunks = 2 * g.num_heads * 16;
+    const int threads = chunks < 256 ? chunks : 256;  // a multiple of 32
+    const dim3 grid((unsigned)((chunks + threads - 1) / threads), (unsigned)(num_tokens < 65535 ? num_tokens : 65535));
+    kv_append_kernel<<<grid, threads, 0, stream>>>(
         const_cast<char*>(g.base), g.block_bytes, (int64_t)layer * g.layer_bytes, g.kv_bytes, g.num_heads,
         static_cast<const uint4*>(k), static_cast<const uint4*>(v), slots, num_tokens, g.num_blocks * kBlockSize,
         status);
