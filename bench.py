@@ -110,11 +110,12 @@ CONFIG_TEXT = {
 # The pool's split-K partition length per workload (0: the library's default, 1,024 tokens), the best measured
 # on this GB300: the batch-32 MHA rows stream in fewer, longer CTAs at 2,048 (0.951 of HBM peak against 0.926
 # at 1,024); the grouped-head workload's 2,300-token rows take one partition each at 4,096, so its 256 CTAs
-# run in one wave (0.936 against 0.788 at 1,024: 768 CTAs over 456 resident slots). The mixed steps keep 1,024:
-# their decode rows run beside the prefill launch, and at 2,048 the 8-chunk step took 29.59 against 29.13 ms
-# (8-bit pool 25.29 against 24.40, grouped heads 14.10 against 12.87).
+# run in one wave (0.936 against 0.788 at 1,024: 768 CTAs over 456 resident slots). In the mixed steps the decode
+# rows run beside the prefill launch, where shorter CTAs fill the SMs it leaves: the FP16 8-chunk step takes
+# 28.50 ms at 768 against 29.13 at 1,024, 29.55 at 512 and 29.59 at 2,048; the 8-bit and grouped-head mixed
+# steps are fastest at 1,024 (24.40 and 12.86 ms; 24.56 and 13.03 at 768).
 CONFIG_PARTITION = {"average_decode": 2048, "long_decode": 2048, "gqa_decode": 4096, "average_decode_int8": 2048,
-                    "shared_prefix_cascade_int8": 768, "shared_prefix_cascade_gqa": 768}
+                    "mixed_prefill": 768, "shared_prefix_cascade_int8": 768, "shared_prefix_cascade_gqa": 768}
 
 CONFIG_DTYPE = {"average_decode_int8": "int8", "mixed_prefill_int8": "int8", "shared_prefix_cascade_int8": "int8"}
 SWAP_BLOCKS, SWAP_POOL = 384, 1024
