@@ -114,8 +114,11 @@ CONFIG_TEXT = {
 # rows run beside the prefill launch, where shorter CTAs fill the SMs it leaves: the FP16 8-chunk step takes
 # 28.50 ms at 768 against 29.13 at 1,024, 29.55 at 512 and 29.59 at 2,048; the 8-bit and grouped-head mixed
 # steps are fastest at 1,024 (24.40 and 12.86 ms; 24.56 and 13.03 at 768).
+# The plain decode over the shared-prefix workload (64 rows of 2,001-2,300 keys) takes 7.34 ms per step at 2,048
+# against 7.95 at 1,024 and 8.05 at 768; its cascade form is fastest at 1,024 (1.99 ms; 2.10 at 768).
 CONFIG_PARTITION = {"average_decode": 2048, "long_decode": 2048, "gqa_decode": 4096, "average_decode_int8": 2048,
-                    "mixed_prefill": 768, "shared_prefix_cascade_int8": 768, "shared_prefix_cascade_gqa": 768}
+                    "mixed_prefill": 768, "shared_prefix_decode": 2048, "shared_prefix_cascade_int8": 768,
+                    "shared_prefix_cascade_gqa": 768}
 
 CONFIG_DTYPE = {"average_decode_int8": "int8", "mixed_prefill_int8": "int8", "shared_prefix_cascade_int8": "int8"}
 SWAP_BLOCKS, SWAP_POOL = 384, 1024
