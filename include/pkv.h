@@ -283,10 +283,9 @@ pkv_status pkv_decode_attn(pkv_pool* pool, int32_t layer, const void* q, const i
  * a pool with one query head per K/V head, 4 rows of 4 query heads for G = 4,
  * one row's 16 heads from G = 16 up), so its K/V tiles are read from memory
  * once per group instead of once per row; the rest of each row runs as in
- * pkv_decode_attn. The two launches run side by side (FP16 pools with one
- * query head per K/V head, and 8-bit pools; grouped heads one after the
- * other), and whichever partial of a row arrives last merges the row's
- * partials in partition order, by the same arithmetic either way. max_group_rows = the largest
+ * pkv_decode_attn. The two launches run side by side, and whichever
+ * partial of a row arrives last merges the row's partials in partition
+ * order, by the same arithmetic either way. max_group_rows = the largest
  * group. Every pool kind: FP16 with any G = num_q_heads / num_heads, and
  * 8-bit (codes dequantised as in pkv_decode_attn). No append: call
  * pkv_kv_append first. Partition plan: a row's shared prefix [0, S) is cut

@@ -784,9 +784,9 @@ pkv_status pkv_decode_attn_cascade(pkv_pool* pool, int32_t layer, const void* q,
                                               pool->status_dev, s);
     if (e != cudaSuccess) return pkv::cuda_fail(e, "cascade (shared prefix) launch");
     // the private keys' launch runs beside the shared one (programmatic launch without the dependency wait: it
-    // reads only inputs that were ready before this call); the last partial of each row merges it. Grouped-head
-    // FP16 pools launch it after the shared one instead: beside it, the two kernels' 67 KB CTAs crowd each other
-    // (0.137 against 0.143 of the HBM peak on unique bytes; MHA 0.47 against 0.41, 8-bit 0.25 against 0.23).
+    // reads only inputs that were ready before this call); the last partial of each row merges it. Fractions of
+    // the HBM peak on unique bytes, beside against after: MHA 0.47 against 0.41, 8-bit 0.25 against 0.23,
+    // grouped heads 0.161 against 0.153.
     if (i8)
         e = pkv::launch_decode_i8(pool->geom, pool->tile_tmap, layer, q, block_tables, max_blocks, ctx_lens, num_seqs,
                                   scale, out, w, pool->partition_tokens, nullptr, nullptr, nullptr, pool->status_dev,
@@ -794,7 +794,7 @@ pkv_status pkv_decode_attn_cascade(pkv_pool* pool, int32_t layer, const void* q,
     else if (pool->geom.group > 1)
         e = pkv::launch_decode_group(pool->geom, pool->tile_tmap, layer, q, block_tables, max_blocks, ctx_lens,
                                      num_seqs, scale, out, w, pool->partition_tokens, nullptr, nullptr, nullptr,
-                                     pool->status_dev, s, 0, group_start, group_blocks, num_groups);
+                                     pool->status_dev, s, 2, group_start, group_blocks, num_groups);
     else
         e = pkv::launch_decode(pool->geom, layer, q, block_tables, max_blocks, ctx_lens, num_seqs, scale, out, w,
                                pool->partition_tokens, nullptr, nullptr, nullptr, pool->status_dev, s, group_start,
